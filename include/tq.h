@@ -1,0 +1,175 @@
+/*
+ * tq.h -- C ABI of the GB300 (sm_103a) TurboQuant rotated KV-cache codec.
+ *
+ * The codec is the one defined on the mlx-bun design page "TurboQuant --
+ * rotation-based quantization", Part A (KV leg), section "Algorithm
+ * (vllm-metal reference semantics, exact)":
+ *   keys   -- no rotation; per-32-group asymmetric affine: signed int8 codes
+ *             (k_bits = 8) or unsigned 2/4/5-bit codes packed little-endian;
+ *             fp16 scale and zero point per group.
+ *   values -- x * signs (a fixed +-1 vector), normalised Walsh-Hadamard
+ *             transform (1/sqrt(d)), per-32-group RMS scale (fp16), index of
+ *             the Lloyd-Max cell of y / (rms + 1e-8), packed little-endian at
+ *             v_bits per value.
+ * Section "Architecture in mlx-bun" defines dequantize-on-fetch attention
+ * (updateAndFetch), and section "Deferred inverse FWHT" the un-rotation of
+ * the attention output once per query row, which tq_decode_attention uses.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *device* are CUDA device memory owned by the caller; the
+ *    library never allocates, frees or synchronises.  Host pointers are
+ *    read or written before the call returns.
+ *  - Arguments are validated on the host before anything is enqueued; a bad
+ *    argument returns an error status and enqueues nothing.
+ *  - Work is enqueued on `stream` and the call returns; device-side faults
+ *    surface at the caller's next synchronisation.  A launch failure returns
+ *    TQ_ERR_CUDA.  Calls on one stream are ordered; calls that touch the same
+ *    cache rows from different streams must be ordered by the caller.
+ *  - Calls are capturable in a CUDA graph (no allocation, no sync).
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers (same type). */
+typedef struct CUstream_st *tq_stream_t;
+
+typedef enum tq_status {
+    TQ_OK = 0,
+    TQ_ERR_NULL = 1,      /* a required pointer is NULL */
+    TQ_ERR_HEAD_DIM = 2,  /* head_dim not in {64, 128, 256, 512} */
+    TQ_ERR_BITS = 3,      /* k_bits not in {2,4,5,8} or v_bits not in {2,3,4,5,8} */
+    TQ_ERR_SHAPE = 4,     /* batch/heads/tokens/strides out of range */
+    TQ_ERR_CAPACITY = 5,  /* rows beyond the cache capacity */
+    TQ_ERR_ALIGN = 6,     /* pointer or stride not 16-byte aligned */
+    TQ_ERR_WORKSPACE = 7, /* workspace missing or too small */
+    TQ_ERR_CUDA = 8,      /* a CUDA launch or query failed */
+    TQ_ERR_UNSUPPORTED = 9 /* valid codec parameters this kernel does not cover */
+} tq_status;
+
+typedef enum tq_dtype { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
+
+/*
+ * The packed cache: five planes in caller-owned device memory, each laid out
+ * [batch][num_kv_heads][capacity][row] row-major, where row is
+ *   k_codes  d*k_bits/8 bytes   (int8 two's complement at 8 bits, else the
+ *                                little-endian bitstream: code i occupies bits
+ *                                [i*b, i*b+b), bit j of the row is bit j%8 of
+ *                                byte j/8)
+ *   k_scale  d/32 fp16 (IEEE binary16 bit patterns)
+ *   k_zero   d/32 fp16
+ *   v_codes  d*v_bits/8 bytes   (little-endian bitstream)
+ *   v_scale  d/32 fp16
+ * Groups of 32 run along head_dim only, so any token range is byte-safe
+ * ("Architecture in mlx-bun": standing invariant).  Plane base pointers must
+ * be 16-byte aligned and capacity a multiple of 16.
+ */
+typedef struct tq_cache {
+    int32_t head_dim;     /* d in {64, 128, 256, 512} */
+    int32_t k_bits;       /* {2, 4, 5, 8} */
+    int32_t v_bits;       /* {2, 3, 4, 5, 8} */
+    int32_t num_kv_heads; /* H >= 1 */
+    int32_t batch;        /* B >= 1 */
+    int32_t reserved;     /* must be 0 */
+    int64_t capacity;     /* token slots per (sequence, kv-head), multiple of 16 */
+    uint8_t *k_codes;     /* device */
+    uint16_t *k_scale;    /* device */
+    uint16_t *k_zero;     /* device */
+    uint8_t *v_codes;     /* device */
+    uint16_t *v_scale;    /* device */
+} tq_cache;
+
+/* Human-readable name of a status. */
+const char *tq_status_string(tq_status status);
+
+/* Bytes one token of one kv-head occupies in the planes:
+ * d*k_bits/8 + 2*(d/32)*2 + d*v_bits/8 + (d/32)*2 (200 at k8v3, d=128; page
+ * "Bytes per token per head").  Returns 0 for invalid parameters. */
+size_t tq_bytes_per_token_head(int32_t head_dim, int32_t k_bits, int32_t v_bits);
+
+/* Size in bytes of each plane of `cache` (k_codes, k_scale, k_zero, v_codes,
+ * v_scale) for its batch, heads and capacity; pointers are not read. */
+tq_status tq_plane_bytes(const tq_cache *cache, size_t out_bytes[5]);
+
+/* The +-1 value sign vector the library applies for head_dim d (host output,
+ * d int8 entries).  Output i of SplitMix64 seeded with 42; sign -1 when its
+ * top bit is set.  The d=64 vector is a prefix of the d=128 one, and so on.
+ * Page: "signs in {+-1}^d ... hardcoded constants per head_dim". */
+tq_status tq_sign_vector(int32_t head_dim, int8_t *host_out);
+
+/* The Lloyd-Max tables for v_bits (host outputs): 2^v_bits centroids and
+ * 2^v_bits - 1 boundaries (midpoints), fp32, ascending; the optimal quantizer
+ * of a unit normal.  Page: "3-bit table: centroids +-{0.24509, 0.75601,
+ * 1.34391, 2.15195}, boundaries +-{0.50055, 1.04996, 1.74793}, 0"; other
+ * widths "iterative Lloyd-Max on a unit normal". */
+tq_status tq_codebook(int32_t v_bits, float *host_centroids, float *host_boundaries);
+
+/*
+ * Append: quantise n_new tokens of K and V and write them into cache rows
+ * [t0, t0 + n_new) of every (sequence, kv-head); no other row is written.
+ * Page: updateAndFetch "quantizes only the newly appended tokens".
+ *  k, v      device bf16, element [b][h][t][j] at b*s[0] + h*s[1] + t*s[2] + j
+ *            (strides in elements, head_dim contiguous); pointers 16-byte
+ *            aligned and strides multiples of 8.
+ *  t0        first row, 0 <= t0 and t0 + n_new <= capacity.
+ * n_new = 0 is a no-op.
+ */
+tq_status tq_encode_append(const tq_cache *cache, const void *k, const int64_t k_strides[3],
+                           const void *v, const int64_t v_strides[3], int64_t t0, int64_t n_new,
+                           tq_stream_t stream);
+
+/*
+ * Fetch: dequantise rows [t0, t0 + n) to K and V, [batch][H][n][d] contiguous,
+ * bf16 (round to nearest even) or fp32 per out_dtype.  Either output may be
+ * NULL to skip it.  Keys: (code + zero) * scale in fp32, the add first (page,
+ * joint K/V decoder paragraph).  Values: signs * FWHT(centroid[code] * rms)
+ * / sqrt(d) ("apply FWHT then multiply signs").  Outputs 16-byte aligned.
+ */
+tq_status tq_decode(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype, void *k_out,
+                    void *v_out, tq_stream_t stream);
+
+/* Workspace bytes tq_decode_attention needs for these sizes (0 if invalid). */
+size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_heads, int64_t seq_len);
+
+/*
+ * Decode attention with dequantise-on-fetch, one query token per sequence:
+ *   out[b][h] = sum_t softmax_t(q[b][h] . k_hat[b][h/G][t] * softmax_scale) v_hat[b][h/G][t]
+ * over cache rows t in [0, seq_len), G = q_heads / num_kv_heads (GQA: q-head
+ * h reads kv-head h / G).  Keys and values are dequantised inside the kernel;
+ * values stay in the rotated domain and the output is un-rotated once per
+ * (sequence, q-head) ("Deferred inverse FWHT").  Accumulation is fp32.
+ *  q        device bf16 [batch][q_heads][d] contiguous, 16-byte aligned.
+ *  out      device fp32 [batch][q_heads][d] contiguous, 16-byte aligned.
+ *  workspace  device scratch of at least tq_attention_workspace_bytes(),
+ *           16-byte aligned; its contents need no initialisation.
+ * The token being generated must have been appended first (tq_encode_append
+ * with t0 = seq_len - 1), as the page's updateAndFetch does.
+ * Returns TQ_ERR_UNSUPPORTED for (d, k_bits, v_bits, q_heads/H) outside the
+ * instantiated set; tq_attention_supported() reports it.
+ */
+tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
+                              float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
+                              tq_stream_t stream);
+
+/* 1 if tq_decode_attention covers these parameters, else 0. */
+int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bits, int32_t group_size);
+
+/*
+ * Device-side error word.  Kernels that wait on asynchronous copies give up
+ * after a bounded number of polls and record a non-zero code here instead of
+ * hanging.  tq_device_error() synchronises the device, copies the word into
+ * *host_code and clears it.
+ */
+tq_status tq_device_error(uint32_t *host_code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

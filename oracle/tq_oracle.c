@@ -323,10 +323,12 @@ static int32_t clip_round(float r, float lo, float hi)
  * reference defect the pages reproduce on purpose. */
 void tqo_key_group(const float *x, int bits, int32_t *idx, uint16_t *scale_h, uint16_t *zero_h)
 {
+    /* Reading: max/min are IEEE maxNum/minNum folds (a NaN element is
+     * skipped; the pages leave NaN inputs open). */
     float mx = x[0], mn = x[0];
     for (int j = 1; j < 32; ++j) {
-        if (x[j] > mx) mx = x[j];
-        if (x[j] < mn) mn = x[j];
+        mx = fmaxf(mx, x[j]);
+        mn = fminf(mn, x[j]);
     }
     float scale, zero, lo, hi;
     if (bits == 8) {
@@ -387,7 +389,7 @@ static void key_group_unpack(const uint8_t *in, int bits, int32_t *idx)
 /* ------------------------------------------------------------------------ */
 /* Pages: y = FWHT(x * signs); scale = sqrt(mean(y^2)) per 32-group;
  * y_n = y/(scale + 1e-8); idx = searchsorted(BOUNDARIES, y_n).
- * Readings: the mean is a sequential fp32 sum divided by 32; searchsorted with
+ * Readings: the mean is the fp32 sum of squares divided by 32; searchsorted with
  * its default (left) side counts the boundaries strictly below y_n, so a tie
  * goes to the lower cell and NaN gives 0. */
 static int32_t searchsorted_left(const float *b, int nb, float y)
@@ -409,8 +411,10 @@ void tqo_value_row(const float *x, int d, const int8_t *signs, int bits, const f
     int nb = (1 << bits) - 1;
     for (int g = 0; g < d / 32; ++g) {
         const float *yg = y + 32 * g;
+        /* Reading: the sum of squares is accumulated in element order with a
+         * fused multiply-add (one rounding per element). */
         float ss = 0.0f;
-        for (int j = 0; j < 32; ++j) ss = ss + yg[j] * yg[j];
+        for (int j = 0; j < 32; ++j) ss = fmaf(yg[j], yg[j], ss);
         float sigma = sqrtf(ss / 32.0f);
         float den = sigma + 1e-8f;
         for (int j = 0; j < 32; ++j) {
