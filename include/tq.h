@@ -37,6 +37,13 @@
 extern "C" {
 #endif
 
+/* Exported symbols of the shared library (the rest is hidden). */
+#if defined(__GNUC__)
+#define TQ_API __attribute__((visibility("default")))
+#else
+#define TQ_API
+#endif
+
 /* cudaStream_t without including the CUDA headers (same type). */
 typedef struct CUstream_st *tq_stream_t;
 
@@ -86,29 +93,29 @@ typedef struct tq_cache {
 } tq_cache;
 
 /* Human-readable name of a status. */
-const char *tq_status_string(tq_status status);
+TQ_API const char *tq_status_string(tq_status status);
 
 /* Bytes one token of one kv-head occupies in the planes:
  * d*k_bits/8 + 2*(d/32)*2 + d*v_bits/8 + (d/32)*2 (200 at k8v3, d=128; page
  * "Bytes per token per head").  Returns 0 for invalid parameters. */
-size_t tq_bytes_per_token_head(int32_t head_dim, int32_t k_bits, int32_t v_bits);
+TQ_API size_t tq_bytes_per_token_head(int32_t head_dim, int32_t k_bits, int32_t v_bits);
 
 /* Size in bytes of each plane of `cache` (k_codes, k_scale, k_zero, v_codes,
  * v_scale) for its batch, heads and capacity; pointers are not read. */
-tq_status tq_plane_bytes(const tq_cache *cache, size_t out_bytes[5]);
+TQ_API tq_status tq_plane_bytes(const tq_cache *cache, size_t out_bytes[5]);
 
 /* The +-1 value sign vector the library applies for head_dim d (host output,
  * d int8 entries).  Output i of SplitMix64 seeded with 42; sign -1 when its
  * top bit is set.  The d=64 vector is a prefix of the d=128 one, and so on.
  * Page: "signs in {+-1}^d ... hardcoded constants per head_dim". */
-tq_status tq_sign_vector(int32_t head_dim, int8_t *host_out);
+TQ_API tq_status tq_sign_vector(int32_t head_dim, int8_t *host_out);
 
 /* The Lloyd-Max tables for v_bits (host outputs): 2^v_bits centroids and
  * 2^v_bits - 1 boundaries (midpoints), fp32, ascending; the optimal quantizer
  * of a unit normal.  Page: "3-bit table: centroids +-{0.24509, 0.75601,
  * 1.34391, 2.15195}, boundaries +-{0.50055, 1.04996, 1.74793}, 0"; other
  * widths "iterative Lloyd-Max on a unit normal". */
-tq_status tq_codebook(int32_t v_bits, float *host_centroids, float *host_boundaries);
+TQ_API tq_status tq_codebook(int32_t v_bits, float *host_centroids, float *host_boundaries);
 
 /*
  * Append: quantise n_new tokens of K and V and write them into cache rows
@@ -120,7 +127,7 @@ tq_status tq_codebook(int32_t v_bits, float *host_centroids, float *host_boundar
  *  t0        first row, 0 <= t0 and t0 + n_new <= capacity.
  * n_new = 0 is a no-op.
  */
-tq_status tq_encode_append(const tq_cache *cache, const void *k, const int64_t k_strides[3],
+TQ_API tq_status tq_encode_append(const tq_cache *cache, const void *k, const int64_t k_strides[3],
                            const void *v, const int64_t v_strides[3], int64_t t0, int64_t n_new,
                            tq_stream_t stream);
 
@@ -131,11 +138,11 @@ tq_status tq_encode_append(const tq_cache *cache, const void *k, const int64_t k
  * joint K/V decoder paragraph).  Values: signs * FWHT(centroid[code] * rms)
  * / sqrt(d) ("apply FWHT then multiply signs").  Outputs 16-byte aligned.
  */
-tq_status tq_decode(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype, void *k_out,
+TQ_API tq_status tq_decode(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype, void *k_out,
                     void *v_out, tq_stream_t stream);
 
 /* Workspace bytes tq_decode_attention needs for these sizes (0 if invalid). */
-size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_heads, int64_t seq_len);
+TQ_API size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_heads, int64_t seq_len);
 
 /*
  * Decode attention with dequantise-on-fetch, one query token per sequence:
@@ -153,12 +160,12 @@ size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_heads, int6
  * Returns TQ_ERR_UNSUPPORTED for (d, k_bits, v_bits, q_heads/H) outside the
  * instantiated set; tq_attention_supported() reports it.
  */
-tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
+TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
                               float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
                               tq_stream_t stream);
 
 /* 1 if tq_decode_attention covers these parameters, else 0. */
-int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bits, int32_t group_size);
+TQ_API int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bits, int32_t group_size);
 
 /*
  * Device-side error word.  Kernels that wait on asynchronous copies give up
@@ -166,7 +173,7 @@ int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bits, int
  * hanging.  tq_device_error() synchronises the device, copies the word into
  * *host_code and clears it.
  */
-tq_status tq_device_error(uint32_t *host_code);
+TQ_API tq_status tq_device_error(uint32_t *host_code);
 
 #ifdef __cplusplus
 }

@@ -222,6 +222,14 @@ int tqo_lloyd_max(int bits, double *centroids, double *boundaries)
         if (newton_step(n, c, bnd) < 1e-15) break;
     /* finish on the Lloyd map itself so the result is its fixed point */
     for (int k = 0; k < 4; ++k, ++steps) lloyd_step(n, c, bnd);
+    /* The density is symmetric, so is its optimal quantizer; the pages print
+     * the middle 3-bit boundary as exactly 0.  Remove the last-bit asymmetry
+     * left by rounding: c_{n-1-i} = -c_i, hence the middle boundary is 0. */
+    for (int i = n / 2; i < n; ++i) {
+        double m = 0.5 * (c[i] - c[n - 1 - i]);
+        c[i] = m;
+        c[n - 1 - i] = -m;
+    }
     midpoints(n, c, bnd);
     for (int i = 1; i < n; ++i) boundaries[i - 1] = bnd[i];
     return steps;

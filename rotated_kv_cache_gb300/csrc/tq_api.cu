@@ -1,0 +1,225 @@
+// tq_api.cu -- the extern "C" entry points declared in include/tq.h: argument
+// validation on the host, then one or more kernel launches on the caller's
+// stream.  Nothing here allocates, frees or synchronises (tq_device_error
+// excepted, which is documented to synchronise).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/tq.h"
+#include "tq_common.cuh"
+#include "tq_kernels.h"
+
+namespace tq {
+
+__device__ uint32_t g_device_error;  // see tq_device_error()
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t *g_err_ptr[kMaxDevices];
+int g_sms[kMaxDevices];
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+}  // namespace
+
+uint32_t *device_error_word()
+{
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<uint32_t *>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+int num_sms()
+{
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sms[dev] = n > 0 ? n : 1;
+    }
+    return g_sms[dev];
+}
+
+}  // namespace tq
+
+namespace {
+
+bool valid_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+bool valid_kbits(int32_t b) { return b == 2 || b == 4 || b == 5 || b == 8; }
+bool valid_vbits(int32_t b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 8; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tq_status check_cache(const tq_cache *c)
+{
+    if (!c) return TQ_ERR_NULL;
+    if (!valid_head_dim(c->head_dim)) return TQ_ERR_HEAD_DIM;
+    if (!valid_kbits(c->k_bits) || !valid_vbits(c->v_bits)) return TQ_ERR_BITS;
+    if (c->num_kv_heads < 1 || c->batch < 1 || c->reserved != 0) return TQ_ERR_SHAPE;
+    if (c->capacity < 16 || c->capacity % 16 != 0 || c->capacity > (int64_t(1) << 31)) return TQ_ERR_SHAPE;
+    if (!c->k_codes || !c->k_scale || !c->k_zero || !c->v_codes || !c->v_scale) return TQ_ERR_NULL;
+    if (!aligned16(c->k_codes) || !aligned16(c->k_scale) || !aligned16(c->k_zero) || !aligned16(c->v_codes) ||
+        !aligned16(c->v_scale))
+        return TQ_ERR_ALIGN;
+    return TQ_OK;
+}
+
+tq::CacheView view(const tq_cache *c)
+{
+    return tq::CacheView{c->head_dim, c->k_bits,  c->v_bits,  c->num_kv_heads, c->batch,
+                         c->capacity, c->k_codes, c->k_scale, c->k_zero,       c->v_codes,
+                         c->v_scale};
+}
+
+tq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *tq_status_string(tq_status s)
+{
+    switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_NULL: return "null pointer";
+    case TQ_ERR_HEAD_DIM: return "head_dim must be 64, 128, 256 or 512";
+    case TQ_ERR_BITS: return "k_bits must be 2, 4, 5 or 8 and v_bits 2, 3, 4, 5 or 8";
+    case TQ_ERR_SHAPE: return "shape, stride or count out of range";
+    case TQ_ERR_CAPACITY: return "rows beyond the cache capacity";
+    case TQ_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case TQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case TQ_ERR_CUDA: return "CUDA launch or query failed";
+    case TQ_ERR_UNSUPPORTED: return "parameters not covered by this kernel";
+    }
+    return "unknown status";
+}
+
+size_t tq_bytes_per_token_head(int32_t d, int32_t kb, int32_t vb)
+{
+    if (!valid_head_dim(d) || !valid_kbits(kb) || !valid_vbits(vb)) return 0;
+    return (size_t)d * kb / 8 + 2 * 2 * (size_t)(d / 32) + (size_t)d * vb / 8 + 2 * (size_t)(d / 32);
+}
+
+tq_status tq_plane_bytes(const tq_cache *c, size_t out[5])
+{
+    if (!c || !out) return TQ_ERR_NULL;
+    if (!valid_head_dim(c->head_dim)) return TQ_ERR_HEAD_DIM;
+    if (!valid_kbits(c->k_bits) || !valid_vbits(c->v_bits)) return TQ_ERR_BITS;
+    if (c->num_kv_heads < 1 || c->batch < 1 || c->capacity < 1) return TQ_ERR_SHAPE;
+    const size_t rows = (size_t)c->batch * c->num_kv_heads * (size_t)c->capacity;
+    const size_t d = (size_t)c->head_dim;
+    out[0] = rows * d * c->k_bits / 8;
+    out[1] = rows * (d / 32) * 2;
+    out[2] = rows * (d / 32) * 2;
+    out[3] = rows * d * c->v_bits / 8;
+    out[4] = rows * (d / 32) * 2;
+    return TQ_OK;
+}
+
+tq_status tq_sign_vector(int32_t d, int8_t *out)
+{
+    if (!out) return TQ_ERR_NULL;
+    if (!valid_head_dim(d)) return TQ_ERR_HEAD_DIM;
+    for (int i = 0; i < d; ++i) out[i] = tq::sign_negative(i) ? -1 : 1;
+    return TQ_OK;
+}
+
+tq_status tq_codebook(int32_t vb, float *centroids, float *boundaries)
+{
+    if (!valid_vbits(vb)) return TQ_ERR_BITS;
+    if (!centroids && !boundaries) return TQ_ERR_NULL;
+    const tq::Tables &t = tq::codebook_tables(vb);
+    for (int i = 0; i < (1 << vb); ++i) {
+        if (centroids) centroids[i] = t.centroids[i];
+        if (boundaries && i + 1 < (1 << vb)) boundaries[i] = t.boundaries[i];
+    }
+    return TQ_OK;
+}
+
+tq_status tq_encode_append(const tq_cache *c, const void *k, const int64_t ks[3], const void *v,
+                           const int64_t vs[3], int64_t t0, int64_t n, tq_stream_t stream)
+{
+    tq_status st = check_cache(c);
+    if (st != TQ_OK) return st;
+    if (t0 < 0 || n < 0) return TQ_ERR_SHAPE;
+    if (t0 + n > c->capacity) return TQ_ERR_CAPACITY;
+    if (n == 0) return TQ_OK;
+    if (!k || !v || !ks || !vs) return TQ_ERR_NULL;
+    if (!aligned16(k) || !aligned16(v)) return TQ_ERR_ALIGN;
+    for (int i = 0; i < 3; ++i) {
+        if (ks[i] < 0 || vs[i] < 0) return TQ_ERR_SHAPE;
+        if (ks[i] % 8 != 0 || vs[i] % 8 != 0) return TQ_ERR_ALIGN;
+    }
+    return cuda_status(tq::launch_encode(view(c), static_cast<const uint16_t *>(k), ks,
+                                         static_cast<const uint16_t *>(v), vs, t0, n, (cudaStream_t)stream));
+}
+
+tq_status tq_decode(const tq_cache *c, int64_t t0, int64_t n, tq_dtype dt, void *k_out, void *v_out,
+                    tq_stream_t stream)
+{
+    tq_status st = check_cache(c);
+    if (st != TQ_OK) return st;
+    if (t0 < 0 || n < 0) return TQ_ERR_SHAPE;
+    if (t0 + n > c->capacity) return TQ_ERR_CAPACITY;
+    if (dt != TQ_BF16 && dt != TQ_F32) return TQ_ERR_SHAPE;
+    if (n == 0 || (!k_out && !v_out)) return TQ_OK;
+    if ((k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out))) return TQ_ERR_ALIGN;
+    return cuda_status(tq::launch_decode(view(c), t0, n, dt == TQ_F32, k_out, v_out, (cudaStream_t)stream));
+}
+
+int tq_attention_supported(int32_t d, int32_t kb, int32_t vb, int32_t group)
+{
+    return tq::attention_supported(d, kb, vb, group) ? 1 : 0;
+}
+
+size_t tq_attention_workspace_bytes(const tq_cache *c, int32_t q_heads, int64_t seq_len)
+{
+    if (check_cache(c) != TQ_OK || q_heads < 1 || q_heads % c->num_kv_heads != 0 || seq_len < 1 ||
+        seq_len > c->capacity)
+        return 0;
+    return tq::attention_workspace_bytes(view(c), q_heads, seq_len);
+}
+
+tq_status tq_decode_attention(const tq_cache *c, const void *q, int32_t q_heads, int64_t seq_len, float scale,
+                              float *out, void *ws, size_t ws_bytes, tq_stream_t stream)
+{
+    tq_status st = check_cache(c);
+    if (st != TQ_OK) return st;
+    if (!q || !out) return TQ_ERR_NULL;
+    if (q_heads < 1 || q_heads % c->num_kv_heads != 0) return TQ_ERR_SHAPE;
+    if (seq_len < 1) return TQ_ERR_SHAPE;
+    if (seq_len > c->capacity) return TQ_ERR_CAPACITY;
+    if (!aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
+    if (!tq::attention_supported(c->head_dim, c->k_bits, c->v_bits, q_heads / c->num_kv_heads))
+        return TQ_ERR_UNSUPPORTED;
+    const size_t need = tq::attention_workspace_bytes(view(c), q_heads, seq_len);
+    if (need > 0 && (!ws || ws_bytes < need)) return TQ_ERR_WORKSPACE;
+    if (ws && !aligned16(ws)) return TQ_ERR_ALIGN;
+    return cuda_status(tq::launch_attention(view(c), static_cast<const uint16_t *>(q), q_heads, seq_len, scale, out,
+                                            ws, ws_bytes, (cudaStream_t)stream));
+}
+
+tq_status tq_device_error(uint32_t *host_code)
+{
+    if (!host_code) return TQ_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
+    uint32_t zero = 0;
+    if (cudaMemcpyFromSymbol(host_code, tq::g_device_error, sizeof(uint32_t)) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaMemcpyToSymbol(tq::g_device_error, &zero, sizeof(uint32_t)) != cudaSuccess) return TQ_ERR_CUDA;
+    return TQ_OK;
+}
+
+}  // extern "C"

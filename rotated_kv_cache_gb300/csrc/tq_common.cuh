@@ -1,0 +1,231 @@
+// tq_common.cuh -- device helpers shared by the codec kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tq {
+
+// ---------------------------------------------------------------- constants
+constexpr uint64_t kSignSeed = 42;  // value signs: SplitMix64 seeded with 42
+
+// Output i of SplitMix64 started at `seed` (Steele, Lea & Flood, OOPSLA 2014).
+__host__ __device__ constexpr uint64_t splitmix64(uint64_t seed, uint64_t i)
+{
+    uint64_t z = seed + (i + 1u) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// Value sign i is -1 when the top bit of output i is set.  Called with
+// compile-time indices inside fully unrolled loops, so it folds to a constant.
+__host__ __device__ constexpr bool sign_negative(int i) { return (splitmix64(kSignSeed, (uint64_t)i) >> 63) != 0; }
+
+__host__ __device__ constexpr float sign_value(int i) { return sign_negative(i) ? -1.0f : 1.0f; }
+
+// 32 sign bits of elements [32w, 32w+32) (bit k = element 32w+k is negative).
+__host__ __device__ constexpr uint32_t sign_word(int w)
+{
+    uint32_t m = 0;
+    for (int k = 0; k < 32; ++k)
+        if (sign_negative(32 * w + k)) m |= 1u << k;
+    return m;
+}
+
+// Device error word codes (see tq_device_error()).
+constexpr uint32_t kErrWaitTimeout = 1u;
+
+// ---------------------------------------------------------------- formats
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// Two fp32 -> packed bf16x2 (round to nearest even), lo in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ---------------------------------------------------------------- PTX: shared memory, mbarrier, bulk copies
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of a barrier, for at most ~2 s of wall time.  On
+// timeout the device error word gets kErrWaitTimeout and false is returned,
+// so a lost copy can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t *err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+            atomicOr(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+
+// Bulk asynchronous copy global -> shared (this CTA), completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Bulk asynchronous copy shared -> global, tracked by the bulk-group counter.
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until the shared-memory sources of all committed bulk stores have been read.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until all committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Order generic-proxy shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// ---------------------------------------------------------------- vector stores of a lane's words
+// Store N 32-bit words to a global address aligned to A bytes (A in {4, 8, 16}).
+template <int N, int A>
+__device__ __forceinline__ void store_words(void *dst, const uint32_t (&w)[N])
+{
+    static_assert(A == 4 || A == 8 || A == 16, "alignment");
+    if constexpr (A == 16 && N % 4 == 0) {
+        uint4 *p = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) p[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else if constexpr (A >= 8 && N % 2 == 0) {
+        uint2 *p = reinterpret_cast<uint2 *>(dst);
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) p[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+    } else {
+        uint32_t *p = reinterpret_cast<uint32_t *>(dst);
+#pragma unroll
+        for (int i = 0; i < N; ++i) p[i] = w[i];
+    }
+}
+
+template <int N, int A>
+__device__ __forceinline__ void load_words(const void *src, uint32_t (&w)[N])
+{
+    if constexpr (A == 16 && N % 4 == 0) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            uint4 v = p[i];
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+    } else if constexpr (A >= 8 && N % 2 == 0) {
+        const uint2 *p = reinterpret_cast<const uint2 *>(src);
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            uint2 v = p[i];
+            w[2 * i] = v.x; w[2 * i + 1] = v.y;
+        }
+    } else {
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(src);
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = p[i];
+    }
+}
+
+__host__ __device__ constexpr int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Largest power of two (<= 16) dividing x.
+__host__ __device__ constexpr int align_of_bytes(int x) { return (x % 16 == 0) ? 16 : (x % 8 == 0) ? 8 : (x % 4 == 0) ? 4 : (x % 2 == 0) ? 2 : 1; }
+
+// ---------------------------------------------------------------- bitstream packing of one 32-group
+// Codes c[0..31] (each < 2^B) -> B little-endian words: code i at bits [iB, iB+B)
+// of the 32B-bit group string.  All shifts are compile-time.
+template <int B>
+__device__ __forceinline__ void pack_group(const uint32_t (&c)[32], uint32_t (&w)[B])
+{
+#pragma unroll
+    for (int k = 0; k < B; ++k) w[k] = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int bit = i * B, word = bit >> 5, off = bit & 31;
+        w[word] |= c[i] << off;
+        if (off + B > 32) w[word + 1] |= c[i] >> (32 - off);
+    }
+}
+
+template <int B>
+__device__ __forceinline__ void unpack_group(const uint32_t (&w)[B], uint32_t (&c)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int bit = i * B, word = bit >> 5, off = bit & 31;
+        uint32_t v = w[word] >> off;
+        if (off + B > 32) v |= w[word + 1] << (32 - off);
+        c[i] = v & ((1u << B) - 1u);
+    }
+}
+
+}  // namespace tq

@@ -1,0 +1,42 @@
+// tq_kernels.h -- internal launch interface between the C ABI and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tq {
+
+struct CacheView {
+    int d, kb, vb, H, B;
+    int64_t cap;
+    uint8_t *k_codes;
+    uint16_t *k_scale, *k_zero;
+    uint8_t *v_codes;
+    uint16_t *v_scale;
+};
+
+struct Tables {
+    float centroids[256];
+    float boundaries[255];
+};
+
+// Host-side tables (computed once per width; thread safe).
+const Tables &codebook_tables(int vb);
+float inv_sqrt_head_dim(int d);  // fl(1/sqrt(d)) rounded from binary64
+
+uint32_t *device_error_word();  // per current device; nullptr on failure
+
+cudaError_t launch_encode(const CacheView &c, const uint16_t *k, const int64_t ks[3], const uint16_t *v,
+                          const int64_t vs[3], int64_t t0, int64_t n, cudaStream_t s);
+
+cudaError_t launch_decode(const CacheView &c, int64_t t0, int64_t n, bool f32, void *k_out, void *v_out,
+                          cudaStream_t s);
+
+bool attention_supported(int d, int kb, int vb, int group);
+size_t attention_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len);
+cudaError_t launch_attention(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
+                             float *out, void *ws, size_t ws_bytes, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace tq

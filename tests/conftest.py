@@ -36,3 +36,23 @@ def golden_rows(name: str) -> list:
             if line and "=" not in line:
                 rows.append(line)
     return rows
+
+
+@pytest.fixture(scope="session")
+def tqlib():
+    """The built C-ABI library (built here if missing; nvcc cross-compiles without a GPU)."""
+    from rotated_kv_cache_gb300 import build
+
+    build.build()
+    import rotated_kv_cache_gb300 as tqm
+
+    return tqm
+
+
+@pytest.fixture(scope="session")
+def cuda(tqlib):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    return tqlib

@@ -118,6 +118,15 @@ def test_lloyd_max_3bit_mse_on_samples():
     assert abs(mse - 0.0345) < 0.001
 
 
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_codebook_exactly_symmetric_with_zero_middle(bits):
+    """Pages print the middle 3-bit boundary as 0; the N(0,1) quantizer is symmetric."""
+    c, b = oracle.codebook(bits)
+    assert np.array_equal(c, -c[::-1]) and np.array_equal(b, -b[::-1])
+    if bits > 1:
+        assert b[len(b) // 2] == 0.0
+
+
 def test_codebook_f32_is_rounded_binary64():
     for bits in (2, 3, 4, 5, 8):
         c64, b64 = oracle.lloyd_max(bits)
