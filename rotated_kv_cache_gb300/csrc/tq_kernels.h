@@ -29,6 +29,17 @@ uint32_t *device_error_word();  // per current device; nullptr on failure
 cudaError_t launch_encode(const CacheView &c, const uint16_t *k, const int64_t ks[3], const uint16_t *v,
                           const int64_t vs[3], int64_t t0, int64_t n, cudaStream_t s);
 
+#define TQ_DECLARE_PER_D(D)                                                                                  \
+    cudaError_t launch_encode_d##D(const CacheView &c, const uint16_t *k, const int64_t ks[3], const uint16_t *v, \
+                                   const int64_t vs[3], int64_t t0, int64_t n, cudaStream_t s);                  \
+    cudaError_t launch_decode_values_d##D(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out,        \
+                                          cudaStream_t s);
+TQ_DECLARE_PER_D(64)
+TQ_DECLARE_PER_D(128)
+TQ_DECLARE_PER_D(256)
+TQ_DECLARE_PER_D(512)
+#undef TQ_DECLARE_PER_D
+
 cudaError_t launch_decode(const CacheView &c, int64_t t0, int64_t n, bool f32, void *k_out, void *v_out,
                           cudaStream_t s);
 

@@ -1,0 +1,221 @@
+"""Encode (append) and decode (fetch) kernels against the CPU oracle.
+
+Packed key bytes, fp16 scales and zero points must match the oracle bit for bit
+(any NaN equal to any NaN); value indices exactly, except indices whose
+normalised input lies within 1e-5 of a boundary (counted, expected 0 because
+the kernels follow the oracle's rounding order).  Decoded K/V: within 1e-3 of
+the row's largest magnitude (the transform mixes a row, so its error scales
+with the row), and bit-exact where the kernel follows the oracle's order.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tq_synth
+from tqtest import (bf16_rne, compare_value_codes, f16_equal, planes_from_device, to_device_bf16)
+
+pytestmark = pytest.mark.gpu
+
+COMBOS = [(d, kb, vb) for d in (64, 128, 256, 512) for kb in (2, 4, 5, 8) for vb in (2, 3, 4, 5, 8)]
+
+
+def _inputs(w, B, H, n, d, t_begin=0):
+    k, v = tq_synth.host_kv(w, B=B, H=H, d=d, t_begin=t_begin, n=n)
+    return k, v
+
+
+def _encode_both(tq, B, H, d, kb, vb, n, t0, cap, w=None, k=None, v=None):
+    w = w or tq_synth.WORKLOADS["sweep"]
+    if k is None:
+        k, v = _inputs(w, B, H, n, d, t_begin=t0)
+    cache = tq.Cache(B, H, d, cap, k_bits=kb, v_bits=vb)
+    for t in cache.planes():  # sentinel bytes: rows outside the append must keep them
+        t.fill_(0x5B if t.element_size() == 1 else 0x5B5B)
+    tq.tq_encode_append(cache, to_device_bf16(k), to_device_bf16(v), t0)
+    torch.cuda.synchronize()
+    ref = oracle.Planes(B, H, d, kb, vb, cache.capacity)
+    oracle.encode(ref, k, v, t0=t0)
+    return cache, planes_from_device(cache), ref, k, v
+
+
+def _assert_planes_match(gpu, ref, t0, n, vfloat, sentinel=True):
+    sl = slice(t0, t0 + n)
+    assert np.array_equal(gpu.k_codes[:, :, sl], ref.k_codes[:, :, sl]), "key codes differ"
+    assert f16_equal(gpu.k_scale[:, :, sl], ref.k_scale[:, :, sl]).all(), "key scales differ"
+    assert f16_equal(gpu.k_zero[:, :, sl], ref.k_zero[:, :, sl]).all(), "key zero points differ"
+    assert f16_equal(gpu.v_scale[:, :, sl], ref.v_scale[:, :, sl]).all(), "value scales differ"
+    B, H = gpu.B, gpu.H
+    rows = [(b, h, t) for b in range(B) for h in range(H) for t in range(n)]
+    bad, exempt = compare_value_codes(gpu, ref, vfloat, rows, t0)
+    assert bad == 0, f"{bad} value indices differ away from a boundary (exempt {exempt})"
+    if sentinel:
+        for a in gpu.arrays():
+            outside = np.concatenate([a[:, :, :t0].ravel(), a[:, :, t0 + n:].ravel()]).view(np.uint8)
+            assert np.all(outside == 0x5B), "append wrote outside its rows"
+    return exempt
+
+
+@pytest.mark.parametrize("d,kb,vb", COMBOS)
+def test_encode_parity_every_width(cuda, d, kb, vb):
+    B, H, n, t0 = 2, 3, 40, 16  # several warp tiles, a ragged tail, an offset append
+    cache, gpu, ref, k, v = _encode_both(cuda, B, H, d, kb, vb, n, t0, 64)
+    exempt = _assert_planes_match(gpu, ref, t0, n, oracle.bf16_bits_to_f32(v))
+    assert exempt == 0
+
+
+@pytest.mark.parametrize("d,kb,vb", COMBOS)
+def test_decode_parity_every_width(cuda, d, kb, vb):
+    B, H, n = 2, 3, 37
+    cache, gpu, ref, k, v = _encode_both(cuda, B, H, d, kb, vb, n, 0, 48)
+    ko, vo = oracle.decode(gpu, 0, n)  # oracle decodes the GPU's own bytes
+    gk, gv = cuda.tq_decode(cache, 0, n, dtype=torch.float32)
+    gk, gv = gk.cpu().numpy(), gv.cpu().numpy()
+    assert np.array_equal(gk.view(np.uint32), ko.view(np.uint32)), "fp32 keys not bit-exact"
+    row_max = np.abs(vo).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(gv - vo) <= 1e-3 * row_max)
+    assert np.array_equal(gv.view(np.uint32), vo.view(np.uint32)), "fp32 values not bit-exact"
+    bk, bv = cuda.tq_decode(cache, 0, n, dtype=torch.bfloat16)
+    assert np.array_equal(bk.cpu().view(torch.int16).numpy().view(np.uint16), bf16_rne(ko))
+    assert np.array_equal(bv.cpu().view(torch.int16).numpy().view(np.uint16), bf16_rne(vo))
+
+
+def test_decode_subrange_and_single_output(cuda):
+    B, H, d, n = 1, 2, 128, 64
+    cache, gpu, ref, k, v = _encode_both(cuda, B, H, d, 8, 3, n, 0, 64)
+    ko, vo = oracle.decode(gpu, 21, 17)
+    gk, _ = cuda.tq_decode(cache, 21, 17, dtype=torch.float32, want_v=False)
+    _, gv = cuda.tq_decode(cache, 21, 17, dtype=torch.float32, want_k=False)
+    assert np.array_equal(gk.cpu().numpy(), ko) and np.array_equal(gv.cpu().numpy(), vo)
+
+
+def test_strided_inputs(cuda):
+    """K/V as views of a [B][T][H][d] projection output (head-interleaved)."""
+    B, H, T, d = 2, 4, 33, 128
+    w = tq_synth.WORKLOADS["prefill"]
+    k, v = _inputs(w, B, H, T, d)
+    kt = to_device_bf16(np.ascontiguousarray(k.transpose(0, 2, 1, 3))).transpose(1, 2)
+    vt = to_device_bf16(np.ascontiguousarray(v.transpose(0, 2, 1, 3))).transpose(1, 2)
+    assert not kt.is_contiguous()
+    cache = cuda.Cache(B, H, d, 48)
+    cuda.tq_encode_append(cache, kt, vt, 0)
+    torch.cuda.synchronize()
+    ref = oracle.Planes(B, H, d, 8, 3, cache.capacity)
+    oracle.encode(ref, k, v)
+    _assert_planes_match(planes_from_device(cache), ref, 0, T, oracle.bf16_bits_to_f32(v), sentinel=False)
+
+
+def test_single_token_appends(cuda):
+    """Decode-step appends: n = 1 at successive t0, like updateAndFetch per token."""
+    B, H, d, T0, steps = 3, 2, 128, 20, 6
+    w = tq_synth.WORKLOADS["decode"]
+    k, v = _inputs(w, B, H, T0 + steps, d)
+    cache = cuda.Cache(B, H, d, 32)
+    cuda.tq_encode_append(cache, to_device_bf16(k[:, :, :T0]), to_device_bf16(v[:, :, :T0]), 0)
+    for s in range(steps):
+        t = T0 + s
+        cuda.tq_encode_append(cache, to_device_bf16(k[:, :, t:t + 1]), to_device_bf16(v[:, :, t:t + 1]), t)
+    torch.cuda.synchronize()
+    ref = oracle.Planes(B, H, d, 8, 3, cache.capacity)
+    oracle.encode(ref, k, v)
+    _assert_planes_match(planes_from_device(cache), ref, 0, T0 + steps, oracle.bf16_bits_to_f32(v), sentinel=False)
+
+
+def _edge_rows(d, rng):
+    """Rows exercising the definition's corner cases, as fp32 before bf16 rounding."""
+    rows = []
+    rows.append(np.zeros(d))                                    # zero groups: scale 0, zero NaN
+    rows.append(np.full(d, 1.5))                                # constant: zero +Inf
+    rows.append(np.full(d, -2.0))                               # constant: zero -Inf
+    r = rng.standard_normal(d); r[::2] = -0.0; rows.append(r)   # signed zeros
+    rows.append(rng.standard_normal(d) * 1e-39)                 # bf16 subnormals
+    rows.append(rng.standard_normal(d) * 3e37)                  # near the top of the range
+    r = rng.standard_normal(d); r[5] = np.nan; rows.append(r)  # NaN element
+    r = rng.standard_normal(d); r[7] = np.inf; r[40 % d] = -np.inf; rows.append(r)
+    r = np.round(rng.standard_normal(d) * 4) / 2; rows.append(r)  # halves: rounding ties
+    r = np.tile([-127.0, 127.0, 0.5, 1.5, -0.5, 2.5], d // 6 + 1)[:d]; rows.append(r)
+    r = rng.standard_normal(d); r[:32] = 7.0; r[3] = 7.0625; rows.append(r)  # near-constant group
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("kb,vb", [(8, 3), (4, 2), (5, 8), (2, 5)])
+def test_edge_values(cuda, d, kb, vb):
+    rng = np.random.default_rng(d * 100 + kb * 10 + vb)
+    kr = _edge_rows(d, rng)
+    vr = _edge_rows(d, rng)[::-1]
+    n = kr.shape[0]
+    k = oracle.f32_to_bf16_bits(kr.astype(np.float32)).reshape(1, 1, n, d)
+    v = oracle.f32_to_bf16_bits(vr.astype(np.float32)).reshape(1, 1, n, d)
+    cache, gpu, ref, _, _ = _encode_both(cuda, 1, 1, d, kb, vb, n, 0, 16, k=k, v=v)
+    _assert_planes_match(gpu, ref, 0, n, oracle.bf16_bits_to_f32(v))
+    # decode of those bytes agrees too (NaN where the oracle has NaN)
+    ko, vo = oracle.decode(gpu, 0, n)
+    gk, gv = cuda.tq_decode(cache, 0, n, dtype=torch.float32)
+    for g, o in ((gk.cpu().numpy(), ko), (gv.cpu().numpy(), vo)):
+        assert np.array_equal(np.isnan(g), np.isnan(o))
+        m = ~np.isnan(o)
+        assert np.array_equal(g[m], o[m])
+
+
+def test_prefill_full_size_bitexact(cuda):
+    """The prefill workload (4 x 8192 tokens x 8 kv-heads x d128, k8v3), every byte."""
+    w = tq_synth.WORKLOADS["prefill"]
+    k, v = tq_synth.host_kv(w)
+    cache = cuda.Cache(w.B, w.H, w.d, w.T, k_bits=w.kb, v_bits=w.vb)
+    kd, vd = to_device_bf16(k), to_device_bf16(v)
+    cuda.tq_encode_append(cache, kd, vd, 0)
+    torch.cuda.synchronize()
+    ref = oracle.Planes(w.B, w.H, w.d, w.kb, w.vb, cache.capacity)
+    oracle.encode(ref, k, v)
+    gpu = planes_from_device(cache)
+    for a, b in zip(gpu.arrays(), ref.arrays()):
+        if a is gpu.v_codes:
+            continue
+        assert f16_equal(a, b).all() if a.dtype == np.uint16 else np.array_equal(a, b)
+    mism = np.nonzero(np.any(gpu.v_codes != ref.v_codes, axis=-1))
+    rows = list(zip(*mism))
+    vf = oracle.bf16_bits_to_f32(v[:, :, :]) if rows else None
+    bad, exempt = compare_value_codes(gpu, ref, vf, rows, 0) if rows else (0, 0)
+    assert bad == 0 and exempt == 0
+    # fetch the whole window back to bf16 and compare with the oracle on sampled rows
+    gk, gv = cuda.tq_decode(cache, 0, w.T, dtype=torch.bfloat16)
+    rng = np.random.default_rng(5)
+    bs, hs = rng.integers(0, w.B, 64), rng.integers(0, w.H, 64)
+    ts = rng.integers(0, w.T, 64)
+    sub = oracle.Planes(1, 1, w.d, w.kb, w.vb, 16)
+    for b, h, t in zip(bs, hs, ts):
+        for a, src in zip(sub.arrays(), gpu.arrays()):
+            a[0, 0, 0] = src[b, h, t]
+        ko, vo = oracle.decode(sub, 0, 1)
+        assert np.array_equal(gk[b, h, t].cpu().view(torch.int16).numpy().view(np.uint16), bf16_rne(ko[0, 0, 0]))
+        assert np.array_equal(gv[b, h, t].cpu().view(torch.int16).numpy().view(np.uint16), bf16_rne(vo[0, 0, 0]))
+
+
+@pytest.mark.parametrize("d,kb,vb", [(512, 8, 3), (256, 5, 4), (64, 2, 2), (64, 4, 3), (256, 8, 2), (512, 4, 4)])
+def test_sweep_full_size_sampled(cuda, d, kb, vb):
+    """The bit-width / head_dim sweep at its full size (8 kv-heads x 16384 tokens):
+    the whole cache is encoded on the GPU; 4096 sampled rows are compared."""
+    w = tq_synth.WORKLOADS["sweep"]
+    H, T = w.H, w.T
+    kd = torch.empty((1, H, T, d), dtype=torch.bfloat16, device="cuda")
+    vd = torch.empty_like(kd)
+    tq_synth.device_kv(w, kd, vd, B=1, H=H, d=d, n=T)
+    cache = cuda.Cache(1, H, d, T, k_bits=kb, v_bits=vb)
+    cuda.tq_encode_append(cache, kd, vd, 0)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(d + kb + vb)
+    hs, ts = rng.integers(0, H, 4096), rng.integers(0, T, 4096)
+    # inputs of the sampled rows, read back from the device (the generator wrote them)
+    k = kd[0, hs, ts].cpu().view(torch.int16).numpy().view(np.uint16)[None, None]
+    v = vd[0, hs, ts].cpu().view(torch.int16).numpy().view(np.uint16)[None, None]
+    ref = oracle.Planes(1, 1, d, kb, vb, 4096)
+    oracle.encode(ref, k, v)
+    g = oracle.Planes(1, 1, d, kb, vb, 4096)
+    for a, src in zip(g.arrays(), cache.planes()):
+        a[0, 0] = src[0, hs, ts].cpu().numpy().view(a.dtype)
+    _assert_planes_match(g, ref, 0, 4096, oracle.bf16_bits_to_f32(v), sentinel=False)
+
+
+def test_no_bounded_wait_gave_up(cuda):
+    assert cuda.tq_device_error() == 0
