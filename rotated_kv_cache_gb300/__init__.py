@@ -133,6 +133,15 @@ class Cache:
         return _CacheStruct(self.head_dim, self.k_bits, self.v_bits, self.num_kv_heads, self.batch, 0,
                             self.capacity, *[t.data_ptr() for t in self.planes()])
 
+    def batch_slice(self, b0: int, nb: int) -> "Cache":
+        """A view of sequences [b0, b0+nb) sharing this cache's storage."""
+        v = Cache.__new__(Cache)
+        v.__dict__.update(self.__dict__)
+        for name in ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale"):
+            setattr(v, name, getattr(self, name)[b0:b0 + nb])
+        v.batch = int(nb)
+        return v
+
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in self.planes())
 

@@ -1,12 +1,695 @@
-// tq_attention.cu -- fused dequantise-on-fetch GQA decode attention (placeholder).
+// tq_attention.cu -- fused dequantise-on-fetch GQA decode attention.
+//
+// Method: mlx-bun "TurboQuant -- rotation-based quantization", Part A:
+// "Architecture in mlx-bun" (dequantize-on-fetch: attention reads the
+// dequantised window; the token being generated is appended first), the
+// "Algorithm" section (key and value dequantisation), and "Deferred inverse
+// FWHT" (attention is linear in V, so the weighted sum is formed in the
+// rotated domain and un-rotated once per query row).  GQA replicates whole
+// kv-heads: q-head h reads kv-head h / G.
+//
+// GB300 design (one GPU, sm_103a):
+//  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
+//    a 4-stage shared-memory ring.  A producer warp issues, per 64-token
+//    stage, one 2-D TMA load of the key codes (128/64-byte swizzle, so the
+//    per-row fragment reads of the MMA are bank-conflict-free) and four 1-D
+//    bulk copies of the other planes, completing on the stage's mbarrier.
+//  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
+//    tokens, N = the G = 8 q-heads sharing the kv-head, K = head_dim.  Key codes
+//    become exact f16 integers with one XOR and byte permutes (1024 + code), so
+//    S = sum_g scale_g * (acc_g + (zero_g - offset) * sum_{j in g} q_j) -- the
+//    per-group affine is applied to the 8-head scores, not to each element.
+//  * PV in the rotated domain (mma.sync, M = 16 dims, N = 8 heads, K = 16
+//    tokens): 3-bit codes are mapped to f16 centroids by byte-permute table
+//    lookups in registers; the per-group RMS scale is folded into P.
+//  * Online softmax (base 2) per warp; warps merge in shared memory; each CTA
+//    writes (max, sum, unnormalised o) per head.  A second kernel merges the
+//    splits (log-sum-exp) and applies the inverse transform and signs once per
+//    (sequence, q-head).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tq_common.cuh"
 #include "tq_kernels.h"
 
 namespace tq {
-bool attention_supported(int, int, int, int) { return false; }
-size_t attention_workspace_bytes(const CacheView &, int, int64_t) { return 0; }
-cudaError_t launch_attention(const CacheView &, const uint16_t *, int, int64_t, float, float *, void *, size_t,
-                             cudaStream_t)
+namespace {
+
+constexpr int kD = 128;            // head_dim covered
+constexpr int kG = 8;              // q-heads per kv-head
+constexpr int kVB = 3;             // value bits covered
+constexpr int kCW = 4;             // compute warps
+constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kStageT = 64;        // tokens per stage
+constexpr int kStages = 4;
+
+__host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int KB>
+struct AGeo {
+    static constexpr int KROW = kD * KB / 8;                   // key code bytes per token
+    static constexpr int K_BYTES = kStageT * KROW;
+    static constexpr int SC_BYTES = kStageT * (kD / 32) * 2;   // one fp16 plane
+    static constexpr int V_BYTES = kStageT * kD * kVB / 8;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_KS = K_BYTES;
+    static constexpr int OFF_KZ = OFF_KS + SC_BYTES;
+    static constexpr int OFF_VS = OFF_KZ + SC_BYTES;
+    static constexpr int OFF_V = OFF_VS + SC_BYTES;
+    static constexpr int STAGE = round_up(OFF_V + V_BYTES + 16, 1024);  // 1024: swizzle atom alignment
+    static constexpr int MERGE = kCW * kG * (kD + 2) * 4;             // per-warp partials
+    static constexpr int SMEM = 1024 /*align slack*/ + kStages * STAGE + (MERGE > 0 ? MERGE : 0) + 2 * kStages * 8;
+    static constexpr float OFFSET = KB == 8 ? 1152.0f : 1024.0f;    // f16 value = OFFSET + code
+};
+
+struct AttnParams {
+    const uint16_t *k_scale, *k_zero, *v_scale;
+    const uint8_t *v_codes;
+    const uint16_t *q;  // [B][QH][D] bf16
+    float *part_o;      // [B][H][S][G][D]
+    float *part_ml;     // [B][H][S][G][2]
+    int H, QH, splits;
+    int64_t cap, seq_len, tokens_per_split;
+    float scale_log2;  // softmax_scale * log2(e)
+    uint32_t *err;
+    uint32_t tl0, tl1, th0, th1;  // f16 centroid bytes: low bytes (c0..c7), high bytes
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
 {
-    return cudaErrorNotSupported;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// f16 pair (c[code0], c[code1]) from s = code0 | code1 << 16 (3-bit codes):
+// byte-permute lookups into the low-byte and high-byte tables of c[0..7].
+__device__ __forceinline__ uint32_t centroid_pair(uint32_t s, const AttnParams &p)
+{
+    const uint32_t sel = __byte_perm(s, 0u, 0x0020u);  // nibble0 = code0, nibble2 = code1
+    const uint32_t lo = __byte_perm(p.tl0, p.tl1, sel);
+    const uint32_t hi = __byte_perm(p.th0, p.th1, sel << 4);
+    return (lo & 0x00FF00FFu) | (hi & 0xFF00FF00u);
+}
+
+// ---------------------------------------------------------------- the split kernel
+template <int KB>
+__global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                  const __grid_constant__ AttnParams p)
+{
+    using A = AGeo<KB>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *stages = smem;
+    float *merge = reinterpret_cast<float *>(smem + kStages * A::STAGE);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * A::STAGE + A::MERGE);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int64_t bh = (int64_t)b * p.H + h;
+    const int64_t t_begin = (int64_t)split * p.tokens_per_split;
+    const int64_t t_end = imin64(p.seq_len, t_begin + p.tokens_per_split);
+    const int n_stages = t_end > t_begin ? (int)((t_end - t_begin + kStageT - 1) / kStageT) : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kCW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kCW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int s = 0; s < n_stages; ++s) {
+                const int slot = s % kStages, k = s / kStages;
+                if (k > 0 && !mbar_wait_bounded(empty0 + 8 * slot, (k - 1) & 1, p.err)) break;
+                const int64_t t = t_begin + (int64_t)s * kStageT;
+                const int rows = (int)imin64(kStageT, p.cap - t);  // multiple of 16
+                const int64_t row0 = bh * p.cap + t;
+                const uint32_t st = smem_addr(stages + slot * A::STAGE), bar = full0 + 8 * slot;
+                mbar_arrive_expect_tx(bar, (uint32_t)(A::K_BYTES + rows * (3 * (kD / 32) * 2 + kD * kVB / 8)));
+                tma_load_2d(st + A::OFF_K, &kmap, 0, (int)row0, bar);
+                bulk_g2s(st + A::OFF_KS, p.k_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
+                bulk_g2s(st + A::OFF_KZ, p.k_zero + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
+                bulk_g2s(st + A::OFF_VS, p.v_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
+                bulk_g2s(st + A::OFF_V, p.v_codes + row0 * (kD * kVB / 8), rows * (kD * kVB / 8), bar);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    const int g = lane >> 2, c = lane & 3;
+    // Q fragments (B operand of QK^T): head n = g; per k-step two f16x2 registers.
+    // The dim order inside a 32-group is permuted to match how key codes unpack.
+    uint32_t bq[8][2];
+    float qs[4][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
+    float ie[2];     // per head: 2^-e * softmax_scale * log2(e)
+    {
+        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * kG + g) * kD;
+        float qv[4][8];
+        float mx = 0.0f;
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * G + 8 * c);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                qv[G][2 * i] = bf16_lo(ww[i]);
+                qv[G][2 * i + 1] = bf16_hi(ww[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(qv[G][i]));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // power-of-two scale so the largest |q| of the head lands in [2^14, 2^15)
+        int e = 0;
+        if (mx > 0.0f && mx < INFINITY) e = 14 - (((int)(__float_as_uint(mx) >> 23) & 0xFF) - 127);
+        e = e < -100 ? -100 : (e > 100 ? 100 : e);
+        const float qscale = ldexpf(1.0f, e);
+        float qsum[4];
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+            float f[8];
+            uint32_t hw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                hw[i] = pack_f16x2(qv[G][2 * i] * qscale, qv[G][2 * i + 1] * qscale);
+                const __half2 hv = *reinterpret_cast<const __half2 *>(&hw[i]);
+                f[2 * i] = __low2float(hv);
+                f[2 * i + 1] = __high2float(hv);
+            }
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s += f[i];
+            qsum[G] = s;
+            if constexpr (KB == 8) {
+                // codes of dims 8c+{0..3} (word 0) then 8c+{4..7} (word 1), pairs in order
+                bq[2 * G][0] = hw[0];
+                bq[2 * G][1] = hw[1];
+                bq[2 * G + 1][0] = hw[2];
+                bq[2 * G + 1][1] = hw[3];
+            } else {
+                // nibble k of the word = dim 8c+k; unpacked pairs are (k, k+4)
+                auto pr = [&](int i, int j) { return pack_f16x2(f[i], f[j]); };
+                bq[2 * G][0] = pr(0, 4);
+                bq[2 * G][1] = pr(1, 5);
+                bq[2 * G + 1][0] = pr(2, 6);
+                bq[2 * G + 1][1] = pr(3, 7);
+            }
+        }
+        // group sums per head: head g lives in lanes 4g..4g+3; gather heads 2c, 2c+1
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+            float s = qsum[G];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            qs[G][0] = __shfl_sync(0xffffffffu, s, (2 * c) * 4);
+            qs[G][1] = __shfl_sync(0xffffffffu, s, (2 * c + 1) * 4);
+        }
+        const float my_ie = ldexpf(1.0f, -e) * p.scale_log2;
+        ie[0] = __shfl_sync(0xffffffffu, my_ie, (2 * c) * 4);
+        ie[1] = __shfl_sync(0xffffffffu, my_ie, (2 * c + 1) * 4);
+    }
+
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+
+    // V field extraction: lane g owns dims 32G + 4g + {0..3}: 12 bits at 96G + 12g
+    const int v_word = (12 * g) >> 5, v_shift = (12 * g) & 31;
+    const int r0 = 16 * warp + g, r1 = r0 + 8;  // key rows of this lane in a stage
+    const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
+
+    bool ok = true;
+    for (int s = 0; s < n_stages; ++s) {
+        const int slot = s % kStages;
+        if (!mbar_wait_bounded(full0 + 8 * slot, (s / kStages) & 1, p.err)) {
+            ok = false;
+            break;
+        }
+        const uint32_t st = smem_addr(stages + slot * A::STAGE);
+        const int64_t tile_t0 = t_begin + (int64_t)s * kStageT + 16 * warp;  // first token of this warp's tile
+
+        // ---------------- S = Q K^T for 16 tokens x 8 heads, per key group
+        float acc[4][4];
+#pragma unroll
+        for (int G = 0; G < 4; ++G)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[G][j] = 0.0f;
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+            if constexpr (KB == 8) {
+                // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
+                const uint32_t chunk = (uint32_t)((2 * G + (c >> 1)) ^ g);
+                const uint32_t off = (chunk << 4) + ((c & 1) << 3);
+                uint2 k0 = lds64(st + A::OFF_K + r0 * A::KROW + off);
+                uint2 k1 = lds64(st + A::OFF_K + r1 * A::KROW + off);
+                k0.x ^= 0x80808080u; k0.y ^= 0x80808080u;
+                k1.x ^= 0x80808080u; k1.y ^= 0x80808080u;
+                const uint32_t C = 0x64646464u;
+                mma16816(acc[G], __byte_perm(k0.x, C, 0x4140), __byte_perm(k1.x, C, 0x4140),
+                         __byte_perm(k0.x, C, 0x4342), __byte_perm(k1.x, C, 0x4342), bq[2 * G][0], bq[2 * G][1]);
+                mma16816(acc[G], __byte_perm(k0.y, C, 0x4140), __byte_perm(k1.y, C, 0x4140),
+                         __byte_perm(k0.y, C, 0x4342), __byte_perm(k1.y, C, 0x4342), bq[2 * G + 1][0],
+                         bq[2 * G + 1][1]);
+            } else {
+                // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
+                const uint32_t off = ((uint32_t)(G ^ ((g >> 1) & 3)) << 4) + 4 * c;
+                const uint32_t w0 = lds32(st + A::OFF_K + r0 * A::KROW + off);
+                const uint32_t w1 = lds32(st + A::OFF_K + r1 * A::KROW + off);
+                const uint32_t M = 0x000F000Fu, C = 0x64006400u;
+                mma16816(acc[G], (w0 & M) | C, (w1 & M) | C, ((w0 >> 4) & M) | C, ((w1 >> 4) & M) | C, bq[2 * G][0],
+                         bq[2 * G][1]);
+                mma16816(acc[G], ((w0 >> 8) & M) | C, ((w1 >> 8) & M) | C, ((w0 >> 12) & M) | C,
+                         ((w1 >> 12) & M) | C, bq[2 * G + 1][0], bq[2 * G + 1][1]);
+            }
+        }
+        // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum)
+        float S[2][2];
+        {
+            const uint2 s0 = lds64(st + A::OFF_KS + r0 * 8), s1 = lds64(st + A::OFF_KS + r1 * 8);
+            const uint2 z0 = lds64(st + A::OFF_KZ + r0 * 8), z1 = lds64(st + A::OFF_KZ + r1 * 8);
+            const uint32_t sw[2][2] = {{s0.x, s0.y}, {s1.x, s1.y}}, zw[2][2] = {{z0.x, z0.y}, {z1.x, z1.y}};
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float sacc = 0.0f;
+#pragma unroll
+                    for (int G = 0; G < 4; ++G) {
+                        const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
+                        const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
+                        const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
+                        sacc = fmaf(sc, fmaf(zc, qs[G][j], acc[G][2 * i + j]), sacc);
+                    }
+                    S[i][j] = sacc * ie[j];
+                }
+            if (tile_t0 + 16 > t_end) {  // ragged tail: mask rows past the range
+                if (tile_t0 + g >= t_end) S[0][0] = S[0][1] = -INFINITY;
+                if (tile_t0 + g + 8 >= t_end) S[1][0] = S[1][1] = -INFINITY;
+            }
+        }
+        // ---------------- online softmax (base 2) for heads 2c, 2c+1
+        float pr[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mt = fmaxf(S[0][j], S[1][j]);
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+            const float mn = fmaxf(m_run[j], mt);
+            const float mu = mn == -INFINITY ? 0.0f : mn;
+            const float alpha = ex2(m_run[j] - mu);
+            m_run[j] = mn;
+            pr[0][j] = ex2(S[0][j] - mu);
+            pr[1][j] = ex2(S[1][j] - mu);
+            l_run[j] = l_run[j] * alpha + pr[0][j] + pr[1][j];
+            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+                for (int mt2 = 0; mt2 < 8; ++mt2) {
+                    o[mt2][j] *= alpha;
+                    o[mt2][2 + j] *= alpha;
+                }
+            }
+        }
+        // ---------------- P^T as the B operand (tokens x heads), transposed in registers
+        const uint32_t pt0 = movmatrix_trans(pack_f16x2(pr[0][0], pr[0][1]));  // tokens 2c, 2c+1; head g
+        const uint32_t pt1 = movmatrix_trans(pack_f16x2(pr[1][0], pr[1][1]));  // tokens 2c+8, 2c+9
+        // value scales of this lane's four tokens (zero past the range)
+        uint2 vs[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            vs[q] = lds64(st + A::OFF_VS + vr[q] * 8);
+            if (tile_t0 + (vr[q] - 16 * warp) >= t_end) vs[q] = make_uint2(0u, 0u);
+        }
+        // ---------------- O^T += V^T P'^T, per value group
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+            const int sh = 16 * (G & 1);
+            const uint32_t sp0 = __byte_perm(G < 2 ? vs[0].x : vs[0].y, G < 2 ? vs[1].x : vs[1].y,
+                                             sh ? 0x7632u : 0x5410u);
+            const uint32_t sp1 = __byte_perm(G < 2 ? vs[2].x : vs[2].y, G < 2 ? vs[3].x : vs[3].y,
+                                             sh ? 0x7632u : 0x5410u);
+            const uint32_t b0 = hmul2(pt0, sp0), b1 = hmul2(pt1, sp1);
+            uint32_t x[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t base = st + A::OFF_V + vr[q] * (kD * kVB / 8) + 4 * (3 * G + v_word);
+                x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift) & 0xFFFu;
+            }
+            const uint32_t z01 = x[0] | (x[1] << 16), z23 = x[2] | (x[3] << 16);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int r = 2 * half;
+                const uint32_t a0 = centroid_pair((z01 >> (3 * r)) & 0x00070007u, p);
+                const uint32_t a1 = centroid_pair((z01 >> (3 * r + 3)) & 0x00070007u, p);
+                const uint32_t a2 = centroid_pair((z23 >> (3 * r)) & 0x00070007u, p);
+                const uint32_t a3 = centroid_pair((z23 >> (3 * r + 3)) & 0x00070007u, p);
+                mma16816(o[2 * G + half], a0, a1, a2, a3, b0, b1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    }
+
+    // ---------------------------------------------------------------- merge the warps
+    // per-lane partial row sums -> per-head sums (lanes with equal c)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+    }
+    float *mw = merge + warp * kG * (kD + 2);  // [head][D] o, then [head] m, [head] l
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int G = mt >> 1, half = mt & 1;
+        const int d0 = 32 * G + 4 * g + 2 * half;  // row g -> d0, row g+8 -> d0 + 1
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mw[(2 * c + j) * kD + d0] = o[mt][j];
+            mw[(2 * c + j) * kD + d0 + 1] = o[mt][2 + j];
+        }
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mw[kG * kD + 2 * c + j] = ok ? m_run[j] : -INFINITY;
+            mw[kG * kD + kG + 2 * c + j] = ok ? l_run[j] : 0.0f;
+        }
+    }
+    named_barrier_sync(1, kCW * 32);
+    // 128 threads: thread -> (head, 8 dims)
+    const int tid = threadIdx.x, hh = tid >> 4, d8 = (tid & 15) * 8;
+    float mmax = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) mmax = fmaxf(mmax, merge[w * kG * (kD + 2) + kG * kD + hh]);
+    const float mu = mmax == -INFINITY ? 0.0f : mmax;
+    float ov[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lsum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+        const float *m2 = merge + w * kG * (kD + 2);
+        const float wt = ex2(m2[kG * kD + hh] - mu);
+        lsum += m2[kG * kD + kG + hh] * wt;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ov[i] += m2[hh * kD + d8 + i] * wt;
+    }
+    const int64_t pidx = (bh * p.splits + split) * kG + hh;
+    float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * kD + d8);
+    dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
+    dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
+    if ((tid & 15) == 0) {
+        p.part_ml[2 * pidx] = mmax;
+        p.part_ml[2 * pidx + 1] = lsum;
+    }
+}
+
+// ---------------------------------------------------------------- combine + deferred un-rotation
+struct CombineParams {
+    const float *part_o, *part_ml;
+    float *out;  // [B][QH][D]
+    int H, QH, splits;
+    float inv_sqrt_d;
+};
+
+// one warp per (sequence, q-head); lane holds dims 4*lane .. 4*lane+3
+__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineParams p)
+{
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const int b = row / p.QH, qh = row % p.QH;
+    const int h = qh / kG, hh = qh % kG;
+    const int64_t base = ((int64_t)b * p.H + h) * p.splits;
+    float mmax = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * kG + hh)]);
+    const float mu = mmax == -INFINITY ? 0.0f : mmax;
+    float x[4] = {0, 0, 0, 0}, l = 0.0f;
+    for (int s = 0; s < p.splits; ++s) {
+        const int64_t pi = (base + s) * kG + hh;
+        const float wt = ex2(p.part_ml[2 * pi] - mu);
+        l += p.part_ml[2 * pi + 1] * wt;
+        const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pi * kD + 4 * lane);
+        x[0] += v.x * wt; x[1] += v.y * wt; x[2] += v.z * wt; x[3] += v.w * wt;
+    }
+    const float inv_l = 1.0f / l;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] *= inv_l;
+    // inverse transform: 2 stages in-lane, 5 across lanes (Sylvester order)
+#pragma unroll
+    for (int hs = 1; hs < 4; hs <<= 1)
+#pragma unroll
+        for (int i = 0; i < 4; i += 2 * hs)
+#pragma unroll
+            for (int j = i; j < i + hs; ++j) {
+                const float a = x[j], bb = x[j + hs];
+                x[j] = a + bb;
+                x[j + hs] = a - bb;
+            }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = upper ? other - x[i] : x[i] + other;
+        }
+    }
+    float4 r;
+    float *rr = &r.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int dim = 4 * lane + i;
+        // signs of dims 0..127, two compile-time words per lane quarter
+        const uint32_t word = dim < 32 ? sign_word(0) : dim < 64 ? sign_word(1) : dim < 96 ? sign_word(2) : sign_word(3);
+        const bool neg = (word >> (dim & 31)) & 1u;
+        rr[i] = x[i] * (neg ? -p.inv_sqrt_d : p.inv_sqrt_d);
+    }
+    *reinterpret_cast<float4 *>(p.out + ((int64_t)b * p.QH + qh) * kD + 4 * lane) = r;
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+struct SplitPlan {
+    int splits;
+    int64_t tokens_per_split;
+};
+
+SplitPlan plan_splits(int B, int H, int64_t seq_len, int ctas_per_sm)
+{
+    const int64_t units = (int64_t)B * H;
+    const int64_t stages = (seq_len + kStageT - 1) / kStageT;
+    const int64_t slots = (int64_t)num_sms() * ctas_per_sm;
+    SplitPlan best{1, stages * kStageT};
+    double best_cost = 1e300;
+    for (int waves = 1; waves <= 16; ++waves) {
+        int64_t s = (waves * slots + units - 1) / units;
+        if (s < 1) s = 1;
+        if (s > stages) s = stages;
+        const int64_t per = (stages + s - 1) / s;  // stages per split
+        const int64_t sp = (stages + per - 1) / per;
+        const int64_t ctas = units * sp;
+        const double cost = (double)((ctas + slots - 1) / slots) * (double)(per + 2);  // +2: fixed cost per CTA
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = SplitPlan{(int)sp, per * kStageT};
+        }
+    }
+    return best;
+}
+
+template <int KB>
+int ctas_per_sm_for()
+{
+    static int cached = 0;  // same on every GB300; only a successful query is kept
+    if (!cached) {
+        int n = 0;
+        if (cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, AGeo<KB>::SMEM) ==
+                cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<KB>, kThreads, AGeo<KB>::SMEM) ==
+                cudaSuccess &&
+            n > 0)
+            cached = n;
+        else
+            return 1;
+    }
+    return cached;
+}
+
+template <int KB>
+cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
+                          void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    using A = AGeo<KB>;
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+    if (e != cudaSuccess) return e;
+    const SplitPlan plan = plan_splits(c.B, c.H, seq_len, ctas_per_sm_for<KB>());
+    const size_t need_o = (size_t)c.B * c.H * plan.splits * kG * kD * 4;
+    const size_t need = need_o + (size_t)c.B * c.H * plan.splits * kG * 2 * 4;
+    if (ws_bytes < need) return cudaErrorInvalidValue;
+
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)A::KROW, (cuuint64_t)c.B * c.H * c.cap};
+    const cuuint64_t gstride[1] = {(cuuint64_t)A::KROW};
+    const cuuint32_t box[2] = {(cuuint32_t)A::KROW, (cuuint32_t)kStageT};
+    const cuuint32_t estride[2] = {1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k_codes, gdim, gstride, box, estride,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, KB == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    AttnParams p{};
+    p.k_scale = c.k_scale;
+    p.k_zero = c.k_zero;
+    p.v_scale = c.v_scale;
+    p.v_codes = c.v_codes;
+    p.q = q;
+    p.part_o = static_cast<float *>(ws);
+    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + need_o);
+    p.H = c.H;
+    p.QH = QH;
+    p.splits = plan.splits;
+    p.cap = c.cap;
+    p.seq_len = seq_len;
+    p.tokens_per_split = plan.tokens_per_split;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = device_error_word();
+    if (!p.err) return cudaErrorInvalidDevice;
+    const Tables &tab = codebook_tables(kVB);
+    uint8_t lo[8], hi[8];
+    for (int i = 0; i < 8; ++i) {
+        const uint16_t hb = __half_as_ushort(__float2half_rn(tab.centroids[i]));
+        lo[i] = (uint8_t)(hb & 0xFF);
+        hi[i] = (uint8_t)(hb >> 8);
+    }
+    p.tl0 = lo[0] | lo[1] << 8 | lo[2] << 16 | (uint32_t)lo[3] << 24;
+    p.tl1 = lo[4] | lo[5] << 8 | lo[6] << 16 | (uint32_t)lo[7] << 24;
+    p.th0 = hi[0] | hi[1] << 8 | hi[2] << 16 | (uint32_t)hi[3] << 24;
+    p.th1 = hi[4] | hi[5] << 8 | hi[6] << 16 | (uint32_t)hi[7] << 24;
+
+    dim3 grid(plan.splits, c.H, c.B);
+    attn_split_kernel<KB><<<grid, kThreads, A::SMEM, s>>>(map, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CombineParams cp{};
+    cp.part_o = p.part_o;
+    cp.part_ml = p.part_ml;
+    cp.out = out;
+    cp.H = c.H;
+    cp.QH = QH;
+    cp.splits = plan.splits;
+    cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
+    const int rows = c.B * QH;  // multiple of 8 (QH = 8 H)
+    attn_combine_kernel<<<rows / 8, 256, 0, s>>>(cp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_supported(int d, int kb, int vb, int group)
+{
+    return d == kD && vb == kVB && group == kG && (kb == 8 || kb == 4);
+}
+
+size_t attention_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)
+{
+    if (!attention_supported(c.d, c.kb, c.vb, q_heads / c.H)) return 0;
+    const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
+    const SplitPlan plan = plan_splits(c.B, c.H, seq_len, per_sm);
+    return (size_t)c.B * c.H * plan.splits * kG * (kD + 2) * 4;
+}
+
+cudaError_t launch_attention(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
+                             float *out, void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    if (c.kb == 8) return run_attention<8>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+    return run_attention<4>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+}
+
 }  // namespace tq

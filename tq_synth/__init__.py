@@ -90,7 +90,7 @@ _P, _I, _L, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
 @lru_cache(maxsize=1)
 def _host():
     so = ctypes.CDLL(build_host())
-    so.tqs_host_kv.argtypes = [_U, _I, _I, _I, _L, _L, ctypes.c_double, _I, _P, _P]
+    so.tqs_host_kv.argtypes = [_U, _I, _I, _I, _L, _L, _I, ctypes.c_double, _I, _P, _P]
     so.tqs_host_q.argtypes = [_U, _L, _I, _I, _I, _P]
     so.tqs_splitmix64.restype = _U
     so.tqs_splitmix64.argtypes = [_U, _U]
@@ -100,7 +100,7 @@ def _host():
 @lru_cache(maxsize=1)
 def _cuda():
     so = ctypes.CDLL(build_cuda())
-    so.tqs_device_kv.argtypes = [_U, _I, _I, _I, _L, _L, ctypes.c_double, _I, _P, _P, _P]
+    so.tqs_device_kv.argtypes = [_U, _I, _I, _I, _L, _L, _I, ctypes.c_double, _I, _P, _P, _P]
     so.tqs_device_kv.restype = _I
     so.tqs_device_q.argtypes = [_U, _L, _I, _I, _I, _P, _P]
     so.tqs_device_q.restype = _I
@@ -108,7 +108,7 @@ def _cuda():
 
 
 def host_kv(w: Workload, B=None, H=None, d=None, t_begin: int = 0, n: int | None = None,
-            want_k: bool = True, want_v: bool = True):
+            want_k: bool = True, want_v: bool = True, b_offset: int = 0):
     """bf16 bits K, V [B][H][n][d] for tokens [t_begin, t_begin+n)."""
     B = w.B if B is None else B
     H = w.H if H is None else H
@@ -116,7 +116,7 @@ def host_kv(w: Workload, B=None, H=None, d=None, t_begin: int = 0, n: int | None
     n = w.T if n is None else n
     k = np.zeros((B, H, n, d), dtype=np.uint16) if want_k else None
     v = np.zeros((B, H, n, d), dtype=np.uint16) if want_v else None
-    _host().tqs_host_kv(w.seed, B, H, d, t_begin, n, w.k_log_sigma, w.v_dist,
+    _host().tqs_host_kv(w.seed, B, H, d, t_begin, n, b_offset, w.k_log_sigma, w.v_dist,
                         None if k is None else k.ctypes.data, None if v is None else v.ctypes.data)
     return k, v
 
@@ -130,7 +130,8 @@ def host_q(w: Workload, step: int, B=None, QH=None, d=None):
     return q
 
 
-def device_kv(w: Workload, k_out, v_out, B=None, H=None, d=None, t_begin: int = 0, n=None, stream=None):
+def device_kv(w: Workload, k_out, v_out, B=None, H=None, d=None, t_begin: int = 0, n=None, stream=None,
+              b_offset: int = 0):
     """Fill device tensors (torch, bf16/int16 [B][H][n][d] contiguous) in place."""
     import torch
 
@@ -142,7 +143,7 @@ def device_kv(w: Workload, k_out, v_out, B=None, H=None, d=None, t_begin: int = 
         if t is not None:
             assert t.is_cuda and t.is_contiguous() and t.numel() == B * H * n * d and t.element_size() == 2
     s = torch.cuda.current_stream().cuda_stream if stream is None else stream
-    rc = _cuda().tqs_device_kv(w.seed, B, H, d, t_begin, n, w.k_log_sigma, w.v_dist,
+    rc = _cuda().tqs_device_kv(w.seed, B, H, d, t_begin, n, b_offset, w.k_log_sigma, w.v_dist,
                                None if k_out is None else k_out.data_ptr(),
                                None if v_out is None else v_out.data_ptr(), s)
     if rc != 0:

@@ -43,7 +43,7 @@ static uint16_t to_bf16(double x)
     return (uint16_t)(u >> 16);
 }
 
-void tqs_host_kv(uint64_t data_seed, int B, int H, int d, int64_t t_begin, int64_t n,
+void tqs_host_kv(uint64_t data_seed, int B, int H, int d, int64_t t_begin, int64_t n, int b_offset,
                  double k_log_sigma, int v_dist, uint16_t *k_out, uint16_t *v_out)
 {
     const uint64_t sk = tqs_splitmix64(data_seed, 0), sv = tqs_splitmix64(data_seed, 1);
@@ -54,7 +54,7 @@ void tqs_host_kv(uint64_t data_seed, int B, int H, int d, int64_t t_begin, int64
             double cs[512];
             for (int j = 0; j < d; ++j) cs[j] = exp(k_log_sigma * tqs_normal(ss, (uint64_t)h * d + j));
             for (int64_t t = 0; t < n; ++t) {
-                const uint64_t base = (((uint64_t)(b * H + h) << 32) + (uint64_t)(t_begin + t)) * (uint64_t)d;
+                const uint64_t base = (((uint64_t)((b + b_offset) * H + h) << 32) + (uint64_t)(t_begin + t)) * (uint64_t)d;
                 const int64_t o = (((int64_t)b * H + h) * n + t) * d;
                 for (int j = 0; j < d; ++j) {
                     if (k_out) k_out[o + j] = to_bf16(tqs_normal(sk, base + j) * cs[j]);

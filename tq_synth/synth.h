@@ -27,8 +27,9 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
-/* Host: K, V bf16 bits, [B][H][n][d] contiguous, tokens [t_begin, t_begin+n). */
-void tqs_host_kv(uint64_t data_seed, int B, int H, int d, int64_t t_begin, int64_t n,
+/* Host: K, V bf16 bits, [B][H][n][d] contiguous, tokens [t_begin, t_begin+n) of
+ * sequences [b_offset, b_offset+B). */
+void tqs_host_kv(uint64_t data_seed, int B, int H, int d, int64_t t_begin, int64_t n, int b_offset,
                  double k_log_sigma, int v_dist, uint16_t *k_out, uint16_t *v_out);
 /* Host: queries of one step, bf16 bits [B][QH][d]. */
 void tqs_host_q(uint64_t data_seed, int64_t step, int B, int QH, int d, uint16_t *q_out);

@@ -50,7 +50,7 @@ __device__ __forceinline__ uint16_t to_bf16(double x)
 
 // one thread per (b, h, t, j); output [B][H][n][d] with row stride `ld` elements
 __global__ void fill_kv(uint64_t sk, uint64_t sv, uint64_t ss, int B, int H, int d, int64_t t_begin,
-                        int64_t n, double k_log_sigma, int v_dist, uint16_t *k_out, uint16_t *v_out)
+                        int64_t n, int b_offset, double k_log_sigma, int v_dist, uint16_t *k_out, uint16_t *v_out)
 {
     const int64_t total = (int64_t)B * H * n * d;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
@@ -59,7 +59,7 @@ __global__ void fill_kv(uint64_t sk, uint64_t sv, uint64_t ss, int B, int H, int
         const int64_t t = (e / d) % n;
         const int64_t bh = e / ((int64_t)d * n);
         const int h = (int)(bh % H);
-        const uint64_t c = (((uint64_t)bh << 32) + (uint64_t)(t_begin + t)) * (uint64_t)d + j;
+        const uint64_t c = (((uint64_t)(bh + (int64_t)b_offset * H) << 32) + (uint64_t)(t_begin + t)) * (uint64_t)d + j;
         if (k_out) k_out[e] = to_bf16(normal(sk, c) * exp(k_log_sigma * normal(ss, (uint64_t)h * d + j)));
         if (v_out) v_out[e] = to_bf16(v_dist == TQS_V_T5 ? t5(sv, c) : normal(sv, c));
     }
@@ -84,11 +84,11 @@ uint64_t host_sm64(uint64_t seed, uint64_t i)
 }  // namespace
 
 extern "C" int tqs_device_kv(uint64_t data_seed, int B, int H, int d, int64_t t_begin, int64_t n,
-                             double k_log_sigma, int v_dist, uint16_t *k_out, uint16_t *v_out,
+                             int b_offset, double k_log_sigma, int v_dist, uint16_t *k_out, uint16_t *v_out,
                              cudaStream_t stream)
 {
     fill_kv<<<4096, 256, 0, stream>>>(host_sm64(data_seed, 0), host_sm64(data_seed, 1),
-                                      host_sm64(data_seed, 2), B, H, d, t_begin, n, k_log_sigma,
+                                      host_sm64(data_seed, 2), B, H, d, t_begin, n, b_offset, k_log_sigma,
                                       v_dist, k_out, v_out);
     return (int)cudaGetLastError();
 }
