@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Benchmark of the TurboQuant KV-codec hot path on GB300.
+
+One step is one pass of the whole path over one batch of synthetic input:
+  1. append  -- quantise a prefill batch (4 seq x 8 kv-heads x 8192 tokens x d128,
+                k8v3) into a packed cache (tq_encode_append);
+  2. fetch   -- dequantise a prefill cache back to bf16 K, V (tq_decode); two
+                caches alternate, so the fetch reads rows written a step earlier,
+                never rows the append just left in L2;
+  3. decode  -- one decode step of the serving workload (32 seq x 64 q-heads over
+                8 kv-heads, 32768 cached tokens): append the new token of every
+                sequence, then fused dequantise-on-fetch attention over 32769
+                rows (tq_decode_attention).
+Every input of a step (134 MB + 134 MB bf16, a 52 MB cache, the 1.68 GB decode
+cache) is larger than L2 or was evicted by the rest of the step.
+
+value = algorithmic bytes of the whole step / step time (GB/s), the bytes being
+the codec's format traffic: bf16 K/V in and packed rows out for the append,
+packed rows in and bf16 out for the fetch, every cached row (200 B per
+token-head) plus q and the output for the attention.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV codec encode/decode GB/s and fused dequant-attn µs/step, % of HBM roofline"
+PREFILL = dict(B=4, H=8, T=8192, d=128, kb=8, vb=3)
+DECODE = dict(B=32, H=8, QH=64, T=32768, d=128, kb=8, vb=3)
+BYTES_PER_TH = 200  # k8v3, d128 (page: "Bytes per token per head")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def algorithmic_bytes(prefill=PREFILL, decode=DECODE):
+    th_pre = prefill["B"] * prefill["H"] * prefill["T"]
+    bf16_row = 2 * prefill["d"] * 2  # K and V bf16
+    enc = th_pre * (bf16_row + BYTES_PER_TH)
+    dec = th_pre * (BYTES_PER_TH + bf16_row)
+    th_new = decode["B"] * decode["H"]
+    app = th_new * (2 * decode["d"] * 2 + BYTES_PER_TH)
+    attn = decode["B"] * decode["H"] * (decode["T"] + 1) * BYTES_PER_TH \
+        + decode["B"] * decode["QH"] * decode["d"] * (2 + 4)  # q in (bf16), out (fp32)
+    return dict(encode=enc, decode=dec, append=app, attention=attn, total=enc + dec + app + attn)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attention_traffic(kernel_hash: str):
+    """DRAM bytes per launch of the attention kernel at this workload, from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "attention_decode_traffic.txt")
+    try:
+        kv = {}
+        with open(p) as f:
+            for line in f:
+                if "=" in line and not line.lstrip().startswith("#"):
+                    k, v = line.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != kernel_hash:
+            return None
+        return float(kv["dram_bytes_per_launch_full_workload"])
+    except Exception:
+        return None
+
+
+def kernel_source_hash() -> str:
+    p = os.path.join(ROOT, "rotated_kv_cache_gb300", "csrc", "tq_attention.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        busy = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from rotated_kv_cache_gb300 import build as libbuild
+
+    libbuild.build()
+    import rotated_kv_cache_gb300 as tq
+    import tq_synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    P, D = PREFILL, DECODE
+    wp, wd = tq_synth.WORKLOADS["prefill"], tq_synth.WORKLOADS["decode"]
+
+    # --- prefill inputs and two caches
+    kp = torch.empty((P["B"], P["H"], P["T"], P["d"]), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    tq_synth.device_kv(wp, kp, vp)
+    pre = [tq.Cache(P["B"], P["H"], P["d"], P["T"], P["kb"], P["vb"], device=dev) for _ in range(2)]
+    for c in pre:
+        tq.tq_encode_append(c, kp, vp, 0)
+    ko = torch.empty_like(kp)
+    vo = torch.empty_like(kp)
+
+    # --- decode cache: the context is generated and encoded in chunks of sequences
+    T = D["T"]
+    dcache = tq.Cache(D["B"], D["H"], D["d"], T + 1, D["kb"], D["vb"], device=dev)
+    for b0 in range(0, D["B"], 4):
+        kc = torch.empty((4, D["H"], T + 1, D["d"]), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        tq_synth.device_kv(wd, kc, vc, B=4, n=T + 1, b_offset=b0)
+        tq.tq_encode_append(dcache.batch_slice(b0, 4), kc[:, :, :T], vc[:, :, :T], 0)
+        del kc, vc
+    knew = torch.empty((D["B"], D["H"], 1, D["d"]), dtype=torch.bfloat16, device=dev)
+    vnew = torch.empty_like(knew)
+    tq_synth.device_kv(wd, knew, vnew, t_begin=T, n=1)
+    q = torch.empty((D["B"], D["QH"], D["d"]), dtype=torch.bfloat16, device=dev)
+    tq_synth.device_q(wd, 0, q)
+    out = torch.empty((D["B"], D["QH"], D["d"]), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attention_workspace_bytes(dcache, D["QH"], T + 1), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+
+    def step(s, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tq.tq_encode_append(pre[s % 2], kp, vp, 0)
+        if ev is not None:
+            ev[1].record(stream)
+        tq.tq_decode(pre[(s + 1) % 2], 0, P["T"], dtype=torch.bfloat16, k_out=ko, v_out=vo)
+        if ev is not None:
+            ev[2].record(stream)
+        tq.tq_encode_append(dcache, knew, vnew, T)  # the step's new token, row T
+        if ev is not None:
+            ev[3].record(stream)
+        tq.tq_decode_attention(dcache, q, T + 1, out=out, workspace=ws)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    assert tq.tq_device_error() == 0
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        t0.record(stream)
+        for s in range(K):
+            step(s, evs[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    parts = {"encode": 0.0, "decode": 0.0, "append": 0.0, "attention": 0.0}
+    for e in evs:
+        parts["encode"] += e[0].elapsed_time(e[1])
+        parts["decode"] += e[1].elapsed_time(e[2])
+        parts["append"] += e[2].elapsed_time(e[3])
+        parts["attention"] += e[3].elapsed_time(e[4])
+    parts = {k: v / K for k, v in parts.items()}
+    assert tq.tq_device_error() == 0
+
+    # --- end to end through the public API with pinned host buffers
+    kp_h, vp_h = kp.cpu().pin_memory(), vp.cpu().pin_memory()
+    kn_h, vn_h, q_h = knew.cpu().pin_memory(), vnew.cpu().pin_memory(), q.cpu().pin_memory()
+    ko_h, vo_h = torch.empty_like(kp_h).pin_memory(), torch.empty_like(vp_h).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step(s):
+        kp.copy_(kp_h, non_blocking=True)
+        vp.copy_(vp_h, non_blocking=True)
+        knew.copy_(kn_h, non_blocking=True)
+        vnew.copy_(vn_h, non_blocking=True)
+        q.copy_(q_h, non_blocking=True)
+        step(s)
+        ko_h.copy_(ko, non_blocking=True)
+        vo_h.copy_(vo, non_blocking=True)
+        out_h.copy_(out, non_blocking=True)
+
+    Ke = max(3, min(K, 20))
+    e2e_step(0)
+    torch.cuda.synchronize()
+    a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(Ke):
+        e2e_step(s)
+    bb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(bb) / Ke
+    h2d = sum(t.numel() * t.element_size() for t in (kp_h, vp_h, kn_h, vn_h, q_h))
+    d2h = sum(t.numel() * t.element_size() for t in (ko_h, vo_h, out_h))
+
+    # --- aggregate over ranks (max time)
+    ms = elapsed_ms / K
+    if world > 1:
+        tt = torch.tensor([ms, e2e_ms] + [parts[k] for k in ("encode", "decode", "append", "attention")],
+                          dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(tt[0]), float(tt[1])
+        parts = dict(zip(("encode", "decode", "append", "attention"), [float(x) for x in tt[2:]]))
+    if rank != 0:
+        return None
+
+    ab = algorithmic_bytes()
+    peak, peak_kind = measured_peaks()
+    gbs = lambda nbytes, t_ms: nbytes / (t_ms * 1e-3) / 1e9  # noqa: E731
+    value = world * ab["total"] / (ms * 1e-3) / 1e9
+    attn_gbs = gbs(ab["attention"], parts["attention"])
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 streams: K ~ N(0,1) x per-channel logN(0,1.5), V ~ Student-t5)",
+        "config": {
+            "workload": "prefill append+fetch (4x8192 tokens x 8 kv-heads x d128, k8v3) + decode step "
+                        "(32 seq x 64 q-heads / 8 kv-heads, 32768 cached tokens + 1 appended, d128, k8v3)",
+            "l2": "inputs larger than L2; the fetch reads the cache appended a step earlier (two caches alternate)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "algorithmic_bytes_per_step": ab["total"],
+        },
+        "parts": {
+            "encode": {"us": round(parts["encode"] * 1e3, 2), "GB/s": round(gbs(ab["encode"], parts["encode"]), 1),
+                       "frac": round(gbs(ab["encode"], parts["encode"]) / peak, 4)},
+            "decode": {"us": round(parts["decode"] * 1e3, 2), "GB/s": round(gbs(ab["decode"], parts["decode"]), 1),
+                       "frac": round(gbs(ab["decode"], parts["decode"]) / peak, 4)},
+            "append_1_token": {"us": round(parts["append"] * 1e3, 2)},
+            "attention": {"us_per_step": round(parts["attention"] * 1e3, 2), "GB/s": round(attn_gbs, 1),
+                          "frac": round(attn_gbs / peak, 4)},
+            "decode_step_us": round((parts["append"] + parts["attention"]) * 1e3, 2),
+        },
+        "roofline": {
+            "kernel": "attn_split_kernel + attn_combine_kernel (timed together through tq_decode_attention)",
+            "bound": "hbm",
+            "achieved": round(attn_gbs, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": round(attn_gbs / peak, 4),
+            "traffic": attention_traffic(kernel_source_hash()),
+            "algorithmic_bytes_per_launch": ab["attention"],
+        },
+        "e2e": {"value": round(world * ab["total"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": 8 * K,
+        "clocks": clocks.summary(),
+    }
+    return line
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline and reference arm)
+class OracleSample:
+    """A bounded slice of the same workload for the CPU oracle: append + fetch of
+    `pre_rows` prefill tokens (all 4 x 8 sequence-heads), and the decode step's
+    attention for `pairs` (sequence, kv-head) pairs (8 q-heads each)."""
+
+    def __init__(self, pre_rows: int, pairs: int):
+        import numpy as np
+
+        import oracle
+        import tq_synth
+
+        self.oracle = oracle
+        P, D = PREFILL, DECODE
+        wp, wd = tq_synth.WORKLOADS["prefill"], tq_synth.WORKLOADS["decode"]
+        self.kp, self.vp = tq_synth.host_kv(wp, n=pre_rows)
+        self.planes = oracle.Planes(P["B"], P["H"], P["d"], P["kb"], P["vb"], (pre_rows + 15) // 16 * 16)
+        oracle.encode(self.planes, self.kp, self.vp)
+        self.pre_rows = pre_rows
+        T = D["T"]
+        self.att = []
+        b = 5  # one sequence; its kv-heads 0 .. pairs-1, 8 q-heads each
+        k, v = tq_synth.host_kv(wd, B=1, H=D["H"], n=T + 1, b_offset=b)
+        qall = tq_synth.host_q(wd, 0, B=D["B"], QH=D["QH"])
+        for h in range(pairs):
+            pl = oracle.Planes(1, 1, D["d"], D["kb"], D["vb"], T + 16)
+            oracle.encode(pl, np.ascontiguousarray(k[:, h:h + 1]), np.ascontiguousarray(v[:, h:h + 1]))
+            self.att.append((pl, np.ascontiguousarray(qall[b:b + 1, 8 * h:8 * h + 8])))
+        th = P["B"] * P["H"] * pre_rows
+        self.bytes = th * (512 + 200) * 2 + pairs * ((T + 1) * BYTES_PER_TH + 8 * D["d"] * 6)
+        self.desc = (f"append+fetch of {pre_rows} tokens x 32 sequence-heads of the prefill batch, and the "
+                     f"decode-step attention of {pairs} (sequence, kv-head) pairs x 8 q-heads over 32769 rows")
+
+    def run_once(self):
+        o = self.oracle
+        o.encode(self.planes, self.kp, self.vp)
+        o.decode(self.planes, 0, self.pre_rows)
+        for pl, q in self.att:
+            o.attention(pl, q, DECODE["T"] + 1)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    cores = cpu_cores()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    sample = OracleSample(pre_rows=256, pairs=2)
+    for _ in range(args.warmup):
+        sample.run_once()
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        sample.run_once()
+        times.append(time.perf_counter() - t)
+    per = sum(times) / len(times)
+    value = sample.bytes / per / 1e9
+    return {
+        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (same seeded streams)",
+        "config": {"workload": "same as the CUDA arm, bounded sample per step", "sample": sample.desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample.desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline():
+    cores = cpu_cores()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    sample = OracleSample(pre_rows=1024, pairs=8)
+    sample.run_once()
+    t = time.perf_counter()
+    sample.run_once()
+    dt = time.perf_counter() - t
+    return {"value": round(sample.bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample.desc, "seconds": round(dt, 2)}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    baseline = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        baseline = cpu_baseline()
+    if rank == 0:
+        line["cpu_baseline"] = baseline
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
