@@ -174,16 +174,17 @@ def run_ours(args, rank, world, local_rank):
     T = D["T"]
     dcache = tq.Cache(D["B"], D["H"], D["d"], T + 1, D["kb"], D["vb"], device=dev)
     for b0 in range(0, D["B"], 4):
-        kc = torch.empty((4, D["H"], T + 1, D["d"]), dtype=torch.bfloat16, device=dev)
+        nb = min(4, D["B"] - b0)
+        kc = torch.empty((nb, D["H"], T + 1, D["d"]), dtype=torch.bfloat16, device=dev)
         vc = torch.empty_like(kc)
-        tq_synth.device_kv(wd, kc, vc, B=4, n=T + 1, b_offset=b0)
-        tq.tq_encode_append(dcache.batch_slice(b0, 4), kc[:, :, :T], vc[:, :, :T], 0)
+        tq_synth.device_kv(wd, kc, vc, B=nb, n=T + 1, b_offset=b0)
+        tq.tq_encode_append(dcache.batch_slice(b0, nb), kc[:, :, :T], vc[:, :, :T], 0)
         del kc, vc
     knew = torch.empty((D["B"], D["H"], 1, D["d"]), dtype=torch.bfloat16, device=dev)
     vnew = torch.empty_like(knew)
-    tq_synth.device_kv(wd, knew, vnew, t_begin=T, n=1)
+    tq_synth.device_kv(wd, knew, vnew, B=D["B"], t_begin=T, n=1)
     q = torch.empty((D["B"], D["QH"], D["d"]), dtype=torch.bfloat16, device=dev)
-    tq_synth.device_q(wd, 0, q)
+    tq_synth.device_q(wd, 0, q, B=D["B"])
     out = torch.empty((D["B"], D["QH"], D["d"]), dtype=torch.float32, device=dev)
     ws = torch.empty(tq.tq_attention_workspace_bytes(dcache, D["QH"], T + 1), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -422,9 +423,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
+                    help="sequences of the decode step (smaller values for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    DECODE["B"] = args.decode_batch
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

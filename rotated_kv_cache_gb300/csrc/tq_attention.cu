@@ -10,10 +10,12 @@
 //
 // GB300 design (one GPU, sm_103a):
 //  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
-//    a 4-stage shared-memory ring.  A producer warp issues, per 64-token
-//    stage, one 2-D TMA load of the key codes (128/64-byte swizzle, so the
-//    per-row fragment reads of the MMA are bank-conflict-free) and four 1-D
-//    bulk copies of the other planes, completing on the stage's mbarrier.
+//    a 3-stage shared-memory ring; each of its 4 warps takes 16 tokens of a
+//    64-token stage.  A stage is one 2-D TMA load of the key codes (128/64-byte
+//    swizzle, so the per-row fragment reads of the MMA are bank-conflict-free)
+//    and four 1-D bulk copies of the other planes, completing on the slot's
+//    mbarrier; the last warp to finish a stage issues the copies that refill
+//    its slot, so no warp is set aside as a producer (4 CTAs fit on an SM).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
 //    tokens, N = the G = 8 q-heads sharing the kv-head, K = head_dim.  Key codes
 //    become exact f16 integers with one XOR and byte permutes (1024 + code), so
@@ -40,10 +42,10 @@ namespace {
 constexpr int kD = 128;            // head_dim covered
 constexpr int kG = 8;              // q-heads per kv-head
 constexpr int kVB = 3;             // value bits covered
-constexpr int kCW = 4;             // compute warps
-constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kCW = 4;             // warps per CTA (all compute; the last to finish a stage refills it)
+constexpr int kThreads = kCW * 32;
 constexpr int kStageT = 64;        // tokens per stage
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -59,8 +61,9 @@ struct AGeo {
     static constexpr int OFF_VS = OFF_KZ + SC_BYTES;
     static constexpr int OFF_V = OFF_VS + SC_BYTES;
     static constexpr int STAGE = round_up(OFF_V + V_BYTES + 16, 1024);  // 1024: swizzle atom alignment
-    static constexpr int MERGE = kCW * kG * (kD + 2) * 4;             // per-warp partials
-    static constexpr int SMEM = 1024 /*align slack*/ + kStages * STAGE + (MERGE > 0 ? MERGE : 0) + 2 * kStages * 8;
+    static constexpr int MERGE = kCW * kG * (kD + 2) * 4;             // per-warp partials (reuse the ring)
+    static constexpr int RING = kStages * STAGE > MERGE ? kStages * STAGE : MERGE;
+    static constexpr int SMEM = 1024 /*align slack*/ + RING + kStages * 8 /*full barriers*/ + kStages * 4 /*counters*/;
     static constexpr float OFFSET = KB == 8 ? 1152.0f : 1024.0f;    // f16 value = OFFSET + code
 };
 
@@ -75,6 +78,7 @@ struct AttnParams {
     float scale_log2;  // softmax_scale * log2(e)
     uint32_t *err;
     uint32_t tl0, tl1, th0, th1;  // f16 centroid bytes: low bytes (c0..c7), high bytes
+    uint32_t k_const, k_flip;     // key byte -> f16 (1024 + byte ^ 0x80) as one logic op (see below)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -139,33 +143,45 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void named_barrier_sync(int id, int threads)
+// Byte permute, default mode (used as an 8-entry table lookup: each selector
+// nibble 0..7 picks one byte of the table held in a and b).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
 }
 
-// f16 pair (c[code0], c[code1]) from s = code0 | code1 << 16 (3-bit codes):
-// byte-permute lookups into the low-byte and high-byte tables of c[0..7].
-__device__ __forceinline__ uint32_t centroid_pair(uint32_t s, const AttnParams &p)
+// Key codes -> a pair of exact f16 integers in one 3-input logic op: where
+// k_const has a bit set the result takes k_flip's bit (the f16 exponent
+// pattern of 1024), elsewhere the code bit xor k_flip's bit (0x80 turns an
+// int8 code into offset binary).  The f16 value is 1024 + (offset) code.
+__device__ __forceinline__ uint32_t kcvt(uint32_t w, const AttnParams &p)
 {
-    const uint32_t sel = __byte_perm(s, 0u, 0x0020u);  // nibble0 = code0, nibble2 = code1
-    const uint32_t lo = __byte_perm(p.tl0, p.tl1, sel);
-    const uint32_t hi = __byte_perm(p.th0, p.th1, sel << 4);
-    return (lo & 0x00FF00FFu) | (hi & 0xFF00FF00u);
+    return (p.k_const & p.k_flip) | (~p.k_const & (w ^ p.k_flip));
+}
+
+// Right shift done on the multiply-add pipe (the integer/logic pipe is the
+// bottleneck of this kernel): x >> k == high word of x * 2^(32-k).
+template <int K>
+__device__ __forceinline__ uint32_t shr_fma(uint32_t x)
+{
+    return __umulhi(x, 1u << (32 - K));
 }
 
 // ---------------------------------------------------------------- the split kernel
 template <int KB>
-__global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                   const __grid_constant__ AttnParams p)
 {
     using A = AGeo<KB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    float *merge = reinterpret_cast<float *>(smem + kStages * A::STAGE);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * A::STAGE + A::MERGE);
-    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStages);
+    float *merge = reinterpret_cast<float *>(smem);  // after the loop, reuses the ring
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + A::RING);
+    uint32_t *done = reinterpret_cast<uint32_t *>(smem + A::RING + kStages * 8);
+    const uint32_t full0 = smem_addr(bars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -174,35 +190,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_co
     const int64_t t_end = imin64(p.seq_len, t_begin + p.tokens_per_split);
     const int n_stages = t_end > t_begin ? (int)((t_end - t_begin + kStageT - 1) / kStageT) : 0;
 
+    // stage s -> ring slot s % kStages: one 2-D TMA load (key codes) and four
+    // 1-D bulk copies (the other planes) completing on the slot's barrier
+    auto issue = [&](int s) {
+        const int slot = s % kStages;
+        const int64_t t = t_begin + (int64_t)s * kStageT;
+        const int rows = (int)imin64(kStageT, p.cap - t);  // multiple of 16
+        const int64_t row0 = bh * p.cap + t;
+        const uint32_t st = smem_addr(stages + slot * A::STAGE), bar = full0 + 8 * slot;
+        mbar_arrive_expect_tx(bar, (uint32_t)(A::K_BYTES + rows * (3 * (kD / 32) * 2 + kD * kVB / 8)));
+        tma_load_2d(st + A::OFF_K, &kmap, 0, (int)row0, bar);
+        bulk_g2s(st + A::OFF_KS, p.k_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
+        bulk_g2s(st + A::OFF_KZ, p.k_zero + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
+        bulk_g2s(st + A::OFF_VS, p.v_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
+        bulk_g2s(st + A::OFF_V, p.v_codes + row0 * (kD * kVB / 8), rows * (kD * kVB / 8), bar);
+    };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kCW);
+            done[s] = 0;
         }
         fence_mbar_init();
+        for (int s = 0; s < kStages && s < n_stages; ++s) issue(s);
     }
     __syncthreads();
-
-    if (warp == kCW) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            for (int s = 0; s < n_stages; ++s) {
-                const int slot = s % kStages, k = s / kStages;
-                if (k > 0 && !mbar_wait_bounded(empty0 + 8 * slot, (k - 1) & 1, p.err)) break;
-                const int64_t t = t_begin + (int64_t)s * kStageT;
-                const int rows = (int)imin64(kStageT, p.cap - t);  // multiple of 16
-                const int64_t row0 = bh * p.cap + t;
-                const uint32_t st = smem_addr(stages + slot * A::STAGE), bar = full0 + 8 * slot;
-                mbar_arrive_expect_tx(bar, (uint32_t)(A::K_BYTES + rows * (3 * (kD / 32) * 2 + kD * kVB / 8)));
-                tma_load_2d(st + A::OFF_K, &kmap, 0, (int)row0, bar);
-                bulk_g2s(st + A::OFF_KS, p.k_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
-                bulk_g2s(st + A::OFF_KZ, p.k_zero + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
-                bulk_g2s(st + A::OFF_VS, p.v_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
-                bulk_g2s(st + A::OFF_V, p.v_codes + row0 * (kD * kVB / 8), rows * (kD * kVB / 8), bar);
-            }
-        }
-        return;
-    }
 
     // ---------------------------------------------------------------- compute warps
     const int g = lane >> 2, c = lane & 3;
@@ -251,11 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_co
             for (int i = 0; i < 8; ++i) s += f[i];
             qsum[G] = s;
             if constexpr (KB == 8) {
-                // codes of dims 8c+{0..3} (word 0) then 8c+{4..7} (word 1), pairs in order
-                bq[2 * G][0] = hw[0];
-                bq[2 * G][1] = hw[1];
-                bq[2 * G + 1][0] = hw[2];
-                bq[2 * G + 1][1] = hw[3];
+                // a word holds dims 8c+{0..3} (then {4..7}); its bytes pair as (0, 2), (1, 3)
+                auto pr = [&](int i, int j) { return pack_f16x2(f[i], f[j]); };
+                bq[2 * G][0] = pr(0, 2);
+                bq[2 * G][1] = pr(1, 3);
+                bq[2 * G + 1][0] = pr(4, 6);
+                bq[2 * G + 1][1] = pr(5, 7);
             } else {
                 // nibble k of the word = dim 8c+k; unpacked pairs are (k, k+4)
                 auto pr = [&](int i, int j) { return pack_f16x2(f[i], f[j]); };
@@ -313,26 +325,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_co
                 // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
                 const uint32_t chunk = (uint32_t)((2 * G + (c >> 1)) ^ g);
                 const uint32_t off = (chunk << 4) + ((c & 1) << 3);
-                uint2 k0 = lds64(st + A::OFF_K + r0 * A::KROW + off);
-                uint2 k1 = lds64(st + A::OFF_K + r1 * A::KROW + off);
-                k0.x ^= 0x80808080u; k0.y ^= 0x80808080u;
-                k1.x ^= 0x80808080u; k1.y ^= 0x80808080u;
-                const uint32_t C = 0x64646464u;
-                mma16816(acc[G], __byte_perm(k0.x, C, 0x4140), __byte_perm(k1.x, C, 0x4140),
-                         __byte_perm(k0.x, C, 0x4342), __byte_perm(k1.x, C, 0x4342), bq[2 * G][0], bq[2 * G][1]);
-                mma16816(acc[G], __byte_perm(k0.y, C, 0x4140), __byte_perm(k1.y, C, 0x4140),
-                         __byte_perm(k0.y, C, 0x4342), __byte_perm(k1.y, C, 0x4342), bq[2 * G + 1][0],
-                         bq[2 * G + 1][1]);
+                const uint2 k0 = lds64(st + A::OFF_K + r0 * A::KROW + off);
+                const uint2 k1 = lds64(st + A::OFF_K + r1 * A::KROW + off);
+                // bytes 0 and 2 (then 1 and 3) of a word -> f16 (1024 + (byte ^ 0x80)):
+                // dims (8c+0, 8c+2), (8c+1, 8c+3), then +4
+                mma16816(acc[G], kcvt(k0.x, p), kcvt(k1.x, p), kcvt(shr_fma<8>(k0.x), p), kcvt(shr_fma<8>(k1.x), p),
+                         bq[2 * G][0], bq[2 * G][1]);
+                mma16816(acc[G], kcvt(k0.y, p), kcvt(k1.y, p), kcvt(shr_fma<8>(k0.y), p), kcvt(shr_fma<8>(k1.y), p),
+                         bq[2 * G + 1][0], bq[2 * G + 1][1]);
             } else {
                 // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
                 const uint32_t off = ((uint32_t)(G ^ ((g >> 1) & 3)) << 4) + 4 * c;
                 const uint32_t w0 = lds32(st + A::OFF_K + r0 * A::KROW + off);
                 const uint32_t w1 = lds32(st + A::OFF_K + r1 * A::KROW + off);
-                const uint32_t M = 0x000F000Fu, C = 0x64006400u;
-                mma16816(acc[G], (w0 & M) | C, (w1 & M) | C, ((w0 >> 4) & M) | C, ((w1 >> 4) & M) | C, bq[2 * G][0],
+                // nibbles k and k+4 -> f16 (1024 + nibble)
+                mma16816(acc[G], kcvt(w0, p), kcvt(w1, p), kcvt(shr_fma<4>(w0), p), kcvt(shr_fma<4>(w1), p), bq[2 * G][0],
                          bq[2 * G][1]);
-                mma16816(acc[G], ((w0 >> 8) & M) | C, ((w1 >> 8) & M) | C, ((w0 >> 12) & M) | C,
-                         ((w1 >> 12) & M) | C, bq[2 * G + 1][0], bq[2 * G + 1][1]);
+                mma16816(acc[G], kcvt(shr_fma<8>(w0), p), kcvt(shr_fma<8>(w1), p), kcvt(shr_fma<12>(w0), p),
+                         kcvt(shr_fma<12>(w1), p), bq[2 * G + 1][0], bq[2 * G + 1][1]);
             }
         }
         // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum)
@@ -361,26 +371,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_co
             }
         }
         // ---------------- online softmax (base 2) for heads 2c, 2c+1
+        // The running max is reduced across the tile's rows only when some lane
+        // sees a score above it (or no max exists yet); otherwise the weights
+        // are 2^(S - m) with the max unchanged, which is the same arithmetic.
         float pr[2][2];
+        const bool raise = S[0][0] > m_run[0] || S[1][0] > m_run[0] || S[0][1] > m_run[1] || S[1][1] > m_run[1] ||
+                           m_run[0] == -INFINITY || m_run[1] == -INFINITY;
+        if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float mt = fmaxf(S[0][j], S[1][j]);
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-            const float mn = fmaxf(m_run[j], mt);
-            const float mu = mn == -INFINITY ? 0.0f : mn;
-            const float alpha = ex2(m_run[j] - mu);
-            m_run[j] = mn;
-            pr[0][j] = ex2(S[0][j] - mu);
-            pr[1][j] = ex2(S[1][j] - mu);
-            l_run[j] = l_run[j] * alpha + pr[0][j] + pr[1][j];
-            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+            for (int j = 0; j < 2; ++j) {
+                float mt = fmaxf(S[0][j], S[1][j]);
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                const float mn = fmaxf(m_run[j], mt);
+                const float mu = mn == -INFINITY ? 0.0f : mn;
+                const float alpha = ex2(m_run[j] - mu);
+                m_run[j] = mn;
+                pr[0][j] = ex2(S[0][j] - mu);
+                pr[1][j] = ex2(S[1][j] - mu);
+                l_run[j] = l_run[j] * alpha + pr[0][j] + pr[1][j];
 #pragma unroll
                 for (int mt2 = 0; mt2 < 8; ++mt2) {
                     o[mt2][j] *= alpha;
                     o[mt2][2 + j] *= alpha;
                 }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                pr[0][j] = ex2(S[0][j] - m_run[j]);
+                pr[1][j] = ex2(S[1][j] - m_run[j]);
+                l_run[j] += pr[0][j] + pr[1][j];
             }
         }
         // ---------------- P^T as the B operand (tokens x heads), transposed in registers
@@ -389,9 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_co
         // value scales of this lane's four tokens (zero past the range)
         uint2 vs[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            vs[q] = lds64(st + A::OFF_VS + vr[q] * 8);
-            if (tile_t0 + (vr[q] - 16 * warp) >= t_end) vs[q] = make_uint2(0u, 0u);
+        for (int q = 0; q < 4; ++q) vs[q] = lds64(st + A::OFF_VS + vr[q] * 8);
+        if (tile_t0 + 16 > t_end) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (tile_t0 + (vr[q] - 16 * warp) >= t_end) vs[q] = make_uint2(0u, 0u);
         }
         // ---------------- O^T += V^T P'^T, per value group
 #pragma unroll
@@ -402,26 +426,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_co
             const uint32_t sp1 = __byte_perm(G < 2 ? vs[2].x : vs[2].y, G < 2 ? vs[3].x : vs[3].y,
                                              sh ? 0x7632u : 0x5410u);
             const uint32_t b0 = hmul2(pt0, sp0), b1 = hmul2(pt1, sp1);
+            uint32_t av[2][2][2];  // [token pair][m-tile half][row g, row g+8]
+            // 12-bit fields (codes of dims 32G + 4g + 0..3 at bits 0, 3, 6, 9) of
+            // the lane's four tokens; bits above 11 are don't-care
             uint32_t x[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t base = st + A::OFF_V + vr[q] * (kD * kVB / 8) + 4 * (3 * G + v_word);
-                x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift) & 0xFFFu;
+                x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
             }
-            const uint32_t z01 = x[0] | (x[1] << 16), z23 = x[2] | (x[3] << 16);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int r = 2 * half;
-                const uint32_t a0 = centroid_pair((z01 >> (3 * r)) & 0x00070007u, p);
-                const uint32_t a1 = centroid_pair((z01 >> (3 * r + 3)) & 0x00070007u, p);
-                const uint32_t a2 = centroid_pair((z23 >> (3 * r)) & 0x00070007u, p);
-                const uint32_t a3 = centroid_pair((z23 >> (3 * r + 3)) & 0x00070007u, p);
-                mma16816(o[2 * G + half], a0, a1, a2, a3, b0, b1);
+            for (int pr2 = 0; pr2 < 2; ++pr2) {  // token pairs (2c, 2c+1) and (2c+8, 2c+9)
+                // both tokens' fields side by side (first in bits 0-15), then one
+                // code per nibble: codes r0..r3 of the first token in nibbles
+                // 0..3, of the second in nibbles 4..7
+                const uint32_t w = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
+                const uint32_t y = (w & 0x003F003Fu) | ((w & 0x0FC00FC0u) * 4u);
+                const uint32_t e = (y & 0x07070707u) | ((y & 0x38383838u) * 2u);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    // selector: codes (r, r+1) of the first token, then of the second
+                    const uint32_t sel = __byte_perm(e, 0u, half ? 0x0031u : 0x0020u);
+                    const uint32_t lo = prmt(p.tl0, p.tl1, sel);  // low f16 bytes of the 4 centroids
+                    const uint32_t hi = prmt(p.th0, p.th1, sel);  // high f16 bytes
+                    av[pr2][half][0] = __byte_perm(lo, hi, 0x6240u);  // dim r: (first, second)
+                    av[pr2][half][1] = __byte_perm(lo, hi, 0x7351u);  // dim r + 1
+                }
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                mma16816(o[2 * G + half], av[0][half][0], av[0][half][1], av[1][half][0], av[1][half][1], b0, b1);
+        }
+        // the last warp to finish this stage refills its slot with stage s + kStages
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&done[slot], 1u) == kCW - 1) {
+                done[slot] = 0;
+                if (s + kStages < n_stages) issue(s + kStages);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
     }
+    __syncthreads();  // every warp is done with the ring before it holds the merge
 
     // ---------------------------------------------------------------- merge the warps
     // per-lane partial row sums -> per-head sums (lanes with equal c)
@@ -449,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const __grid_co
             mw[kG * kD + kG + 2 * c + j] = ok ? l_run[j] : 0.0f;
         }
     }
-    named_barrier_sync(1, kCW * 32);
+    __syncthreads();
     // 128 threads: thread -> (head, 8 dims)
     const int tid = threadIdx.x, hh = tid >> 4, d8 = (tid & 15) * 8;
     float mmax = -INFINITY;
@@ -651,6 +697,9 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     p.tl1 = lo[4] | lo[5] << 8 | lo[6] << 16 | (uint32_t)lo[7] << 24;
     p.th0 = hi[0] | hi[1] << 8 | hi[2] << 16 | (uint32_t)hi[3] << 24;
     p.th1 = hi[4] | hi[5] << 8 | hi[6] << 16 | (uint32_t)hi[7] << 24;
+    // bits where R1 is set take R2; the others take byte ^ R2 (flip bit 7 and 23)
+    p.k_const = KB == 8 ? 0xFF00FF00u : 0xFFF0FFF0u;
+    p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
 
     dim3 grid(plan.splits, c.H, c.B);
     attn_split_kernel<KB><<<grid, kThreads, A::SMEM, s>>>(map, p);

@@ -211,8 +211,8 @@ __device__ __forceinline__ void pack_group(const uint32_t (&c)[32], uint32_t (&w
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int bit = i * B, word = bit >> 5, off = bit & 31;
-        w[word] |= c[i] << off;
-        if (off + B > 32) w[word + 1] |= c[i] >> (32 - off);
+        w[word] += c[i] << off;  // fields do not overlap: add == or (one IMAD)
+        if (off + B > 32) w[word + 1] += c[i] >> (32 - off);
     }
 }
 

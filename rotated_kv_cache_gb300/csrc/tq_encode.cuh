@@ -103,14 +103,32 @@ __device__ __forceinline__ void key_group(const float (&x)[32], uint32_t (&code)
         lo = 0.0f;
         hi = maxv;
     }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float r = __fsub_rn(__fdiv_rn(x[j], scale), zero);
-        // clip (NaN -> lo, IEEE maxNum/minNum), then round to nearest even by
-        // the 1.5*2^23 shift: |value| <= 127 so the integer lands in the low bits
-        const float c = fminf(fmaxf(r, lo), hi);
+    // idx = clip(round(x/scale - zero)): clip first (NaN -> lo, IEEE maxNum/
+    // minNum), then round to nearest even by the 1.5*2^23 shift (|value| <= 127,
+    // so the integer lands in the low bits).
+    auto code_of = [&](float q) {
+        const float c = fminf(fmaxf(__fsub_rn(q, zero), lo), hi);
         const uint32_t t = __float_as_uint(__fadd_rn(c, 12582912.0f)) - 0x4B400000u;
-        code[j] = BITS == 8 ? (t & 0xFFu) : t;
+        return BITS == 8 ? (t & 0xFFu) : t;
+    };
+    if (scale >= 0x1p-100f && scale <= 0x1p100f) {
+        // x/scale correctly rounded without a division (Markstein's theorem:
+        // with rc = RN(1/scale) and q0 within one ulp of x/scale, q0 + (x -
+        // scale*q0)*rc rounds to RN(x/scale)).  Bf16 keys inside a group with
+        // max != min keep |x/scale| <= 254*2^8, so nothing overflows; a
+        // quotient small enough to be inexact is below 1/4 and rounds to the
+        // same code either way.
+        const float rc = __frcp_rn(scale);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float q0 = __fmul_rn(x[j], rc);
+            const float e = __fmaf_rn(-scale, q0, x[j]);
+            code[j] = code_of(__fmaf_rn(e, rc, q0));
+        }
+    } else {
+        // zero, subnormal, huge, Inf or NaN scale: IEEE division
+#pragma unroll
+        for (int j = 0; j < 32; ++j) code[j] = code_of(__fdiv_rn(x[j], scale));
     }
     sc = f32_to_f16_bits(scale);
     zr = f32_to_f16_bits(zero);
@@ -257,8 +275,33 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
         const float sigma = __fsqrt_rn(__fdiv_rn(ss, 32.0f));
         const float den = __fadd_rn(sigma, 1e-8f);
         uint32_t code[32];
+        if (den < INFINITY) {
+            // The index counts the boundaries b below y/den.  Comparing y with
+            // b*den instead needs no division; the two can differ only when
+            // y/den lies within a few ulps of a boundary.
+            if constexpr (BITS <= 3) {
+                constexpr int H = 1 << (BITS - 1);  // the table is antisymmetric, b[H-1] = 0
+                float P[H - 1];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) code[j] = value_index<BITS>(p, sbnd, __fdiv_rn(y[j], den));
+                for (int k = 0; k < H - 1; ++k) P[k] = __fmul_rn(p.bnd[H + k], den);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float a = fabsf(y[j]);
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int k = 0; k < H - 1; ++k) m += a > P[k] ? 1u : 0u;
+                    code[j] = y[j] > 0.0f ? H + m : H - 1 - m;
+                }
+            } else {
+                const float rden = __frcp_rn(den);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) code[j] = value_index<BITS>(p, sbnd, __fmul_rn(y[j], rden));
+            }
+        } else {
+            // non-finite row (Inf/NaN inputs): the definition step by step
+#pragma unroll
+            for (int j = 0; j < 32; ++j) code[j] = value_index<BITS>(p, sbnd, __fdiv_rn(y[j], den));
+        }
         uint32_t gw[BITS];
         pack_group<BITS>(code, gw);
 #pragma unroll

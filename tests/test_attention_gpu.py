@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import tq_synth
-from tqtest import f16_equal, planes_from_device, to_device_bf16
+from tqtest import compare_value_codes, f16_equal, planes_from_device, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -136,10 +136,18 @@ def _full_size_check(tq, w, B, samples, chunk_b=4):
         v = vd[:, h:h + 1].cpu().view(torch.int16).numpy().view(np.uint16)
         ref = oracle.Planes(1, 1, d, w.kb, w.vb, cache.capacity)
         oracle.encode(ref, k, v)
-        for a, src in zip(ref.arrays(), cache.planes()):
+        g = oracle.Planes(1, 1, d, w.kb, w.vb, cache.capacity)
+        for a, ga, src in zip(ref.arrays(), g.arrays(), cache.planes()):
             got = src[b, h, :T + 1].cpu().numpy().view(a.dtype)
+            ga[0, 0, :T + 1] = got
+            if a is ref.v_codes:
+                continue
             assert (f16_equal(got, a[0, 0, :T + 1]).all() if a.dtype == np.uint16
                     else np.array_equal(got, a[0, 0, :T + 1])), "device cache differs from the oracle encoding"
+        rows = [(0, 0, int(t)) for t in np.nonzero(np.any(g.v_codes[0, 0, :T + 1] != ref.v_codes[0, 0, :T + 1],
+                                                             axis=-1))[0]]
+        bad, exempt = compare_value_codes(g, ref, oracle.bf16_bits_to_f32(v), rows, 0) if rows else (0, 0)
+        assert bad == 0 and exempt <= 1e-5 * v.size, (bad, exempt)
         want = oracle.attention(ref, qh[b:b + 1, h * G:(h + 1) * G], T + 1)
         err = np.abs(out[b, h * G:(h + 1) * G] - want[0]).max()
         assert err < TOL, (b, h, err)
