@@ -57,7 +57,8 @@ typedef enum tq_status {
     TQ_ERR_ALIGN = 6,     /* pointer or stride not 16-byte aligned */
     TQ_ERR_WORKSPACE = 7, /* workspace missing or too small */
     TQ_ERR_CUDA = 8,      /* a CUDA launch or query failed */
-    TQ_ERR_UNSUPPORTED = 9 /* valid codec parameters this kernel does not cover */
+    TQ_ERR_UNSUPPORTED = 9, /* valid codec parameters this kernel does not cover */
+    TQ_ERR_SCRATCH = 10     /* too large for the library's built-in scratch (tq_decode_attention_noalloc) */
 } tq_status;
 
 typedef enum tq_dtype { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
@@ -163,6 +164,32 @@ TQ_API size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_head
 TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
                               float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
                               tq_stream_t stream);
+
+/*
+ * Decode attention without any device allocation -- the pages have no
+ * counterpart to this entry point; it exists for callers that cannot obtain
+ * scratch memory.  Same arguments, output and tolerance as tq_decode_attention
+ * minus the workspace.  Typical callers: code running inside another
+ * framework's memory manager that may not call cudaMalloc/cudaFree itself
+ * (both can synchronise the device and fragment a pool someone else owns),
+ * and plugin-style integrations with no allocator handle to pass a workspace
+ * from.
+ *  - Scratch: a fixed 16 MiB array inside the library, reserved on every GPU
+ *    that loads the library for the life of the process.  The split count is
+ *    reduced when needed so the partials fit; if even one split needs more
+ *    than 16 MiB (batch * num_kv_heads * q_heads/num_kv_heads * (d+2) * 4
+ *    bytes, i.e. batch * num_kv_heads > 4032 at 8 q-heads per kv-head, d=128),
+ *    the call returns TQ_ERR_SCRATCH and launches nothing.
+ *  - The first call on each device looks up the array's device address (a
+ *    runtime query, not an allocation); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero.  Calls whose kernels overlap on the
+ *    GPU (different streams, or different host threads) race on it: order
+ *    them.
+ */
+TQ_API tq_status tq_decode_attention_noalloc(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
+                                             float softmax_scale, float *out, tq_stream_t stream);
 
 /* 1 if tq_decode_attention covers these parameters, else 0. */
 TQ_API int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bits, int32_t group_size);

@@ -22,7 +22,7 @@ from . import build as _build
 __all__ = [
     "Cache", "TQError", "lib", "tq_bytes_per_token_head", "tq_sign_vector", "tq_codebook",
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
-    "tq_attention_supported", "tq_device_error", "tq_plane_bytes",
+    "tq_attention_supported", "tq_device_error", "tq_plane_bytes", "tq_decode_attention_noalloc",
 ]
 
 HEAD_DIMS = (64, 128, 256, 512)
@@ -33,7 +33,7 @@ TQ_BF16, TQ_F32 = 0, 1
 EXPORTS = (
     "tq_status_string", "tq_bytes_per_token_head", "tq_plane_bytes", "tq_sign_vector", "tq_codebook",
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
-    "tq_attention_supported", "tq_device_error",
+    "tq_attention_supported", "tq_device_error", "tq_decode_attention_noalloc",
 )
 
 
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
     so.tq_decode_attention.argtypes = [_CP, _P, _I32, _I64, ctypes.c_float, _P, _P, _SZ, _P]
     so.tq_attention_supported.argtypes = [_I32, _I32, _I32, _I32]
     so.tq_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    so.tq_decode_attention_noalloc.argtypes = [_CP, _P, _I32, _I64, ctypes.c_float, _P, _P]
     for name in EXPORTS:
         if name not in ("tq_status_string", "tq_bytes_per_token_head", "tq_attention_workspace_bytes",
                         "tq_attention_supported"):
@@ -246,6 +247,24 @@ def tq_decode_attention(cache: Cache, q: torch.Tensor, seq_len: int, softmax_sca
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().tq_decode_attention(ctypes.byref(s), q.data_ptr(), int(QH), int(seq_len), scale,
                                      out.data_ptr(), ws_ptr, ws_bytes, _stream(stream)), "tq_decode_attention")
+    return out
+
+
+def tq_decode_attention_noalloc(cache: Cache, q: torch.Tensor, seq_len: int, softmax_scale: float | None = None,
+                                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """tq_decode_attention without a workspace: for callers that cannot allocate
+    device memory.  The library's built-in 16 MiB scratch holds the partials;
+    concurrent calls race on it (see include/tq.h)."""
+    _require_cuda(q)
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bfloat16 [batch][q_heads][head_dim]")
+    B, QH, d = q.shape
+    if out is None:
+        out = torch.empty((B, QH, d), dtype=torch.float32, device=q.device)
+    scale = (1.0 / d ** 0.5) if softmax_scale is None else float(softmax_scale)
+    s = cache.struct()
+    _check(lib().tq_decode_attention_noalloc(ctypes.byref(s), q.data_ptr(), int(QH), int(seq_len), scale,
+                                             out.data_ptr(), _stream(stream)), "tq_decode_attention_noalloc")
     return out
 
 

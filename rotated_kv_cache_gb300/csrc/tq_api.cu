@@ -103,6 +103,7 @@ const char *tq_status_string(tq_status s)
     case TQ_ERR_WORKSPACE: return "workspace missing or too small";
     case TQ_ERR_CUDA: return "CUDA launch or query failed";
     case TQ_ERR_UNSUPPORTED: return "parameters not covered by this kernel";
+    case TQ_ERR_SCRATCH: return "problem too large for the library's built-in 16 MiB scratch";
     }
     return "unknown status";
 }
@@ -210,6 +211,23 @@ tq_status tq_decode_attention(const tq_cache *c, const void *q, int32_t q_heads,
     if (ws && !aligned16(ws)) return TQ_ERR_ALIGN;
     return cuda_status(tq::launch_attention(view(c), static_cast<const uint16_t *>(q), q_heads, seq_len, scale, out,
                                             ws, ws_bytes, (cudaStream_t)stream));
+}
+
+tq_status tq_decode_attention_noalloc(const tq_cache *c, const void *q, int32_t q_heads, int64_t seq_len,
+                                      float scale, float *out, tq_stream_t stream)
+{
+    tq_status st = check_cache(c);
+    if (st != TQ_OK) return st;
+    if (!q || !out) return TQ_ERR_NULL;
+    if (q_heads < 1 || q_heads % c->num_kv_heads != 0) return TQ_ERR_SHAPE;
+    if (seq_len < 1) return TQ_ERR_SHAPE;
+    if (seq_len > c->capacity) return TQ_ERR_CAPACITY;
+    if (!aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
+    if (!tq::attention_supported(c->head_dim, c->k_bits, c->v_bits, q_heads / c->num_kv_heads))
+        return TQ_ERR_UNSUPPORTED;
+    if (!tq::noalloc_fits(view(c))) return TQ_ERR_SCRATCH;
+    return cuda_status(tq::launch_attention_noalloc(view(c), static_cast<const uint16_t *>(q), q_heads, seq_len,
+                                                    scale, out, (cudaStream_t)stream));
 }
 
 tq_status tq_device_error(uint32_t *host_code)

@@ -742,3 +742,133 @@ cudaError_t launch_attention(const CacheView &c, const uint16_t *q, int q_heads,
 }
 
 }  // namespace tq
+
+// ---------------------------------------------------------------- allocation-free variant
+// Same kernels as launch_attention, but the split partials live in a fixed
+// array that belongs to the library instead of a caller-provided workspace.
+namespace tq {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB on every device that loads the library
+
+// Holds the (max, sum, unnormalised output) partials of the splits.  Every
+// call overwrites the part it uses before reading it, so nothing here has to
+// start at zero; calls that overlap on the GPU share it and would race.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevicesNoAlloc = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevicesNoAlloc];
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+void *noalloc_scratch_address()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesNoAlloc) return nullptr;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+template <int KB>
+cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale,
+                                        float *out, void *scratch, const SplitPlan &plan, cudaStream_t s)
+{
+    using A = AGeo<KB>;
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+    if (e != cudaSuccess) return e;
+    const size_t need_o = (size_t)c.B * c.H * plan.splits * kG * kD * 4;
+
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)A::KROW, (cuuint64_t)c.B * c.H * c.cap};
+    const cuuint64_t gstride[1] = {(cuuint64_t)A::KROW};
+    const cuuint32_t box[2] = {(cuuint32_t)A::KROW, (cuuint32_t)kStageT};
+    const cuuint32_t estride[2] = {1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k_codes, gdim, gstride, box, estride,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, KB == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    AttnParams p{};
+    p.k_scale = c.k_scale;
+    p.k_zero = c.k_zero;
+    p.v_scale = c.v_scale;
+    p.v_codes = c.v_codes;
+    p.q = q;
+    p.part_o = static_cast<float *>(scratch);
+    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + need_o);
+    p.H = c.H;
+    p.QH = QH;
+    p.splits = plan.splits;
+    p.cap = c.cap;
+    p.seq_len = seq_len;
+    p.tokens_per_split = plan.tokens_per_split;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = device_error_word();
+    if (!p.err) return cudaErrorInvalidDevice;
+    const Tables &tab = codebook_tables(kVB);
+    uint8_t lo[8], hi[8];
+    for (int i = 0; i < 8; ++i) {
+        const uint16_t hb = __half_as_ushort(__float2half_rn(tab.centroids[i]));
+        lo[i] = (uint8_t)(hb & 0xFF);
+        hi[i] = (uint8_t)(hb >> 8);
+    }
+    p.tl0 = lo[0] | lo[1] << 8 | lo[2] << 16 | (uint32_t)lo[3] << 24;
+    p.tl1 = lo[4] | lo[5] << 8 | lo[6] << 16 | (uint32_t)lo[7] << 24;
+    p.th0 = hi[0] | hi[1] << 8 | hi[2] << 16 | (uint32_t)hi[3] << 24;
+    p.th1 = hi[4] | hi[5] << 8 | hi[6] << 16 | (uint32_t)hi[7] << 24;
+    p.k_const = KB == 8 ? 0xFF00FF00u : 0xFFF0FFF0u;
+    p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
+
+    dim3 grid(plan.splits, c.H, c.B);
+    attn_split_kernel<KB><<<grid, kThreads, A::SMEM, s>>>(map, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CombineParams cp{};
+    cp.part_o = p.part_o;
+    cp.part_ml = p.part_ml;
+    cp.out = out;
+    cp.H = c.H;
+    cp.QH = QH;
+    cp.splits = plan.splits;
+    cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
+    attn_combine_kernel<<<c.B * QH / 8, 256, 0, s>>>(cp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+bool noalloc_fits(const CacheView &c) { return (size_t)c.B * c.H * kG * (kD + 2) * 4 <= kNoAllocScratchBytes; }
+
+cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
+                                     float *out, cudaStream_t s)
+{
+    void *scratch = noalloc_scratch_address();
+    if (!scratch) return cudaErrorInvalidSymbol;
+    // the usual split plan, with fewer splits if its partials would not fit
+    const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
+    SplitPlan plan = plan_splits(c.B, c.H, seq_len, per_sm);
+    const size_t per_split = (size_t)c.B * c.H * kG * (kD + 2) * 4;
+    const int64_t max_splits = (int64_t)(kNoAllocScratchBytes / per_split);
+    if (max_splits < 1) return cudaErrorInvalidValue;
+    if (plan.splits > max_splits) {
+        const int64_t stages = (seq_len + kStageT - 1) / kStageT;
+        const int64_t per = (stages + max_splits - 1) / max_splits;
+        plan = SplitPlan{(int)((stages + per - 1) / per), per * kStageT};
+    }
+    if (c.kb == 8) return run_attention_fixed_scratch<8>(c, q, q_heads, seq_len, scale, out, scratch, plan, s);
+    return run_attention_fixed_scratch<4>(c, q, q_heads, seq_len, scale, out, scratch, plan, s);
+}
+
+}  // namespace tq

@@ -103,5 +103,5 @@ def test_refusals_before_launch(tqlib):
     assert L.tq_decode_attention(ctypes.byref(s), 0x10000, 4, 33, 1.0, 0x20000, None, 0, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_decode_attention(ctypes.byref(s), None, 4, 8, 1.0, 0x20000, None, 0, None) == S["TQ_ERR_NULL"]
     assert L.tq_attention_workspace_bytes(ctypes.byref(s), 3, 8) == 0
-    for st in range(10):
+    for st in range(11):
         assert L.tq_status_string(st)

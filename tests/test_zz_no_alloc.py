@@ -1,0 +1,97 @@
+"""tq_decode_attention_noalloc (decode attention with the library's own fixed
+scratch, for callers that cannot allocate device memory) against
+tq_decode_attention on the same cache and queries.
+
+Collected last on purpose: the scratch is shared process state, so this file
+checks it both in a fresh process and after every other test has run.  Each
+case makes two calls in a row with different queries, so a second call that
+read the first call's partials would show.  Tolerance: the attention tests'
+2e-3 max-abs (both entry points run the same kernels, so the outputs agree far
+more closely unless the split count differs).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import tq_synth
+from tqtest import to_device_bf16
+
+TOL = 2e-3
+SCRATCH_BYTES = 16 << 20
+
+
+def _noalloc(tq, cache, q, T, scale):
+    """One call through the C ABI; returns the fp32 output."""
+    B, QH, d = q.shape
+    out = torch.full((B, QH, d), float("nan"), dtype=torch.float32, device=q.device)
+    s = cache.struct()
+    st = tq.lib().tq_decode_attention_noalloc(ctypes.byref(s), q.data_ptr(), QH, T, scale, out.data_ptr(),
+                                              torch.cuda.current_stream().cuda_stream)
+    assert st == 0, tq.lib().tq_status_string(st)
+    return out
+
+
+def _two_calls_match(tq, cache, qs, T):
+    scale = 1.0 / np.sqrt(qs[0].shape[-1])
+    got = [_noalloc(tq, cache, q, T, scale) for q in qs]  # back to back, same scratch
+    for q, g in zip(qs, got):
+        want = tq.tq_decode_attention(cache, q, T, softmax_scale=scale)
+        err = (g - want).abs().max().item()
+        assert err < TOL, err
+    assert tq.tq_device_error() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kb", [8, 4])
+def test_noalloc_small_ragged(cuda, kb):
+    w = tq_synth.WORKLOADS["decode"]
+    B, H, T = 2, 2, 1000
+    k, v = tq_synth.host_kv(w, B=B, H=H, n=T)
+    cache = cuda.Cache(B, H, w.d, T, k_bits=kb, v_bits=w.vb)
+    cuda.tq_encode_append(cache, to_device_bf16(k), to_device_bf16(v), 0)
+    qs = [to_device_bf16(tq_synth.host_q(w, step, B=B, QH=8 * H)) for step in (0, 1)]
+    _two_calls_match(cuda, cache, qs, T)
+
+
+@pytest.mark.gpu
+def test_noalloc_fewer_splits_than_usual(cuda):
+    """64 sequences x 8 kv-heads x 8193 rows: the usual split plan needs more
+    than the 16 MiB scratch, so this entry point runs with fewer splits."""
+    w = tq_synth.WORKLOADS["decode"]
+    B, H, T = 64, 8, 8193
+    cache = cuda.Cache(B, H, w.d, T, k_bits=8, v_bits=w.vb)
+    k = torch.empty((B, H, T, w.d), dtype=torch.int16, device="cuda")
+    v = torch.empty_like(k)
+    tq_synth.device_kv(w, k, v, B=B, H=H, n=T)
+    cuda.tq_encode_append(cache, k.view(torch.bfloat16), v.view(torch.bfloat16), 0)
+    del k, v
+    assert cuda.tq_attention_workspace_bytes(cache, 8 * H, T) > SCRATCH_BYTES
+    qs = []
+    for step in (0, 1):
+        q = torch.empty((B, 8 * H, w.d), dtype=torch.int16, device="cuda")
+        tq_synth.device_q(w, step, q, B=B, QH=8 * H)
+        qs.append(q.view(torch.bfloat16))
+    _two_calls_match(cuda, cache, qs, T)
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch(tqlib):
+    """batch x kv-heads above 4032 cannot fit even one split: refused before
+    any CUDA call (so this runs without a GPU; the pointers are never read)."""
+    L = tqlib.lib()
+    S = {n: i for i, n in enumerate(["TQ_OK", "TQ_ERR_NULL", "TQ_ERR_HEAD_DIM", "TQ_ERR_BITS", "TQ_ERR_SHAPE",
+                                     "TQ_ERR_CAPACITY", "TQ_ERR_ALIGN", "TQ_ERR_WORKSPACE", "TQ_ERR_CUDA",
+                                     "TQ_ERR_UNSUPPORTED", "TQ_ERR_SCRATCH"])}
+    def status(B, H):
+        s = tqlib._CacheStruct(128, 8, 3, H, B, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+        return L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8 * H, 16, 1.0, 0x20000, None)
+    assert status(4033, 1) == S["TQ_ERR_SCRATCH"]
+    assert status(1, 4033) == S["TQ_ERR_SCRATCH"]
+    assert status(37, 109) == S["TQ_ERR_SCRATCH"]  # 4033 units
+    assert "16 MiB" in L.tq_status_string(S["TQ_ERR_SCRATCH"]).decode()
+    # the usual argument checks still come first
+    s = tqlib._CacheStruct(128, 8, 3, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+    assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 17, 1.0, 0x20000, None) == S["TQ_ERR_CAPACITY"]
+    assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 16, 1.0, 0x20004, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 4, 16, 1.0, 0x20000, None) == S["TQ_ERR_UNSUPPORTED"]
