@@ -88,6 +88,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As above, but a thread whose phase is not complete sleeps in hardware until
+// it completes or up to `ns` nanoseconds pass, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns()
 {
     uint64_t t;
@@ -95,16 +110,18 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
-// Wait for phase `parity` of a barrier, for at most ~2 s of wall time.  On
+// Wait for phase `parity` of a barrier, for at most ~2 s of wall time.  The
+// waiting thread sleeps in hardware between checks (woken when the phase
+// completes), so waiting warps take no issue slots from working ones.  On
 // timeout the device error word gets kErrWaitTimeout and false is returned,
 // so a lost copy can never hang the GPU.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t *err)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+        if (global_timer_ns() - t0 > 2000000000ull) {
             atomicOr(err, kErrWaitTimeout);
             return false;
         }
@@ -195,10 +212,84 @@ __device__ __forceinline__ void load_words(const void *src, uint32_t (&w)[N])
     }
 }
 
+// One 32-byte store (address 32-byte aligned): a lane fills whole 32-byte
+// sectors, so a warp's store moves no partial sectors.
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4),
+                 "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 __host__ __device__ constexpr int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Division by a run-time constant d >= 1 for dividends x < 2^31: q = (x * m) >> sh
+// with sh = 31 + ceil(log2 d), m = ceil(2^sh / d) < 2^32 (Granlund & Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994, Thm 4.2).
+struct FastDiv {
+    uint32_t m, sh;
+};
+
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint32_t sh = 31 + l;
+    return FastDiv{(uint32_t)(((1ull << sh) + d - 1) / d), sh};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t x, FastDiv f) { return (uint32_t)(((uint64_t)x * f.m) >> f.sh); }
 
 // Largest power of two (<= 16) dividing x.
 __host__ __device__ constexpr int align_of_bytes(int x) { return (x % 16 == 0) ? 16 : (x % 8 == 0) ? 8 : (x % 4 == 0) ? 4 : (x % 2 == 0) ? 2 : 1; }
+
+// ---------------------------------------------------------------- Walsh-Hadamard transform on fp32 pairs
+// a - b, rounded once (b * -1 is exact)
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
+
+// One butterfly stage of stride H over 32 pairs: (a, b) -> (a + b, a - b).
+template <int H>
+__device__ __forceinline__ void bfly_stage(float2 (&P)[32])
+{
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        const int j = (t / H) * 2 * H + t % H;
+        const float2 s = __fadd2_rn(P[j], P[j + H]);
+        P[j + H] = fsub2(P[j], P[j + H]);
+        P[j] = s;
+    }
+}
+
+// Unnormalised Sylvester transform of a 64*LPR-element row held by LPR lanes
+// (lane = part * ROWS + row), each lane holding P[j] = (element 64 part + j,
+// element 64 part + j + 32).  Stages run in the definition's order, strides
+// 1, 2, 4, ...: 1..16 on pairs, 32 inside each pair, 64.. across the row's
+// lanes by shuffle (the lane with the part bit clear keeps a + b, the other
+// a - b), so the result is bit-identical to the plain in-order butterfly.
+template <int LPR, int ROWS>
+__device__ __forceinline__ void fwht_pairs(float2 (&P)[32], int part)
+{
+    bfly_stage<1>(P);
+    bfly_stage<2>(P);
+    bfly_stage<4>(P);
+    bfly_stage<8>(P);
+    bfly_stage<16>(P);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) P[j] = make_float2(__fadd_rn(P[j].x, P[j].y), __fsub_rn(P[j].x, P[j].y));
+#pragma unroll
+    for (int s = 1; s < LPR; s <<= 1) {
+        const float g = (part & s) ? -1.0f : 1.0f;
+        const float2 g2 = make_float2(g, g);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            float2 o;
+            o.x = __shfl_xor_sync(0xffffffffu, P[j].x, ROWS * s);
+            o.y = __shfl_xor_sync(0xffffffffu, P[j].y, ROWS * s);
+            P[j] = __ffma2_rn(P[j], g2, o);
+        }
+    }
+}
 
 // ---------------------------------------------------------------- bitstream packing of one 32-group
 // Codes c[0..31] (each < 2^B) -> B little-endian words: code i at bits [iB, iB+B)

@@ -7,13 +7,16 @@
 // scale) then the sign flip ("apply FWHT then multiply signs", earlier copy of
 // the page), the transform normalised by 1/sqrt(d).
 //
-// GB300 layout.  Keys are elementwise: each thread converts a run of codes
-// whose bytes are 4-byte aligned (8 codes at 8/4 bits, 16 at 2 bits, one
-// 32-group at 5 bits), so loads and stores of a warp are contiguous.  Values
-// need whole rows: one lane owns E = min(d, 128) elements of a row (d/E lanes
-// per row), runs the inverse transform in registers (sign and 1/sqrt(d) fused
-// into the last multiply) and writes its slice through a padded shared-memory
-// slot with a bulk asynchronous store (cp.async.bulk shared -> global).
+// GB300 layout.  Keys are elementwise: a thread converts one 32-group, the
+// grid's y axis walks the (sequence, kv-head) pairs, so a warp's loads and
+// stores are contiguous and no division is needed.  A code becomes a float
+// by placing it in the low mantissa bits of 1.5*2^23 (one byte permute or
+// mask); subtracting 1.5*2^23 - zero then gives idx + zero exactly (both are
+// integers below 2^24), and the multiply by the scale is the definition's.
+// Values need whole rows: as in the encoder a lane holds 64 elements as
+// fp32 pairs (element j, element j+32), the row spread over d/64 lanes; the
+// inverse transform runs in the definition's stage order with packed .f32x2
+// arithmetic, and the sign flip rides on the final multiply by +-1/sqrt(d).
 #pragma once
 #include "tq_common.cuh"
 #include "tq_kernels.h"
@@ -22,57 +25,74 @@ namespace tq {
 namespace {
 
 // ------------------------------------------------------------------ keys
-template <int KB>
-struct KeyRun {
-    static constexpr int CODES = KB == 8 ? 8 : KB == 4 ? 8 : KB == 2 ? 16 : 32;
-    static constexpr int WORDS = CODES * KB / 32;
-};
-
 struct KeyDecodeParams {
     const uint8_t *codes;
     const uint16_t *scale, *zero;
     void *out;
-    int64_t cap, t0, n, runs;  // runs = B*H*n*d / CODES
+    int64_t cap, t0, n, groups_per_bh, BH;
     int d;
 };
+
+// 32 codes of one group -> the float bit patterns of 1.5*2^23 + u with u = code
+// (unsigned) or code + 128 (signed 8-bit)
+template <int KB>
+__device__ __forceinline__ void magic_codes(const uint32_t (&w)[KB], uint32_t (&m)[32])
+{
+    if constexpr (KB == 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t u = w[i] ^ 0x80808080u;  // int8 -> code + 128
+#pragma unroll
+            for (int k = 0; k < 4; ++k) m[4 * i + k] = __byte_perm(u, 0x4B400000u, 0x7650 + k);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int bit = j * KB, word = bit >> 5, off = bit & 31;
+            uint32_t c = (off + KB <= 32) ? (w[word] >> off) : __funnelshift_r(w[word], w[word + 1], off);
+            m[j] = (c & ((1u << KB) - 1u)) | 0x4B400000u;
+        }
+    }
+}
 
 template <int KB, bool F32>
 __global__ void __launch_bounds__(256) decode_key_kernel(const __grid_constant__ KeyDecodeParams p)
 {
-    using R = KeyRun<KB>;
-    const int runs_per_row = p.d / R::CODES;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < p.runs; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t orow = i / runs_per_row;  // output row = (bh, t)
-        const int ri = (int)(i - orow * runs_per_row);
-        const int64_t bh = orow / p.n, t = orow - bh * p.n;
-        const int64_t crow = bh * p.cap + p.t0 + t;
-        const int e0 = ri * R::CODES;  // first element of the run
-        uint32_t w[R::WORDS];
-        load_words<R::WORDS, align_of_bytes(R::WORDS * 4)>(p.codes + crow * (p.d * KB / 8) + e0 * KB / 8, w);
-        const int g = e0 / 32;
-        const float s = f16_bits_to_f32(p.scale[crow * (p.d / 32) + g]);
-        const float z = f16_bits_to_f32(p.zero[crow * (p.d / 32) + g]);
-        float x[R::CODES];
+    const int64_t gi = (int64_t)blockIdx.x * 256 + threadIdx.x;  // group within the (sequence, kv-head)'s n rows
+    if (gi >= p.groups_per_bh) return;
+    constexpr int A = align_of_bytes(4 * KB);
+    for (int64_t bh = blockIdx.y; bh < p.BH; bh += gridDim.y) {
+        // rows t0 .. t0+n-1 of one (sequence, kv-head) are contiguous in every plane
+        const int64_t row0 = bh * p.cap + p.t0;
+        uint32_t w[KB];
+        load_words<KB, A>(p.codes + row0 * (p.d * KB / 8) + gi * (4 * KB), w);
+        const int64_t mi = row0 * (p.d / 32) + gi;
+        const float s = f16_bits_to_f32(p.scale[mi]), z = f16_bits_to_f32(p.zero[mi]);
+        // 1.5*2^23 + u - (1.5*2^23 + bias - zero) = idx + zero, exactly
+        const float zz = __fsub_rn(KB == 8 ? 12583040.0f : 12582912.0f, z);
+        uint32_t m[32];
+        magic_codes<KB>(w, m);
+        const float2 nz2 = make_float2(-zz, -zz), s2 = make_float2(s, s);
+        float2 x[16];
 #pragma unroll
-        for (int j = 0; j < R::CODES; ++j) {
-            const int bit = j * KB;
-            uint32_t c = w[bit >> 5] >> (bit & 31);
-            if ((bit & 31) + KB > 32) c |= w[(bit >> 5) + 1] << (32 - (bit & 31));
-            c &= (1u << KB) - 1u;
-            const float fi = KB == 8 ? (float)(int32_t)(int8_t)c : (float)c;
-            x[j] = __fmul_rn(__fadd_rn(fi, z), s);
-        }
-        const int64_t o = orow * p.d + e0;
+        for (int k = 0; k < 16; ++k)
+            x[k] = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(m[2 * k]), __uint_as_float(m[2 * k + 1])), nz2), s2);
+        const int64_t o = bh * p.n * p.d + gi * 32;  // whole 32-byte sectors per store
         if constexpr (F32) {
-            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o);
+            float *dst = static_cast<float *>(p.out) + o;
 #pragma unroll
-            for (int j = 0; j < R::CODES / 4; ++j) dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+            for (int j = 0; j < 4; ++j)
+                st_global_v8(dst + 8 * j, __float_as_uint(x[4 * j].x), __float_as_uint(x[4 * j].y), __float_as_uint(x[4 * j + 1].x),
+                             __float_as_uint(x[4 * j + 1].y), __float_as_uint(x[4 * j + 2].x), __float_as_uint(x[4 * j + 2].y),
+                             __float_as_uint(x[4 * j + 3].x), __float_as_uint(x[4 * j + 3].y));
         } else {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + o);
+            uint16_t *dst = static_cast<uint16_t *>(p.out) + o;
 #pragma unroll
-            for (int j = 0; j < R::CODES / 8; ++j)
-                dst[j] = make_uint4(pack_bf16x2(x[8 * j], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
-                                    pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+            for (int j = 0; j < 2; ++j)
+                st_global_v8(dst + 16 * j, pack_bf16x2(x[8 * j].x, x[8 * j].y), pack_bf16x2(x[8 * j + 1].x, x[8 * j + 1].y),
+                             pack_bf16x2(x[8 * j + 2].x, x[8 * j + 2].y), pack_bf16x2(x[8 * j + 3].x, x[8 * j + 3].y),
+                             pack_bf16x2(x[8 * j + 4].x, x[8 * j + 4].y), pack_bf16x2(x[8 * j + 5].x, x[8 * j + 5].y),
+                             pack_bf16x2(x[8 * j + 6].x, x[8 * j + 6].y), pack_bf16x2(x[8 * j + 7].x, x[8 * j + 7].y));
         }
     }
 }
@@ -80,14 +100,10 @@ __global__ void __launch_bounds__(256) decode_key_kernel(const __grid_constant__
 // ------------------------------------------------------------------ values
 constexpr int kVWarps = 4;
 
-template <int D, bool F32>
+template <int D>
 struct VGeo {
-    static constexpr int E = D < 128 ? D : 128;
-    static constexpr int LPR = D / E;
-    static constexpr int ROWS = 32 / LPR;
-    static constexpr int OB = F32 ? 4 : 2;          // output bytes per element
-    static constexpr int SLOT = E * OB + 16;        // padded lane slot
-    static constexpr int NG = E / 32;
+    static constexpr int LPR = D / 64;     // lanes per row, 64 elements each
+    static constexpr int ROWS = 32 / LPR;  // rows per warp tile
 };
 
 struct ValueDecodeParams {
@@ -95,121 +111,131 @@ struct ValueDecodeParams {
     const uint16_t *scale;
     void *out;
     int H;
-    int64_t cap, t0, n, tiles_per_bh, items;
+    int64_t cap, t0, n;
+    uint32_t tiles_per_bh, items;  // items < 2^31
+    FastDiv div_tiles;
     float inv_sqrt_d;
     float cen[256];
 };
 
-template <int E>
-__device__ __forceinline__ void fwht_local_d(float (&x)[E])
+// Byte offset (4 * code) of code j of a group's VB-bit little-endian stream.
+template <int VB>
+__device__ __forceinline__ uint32_t code_offset(const uint32_t *w, int j)
 {
-#pragma unroll
-    for (int h = 1; h < E; h <<= 1)
-#pragma unroll
-        for (int i = 0; i < E; i += 2 * h)
-#pragma unroll
-            for (int j = i; j < i + h; ++j) {
-                const float a = x[j], b = x[j + h];
-                x[j] = __fadd_rn(a, b);
-                x[j + h] = __fsub_rn(a, b);
-            }
+    constexpr uint32_t mask = ((1u << VB) - 1u) << 2;
+    const int b = j * VB - 2;  // stream bit that lands on bit 0
+    if (b < 0) return (w[0] << -b) & mask;
+    const int word = b >> 5, off = b & 31;
+    if (off + VB + 2 <= 32) return (w[word] >> off) & mask;
+    return __funnelshift_r(w[word], w[word + 1], off) & mask;
 }
 
-template <int E>
-__device__ __forceinline__ void fwht_cross_d(float (&x)[E], int s, bool upper)
+template <int D, int VB>
+__device__ __forceinline__ void load_value_lane(const ValueDecodeParams &p, int64_t crow, int part, uint32_t (&w)[2 * VB],
+                                                uint32_t &sc)
 {
-    const float sg = upper ? -1.0f : 1.0f;
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-        const float other = __shfl_xor_sync(0xffffffffu, x[j], s);
-        x[j] = __fmaf_rn(x[j], sg, other);
-    }
+    constexpr int RB = D * VB / 8, LB = 8 * VB;
+    constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
+    load_words<2 * VB, A>(p.codes + crow * RB + part * LB, w);
+    sc = *reinterpret_cast<const uint32_t *>(p.scale + crow * (D / 32) + 2 * part);
 }
 
 template <int D, int VB, bool F32>
 __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid_constant__ ValueDecodeParams p)
 {
-    using G = VGeo<D, F32>;
-    constexpr int E = G::E;
-    extern __shared__ __align__(128) uint8_t smem[];
-    float *scen = reinterpret_cast<float *>(smem);
-    uint8_t *slots = smem + 1024;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    using G = VGeo<D>;
+    __shared__ __align__(16) float scen[1 << VB];
+    __shared__ __align__(16) float2 smul[G::LPR][34];  // (+-1/sqrt d) of elements (j, j+32) of each part, padded
     for (int i = threadIdx.x; i < (1 << VB); i += blockDim.x) scen[i] = p.cen[i];
+    for (int i = threadIdx.x; i < G::LPR * 32; i += blockDim.x) {
+        const int part = i >> 5, j = i & 31, e = 64 * part + j;
+        smul[part][j] = make_float2(sign_negative(e) ? -p.inv_sqrt_d : p.inv_sqrt_d,
+                                    sign_negative(e + 32) ? -p.inv_sqrt_d : p.inv_sqrt_d);
+    }
     __syncthreads();
-    const uint32_t slot = smem_addr(slots + (warp * 32 + lane) * G::SLOT);
-    const int r = lane / G::LPR, part = lane % G::LPR;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane % G::ROWS, part = lane / G::ROWS;
+    const char *cen = reinterpret_cast<const char *>(scen);
 
-    const int64_t W = (int64_t)gridDim.x * kVWarps;
-    for (int64_t item = (int64_t)blockIdx.x * kVWarps + warp; item < p.items; item += W) {
-        const int64_t bh = item / p.tiles_per_bh;
-        const int64_t t = (item - bh * p.tiles_per_bh) * G::ROWS + r;
+    const uint32_t W = gridDim.x * kVWarps;
+    uint32_t item = blockIdx.x * kVWarps + warp;
+    // the next tile's codes are loaded while this one is transformed
+    uint32_t nw[2 * VB], nsc = 0;
+    auto locate = [&](uint32_t it, int64_t &t, int64_t &crow, uint32_t &bh) {
+        bh = fast_div(it, p.div_tiles);
+        t = (int64_t)(it - bh * p.tiles_per_bh) * G::ROWS + r;
+        crow = (int64_t)bh * p.cap + p.t0 + t;
+    };
+    if (item < p.items) {
+        int64_t t, crow;
+        uint32_t bh;
+        locate(item, t, crow, bh);
+        if (t < p.n) load_value_lane<D, VB>(p, crow, part, nw, nsc);
+    }
+    for (; item < p.items; item += W) {
+        uint32_t w[2 * VB], sc = nsc;
+#pragma unroll
+        for (int k = 0; k < 2 * VB; ++k) w[k] = nw[k];
+        int64_t t, crow;
+        uint32_t bh;
+        locate(item, t, crow, bh);
         const bool valid = t < p.n;
-        const int64_t crow = bh * p.cap + p.t0 + (valid ? t : 0);
-        float x[E];
+        if (item + W < p.items) {
+            int64_t t1, crow1;
+            uint32_t bh1;
+            locate(item + W, t1, crow1, bh1);
+            if (t1 < p.n) load_value_lane<D, VB>(p, crow1, part, nw, nsc);
+        }
+        float2 P[32];
         if (valid) {
-            constexpr int LW = E * VB / 32, RB = D * VB / 8, LB = E * VB / 8;
-            constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
-            uint32_t w[LW];
-            load_words<LW, A>(p.codes + crow * RB + part * LB, w);
+            const float s0 = f16_bits_to_f32((uint16_t)(sc & 0xFFFFu)), s1 = f16_bits_to_f32((uint16_t)(sc >> 16));
+            const float2 s2 = make_float2(s0, s1);
 #pragma unroll
-            for (int g = 0; g < G::NG; ++g) {
-                const float s = f16_bits_to_f32(p.scale[crow * (D / 32) + part * G::NG + g]);
-                uint32_t gw[VB], c[32];
-#pragma unroll
-                for (int k = 0; k < VB; ++k) gw[k] = w[g * VB + k];
-                unpack_group<VB>(gw, c);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[32 * g + j] = __fmul_rn(scen[c[j]], s);
+            for (int j = 0; j < 32; ++j) {
+                const float c0 = *reinterpret_cast<const float *>(cen + code_offset<VB>(w, j));
+                const float c1 = *reinterpret_cast<const float *>(cen + code_offset<VB>(w + VB, j));
+                P[j] = __fmul2_rn(make_float2(c0, c1), s2);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < E; ++j) x[j] = 0.0f;
+            for (int j = 0; j < 32; ++j) P[j] = make_float2(0.0f, 0.0f);
         }
-        fwht_local_d<E>(x);
-        if constexpr (G::LPR >= 2) fwht_cross_d<E>(x, 1, (part & 1) != 0);
-        if constexpr (G::LPR >= 4) fwht_cross_d<E>(x, 2, (part & 2) != 0);
-        // out = sign * (z * fl(1/sqrt d)); the sign flip is exact, so it is
-        // fused into the multiplier
-        if constexpr (G::LPR == 1) {
+        fwht_pairs<G::LPR, G::ROWS>(P, part);
+        if (valid) {
 #pragma unroll
-            for (int j = 0; j < E; ++j) x[j] = __fmul_rn(x[j], sign_negative(j) ? -p.inv_sqrt_d : p.inv_sqrt_d);
-        } else {
+            for (int j = 0; j < 32; j += 2) {
+                const float4 m = *reinterpret_cast<const float4 *>(&smul[part][j]);
+                P[j] = __fmul2_rn(P[j], make_float2(m.x, m.y));
+                P[j + 1] = __fmul2_rn(P[j + 1], make_float2(m.z, m.w));
+            }
+            const int64_t o = ((int64_t)bh * p.n + t) * D + 64 * part;  // whole 32-byte sectors per store
+            if constexpr (F32) {
+                float *dst = static_cast<float *>(p.out) + o;
 #pragma unroll
-            for (int wv = 0; wv < E / 32; ++wv) {
-                uint32_t m = sign_word(wv);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 *q = P + 8 * i;
+                    st_global_v8(dst + 8 * i, __float_as_uint(q[0].x), __float_as_uint(q[1].x), __float_as_uint(q[2].x),
+                                 __float_as_uint(q[3].x), __float_as_uint(q[4].x), __float_as_uint(q[5].x),
+                                 __float_as_uint(q[6].x), __float_as_uint(q[7].x));
+                    st_global_v8(dst + 32 + 8 * i, __float_as_uint(q[0].y), __float_as_uint(q[1].y), __float_as_uint(q[2].y),
+                                 __float_as_uint(q[3].y), __float_as_uint(q[4].y), __float_as_uint(q[5].y),
+                                 __float_as_uint(q[6].y), __float_as_uint(q[7].y));
+                }
+            } else {
+                uint16_t *dst = static_cast<uint16_t *>(p.out) + o;
 #pragma unroll
-                for (int q = 1; q < G::LPR; ++q)
-                    if (part == q) m = sign_word(q * (E / 32) + wv);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float y = __fmul_rn(x[32 * wv + k], p.inv_sqrt_d);
-                    x[32 * wv + k] = __uint_as_float(__float_as_uint(y) ^ ((m << (31 - k)) & 0x80000000u));
+                for (int i = 0; i < 2; ++i) {
+                    const float2 *q = P + 16 * i;
+                    st_global_v8(dst + 16 * i, pack_bf16x2(q[0].x, q[1].x), pack_bf16x2(q[2].x, q[3].x), pack_bf16x2(q[4].x, q[5].x),
+                                 pack_bf16x2(q[6].x, q[7].x), pack_bf16x2(q[8].x, q[9].x), pack_bf16x2(q[10].x, q[11].x),
+                                 pack_bf16x2(q[12].x, q[13].x), pack_bf16x2(q[14].x, q[15].x));
+                    st_global_v8(dst + 32 + 16 * i, pack_bf16x2(q[0].y, q[1].y), pack_bf16x2(q[2].y, q[3].y),
+                                 pack_bf16x2(q[4].y, q[5].y), pack_bf16x2(q[6].y, q[7].y), pack_bf16x2(q[8].y, q[9].y),
+                                 pack_bf16x2(q[10].y, q[11].y), pack_bf16x2(q[12].y, q[13].y), pack_bf16x2(q[14].y, q[15].y));
                 }
             }
         }
-        // previous bulk store from this slot must have read it
-        bulk_wait_read0();
-        if (valid) {
-            if constexpr (F32) {
-#pragma unroll
-                for (int i = 0; i < E / 4; ++i)
-                    sts128(slot + 16 * i, make_uint4(__float_as_uint(x[4 * i]), __float_as_uint(x[4 * i + 1]),
-                                                     __float_as_uint(x[4 * i + 2]), __float_as_uint(x[4 * i + 3])));
-            } else {
-#pragma unroll
-                for (int i = 0; i < E / 8; ++i)
-                    sts128(slot + 16 * i, make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
-                                                     pack_bf16x2(x[8 * i + 4], x[8 * i + 5]),
-                                                     pack_bf16x2(x[8 * i + 6], x[8 * i + 7])));
-            }
-            fence_proxy_async_smem();
-            uint8_t *dst = static_cast<uint8_t *>(p.out) + ((bh * p.n + t) * D + part * E) * G::OB;
-            bulk_s2g(dst, slot, E * G::OB);
-            bulk_commit();
-        }
     }
-    bulk_wait0();
 }
 
 template <int KB, bool F32>
@@ -224,9 +250,11 @@ cudaError_t run_key(const CacheView &c, int64_t t0, int64_t n, void *out, cudaSt
     p.t0 = t0;
     p.n = n;
     p.d = c.d;
-    p.runs = (int64_t)c.B * c.H * n * c.d / KeyRun<KB>::CODES;
-    const int64_t blocks = (p.runs + 255) / 256;
-    const int grid = (int)imin64(blocks, (int64_t)num_sms() * 8);
+    p.groups_per_bh = n * (c.d / 32);
+    p.BH = (int64_t)c.B * c.H;
+    const int64_t bx = (p.groups_per_bh + 255) / 256;
+    if (bx >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)bx, (unsigned)imin64(p.BH, 65535));
     decode_key_kernel<KB, F32><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
@@ -234,7 +262,7 @@ cudaError_t run_key(const CacheView &c, int64_t t0, int64_t n, void *out, cudaSt
 template <int D, int VB, bool F32>
 cudaError_t run_value(const CacheView &c, int64_t t0, int64_t n, void *out, cudaStream_t s)
 {
-    using G = VGeo<D, F32>;
+    using G = VGeo<D>;
     ValueDecodeParams p{};
     p.codes = c.v_codes;
     p.scale = c.v_scale;
@@ -243,21 +271,25 @@ cudaError_t run_value(const CacheView &c, int64_t t0, int64_t n, void *out, cuda
     p.cap = c.cap;
     p.t0 = t0;
     p.n = n;
-    p.tiles_per_bh = (n + G::ROWS - 1) / G::ROWS;
-    p.items = p.tiles_per_bh * (int64_t)c.B * c.H;
+    const int64_t tiles = (n + G::ROWS - 1) / G::ROWS, items = tiles * (int64_t)c.B * c.H;
+    if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    p.tiles_per_bh = (uint32_t)tiles;
+    p.items = (uint32_t)items;
+    p.div_tiles = make_fastdiv(tiles > 0 ? (uint32_t)tiles : 1u);
     p.inv_sqrt_d = inv_sqrt_head_dim(D);
     const Tables &tab = codebook_tables(VB);
     for (int i = 0; i < (1 << VB); ++i) p.cen[i] = tab.centroids[i];
-    const size_t smem = 1024 + (size_t)kVWarps * 32 * G::SLOT;
     auto kern = decode_value_kernel<D, VB, F32>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kVWarps * 32, smem);
-    if (per_sm < 1) per_sm = 1;
-    const int64_t want = (p.items + kVWarps - 1) / kVWarps;
+    static int per_sm = 0;  // same on every GB300; only a successful query is kept
+    if (!per_sm) {
+        int k = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, kVWarps * 32, 0);
+        if (e != cudaSuccess) return e;
+        per_sm = k > 0 ? k : 1;
+    }
+    const int64_t want = (items + kVWarps - 1) / kVWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
-    kern<<<grid, kVWarps * 32, smem, s>>>(p);
+    kern<<<grid, kVWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 

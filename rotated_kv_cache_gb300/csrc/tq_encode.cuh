@@ -9,15 +9,21 @@
 //   values y = FWHT(x * signs)/sqrt(d); per 32-group rms = sqrt(mean(y^2));
 //          idx = searchsorted(boundaries, y/(rms + 1e-8)); little-endian pack.
 //
-// GB300 layout: one warp processes a tile of token rows of one (sequence,
-// kv-head).  Each lane owns E = min(d, 128) consecutive elements of a row
-// (d/E lanes per row), brought into a padded shared-memory slot by a bulk
-// asynchronous copy (cp.async.bulk, completion on a per-warp mbarrier; two
-// slots per warp so the next tile streams in while this one is computed).
-// The Walsh-Hadamard transform runs in registers: log2(E) local butterfly
-// stages with the sign flip folded in at compile time, then log2(d/E)
-// stages across lanes by shuffle.  Stage order and every rounding step follow
-// the definition, so codes and scales are reproducible bit for bit.
+// GB300 layout.  A warp processes a tile of token rows of one (sequence,
+// kv-head); each row reaches shared memory by one bulk asynchronous copy
+// (cp.async.bulk, completion on a per-warp mbarrier, two tiles in flight per
+// warp).  A row is split over LPR lanes, lane = part * ROWS + row:
+//   keys    32 elements per lane = one quantisation group, so the group's
+//           max/min, scale and zero point never leave the lane;
+//   values  64 elements per lane = two RMS groups, held as fp32 pairs
+//           (element j, element j+32).  Butterfly strides 1..16 run on the
+//           pairs with packed .f32x2 arithmetic, stride 32 inside each pair,
+//           strides 64.. across the row's lanes by shuffle; the two groups'
+//           sums of squares run as one packed chain.
+// Every rounding step is the definition's, in its order: codes, scales and
+// zero points are reproducible bit for bit, except a value index whose
+// normalised input lies within a few ulps of a boundary (thresholds are
+// compared instead of dividing).
 #pragma once
 #include "tq_common.cuh"
 #include "tq_kernels.h"
@@ -27,14 +33,21 @@ namespace {
 
 constexpr int kWarps = 4;  // warps per CTA
 
-template <int D>
-struct Geo {
-    static constexpr int E = D < 128 ? D : 128;  // elements per lane
-    static constexpr int LPR = D / E;             // lanes per row
-    static constexpr int ROWS = 32 / LPR;         // rows per warp tile
-    static constexpr int SLOT = E * 2 + 16;       // bytes per lane slot (odd multiple of 16: no bank conflicts)
-    static constexpr int TILE = 32 * SLOT;
-    static constexpr int NG = E / 32;             // groups per lane
+template <int D, bool KEY>
+struct EGeo {
+    static constexpr int E = KEY ? 32 : 64;  // elements per lane
+    static constexpr int LPR = D / E;         // lanes per row
+    static constexpr int ROWS = 32 / LPR;     // rows per warp tile
+    static constexpr int RS = 2 * D + 16;     // row slot bytes: 16 mod 128, so 8 rows' 16-byte reads hit 8 bank groups
+    static constexpr int TILE = ROWS * RS;
+    static constexpr int MTAB = KEY ? 0 : LPR * 272;  // value sign masks: 16 x 16 bytes (+16 pad) per part
+};
+
+// value tiles stage their packed codes (ROWS rows x row bytes, 16-byte multiple)
+template <int D, int BITS>
+struct VStage {
+    static constexpr int RB = D * BITS / 8;
+    static constexpr int BYTES = (EGeo<D, false>::ROWS * RB + 15) / 16 * 16;
 };
 
 struct EncodeParams {
@@ -44,46 +57,89 @@ struct EncodeParams {
     uint16_t *scale, *zero;
     int H;
     int64_t cap, t0, n;
-    int64_t tiles_per_bh, items;
+    uint32_t tiles_per_bh, items;  // items < 2^31
+    FastDiv div_tiles, div_h;      // x / tiles_per_bh, x / H
     float inv_sqrt_d;
     uint32_t *err;
     float bnd[255];  // value boundaries (ascending)
 };
 
-template <int D>
-__device__ __forceinline__ void issue_tile(const EncodeParams &p, int64_t item, uint32_t buf, uint32_t bar, int lane)
+template <int D, bool KEY>
+__device__ __forceinline__ void issue_tile(const EncodeParams &p, uint32_t item, uint32_t buf, uint32_t bar, int lane)
 {
-    using G = Geo<D>;
-    const int64_t bh = item / p.tiles_per_bh;
-    const int64_t t_first = (item - bh * p.tiles_per_bh) * G::ROWS;
+    using G = EGeo<D, KEY>;
+    const uint32_t bh = fast_div(item, p.div_tiles);
+    const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::ROWS;
     const int rows = (int)imin64(G::ROWS, p.n - t_first);
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows * G::LPR * G::E * 2));
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows * D * 2));
     __syncwarp();
-    const int r = lane / G::LPR, part = lane % G::LPR;
-    if (r < rows) {
-        const int64_t b = bh / p.H, h = bh - b * p.H;
-        const uint16_t *src = p.src + b * p.sb + h * p.sh + (t_first + r) * p.st + part * G::E;
-        bulk_g2s(buf + lane * G::SLOT, src, G::E * 2, bar);
+    if (lane < rows) {
+        const uint32_t b = fast_div(bh, p.div_h), h = bh - b * (uint32_t)p.H;
+        bulk_g2s(buf + lane * G::RS, p.src + b * p.sb + h * p.sh + (t_first + lane) * p.st, D * 2, bar);
     }
 }
 
-// 32 bf16 of a lane slot -> fp32
-__device__ __forceinline__ void load_group(uint32_t a, float (&x)[32])
+// ------------------------------------------------------------------ packed helpers
+__device__ __forceinline__ uint32_t fbits(float f) { return __float_as_uint(f); }
+
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b)
 {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 v = lds128(a + 16 * i);
-        x[8 * i + 0] = bf16_lo(v.x); x[8 * i + 1] = bf16_hi(v.x);
-        x[8 * i + 2] = bf16_lo(v.y); x[8 * i + 3] = bf16_hi(v.y);
-        x[8 * i + 4] = bf16_lo(v.z); x[8 * i + 5] = bf16_hi(v.z);
-        x[8 * i + 6] = bf16_lo(v.w); x[8 * i + 7] = bf16_hi(v.w);
-    }
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// RN(x/y) from RN(1/y) (Markstein's correction step; exact for quotients in
+// the normal range -- see tests/helpers/markstein_check.c).
+__device__ __forceinline__ float ms_div(float x, float y, float ry)
+{
+    const float q0 = __fmul_rn(x, ry);
+    return __fmaf_rn(__fmaf_rn(-y, q0, x), ry, q0);
 }
 
 // ------------------------------------------------------------------ keys
-template <int BITS>
-__device__ __forceinline__ void key_group(const float (&x)[32], uint32_t (&code)[32], uint16_t &sc, uint16_t &zr)
+// Pack codes given as 0x4B400000 + code (code < 2^BITS) into the BITS-bit
+// little-endian stream: accumulate the sums, then subtract what the constant
+// 0x4B400000 part contributed (fields do not overlap, so adding is or-ing).
+template <int B>
+__device__ __forceinline__ void pack_magic(const uint32_t (&m)[32], uint32_t (&w)[B])
 {
+    constexpr uint32_t M = 0x4B400000u;
+    uint32_t corr[B] = {};
+#pragma unroll
+    for (int k = 0; k < B; ++k) w[k] = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int bit = i * B, word = bit >> 5, off = bit & 31;
+        w[word] += m[i] << off;
+        corr[word] += M << off;
+        if (off + B > 32) {
+            w[word + 1] += m[i] >> (32 - off);
+            corr[word + 1] += M >> (32 - off);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < B; ++k) w[k] -= corr[k];
+}
+
+// The definition step by step (IEEE division), for groups the fast path does
+// not cover: NaN/Inf inside, constant groups, scales outside [2^-100, 2^100].
+template <int BITS>
+__device__ __noinline__ void key_group_exact(const uint32_t (&w)[16], uint32_t (&out)[BITS], uint16_t &sc, uint16_t &zr)
+{
+    float x[32];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        x[2 * k] = bf16_lo(w[k]);
+        x[2 * k + 1] = bf16_hi(w[k]);
+    }
     float mx = x[0], mn = x[0];
 #pragma unroll
     for (int j = 1; j < 32; ++j) {
@@ -103,115 +159,121 @@ __device__ __forceinline__ void key_group(const float (&x)[32], uint32_t (&code)
         lo = 0.0f;
         hi = maxv;
     }
-    // idx = clip(round(x/scale - zero)): clip first (NaN -> lo, IEEE maxNum/
-    // minNum), then round to nearest even by the 1.5*2^23 shift (|value| <= 127,
-    // so the integer lands in the low bits).
-    auto code_of = [&](float q) {
-        const float c = fminf(fmaxf(__fsub_rn(q, zero), lo), hi);
-        const uint32_t t = __float_as_uint(__fadd_rn(c, 12582912.0f)) - 0x4B400000u;
-        return BITS == 8 ? (t & 0xFFu) : t;
-    };
-    if (scale >= 0x1p-100f && scale <= 0x1p100f) {
-        // x/scale correctly rounded without a division (Markstein's theorem:
-        // with rc = RN(1/scale) and q0 within one ulp of x/scale, q0 + (x -
-        // scale*q0)*rc rounds to RN(x/scale)).  Bf16 keys inside a group with
-        // max != min keep |x/scale| <= 254*2^8, so nothing overflows; a
-        // quotient small enough to be inexact is below 1/4 and rounds to the
-        // same code either way.
-        const float rc = __frcp_rn(scale);
+    uint32_t code[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float q0 = __fmul_rn(x[j], rc);
-            const float e = __fmaf_rn(-scale, q0, x[j]);
-            code[j] = code_of(__fmaf_rn(e, rc, q0));
+    for (int j = 0; j < 32; ++j) {
+        // round, then clip (NaN -> lo, IEEE maxNum/minNum)
+        const float c = fminf(fmaxf(rintf(__fsub_rn(__fdiv_rn(x[j], scale), zero)), lo), hi);
+        code[j] = (uint32_t)(int)c & ((1u << BITS) - 1u);
+    }
+    pack_group<BITS>(code, out);
+    sc = f32_to_f16_bits(scale);
+    zr = f32_to_f16_bits(zero);
+}
+
+// One group of 32 keys (16 bf16 pairs) -> BITS packed words, fp16 scale and zero.
+template <int BITS>
+__device__ __forceinline__ void key_group(const uint32_t (&w)[16], uint32_t (&out)[BITS], uint16_t &sc, uint16_t &zr)
+{
+    // max propagates NaN (a NaN anywhere takes the exact path); min skips it
+    uint32_t a[8], b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        a[k] = bf16x2_max_nan(w[2 * k], w[2 * k + 1]);
+        b[k] = bf16x2_min(w[2 * k], w[2 * k + 1]);
+    }
+#pragma unroll
+    for (int s = 4; s >= 1; s >>= 1)
+#pragma unroll
+        for (int k = 0; k < s; ++k) {
+            a[k] = bf16x2_max_nan(a[k], a[k + s]);
+            b[k] = bf16x2_min(b[k], b[k + s]);
         }
-    } else {
-        // zero, subnormal, huge, Inf or NaN scale: IEEE division
+    const bool nan = (a[0] & 0x7FFFu) > 0x7F80u || (a[0] & 0x7FFF0000u) > 0x7F800000u;
+    const float mx = fmaxf(bf16_lo(a[0]), bf16_hi(a[0])), mn = fminf(bf16_lo(b[0]), bf16_hi(b[0]));
+    const float d = __fsub_rn(mx, mn);
+    constexpr float C = BITS == 8 ? 254.0f : (float)((1 << BITS) - 1);
+    constexpr float RC = BITS == 8 ? 0x1.020408p-8f : BITS == 2 ? 0x1.555556p-2f : BITS == 4 ? 0x1.111112p-4f : 0x1.08421p-5f;
+    const bool d_ok = !nan && d >= 0x1p-100f && d <= 0x1p100f;
+    const float scale = ms_div(d, C, RC);
+    if (!(d_ok && scale >= 0x1p-100f && scale <= 0x1p100f)) {
+        key_group_exact<BITS>(w, out, sc, zr);
+        return;
+    }
+    const float rc = __frcp_rn(scale);
+    const float zero = BITS == 8 ? rintf(ms_div(__fadd_rn(mx, mn), 2.0f * scale, 0.5f * rc)) : rintf(ms_div(mn, scale, rc));
+    if (!(fabsf(zero) <= 0x1p24f)) {  // max + min overflowed: the exact path clips as the definition does
+        key_group_exact<BITS>(w, out, sc, zr);
+        return;
+    }
+    // idx = clip(round(RN(RN(x/scale) - zero))), the quotient by Markstein's
+    // step.  The code is monotone in x, so when the group's min and max land
+    // inside [lo, hi] no element needs the clip (otherwise, a rare case, the
+    // exact path clips).  The rounding adds 1.5*2^23 (|value| <= 128 here), so
+    // each code sits in the low bits of the sum.
+    constexpr float LO = BITS == 8 ? -127.0f : 0.0f, HI = BITS == 8 ? 127.0f : (float)((1 << BITS) - 1);
+    if (!(rintf(__fsub_rn(ms_div(mn, scale, rc), zero)) >= LO && rintf(__fsub_rn(ms_div(mx, scale, rc), zero)) <= HI)) {
+        key_group_exact<BITS>(w, out, sc, zr);
+        return;
+    }
+    const float2 rc2 = make_float2(rc, rc), ns2 = make_float2(-scale, -scale), nz2 = make_float2(-zero, -zero);
+    const float2 mg2 = make_float2(12582912.0f, 12582912.0f);
+    uint32_t m[32];  // 0x4B400000 + code
 #pragma unroll
-        for (int j = 0; j < 32; ++j) code[j] = code_of(__fdiv_rn(x[j], scale));
+    for (int k = 0; k < 16; ++k) {
+        const float2 x = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
+        const float2 q0 = __fmul2_rn(x, rc2);
+        const float2 q = __ffma2_rn(__ffma2_rn(ns2, q0, x), rc2, q0);
+        const float2 c = __fadd2_rn(__fadd2_rn(q, nz2), mg2);
+        m[2 * k] = fbits(c.x);
+        m[2 * k + 1] = fbits(c.y);
+    }
+    if constexpr (BITS == 8) {
+        // low bytes are the codes in two's complement
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            out[i] = __byte_perm(__byte_perm(m[4 * i], m[4 * i + 1], 0x0040), __byte_perm(m[4 * i + 2], m[4 * i + 3], 0x0040),
+                                 0x5410);
+    } else {
+        pack_magic<BITS>(m, out);
     }
     sc = f32_to_f16_bits(scale);
     zr = f32_to_f16_bits(zero);
 }
 
 template <int D, int BITS>
-__device__ __forceinline__ void encode_key_lane(const EncodeParams &p, uint32_t slot, int64_t crow, int part)
+__device__ __forceinline__ void encode_key_lane(const EncodeParams &p, uint32_t a, int64_t crow, int part)
 {
-    using G = Geo<D>;
-    constexpr int LW = G::E * BITS / 32;  // output words per lane
-    uint32_t w[LW];
-    uint16_t sc[G::NG], zr[G::NG];
+    uint32_t w[16];
 #pragma unroll
-    for (int g = 0; g < G::NG; ++g) {
-        float x[32];
-        uint32_t code[32];
-        load_group(slot + 64 * g, x);
-        key_group<BITS>(x, code, sc[g], zr[g]);
-        uint32_t gw[BITS];
-        pack_group<BITS>(code, gw);
-#pragma unroll
-        for (int k = 0; k < BITS; ++k) w[g * BITS + k] = gw[k];
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = lds128(a + 16 * i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
-    constexpr int RB = D * BITS / 8, LB = G::E * BITS / 8;
-    constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
-    store_words<LW, A>(p.codes + crow * RB + part * LB, w);
-    uint32_t sw[G::NG / 2 > 0 ? G::NG / 2 : 1], zw[G::NG / 2 > 0 ? G::NG / 2 : 1];
-#pragma unroll
-    for (int i = 0; i < G::NG / 2; ++i) {
-        sw[i] = (uint32_t)sc[2 * i] | ((uint32_t)sc[2 * i + 1] << 16);
-        zw[i] = (uint32_t)zr[2 * i] | ((uint32_t)zr[2 * i + 1] << 16);
+    uint32_t out[BITS];
+    uint16_t sc, zr;
+    key_group<BITS>(w, out, sc, zr);
+    constexpr int RB = D * BITS / 8, LB = 4 * BITS;
+    if constexpr (BITS == 8) {
+        st_global_v8(p.codes + crow * RB + part * LB, out[0], out[1], out[2], out[3], out[4], out[5], out[6], out[7]);
+    } else {
+        constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
+        store_words<BITS, A>(p.codes + crow * RB + part * LB, out);
     }
-    constexpr int SA = align_of_bytes(D / 16) < align_of_bytes(G::NG * 2) ? align_of_bytes(D / 16)
-                                                                         : align_of_bytes(G::NG * 2);
-    store_words<G::NG / 2, SA>(p.scale + crow * (D / 32) + part * G::NG, sw);
-    store_words<G::NG / 2, SA>(p.zero + crow * (D / 32) + part * G::NG, zw);
+    p.scale[crow * (D / 32) + part] = sc;
+    p.zero[crow * (D / 32) + part] = zr;
 }
 
 // ------------------------------------------------------------------ values
-// Local Sylvester butterflies, strides 1 .. E/2, in place.
-template <int E>
-__device__ __forceinline__ void fwht_local(float (&x)[E])
-{
-#pragma unroll
-    for (int h = 1; h < E; h <<= 1)
-#pragma unroll
-        for (int i = 0; i < E; i += 2 * h)
-#pragma unroll
-            for (int j = i; j < i + h; ++j) {
-                const float a = x[j], b = x[j + h];
-                x[j] = __fadd_rn(a, b);
-                x[j + h] = __fsub_rn(a, b);
-            }
-}
-
-// Butterflies across lanes: stride E*s pairs lane bit s clear (a) with set (b);
-// the clear lane keeps a + b, the set lane a - b.
-template <int E>
-__device__ __forceinline__ void fwht_cross(float (&x)[E], int lane_bit_s, bool upper)
-{
-    const float sg = upper ? -1.0f : 1.0f;
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-        const float other = __shfl_xor_sync(0xffffffffu, x[j], lane_bit_s);
-        x[j] = __fmaf_rn(x[j], sg, other);  // exact product: a + b, or a - b
-    }
-}
-
-template <int NB>
-__device__ __forceinline__ uint32_t count_below_linear(const float *bnd, float y)
-{
-    uint32_t k = 0;
-#pragma unroll
-    for (int i = 0; i < NB; ++i) k += (bnd[i] < y) ? 1u : 0u;
-    return k;
-}
-
 // number of boundaries strictly below y (searchsorted, side = left); NaN -> 0
 template <int BITS>
 __device__ __forceinline__ uint32_t value_index(const EncodeParams &p, const float *sbnd, float y)
 {
     if constexpr (BITS <= 3) {
-        return count_below_linear<(1 << BITS) - 1>(p.bnd, y);
+        uint32_t k = 0;
+#pragma unroll
+        for (int i = 0; i < (1 << BITS) - 1; ++i) k += (p.bnd[i] < y) ? 1u : 0u;
+        return k;
     } else {
         uint32_t pos = 0;
 #pragma unroll
@@ -221,119 +283,165 @@ __device__ __forceinline__ uint32_t value_index(const EncodeParams &p, const flo
     }
 }
 
-template <int D, int BITS>
-__device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const float *sbnd, uint32_t slot, int64_t crow,
-                                                  int part, bool row_valid)
+template <int BITS>
+__device__ __forceinline__ void put_code(uint32_t (&w)[BITS], int j, uint32_t c)
 {
-    using G = Geo<D>;
-    constexpr int E = G::E;
-    float x[E];
-    if (row_valid) {
-#pragma unroll
-        for (int i = 0; i < E / 8; ++i) {
-            uint4 v = lds128(slot + 16 * i);
-            x[8 * i + 0] = bf16_lo(v.x); x[8 * i + 1] = bf16_hi(v.x);
-            x[8 * i + 2] = bf16_lo(v.y); x[8 * i + 3] = bf16_hi(v.y);
-            x[8 * i + 4] = bf16_lo(v.z); x[8 * i + 5] = bf16_hi(v.z);
-            x[8 * i + 6] = bf16_lo(v.w); x[8 * i + 7] = bf16_hi(v.w);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < E; ++j) x[j] = 0.0f;
-    }
-    // x * signs (exact)
-    if constexpr (G::LPR == 1) {
-#pragma unroll
-        for (int j = 0; j < E; ++j) x[j] = x[j] * sign_value(j);
-    } else {
-#pragma unroll
-        for (int w = 0; w < E / 32; ++w) {
-            uint32_t m = sign_word(w);
-#pragma unroll
-            for (int q = 1; q < G::LPR; ++q)
-                if (part == q) m = sign_word(q * (E / 32) + w);
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                x[32 * w + k] = __uint_as_float(__float_as_uint(x[32 * w + k]) ^ ((m << (31 - k)) & 0x80000000u));
-        }
-    }
-    fwht_local<E>(x);
-    if constexpr (G::LPR >= 2) fwht_cross<E>(x, 1, (part & 1) != 0);
-    if constexpr (G::LPR >= 4) fwht_cross<E>(x, 2, (part & 2) != 0);
-    if (!row_valid) return;
+    // j is a compile-time index inside unrolled loops; fields do not overlap
+    const int bit = j * BITS, word = bit >> 5, off = bit & 31;
+    w[word] += c << off;
+    if (off + BITS > 32) w[word + 1] += c >> (32 - off);
+}
 
-    uint32_t w[E * BITS / 32];
-    uint16_t sc[G::NG];
+// Value codes of a warp tile are written to a shared staging area (rows x
+// row bytes, the tile's own layout in the cache) and leave in one bulk store.
+template <int D, int BITS>
+__device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const float *sbnd, uint32_t a, uint32_t mtab,
+                                                  uint32_t stage, int64_t crow, int r, int part, bool valid)
+{
+    using G = EGeo<D, false>;
+    float2 P[32];  // P[j] = (element j, element j + 32) of this lane's 64
+    if (valid) {
 #pragma unroll
-    for (int g = 0; g < G::NG; ++g) {
-        float y[32];
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = lds128(a + 16 * i), v = lds128(a + 64 + 16 * i);
+            const uint32_t uw[4] = {u.x, u.y, u.z, u.w}, vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(x[32 * g + j], p.inv_sqrt_d);
-        float ss = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ss = __fmaf_rn(y[j], y[j], ss);
-        const float sigma = __fsqrt_rn(__fdiv_rn(ss, 32.0f));
-        const float den = __fadd_rn(sigma, 1e-8f);
-        uint32_t code[32];
-        if (den < INFINITY) {
-            // The index counts the boundaries b below y/den.  Comparing y with
-            // b*den instead needs no division; the two can differ only when
-            // y/den lies within a few ulps of a boundary.
-            if constexpr (BITS <= 3) {
-                constexpr int H = 1 << (BITS - 1);  // the table is antisymmetric, b[H-1] = 0
-                float P[H - 1];
-#pragma unroll
-                for (int k = 0; k < H - 1; ++k) P[k] = __fmul_rn(p.bnd[H + k], den);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float a = fabsf(y[j]);
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int k = 0; k < H - 1; ++k) m += a > P[k] ? 1u : 0u;
-                    code[j] = y[j] > 0.0f ? H + m : H - 1 - m;
-                }
-            } else {
-                const float rden = __frcp_rn(den);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) code[j] = value_index<BITS>(p, sbnd, __fmul_rn(y[j], rden));
+            for (int q = 0; q < 4; ++q) {
+                const int k = 4 * i + q;
+                // sign masks of elements 2k, 2k+1, 2k+32, 2k+33 (bit 31 set = negate)
+                const uint4 m = lds128(mtab + 16 * k);
+                P[2 * k] = make_float2(__uint_as_float(uw[q] * 0x10000u + m.x), __uint_as_float(vw[q] * 0x10000u + m.z));
+                P[2 * k + 1] = make_float2(__uint_as_float((uw[q] & 0xFFFF0000u) ^ m.y),
+                                           __uint_as_float((vw[q] & 0xFFFF0000u) ^ m.w));
             }
-        } else {
-            // non-finite row (Inf/NaN inputs): the definition step by step
-#pragma unroll
-            for (int j = 0; j < 32; ++j) code[j] = value_index<BITS>(p, sbnd, __fdiv_rn(y[j], den));
         }
-        uint32_t gw[BITS];
-        pack_group<BITS>(code, gw);
+    } else {
 #pragma unroll
-        for (int k = 0; k < BITS; ++k) w[g * BITS + k] = gw[k];
-        sc[g] = f32_to_f16_bits(sigma);
+        for (int j = 0; j < 32; ++j) P[j] = make_float2(0.0f, 0.0f);
     }
-    constexpr int RB = D * BITS / 8, LB = E * BITS / 8;
-    constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
-    store_words<E * BITS / 32, A>(p.codes + crow * RB + part * LB, w);
-    uint32_t sw[G::NG / 2];
+    fwht_pairs<G::LPR, G::ROWS>(P, part);
+    if (!valid) return;
+    // y = z / sqrt(d); both groups' sums of squares in element order
+    const float2 c2 = make_float2(p.inv_sqrt_d, p.inv_sqrt_d);
+    float2 ss = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int i = 0; i < G::NG / 2; ++i) sw[i] = (uint32_t)sc[2 * i] | ((uint32_t)sc[2 * i + 1] << 16);
-    constexpr int SA = align_of_bytes(D / 16) < align_of_bytes(G::NG * 2) ? align_of_bytes(D / 16)
-                                                                         : align_of_bytes(G::NG * 2);
-    store_words<G::NG / 2, SA>(p.scale + crow * (D / 32) + part * G::NG, sw);
+    for (int j = 0; j < 32; ++j) {
+        P[j] = __fmul2_rn(P[j], c2);
+        ss = __ffma2_rn(P[j], P[j], ss);
+    }
+    const float2 ms = __fmul2_rn(ss, make_float2(0.03125f, 0.03125f));  // /32, exact
+    const float sig0 = __fsqrt_rn(ms.x), sig1 = __fsqrt_rn(ms.y);
+    const float den0 = __fadd_rn(sig0, 1e-8f), den1 = __fadd_rn(sig1, 1e-8f);
+    uint32_t w0[BITS], w1[BITS];
+#pragma unroll
+    for (int k = 0; k < BITS; ++k) w0[k] = w1[k] = 0;
+    bool done = false;
+    if constexpr (BITS <= 3) {
+        if (den0 < INFINITY && den1 < INFINITY) {
+            // The index counts the boundaries b below y/den.  The table is
+            // antisymmetric with b[H-1] = 0, so with m = #{positive b : |y| <
+            // b*den} the index is m for y <= 0 and 2H-1-m for y > 0.  |y| < b*den
+            // is tested as y*y - (b*den)^2 < 0 (one fused step per pair); it can
+            // differ from the division only within a few ulps of a boundary.
+            constexpr int H = 1 << (BITS - 1);
+            float2 nq[H - 1];
+#pragma unroll
+            for (int k = 0; k < H - 1; ++k) {
+                const float t0 = __fmul_rn(p.bnd[H + k], den0), t1 = __fmul_rn(p.bnd[H + k], den1);
+                nq[k] = make_float2(-__fmul_rn(t0, t0), -__fmul_rn(t1, t1));
+            }
+            // The thresholds tested are a thermometer code (s_k = [|y| < P_k]
+            // rises with k), so m's bits are s_2 (bit 1) and s_1^s_2^s_3 (bit 0),
+            // and every code bit is that bit xor [y > 0] -- all read from bit 31
+            // of the fused results, combined with three-input logic, and shifted
+            // straight into the group's words, highest stream bit first.
+            const float2 m1 = make_float2(-1.0f, -1.0f), z2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int j = 31; j >= 0; --j) {
+                float2 e[H - 1];
+#pragma unroll
+                for (int k = 0; k < H - 1; ++k) e[k] = __ffma2_rn(P[j], P[j], nq[k]);  // sign set iff y^2 < P_k^2
+                const float2 n = __ffma2_rn(P[j], m1, z2);                             // sign set iff y > 0 (+0 for y = +-0)
+                uint32_t c0[BITS], c1[BITS];  // code bits of element j of each group in bit 31, highest first
+                if constexpr (BITS == 3) {
+                    const uint32_t ax = fbits(e[1].x) ^ fbits(n.x), ay = fbits(e[1].y) ^ fbits(n.y);
+                    c0[0] = fbits(n.x); c0[1] = ax; c0[2] = fbits(e[0].x) ^ fbits(e[2].x) ^ ax;
+                    c1[0] = fbits(n.y); c1[1] = ay; c1[2] = fbits(e[0].y) ^ fbits(e[2].y) ^ ay;
+                } else {
+                    c0[0] = fbits(n.x); c0[1] = fbits(e[0].x) ^ fbits(n.x);
+                    c1[0] = fbits(n.y); c1[1] = fbits(e[0].y) ^ fbits(n.y);
+                }
+#pragma unroll
+                for (int q = 0; q < BITS; ++q) {
+                    const int word = (j * BITS + BITS - 1 - q) >> 5;
+                    w0[word] = __funnelshift_l(c0[q], w0[word], 1);
+                    w1[word] = __funnelshift_l(c1[q], w1[word], 1);
+                }
+            }
+            done = true;
+        }
+    }
+    if (!done) {
+        const bool fin0 = den0 < INFINITY, fin1 = den1 < INFINITY;
+        const float r0 = __frcp_rn(den0), r1 = __frcp_rn(den1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            // finite rows: y * RN(1/den), within an ulp of the quotient; others the definition's division
+            const float q0 = fin0 ? __fmul_rn(P[j].x, r0) : __fdiv_rn(P[j].x, den0);
+            const float q1 = fin1 ? __fmul_rn(P[j].y, r1) : __fdiv_rn(P[j].y, den1);
+            put_code<BITS>(w0, j, value_index<BITS>(p, sbnd, q0));
+            put_code<BITS>(w1, j, value_index<BITS>(p, sbnd, q1));
+        }
+    }
+    uint32_t w[2 * BITS];
+#pragma unroll
+    for (int k = 0; k < BITS; ++k) {
+        w[k] = w0[k];
+        w[BITS + k] = w1[k];
+    }
+    constexpr int RB = D * BITS / 8, LB = 8 * BITS;
+    constexpr int A = align_of_bytes(LB) < 8 ? align_of_bytes(LB) : 8;
+    const uint32_t at = stage + r * RB + part * LB;
+#pragma unroll
+    for (int i = 0; i < 2 * BITS; i += A / 4) {
+        if constexpr (A == 8)
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(at + 4 * i), "r"(w[i]), "r"(w[i + 1]) : "memory");
+        else
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(at + 4 * i), "r"(w[i]) : "memory");
+    }
+    const uint32_t sw = (uint32_t)f32_to_f16_bits(sig0) | ((uint32_t)f32_to_f16_bits(sig1) << 16);
+    *reinterpret_cast<uint32_t *>(p.scale + crow * (D / 32) + 2 * part) = sw;
 }
 
 // ------------------------------------------------------------------ kernel
 template <int D, int BITS, bool KEY>
 __global__ void __launch_bounds__(kWarps * 32) encode_kernel(const __grid_constant__ EncodeParams p)
 {
-    using G = Geo<D>;
+    using G = EGeo<D, KEY>;
+    constexpr int SB = (!KEY && BITS > 3) ? 1024 : 0;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // 2 per warp
     float *sbnd = reinterpret_cast<float *>(smem + 16 * kWarps);
-    uint8_t *tiles = smem + 16 * kWarps + (KEY || BITS <= 3 ? 0 : 1024);
+    uint8_t *mtab = smem + 16 * kWarps + SB;
+    constexpr int STG = KEY ? 0 : VStage<D, BITS>::BYTES;
+    uint8_t *stages = mtab + G::MTAB;  // value code staging, one per warp
+    uint8_t *tiles = stages + kWarps * STG;
     const uint32_t buf0 = smem_addr(tiles + warp * 2 * G::TILE), buf1 = buf0 + G::TILE;
     const uint32_t bar0 = smem_addr(&bars[2 * warp]), bar1 = bar0 + 8;
 
-    if constexpr (!KEY && BITS > 3) {
+    if constexpr (SB > 0) {
         for (int i = threadIdx.x; i < (1 << BITS) - 1; i += blockDim.x) sbnd[i] = p.bnd[i];
+    }
+    if constexpr (!KEY) {
+        // sign masks: entry (part, k) = elements 64 part + {2k, 2k+1, 2k+32, 2k+33}
+        for (int i = threadIdx.x; i < G::LPR * 16; i += blockDim.x) {
+            const int part = i >> 4, k = i & 15, e = 64 * part + 2 * k;
+            const uint4 m = make_uint4(sign_negative(e) ? 0x80000000u : 0u, sign_negative(e + 1) ? 0x80000000u : 0u,
+                                       sign_negative(e + 32) ? 0x80000000u : 0u,
+                                       sign_negative(e + 33) ? 0x80000000u : 0u);
+            *reinterpret_cast<uint4 *>(mtab + part * 272 + 16 * k) = m;
+        }
     }
     if (lane == 0) {
         mbar_init(bar0, 1);
@@ -342,50 +450,74 @@ __global__ void __launch_bounds__(kWarps * 32) encode_kernel(const __grid_consta
     }
     __syncthreads();
 
-    const int64_t W = (int64_t)gridDim.x * kWarps;
-    int64_t item = (int64_t)blockIdx.x * kWarps + warp;
-    if (item < p.items) issue_tile<D>(p, item, buf0, bar0, lane);
+    const int r = lane % G::ROWS, part = lane / G::ROWS;
+    const uint32_t my_mtab = smem_addr(mtab) + part * 272;
+    const uint32_t W = gridDim.x * kWarps;
+    uint32_t item = blockIdx.x * kWarps + warp;
+    if (item < p.items) issue_tile<D, KEY>(p, item, buf0, bar0, lane);
     for (uint32_t k = 0; item < p.items; item += W, ++k) {
-        const int64_t next = item + W;
+        const uint32_t next = item + W;
         const uint32_t buf = (k & 1) ? buf1 : buf0, bar = (k & 1) ? bar1 : bar0;
-        if (next < p.items) issue_tile<D>(p, next, (k & 1) ? buf0 : buf1, (k & 1) ? bar0 : bar1, lane);
+        if (next < p.items) issue_tile<D, KEY>(p, next, (k & 1) ? buf0 : buf1, (k & 1) ? bar0 : bar1, lane);
         if (!mbar_wait_bounded(bar, (k >> 1) & 1, p.err)) {
             // give the other copy a bounded chance to land before leaving
             if (next < p.items) mbar_wait_bounded((k & 1) ? bar0 : bar1, ((k + 1) >> 1) & 1, p.err);
+            if (!KEY && lane == 0) bulk_wait0();
             return;
         }
-        const int64_t bh = item / p.tiles_per_bh;
-        const int64_t t_first = (item - bh * p.tiles_per_bh) * G::ROWS;
-        const int r = lane / G::LPR, part = lane % G::LPR;
+        const uint32_t bh = fast_div(item, p.div_tiles);
+        const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::ROWS;
         const bool valid = t_first + r < p.n;
-        const int64_t crow = bh * p.cap + p.t0 + t_first + r;
-        const uint32_t slot = buf + lane * G::SLOT;
+        const int64_t crow = (int64_t)bh * p.cap + p.t0 + t_first + r;
+        const uint32_t a = buf + r * G::RS + part * (G::E * 2);
         if constexpr (KEY) {
-            if (valid) encode_key_lane<D, BITS>(p, slot, crow, part);
+            if (valid) encode_key_lane<D, BITS>(p, a, crow, part);
         } else {
+            constexpr int RB = VStage<D, BITS>::RB;
+            const uint32_t stage = smem_addr(stages + warp * STG);
+            // the previous tile's bulk store must have read the staging area
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
             // every lane of a row joins the cross-lane stages, so no early exit
-            encode_value_lane<D, BITS>(p, sbnd, slot, crow, part, valid);
+            encode_value_lane<D, BITS>(p, sbnd, a, my_mtab, stage, crow, r, part, valid);
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int rows = (int)imin64(G::ROWS, p.n - t_first);
+            uint8_t *dst = p.codes + (crow - r) * RB;
+            if (((uintptr_t)dst & 15) == 0 && (rows * RB) % 16 == 0) {
+                if (lane == 0) {
+                    bulk_s2g(dst, stage, (uint32_t)(rows * RB));
+                    bulk_commit();
+                }
+            } else {
+                // destination or size not a multiple of 16 bytes (row bytes are a multiple of 8): plain stores
+                for (int i = 8 * lane; i < rows * RB; i += 256)
+                    *reinterpret_cast<uint2 *>(dst + i) = *reinterpret_cast<const uint2 *>(stages + warp * STG + i);
+            }
         }
         __syncwarp();
     }
+    // staged value codes: the bulk stores must have read shared memory before the CTA ends
+    if (!KEY && lane == 0) bulk_wait0();
 }
 
 template <int D, int BITS, bool KEY>
 cudaError_t run(const EncodeParams &p, cudaStream_t s)
 {
-    using G = Geo<D>;
-    const size_t smem = 16 * kWarps + (KEY || BITS <= 3 ? 0 : 1024) + (size_t)kWarps * 2 * G::TILE;
+    using G = EGeo<D, KEY>;
+    const size_t smem = 16 * kWarps + ((!KEY && BITS > 3) ? 1024 : 0) + G::MTAB +
+                        (size_t)kWarps * (KEY ? 0 : VStage<D, BITS>::BYTES) + (size_t)kWarps * 2 * G::TILE;
     auto kern = encode_kernel<D, BITS, KEY>;
-    static bool configured = false;  // attribute set once per process (idempotent)
-    if (!configured) {
+    static int per_sm = 0;  // same on every GB300; only a successful query is kept
+    if (!per_sm) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, smem);
+        if (e != cudaSuccess) return e;
+        per_sm = n > 0 ? n : 1;
     }
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem);
-    if (per_sm < 1) per_sm = 1;
-    const int64_t want = (p.items + kWarps - 1) / kWarps;
+    const int64_t want = ((int64_t)p.items + kWarps - 1) / kWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
     kern<<<grid, kWarps * 32, smem, s>>>(p);
     return cudaGetLastError();
@@ -416,18 +548,27 @@ cudaError_t dispatch_value(int vb, const EncodeParams &p, cudaStream_t s)
     return cudaErrorInvalidValue;
 }
 
+// Tiles of `rows` token rows per (sequence, kv-head); false if the count
+// does not fit the kernels' 31-bit item index.
+inline bool set_items(EncodeParams &p, int64_t n, int rows, const CacheView &c)
+{
+    const int64_t tiles = (n + rows - 1) / rows, items = tiles * (int64_t)c.B * c.H;
+    if (items >= (int64_t(1) << 31)) return false;
+    p.tiles_per_bh = (uint32_t)tiles;
+    p.items = (uint32_t)items;
+    p.div_tiles = make_fastdiv(tiles > 0 ? (uint32_t)tiles : 1u);
+    return true;
+}
+
 template <int D>
 cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3], const uint16_t *v,
                      const int64_t vs[3], int64_t t0, int64_t n, cudaStream_t s)
 {
-    using G = Geo<D>;
     EncodeParams p{};
     p.H = c.H;
     p.cap = c.cap;
     p.t0 = t0;
     p.n = n;
-    p.tiles_per_bh = (n + G::ROWS - 1) / G::ROWS;
-    p.items = p.tiles_per_bh * (int64_t)c.B * c.H;
     p.inv_sqrt_d = inv_sqrt_head_dim(D);
     p.err = device_error_word();
     if (!p.err) return cudaErrorInvalidDevice;
@@ -439,6 +580,8 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     p.codes = c.k_codes;
     p.scale = c.k_scale;
     p.zero = c.k_zero;
+    p.div_h = make_fastdiv((uint32_t)c.H);
+    if (!set_items(p, n, EGeo<D, true>::ROWS, c)) return cudaErrorInvalidValue;
     cudaError_t e = dispatch_key<D>(c.kb, p, s);
     if (e != cudaSuccess) return e;
 
@@ -447,6 +590,7 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     p.codes = c.v_codes;
     p.scale = c.v_scale;
     p.zero = nullptr;
+    if (!set_items(p, n, EGeo<D, false>::ROWS, c)) return cudaErrorInvalidValue;
     return dispatch_value<D>(c.vb, p, s);
 }
 

@@ -7,7 +7,14 @@
  * subnormal and near-constant groups), derives scale and zero as the codec does,
  * and counts elements whose index differs from the one IEEE division gives.
  * CPU fmaf and 1.0f/x are IEEE-exact, like the GPU's fused multiply-add and its
- * correctly rounded reciprocal.  Prints "<elements> <mismatches>".
+ * correctly rounded reciprocal.
+ *
+ * The per-group parameters are checked the same way, bit for bit (the sign of
+ * a zero included): scale = (max-min)/C for C in {254, 3, 15, 31} through the
+ * constant reciprocal RN(1/C) whenever max-min lies in [2^-100, 2^100], the
+ * signed zero point (max+min)/(2 scale) through RN(1/scale)/2, and the unsigned
+ * zero point min/scale through RN(1/scale).  Prints "<elements> <mismatches>
+ * <groups> <parameter mismatches>".
  */
 #include <math.h>
 #include <stdint.h>
@@ -24,9 +31,35 @@ static float bf16r(float f)
     float g; memcpy(&g, &u, 4); return g;
 }
 
+static uint32_t bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+static float markstein(float x, float y, float ry)
+{
+    const float q0 = x * ry, e = fmaf(-y, q0, x);
+    return fmaf(e, ry, q0);
+}
+
+/* 1 if any per-group parameter from the division-free forms differs from IEEE division */
+static int params_differ(float mx, float mn)
+{
+    static const float C[4] = {254.0f, 3.0f, 15.0f, 31.0f};
+    const float d = mx - mn;
+    if (!(d >= 0x1p-100f && d <= 0x1p100f)) return 0;
+    int bad = 0;
+    for (int c = 0; c < 4; ++c) {
+        const float scale = d / C[c];
+        bad |= bits(markstein(d, C[c], 1.0f / C[c])) != bits(scale);
+        if (!(scale >= 0x1p-100f && scale <= 0x1p100f)) continue;
+        const float rc = 1.0f / scale;
+        if (c == 0) bad |= bits(rintf(markstein(mx + mn, 2.0f * scale, 0.5f * rc))) != bits(rintf((mx + mn) / (2.0f * scale)));
+        else bad |= bits(rintf(markstein(mn, scale, rc))) != bits(rintf(mn / scale));
+    }
+    return bad;
+}
+
 int main(int argc, char **argv)
 {
-    long groups = argc > 1 ? atol(argv[1]) : 200000, elems = 0, bad = 0;
+    long groups = argc > 1 ? atol(argv[1]) : 200000, elems = 0, bad = 0, pgroups = 0, pbad = 0;
     for (long it = 0; it < groups; ++it) {
         float x[32];
         int mode = (int)(it % 4), e0 = (int)(rnd() % 270) - 140;
@@ -41,6 +74,13 @@ int main(int argc, char **argv)
         }
         float mx = x[0], mn = x[0];
         for (int j = 1; j < 32; ++j) { mx = fmaxf(mx, x[j]); mn = fminf(mn, x[j]); }
+        ++pgroups;
+        pbad += params_differ(mx, mn);
+        {   /* arbitrary fp32 max/min pairs as well (not only bf16 groups) */
+            uint32_t a = (uint32_t)rnd(), b = (uint32_t)rnd();
+            float fa, fb; memcpy(&fa, &a, 4); memcpy(&fb, &b, 4);
+            if (isfinite(fa) && isfinite(fb)) { ++pgroups; pbad += params_differ(fmaxf(fa, fb), fminf(fa, fb)); }
+        }
         for (int signed8 = 0; signed8 < 2; ++signed8) {
             float scale, zero, lo, hi;
             if (signed8) { scale = (mx - mn) / 254.0f; zero = rintf((mx + mn) / (2.0f * scale)); lo = -127; hi = 127; }
@@ -56,6 +96,6 @@ int main(int argc, char **argv)
             }
         }
     }
-    printf("%ld %ld\n", elems, bad);
+    printf("%ld %ld %ld %ld\n", elems, bad, pgroups, pbad);
     return 0;
 }
