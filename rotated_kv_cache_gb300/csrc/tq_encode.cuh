@@ -35,11 +35,19 @@ constexpr int kWarps = 4;  // warps per CTA
 
 template <int D, bool KEY>
 struct EGeo {
-    static constexpr int E = KEY ? 32 : 64;  // elements per lane
-    static constexpr int LPR = D / E;         // lanes per row
-    static constexpr int ROWS = 32 / LPR;     // rows per warp tile
-    static constexpr int RS = 2 * D + 16;     // row slot bytes: 16 mod 128, so 8 rows' 16-byte reads hit 8 bank groups
-    static constexpr int TILE = ROWS * RS;
+    static constexpr int E = KEY ? 32 : 64;   // elements per lane and row
+    static constexpr int LPR = D / E;          // lanes per row
+    static constexpr int ROWS = 32 / LPR;      // rows one pass of the warp covers
+    static constexpr int RPL = KEY ? 4 : 1;    // rows per lane: independent key groups interleave
+    static constexpr int TROWS = ROWS * RPL;   // rows per warp tile
+    // Two tile layouts, one read formula (chunk k of a row's 64-column box at
+    // base + 16 * (k ^ xr)):
+    //   tensor copy  D/64 boxes of TROWS x 128 bytes, 128-byte swizzle (xr = row & 7)
+    //   row copies   rows RS bytes apart, RS = 16 mod 128 (xr = 0)
+    // either way 8 rows' 16-byte reads hit 8 different bank groups.
+    static constexpr int RS = 2 * D + 16;
+    static constexpr int BOX = (TROWS * 128 + 1023) / 1024 * 1024;  // box stride: swizzle atoms are 1024-aligned
+    static constexpr int TILE = ((TROWS * RS > (D / 64) * BOX ? TROWS * RS : (D / 64) * BOX) + 1023) / 1024 * 1024;
     static constexpr int MTAB = KEY ? 0 : LPR * 272;  // value sign masks: 16 x 16 bytes (+16 pad) per part
 };
 
@@ -61,22 +69,43 @@ struct EncodeParams {
     FastDiv div_tiles, div_h;      // x / tiles_per_bh, x / H
     float inv_sqrt_d;
     uint32_t *err;
+    int use_tma;     // tiles arrive by tensor copies of the map (else one bulk copy per row)
     float bnd[255];  // value boundaries (ascending)
 };
 
 template <int D, bool KEY>
-__device__ __forceinline__ void issue_tile(const EncodeParams &p, uint32_t item, uint32_t buf, uint32_t bar, int lane)
+__device__ __forceinline__ void issue_tile(const EncodeParams &p, const CUtensorMap &map, uint32_t item, uint32_t buf,
+                                           uint32_t bar, int lane)
 {
     using G = EGeo<D, KEY>;
     const uint32_t bh = fast_div(item, p.div_tiles);
-    const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::ROWS;
-    const int rows = (int)imin64(G::ROWS, p.n - t_first);
+    const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::TROWS;
+    const uint32_t b = fast_div(bh, p.div_h), h = bh - b * (uint32_t)p.H;
+    if (p.use_tma) {
+        // one tensor copy per 64-column box; rows past n arrive as zeros
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, (uint32_t)((D / 64) * G::TROWS * 128));
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_load_4d(buf + c * G::BOX, &map, 64 * c, (int)t_first, (int)h, (int)b, bar);
+        }
+        return;
+    }
+    const int rows = (int)imin64(G::TROWS, p.n - t_first);
     if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows * D * 2));
     __syncwarp();
     if (lane < rows) {
-        const uint32_t b = fast_div(bh, p.div_h), h = bh - b * (uint32_t)p.H;
-        bulk_g2s(buf + lane * G::RS, p.src + b * p.sb + h * p.sh + (t_first + lane) * p.st, D * 2, bar);
+        const uint16_t *src = p.src + b * p.sb + h * p.sh + t_first * p.st;
+        for (int row = lane; row < rows; row += 32) bulk_g2s(buf + row * G::RS, src + row * p.st, D * 2, bar);
     }
+}
+
+// Shared-memory base of a row's 64-column box c and the chunk xor for it.
+template <int D, bool KEY>
+__device__ __forceinline__ uint32_t box_base(const EncodeParams &p, uint32_t buf, int row, int c, uint32_t &xr)
+{
+    using G = EGeo<D, KEY>;
+    xr = p.use_tma ? (uint32_t)(row & 7) : 0u;
+    return p.use_tma ? buf + c * G::BOX + row * 128 : buf + row * G::RS + 128 * c;
 }
 
 // ------------------------------------------------------------------ packed helpers
@@ -131,14 +160,22 @@ __device__ __forceinline__ void pack_magic(const uint32_t (&m)[32], uint32_t (&w
 
 // The definition step by step (IEEE division), for groups the fast path does
 // not cover: NaN/Inf inside, constant groups, scales outside [2^-100, 2^100].
+// It reads its 32 keys from the shared tile (a) and writes the group's codes,
+// scale and zero point itself.
 template <int BITS>
-__device__ __noinline__ void key_group_exact(const uint32_t (&w)[16], uint32_t (&out)[BITS], uint16_t &sc, uint16_t &zr)
+__device__ __noinline__ void key_group_exact(uint32_t a, uint32_t ch0, uint32_t xr, uint8_t *codes, uint16_t *scale_at,
+                                             uint16_t *zero_at)
 {
     float x[32];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        x[2 * k] = bf16_lo(w[k]);
-        x[2 * k + 1] = bf16_hi(w[k]);
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = lds128(a + 16 * ((ch0 + i) ^ xr));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            x[8 * i + 2 * q] = bf16_lo(u[q]);
+            x[8 * i + 2 * q + 1] = bf16_hi(u[q]);
+        }
     }
     float mx = x[0], mn = x[0];
 #pragma unroll
@@ -166,14 +203,23 @@ __device__ __noinline__ void key_group_exact(const uint32_t (&w)[16], uint32_t (
         const float c = fminf(fmaxf(rintf(__fsub_rn(__fdiv_rn(x[j], scale), zero)), lo), hi);
         code[j] = (uint32_t)(int)c & ((1u << BITS) - 1u);
     }
+    uint32_t out[BITS];
     pack_group<BITS>(code, out);
-    sc = f32_to_f16_bits(scale);
-    zr = f32_to_f16_bits(zero);
+    store_words<BITS, align_of_bytes(4 * BITS) < 8 ? align_of_bytes(4 * BITS) : 8>(codes, out);
+    *scale_at = f32_to_f16_bits(scale);
+    *zero_at = f32_to_f16_bits(zero);
 }
 
-// One group of 32 keys (16 bf16 pairs) -> BITS packed words, fp16 scale and zero.
+// Per-group key parameters, computed without branches; ok is false where the
+// fast element pass does not apply (NaN/Inf inside, constant or extreme
+// groups, max + min overflowing, or a code that would need the clip).
+struct KeyParams {
+    float scale, rc, zero;
+    bool ok;
+};
+
 template <int BITS>
-__device__ __forceinline__ void key_group(const uint32_t (&w)[16], uint32_t (&out)[BITS], uint16_t &sc, uint16_t &zr)
+__device__ __forceinline__ KeyParams key_params(const uint32_t (&w)[16])
 {
     // max propagates NaN (a NaN anywhere takes the exact path); min skips it
     uint32_t a[8], b[8];
@@ -194,39 +240,38 @@ __device__ __forceinline__ void key_group(const uint32_t (&w)[16], uint32_t (&ou
     const float d = __fsub_rn(mx, mn);
     constexpr float C = BITS == 8 ? 254.0f : (float)((1 << BITS) - 1);
     constexpr float RC = BITS == 8 ? 0x1.020408p-8f : BITS == 2 ? 0x1.555556p-2f : BITS == 4 ? 0x1.111112p-4f : 0x1.08421p-5f;
-    const bool d_ok = !nan && d >= 0x1p-100f && d <= 0x1p100f;
-    const float scale = ms_div(d, C, RC);
-    if (!(d_ok && scale >= 0x1p-100f && scale <= 0x1p100f)) {
-        key_group_exact<BITS>(w, out, sc, zr);
-        return;
-    }
-    const float rc = __frcp_rn(scale);
-    const float zero = BITS == 8 ? rintf(ms_div(__fadd_rn(mx, mn), 2.0f * scale, 0.5f * rc)) : rintf(ms_div(mn, scale, rc));
-    if (!(fabsf(zero) <= 0x1p24f)) {  // max + min overflowed: the exact path clips as the definition does
-        key_group_exact<BITS>(w, out, sc, zr);
-        return;
-    }
-    // idx = clip(round(RN(RN(x/scale) - zero))), the quotient by Markstein's
-    // step.  The code is monotone in x, so when the group's min and max land
-    // inside [lo, hi] no element needs the clip (otherwise, a rare case, the
-    // exact path clips).  The rounding adds 1.5*2^23 (|value| <= 128 here), so
-    // each code sits in the low bits of the sum.
+    KeyParams k;
+    k.scale = ms_div(d, C, RC);
+    k.rc = __frcp_rn(k.scale);
+    k.zero = BITS == 8 ? rintf(ms_div(__fadd_rn(mx, mn), 2.0f * k.scale, 0.5f * k.rc)) : rintf(ms_div(mn, k.scale, k.rc));
+    // The code RN(RN(x/scale) - zero), rounded, is monotone in x: when the
+    // group's min and max land inside [lo, hi], no element needs the clip.
     constexpr float LO = BITS == 8 ? -127.0f : 0.0f, HI = BITS == 8 ? 127.0f : (float)((1 << BITS) - 1);
-    if (!(rintf(__fsub_rn(ms_div(mn, scale, rc), zero)) >= LO && rintf(__fsub_rn(ms_div(mx, scale, rc), zero)) <= HI)) {
-        key_group_exact<BITS>(w, out, sc, zr);
-        return;
-    }
-    const float2 rc2 = make_float2(rc, rc), ns2 = make_float2(-scale, -scale), nz2 = make_float2(-zero, -zero);
+    const float r_lo = rintf(__fsub_rn(ms_div(mn, k.scale, k.rc), k.zero));
+    const float r_hi = rintf(__fsub_rn(ms_div(mx, k.scale, k.rc), k.zero));
+    // one branch-free predicate (every comparison is false for NaN)
+    k.ok = !nan & (d >= 0x1p-100f) & (d <= 0x1p100f) & (k.scale >= 0x1p-100f) & (k.scale <= 0x1p100f) &
+           (fabsf(k.zero) <= 0x1p24f) & (r_lo >= LO) & (r_hi <= HI);
+    return k;
+}
+
+// idx = round(RN(RN(x/scale) - zero)) for a group that needs no clip: the
+// quotient by Markstein's step on fp32 pairs, the rounding by adding 1.5*2^23
+// (|value| <= 128 here), so each code sits in the low bits of the sum.
+template <int BITS>
+__device__ __forceinline__ void key_codes_fast(const uint32_t (&w)[16], const KeyParams &k, uint32_t (&out)[BITS])
+{
+    const float2 rc2 = make_float2(k.rc, k.rc), ns2 = make_float2(-k.scale, -k.scale), nz2 = make_float2(-k.zero, -k.zero);
     const float2 mg2 = make_float2(12582912.0f, 12582912.0f);
     uint32_t m[32];  // 0x4B400000 + code
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const float2 x = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
+    for (int i = 0; i < 16; ++i) {
+        const float2 x = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
         const float2 q0 = __fmul2_rn(x, rc2);
         const float2 q = __ffma2_rn(__ffma2_rn(ns2, q0, x), rc2, q0);
         const float2 c = __fadd2_rn(__fadd2_rn(q, nz2), mg2);
-        m[2 * k] = fbits(c.x);
-        m[2 * k + 1] = fbits(c.y);
+        m[2 * i] = fbits(c.x);
+        m[2 * i + 1] = fbits(c.y);
     }
     if constexpr (BITS == 8) {
         // low bytes are the codes in two's complement
@@ -237,31 +282,62 @@ __device__ __forceinline__ void key_group(const uint32_t (&w)[16], uint32_t (&ou
     } else {
         pack_magic<BITS>(m, out);
     }
-    sc = f32_to_f16_bits(scale);
-    zr = f32_to_f16_bits(zero);
 }
 
+// A lane's RPL key groups (rows r, r + ROWS, ...): parameters for all first,
+// then the element passes, so the groups' dependency chains interleave.
 template <int D, int BITS>
-__device__ __forceinline__ void encode_key_lane(const EncodeParams &p, uint32_t a, int64_t crow, int part)
+__device__ __forceinline__ void encode_key_lane(const EncodeParams &p, uint32_t buf, int r, int64_t crow, int part,
+                                                int nvalid)
 {
-    uint32_t w[16];
+    using G = EGeo<D, true>;
+    constexpr int R = G::RPL;
+    const uint32_t lo = 4 * (part & 1);  // first 16-byte chunk of this lane's 32 keys in the 64-column box
+    uint32_t base[R], xr[R];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint4 v = lds128(a + 16 * i);
-        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    for (int g = 0; g < R; ++g) base[g] = box_base<D, true>(p, buf, r + g * G::ROWS, part >> 1, xr[g]);
+    uint32_t w[R][16];
+#pragma unroll
+    for (int g = 0; g < R; ++g) {
+        if (g < nvalid) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = lds128(base[g] + 16 * ((lo + i) ^ xr[g]));
+                w[g][4 * i] = v.x; w[g][4 * i + 1] = v.y; w[g][4 * i + 2] = v.z; w[g][4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[g][i] = 0x3F803F80u;  // 1.0 pairs: a harmless stand-in
+        }
     }
-    uint32_t out[BITS];
-    uint16_t sc, zr;
-    key_group<BITS>(w, out, sc, zr);
+    KeyParams kp[R];
+    bool all = true;
+#pragma unroll
+    for (int g = 0; g < R; ++g) {
+        kp[g] = key_params<BITS>(w[g]);
+        all &= kp[g].ok | (g >= nvalid);
+    }
     constexpr int RB = D * BITS / 8, LB = 4 * BITS;
-    if constexpr (BITS == 8) {
-        st_global_v8(p.codes + crow * RB + part * LB, out[0], out[1], out[2], out[3], out[4], out[5], out[6], out[7]);
-    } else {
-        constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
-        store_words<BITS, A>(p.codes + crow * RB + part * LB, out);
+#pragma unroll
+    for (int g = 0; g < R; ++g) {
+        if (g >= nvalid) break;
+        const int64_t row = crow + g * G::ROWS;
+        if (!all && !kp[g].ok) {
+            key_group_exact<BITS>(base[g], lo, xr[g], p.codes + row * RB + part * LB, p.scale + row * (D / 32) + part,
+                                  p.zero + row * (D / 32) + part);
+            continue;
+        }
+        uint32_t out[BITS];
+        key_codes_fast<BITS>(w[g], kp[g], out);
+        if constexpr (BITS == 8) {
+            st_global_v8(p.codes + row * RB + part * LB, out[0], out[1], out[2], out[3], out[4], out[5], out[6], out[7]);
+        } else {
+            constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
+            store_words<BITS, A>(p.codes + row * RB + part * LB, out);
+        }
+        p.scale[row * (D / 32) + part] = f32_to_f16_bits(kp[g].scale);
+        p.zero[row * (D / 32) + part] = f32_to_f16_bits(kp[g].zero);
     }
-    p.scale[crow * (D / 32) + part] = sc;
-    p.zero[crow * (D / 32) + part] = zr;
 }
 
 // ------------------------------------------------------------------ values
@@ -295,15 +371,15 @@ __device__ __forceinline__ void put_code(uint32_t (&w)[BITS], int j, uint32_t c)
 // Value codes of a warp tile are written to a shared staging area (rows x
 // row bytes, the tile's own layout in the cache) and leave in one bulk store.
 template <int D, int BITS>
-__device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const float *sbnd, uint32_t a, uint32_t mtab,
-                                                  uint32_t stage, int64_t crow, int r, int part, bool valid)
+__device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const float *sbnd, uint32_t a, uint32_t xr,
+                                                  uint32_t mtab, uint32_t stage, int64_t crow, int r, int part, bool valid)
 {
     using G = EGeo<D, false>;
     float2 P[32];  // P[j] = (element j, element j + 32) of this lane's 64
     if (valid) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint4 u = lds128(a + 16 * i), v = lds128(a + 64 + 16 * i);
+            const uint4 u = lds128(a + 16 * (i ^ xr)), v = lds128(a + 16 * ((4 + i) ^ xr));
             const uint32_t uw[4] = {u.x, u.y, u.z, u.w}, vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -415,18 +491,22 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
 
 // ------------------------------------------------------------------ kernel
 template <int D, int BITS, bool KEY>
-__global__ void __launch_bounds__(kWarps * 32) encode_kernel(const __grid_constant__ EncodeParams p)
+__global__ void __launch_bounds__(kWarps * 32)
+    encode_kernel(const __grid_constant__ EncodeParams p, const __grid_constant__ CUtensorMap map)
 {
     using G = EGeo<D, KEY>;
     constexpr int SB = (!KEY && BITS > 3) ? 1024 : 0;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // tiles need 1024-byte alignment (swizzle atoms); the rest follows them
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // 2 per warp
-    float *sbnd = reinterpret_cast<float *>(smem + 16 * kWarps);
-    uint8_t *mtab = smem + 16 * kWarps + SB;
     constexpr int STG = KEY ? 0 : VStage<D, BITS>::BYTES;
+    uint8_t *tiles = smem;
+    uint8_t *rest = tiles + kWarps * 2 * G::TILE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rest);  // 2 per warp
+    float *sbnd = reinterpret_cast<float *>(rest + 16 * kWarps);
+    uint8_t *mtab = rest + 16 * kWarps + SB;
     uint8_t *stages = mtab + G::MTAB;  // value code staging, one per warp
-    uint8_t *tiles = stages + kWarps * STG;
     const uint32_t buf0 = smem_addr(tiles + warp * 2 * G::TILE), buf1 = buf0 + G::TILE;
     const uint32_t bar0 = smem_addr(&bars[2 * warp]), bar1 = bar0 + 8;
 
@@ -454,11 +534,11 @@ __global__ void __launch_bounds__(kWarps * 32) encode_kernel(const __grid_consta
     const uint32_t my_mtab = smem_addr(mtab) + part * 272;
     const uint32_t W = gridDim.x * kWarps;
     uint32_t item = blockIdx.x * kWarps + warp;
-    if (item < p.items) issue_tile<D, KEY>(p, item, buf0, bar0, lane);
+    if (item < p.items) issue_tile<D, KEY>(p, map, item, buf0, bar0, lane);
     for (uint32_t k = 0; item < p.items; item += W, ++k) {
         const uint32_t next = item + W;
         const uint32_t buf = (k & 1) ? buf1 : buf0, bar = (k & 1) ? bar1 : bar0;
-        if (next < p.items) issue_tile<D, KEY>(p, next, (k & 1) ? buf0 : buf1, (k & 1) ? bar0 : bar1, lane);
+        if (next < p.items) issue_tile<D, KEY>(p, map, next, (k & 1) ? buf0 : buf1, (k & 1) ? bar0 : bar1, lane);
         if (!mbar_wait_bounded(bar, (k >> 1) & 1, p.err)) {
             // give the other copy a bounded chance to land before leaving
             if (next < p.items) mbar_wait_bounded((k & 1) ? bar0 : bar1, ((k + 1) >> 1) & 1, p.err);
@@ -466,12 +546,13 @@ __global__ void __launch_bounds__(kWarps * 32) encode_kernel(const __grid_consta
             return;
         }
         const uint32_t bh = fast_div(item, p.div_tiles);
-        const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::ROWS;
+        const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::TROWS;
         const bool valid = t_first + r < p.n;
         const int64_t crow = (int64_t)bh * p.cap + p.t0 + t_first + r;
-        const uint32_t a = buf + r * G::RS + part * (G::E * 2);
         if constexpr (KEY) {
-            if (valid) encode_key_lane<D, BITS>(p, a, crow, part);
+            // rows r, r + ROWS, ... of the tile that exist
+            const int nvalid = (int)imin64(G::RPL, (p.n - t_first - r + G::ROWS - 1) / G::ROWS);
+            if (valid) encode_key_lane<D, BITS>(p, buf, r, crow, part, nvalid);
         } else {
             constexpr int RB = VStage<D, BITS>::RB;
             const uint32_t stage = smem_addr(stages + warp * STG);
@@ -479,10 +560,12 @@ __global__ void __launch_bounds__(kWarps * 32) encode_kernel(const __grid_consta
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
             // every lane of a row joins the cross-lane stages, so no early exit
-            encode_value_lane<D, BITS>(p, sbnd, a, my_mtab, stage, crow, r, part, valid);
+            uint32_t xr;
+            const uint32_t a = box_base<D, false>(p, buf, r, part, xr);
+            encode_value_lane<D, BITS>(p, sbnd, a, xr, my_mtab, stage, crow, r, part, valid);
             fence_proxy_async_smem();
             __syncwarp();
-            const int rows = (int)imin64(G::ROWS, p.n - t_first);
+            const int rows = (int)imin64(G::TROWS, p.n - t_first);
             uint8_t *dst = p.codes + (crow - r) * RB;
             if (((uintptr_t)dst & 15) == 0 && (rows * RB) % 16 == 0) {
                 if (lane == 0) {
@@ -502,11 +585,11 @@ __global__ void __launch_bounds__(kWarps * 32) encode_kernel(const __grid_consta
 }
 
 template <int D, int BITS, bool KEY>
-cudaError_t run(const EncodeParams &p, cudaStream_t s)
+cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
 {
     using G = EGeo<D, KEY>;
-    const size_t smem = 16 * kWarps + ((!KEY && BITS > 3) ? 1024 : 0) + G::MTAB +
-                        (size_t)kWarps * (KEY ? 0 : VStage<D, BITS>::BYTES) + (size_t)kWarps * 2 * G::TILE;
+    const size_t smem = 1024 /*alignment slack*/ + (size_t)kWarps * 2 * G::TILE + 16 * kWarps +
+                        ((!KEY && BITS > 3) ? 1024 : 0) + G::MTAB + (size_t)kWarps * (KEY ? 0 : VStage<D, BITS>::BYTES);
     auto kern = encode_kernel<D, BITS, KEY>;
     static int per_sm = 0;  // same on every GB300; only a successful query is kept
     if (!per_sm) {
@@ -519,33 +602,50 @@ cudaError_t run(const EncodeParams &p, cudaStream_t s)
     }
     const int64_t want = ((int64_t)p.items + kWarps - 1) / kWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
-    kern<<<grid, kWarps * 32, smem, s>>>(p);
+    kern<<<grid, kWarps * 32, smem, s>>>(p, map);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t dispatch_key(int kb, const EncodeParams &p, cudaStream_t s)
+cudaError_t dispatch_key(int kb, const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
 {
     switch (kb) {
-    case 2: return run<D, 2, true>(p, s);
-    case 4: return run<D, 4, true>(p, s);
-    case 5: return run<D, 5, true>(p, s);
-    case 8: return run<D, 8, true>(p, s);
+    case 2: return run<D, 2, true>(p, map, s);
+    case 4: return run<D, 4, true>(p, map, s);
+    case 5: return run<D, 5, true>(p, map, s);
+    case 8: return run<D, 8, true>(p, map, s);
     }
     return cudaErrorInvalidValue;
 }
 
 template <int D>
-cudaError_t dispatch_value(int vb, const EncodeParams &p, cudaStream_t s)
+cudaError_t dispatch_value(int vb, const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
 {
     switch (vb) {
-    case 2: return run<D, 2, false>(p, s);
-    case 3: return run<D, 3, false>(p, s);
-    case 4: return run<D, 4, false>(p, s);
-    case 5: return run<D, 5, false>(p, s);
-    case 8: return run<D, 8, false>(p, s);
+    case 2: return run<D, 2, false>(p, map, s);
+    case 3: return run<D, 3, false>(p, map, s);
+    case 4: return run<D, 4, false>(p, map, s);
+    case 5: return run<D, 5, false>(p, map, s);
+    case 8: return run<D, 8, false>(p, map, s);
     }
     return cudaErrorInvalidValue;
+}
+
+// Tensor map over the [B][H][n][D] bf16 input (any strides the API accepts):
+// boxes of 64 columns x rows, 128-byte swizzle.  False if the driver refuses
+// it (the kernels then copy row by row).
+inline bool input_map(CUtensorMap *map, const uint16_t *src, int D, int64_t n, int H, int B, const int64_t st[3],
+                      int rows)
+{
+    auto fn = tensor_map_encoder();
+    if (!fn || n >= (int64_t(1) << 31)) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)n, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(src), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Tiles of `rows` token rows per (sequence, kv-head); false if the count
@@ -575,14 +675,16 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     const Tables &tab = codebook_tables(c.vb);
     for (int i = 0; i < (1 << c.vb) - 1; ++i) p.bnd[i] = tab.boundaries[i];
 
+    CUtensorMap map{};
     p.src = k;
     p.sb = ks[0]; p.sh = ks[1]; p.st = ks[2];
     p.codes = c.k_codes;
     p.scale = c.k_scale;
     p.zero = c.k_zero;
     p.div_h = make_fastdiv((uint32_t)c.H);
-    if (!set_items(p, n, EGeo<D, true>::ROWS, c)) return cudaErrorInvalidValue;
-    cudaError_t e = dispatch_key<D>(c.kb, p, s);
+    if (!set_items(p, n, EGeo<D, true>::TROWS, c)) return cudaErrorInvalidValue;
+    p.use_tma = input_map(&map, k, D, n, c.H, c.B, ks, EGeo<D, true>::TROWS) ? 1 : 0;
+    cudaError_t e = dispatch_key<D>(c.kb, p, map, s);
     if (e != cudaSuccess) return e;
 
     p.src = v;
@@ -590,8 +692,9 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     p.codes = c.v_codes;
     p.scale = c.v_scale;
     p.zero = nullptr;
-    if (!set_items(p, n, EGeo<D, false>::ROWS, c)) return cudaErrorInvalidValue;
-    return dispatch_value<D>(c.vb, p, s);
+    if (!set_items(p, n, EGeo<D, false>::TROWS, c)) return cudaErrorInvalidValue;
+    p.use_tma = input_map(&map, v, D, n, c.H, c.B, vs, EGeo<D, false>::TROWS) ? 1 : 0;
+    return dispatch_value<D>(c.vb, p, map, s);
 }
 
 }  // namespace

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 namespace tq {
@@ -25,6 +26,9 @@ const Tables &codebook_tables(int vb);
 float inv_sqrt_head_dim(int d);  // fl(1/sqrt(d)) rounded from binary64
 
 uint32_t *device_error_word();  // per current device; nullptr on failure
+
+// cuTensorMapEncodeTiled from the driver, or nullptr when unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_encode(const CacheView &c, const uint16_t *k, const int64_t ks[3], const uint16_t *v,
                           const int64_t vs[3], int64_t t0, int64_t n, cudaStream_t s);

@@ -107,6 +107,25 @@ def test_strided_inputs(cuda):
     _assert_planes_match(planes_from_device(cache), ref, 0, T, oracle.bf16_bits_to_f32(v), sentinel=False)
 
 
+def test_broadcast_strides(cuda):
+    """K/V expanded over the kv-heads (head stride 0) and over the batch (batch stride 0)."""
+    B, H, T, d = 3, 4, 37, 128
+    w = tq_synth.WORKLOADS["prefill"]
+    k, v = _inputs(w, 1, 1, T, d)
+    kb = np.broadcast_to(k, (B, H, T, d))
+    vb = np.broadcast_to(v, (B, H, T, d))
+    kt = to_device_bf16(np.ascontiguousarray(k)).expand(B, H, T, d)
+    vt = to_device_bf16(np.ascontiguousarray(v)).expand(B, H, T, d)
+    assert kt.stride()[:2] == (0, 0)
+    cache = cuda.Cache(B, H, d, 48)
+    cuda.tq_encode_append(cache, kt, vt, 5)
+    torch.cuda.synchronize()
+    ref = oracle.Planes(B, H, d, 8, 3, cache.capacity)
+    oracle.encode(ref, np.ascontiguousarray(kb), np.ascontiguousarray(vb), t0=5)
+    _assert_planes_match(planes_from_device(cache), ref, 5, T, oracle.bf16_bits_to_f32(np.ascontiguousarray(vb)),
+                         sentinel=False)
+
+
 def test_single_token_appends(cuda):
     """Decode-step appends: n = 1 at successive t0, like updateAndFetch per token."""
     B, H, d, T0, steps = 3, 2, 128, 20, 6
