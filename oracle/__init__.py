@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
     so.tqo_key_group_dequant.argtypes = [_P, ctypes.c_uint16, ctypes.c_uint16, _P]
     so.tqo_value_row.argtypes = [_P, _I, _P, _I, _P, _P, _P, _P]
     so.tqo_value_row_dequant.argtypes = [_P, _P, _I, _P, _P, _P]
+    so.tqo_value_row_rotated.argtypes = [_P, _P, _I, _P, _P]
+    so.tqo_unrotate.argtypes = [_P, _I, _P, _P]
+    so.tqo_decode_rotated.argtypes = [_I, _I, _I, _I, _L, _L, _L, _P, _P, _P, _P]
     so.tqo_bytes_per_token_head.restype = _L
     so.tqo_bytes_per_token_head.argtypes = [_I, _I, _I]
     so.tqo_encode.argtypes = [_I, _I, _I, _I, _I, _L, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P]
@@ -215,6 +218,28 @@ def value_row_dequant(idx, scale_bits, bits: int, signs=None, centroids=None) ->
     return out
 
 
+def value_row_rotated(idx, scale_bits, bits: int, centroids=None) -> np.ndarray:
+    """centroid[idx] * rms: a value row before the inverse transform (deferred fetch)."""
+    i = np.ascontiguousarray(idx, dtype=np.int32)
+    sc = np.ascontiguousarray(scale_bits, dtype=np.uint16)
+    c = codebook(bits)[0] if centroids is None else np.ascontiguousarray(centroids, dtype=np.float32)
+    out = np.zeros(i.size, dtype=np.float32)
+    lib().tqo_value_row_rotated(_ptr(i), _ptr(sc), i.size, _ptr(c), _ptr(out))
+    return out
+
+
+def unrotate(x, signs=None) -> np.ndarray:
+    """signs * FWHT(x)/sqrt(d) for each row of x ([..., d], fp32)."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    d = a.shape[-1]
+    s = sign_vector(d) if signs is None else np.ascontiguousarray(signs, dtype=np.int8)
+    rows = a.reshape(-1, d)
+    out = np.zeros_like(rows)
+    for r in range(rows.shape[0]):
+        lib().tqo_unrotate(_ptr(rows[r]), d, _ptr(s), _ptr(out[r]))
+    return out.reshape(a.shape)
+
+
 def bytes_per_token_head(d: int, kb: int, vb: int) -> int:
     return int(lib().tqo_bytes_per_token_head(d, kb, vb))
 
@@ -263,6 +288,29 @@ def decode(planes: Planes, t0: int, n: int, want_k: bool = True, want_v: bool = 
     if rc != 0:
         raise ValueError("oracle decode: bad arguments")
     return ko, vo
+
+
+def decode_rotated(planes: Planes, t0: int, n: int) -> np.ndarray:
+    """Value rows [t0, t0+n) in the rotated domain, fp32 [B][H][n][d]."""
+    p = planes
+    vo = np.zeros((p.B, p.H, n, p.d), dtype=np.float32)
+    rc = lib().tqo_decode_rotated(p.B, p.H, p.d, p.vb, p.cap, t0, n, _ptr(p.v_codes), _ptr(p.v_scale),
+                                  _ptr(codebook(p.vb)[0]), _ptr(vo))
+    if rc != 0:
+        raise ValueError("oracle decode_rotated: bad arguments")
+    return vo
+
+
+def copy_rows(dst: Planes, dst_t0: int, src: Planes, src_t0: int, n: int) -> None:
+    """Token rows of every plane, byte for byte (token slices are byte-safe:
+    quantisation groups run along head_dim only)."""
+    for a, b in zip(dst.arrays(), src.arrays()):
+        a[:, :, dst_t0:dst_t0 + n] = b[:, :, src_t0:src_t0 + n]
+
+
+def clear_rows(planes: Planes, t0: int, n: int) -> None:
+    for a in planes.arrays():
+        a[:, :, t0:t0 + n] = 0
 
 
 def attention(planes: Planes, q_bf16: np.ndarray, seq_len: int, softmax_scale: float | None = None,

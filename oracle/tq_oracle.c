@@ -446,6 +446,26 @@ void tqo_value_row_dequant(const int32_t *idx, const uint16_t *scale_h, int d, c
     for (int j = 0; j < d; ++j) out[j] = y[j] * (float)signs[j];
 }
 
+/* Deferred fetch (page section "Deferred inverse FWHT": attention is linear in
+ * V, so the weighted sum can be formed in the rotated domain and brought back
+ * once per output row): the value row before the inverse transform,
+ * centroid[idx] * rms -- the first step of tqo_value_row_dequant. */
+void tqo_value_row_rotated(const int32_t *idx, const uint16_t *scale_h, int d, const float *centroids, float *out)
+{
+    for (int j = 0; j < d; ++j) out[j] = centroids[idx[j]] * tqo_f16_to_f32(scale_h[j / 32]);
+}
+
+/* The page's unrotateValues: a vector formed in the rotated domain back to
+ * the model's basis, signs * FWHT(x)/sqrt(d) -- the second half of
+ * tqo_value_row_dequant, in the same order. */
+void tqo_unrotate(const float *x, int d, const int8_t *signs, float *out)
+{
+    float y[512];
+    for (int j = 0; j < d; ++j) y[j] = x[j];
+    tqo_fwht(y, d);
+    for (int j = 0; j < d; ++j) out[j] = y[j] * (float)signs[j];
+}
+
 /* ------------------------------------------------------------------------ */
 /* Whole-cache operations on the plane layout                                 */
 /* ------------------------------------------------------------------------ */
@@ -526,6 +546,28 @@ int tqo_decode(int B, int H, int d, int kb, int vb, int64_t cap, int64_t t0, int
                     for (int j = 0; j < d; ++j) idx[j] = (int32_t)u[j];
                     tqo_value_row_dequant(idx, &v_scale[row * g], d, signs, centroids, v_out + dst);
                 }
+            }
+    return TQO_OK;
+}
+
+/* Rows [t0, t0+n) of the value planes in the rotated domain (fp32). */
+int tqo_decode_rotated(int B, int H, int d, int vb, int64_t cap, int64_t t0, int64_t n, const uint8_t *v_codes,
+                       const uint16_t *v_scale, const float *centroids, float *v_out)
+{
+    if (!valid_dims(d, 8, vb) || t0 < 0 || n < 0 || t0 + n > cap) return TQO_BAD_ARG;
+    const int g = d / 32;
+    const int64_t vr = (int64_t)d * vb / 8;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int64_t t = 0; t < n; ++t) {
+                const int64_t dst = (((int64_t)b * H + h) * n + t) * d;
+                const int64_t row = ((int64_t)b * H + h) * cap + t0 + t;
+                int32_t idx[512];
+                uint32_t u[512];
+                tqo_unpack_bits(v_codes + row * vr, d, vb, u);
+                for (int j = 0; j < d; ++j) idx[j] = (int32_t)u[j];
+                tqo_value_row_rotated(idx, &v_scale[row * g], d, centroids, v_out + dst);
             }
     return TQO_OK;
 }

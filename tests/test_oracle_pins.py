@@ -405,3 +405,87 @@ def test_attention_deferred_unrotation_equals_eager():
         eager += w[t] * oracle.value_row_dequant(idx, sc, 3)
     deferred = signs * oracle.fwht(np.sum([w[t] * rot[t] for t in range(T)], axis=0).astype(np.float32))
     assert np.max(np.abs(deferred - eager)) < 1e-5
+
+
+# ---------------------------------------------------------------- deferred fetch (page: "Deferred inverse FWHT")
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_unrotate_basis_vectors_closed_form(d):
+    """unrotate(e_k)_j = s_j * (-1)^popcount(j & k) * fl(1/sqrt d): the Sylvester
+    index convention, the normalisation and signs applied last, exactly."""
+    s = oracle.sign_vector(d).astype(np.float32)
+    c = np.float32(1.0 / math.sqrt(d))
+    for k in (0, 1, 5, d // 2, d - 1):
+        e = np.zeros(d, dtype=np.float32)
+        e[k] = 1.0
+        want = np.array([s[j] * (-1.0 if bin(j & k).count("1") % 2 else 1.0) for j in range(d)], dtype=np.float32) * c
+        assert np.array_equal(oracle.unrotate(e), want)
+
+
+@pytest.mark.parametrize("d", [64, 128, 512])
+def test_unrotate_inverts_the_encoder_rotation(d):
+    """The encoder rotates y = FWHT(x * s)/sqrt(d); H H = d I and s * s = 1, so
+    unrotate(y) = x up to fp32 rounding."""
+    rng = np.random.default_rng(d)
+    x = rng.standard_normal(d).astype(np.float32)
+    y = oracle.fwht(x * oracle.sign_vector(d).astype(np.float32))
+    back = oracle.unrotate(y)
+    assert np.max(np.abs(back - x)) < 2e-6 * np.max(np.abs(x)) * math.log2(d)
+    assert abs(np.linalg.norm(back) - np.linalg.norm(x)) < 1e-5 * np.linalg.norm(x)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_rotated_row_then_unrotate_is_the_dequantised_row(bits):
+    """Deferred and eager paths split the same formula: centroid[idx]*rms, then
+    signs * FWHT(.)/sqrt(d) -- identical arithmetic for a single row."""
+    rng = np.random.default_rng(bits)
+    d = 128
+    idx = rng.integers(0, 1 << bits, d)
+    sc = oracle.f32_to_f16_bits(rng.uniform(0.1, 3.0, d // 32).astype(np.float32))
+    rot = oracle.value_row_rotated(idx, sc, bits)
+    c = oracle.codebook(bits)[0]
+    assert np.array_equal(rot, (c[idx] * np.repeat(oracle.f16_bits_to_f32(sc), 32)).astype(np.float32))
+    assert np.array_equal(oracle.unrotate(rot), oracle.value_row_dequant(idx, sc, bits))
+
+
+def test_deferred_weighted_sum_equals_eager():
+    """The page's identity InvFWHT(sum w_i v_i) = sum w_i InvFWHT(v_i), in fp32."""
+    rng = np.random.default_rng(7)
+    d, n = 128, 50
+    idx = rng.integers(0, 8, (n, d))
+    sc = oracle.f32_to_f16_bits(rng.uniform(0.1, 3.0, (n, d // 32)).astype(np.float32))
+    w = rng.dirichlet(np.ones(n))
+    rot = np.stack([oracle.value_row_rotated(idx[i], sc[i], 3) for i in range(n)]).astype(np.float64)
+    eager = np.stack([oracle.value_row_dequant(idx[i], sc[i], 3) for i in range(n)]).astype(np.float64)
+    deferred = oracle.unrotate((w @ rot).astype(np.float32))
+    assert np.max(np.abs(deferred - w @ eager)) < 1e-5 * np.max(np.abs(w @ eager))
+
+
+# ---------------------------------------------------------------- cache lifecycle (token slices are byte-safe)
+def test_copy_rows_then_decode_equals_source_rows():
+    rng = np.random.default_rng(11)
+    B, H, d, T = 2, 2, 64, 20
+    k = oracle.f32_to_bf16_bits(rng.standard_normal((B, H, T, d)).astype(np.float32)).reshape(B, H, T, d)
+    v = oracle.f32_to_bf16_bits(rng.standard_normal((B, H, T, d)).astype(np.float32)).reshape(B, H, T, d)
+    src = oracle.Planes(B, H, d, 4, 3, 32)
+    oracle.encode(src, k, v)
+    dst = oracle.Planes(B, H, d, 4, 3, 48)  # larger capacity: growth
+    oracle.copy_rows(dst, 7, src, 3, 12)
+    for a, b in zip(oracle.decode(dst, 7, 12), oracle.decode(src, 3, 12)):
+        assert np.array_equal(a, b)
+    assert all(np.all(a[:, :, :7] == 0) and np.all(a[:, :, 19:] == 0) for a in dst.arrays())
+
+
+def test_trim_then_reappend_equals_encoding_the_kept_and_new_tokens():
+    rng = np.random.default_rng(12)
+    B, H, d = 1, 3, 128
+    k = oracle.f32_to_bf16_bits(rng.standard_normal((B, H, 30, d)).astype(np.float32)).reshape(B, H, 30, d)
+    v = oracle.f32_to_bf16_bits(rng.standard_normal((B, H, 30, d)).astype(np.float32)).reshape(B, H, 30, d)
+    cache = oracle.Planes(B, H, d, 8, 3, 32)
+    oracle.encode(cache, k[:, :, :20], v[:, :, :20])
+    oracle.clear_rows(cache, 12, 20)            # trim to 12 tokens
+    oracle.encode(cache, k[:, :, 20:30], v[:, :, 20:30], t0=12)
+    fresh = oracle.Planes(B, H, d, 8, 3, 32)
+    keep = np.concatenate([k[:, :, :12], k[:, :, 20:30]], axis=2), np.concatenate([v[:, :, :12], v[:, :, 20:30]], axis=2)
+    oracle.encode(fresh, *keep)
+    for a, b in zip(cache.arrays(), fresh.arrays()):
+        assert np.array_equal(a, b)
