@@ -142,6 +142,51 @@ TQ_API tq_status tq_encode_append(const tq_cache *cache, const void *k, const in
 TQ_API tq_status tq_decode(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype, void *k_out,
                     void *v_out, tq_stream_t stream);
 
+/*
+ * Deferred fetch: value rows [t0, t0 + n) still in the rotated domain,
+ * centroid[code] * rms per element with no inverse transform and no signs,
+ * [batch][H][n][d] contiguous, fp32 or bf16 (round to nearest even of the fp32
+ * product).  Page section "Deferred inverse FWHT": attention is linear in the
+ * values, so an attention kernel outside this library can form its weighted
+ * sum on these rows and bring the result back once per query row with
+ * tq_unrotate.  v_out 16-byte aligned.
+ */
+TQ_API tq_status tq_decode_values_rotated(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype,
+                                          void *v_out, tq_stream_t stream);
+
+/*
+ * Un-rotation of vectors formed in the rotated domain: out = signs *
+ * FWHT(x) / sqrt(d) for each of `rows` rows of head_dim elements (the second
+ * half of the value dequantisation; page section "Deferred inverse FWHT").
+ *  x, out    device, [rows][head_dim] contiguous, fp32 or bf16 each
+ *            (in_dtype, out_dtype); 16-byte aligned; out may equal x when the
+ *            dtypes match (in place).
+ * rows = 0 is a no-op.
+ */
+TQ_API tq_status tq_unrotate(int32_t head_dim, tq_dtype in_dtype, const void *x, int64_t rows, tq_dtype out_dtype,
+                             void *out, tq_stream_t stream);
+
+/*
+ * Cache lifecycle: copy token rows [src_t0, src_t0 + n) of every (sequence,
+ * kv-head) of `src` into rows [dst_t0, dst_t0 + n) of `dst`, all five planes,
+ * byte for byte.  Groups run along head_dim only, so token slices are
+ * byte-safe (page section "Architecture in mlx-bun"); with it the caller
+ * snapshots, restores and clones caches and grows capacity (copy into a
+ * larger cache).  The two caches must agree in head_dim, bit widths, kv-heads
+ * and batch; capacities may differ.  Within one cache the ranges must not
+ * overlap unless identical (then nothing moves).  n = 0 is a no-op.
+ */
+TQ_API tq_status tq_cache_copy_rows(const tq_cache *dst, int64_t dst_t0, const tq_cache *src, int64_t src_t0,
+                                    int64_t n, tq_stream_t stream);
+
+/*
+ * Cache lifecycle: zero token rows [t0, t0 + n) of every (sequence, kv-head),
+ * all planes.  Trimming a cache to length L is clearing [L, capacity): rows
+ * appended there afterwards give the same bytes as in a cache that never held
+ * the trimmed tokens.  n = 0 is a no-op.
+ */
+TQ_API tq_status tq_cache_clear_rows(const tq_cache *cache, int64_t t0, int64_t n, tq_stream_t stream);
+
 /* Workspace bytes tq_decode_attention needs for these sizes (0 if invalid). */
 TQ_API size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_heads, int64_t seq_len);
 

@@ -294,8 +294,9 @@ def decode_rotated(planes: Planes, t0: int, n: int) -> np.ndarray:
     """Value rows [t0, t0+n) in the rotated domain, fp32 [B][H][n][d]."""
     p = planes
     vo = np.zeros((p.B, p.H, n, p.d), dtype=np.float32)
-    rc = lib().tqo_decode_rotated(p.B, p.H, p.d, p.vb, p.cap, t0, n, _ptr(p.v_codes), _ptr(p.v_scale),
-                                  _ptr(codebook(p.vb)[0]), _ptr(vo))
+    cen = codebook(p.vb)[0]  # held for the duration of the call
+    rc = lib().tqo_decode_rotated(p.B, p.H, p.d, p.vb, p.cap, t0, n, _ptr(p.v_codes), _ptr(p.v_scale), _ptr(cen),
+                                  _ptr(vo))
     if rc != 0:
         raise ValueError("oracle decode_rotated: bad arguments")
     return vo

@@ -23,6 +23,7 @@ __all__ = [
     "Cache", "TQError", "lib", "tq_bytes_per_token_head", "tq_sign_vector", "tq_codebook",
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
     "tq_attention_supported", "tq_device_error", "tq_plane_bytes", "tq_decode_attention_noalloc",
+    "tq_decode_values_rotated", "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows",
 ]
 
 HEAD_DIMS = (64, 128, 256, 512)
@@ -33,7 +34,8 @@ TQ_BF16, TQ_F32 = 0, 1
 EXPORTS = (
     "tq_status_string", "tq_bytes_per_token_head", "tq_plane_bytes", "tq_sign_vector", "tq_codebook",
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
-    "tq_attention_supported", "tq_device_error", "tq_decode_attention_noalloc",
+    "tq_attention_supported", "tq_device_error", "tq_decode_attention_noalloc", "tq_decode_values_rotated",
+    "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows",
 )
 
 
@@ -82,6 +84,10 @@ def lib() -> ctypes.CDLL:
     so.tq_attention_supported.argtypes = [_I32, _I32, _I32, _I32]
     so.tq_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     so.tq_decode_attention_noalloc.argtypes = [_CP, _P, _I32, _I64, ctypes.c_float, _P, _P]
+    so.tq_decode_values_rotated.argtypes = [_CP, _I64, _I64, ctypes.c_int, _P, _P]
+    so.tq_unrotate.argtypes = [_I32, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P]
+    so.tq_cache_copy_rows.argtypes = [_CP, _I64, _CP, _I64, _I64, _P]
+    so.tq_cache_clear_rows.argtypes = [_CP, _I64, _I64, _P]
     for name in EXPORTS:
         if name not in ("tq_status_string", "tq_bytes_per_token_head", "tq_attention_workspace_bytes",
                         "tq_attention_supported"):
@@ -219,6 +225,55 @@ def tq_decode(cache: Cache, t0: int, n: int, dtype=torch.bfloat16, want_k: bool 
                            k_out.data_ptr() if want_k else None, v_out.data_ptr() if want_v else None,
                            _stream(stream)), "tq_decode")
     return (k_out if want_k else None), (v_out if want_v else None)
+
+
+def _dtype_code(dtype) -> int:
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("dtype must be bfloat16 or float32")
+    return TQ_F32 if dtype == torch.float32 else TQ_BF16
+
+
+def tq_decode_values_rotated(cache: Cache, t0: int, n: int, dtype=torch.float32, out: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """Value rows [t0, t0+n) in the rotated domain (centroid[code] * rms) as [B][H][n][d]."""
+    shape = (cache.batch, cache.num_kv_heads, int(n), cache.head_dim)
+    if out is None:
+        out = torch.empty(shape, dtype=dtype, device=cache.k_codes.device)
+    if out.dtype != dtype or tuple(out.shape) != shape or not out.is_contiguous():
+        raise ValueError("output must be contiguous [B][H][n][d] of the requested dtype")
+    s = cache.struct()
+    _check(lib().tq_decode_values_rotated(ctypes.byref(s), int(t0), int(n), _dtype_code(dtype), out.data_ptr(),
+                                          _stream(stream)), "tq_decode_values_rotated")
+    return out
+
+
+def tq_unrotate(x: torch.Tensor, out: torch.Tensor | None = None, dtype=None, stream=None) -> torch.Tensor:
+    """signs * FWHT(x)/sqrt(d) for every row of x ([..., d] contiguous, fp32 or bf16)."""
+    _require_cuda(x)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    dtype = x.dtype if dtype is None else dtype
+    if out is None:
+        out = torch.empty(x.shape, dtype=dtype, device=x.device)
+    if out.dtype != dtype or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be contiguous, shaped like x, of the requested dtype")
+    d = x.shape[-1]
+    _check(lib().tq_unrotate(int(d), _dtype_code(x.dtype), x.data_ptr(), int(x.numel() // d), _dtype_code(dtype),
+                             out.data_ptr(), _stream(stream)), "tq_unrotate")
+    return out
+
+
+def tq_cache_copy_rows(dst: Cache, dst_t0: int, src: Cache, src_t0: int, n: int, stream=None) -> None:
+    """Token rows [src_t0, src_t0+n) of every (sequence, kv-head) of src -> rows [dst_t0, ...) of dst, byte for byte."""
+    a, b = dst.struct(), src.struct()
+    _check(lib().tq_cache_copy_rows(ctypes.byref(a), int(dst_t0), ctypes.byref(b), int(src_t0), int(n),
+                                    _stream(stream)), "tq_cache_copy_rows")
+
+
+def tq_cache_clear_rows(cache: Cache, t0: int, n: int, stream=None) -> None:
+    """Zero token rows [t0, t0+n) of every (sequence, kv-head), all planes (trim)."""
+    s = cache.struct()
+    _check(lib().tq_cache_clear_rows(ctypes.byref(s), int(t0), int(n), _stream(stream)), "tq_cache_clear_rows")
 
 
 def tq_attention_workspace_bytes(cache: Cache, q_heads: int, seq_len: int) -> int:

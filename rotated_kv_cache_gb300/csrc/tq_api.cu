@@ -181,6 +181,63 @@ tq_status tq_decode(const tq_cache *c, int64_t t0, int64_t n, tq_dtype dt, void 
     return cuda_status(tq::launch_decode(view(c), t0, n, dt == TQ_F32, k_out, v_out, (cudaStream_t)stream));
 }
 
+tq_status tq_decode_values_rotated(const tq_cache *c, int64_t t0, int64_t n, tq_dtype dt, void *v_out,
+                                   tq_stream_t stream)
+{
+    tq_status st = check_cache(c);
+    if (st != TQ_OK) return st;
+    if (t0 < 0 || n < 0) return TQ_ERR_SHAPE;
+    if (t0 + n > c->capacity) return TQ_ERR_CAPACITY;
+    if (dt != TQ_BF16 && dt != TQ_F32) return TQ_ERR_SHAPE;
+    if (n == 0) return TQ_OK;
+    if (!v_out) return TQ_ERR_NULL;
+    if (!aligned16(v_out)) return TQ_ERR_ALIGN;
+    return cuda_status(tq::launch_decode_rotated(view(c), t0, n, dt == TQ_F32, v_out, (cudaStream_t)stream));
+}
+
+tq_status tq_unrotate(int32_t d, tq_dtype in_dt, const void *x, int64_t rows, tq_dtype out_dt, void *out,
+                      tq_stream_t stream)
+{
+    if (!valid_head_dim(d)) return TQ_ERR_HEAD_DIM;
+    if ((in_dt != TQ_BF16 && in_dt != TQ_F32) || (out_dt != TQ_BF16 && out_dt != TQ_F32) || rows < 0) return TQ_ERR_SHAPE;
+    if (rows == 0) return TQ_OK;
+    if (!x || !out) return TQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(out)) return TQ_ERR_ALIGN;
+    if (x == out && in_dt != out_dt) return TQ_ERR_SHAPE;  // in place only with equal element sizes
+    return cuda_status(tq::launch_unrotate(d, in_dt == TQ_F32, x, rows, out_dt == TQ_F32, out, (cudaStream_t)stream));
+}
+
+tq_status tq_cache_copy_rows(const tq_cache *dst, int64_t dst_t0, const tq_cache *src, int64_t src_t0, int64_t n,
+                             tq_stream_t stream)
+{
+    tq_status st = check_cache(dst);
+    if (st != TQ_OK) return st;
+    st = check_cache(src);
+    if (st != TQ_OK) return st;
+    if (dst->head_dim != src->head_dim || dst->k_bits != src->k_bits || dst->v_bits != src->v_bits ||
+        dst->num_kv_heads != src->num_kv_heads || dst->batch != src->batch)
+        return TQ_ERR_SHAPE;
+    if (dst_t0 < 0 || src_t0 < 0 || n < 0) return TQ_ERR_SHAPE;
+    if (dst_t0 + n > dst->capacity || src_t0 + n > src->capacity) return TQ_ERR_CAPACITY;
+    if (n == 0) return TQ_OK;
+    if (dst->k_codes == src->k_codes) {  // the same cache
+        if (dst_t0 == src_t0) return TQ_OK;
+        if (dst_t0 < src_t0 + n && src_t0 < dst_t0 + n) return TQ_ERR_SHAPE;
+    }
+    const tq::CacheView sv = view(src);
+    return cuda_status(tq::launch_copy_rows(view(dst), dst_t0, &sv, src_t0, n, (cudaStream_t)stream));
+}
+
+tq_status tq_cache_clear_rows(const tq_cache *c, int64_t t0, int64_t n, tq_stream_t stream)
+{
+    tq_status st = check_cache(c);
+    if (st != TQ_OK) return st;
+    if (t0 < 0 || n < 0) return TQ_ERR_SHAPE;
+    if (t0 + n > c->capacity) return TQ_ERR_CAPACITY;
+    if (n == 0) return TQ_OK;
+    return cuda_status(tq::launch_copy_rows(view(c), t0, nullptr, 0, n, (cudaStream_t)stream));
+}
+
 int tq_attention_supported(int32_t d, int32_t kb, int32_t vb, int32_t group)
 {
     return tq::attention_supported(d, kb, vb, group) ? 1 : 0;

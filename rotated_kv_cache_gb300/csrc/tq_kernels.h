@@ -44,6 +44,12 @@ TQ_DECLARE_PER_D(256)
 TQ_DECLARE_PER_D(512)
 #undef TQ_DECLARE_PER_D
 
+// Deferred fetch, un-rotation and cache row copy / clear (src null: zeros).
+cudaError_t launch_decode_rotated(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out, cudaStream_t s);
+cudaError_t launch_unrotate(int d, bool in_f32, const void *x, int64_t rows, bool out_f32, void *out, cudaStream_t s);
+cudaError_t launch_copy_rows(const CacheView &dst, int64_t dst_t0, const CacheView *src, int64_t src_t0, int64_t n,
+                             cudaStream_t s);
+
 cudaError_t launch_decode(const CacheView &c, int64_t t0, int64_t n, bool f32, void *k_out, void *v_out,
                           cudaStream_t s);
 

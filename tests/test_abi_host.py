@@ -105,3 +105,38 @@ def test_refusals_before_launch(tqlib):
     assert L.tq_attention_workspace_bytes(ctypes.byref(s), 3, 8) == 0
     for st in range(11):
         assert L.tq_status_string(st)
+
+
+def test_lifecycle_and_deferred_refusals(tqlib):
+    """Argument checks of the deferred fetch, un-rotation and row copy/clear
+    return before any launch (fake, never-read pointers)."""
+    S = {name: i for i, name in enumerate(
+        ["TQ_OK", "TQ_ERR_NULL", "TQ_ERR_HEAD_DIM", "TQ_ERR_BITS", "TQ_ERR_SHAPE", "TQ_ERR_CAPACITY",
+         "TQ_ERR_ALIGN", "TQ_ERR_WORKSPACE", "TQ_ERR_CUDA", "TQ_ERR_UNSUPPORTED"])}
+    L = tqlib.lib()
+    a, b = _struct(tqlib), _struct(tqlib)
+    c = _struct(tqlib, k_codes=0x11000, k_scale=0x12000, k_zero=0x13000, v_codes=0x14000, v_scale=0x15000)
+    assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 40, 1, 0x10000, None) == S["TQ_ERR_CAPACITY"]
+    assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 5, 0x10000, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 1, None, None) == S["TQ_ERR_NULL"]
+    assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 1, 0x10008, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 0, 1, None, None) == S["TQ_OK"]
+    assert L.tq_unrotate(96, 1, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_HEAD_DIM"]
+    assert L.tq_unrotate(128, 2, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_unrotate(128, 1, 0x10000, -1, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_unrotate(128, 1, 0x10000, 4, 0, 0x10000, None) == S["TQ_ERR_SHAPE"]  # in place, different sizes
+    assert L.tq_unrotate(128, 1, 0x10004, 4, 1, 0x20000, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_unrotate(128, 1, None, 4, 1, 0x20000, None) == S["TQ_ERR_NULL"]
+    assert L.tq_unrotate(128, 1, None, 0, 1, None, None) == S["TQ_OK"]
+    big = _struct(tqlib, capacity=64)
+    other = _struct(tqlib, head_dim=64)
+    assert L.tq_cache_copy_rows(ctypes.byref(c), 0, ctypes.byref(other), 0, 4, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_cache_copy_rows(ctypes.byref(c), 30, ctypes.byref(b), 0, 4, None) == S["TQ_ERR_CAPACITY"]
+    assert L.tq_cache_copy_rows(ctypes.byref(c), 0, ctypes.byref(big), 40, 30, None) == S["TQ_ERR_CAPACITY"]
+    assert L.tq_cache_copy_rows(ctypes.byref(a), 4, ctypes.byref(b), 0, 8, None) == S["TQ_ERR_SHAPE"]  # overlap
+    assert L.tq_cache_copy_rows(ctypes.byref(a), 5, ctypes.byref(b), 5, 8, None) == S["TQ_OK"]        # identical
+    assert L.tq_cache_copy_rows(ctypes.byref(a), -1, ctypes.byref(b), 0, 8, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_cache_copy_rows(ctypes.byref(c), 0, ctypes.byref(b), 0, 0, None) == S["TQ_OK"]
+    assert L.tq_cache_clear_rows(ctypes.byref(a), 30, 4, None) == S["TQ_ERR_CAPACITY"]
+    assert L.tq_cache_clear_rows(ctypes.byref(a), 3, -1, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_cache_clear_rows(ctypes.byref(a), 3, 0, None) == S["TQ_OK"]

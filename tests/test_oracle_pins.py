@@ -452,7 +452,7 @@ def test_deferred_weighted_sum_equals_eager():
     rng = np.random.default_rng(7)
     d, n = 128, 50
     idx = rng.integers(0, 8, (n, d))
-    sc = oracle.f32_to_f16_bits(rng.uniform(0.1, 3.0, (n, d // 32)).astype(np.float32))
+    sc = oracle.f32_to_f16_bits(rng.uniform(0.1, 3.0, (n, d // 32)).astype(np.float32)).reshape(n, d // 32)
     w = rng.dirichlet(np.ones(n))
     rot = np.stack([oracle.value_row_rotated(idx[i], sc[i], 3) for i in range(n)]).astype(np.float64)
     eager = np.stack([oracle.value_row_dequant(idx[i], sc[i], 3) for i in range(n)]).astype(np.float64)
