@@ -75,7 +75,7 @@ typedef enum tq_dtype { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
  *   v_codes  d*v_bits/8 bytes   (little-endian bitstream)
  *   v_scale  d/32 fp16
  * Groups of 32 run along head_dim only, so any token range is byte-safe
- * ("Architecture in mlx-bun": standing invariant).  Plane base pointers must
+ * (section "Architecture in mlx-bun" keeps this as a standing rule).  Plane base pointers must
  * be 16-byte aligned and capacity a multiple of 16.
  */
 typedef struct tq_cache {
@@ -98,7 +98,7 @@ TQ_API const char *tq_status_string(tq_status status);
 
 /* Bytes one token of one kv-head occupies in the planes:
  * d*k_bits/8 + 2*(d/32)*2 + d*v_bits/8 + (d/32)*2 (200 at k8v3, d=128; page
- * "Bytes per token per head").  Returns 0 for invalid parameters. */
+ * "Algorithm", its bytes-per-token-head figure).  Returns 0 for invalid parameters. */
 TQ_API size_t tq_bytes_per_token_head(int32_t head_dim, int32_t k_bits, int32_t v_bits);
 
 /* Size in bytes of each plane of `cache` (k_codes, k_scale, k_zero, v_codes,
@@ -108,20 +108,20 @@ TQ_API tq_status tq_plane_bytes(const tq_cache *cache, size_t out_bytes[5]);
 /* The +-1 value sign vector the library applies for head_dim d (host output,
  * d int8 entries).  Output i of SplitMix64 seeded with 42; sign -1 when its
  * top bit is set.  The d=64 vector is a prefix of the d=128 one, and so on.
- * Page: "signs in {+-1}^d ... hardcoded constants per head_dim". */
+ * The page fixes one +-1 vector per head_dim, generated once and hardcoded. */
 TQ_API tq_status tq_sign_vector(int32_t head_dim, int8_t *host_out);
 
 /* The Lloyd-Max tables for v_bits (host outputs): 2^v_bits centroids and
  * 2^v_bits - 1 boundaries (midpoints), fp32, ascending; the optimal quantizer
- * of a unit normal.  Page: "3-bit table: centroids +-{0.24509, 0.75601,
- * 1.34391, 2.15195}, boundaries +-{0.50055, 1.04996, 1.74793}, 0"; other
- * widths "iterative Lloyd-Max on a unit normal". */
+ * of a unit normal.  The page prints the 3-bit table (centroids +-0.24509,
+ * +-0.75601, +-1.34391, +-2.15195; boundaries +-0.50055, +-1.04996, +-1.74793
+ * and 0) and obtains the other widths by Lloyd-Max iteration on a unit normal. */
 TQ_API tq_status tq_codebook(int32_t v_bits, float *host_centroids, float *host_boundaries);
 
 /*
  * Append: quantise n_new tokens of K and V and write them into cache rows
  * [t0, t0 + n_new) of every (sequence, kv-head); no other row is written.
- * Page: updateAndFetch "quantizes only the newly appended tokens".
+ * Page: updateAndFetch quantises just the tokens appended by the call.
  *  k, v      device bf16, element [b][h][t][j] at b*s[0] + h*s[1] + t*s[2] + j
  *            (strides in elements, head_dim contiguous); pointers 16-byte
  *            aligned and strides multiples of 8.
@@ -137,7 +137,7 @@ TQ_API tq_status tq_encode_append(const tq_cache *cache, const void *k, const in
  * bf16 (round to nearest even) or fp32 per out_dtype.  Either output may be
  * NULL to skip it.  Keys: (code + zero) * scale in fp32, the add first (page,
  * joint K/V decoder paragraph).  Values: signs * FWHT(centroid[code] * rms)
- * / sqrt(d) ("apply FWHT then multiply signs").  Outputs 16-byte aligned.
+ * / sqrt(d) (the transform first, the sign multiply after it).  Outputs 16-byte aligned.
  */
 TQ_API tq_status tq_decode(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype, void *k_out,
                     void *v_out, tq_stream_t stream);

@@ -123,7 +123,7 @@ void tqo_sign_vector(int d, uint64_t seed, int8_t *out)
 /* ------------------------------------------------------------------------ */
 /* Lloyd-Max codebook for a unit normal                                      */
 /* ------------------------------------------------------------------------ */
-/* The pages: "iterative Lloyd-Max on a unit normal", generated once and
+/* The pages obtain the tables by Lloyd-Max iteration on a unit normal, once,
  * hardcoded; the 3-bit table is printed.  Reading: the optimal quantizer of
  * N(0,1) itself (the fixed point of the two Lloyd-Max conditions), computed on
  * the analytic density rather than on samples:
@@ -263,7 +263,7 @@ double tqo_normal_mse(int n, const double *c, const double *b)
 }
 
 /* ------------------------------------------------------------------------ */
-/* Little-endian bitstream (pages: "element i at bits [i*b, i*b+b)")          */
+/* Little-endian bitstream (pages: element i occupies bits i*b .. i*b+b-1)   */
 /* ------------------------------------------------------------------------ */
 /* Reading: bit j of the stream is bit (j mod 8) of byte floor(j/8). */
 void tqo_pack_bits(const uint32_t *vals, int n, int bits, uint8_t *out)
@@ -291,7 +291,7 @@ void tqo_unpack_bits(const uint8_t *in, int n, int bits, uint32_t *vals)
 /* ------------------------------------------------------------------------ */
 /* Normalised Walsh-Hadamard transform                                       */
 /* ------------------------------------------------------------------------ */
-/* Pages: "y = FWHT(x * signs) ... FWHT normalizes by 1/sqrt(d)"; the inverse is
+/* Pages: y is the FWHT of x * signs, normalised by 1/sqrt(d); the inverse is
  * the same transform (an involution once normalised).  Reading: Sylvester
  * (natural) order, butterflies (a, b) -> (a + b, a - b) with strides
  * 1, 2, 4, ..., d/2, then every element times fl(1/sqrt(d)). */
@@ -360,7 +360,7 @@ void tqo_key_group(const float *x, int bits, int32_t *idx, uint16_t *scale_h, ui
     *zero_h = tqo_f32_to_f16(zero);
 }
 
-/* Pages: "Dequant (both): x_hat = (idx + zero) * scale", fp32 add before the
+/* Pages: keys dequantise as (idx + zero) * scale, the fp32 add before the
  * multiply, with the stored fp16 scale and zero. */
 void tqo_key_group_dequant(const int32_t *idx, uint16_t scale_h, uint16_t zero_h, float *out)
 {

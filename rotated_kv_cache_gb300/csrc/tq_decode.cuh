@@ -2,10 +2,10 @@
 //
 // Method: mlx-bun "TurboQuant -- rotation-based quantization", Part A,
 // "Algorithm": keys x_hat = (idx + zero) * scale with the fp16 scale and zero,
-// fp32 add before the multiply (the joint K/V decoder paragraph keeps "K's f32
-// addition before multiplication"); values x_hat = InvFWHT(centroid[idx] *
-// scale) then the sign flip ("apply FWHT then multiply signs", earlier copy of
-// the page), the transform normalised by 1/sqrt(d).
+// the fp32 add done before the multiply (the joint K/V decoder paragraph
+// keeps that order); values x_hat = InvFWHT(centroid[idx] * scale) followed by
+// the sign flip (the page's earlier copy orders the transform before the sign
+// multiply), the transform normalised by 1/sqrt(d).
 //
 // GB300 layout.  Keys are elementwise: a thread converts one 32-group, the
 // grid's y axis walks the (sequence, kv-head) pairs, so a warp's loads and

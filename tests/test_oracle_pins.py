@@ -139,7 +139,7 @@ def test_codebook_f32_is_rounded_binary64():
 def test_pack_worked_example():
     # element i at bits [3i, 3i+3), LSB first:
     # byte0 = 0 | 1<<3 | (2&3)<<6 = 0x88; byte1 = (2>>2) | 3<<1 | 4<<4 | (5&1)<<7 = 0xC6;
-    # byte2 = (5>>1) | 6<<2 | 7<<5 = 0xFA.  Pages: "3-bit: 8 values -> 3 bytes".
+    # byte2 = (5>>1) | 6<<2 | 7<<5 = 0xFA.  The pages: 8 three-bit values fill 3 bytes.
     assert oracle.pack_bits(np.arange(8), 3).tolist() == [0x88, 0xC6, 0xFA]
 
 
