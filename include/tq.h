@@ -203,8 +203,10 @@ TQ_API size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_head
  *           16-byte aligned; its contents need no initialisation.
  * The token being generated must have been appended first (tq_encode_append
  * with t0 = seq_len - 1), as the page's updateAndFetch does.
- * Returns TQ_ERR_UNSUPPORTED for (d, k_bits, v_bits, q_heads/H) outside the
- * instantiated set; tq_attention_supported() reports it.
+ * Every head_dim, bit pair and group size G >= 1 is covered: head_dim 128
+ * with 8- or 4-bit keys, 3-bit values and G = 8 run a specialised kernel, the
+ * rest a generic one (code widths read at run time, groups in blocks of 8
+ * q-heads); both meet the same tolerance.
  */
 TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
                               float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
@@ -214,7 +216,9 @@ TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32
  * Decode attention without any device allocation -- the pages have no
  * counterpart to this entry point; it exists for callers that cannot obtain
  * scratch memory.  Same arguments, output and tolerance as tq_decode_attention
- * minus the workspace.  Typical callers: code running inside another
+ * minus the workspace, for the specialised parameters only (head_dim 128, 8-
+ * or 4-bit keys, 3-bit values, 8 q-heads per kv-head; others return
+ * TQ_ERR_UNSUPPORTED).  Typical callers: code running inside another
  * framework's memory manager that may not call cudaMalloc/cudaFree itself
  * (both can synchronise the device and fragment a pool someone else owns),
  * and plugin-style integrations with no allocator handle to pass a workspace
@@ -236,7 +240,8 @@ TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32
 TQ_API tq_status tq_decode_attention_noalloc(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
                                              float softmax_scale, float *out, tq_stream_t stream);
 
-/* 1 if tq_decode_attention covers these parameters, else 0. */
+/* 1 if tq_decode_attention covers these parameters (every valid head_dim and
+ * bit pair, group_size >= 1), else 0. */
 TQ_API int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bits, int32_t group_size);
 
 /*

@@ -240,15 +240,29 @@ tq_status tq_cache_clear_rows(const tq_cache *c, int64_t t0, int64_t n, tq_strea
 
 int tq_attention_supported(int32_t d, int32_t kb, int32_t vb, int32_t group)
 {
-    return tq::attention_supported(d, kb, vb, group) ? 1 : 0;
+    return valid_head_dim(d) && valid_kbits(kb) && valid_vbits(vb) && group >= 1 ? 1 : 0;
 }
+
+namespace {
+// the specialised kernel where it applies, the generic one elsewhere
+bool specialised(const tq_cache *c, int32_t q_heads)
+{
+    return tq::attention_supported(c->head_dim, c->k_bits, c->v_bits, q_heads / c->num_kv_heads);
+}
+
+size_t workspace_bytes(const tq_cache *c, int32_t q_heads, int64_t seq_len)
+{
+    return specialised(c, q_heads) ? tq::attention_workspace_bytes(view(c), q_heads, seq_len)
+                                   : tq::attention_generic_workspace_bytes(view(c), q_heads, seq_len);
+}
+}  // namespace
 
 size_t tq_attention_workspace_bytes(const tq_cache *c, int32_t q_heads, int64_t seq_len)
 {
     if (check_cache(c) != TQ_OK || q_heads < 1 || q_heads % c->num_kv_heads != 0 || seq_len < 1 ||
         seq_len > c->capacity)
         return 0;
-    return tq::attention_workspace_bytes(view(c), q_heads, seq_len);
+    return workspace_bytes(c, q_heads, seq_len);
 }
 
 tq_status tq_decode_attention(const tq_cache *c, const void *q, int32_t q_heads, int64_t seq_len, float scale,
@@ -261,13 +275,15 @@ tq_status tq_decode_attention(const tq_cache *c, const void *q, int32_t q_heads,
     if (seq_len < 1) return TQ_ERR_SHAPE;
     if (seq_len > c->capacity) return TQ_ERR_CAPACITY;
     if (!aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
-    if (!tq::attention_supported(c->head_dim, c->k_bits, c->v_bits, q_heads / c->num_kv_heads))
-        return TQ_ERR_UNSUPPORTED;
-    const size_t need = tq::attention_workspace_bytes(view(c), q_heads, seq_len);
-    if (need > 0 && (!ws || ws_bytes < need)) return TQ_ERR_WORKSPACE;
-    if (ws && !aligned16(ws)) return TQ_ERR_ALIGN;
-    return cuda_status(tq::launch_attention(view(c), static_cast<const uint16_t *>(q), q_heads, seq_len, scale, out,
-                                            ws, ws_bytes, (cudaStream_t)stream));
+    const size_t need = workspace_bytes(c, q_heads, seq_len);
+    if (need == 0) return TQ_ERR_CUDA;  // the occupancy query failed
+    if (!ws || ws_bytes < need) return TQ_ERR_WORKSPACE;
+    if (!aligned16(ws)) return TQ_ERR_ALIGN;
+    const uint16_t *qh = static_cast<const uint16_t *>(q);
+    if (specialised(c, q_heads))
+        return cuda_status(tq::launch_attention(view(c), qh, q_heads, seq_len, scale, out, ws, ws_bytes, (cudaStream_t)stream));
+    return cuda_status(
+        tq::launch_attention_generic(view(c), qh, q_heads, seq_len, scale, out, ws, ws_bytes, (cudaStream_t)stream));
 }
 
 tq_status tq_decode_attention_noalloc(const tq_cache *c, const void *q, int32_t q_heads, int64_t seq_len,

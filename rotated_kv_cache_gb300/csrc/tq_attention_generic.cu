@@ -1,0 +1,630 @@
+// tq_attention_generic.cu -- fused dequantise-on-fetch decode attention for
+// every head_dim, bit pair and GQA group size.  The kernel in
+// tq_attention.cu is the specialised path for head_dim 128, 8- or 4-bit keys,
+// 3-bit values and groups of 8 q-heads; this one covers the rest with the
+// same method and the same tolerance.
+//
+// Method: mlx-bun "TurboQuant -- rotation-based quantization", Part A:
+// "Architecture in mlx-bun" (attention reads the dequantised window),
+// "Algorithm" (key (code + zero) * scale, value centroid[code] * rms) and
+// "Deferred inverse FWHT" (the weighted sum is formed in the rotated domain
+// and un-rotated once per query row).
+//
+// Design, as in the specialised kernel: split-KV CTAs stream 64-token stages
+// through a shared-memory ring (bulk copies completing on an mbarrier; the
+// last warp to finish a stage refills it); each of the 4 warps takes 16
+// tokens.  QK^T and PV run on mma.sync m16n8k16 (f16 in, f32 accumulate) with
+// N = 8 q-heads per CTA; groups larger than 8 use several CTAs (head blocks),
+// smaller ones mask the unused columns.  Key codes enter the MMA as exact f16
+// integers (1024 + code) and the per-group affine is applied to the scores;
+// value codes are looked up in an f16 centroid table and the rms is folded
+// into P.  Code widths are run-time values here (one kernel per head_dim),
+// extracted with funnel shifts from the packed rows.
+#include <cuda.h>
+
+#include "tq_common.cuh"
+#include "tq_kernels.h"
+
+namespace tq {
+namespace {
+
+constexpr int gW = 4;               // warps per CTA
+constexpr int gThreads = gW * 32;
+constexpr int gT = 64;              // tokens per stage
+constexpr int gN = 8;               // q-heads per CTA (the MMA's N)
+constexpr int gMaxStages = 3;
+
+struct GenParams {
+    const uint8_t *k_codes, *v_codes;
+    const uint16_t *k_scale, *k_zero, *v_scale;
+    const uint16_t *q;  // [B][QH][D] bf16
+    float *part_o;      // [B][H][HB][S][8][D]
+    float *part_ml;     // [B][H][HB][S][8][2]
+    uint32_t *err;
+    int H, QH, G, HB, splits, kb, vb, stages;
+    int64_t cap, seq_len, tokens_per_split;
+    int rbk, rbv;                                  // packed row bytes of keys and values
+    int off_ks, off_kz, off_vs, off_v, stage_bytes;  // stage layout (keys at 0)
+    float scale_log2, koff;                        // softmax scale * log2(e); f16 offset of a key code
+    uint16_t cen[256];                             // value centroids as f16 bits
+};
+
+__device__ __forceinline__ void g_mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                      uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t g_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t g_pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t g_hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ float g_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t g_lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t g_lds16(uint32_t a)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint2 g_lds64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+// Key codes of dims 32G + 8c .. +7 of one packed row -> four f16x2 pairs
+// (dims 2p, 2p+1), each half koff + code with koff = 1024 (unsigned codes) or
+// 1152 (int8 codes, stored offset by 128).
+__device__ __forceinline__ void key_pairs(uint32_t row, int G, int c, int kb, uint32_t (&pr)[4])
+{
+    const int off = (4 * G + c) * kb;  // byte offset of the 8 codes (8 * kb bits)
+    const uint32_t a = row + (off & ~3);
+    const uint32_t lo = g_lds32(a), hi = g_lds32(a + 4);
+    const int sh = (off & 3) * 8;
+    uint64_t v = ((uint64_t)hi << 32 | lo) >> sh;
+    if (kb == 8) {
+        v ^= 0x8080808080808080ull;  // int8 -> code + 128
+        const uint32_t l = (uint32_t)v, h = (uint32_t)(v >> 32);
+        pr[0] = __byte_perm(l, 0x64646464u, 0x5140);
+        pr[1] = __byte_perm(l, 0x64646464u, 0x5342);
+        pr[2] = __byte_perm(h, 0x64646464u, 0x5140);
+        pr[3] = __byte_perm(h, 0x64646464u, 0x5342);
+        return;
+    }
+    const uint32_t mask = (1u << kb) - 1u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t c0 = (uint32_t)(v >> (2 * p * kb)) & mask, c1 = (uint32_t)(v >> ((2 * p + 1) * kb)) & mask;
+        pr[p] = (c0 | (c1 << 16)) | 0x64006400u;
+    }
+}
+
+// Value codes of dims 32G + 4g .. +3 of one packed row -> their f16 centroids.
+__device__ __forceinline__ void value_quad(uint32_t row, int G, int g, int vb, uint32_t lut, uint32_t (&h)[4])
+{
+    const int b = (32 * G + 4 * g) * vb;
+    const uint32_t a = row + 4 * (b >> 5);
+    const uint32_t x = __funnelshift_r(g_lds32(a), g_lds32(a + 4), b & 31);
+    const uint32_t mask = (1u << vb) - 1u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = g_lds16(lut + 2 * ((x >> (k * vb)) & mask));
+}
+
+template <int D>
+struct GGeo {
+    static constexpr int NG = D / 32;
+    static constexpr int KS = D / 16;                       // k-steps of QK^T, m-tiles of PV
+    static constexpr int QF = gN * KS * 4 * 8;               // q fragments: [head][k-step][c] x (b0, b1)
+    static constexpr int QS = (NG + 1) * gN * 4;             // group sums of the f16 q, then per-head score scale
+    static constexpr int MERGE = gW * gN * (D + 2) * 4;      // per-warp partials (reuse the ring)
+};
+
+template <int D>
+__global__ void __launch_bounds__(gThreads, D >= 512 ? 1 : D >= 256 ? 2 : 3)
+    attn_generic_kernel(const __grid_constant__ GenParams p)
+{
+    using A = GGeo<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int ring = p.stages * p.stage_bytes > A::MERGE ? p.stages * p.stage_bytes : A::MERGE;
+    uint8_t *stages = smem;
+    float *merge = reinterpret_cast<float *>(smem);
+    uint8_t *qf = smem + ring;
+    float *qsum = reinterpret_cast<float *>(qf + A::QF);
+    uint16_t *lut = reinterpret_cast<uint16_t *>(qf + A::QF + A::QS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(qf + A::QF + A::QS + 512);
+    uint32_t *done = reinterpret_cast<uint32_t *>(bars + gMaxStages);
+    const uint32_t full0 = smem_addr(bars);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, h = blockIdx.y / p.HB, hb = blockIdx.y - h * p.HB, b = blockIdx.z;
+    const int64_t bh = (int64_t)b * p.H + h;
+    const int64_t t_begin = (int64_t)split * p.tokens_per_split;
+    const int64_t t_end = imin64(p.seq_len, t_begin + p.tokens_per_split);
+    const int n_stages = t_end > t_begin ? (int)((t_end - t_begin + gT - 1) / gT) : 0;
+    const int NG = D / 32;
+
+    auto issue = [&](int s) {
+        const int slot = s % p.stages;
+        const int64_t t = t_begin + (int64_t)s * gT;
+        const int rows = (int)imin64(gT, p.cap - t);
+        const int64_t row0 = bh * p.cap + t;
+        const uint32_t st = smem_addr(stages + slot * p.stage_bytes), bar = full0 + 8 * slot;
+        mbar_arrive_expect_tx(bar, (uint32_t)(rows * (p.rbk + p.rbv + 3 * NG * 2)));
+        bulk_g2s(st, p.k_codes + row0 * p.rbk, rows * p.rbk, bar);
+        bulk_g2s(st + p.off_ks, p.k_scale + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + p.off_kz, p.k_zero + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + p.off_vs, p.v_scale + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + p.off_v, p.v_codes + row0 * p.rbv, rows * p.rbv, bar);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            done[s] = 0;
+        }
+        fence_mbar_init();
+        for (int s = 0; s < p.stages && s < n_stages; ++s) issue(s);
+    }
+    for (int i = threadIdx.x; i < (1 << p.vb); i += blockDim.x) lut[i] = p.cen[i];
+
+    // ---------------------------------------------------------------- q of the CTA's 8 heads
+    // Warp w prepares heads 2w, 2w+1; lane l holds dims 4 (l % 16) + 64 j + {0..3}
+    // of head 2w + l / 16.  Each head is scaled by a power of two so its largest
+    // |q| lands in [2^14, 2^15) before the f16 rounding; heads past the group
+    // are zero.
+    {
+        const int n = 2 * warp + (lane >> 4), l16 = lane & 15;
+        const int qh = h * p.G + hb * gN + n;
+        const bool real = hb * gN + n < p.G;
+        float qv[D / 64][4];
+        float mx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) {
+            uint2 w = make_uint2(0u, 0u);
+            if (real) w = *reinterpret_cast<const uint2 *>(p.q + ((int64_t)b * p.QH + qh) * D + 64 * j + 4 * l16);
+            qv[j][0] = bf16_lo(w.x); qv[j][1] = bf16_hi(w.x); qv[j][2] = bf16_lo(w.y); qv[j][3] = bf16_hi(w.y);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qv[j][i]));
+        }
+#pragma unroll
+        for (int m = 1; m < 16; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        int e = 0;
+        if (mx > 0.0f && mx < INFINITY) e = 14 - (((int)(__float_as_uint(mx) >> 23) & 0xFF) - 127);
+        e = e < -100 ? -100 : (e > 100 ? 100 : e);
+        const float qscale = ldexpf(1.0f, e);
+        // dims 64j + 4 l16 + {0..3} lie in group G = 2j + l16 / 8 at offset 4 (l16 % 8);
+        // fragment slot (k-step 2G + jj, c, b0/b1) holds dims 8c + 4jj + {0,1} / {2,3}
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) {
+            const int G = 2 * j + (l16 >> 3), o = 4 * (l16 & 7), c = o >> 3, jj = (o >> 2) & 1;
+            float f[4];
+            uint32_t hw[2];
+            hw[0] = g_pack_f16x2(qv[j][0] * qscale, qv[j][1] * qscale);
+            hw[1] = g_pack_f16x2(qv[j][2] * qscale, qv[j][3] * qscale);
+            f[0] = __low2float(*reinterpret_cast<__half2 *>(&hw[0]));
+            f[1] = __high2float(*reinterpret_cast<__half2 *>(&hw[0]));
+            f[2] = __low2float(*reinterpret_cast<__half2 *>(&hw[1]));
+            f[3] = __high2float(*reinterpret_cast<__half2 *>(&hw[1]));
+            uint32_t *slot = reinterpret_cast<uint32_t *>(qf + ((n * A::KS + 2 * G + jj) * 4 + c) * 8);
+            slot[0] = hw[0];
+            slot[1] = hw[1];
+            float s = (f[0] + f[1]) + (f[2] + f[3]);
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            if ((l16 & 7) == 0) qsum[G * gN + n] = s;
+        }
+        if (l16 == 0) qsum[NG * gN + n] = ldexpf(1.0f, -e) * p.scale_log2;  // stored after the sums
+    }
+    __syncthreads();
+
+    const int g = lane >> 2, c = lane & 3;
+    const float ie0 = qsum[NG * gN + 2 * c], ie1 = qsum[NG * gN + 2 * c + 1];
+    float o[A::KS][4];
+#pragma unroll
+    for (int i = 0; i < A::KS; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+    const int r0 = 16 * warp + g, r1 = r0 + 8;
+    const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
+    const uint32_t qf_lane = smem_addr(qf) + (g * A::KS * 4 + c) * 8, lut_a = smem_addr(lut);
+
+    bool ok = true;
+    for (int s = 0; s < n_stages; ++s) {
+        const int slot = s % p.stages;
+        if (!mbar_wait_bounded(full0 + 8 * slot, (s / p.stages) & 1, p.err)) {
+            ok = false;
+            break;
+        }
+        const uint32_t st = smem_addr(stages + slot * p.stage_bytes);
+        const int64_t tile_t0 = t_begin + (int64_t)s * gT + 16 * warp;
+
+        // ---------------- S = Q K^T, group by group, with the group affine
+        float S[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+#pragma unroll 1
+        for (int G = 0; G < A::NG; ++G) {
+            uint32_t k0[4], k1[4];
+            key_pairs(st + r0 * p.rbk, G, c, p.kb, k0);
+            key_pairs(st + r1 * p.rbk, G, c, p.kb, k1);
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const uint2 bq = g_lds64(qf_lane + (2 * G + jj) * 32);
+                g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq.x, bq.y);
+            }
+            const float sc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (r0 * NG + G) * 2));
+            const float sc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (r1 * NG + G) * 2));
+            const float zc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (r0 * NG + G) * 2)) - p.koff;
+            const float zc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (r1 * NG + G) * 2)) - p.koff;
+            const float qs0 = qsum[G * gN + 2 * c], qs1 = qsum[G * gN + 2 * c + 1];
+            S[0][0] = fmaf(sc0, fmaf(zc0, qs0, acc[0]), S[0][0]);
+            S[0][1] = fmaf(sc0, fmaf(zc0, qs1, acc[1]), S[0][1]);
+            S[1][0] = fmaf(sc1, fmaf(zc1, qs0, acc[2]), S[1][0]);
+            S[1][1] = fmaf(sc1, fmaf(zc1, qs1, acc[3]), S[1][1]);
+        }
+        S[0][0] *= ie0; S[1][0] *= ie0;
+        S[0][1] *= ie1; S[1][1] *= ie1;
+        if (tile_t0 + 16 > t_end) {
+            if (tile_t0 + g >= t_end) S[0][0] = S[0][1] = -INFINITY;
+            if (tile_t0 + g + 8 >= t_end) S[1][0] = S[1][1] = -INFINITY;
+        }
+        // ---------------- online softmax (base 2), heads 2c, 2c+1
+        float pr[2][2];
+        const bool raise = S[0][0] > m_run[0] || S[1][0] > m_run[0] || S[0][1] > m_run[1] || S[1][1] > m_run[1] ||
+                           m_run[0] == -INFINITY || m_run[1] == -INFINITY;
+        if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float mt = fmaxf(S[0][j], S[1][j]);
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                const float mn = fmaxf(m_run[j], mt);
+                const float mu = mn == -INFINITY ? 0.0f : mn;
+                const float alpha = g_ex2(m_run[j] - mu);
+                m_run[j] = mn;
+                pr[0][j] = g_ex2(S[0][j] - mu);
+                pr[1][j] = g_ex2(S[1][j] - mu);
+                l_run[j] = l_run[j] * alpha + pr[0][j] + pr[1][j];
+#pragma unroll
+                for (int mt2 = 0; mt2 < A::KS; ++mt2) {
+                    o[mt2][j] *= alpha;
+                    o[mt2][2 + j] *= alpha;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                pr[0][j] = g_ex2(S[0][j] - m_run[j]);
+                pr[1][j] = g_ex2(S[1][j] - m_run[j]);
+                l_run[j] += pr[0][j] + pr[1][j];
+            }
+        }
+        const uint32_t pt0 = g_trans(g_pack_f16x2(pr[0][0], pr[0][1]));  // tokens 2c, 2c+1; head g
+        const uint32_t pt1 = g_trans(g_pack_f16x2(pr[1][0], pr[1][1]));  // tokens 2c+8, 2c+9
+        bool vlive[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) vlive[q] = tile_t0 + (vr[q] - 16 * warp) < t_end;
+        // ---------------- O^T += V^T (P * rms)^T, group by group
+#pragma unroll
+        for (int G = 0; G < A::NG; ++G) {
+            uint32_t sv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sv[q] = vlive[q] ? g_lds16(st + p.off_vs + (vr[q] * NG + G) * 2) : 0u;
+            const uint32_t b0 = g_hmul2(pt0, sv[0] | (sv[1] << 16)), b1 = g_hmul2(pt1, sv[2] | (sv[3] << 16));
+            uint32_t hv[4][4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) value_quad(st + p.off_v + vr[q] * p.rbv, G, g, p.vb, lut_a, hv[q]);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                // rows g, g+8 of the m-tile: dims 32G + 4g + 2 half + {0, 1}
+                const int r = 2 * half;
+                g_mma(o[2 * G + half], hv[0][r] | (hv[1][r] << 16), hv[0][r + 1] | (hv[1][r + 1] << 16),
+                      hv[2][r] | (hv[3][r] << 16), hv[2][r + 1] | (hv[3][r + 1] << 16), b0, b1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&done[slot], 1u) == gW - 1) {
+                done[slot] = 0;
+                if (s + p.stages < n_stages) issue(s + p.stages);
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- merge the warps
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+    }
+    float *mw = merge + warp * gN * (D + 2);  // [head][D] o, then [head] m, [head] l
+#pragma unroll
+    for (int mt = 0; mt < A::KS; ++mt) {
+        const int G = mt >> 1, half = mt & 1;
+        const int d0 = 32 * G + 4 * g + 2 * half;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mw[(2 * c + j) * D + d0] = o[mt][j];
+            mw[(2 * c + j) * D + d0 + 1] = o[mt][2 + j];
+        }
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mw[gN * D + 2 * c + j] = ok ? m_run[j] : -INFINITY;
+            mw[gN * D + gN + 2 * c + j] = ok ? l_run[j] : 0.0f;
+        }
+    }
+    __syncthreads();
+    // thread -> (head hh, a D/16 slice of dims)
+    constexpr int PER = D / 16;
+    const int hh = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * PER;
+    float mmax = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < gW; ++w) mmax = fmaxf(mmax, merge[w * gN * (D + 2) + gN * D + hh]);
+    const float mu = mmax == -INFINITY ? 0.0f : mmax;
+    float ov[PER], lsum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) ov[i] = 0.0f;
+#pragma unroll
+    for (int w = 0; w < gW; ++w) {
+        const float *m2 = merge + w * gN * (D + 2);
+        const float wt = g_ex2(m2[gN * D + hh] - mu);
+        lsum += m2[gN * D + gN + hh] * wt;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) ov[i] += m2[hh * D + d0 + i] * wt;
+    }
+    const int64_t pidx = ((bh * p.HB + hb) * p.splits + split) * gN + hh;
+    float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * D + d0);
+#pragma unroll
+    for (int i = 0; i < PER / 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+    if ((threadIdx.x & 15) == 0) {
+        p.part_ml[2 * pidx] = mmax;
+        p.part_ml[2 * pidx + 1] = lsum;
+    }
+}
+
+// ---------------------------------------------------------------- combine + deferred un-rotation
+struct GenCombineParams {
+    const float *part_o, *part_ml;
+    float *out;  // [B][QH][D]
+    int H, QH, G, HB, splits, rows;
+    float inv_sqrt_d;
+};
+
+// one warp per (sequence, q-head); lane holds dims PER*lane .. +PER-1
+template <int D>
+__global__ void __launch_bounds__(256) attn_generic_combine(const __grid_constant__ GenCombineParams p)
+{
+    constexpr int PER = D / 32;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= p.rows) return;
+    const int b = row / p.QH, qh = row % p.QH;
+    const int h = qh / p.G, w = qh % p.G, hb = w / gN, n = w % gN;
+    const int64_t base = (((int64_t)b * p.H + h) * p.HB + hb) * p.splits;
+    float mmax = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * gN + n)]);
+    const float mu = mmax == -INFINITY ? 0.0f : mmax;
+    float x[PER], l = 0.0f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = 0.0f;
+    for (int s = 0; s < p.splits; ++s) {
+        const int64_t pi = (base + s) * gN + n;
+        const float wt = g_ex2(p.part_ml[2 * pi] - mu);
+        l += p.part_ml[2 * pi + 1] * wt;
+        const float *src = p.part_o + pi * D + PER * lane;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) x[i] += src[i] * wt;
+    }
+    const float inv_l = 1.0f / l;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] *= inv_l;
+    // inverse transform in Sylvester order: log2(PER) stages in-lane, 5 across lanes
+#pragma unroll
+    for (int hs = 1; hs < PER; hs <<= 1)
+#pragma unroll
+        for (int i = 0; i < PER; i += 2 * hs)
+#pragma unroll
+            for (int j = i; j < i + hs; ++j) {
+                const float a = x[j], bb = x[j + hs];
+                x[j] = a + bb;
+                x[j + hs] = a - bb;
+            }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = upper ? other - x[i] : x[i] + other;
+        }
+    }
+    float *dst = p.out + ((int64_t)b * p.QH + qh) * D + PER * lane;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) dst[i] = x[i] * (sign_negative(PER * lane + i) ? -p.inv_sqrt_d : p.inv_sqrt_d);
+}
+
+// ---------------------------------------------------------------- host side
+struct GenPlan {
+    int splits, stages, stage_bytes, smem;
+    int64_t tokens_per_split;
+    int off_ks, off_kz, off_vs, off_v;
+};
+
+template <int D>
+int gen_ctas_per_sm(int smem)
+{
+    int n = 0;
+    auto kern = attn_generic_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, gThreads, smem) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int D>
+bool gen_plan(const CacheView &c, int q_heads, int64_t seq_len, GenPlan &pl)
+{
+    using A = GGeo<D>;
+    const int NG = D / 32, rbk = D * c.kb / 8, rbv = D * c.vb / 8;
+    auto r16 = [](int x) { return (x + 15) / 16 * 16; };
+    pl.off_ks = r16(gT * rbk);
+    pl.off_kz = pl.off_ks + r16(gT * NG * 2);
+    pl.off_vs = pl.off_kz + r16(gT * NG * 2);
+    pl.off_v = pl.off_vs + r16(gT * NG * 2);
+    pl.stage_bytes = (pl.off_v + gT * rbv + 16 + 127) / 128 * 128;
+    pl.stages = 3 * pl.stage_bytes <= 80 * 1024 ? 3 : 2;
+    const int ring = pl.stages * pl.stage_bytes > A::MERGE ? pl.stages * pl.stage_bytes : A::MERGE;
+    pl.smem = 128 /*align slack*/ + ring + A::QF + A::QS + 512 /*lut*/ + gMaxStages * 12 /*barriers, counters*/;
+    const int per_sm = gen_ctas_per_sm<D>(pl.smem);
+    if (per_sm < 1) return false;
+    const int G = q_heads / c.H, HB = (G + gN - 1) / gN;
+    const int64_t units = (int64_t)c.B * c.H * HB;
+    const int64_t nst = (seq_len + gT - 1) / gT;
+    const int64_t slots = (int64_t)num_sms() * per_sm;
+    pl.splits = 1;
+    pl.tokens_per_split = nst * gT;
+    double best = 1e300;
+    for (int waves = 1; waves <= 16; ++waves) {
+        int64_t s = (waves * slots + units - 1) / units;
+        if (s < 1) s = 1;
+        if (s > nst) s = nst;
+        const int64_t per = (nst + s - 1) / s, sp = (nst + per - 1) / per;
+        const double cost = (double)((units * sp + slots - 1) / slots) * (double)(per + 2);
+        if (cost < best - 1e-9) {
+            best = cost;
+            pl.splits = (int)sp;
+            pl.tokens_per_split = per * gT;
+        }
+    }
+    return true;
+}
+
+template <int D>
+size_t gen_workspace(const CacheView &c, int q_heads, int64_t seq_len)
+{
+    GenPlan pl;
+    if (!gen_plan<D>(c, q_heads, seq_len, pl)) return 0;
+    const int HB = (q_heads / c.H + gN - 1) / gN;
+    return (size_t)c.B * c.H * HB * pl.splits * gN * (D + 2) * 4;
+}
+
+template <int D>
+cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out, void *ws,
+                    size_t ws_bytes, cudaStream_t s)
+{
+    GenPlan pl;
+    if (!gen_plan<D>(c, QH, seq_len, pl)) return cudaErrorInvalidConfiguration;
+    const int G = QH / c.H, HB = (G + gN - 1) / gN;
+    const size_t need_o = (size_t)c.B * c.H * HB * pl.splits * gN * D * 4;
+    const size_t need = need_o + (size_t)c.B * c.H * HB * pl.splits * gN * 2 * 4;
+    if (ws_bytes < need) return cudaErrorInvalidValue;
+    GenParams p{};
+    p.k_codes = c.k_codes;
+    p.v_codes = c.v_codes;
+    p.k_scale = c.k_scale;
+    p.k_zero = c.k_zero;
+    p.v_scale = c.v_scale;
+    p.q = q;
+    p.part_o = static_cast<float *>(ws);
+    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + need_o);
+    p.err = device_error_word();
+    if (!p.err) return cudaErrorInvalidDevice;
+    p.H = c.H;
+    p.QH = QH;
+    p.G = G;
+    p.HB = HB;
+    p.splits = pl.splits;
+    p.kb = c.kb;
+    p.vb = c.vb;
+    p.stages = pl.stages;
+    p.cap = c.cap;
+    p.seq_len = seq_len;
+    p.tokens_per_split = pl.tokens_per_split;
+    p.rbk = D * c.kb / 8;
+    p.rbv = D * c.vb / 8;
+    p.off_ks = pl.off_ks;
+    p.off_kz = pl.off_kz;
+    p.off_vs = pl.off_vs;
+    p.off_v = pl.off_v;
+    p.stage_bytes = pl.stage_bytes;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.koff = c.kb == 8 ? 1152.0f : 1024.0f;
+    const Tables &tab = codebook_tables(c.vb);
+    for (int i = 0; i < (1 << c.vb); ++i) p.cen[i] = __half_as_ushort(__float2half_rn(tab.centroids[i]));
+    if ((int64_t)c.H * HB > 65535 || c.B > 65535) return cudaErrorInvalidValue;
+    attn_generic_kernel<D><<<dim3(pl.splits, c.H * HB, c.B), gThreads, pl.smem, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int rows = c.B * QH;
+    GenCombineParams cp{p.part_o, p.part_ml, out, c.H, QH, G, HB, pl.splits, rows, inv_sqrt_head_dim(D)};
+    attn_generic_combine<D><<<(rows + 7) / 8, 256, 0, s>>>(cp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)
+{
+    switch (c.d) {
+    case 64: return gen_workspace<64>(c, q_heads, seq_len);
+    case 128: return gen_workspace<128>(c, q_heads, seq_len);
+    case 256: return gen_workspace<256>(c, q_heads, seq_len);
+    case 512: return gen_workspace<512>(c, q_heads, seq_len);
+    }
+    return 0;
+}
+
+cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
+                                     float *out, void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    switch (c.d) {
+    case 64: return gen_run<64>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+    case 128: return gen_run<128>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+    case 256: return gen_run<256>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+    case 512: return gen_run<512>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tq

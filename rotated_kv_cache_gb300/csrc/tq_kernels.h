@@ -44,6 +44,12 @@ TQ_DECLARE_PER_D(256)
 TQ_DECLARE_PER_D(512)
 #undef TQ_DECLARE_PER_D
 
+// Attention for every head_dim, bit pair and group size (the specialised
+// kernel above covers d128, k8/k4, v3, groups of 8).
+size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len);
+cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
+                                     float *out, void *ws, size_t ws_bytes, cudaStream_t s);
+
 // Deferred fetch, un-rotation and cache row copy / clear (src null: zeros).
 cudaError_t launch_decode_rotated(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out, cudaStream_t s);
 cudaError_t launch_unrotate(int d, bool in_f32, const void *x, int64_t rows, bool out_f32, void *out, cudaStream_t s);

@@ -1,0 +1,65 @@
+"""Decode attention for every head_dim, bit pair and GQA group size (the
+generic kernel; head_dim 128 k8/k4 v3 with groups of 8 take the specialised
+kernel) against the binary64 oracle.  Tolerance: 2e-3 max-abs on the fp32
+output, as for the specialised kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tq_synth
+from tqtest import planes_from_device, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+COMBOS = [(d, kb, vb) for d in (64, 128, 256, 512) for kb in (2, 4, 5, 8) for vb in (2, 3, 4, 5, 8)]
+
+
+def _run(tq, d, kb, vb, B, H, G, T, cap=None, step=0, w=None):
+    w = w or tq_synth.WORKLOADS["sweep"]
+    k, v = tq_synth.host_kv(w, B=B, H=H, d=d, n=T)
+    cache = tq.Cache(B, H, d, cap or T, k_bits=kb, v_bits=vb)
+    tq.tq_encode_append(cache, to_device_bf16(k), to_device_bf16(v), 0)
+    q = tq_synth.host_q(tq_synth.WORKLOADS["decode"], step, B=B, QH=G * H, d=d)
+    out = tq.tq_decode_attention(cache, to_device_bf16(q), T)
+    # the oracle attends over the GPU's own bytes (the codec is checked separately)
+    want = oracle.attention(planes_from_device(cache), q, T)
+    return np.abs(out.cpu().numpy().astype(np.float64) - want).max()
+
+
+@pytest.mark.parametrize("d,kb,vb", COMBOS)
+def test_every_width_and_head_dim(cuda, d, kb, vb):
+    err = _run(cuda, d, kb, vb, B=2, H=2, G=8, T=137)
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 6, 12, 16])
+def test_group_sizes(cuda, G):
+    err = _run(cuda, 128, 8, 3, B=2, H=3, G=G, T=201, step=G)
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("d,kb,vb,G,T", [(256, 4, 2, 4, 5000), (64, 8, 4, 8, 9000), (512, 5, 3, 2, 1500)])
+def test_long_contexts_split(cuda, d, kb, vb, G, T):
+    """Several splits per (sequence, kv-head) and ragged stage tails."""
+    err = _run(cuda, d, kb, vb, B=1, H=2, G=G, T=T, cap=T + 11 + (16 - (T + 11) % 16) % 16)
+    assert err < TOL, err
+
+
+def test_single_row_and_decode_step_flow(cuda):
+    w = tq_synth.WORKLOADS["decode"]
+    d, kb, vb, B, H, G = 256, 8, 2, 2, 2, 4
+    k, v = tq_synth.host_kv(tq_synth.WORKLOADS["sweep"], B=B, H=H, d=d, n=40)
+    cache = cuda.Cache(B, H, d, 48, k_bits=kb, v_bits=vb)
+    ref = oracle.Planes(B, H, d, kb, vb, cache.capacity)
+    for t in (0, 1, 2, 39):
+        if t == 39:
+            cuda.tq_encode_append(cache, to_device_bf16(k[:, :, 3:39]), to_device_bf16(v[:, :, 3:39]), 3)
+        cuda.tq_encode_append(cache, to_device_bf16(k[:, :, t:t + 1]), to_device_bf16(v[:, :, t:t + 1]), t)
+        q = tq_synth.host_q(w, t, B=B, QH=G * H, d=d)
+        out = cuda.tq_decode_attention(cache, to_device_bf16(q), t + 1)
+        want = oracle.attention(planes_from_device(cache), q, t + 1)
+        assert np.abs(out.cpu().numpy() - want).max() < TOL
+    assert cuda.tq_device_error() == 0

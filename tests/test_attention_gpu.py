@@ -99,11 +99,10 @@ def test_attention_refusals(cuda):
     with pytest.raises(cuda.TQError) as e:
         cuda.tq_decode_attention(cache, q, 40, workspace=small)
     assert e.value.status == 7
-    c2 = cuda.Cache(1, 2, 64, 64, k_bits=8, v_bits=3)
-    with pytest.raises(cuda.TQError) as e:
-        cuda.tq_decode_attention(c2, torch.zeros((1, 16, 64), dtype=torch.bfloat16, device="cuda"), 10)
-    assert e.value.status == 9
-    assert not cuda.tq_attention_supported(128, 8, 2, 8) and cuda.tq_attention_supported(128, 4, 3, 8)
+    # every valid (head_dim, k_bits, v_bits) and group >= 1 is covered; nothing else
+    assert all(cuda.tq_attention_supported(d, kb, vb, g) for d in (64, 128, 256, 512) for kb in (2, 4, 5, 8)
+               for vb in (2, 3, 4, 5, 8) for g in (1, 8, 16))
+    assert not any(cuda.tq_attention_supported(*a) for a in ((96, 8, 3, 8), (128, 3, 3, 8), (128, 8, 6, 8), (128, 8, 3, 0)))
 
 
 def _full_size_check(tq, w, B, samples, chunk_b=4):
