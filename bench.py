@@ -20,6 +20,9 @@ packed rows in and bf16 out for the fetch, every cached row (200 B per
 token-head) plus q and the output for the attention.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       python bench.py --sweep   (one JSON line per path beyond the headline step:
+                                  attention at other widths/head dims/groups, the
+                                  deferred fetch, the un-rotation, row copies)
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (weak scaling, no collective on the data path); rank 0 prints one JSON line.
 """
@@ -40,7 +43,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KV codec encode/decode GB/s and fused dequant-attn µs/step, % of HBM roofline"
 PREFILL = dict(B=4, H=8, T=8192, d=128, kb=8, vb=3)
 DECODE = dict(B=32, H=8, QH=64, T=32768, d=128, kb=8, vb=3)
-BYTES_PER_TH = 200  # k8v3, d128 (page: "Bytes per token per head")
+BYTES_PER_TH = 200  # k8v3, d128 (page section "Algorithm", bytes per token-head)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -416,6 +419,90 @@ def cpu_baseline():
 
 
 # ------------------------------------------------------------------ main
+# ------------------------------------------------------------------ sweep of the other paths
+def run_sweep():
+    """Device-timed throughput of the paths beyond the headline step, each on
+    inputs larger than L2: CUDA events on the launching stream around 20 calls
+    after 3 warm-up calls, median.  GB/s counts the format bytes each call must
+    move (cache rows read, outputs written)."""
+    import torch
+
+    import rotated_kv_cache_gb300 as tq
+    import tq_synth
+
+    torch.cuda.set_device(0)
+    peak, kind = measured_peaks()
+    st = torch.cuda.current_stream()
+
+    def timed(fn, reps=20, rounds=3):
+        # reps calls back to back between two events (the queue stays full, so
+        # host launch time is hidden), median over rounds
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(rounds):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for _ in range(reps):
+                fn()
+            b.record(st)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / reps)
+        return statistics.median(ts)
+
+    def emit(kind_, config, us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"sweep": kind_, "config": config, "us": round(us, 2), "GB/s": round(gbs, 1),
+                          "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": kind}), flush=True)
+
+    def filled_cache(B, H, d, T, kb, vb, w):
+        cache = tq.Cache(B, H, d, T + (16 - T % 16) % 16, k_bits=kb, v_bits=vb)
+        for b0 in range(B):
+            k = torch.empty((1, H, T, d), dtype=torch.int16, device="cuda")
+            v = torch.empty_like(k)
+            tq_synth.device_kv(w, k, v, B=1, H=H, d=d, n=T, b_offset=b0)
+            tq.tq_encode_append(cache.batch_slice(b0, 1), k.view(torch.bfloat16), v.view(torch.bfloat16), 0)
+            del k, v
+        return cache
+
+    w = tq_synth.WORKLOADS["decode"]
+    H, T = 8, 32769
+    for d, kb, vb, G in [(128, 8, 3, 8), (128, 4, 3, 8), (128, 4, 2, 8), (128, 8, 4, 8), (128, 5, 2, 8),
+                         (128, 8, 3, 4), (128, 8, 3, 16), (64, 8, 3, 8), (256, 8, 3, 8), (512, 4, 3, 4)]:
+        bpt = tq.tq_bytes_per_token_head(d, kb, vb)
+        B = max(1, round(4e8 / (H * T * bpt)))
+        cache = filled_cache(B, H, d, T, kb, vb, w)
+        q = torch.empty((B, G * H, d), dtype=torch.int16, device="cuda")
+        tq_synth.device_q(w, 0, q, B=B, QH=G * H, d=d)
+        qb = q.view(torch.bfloat16)
+        out = torch.empty((B, G * H, d), dtype=torch.float32, device="cuda")
+        ws = torch.empty(tq.tq_attention_workspace_bytes(cache, G * H, T), dtype=torch.uint8, device="cuda")
+        us = timed(lambda: tq.tq_decode_attention(cache, qb, T, out=out, workspace=ws))
+        path = "specialised" if (d, vb, G) == (128, 3, 8) and kb in (8, 4) else "generic"
+        emit("attention", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": kb, "vb": vb, "group": G, "kernel": path},
+             us, B * H * T * bpt + B * G * H * d * 6)
+        del cache, ws, out, q
+    # deferred fetch and un-rotation, row copies: prefill-shaped cache of 32768 rows
+    pw = tq_synth.WORKLOADS["prefill"]
+    B, H, T, d = 4, 8, 32768, 128
+    cache = filled_cache(B, H, d, T, 8, 3, pw)
+    vr = torch.empty((B, H, T, d), dtype=torch.bfloat16, device="cuda")
+    us = timed(lambda: tq.tq_decode_values_rotated(cache, 0, T, dtype=torch.bfloat16, out=vr))
+    emit("rotated_fetch", {"B": B, "kv_heads": H, "rows": T, "d": d, "vb": 3, "out": "bf16"}, us,
+         B * H * T * (48 + 8 + d * 2))
+    x = torch.randn((B * H * T // 4, d), dtype=torch.float32, device="cuda")
+    y = torch.empty_like(x)
+    us = timed(lambda: tq.tq_unrotate(x, out=y))
+    emit("unrotate", {"rows": x.shape[0], "d": d, "in": "fp32", "out": "fp32"}, us, 2 * x.numel() * 4)
+    del x, y, vr
+    snap = tq.Cache(B, H, d, T)
+    us = timed(lambda: tq.tq_cache_copy_rows(snap, 0, cache, 0, T))
+    emit("copy_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, 2 * B * H * T * 200)
+    us = timed(lambda: tq.tq_cache_clear_rows(snap, 0, T))
+    emit("clear_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, B * H * T * 200)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,7 +512,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="sequences of the decode step (smaller values for profiling captures)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="measure the paths beyond the headline step instead (one JSON line each)")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep()
+        return
     if args.warmup < 3:
         args.warmup = 3
     DECODE["B"] = args.decode_batch

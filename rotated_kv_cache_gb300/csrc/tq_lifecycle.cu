@@ -227,27 +227,33 @@ struct CopyParams {
     const uint8_t *src[5];  // null: write zeros
     uint8_t *dst[5];
     int64_t row_bytes[5];
-    int64_t src_row0_bh_stride, dst_row0_bh_stride;  // rows between (sequence, kv-head) blocks: the capacities
-    int64_t src_t0, dst_t0, n, BH;
-    int vec16[5];  // 1 when both segments start 16-byte aligned and their length is a multiple of 16
+    int64_t src_bh_rows, dst_bh_rows;  // rows between (sequence, kv-head) blocks: the capacities
+    int64_t src_t0, dst_t0;
+    uint32_t words[5];     // words per (sequence, kv-head) segment
+    FastDiv div_words[5];
+    uint32_t total[5];     // words of the plane over all segments (< 2^31)
+    int vec16[5];          // 16-byte words when both sides start 16-byte aligned and the length allows
 };
 
+// blockIdx.y = plane; the plane's (segment, word) space is walked grid-stride
 __global__ void __launch_bounds__(256) copy_rows_kernel(const __grid_constant__ CopyParams p)
 {
-    const int plane = blockIdx.z;
-    const int64_t rb = p.row_bytes[plane], len = p.n * rb;
+    const int plane = blockIdx.y;
+    const int64_t rb = p.row_bytes[plane];
     const uint8_t *src_plane = p.src[plane];
     uint8_t *dst_plane = p.dst[plane];
-    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nthr = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t bh = blockIdx.y; bh < p.BH; bh += gridDim.y) {
-        uint8_t *d = dst_plane + (bh * p.dst_row0_bh_stride + p.dst_t0) * rb;
-        const uint8_t *sp = src_plane ? src_plane + (bh * p.src_row0_bh_stride + p.src_t0) * rb : nullptr;
+    const uint32_t words = p.words[plane], total = p.total[plane];
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const uint32_t bh = fast_div(i, p.div_words[plane]), w = i - bh * words;
+        uint8_t *d = dst_plane + (bh * p.dst_bh_rows + p.dst_t0) * rb;
         if (p.vec16[plane]) {
-            for (int64_t i = tid; i < len / 16; i += nthr)
-                reinterpret_cast<uint4 *>(d)[i] = sp ? reinterpret_cast<const uint4 *>(sp)[i] : make_uint4(0, 0, 0, 0);
+            const uint4 v = src_plane ? reinterpret_cast<const uint4 *>(src_plane + (bh * p.src_bh_rows + p.src_t0) * rb)[w]
+                                      : make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(d)[w] = v;
         } else {
-            for (int64_t i = tid; i < len / 4; i += nthr)
-                reinterpret_cast<uint32_t *>(d)[i] = sp ? reinterpret_cast<const uint32_t *>(sp)[i] : 0u;
+            const uint32_t v = src_plane ? reinterpret_cast<const uint32_t *>(src_plane + (bh * p.src_bh_rows + p.src_t0) * rb)[w]
+                                         : 0u;
+            reinterpret_cast<uint32_t *>(d)[w] = v;
         }
     }
 }
@@ -286,24 +292,28 @@ cudaError_t launch_copy_rows(const CacheView &dst, int64_t dst_t0, const CacheVi
         sp[3] = src->v_codes;
         sp[4] = reinterpret_cast<const uint8_t *>(src->v_scale);
     }
-    p.src_row0_bh_stride = src ? src->cap : 0;
-    p.dst_row0_bh_stride = dst.cap;
+    p.src_bh_rows = src ? src->cap : 0;
+    p.dst_bh_rows = dst.cap;
     p.src_t0 = src_t0;
     p.dst_t0 = dst_t0;
-    p.n = n;
-    p.BH = (int64_t)dst.B * dst.H;
-    int64_t longest = 0;
+    const int64_t BH = (int64_t)dst.B * dst.H;
+    int64_t most = 0;
     for (int i = 0; i < 5; ++i) {
         p.src[i] = sp[i];
         p.dst[i] = dp[i];
         p.row_bytes[i] = rb[i];
-        // every (sequence, kv-head) segment starts at a multiple of cap * rb (cap % 16 == 0) plus t0 * rb
+        // a segment starts at a multiple of cap * rb (cap % 16 == 0) plus t0 * rb
         const bool a = (dst_t0 * rb[i]) % 16 == 0 && (!src || (src_t0 * rb[i]) % 16 == 0) && (n * rb[i]) % 16 == 0;
-        p.vec16[i] = a ? 1 : 0;
-        longest = longest > n * rb[i] ? longest : n * rb[i];
+        p.vec16[i] = a ? 1 : 0;  // every plane row is a multiple of 4 bytes, so 4-byte words always fit
+        const int64_t words = n * rb[i] / (a ? 16 : 4), total = words * BH;
+        if (words >= (int64_t(1) << 31) || total >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+        p.words[i] = (uint32_t)words;
+        p.div_words[i] = make_fastdiv(words > 0 ? (uint32_t)words : 1u);
+        p.total[i] = (uint32_t)total;
+        most = most > total ? most : total;
     }
-    const int64_t bx = imin64((longest / 4 + 255) / 256, 1024);
-    copy_rows_kernel<<<dim3((unsigned)(bx > 0 ? bx : 1), (unsigned)imin64(p.BH, 65535), 5), 256, 0, s>>>(p);
+    const int64_t blocks = imin64((most + 255) / 256, (int64_t)num_sms() * 8);
+    copy_rows_kernel<<<dim3((unsigned)(blocks > 0 ? blocks : 1), 5), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
