@@ -331,3 +331,17 @@ def attention(planes: Planes, q_bf16: np.ndarray, seq_len: int, softmax_scale: f
     if rc != 0:
         raise ValueError("oracle attention: bad arguments")
     return out
+
+
+
+def attention_multi(planes: Planes, q_bf16: np.ndarray, seq_len: int, softmax_scale: float | None = None) -> np.ndarray:
+    """M query rows per sequence: q bf16 bits [B][M][QH][d], the M newest cache
+    rows being the queries' own.  Query i attends causally to rows
+    [0, seq_len - M + i] -- the plain attention of each query over its visible
+    prefix (the page's multi-token forward shapes).  Returns float64 [B][M][QH][d]."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    M = q.shape[1]
+    out = np.zeros(q.shape, dtype=np.float64)
+    for i in range(M):
+        out[:, i] = attention(planes, np.ascontiguousarray(q[:, i]), seq_len - M + i + 1, softmax_scale)
+    return out

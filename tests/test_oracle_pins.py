@@ -489,3 +489,44 @@ def test_trim_then_reappend_equals_encoding_the_kept_and_new_tokens():
     oracle.encode(fresh, *keep)
     for a, b in zip(cache.arrays(), fresh.arrays()):
         assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- multi-token queries (causal)
+def _mt_planes(seed, B=1, H=2, d=64, T=24):
+    rng = np.random.default_rng(seed)
+    k = oracle.f32_to_bf16_bits(rng.standard_normal((B, H, T, d)).astype(np.float32)).reshape(B, H, T, d)
+    v = oracle.f32_to_bf16_bits(rng.standard_normal((B, H, T, d)).astype(np.float32)).reshape(B, H, T, d)
+    p = oracle.Planes(B, H, d, 8, 3, 32)
+    oracle.encode(p, k, v)
+    return p, rng
+
+
+def test_multi_token_one_query_is_decode_attention():
+    p, rng = _mt_planes(21)
+    q = oracle.f32_to_bf16_bits(rng.standard_normal((1, 1, 8, 64)).astype(np.float32)).reshape(1, 1, 8, 64)
+    assert np.array_equal(oracle.attention_multi(p, q, 20)[:, 0], oracle.attention(p, q[:, 0], 20))
+
+
+def test_multi_token_causality():
+    """Query i must not see rows past its own position: changing those rows
+    leaves it unchanged, while the last query (which sees them) changes."""
+    p, rng = _mt_planes(22)
+    M, T = 4, 20
+    q = oracle.f32_to_bf16_bits(rng.standard_normal((1, M, 8, 64)).astype(np.float32)).reshape(1, M, 8, 64)
+    base = oracle.attention_multi(p, q, T)
+    p.v_codes[:, :, T - 1] ^= 0x5A   # the newest row, visible to query M-1 only
+    p.k_codes[:, :, T - 1] ^= 0x33
+    moved = oracle.attention_multi(p, q, T)
+    assert np.array_equal(moved[:, :M - 1], base[:, :M - 1])
+    assert not np.array_equal(moved[:, M - 1], base[:, M - 1])
+
+
+def test_multi_token_first_query_sees_its_own_row():
+    """With one visible key the output is that row's value (closed form, T = 1)."""
+    p, rng = _mt_planes(23)
+    M = 3
+    q = oracle.f32_to_bf16_bits(rng.standard_normal((1, M, 8, 64)).astype(np.float32)).reshape(1, M, 8, 64)
+    out = oracle.attention_multi(p, q, M)          # query 0 sees row 0 only
+    _, v = oracle.decode(p, 0, 1)
+    for qh in range(8):
+        assert np.allclose(out[0, 0, qh], v[0, qh // 4, 0], rtol=0, atol=1e-6)
