@@ -451,10 +451,13 @@ def run_sweep():
             ts.append(a.elapsed_time(b) * 1e3 / reps)
         return statistics.median(ts)
 
-    def emit(kind_, config, us, nbytes):
+    def emit(kind_, config, us, nbytes, flops=None):
         gbs = nbytes / (us * 1e-6) / 1e9
-        print(json.dumps({"sweep": kind_, "config": config, "us": round(us, 2), "GB/s": round(gbs, 1),
-                          "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": kind}), flush=True)
+        line = {"sweep": kind_, "config": config, "us": round(us, 2), "GB/s": round(gbs, 1),
+                "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": kind}
+        if flops is not None:
+            line["TFLOP/s"] = round(flops / (us * 1e-6) / 1e12, 1)
+        print(json.dumps(line), flush=True)
 
     def filled_cache(B, H, d, T, kb, vb, w):
         cache = tq.Cache(B, H, d, T + (16 - T % 16) % 16, k_bits=kb, v_bits=vb)
@@ -483,6 +486,24 @@ def run_sweep():
         emit("attention", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": kb, "vb": vb, "group": G, "kernel": path},
              us, B * H * T * bpt + B * G * H * d * 6)
         del cache, ws, out, q
+    # multi-token attention: chunks of M = 4 and 128 query rows (the page's
+    # forward shapes) over a 32769-row cache.  The MMA work is 4 d flops per
+    # (column, cache row), a column being one (query row, q-head).
+    d, kb, vb, G, B = 128, 8, 3, 8, 8
+    cache = filled_cache(B, H, d, T, kb, vb, w)
+    bpt = tq.tq_bytes_per_token_head(d, kb, vb)
+    for M in (4, 128):
+        q = torch.empty((B, M * G * H, d), dtype=torch.int16, device="cuda")
+        tq_synth.device_q(w, 0, q, B=B, QH=M * G * H, d=d)
+        qb = q.view(torch.bfloat16).view(B, M, G * H, d)
+        out = torch.empty((B, M, G * H, d), dtype=torch.float32, device="cuda")
+        ws = torch.empty(tq.tq_multi_token_workspace_bytes(cache, G * H, M, T), dtype=torch.uint8, device="cuda")
+        us = timed(lambda: tq.tq_multi_token_attention(cache, qb, T, out=out, workspace=ws))
+        emit("multi_token_attention", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": kb, "vb": vb, "group": G,
+                                       "m_queries": M}, us, B * H * T * bpt + B * M * G * H * d * 6,
+             flops=4.0 * d * G * M * B * H * T)
+        del q, qb, out, ws
+    del cache
     # deferred fetch and un-rotation, row copies: prefill-shaped cache of 32768 rows
     pw = tq_synth.WORKLOADS["prefill"]
     B, H, T, d = 4, 8, 32768, 128

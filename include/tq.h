@@ -240,6 +240,37 @@ TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32
 TQ_API tq_status tq_decode_attention_noalloc(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
                                              float softmax_scale, float *out, tq_stream_t stream);
 
+/* Workspace bytes tq_multi_token_attention needs for these sizes (0 if invalid). */
+TQ_API size_t tq_multi_token_workspace_bytes(const tq_cache *cache, int32_t q_heads, int64_t m_queries,
+                                             int64_t seq_len);
+
+/*
+ * Causal attention for M query rows per sequence, the forward pass of a chunk
+ * of M tokens appended together (the page's multi-token forward shapes are
+ * M = 1, 4 and 128: "Packed-value decode fusion investigation"; chunked
+ * prefill and speculative verification take the same form).  The chunk's own
+ * rows are the cache's last M rows, appended first (tq_encode_append with
+ * t0 = seq_len - M, n = M); query row i (0-based) sees rows
+ * [0, seq_len - M + i], itself included and the later rows of the chunk not:
+ *   out[b][i][h] = sum_{t <= seq_len-M+i} softmax_t(q[b][i][h] . k_hat[b][h/G][t]
+ *                  * softmax_scale) v_hat[b][h/G][t]
+ * Same dequantise-on-fetch method, deferred un-rotation, fp32 accumulation
+ * and tolerance as tq_decode_attention, for every head_dim, bit pair and
+ * group size; M = 1 gives decode attention.  The cache rows of one kv-head are
+ * read once for up to 32 (query row, q-head) pairs at head_dim <= 128, 16 at
+ * 256 and 8 at 512.
+ *  q        device bf16 [batch][M][q_heads][d] contiguous, 16-byte aligned.
+ *  out      device fp32 [batch][M][q_heads][d] contiguous, 16-byte aligned.
+ *  workspace  device scratch of at least tq_multi_token_workspace_bytes(),
+ *           16-byte aligned; its contents need no initialisation.
+ * Errors: TQ_ERR_SHAPE if M < 1, M > seq_len, or batch * M * q_heads or
+ * num_kv_heads * ceil(M * G / 8) is too large for one launch (2^30 rows,
+ * 65535 column blocks); otherwise as tq_decode_attention.
+ */
+TQ_API tq_status tq_multi_token_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t m_queries,
+                                          int64_t seq_len, float softmax_scale, float *out, void *workspace,
+                                          size_t workspace_bytes, tq_stream_t stream);
+
 /* 1 if tq_decode_attention covers these parameters (every valid head_dim and
  * bit pair, group_size >= 1), else 0. */
 TQ_API int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bits, int32_t group_size);

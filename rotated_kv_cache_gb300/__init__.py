@@ -24,6 +24,7 @@ __all__ = [
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
     "tq_attention_supported", "tq_device_error", "tq_plane_bytes", "tq_decode_attention_noalloc",
     "tq_decode_values_rotated", "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows",
+    "tq_multi_token_workspace_bytes", "tq_multi_token_attention",
 ]
 
 HEAD_DIMS = (64, 128, 256, 512)
@@ -35,7 +36,8 @@ EXPORTS = (
     "tq_status_string", "tq_bytes_per_token_head", "tq_plane_bytes", "tq_sign_vector", "tq_codebook",
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
     "tq_attention_supported", "tq_device_error", "tq_decode_attention_noalloc", "tq_decode_values_rotated",
-    "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows",
+    "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows", "tq_multi_token_workspace_bytes",
+    "tq_multi_token_attention",
 )
 
 
@@ -88,9 +90,12 @@ def lib() -> ctypes.CDLL:
     so.tq_unrotate.argtypes = [_I32, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P]
     so.tq_cache_copy_rows.argtypes = [_CP, _I64, _CP, _I64, _I64, _P]
     so.tq_cache_clear_rows.argtypes = [_CP, _I64, _I64, _P]
+    so.tq_multi_token_workspace_bytes.restype = _SZ
+    so.tq_multi_token_workspace_bytes.argtypes = [_CP, _I32, _I64, _I64]
+    so.tq_multi_token_attention.argtypes = [_CP, _P, _I32, _I64, _I64, ctypes.c_float, _P, _P, _SZ, _P]
     for name in EXPORTS:
         if name not in ("tq_status_string", "tq_bytes_per_token_head", "tq_attention_workspace_bytes",
-                        "tq_attention_supported"):
+                        "tq_attention_supported", "tq_multi_token_workspace_bytes"):
             getattr(so, name).restype = ctypes.c_int
     so.tq_attention_supported.restype = ctypes.c_int
     return so
@@ -320,6 +325,37 @@ def tq_decode_attention_noalloc(cache: Cache, q: torch.Tensor, seq_len: int, sof
     s = cache.struct()
     _check(lib().tq_decode_attention_noalloc(ctypes.byref(s), q.data_ptr(), int(QH), int(seq_len), scale,
                                              out.data_ptr(), _stream(stream)), "tq_decode_attention_noalloc")
+    return out
+
+
+def tq_multi_token_workspace_bytes(cache: Cache, q_heads: int, m_queries: int, seq_len: int) -> int:
+    s = cache.struct()
+    return int(lib().tq_multi_token_workspace_bytes(ctypes.byref(s), int(q_heads), int(m_queries), int(seq_len)))
+
+
+def tq_multi_token_attention(cache: Cache, q: torch.Tensor, seq_len: int, softmax_scale: float | None = None,
+                             out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """Causal attention of M query rows per sequence over cache rows [0, seq_len):
+    q bf16 [B][M][QH][d] -> fp32 [B][M][QH][d]; row i sees rows [0, seq_len - M + i]."""
+    _require_cuda(q)
+    if q.dtype != torch.bfloat16 or q.dim() != 4 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bfloat16 [batch][m_queries][q_heads][head_dim]")
+    B, M, QH, d = q.shape
+    if B != cache.batch or d != cache.head_dim:
+        raise ValueError("q does not match the cache")
+    if out is None:
+        out = torch.empty((B, M, QH, d), dtype=torch.float32, device=q.device)
+    need = tq_multi_token_workspace_bytes(cache, QH, M, seq_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    scale = (1.0 / d ** 0.5) if softmax_scale is None else float(softmax_scale)
+    s = cache.struct()
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().tq_multi_token_attention(ctypes.byref(s), q.data_ptr(), int(QH), int(M), int(seq_len), scale,
+                                          out.data_ptr(), ws_ptr, ws_bytes, _stream(stream)),
+           "tq_multi_token_attention")
     return out
 
 

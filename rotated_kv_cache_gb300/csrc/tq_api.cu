@@ -253,7 +253,7 @@ bool specialised(const tq_cache *c, int32_t q_heads)
 size_t workspace_bytes(const tq_cache *c, int32_t q_heads, int64_t seq_len)
 {
     return specialised(c, q_heads) ? tq::attention_workspace_bytes(view(c), q_heads, seq_len)
-                                   : tq::attention_generic_workspace_bytes(view(c), q_heads, seq_len);
+                                   : tq::attention_generic_workspace_bytes(view(c), q_heads, 1, seq_len);
 }
 }  // namespace
 
@@ -283,7 +283,43 @@ tq_status tq_decode_attention(const tq_cache *c, const void *q, int32_t q_heads,
     if (specialised(c, q_heads))
         return cuda_status(tq::launch_attention(view(c), qh, q_heads, seq_len, scale, out, ws, ws_bytes, (cudaStream_t)stream));
     return cuda_status(
-        tq::launch_attention_generic(view(c), qh, q_heads, seq_len, scale, out, ws, ws_bytes, (cudaStream_t)stream));
+        tq::launch_attention_generic(view(c), qh, q_heads, 1, seq_len, scale, out, ws, ws_bytes, (cudaStream_t)stream));
+}
+
+namespace {
+tq_status check_multi(const tq_cache *c, int32_t q_heads, int64_t m, int64_t seq_len)
+{
+    if (q_heads < 1 || q_heads % c->num_kv_heads != 0) return TQ_ERR_SHAPE;
+    if (seq_len < 1 || m < 1 || m > seq_len) return TQ_ERR_SHAPE;
+    if (seq_len > c->capacity) return TQ_ERR_CAPACITY;
+    const int64_t group = q_heads / c->num_kv_heads;
+    if ((int64_t)c->batch * m * q_heads > (int64_t(1) << 30)) return TQ_ERR_SHAPE;
+    if ((int64_t)c->num_kv_heads * ((m * group + 7) / 8) > 65535) return TQ_ERR_SHAPE;
+    return TQ_OK;
+}
+}  // namespace
+
+size_t tq_multi_token_workspace_bytes(const tq_cache *c, int32_t q_heads, int64_t m, int64_t seq_len)
+{
+    if (check_cache(c) != TQ_OK || check_multi(c, q_heads, m, seq_len) != TQ_OK) return 0;
+    return tq::attention_generic_workspace_bytes(view(c), q_heads, m, seq_len);
+}
+
+tq_status tq_multi_token_attention(const tq_cache *c, const void *q, int32_t q_heads, int64_t m, int64_t seq_len,
+                                   float scale, float *out, void *ws, size_t ws_bytes, tq_stream_t stream)
+{
+    tq_status st = check_cache(c);
+    if (st != TQ_OK) return st;
+    if (!q || !out) return TQ_ERR_NULL;
+    st = check_multi(c, q_heads, m, seq_len);
+    if (st != TQ_OK) return st;
+    if (!aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
+    const size_t need = tq::attention_generic_workspace_bytes(view(c), q_heads, m, seq_len);
+    if (need == 0) return TQ_ERR_CUDA;  // the occupancy query failed
+    if (!ws || ws_bytes < need) return TQ_ERR_WORKSPACE;
+    if (!aligned16(ws)) return TQ_ERR_ALIGN;
+    return cuda_status(tq::launch_attention_generic(view(c), static_cast<const uint16_t *>(q), q_heads, m, seq_len,
+                                                    scale, out, ws, ws_bytes, (cudaStream_t)stream));
 }
 
 tq_status tq_decode_attention_noalloc(const tq_cache *c, const void *q, int32_t q_heads, int64_t seq_len,

@@ -1,25 +1,32 @@
-// tq_attention_generic.cu -- fused dequantise-on-fetch decode attention for
-// every head_dim, bit pair and GQA group size.  The kernel in
-// tq_attention.cu is the specialised path for head_dim 128, 8- or 4-bit keys,
-// 3-bit values and groups of 8 q-heads; this one covers the rest with the
-// same method and the same tolerance.
+// tq_attention_generic.cu -- fused dequantise-on-fetch attention for every
+// head_dim, bit pair and GQA group size, with one or several query rows per
+// sequence.  The kernel in tq_attention.cu is the specialised one-row path for
+// head_dim 128, 8- or 4-bit keys, 3-bit values and groups of 8 q-heads; this
+// one covers the rest with the same method and the same tolerance.
 //
 // Method: mlx-bun "TurboQuant -- rotation-based quantization", Part A:
 // "Architecture in mlx-bun" (attention reads the dequantised window),
-// "Algorithm" (key (code + zero) * scale, value centroid[code] * rms) and
+// "Algorithm" (key (code + zero) * scale, value centroid[code] * rms),
 // "Deferred inverse FWHT" (the weighted sum is formed in the rotated domain
-// and un-rotated once per query row).
+// and un-rotated once per query row), and "Packed-value decode fusion
+// investigation" (forward passes that append M = 1, 4 or 128 rows and attend
+// to the cache including them: query row i of M sees the rows before
+// seq_len - M + i + 1).
 //
 // Design, as in the specialised kernel: split-KV CTAs stream 64-token stages
 // through a shared-memory ring (bulk copies completing on an mbarrier; the
 // last warp to finish a stage refills it); each of the 4 warps takes 16
-// tokens.  QK^T and PV run on mma.sync m16n8k16 (f16 in, f32 accumulate) with
-// N = 8 q-heads per CTA; groups larger than 8 use several CTAs (head blocks),
-// smaller ones mask the unused columns.  Key codes enter the MMA as exact f16
-// integers (1024 + code) and the per-group affine is applied to the scores;
-// value codes are looked up in an f16 centroid table and the rms is folded
-// into P.  Code widths are run-time values here (one kernel per head_dim),
-// extracted with funnel shifts from the packed rows.
+// tokens.  QK^T and PV run on mma.sync m16n8k16 (f16 in, f32 accumulate).
+// The MMA's N runs over "columns", a column being one (query row, q-head) of
+// the kv-head's G * M; a CTA takes NB blocks of 8 columns (NB = 1, 2 or 4 by
+// head_dim), so each dequantised key and value fragment feeds NB MMAs and a
+// kv-head whose columns fit in one CTA reads its cache rows once.  More
+// columns use several CTAs (column blocks); unused columns are masked.  Key
+// codes enter the MMA as exact f16 integers (1024 + code) and the per-group
+// affine is applied to the scores; value codes are looked up in an f16
+// centroid table and the rms is folded into P.  Code widths are run-time
+// values here (one kernel per head_dim and NB), extracted with funnel shifts
+// from the packed rows.
 #include <cuda.h>
 
 #include "tq_common.cuh"
@@ -37,12 +44,13 @@ constexpr int gMaxStages = 3;
 struct GenParams {
     const uint8_t *k_codes, *v_codes;
     const uint16_t *k_scale, *k_zero, *v_scale;
-    const uint16_t *q;  // [B][QH][D] bf16
-    float *part_o;      // [B][H][HB][S][8][D]
-    float *part_ml;     // [B][H][HB][S][8][2]
+    const uint16_t *q;  // [B][M][QH][D] bf16
+    float *part_o;      // [B][H][HB][S][CB][D]
+    float *part_ml;     // [B][H][HB][S][CB][2]
     uint32_t *err;
-    int H, QH, G, HB, splits, kb, vb, stages;
+    int H, QH, G, M, cols, HB, splits, kb, vb, stages;  // cols = G * M columns per kv-head
     int64_t cap, seq_len, tokens_per_split;
+    int64_t base0;                                 // seq_len - M + 1: query row i sees rows [0, base0 + i)
     int rbk, rbv;                                  // packed row bytes of keys and values
     int off_ks, off_kz, off_vs, off_v, stage_bytes;  // stage layout (keys at 0)
     float scale_log2, koff;                        // softmax scale * log2(e); f16 offset of a key code
@@ -146,20 +154,25 @@ __device__ __forceinline__ void value_quad(uint32_t row, int G, int g, int vb, u
     for (int k = 0; k < 4; ++k) h[k] = g_lds16(lut + 2 * ((x >> (k * vb)) & mask));
 }
 
-template <int D>
+template <int D, int NB>
 struct GGeo {
     static constexpr int NG = D / 32;
     static constexpr int KS = D / 16;                       // k-steps of QK^T, m-tiles of PV
-    static constexpr int QF = gN * KS * 4 * 8;               // q fragments: [head][k-step][c] x (b0, b1)
-    static constexpr int QS = (NG + 1) * gN * 4;             // group sums of the f16 q, then per-head score scale
-    static constexpr int MERGE = gW * gN * (D + 2) * 4;      // per-warp partials (reuse the ring)
+    static constexpr int CB = gN * NB;                      // columns per CTA
+    static constexpr int QF = CB * KS * 4 * 8;              // q fragments: [column][k-step][c] x (b0, b1)
+    static constexpr int QS = (NG + 1) * CB * 4;            // group sums of the f16 q, then per-column score scale
+    static constexpr int MERGE = gW * CB * (D + 2) * 4;     // per-warp partials (reuse the ring)
+    // resident CTAs per SM the register budget is sized for: the output
+    // accumulators take D * NB / 4 registers a thread
+    static constexpr int MIN_BLOCKS = D >= 512 ? 1 : (D * NB / 4 <= 32 ? 3 : 2);
 };
 
-template <int D>
-__global__ void __launch_bounds__(gThreads, D >= 512 ? 1 : D >= 256 ? 2 : 3)
+template <int D, int NB>
+__global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
     attn_generic_kernel(const __grid_constant__ GenParams p)
 {
-    using A = GGeo<D>;
+    using A = GGeo<D, NB>;
+    constexpr int CB = A::CB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int ring = p.stages * p.stage_bytes > A::MERGE ? p.stages * p.stage_bytes : A::MERGE;
@@ -175,8 +188,13 @@ __global__ void __launch_bounds__(gThreads, D >= 512 ? 1 : D >= 256 ? 2 : 3)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, h = blockIdx.y / p.HB, hb = blockIdx.y - h * p.HB, b = blockIdx.z;
     const int64_t bh = (int64_t)b * p.H + h;
+    // columns col0 .. col0 + CB - 1; column col is query row col / G, q-head
+    // h G + col % G; query row i sees cache rows [0, base0 + i)
+    const int col0 = hb * CB;
+    const int col_last = (p.cols < col0 + CB ? p.cols : col0 + CB) - 1;
+    const int64_t lim_lo = p.base0 + col0 / p.G, lim_hi = p.base0 + col_last / p.G;
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
-    const int64_t t_end = imin64(p.seq_len, t_begin + p.tokens_per_split);
+    const int64_t t_end = imin64(lim_hi, t_begin + p.tokens_per_split);
     const int n_stages = t_end > t_begin ? (int)((t_end - t_begin + gT - 1) / gT) : 0;
     const int NG = D / 32;
 
@@ -203,21 +221,24 @@ __global__ void __launch_bounds__(gThreads, D >= 512 ? 1 : D >= 256 ? 2 : 3)
     }
     for (int i = threadIdx.x; i < (1 << p.vb); i += blockDim.x) lut[i] = p.cen[i];
 
-    // ---------------------------------------------------------------- q of the CTA's 8 heads
-    // Warp w prepares heads 2w, 2w+1; lane l holds dims 4 (l % 16) + 64 j + {0..3}
-    // of head 2w + l / 16.  Each head is scaled by a power of two so its largest
-    // |q| lands in [2^14, 2^15) before the f16 rounding; heads past the group
-    // are zero.
-    {
-        const int n = 2 * warp + (lane >> 4), l16 = lane & 15;
-        const int qh = h * p.G + hb * gN + n;
-        const bool real = hb * gN + n < p.G;
+    // ---------------------------------------------------------------- q of the CTA's columns
+    // Per block of 8 columns, warp w prepares columns 2w, 2w+1; lane l holds
+    // dims 4 (l % 16) + 64 j + {0..3} of column 2w + l / 16.  Each column is
+    // scaled by a power of two so its largest |q| lands in [2^14, 2^15) before
+    // the f16 rounding; columns past the last are zero.
+#pragma unroll 1
+    for (int nb = 0; nb < NB; ++nb) {
+        const int n = nb * gN + 2 * warp + (lane >> 4), l16 = lane & 15;
+        const int col = col0 + n;
+        const bool real = col < p.cols;
+        const int qi = real ? col / p.G : 0, qw = real ? col - qi * p.G : 0;
+        const uint16_t *qrow = p.q + (((int64_t)b * p.M + qi) * p.QH + (int64_t)h * p.G + qw) * D;
         float qv[D / 64][4];
         float mx = 0.0f;
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
             uint2 w = make_uint2(0u, 0u);
-            if (real) w = *reinterpret_cast<const uint2 *>(p.q + ((int64_t)b * p.QH + qh) * D + 64 * j + 4 * l16);
+            if (real) w = *reinterpret_cast<const uint2 *>(qrow + 64 * j + 4 * l16);
             qv[j][0] = bf16_lo(w.x); qv[j][1] = bf16_hi(w.x); qv[j][2] = bf16_lo(w.y); qv[j][3] = bf16_hi(w.y);
 #pragma unroll
             for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qv[j][i]));
@@ -248,22 +269,29 @@ __global__ void __launch_bounds__(gThreads, D >= 512 ? 1 : D >= 256 ? 2 : 3)
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             s += __shfl_xor_sync(0xffffffffu, s, 4);
-            if ((l16 & 7) == 0) qsum[G * gN + n] = s;
+            if ((l16 & 7) == 0) qsum[G * CB + n] = s;
         }
-        if (l16 == 0) qsum[NG * gN + n] = ldexpf(1.0f, -e) * p.scale_log2;  // stored after the sums
+        if (l16 == 0) qsum[NG * CB + n] = ldexpf(1.0f, -e) * p.scale_log2;  // stored after the sums
     }
     __syncthreads();
 
     const int g = lane >> 2, c = lane & 3;
-    const float ie0 = qsum[NG * gN + 2 * c], ie1 = qsum[NG * gN + 2 * c + 1];
-    float o[A::KS][4];
+    float o[NB][A::KS][4];
 #pragma unroll
-    for (int i = 0; i < A::KS; ++i)
+    for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+        for (int i = 0; i < A::KS; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[nb][i][j] = 0.0f;
+    float m_run[NB][2], l_run[NB][2];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        m_run[nb][0] = m_run[nb][1] = -INFINITY;
+        l_run[nb][0] = l_run[nb][1] = 0.0f;
+    }
     const int r0 = 16 * warp + g, r1 = r0 + 8;
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
+    constexpr int QF_NB = gN * A::KS * 4 * 8;  // bytes of q fragments per block of 8 columns
     const uint32_t qf_lane = smem_addr(qf) + (g * A::KS * 4 + c) * 8, lut_a = smem_addr(lut);
 
     bool ok = true;
@@ -276,88 +304,132 @@ __global__ void __launch_bounds__(gThreads, D >= 512 ? 1 : D >= 256 ? 2 : 3)
         const uint32_t st = smem_addr(stages + slot * p.stage_bytes);
         const int64_t tile_t0 = t_begin + (int64_t)s * gT + 16 * warp;
 
-        // ---------------- S = Q K^T, group by group, with the group affine
-        float S[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+        // ---------------- S = Q K^T, group by group, with the group affine;
+        // the dequantised key fragments serve every block of columns
+        float S[NB][2][2];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) S[nb][0][0] = S[nb][0][1] = S[nb][1][0] = S[nb][1][1] = 0.0f;
 #pragma unroll 1
         for (int G = 0; G < A::NG; ++G) {
             uint32_t k0[4], k1[4];
             key_pairs(st + r0 * p.rbk, G, c, p.kb, k0);
             key_pairs(st + r1 * p.rbk, G, c, p.kb, k1);
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const uint2 bq = g_lds64(qf_lane + (2 * G + jj) * 32);
-                g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq.x, bq.y);
-            }
             const float sc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (r0 * NG + G) * 2));
             const float sc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (r1 * NG + G) * 2));
             const float zc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (r0 * NG + G) * 2)) - p.koff;
             const float zc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (r1 * NG + G) * 2)) - p.koff;
-            const float qs0 = qsum[G * gN + 2 * c], qs1 = qsum[G * gN + 2 * c + 1];
-            S[0][0] = fmaf(sc0, fmaf(zc0, qs0, acc[0]), S[0][0]);
-            S[0][1] = fmaf(sc0, fmaf(zc0, qs1, acc[1]), S[0][1]);
-            S[1][0] = fmaf(sc1, fmaf(zc1, qs0, acc[2]), S[1][0]);
-            S[1][1] = fmaf(sc1, fmaf(zc1, qs1, acc[3]), S[1][1]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const uint2 bq = g_lds64(qf_lane + nb * QF_NB + (2 * G + jj) * 32);
+                    g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq.x, bq.y);
+                }
+                const float qs0 = qsum[G * CB + nb * gN + 2 * c], qs1 = qsum[G * CB + nb * gN + 2 * c + 1];
+                S[nb][0][0] = fmaf(sc0, fmaf(zc0, qs0, acc[0]), S[nb][0][0]);
+                S[nb][0][1] = fmaf(sc0, fmaf(zc0, qs1, acc[1]), S[nb][0][1]);
+                S[nb][1][0] = fmaf(sc1, fmaf(zc1, qs0, acc[2]), S[nb][1][0]);
+                S[nb][1][1] = fmaf(sc1, fmaf(zc1, qs1, acc[3]), S[nb][1][1]);
+            }
         }
-        S[0][0] *= ie0; S[1][0] *= ie0;
-        S[0][1] *= ie1; S[1][1] *= ie1;
-        if (tile_t0 + 16 > t_end) {
-            if (tile_t0 + g >= t_end) S[0][0] = S[0][1] = -INFINITY;
-            if (tile_t0 + g + 8 >= t_end) S[1][0] = S[1][1] = -INFINITY;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const float ie0 = qsum[NG * CB + nb * gN + 2 * c], ie1 = qsum[NG * CB + nb * gN + 2 * c + 1];
+            S[nb][0][0] *= ie0; S[nb][1][0] *= ie0;
+            S[nb][0][1] *= ie1; S[nb][1][1] *= ie1;
         }
-        // ---------------- online softmax (base 2), heads 2c, 2c+1
-        float pr[2][2];
-        const bool raise = S[0][0] > m_run[0] || S[1][0] > m_run[0] || S[0][1] > m_run[1] || S[1][1] > m_run[1] ||
-                           m_run[0] == -INFINITY || m_run[1] == -INFINITY;
+        // causal mask: row t is hidden from query row i when t >= base0 + i
+        // (this also hides every row past t_end, which is at most the last
+        // column's limit, or the split's end when the tile stops there)
+        if (tile_t0 + 16 > lim_lo) {
+            const int64_t ta = tile_t0 + g - p.base0, tb = ta + 8;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int col = col0 + nb * gN + 2 * c + j;
+                    const int64_t qi = col < p.cols ? col / p.G : p.M - 1;
+                    if (ta >= qi) S[nb][0][j] = -INFINITY;
+                    if (tb >= qi) S[nb][1][j] = -INFINITY;
+                }
+        }
+        // ---------------- online softmax (base 2), columns 2c, 2c+1 of each block
+        float pr[NB][2][2];
+        bool raise = false;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                raise |= S[nb][0][j] > m_run[nb][j] || S[nb][1][j] > m_run[nb][j] || m_run[nb][j] == -INFINITY;
         if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mt = fmaxf(S[0][j], S[1][j]);
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-                const float mn = fmaxf(m_run[j], mt);
-                const float mu = mn == -INFINITY ? 0.0f : mn;
-                const float alpha = g_ex2(m_run[j] - mu);
-                m_run[j] = mn;
-                pr[0][j] = g_ex2(S[0][j] - mu);
-                pr[1][j] = g_ex2(S[1][j] - mu);
-                l_run[j] = l_run[j] * alpha + pr[0][j] + pr[1][j];
+            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-                for (int mt2 = 0; mt2 < A::KS; ++mt2) {
-                    o[mt2][j] *= alpha;
-                    o[mt2][2 + j] *= alpha;
+                for (int j = 0; j < 2; ++j) {
+                    float mt = fmaxf(S[nb][0][j], S[nb][1][j]);
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                    const float mn = fmaxf(m_run[nb][j], mt);
+                    const float mu = mn == -INFINITY ? 0.0f : mn;
+                    const float alpha = g_ex2(m_run[nb][j] - mu);
+                    m_run[nb][j] = mn;
+                    pr[nb][0][j] = g_ex2(S[nb][0][j] - mu);
+                    pr[nb][1][j] = g_ex2(S[nb][1][j] - mu);
+                    l_run[nb][j] = l_run[nb][j] * alpha + pr[nb][0][j] + pr[nb][1][j];
+#pragma unroll
+                    for (int mt2 = 0; mt2 < A::KS; ++mt2) {
+                        o[nb][mt2][j] *= alpha;
+                        o[nb][mt2][2 + j] *= alpha;
+                    }
                 }
-            }
         } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                pr[0][j] = g_ex2(S[0][j] - m_run[j]);
-                pr[1][j] = g_ex2(S[1][j] - m_run[j]);
-                l_run[j] += pr[0][j] + pr[1][j];
-            }
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    pr[nb][0][j] = g_ex2(S[nb][0][j] - m_run[nb][j]);
+                    pr[nb][1][j] = g_ex2(S[nb][1][j] - m_run[nb][j]);
+                    l_run[nb][j] += pr[nb][0][j] + pr[nb][1][j];
+                }
         }
-        const uint32_t pt0 = g_trans(g_pack_f16x2(pr[0][0], pr[0][1]));  // tokens 2c, 2c+1; head g
-        const uint32_t pt1 = g_trans(g_pack_f16x2(pr[1][0], pr[1][1]));  // tokens 2c+8, 2c+9
+        uint32_t pt0[NB], pt1[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            pt0[nb] = g_trans(g_pack_f16x2(pr[nb][0][0], pr[nb][0][1]));  // tokens 2c, 2c+1; column g
+            pt1[nb] = g_trans(g_pack_f16x2(pr[nb][1][0], pr[nb][1][1]));  // tokens 2c+8, 2c+9
+        }
         bool vlive[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) vlive[q] = tile_t0 + (vr[q] - 16 * warp) < t_end;
-        // ---------------- O^T += V^T (P * rms)^T, group by group
+        // ---------------- O^T += V^T (P * rms)^T, group by group; the value
+        // fragments serve every block of columns
 #pragma unroll
         for (int G = 0; G < A::NG; ++G) {
             uint32_t sv[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) sv[q] = vlive[q] ? g_lds16(st + p.off_vs + (vr[q] * NG + G) * 2) : 0u;
-            const uint32_t b0 = g_hmul2(pt0, sv[0] | (sv[1] << 16)), b1 = g_hmul2(pt1, sv[2] | (sv[3] << 16));
+            const uint32_t sv01 = sv[0] | (sv[1] << 16), sv23 = sv[2] | (sv[3] << 16);
             uint32_t hv[4][4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) value_quad(st + p.off_v + vr[q] * p.rbv, G, g, p.vb, lut_a, hv[q]);
+            uint32_t a[2][4];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 // rows g, g+8 of the m-tile: dims 32G + 4g + 2 half + {0, 1}
                 const int r = 2 * half;
-                g_mma(o[2 * G + half], hv[0][r] | (hv[1][r] << 16), hv[0][r + 1] | (hv[1][r + 1] << 16),
-                      hv[2][r] | (hv[3][r] << 16), hv[2][r + 1] | (hv[3][r + 1] << 16), b0, b1);
+                a[half][0] = hv[0][r] | (hv[1][r] << 16);
+                a[half][1] = hv[0][r + 1] | (hv[1][r + 1] << 16);
+                a[half][2] = hv[2][r] | (hv[3][r] << 16);
+                a[half][3] = hv[2][r + 1] | (hv[3][r + 1] << 16);
+            }
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const uint32_t b0 = g_hmul2(pt0[nb], sv01), b1 = g_hmul2(pt1[nb], sv23);
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+                    g_mma(o[nb][2 * G + half], a[half][0], a[half][1], a[half][2], a[half][3], b0, b1);
             }
         }
         __syncwarp();
@@ -372,101 +444,109 @@ __global__ void __launch_bounds__(gThreads, D >= 512 ? 1 : D >= 256 ? 2 : 3)
     __syncthreads();
 
     // ---------------------------------------------------------------- merge the warps
+    float *mw = merge + warp * CB * (D + 2);  // [column][D] o, then [column] m, [column] l
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
-    }
-    float *mw = merge + warp * gN * (D + 2);  // [head][D] o, then [head] m, [head] l
-#pragma unroll
-    for (int mt = 0; mt < A::KS; ++mt) {
-        const int G = mt >> 1, half = mt & 1;
-        const int d0 = 32 * G + 4 * g + 2 * half;
+    for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            mw[(2 * c + j) * D + d0] = o[mt][j];
-            mw[(2 * c + j) * D + d0 + 1] = o[mt][2 + j];
+            l_run[nb][j] += __shfl_xor_sync(0xffffffffu, l_run[nb][j], 4);
+            l_run[nb][j] += __shfl_xor_sync(0xffffffffu, l_run[nb][j], 8);
+            l_run[nb][j] += __shfl_xor_sync(0xffffffffu, l_run[nb][j], 16);
         }
-    }
-    if (g == 0) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            mw[gN * D + 2 * c + j] = ok ? m_run[j] : -INFINITY;
-            mw[gN * D + gN + 2 * c + j] = ok ? l_run[j] : 0.0f;
+        for (int mt = 0; mt < A::KS; ++mt) {
+            const int G = mt >> 1, half = mt & 1;
+            const int d0 = 32 * G + 4 * g + 2 * half;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                mw[(nb * gN + 2 * c + j) * D + d0] = o[nb][mt][j];
+                mw[(nb * gN + 2 * c + j) * D + d0 + 1] = o[nb][mt][2 + j];
+            }
+        }
+        if (g == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                mw[CB * D + nb * gN + 2 * c + j] = ok ? m_run[nb][j] : -INFINITY;
+                mw[CB * D + CB + nb * gN + 2 * c + j] = ok ? l_run[nb][j] : 0.0f;
+            }
         }
     }
     __syncthreads();
-    // thread -> (head hh, a D/16 slice of dims)
+    // thread -> (column hh, a D/16 slice of dims), one block of 8 columns at a time
     constexpr int PER = D / 16;
-    const int hh = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * PER;
-    float mmax = -INFINITY;
+    const int d0 = (threadIdx.x & 15) * PER;
+#pragma unroll 1
+    for (int nb = 0; nb < NB; ++nb) {
+        const int hh = nb * gN + (threadIdx.x >> 4);
+        float mmax = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < gW; ++w) mmax = fmaxf(mmax, merge[w * gN * (D + 2) + gN * D + hh]);
-    const float mu = mmax == -INFINITY ? 0.0f : mmax;
-    float ov[PER], lsum = 0.0f;
+        for (int w = 0; w < gW; ++w) mmax = fmaxf(mmax, merge[w * CB * (D + 2) + CB * D + hh]);
+        const float mu = mmax == -INFINITY ? 0.0f : mmax;
+        float ov[PER], lsum = 0.0f;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) ov[i] = 0.0f;
+        for (int i = 0; i < PER; ++i) ov[i] = 0.0f;
 #pragma unroll
-    for (int w = 0; w < gW; ++w) {
-        const float *m2 = merge + w * gN * (D + 2);
-        const float wt = g_ex2(m2[gN * D + hh] - mu);
-        lsum += m2[gN * D + gN + hh] * wt;
+        for (int w = 0; w < gW; ++w) {
+            const float *m2 = merge + w * CB * (D + 2);
+            const float wt = g_ex2(m2[CB * D + hh] - mu);
+            lsum += m2[CB * D + CB + hh] * wt;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) ov[i] += m2[hh * D + d0 + i] * wt;
-    }
-    const int64_t pidx = ((bh * p.HB + hb) * p.splits + split) * gN + hh;
-    float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * D + d0);
+            for (int i = 0; i < PER; ++i) ov[i] += m2[hh * D + d0 + i] * wt;
+        }
+        const int64_t pidx = ((bh * p.HB + hb) * p.splits + split) * CB + hh;
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * D + d0);
 #pragma unroll
-    for (int i = 0; i < PER / 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
-    if ((threadIdx.x & 15) == 0) {
-        p.part_ml[2 * pidx] = mmax;
-        p.part_ml[2 * pidx + 1] = lsum;
+        for (int i = 0; i < PER / 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+        if ((threadIdx.x & 15) == 0) {
+            p.part_ml[2 * pidx] = mmax;
+            p.part_ml[2 * pidx + 1] = lsum;
+        }
     }
 }
 
 // ---------------------------------------------------------------- combine + deferred un-rotation
 struct GenCombineParams {
     const float *part_o, *part_ml;
-    float *out;  // [B][QH][D]
-    int H, QH, G, HB, splits, rows;
+    float *out;  // [B][M][QH][D]
+    int H, QH, G, M, HB, CB, splits, rows;
     float inv_sqrt_d;
 };
 
-// one warp per (sequence, q-head); lane holds dims PER*lane .. +PER-1
+// one warp per (sequence, query row, q-head); lane holds dims PER*lane .. +PER-1
 template <int D>
 __global__ void __launch_bounds__(256) attn_generic_combine(const __grid_constant__ GenCombineParams p)
 {
     constexpr int PER = D / 32;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= p.rows) return;
-    const int b = row / p.QH, qh = row % p.QH;
-    const int h = qh / p.G, w = qh % p.G, hb = w / gN, n = w % gN;
+    const int per_seq = p.M * p.QH;
+    const int b = row / per_seq, rem = row - b * per_seq, i = rem / p.QH, qh = rem - i * p.QH;
+    const int h = qh / p.G, col = i * p.G + (qh - h * p.G), hb = col / p.CB, n = col - hb * p.CB;
     const int64_t base = (((int64_t)b * p.H + h) * p.HB + hb) * p.splits;
     float mmax = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * gN + n)]);
+    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * p.CB + n)]);
     const float mu = mmax == -INFINITY ? 0.0f : mmax;
     float x[PER], l = 0.0f;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) x[i] = 0.0f;
+    for (int k = 0; k < PER; ++k) x[k] = 0.0f;
     for (int s = 0; s < p.splits; ++s) {
-        const int64_t pi = (base + s) * gN + n;
+        const int64_t pi = (base + s) * p.CB + n;
         const float wt = g_ex2(p.part_ml[2 * pi] - mu);
         l += p.part_ml[2 * pi + 1] * wt;
         const float *src = p.part_o + pi * D + PER * lane;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) x[i] += src[i] * wt;
+        for (int k = 0; k < PER; ++k) x[k] += src[k] * wt;
     }
     const float inv_l = 1.0f / l;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) x[i] *= inv_l;
+    for (int k = 0; k < PER; ++k) x[k] *= inv_l;
     // inverse transform in Sylvester order: log2(PER) stages in-lane, 5 across lanes
 #pragma unroll
     for (int hs = 1; hs < PER; hs <<= 1)
 #pragma unroll
-        for (int i = 0; i < PER; i += 2 * hs)
+        for (int k = 0; k < PER; k += 2 * hs)
 #pragma unroll
-            for (int j = i; j < i + hs; ++j) {
+            for (int j = k; j < k + hs; ++j) {
                 const float a = x[j], bb = x[j + hs];
                 x[j] = a + bb;
                 x[j + hs] = a - bb;
@@ -475,39 +555,50 @@ __global__ void __launch_bounds__(256) attn_generic_combine(const __grid_constan
     for (int m = 1; m < 32; m <<= 1) {
         const bool upper = (lane & m) != 0;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = upper ? other - x[i] : x[i] + other;
+        for (int k = 0; k < PER; ++k) {
+            const float other = __shfl_xor_sync(0xffffffffu, x[k], m);
+            x[k] = upper ? other - x[k] : x[k] + other;
         }
     }
-    float *dst = p.out + ((int64_t)b * p.QH + qh) * D + PER * lane;
+    float *dst = p.out + (int64_t)row * D + PER * lane;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) dst[i] = x[i] * (sign_negative(PER * lane + i) ? -p.inv_sqrt_d : p.inv_sqrt_d);
+    for (int k = 0; k < PER; ++k) dst[k] = x[k] * (sign_negative(PER * lane + k) ? -p.inv_sqrt_d : p.inv_sqrt_d);
 }
 
 // ---------------------------------------------------------------- host side
 struct GenPlan {
-    int splits, stages, stage_bytes, smem;
+    int nb, hb, splits, stages, stage_bytes, smem;
     int64_t tokens_per_split;
     int off_ks, off_kz, off_vs, off_v;
 };
 
-template <int D>
+// blocks of 8 columns per CTA: enough to cover the columns of one kv-head in
+// a single pass over its cache rows, capped by the accumulator registers
+inline int gen_nb(int d, int64_t cols)
+{
+    const int cap = d <= 128 ? 4 : (d == 256 ? 2 : 1);
+    const int64_t need = (cols + gN - 1) / gN;
+    const int nb = need <= 1 ? 1 : (need <= 2 ? 2 : 4);
+    return nb < cap ? nb : cap;
+}
+
+template <int D, int NB>
 int gen_ctas_per_sm(int smem)
 {
     int n = 0;
-    auto kern = attn_generic_kernel<D>;
+    auto kern = attn_generic_kernel<D, NB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, gThreads, smem) != cudaSuccess) return 0;
     return n;
 }
 
-template <int D>
-bool gen_plan(const CacheView &c, int q_heads, int64_t seq_len, GenPlan &pl)
+template <int D, int NB>
+bool gen_plan_nb(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, GenPlan &pl)
 {
-    using A = GGeo<D>;
+    using A = GGeo<D, NB>;
     const int NG = D / 32, rbk = D * c.kb / 8, rbv = D * c.vb / 8;
     auto r16 = [](int x) { return (x + 15) / 16 * 16; };
+    pl.nb = NB;
     pl.off_ks = r16(gT * rbk);
     pl.off_kz = pl.off_ks + r16(gT * NG * 2);
     pl.off_vs = pl.off_kz + r16(gT * NG * 2);
@@ -516,10 +607,11 @@ bool gen_plan(const CacheView &c, int q_heads, int64_t seq_len, GenPlan &pl)
     pl.stages = 3 * pl.stage_bytes <= 80 * 1024 ? 3 : 2;
     const int ring = pl.stages * pl.stage_bytes > A::MERGE ? pl.stages * pl.stage_bytes : A::MERGE;
     pl.smem = 128 /*align slack*/ + ring + A::QF + A::QS + 512 /*lut*/ + gMaxStages * 12 /*barriers, counters*/;
-    const int per_sm = gen_ctas_per_sm<D>(pl.smem);
+    const int per_sm = gen_ctas_per_sm<D, NB>(pl.smem);
     if (per_sm < 1) return false;
-    const int G = q_heads / c.H, HB = (G + gN - 1) / gN;
-    const int64_t units = (int64_t)c.B * c.H * HB;
+    const int64_t cols = (int64_t)(q_heads / c.H) * m;
+    pl.hb = (int)((cols + A::CB - 1) / A::CB);
+    const int64_t units = (int64_t)c.B * c.H * pl.hb;
     const int64_t nst = (seq_len + gT - 1) / gT;
     const int64_t slots = (int64_t)num_sms() * per_sm;
     pl.splits = 1;
@@ -541,24 +633,34 @@ bool gen_plan(const CacheView &c, int q_heads, int64_t seq_len, GenPlan &pl)
 }
 
 template <int D>
-size_t gen_workspace(const CacheView &c, int q_heads, int64_t seq_len)
+bool gen_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, GenPlan &pl)
 {
-    GenPlan pl;
-    if (!gen_plan<D>(c, q_heads, seq_len, pl)) return 0;
-    const int HB = (q_heads / c.H + gN - 1) / gN;
-    return (size_t)c.B * c.H * HB * pl.splits * gN * (D + 2) * 4;
+    switch (gen_nb(D, (int64_t)(q_heads / c.H) * m)) {
+    case 1: return gen_plan_nb<D, 1>(c, q_heads, m, seq_len, pl);
+    case 2: if constexpr (D <= 256) return gen_plan_nb<D, 2>(c, q_heads, m, seq_len, pl); break;
+    case 4: if constexpr (D <= 128) return gen_plan_nb<D, 4>(c, q_heads, m, seq_len, pl); break;
+    }
+    return false;
 }
 
 template <int D>
-cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out, void *ws,
-                    size_t ws_bytes, cudaStream_t s)
+size_t gen_workspace(const CacheView &c, int q_heads, int64_t m, int64_t seq_len)
 {
     GenPlan pl;
-    if (!gen_plan<D>(c, QH, seq_len, pl)) return cudaErrorInvalidConfiguration;
-    const int G = QH / c.H, HB = (G + gN - 1) / gN;
-    const size_t need_o = (size_t)c.B * c.H * HB * pl.splits * gN * D * 4;
-    const size_t need = need_o + (size_t)c.B * c.H * HB * pl.splits * gN * 2 * 4;
-    if (ws_bytes < need) return cudaErrorInvalidValue;
+    if (!gen_plan<D>(c, q_heads, m, seq_len, pl)) return 0;
+    return (size_t)c.B * c.H * pl.hb * pl.splits * gN * pl.nb * (D + 2) * 4;
+}
+
+template <int D>
+cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, int64_t seq_len, float scale, float *out,
+                    void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    GenPlan pl;
+    if (!gen_plan<D>(c, QH, m, seq_len, pl)) return cudaErrorInvalidConfiguration;
+    const int G = QH / c.H, CB = gN * pl.nb;
+    const size_t parts = (size_t)c.B * c.H * pl.hb * pl.splits * CB;
+    const size_t need_o = parts * D * 4;
+    if (ws_bytes < need_o + parts * 2 * 4) return cudaErrorInvalidValue;
     GenParams p{};
     p.k_codes = c.k_codes;
     p.v_codes = c.v_codes;
@@ -573,7 +675,9 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t seq_l
     p.H = c.H;
     p.QH = QH;
     p.G = G;
-    p.HB = HB;
+    p.M = (int)m;
+    p.cols = G * (int)m;
+    p.HB = pl.hb;
     p.splits = pl.splits;
     p.kb = c.kb;
     p.vb = c.vb;
@@ -581,6 +685,7 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t seq_l
     p.cap = c.cap;
     p.seq_len = seq_len;
     p.tokens_per_split = pl.tokens_per_split;
+    p.base0 = seq_len - m + 1;
     p.rbk = D * c.kb / 8;
     p.rbv = D * c.vb / 8;
     p.off_ks = pl.off_ks;
@@ -592,37 +697,43 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t seq_l
     p.koff = c.kb == 8 ? 1152.0f : 1024.0f;
     const Tables &tab = codebook_tables(c.vb);
     for (int i = 0; i < (1 << c.vb); ++i) p.cen[i] = __half_as_ushort(__float2half_rn(tab.centroids[i]));
-    if ((int64_t)c.H * HB > 65535 || c.B > 65535) return cudaErrorInvalidValue;
-    attn_generic_kernel<D><<<dim3(pl.splits, c.H * HB, c.B), gThreads, pl.smem, s>>>(p);
+    if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
+    const dim3 grid(pl.splits, c.H * pl.hb, c.B);
+    switch (pl.nb) {
+    case 1: attn_generic_kernel<D, 1><<<grid, gThreads, pl.smem, s>>>(p); break;
+    case 2: if constexpr (D <= 256) attn_generic_kernel<D, 2><<<grid, gThreads, pl.smem, s>>>(p); break;
+    case 4: if constexpr (D <= 128) attn_generic_kernel<D, 4><<<grid, gThreads, pl.smem, s>>>(p); break;
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int rows = c.B * QH;
-    GenCombineParams cp{p.part_o, p.part_ml, out, c.H, QH, G, HB, pl.splits, rows, inv_sqrt_head_dim(D)};
+    const int rows = c.B * (int)m * QH;
+    GenCombineParams cp{p.part_o, p.part_ml, out, c.H, QH, G, (int)m, pl.hb, CB, pl.splits, rows,
+                        inv_sqrt_head_dim(D)};
     attn_generic_combine<D><<<(rows + 7) / 8, 256, 0, s>>>(cp);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)
+size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_t m, int64_t seq_len)
 {
     switch (c.d) {
-    case 64: return gen_workspace<64>(c, q_heads, seq_len);
-    case 128: return gen_workspace<128>(c, q_heads, seq_len);
-    case 256: return gen_workspace<256>(c, q_heads, seq_len);
-    case 512: return gen_workspace<512>(c, q_heads, seq_len);
+    case 64: return gen_workspace<64>(c, q_heads, m, seq_len);
+    case 128: return gen_workspace<128>(c, q_heads, m, seq_len);
+    case 256: return gen_workspace<256>(c, q_heads, m, seq_len);
+    case 512: return gen_workspace<512>(c, q_heads, m, seq_len);
     }
     return 0;
 }
 
-cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
-                                     float *out, void *ws, size_t ws_bytes, cudaStream_t s)
+cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int q_heads, int64_t m, int64_t seq_len,
+                                     float scale, float *out, void *ws, size_t ws_bytes, cudaStream_t s)
 {
     switch (c.d) {
-    case 64: return gen_run<64>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
-    case 128: return gen_run<128>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
-    case 256: return gen_run<256>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
-    case 512: return gen_run<512>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+    case 64: return gen_run<64>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
+    case 128: return gen_run<128>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
+    case 256: return gen_run<256>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
+    case 512: return gen_run<512>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -46,9 +46,11 @@ TQ_DECLARE_PER_D(512)
 
 // Attention for every head_dim, bit pair and group size (the specialised
 // kernel above covers d128, k8/k4, v3, groups of 8).
-size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len);
-cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
-                                     float *out, void *ws, size_t ws_bytes, cudaStream_t s);
+// M query rows per sequence (q and out [B][M][q_heads][d]); query row i sees
+// cache rows [0, seq_len - M + i].  M = 1 is plain decode attention.
+size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_t m, int64_t seq_len);
+cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int q_heads, int64_t m, int64_t seq_len,
+                                     float scale, float *out, void *ws, size_t ws_bytes, cudaStream_t s);
 
 // Deferred fetch, un-rotation and cache row copy / clear (src null: zeros).
 cudaError_t launch_decode_rotated(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out, cudaStream_t s);

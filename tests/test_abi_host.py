@@ -140,3 +140,25 @@ def test_lifecycle_and_deferred_refusals(tqlib):
     assert L.tq_cache_clear_rows(ctypes.byref(a), 30, 4, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_cache_clear_rows(ctypes.byref(a), 3, -1, None) == S["TQ_ERR_SHAPE"]
     assert L.tq_cache_clear_rows(ctypes.byref(a), 3, 0, None) == S["TQ_OK"]
+
+
+def test_multi_token_refusals(tqlib):
+    """Argument checks of the multi-token attention return before any launch."""
+    S = {name: i for i, name in enumerate(
+        ["TQ_OK", "TQ_ERR_NULL", "TQ_ERR_HEAD_DIM", "TQ_ERR_BITS", "TQ_ERR_SHAPE", "TQ_ERR_CAPACITY",
+         "TQ_ERR_ALIGN", "TQ_ERR_WORKSPACE", "TQ_ERR_CUDA", "TQ_ERR_UNSUPPORTED"])}
+    L = tqlib.lib()
+    s = _struct(tqlib)  # 2 kv-heads, capacity 32
+    call = lambda qh, m, T, q=0x10000, out=0x20000: L.tq_multi_token_attention(  # noqa: E731
+        ctypes.byref(s), q, qh, m, T, 1.0, out, None, 0, None)
+    assert call(3, 2, 8) == S["TQ_ERR_SHAPE"]          # q_heads not a multiple of kv-heads
+    assert call(4, 0, 8) == S["TQ_ERR_SHAPE"]          # no query rows
+    assert call(4, 9, 8) == S["TQ_ERR_SHAPE"]          # more query rows than cache rows
+    assert call(4, 2, 33) == S["TQ_ERR_CAPACITY"]
+    assert call(4, 2, 8, q=None) == S["TQ_ERR_NULL"]
+    assert call(4, 2, 8, out=0x20008) == S["TQ_ERR_ALIGN"]
+    big = _struct(tqlib, capacity=1 << 20)
+    assert L.tq_multi_token_attention(ctypes.byref(big), 0x10000, 2 * 4096, 1 << 18, 1 << 18, 1.0, 0x20000, None, 0,
+                                      None) == S["TQ_ERR_SHAPE"]  # 2^31 output rows
+    assert L.tq_multi_token_workspace_bytes(ctypes.byref(s), 4, 9, 8) == 0
+    assert L.tq_multi_token_workspace_bytes(ctypes.byref(s), 3, 2, 8) == 0
