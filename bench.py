@@ -420,7 +420,7 @@ def cpu_baseline():
 
 # ------------------------------------------------------------------ main
 # ------------------------------------------------------------------ sweep of the other paths
-def run_sweep():
+def run_sweep(only=None):
     """Device-timed throughput of the paths beyond the headline step, each on
     inputs larger than L2: CUDA events on the launching stream around 20 calls
     after 3 warm-up calls, median.  GB/s counts the format bytes each call must
@@ -469,9 +469,10 @@ def run_sweep():
             del k, v
         return cache
 
+    want = (lambda kind_: True) if not only else (lambda kind_: kind_ in only)
     w = tq_synth.WORKLOADS["decode"]
     H, T = 8, 32769
-    for d, kb, vb, G in [(128, 8, 3, 8), (128, 4, 3, 8), (128, 4, 2, 8), (128, 8, 4, 8), (128, 5, 2, 8),
+    for d, kb, vb, G in [] if not want("attention") else [(128, 8, 3, 8), (128, 4, 3, 8), (128, 4, 2, 8), (128, 8, 4, 8), (128, 5, 2, 8),
                          (128, 8, 3, 4), (128, 8, 3, 16), (64, 8, 3, 8), (256, 8, 3, 8), (512, 4, 3, 4)]:
         bpt = tq.tq_bytes_per_token_head(d, kb, vb)
         B = max(1, round(4e8 / (H * T * bpt)))
@@ -490,9 +491,9 @@ def run_sweep():
     # forward shapes) over a 32769-row cache.  The MMA work is 4 d flops per
     # (column, cache row), a column being one (query row, q-head).
     d, kb, vb, G, B = 128, 8, 3, 8, 8
-    cache = filled_cache(B, H, d, T, kb, vb, w)
+    cache = filled_cache(B, H, d, T, kb, vb, w) if want("multi_token_attention") else None
     bpt = tq.tq_bytes_per_token_head(d, kb, vb)
-    for M in (4, 128):
+    for M in (4, 128) if cache is not None else ():
         q = torch.empty((B, M * G * H, d), dtype=torch.int16, device="cuda")
         tq_synth.device_q(w, 0, q, B=B, QH=M * G * H, d=d)
         qb = q.view(torch.bfloat16).view(B, M, G * H, d)
@@ -505,23 +506,29 @@ def run_sweep():
         del q, qb, out, ws
     del cache
     # deferred fetch and un-rotation, row copies: prefill-shaped cache of 32768 rows
+    if not any(want(k_) for k_ in ("rotated_fetch", "unrotate", "copy_rows", "clear_rows")):
+        return
     pw = tq_synth.WORKLOADS["prefill"]
     B, H, T, d = 4, 8, 32768, 128
     cache = filled_cache(B, H, d, T, 8, 3, pw)
     vr = torch.empty((B, H, T, d), dtype=torch.bfloat16, device="cuda")
     us = timed(lambda: tq.tq_decode_values_rotated(cache, 0, T, dtype=torch.bfloat16, out=vr))
-    emit("rotated_fetch", {"B": B, "kv_heads": H, "rows": T, "d": d, "vb": 3, "out": "bf16"}, us,
-         B * H * T * (48 + 8 + d * 2))
+    if want("rotated_fetch"):
+        emit("rotated_fetch", {"B": B, "kv_heads": H, "rows": T, "d": d, "vb": 3, "out": "bf16"}, us,
+             B * H * T * (48 + 8 + d * 2))
     x = torch.randn((B * H * T // 4, d), dtype=torch.float32, device="cuda")
     y = torch.empty_like(x)
     us = timed(lambda: tq.tq_unrotate(x, out=y))
-    emit("unrotate", {"rows": x.shape[0], "d": d, "in": "fp32", "out": "fp32"}, us, 2 * x.numel() * 4)
+    if want("unrotate"):
+        emit("unrotate", {"rows": x.shape[0], "d": d, "in": "fp32", "out": "fp32"}, us, 2 * x.numel() * 4)
     del x, y, vr
     snap = tq.Cache(B, H, d, T)
     us = timed(lambda: tq.tq_cache_copy_rows(snap, 0, cache, 0, T))
-    emit("copy_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, 2 * B * H * T * 200)
+    if want("copy_rows"):
+        emit("copy_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, 2 * B * H * T * 200)
     us = timed(lambda: tq.tq_cache_clear_rows(snap, 0, T))
-    emit("clear_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, B * H * T * 200)
+    if want("clear_rows"):
+        emit("clear_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, B * H * T * 200)
 
 
 def main():
@@ -535,9 +542,12 @@ def main():
                     help="sequences of the decode step (smaller values for profiling captures)")
     ap.add_argument("--sweep", action="store_true",
                     help="measure the paths beyond the headline step instead (one JSON line each)")
+    ap.add_argument("--only", default="",
+                    help="with --sweep: comma-separated kinds to run (attention, multi_token_attention, "
+                         "rotated_fetch, unrotate, copy_rows, clear_rows)")
     args = ap.parse_args()
     if args.sweep:
-        run_sweep()
+        run_sweep(set(filter(None, args.only.split(","))))
         return
     if args.warmup < 3:
         args.warmup = 3
