@@ -297,12 +297,20 @@ tq_status check_multi(const tq_cache *c, int32_t q_heads, int64_t m, int64_t seq
     if ((int64_t)c->num_kv_heads * ((m * group + 7) / 8) > 65535) return TQ_ERR_SHAPE;
     return TQ_OK;
 }
+
+// wide chunks (at least 128 columns per kv-head, head_dim 64/128) run on the
+// tcgen05 kernel, the rest on the generic mma.sync kernel
+size_t multi_workspace_bytes(const tq_cache *c, int32_t q_heads, int64_t m, int64_t seq_len)
+{
+    return tq::attention_tc_applies(view(c), q_heads, m) ? tq::attention_tc_workspace_bytes(view(c), q_heads, m, seq_len)
+                                                         : tq::attention_generic_workspace_bytes(view(c), q_heads, m, seq_len);
+}
 }  // namespace
 
 size_t tq_multi_token_workspace_bytes(const tq_cache *c, int32_t q_heads, int64_t m, int64_t seq_len)
 {
     if (check_cache(c) != TQ_OK || check_multi(c, q_heads, m, seq_len) != TQ_OK) return 0;
-    return tq::attention_generic_workspace_bytes(view(c), q_heads, m, seq_len);
+    return multi_workspace_bytes(c, q_heads, m, seq_len);
 }
 
 tq_status tq_multi_token_attention(const tq_cache *c, const void *q, int32_t q_heads, int64_t m, int64_t seq_len,
@@ -314,12 +322,16 @@ tq_status tq_multi_token_attention(const tq_cache *c, const void *q, int32_t q_h
     st = check_multi(c, q_heads, m, seq_len);
     if (st != TQ_OK) return st;
     if (!aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
-    const size_t need = tq::attention_generic_workspace_bytes(view(c), q_heads, m, seq_len);
+    const size_t need = multi_workspace_bytes(c, q_heads, m, seq_len);
     if (need == 0) return TQ_ERR_CUDA;  // the occupancy query failed
     if (!ws || ws_bytes < need) return TQ_ERR_WORKSPACE;
     if (!aligned16(ws)) return TQ_ERR_ALIGN;
-    return cuda_status(tq::launch_attention_generic(view(c), static_cast<const uint16_t *>(q), q_heads, m, seq_len,
-                                                    scale, out, ws, ws_bytes, (cudaStream_t)stream));
+    const uint16_t *qh = static_cast<const uint16_t *>(q);
+    if (tq::attention_tc_applies(view(c), q_heads, m))
+        return cuda_status(
+            tq::launch_attention_tc(view(c), qh, q_heads, m, seq_len, scale, out, ws, ws_bytes, (cudaStream_t)stream));
+    return cuda_status(
+        tq::launch_attention_generic(view(c), qh, q_heads, m, seq_len, scale, out, ws, ws_bytes, (cudaStream_t)stream));
 }
 
 tq_status tq_decode_attention_noalloc(const tq_cache *c, const void *q, int32_t q_heads, int64_t seq_len,

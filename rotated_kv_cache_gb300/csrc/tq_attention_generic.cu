@@ -715,6 +715,22 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
 
 }  // namespace
 
+cudaError_t launch_attention_combine_parts(int d, const float *part_o, const float *part_ml, float *out, int B, int H,
+                                           int QH, int m, int hb, int cb, int splits, cudaStream_t s)
+{
+    const int rows = B * m * QH;
+    GenCombineParams cp{part_o, part_ml, out, H, QH, QH / H, m, hb, cb, splits, rows, inv_sqrt_head_dim(d)};
+    const dim3 grid((rows + 7) / 8);
+    switch (d) {
+    case 64: attn_generic_combine<64><<<grid, 256, 0, s>>>(cp); break;
+    case 128: attn_generic_combine<128><<<grid, 256, 0, s>>>(cp); break;
+    case 256: attn_generic_combine<256><<<grid, 256, 0, s>>>(cp); break;
+    case 512: attn_generic_combine<512><<<grid, 256, 0, s>>>(cp); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_t m, int64_t seq_len)
 {
     switch (c.d) {

@@ -1,0 +1,620 @@
+// tq_attention_tc.cu -- multi-token attention on the fifth-generation tensor
+// cores (tcgen05), for chunks wide enough to fill the MMA's 128 rows.
+//
+// Method: mlx-bun "TurboQuant -- rotation-based quantization", Part A:
+// "Algorithm" (key (code + zero) * scale, value centroid[code] * rms),
+// "Deferred inverse FWHT" (the weighted sum is formed in the rotated domain
+// and un-rotated once per query row), and "Packed-value decode fusion
+// investigation" (forward passes appending M = 1, 4 or 128 rows; query row i
+// of M sees the cache rows before seq_len - M + i + 1).  Same operation,
+// partial layout and combine as the generic kernel; this one runs when a
+// kv-head has at least 128 (query row, q-head) columns, where the work is a
+// dense contraction (at M = 128 and 8 q-heads per kv-head, 1024 columns).
+//
+// Design.  A CTA is two warpgroups; each owns 128 columns of one kv-head
+// (the MMA's M = 128, one column per tensor-memory lane and per thread) and
+// the CTA streams the kv-head's rows of one split in 64-row stages:
+//  1. one thread keeps two packed stages in flight with bulk copies
+//     completing on mbarriers;
+//  2. all 256 threads dequantise the stage into shared memory as f16 MMA
+//     operands with 128-byte swizzle: keys as a two-term split
+//     k = hi + lo (hi = f16(k), lo = f16(k - hi)), so the scores keep the
+//     fp32 key (f16 alone costs ~1e-2 on heavy-tailed keys), K-major; values
+//     centroid * rms, MN-major (rows of dims, as stored).  Each tile is
+//     scaled by a power of two chosen from its group metadata so the f16
+//     range always holds it; the scale is undone on the scores and outputs;
+//  3. one thread issues S = Q K^T (hi and lo into one accumulator) for both
+//     warpgroups into tensor memory and commits to per-warpgroup mbarriers;
+//  4. each thread reads its column's 64 scores (tcgen05.ld), applies the
+//     causal limit, runs the online base-2 softmax in registers and writes
+//     its row of P (f16, K-major) to shared memory;
+//  5. the warpgroup's first thread issues O_stage = P V into tensor memory;
+//     each thread adds its row of O_stage into its register accumulator,
+//     rescaled by the running maximum.
+// The output of a CTA is the per-column (o, m, l) partial; the generic
+// kernel's combine merges the splits and un-rotates.  Every wait is bounded
+// (mbarrier with a timeout that sets the device error word).
+#include <cuda.h>
+
+#include "tq_common.cuh"
+#include "tq_kernels.h"
+
+namespace tq {
+namespace {
+
+constexpr int tcT = 64;            // cache rows per stage (the QK MMA's N, the PV MMA's K)
+constexpr int tcWG = 2;            // warpgroups per CTA
+constexpr int tcThreads = 128 * tcWG;
+constexpr int tcCB = 128 * tcWG;   // columns per CTA
+constexpr int tcRing = 2;          // packed stages in flight
+
+struct TcParams {
+    const uint8_t *k_codes, *v_codes;
+    const uint16_t *k_scale, *k_zero, *v_scale;
+    const uint16_t *q;  // [B][M][QH][D] bf16
+    float *part_o;      // [B][H][HB][S][256][D]
+    float *part_ml;     // [B][H][HB][S][256][2]
+    uint32_t *err;
+    int H, QH, G, M, cols, HB, splits, kb, vb;
+    int64_t cap, seq_len, tokens_per_split, base0;
+    int rbk, rbv, off_ks, off_kz, off_vs, off_v, stage_bytes;
+    float scale_log2;   // softmax scale * log2(e)
+    float kcmax;        // largest |key code| (127 or 2^kb - 1)
+    float vcmax;        // largest |centroid|
+    float cen[256];     // value centroids (fp32)
+};
+
+// ---------------------------------------------------------------- tcgen05 / descriptor helpers
+// Shared-memory matrix descriptor: 128-byte swizzle, descriptor version 1.
+// lbo / sbo in bytes (K-major tiles: sbo = 1024 between 8-row groups, lbo
+// unused; MN-major tiles: lbo between 64-element blocks of the M/N extent,
+// sbo between 8-row groups of K).
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | (uint64_t)((lbo >> 4) & 0x3FFF) << 16 |
+           (uint64_t)((sbo >> 4) & 0x3FFF) << 32 | (uint64_t)1 << 46 | (uint64_t)2 << 61;
+}
+
+// Instruction descriptor, kind::f16: f16 A and B, f32 accumulator, M x N,
+// A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1).
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, int b_mn)
+{
+    return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+__device__ __forceinline__ float tc_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t tc_pack_f16(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t tc_lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// Byte offset of element (r, k) in a K-major tile of R rows (64-element K blocks
+// of R * 128 bytes; 16-byte chunks XOR-swizzled by r % 8).
+__host__ __device__ constexpr uint32_t kmaj_off(int R, int r, int k)
+{
+    return (uint32_t)((k / 64) * (R * 128) + (r / 8) * 1024 + (r % 8) * 128 + ((((k % 64) / 8) ^ (r % 8)) * 16) +
+                      (k % 8) * 2);
+}
+
+// Byte offset of element (k = cache row, n = dim) of the MN-major value tile
+// (N dims: 64-dim blocks 1024 bytes apart inside each group of 8 rows).
+template <int N>
+__host__ __device__ constexpr uint32_t mnmaj_off(int k, int n)
+{
+    return (uint32_t)((k / 8) * (N / 64) * 1024 + (n / 64) * 1024 + (k % 8) * 128 + ((((n % 64) / 8) ^ (k % 8)) * 16) +
+                      (n % 8) * 2);
+}
+
+// power-of-two exponent e with bound * 2^e in [2^13, 2^14) (0 if the bound is
+// zero or not finite), clamped to [-100, 100]
+__device__ __forceinline__ int tile_exponent(float bound)
+{
+    if (!(bound > 0.0f) || !(bound < INFINITY)) return 0;
+    const int e = 13 - (((int)(__float_as_uint(bound) >> 23) & 0xFF) - 127);
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+template <int D>
+struct TcGeo {
+    static constexpr int NG = D / 32;
+    static constexpr int KT = tcT * D * 2;     // one key tile (hi or lo): 64 rows x D f16
+    static constexpr int VT = tcT * D * 2;     // value tile
+    static constexpr int QT = 128 * D * 2;     // one warpgroup's q tile
+    static constexpr int PT = 128 * tcT * 2;   // one warpgroup's P tile
+    static constexpr int OFF_KH = 0, OFF_KL = KT, OFF_V = 2 * KT, OFF_Q = 2 * KT + VT, OFF_P = OFF_Q + tcWG * QT;
+    static constexpr int OFF_RING = OFF_P + tcWG * PT;  // packed stages follow (stage_bytes each)
+    static constexpr int SPAN = 64 + D;                  // tensor-memory columns per warpgroup: S, then O
+    static constexpr int TMEM_COLS = tcWG * SPAN <= 256 ? 256 : 512;
+    static constexpr int WG_COLS = TMEM_COLS / tcWG;
+};
+
+template <int D>
+__global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p)
+{
+    using A = TcGeo<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ring = smem + A::OFF_RING;
+    float *lut = reinterpret_cast<float *>(ring + tcRing * p.stage_bytes);
+    float *red = lut + 256;                                      // [2][8] per-warp maxima
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + 16);     // full[tcRing], s[2], o[2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + tcRing + 4);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t full0 = smem_addr(bars), bar_s0 = full0 + 8 * tcRing, bar_o0 = bar_s0 + 16;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = tid >> 7, ltid = tid & 127, wq = warp & 3;
+    const int split = blockIdx.x, h = blockIdx.y / p.HB, hb = blockIdx.y - h * p.HB, b = blockIdx.z;
+    const int64_t bh = (int64_t)b * p.H + h;
+    const int col0 = hb * tcCB;
+    const int col_last = (p.cols < col0 + tcCB ? p.cols : col0 + tcCB) - 1;
+    const int64_t lim_lo = p.base0 + col0 / p.G, lim_hi = p.base0 + col_last / p.G;
+    const int64_t t_begin = (int64_t)split * p.tokens_per_split;
+    const int64_t t_end = imin64(lim_hi, t_begin + p.tokens_per_split);
+    const int n_stages = t_end > t_begin ? (int)((t_end - t_begin + tcT - 1) / tcT) : 0;
+    constexpr int NG = A::NG;
+
+    auto issue = [&](int s) {
+        const int slot = s % tcRing;
+        const int64_t t = t_begin + (int64_t)s * tcT;
+        const int rows = (int)imin64(tcT, p.cap - t);
+        const int64_t row0 = bh * p.cap + t;
+        const uint32_t st = smem_addr(ring + slot * p.stage_bytes), bar = full0 + 8 * slot;
+        mbar_arrive_expect_tx(bar, (uint32_t)(rows * (p.rbk + p.rbv + 3 * NG * 2)));
+        bulk_g2s(st, p.k_codes + row0 * p.rbk, rows * p.rbk, bar);
+        bulk_g2s(st + p.off_ks, p.k_scale + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + p.off_kz, p.k_zero + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + p.off_vs, p.v_scale + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + p.off_v, p.v_codes + row0 * p.rbv, rows * p.rbv, bar);
+    };
+    int issued = 0;
+    if (tid == 0) {
+        for (int s = 0; s < tcRing; ++s) mbar_init(full0 + 8 * s, 1);
+        for (int w = 0; w < tcWG; ++w) {
+            mbar_init(bar_s0 + 8 * w, 1);
+            mbar_init(bar_o0 + 8 * w, 1);
+        }
+        fence_mbar_init();
+        for (; issued < tcRing && issued < n_stages; ++issued) issue(issued);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tslot)),
+                     "r"(A::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int i = tid; i < (1 << p.vb); i += tcThreads) lut[i] = p.cen[i];
+
+    // ---------------------------------------------------------------- q of this thread's column
+    // Scaled by a power of two so its largest |q| lands in [2^14, 2^15): the
+    // bf16 values are then exact in f16.  Row ltid of the warpgroup's K-major tile.
+    const int col = col0 + 128 * wg + ltid;
+    const bool real = col < p.cols;
+    const int qi = real ? col / p.G : p.M - 1;
+    float ie;
+    {
+        const int qw = real ? col - qi * p.G : 0;
+        const uint16_t *qrow = p.q + (((int64_t)b * p.M + qi) * p.QH + (int64_t)h * p.G + qw) * D;
+        float mx = 0.0f;
+        if (real)
+            for (int c8 = 0; c8 < D / 8; ++c8) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 8 * c8);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(ww[i])), fabsf(bf16_hi(ww[i]))));
+            }
+        int e = 0;
+        if (mx > 0.0f && mx < INFINITY) e = 14 - (((int)(__float_as_uint(mx) >> 23) & 0xFF) - 127);
+        e = e < -100 ? -100 : (e > 100 ? 100 : e);
+        const float qs = ldexpf(1.0f, e);
+        ie = ldexpf(1.0f, -e) * p.scale_log2;
+        const uint32_t qt = sbase + A::OFF_Q + wg * A::QT;
+        for (int c8 = 0; c8 < D / 8; ++c8) {
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (real) w = *reinterpret_cast<const uint4 *>(qrow + 8 * c8);
+            uint4 hv;
+            hv.x = tc_pack_f16(bf16_lo(w.x) * qs, bf16_hi(w.x) * qs);
+            hv.y = tc_pack_f16(bf16_lo(w.y) * qs, bf16_hi(w.y) * qs);
+            hv.z = tc_pack_f16(bf16_lo(w.z) * qs, bf16_hi(w.z) * qs);
+            hv.w = tc_pack_f16(bf16_lo(w.w) * qs, bf16_hi(w.w) * qs);
+            sts128(qt + kmaj_off(128, ltid, 8 * c8), hv);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t t_s = tmem + wg * A::WG_COLS, t_o = t_s + 64;
+    const uint32_t t_lane = (uint32_t)(32 * wq) << 16;
+
+    float o[D];
+#pragma unroll
+    for (int j = 0; j < D; ++j) o[j] = 0.0f;
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    const uint32_t lut_a = smem_addr(lut);
+    const float magic_off = p.kb == 8 ? 8388736.0f : 8388608.0f;  // 2^23 (+ 128: int8 codes read as code + 128)
+    const uint32_t code_flip = p.kb == 8 ? 0x80u : 0u;
+    const uint32_t kmask = (1u << p.kb) - 1u, vmask = (1u << p.vb) - 1u;
+
+    int s = 0;
+    for (; s < n_stages; ++s) {
+        const int slot = s % tcRing;
+        const bool arrived = mbar_wait_bounded(full0 + 8 * slot, (s / tcRing) & 1, p.err);
+        const uint32_t st = smem_addr(ring + slot * p.stage_bytes);
+        const int64_t t0 = t_begin + (int64_t)s * tcT;
+        const int live = (int)imin64(tcT, t_end - t0);  // rows below t_end
+
+        // ---------------- tile exponents from the group metadata of the live rows
+        float bk = 0.0f, bv = 0.0f;
+        if (arrived)
+            for (int i = tid; i < tcT * NG; i += tcThreads)
+                if (i / NG < live) {
+                    const float sc = fabsf(f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_ks + 2 * i)));
+                    const float zc = fabsf(f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_kz + 2 * i)));
+                    const float sv = fabsf(f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_vs + 2 * i)));
+                    bk = fmaxf(bk, sc * (zc + p.kcmax));
+                    bv = fmaxf(bv, sv * p.vcmax);
+                }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) {
+            bk = fmaxf(bk, __shfl_xor_sync(0xffffffffu, bk, m));
+            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, m));
+        }
+        if (lane == 0) {
+            red[warp] = bk;
+            red[8 + warp] = bv;
+        }
+        if (!__syncthreads_and(arrived && ok)) {
+            ok = false;
+            break;
+        }
+        float mk = 0.0f, mv = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            mk = fmaxf(mk, red[w]);
+            mv = fmaxf(mv, red[8 + w]);
+        }
+        const int ek = tile_exponent(mk), ev = tile_exponent(mv);
+        const float sk = ldexpf(1.0f, ek), svs = ldexpf(1.0f, ev);
+
+        // ---------------- dequantise keys (hi, lo) and values into the operand tiles
+        for (int it = tid; it < tcT * (D / 8); it += tcThreads) {
+            const int t = it / (D / 8), c8 = it - t * (D / 8), G = c8 >> 2;
+            uint4 hi4 = make_uint4(0u, 0u, 0u, 0u), lo4 = hi4, v4 = hi4;
+            if (t < live) {
+                // keys: 8 codes of kb bits at byte c8 * kb of row t
+                const float sc = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_ks + 2 * (t * NG + G))) * sk;
+                const float zc = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_kz + 2 * (t * NG + G)));
+                const float cz = magic_off - zc;  // exact: |zero| <= 65504
+                const int kbyte = c8 * p.kb;
+                const uint32_t ka = st + t * p.rbk + (kbyte & ~3);
+                const uint64_t kw = ((uint64_t)tc_lds32(ka + 4) << 32 | tc_lds32(ka)) >> ((kbyte & 3) * 8);
+                float kv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t code = ((uint32_t)(kw >> (i * p.kb)) & kmask) ^ code_flip;
+                    kv[i] = (__uint_as_float(0x4B000000u | code) - cz) * sc;
+                }
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    hw[i] = tc_pack_f16(kv[2 * i], kv[2 * i + 1]);
+                    const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hw[i]));
+                    lw[i] = tc_pack_f16(kv[2 * i] - hf.x, kv[2 * i + 1] - hf.y);
+                }
+                hi4 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                lo4 = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                // values: 8 codes of vb bits at bit 8 * c8 * vb of row t
+                const float sv = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_vs + 2 * (t * NG + G))) * svs;
+                const int vbit = 8 * c8 * p.vb;
+                const uint32_t va = st + p.off_v + t * p.rbv + 4 * (vbit >> 5);
+                const uint64_t vw = ((uint64_t)tc_lds32(va + 4) << 32 | tc_lds32(va)) >> (vbit & 31);
+                float vv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t code = (uint32_t)(vw >> (i * p.vb)) & vmask;
+                    vv[i] = __uint_as_float(tc_lds32(lut_a + 4 * code)) * sv;
+                }
+                v4 = make_uint4(tc_pack_f16(vv[0], vv[1]), tc_pack_f16(vv[2], vv[3]), tc_pack_f16(vv[4], vv[5]),
+                                tc_pack_f16(vv[6], vv[7]));
+            }
+            sts128(sbase + A::OFF_KH + kmaj_off(tcT, t, 8 * c8), hi4);
+            sts128(sbase + A::OFF_KL + kmaj_off(tcT, t, 8 * c8), lo4);
+            sts128(sbase + A::OFF_V + mnmaj_off<D>(t, 8 * c8), v4);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();  // operands written; the packed slot is free
+        tc_fence_after();
+        if (tid == 0) {
+            if (issued < n_stages) issue(issued++);
+            // ---------------- S = Q K^T for both warpgroups (hi then lo into one accumulator)
+            constexpr uint32_t idesc_qk = tc_idesc(128, tcT, 0);
+#pragma unroll 1
+            for (int w = 0; w < tcWG; ++w) {
+                const uint32_t qt = sbase + A::OFF_Q + w * A::QT;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk / 4) * (tcT * 128) + (kk % 4) * 32;
+                    const uint64_t da = tc_desc(qt + (kk / 4) * (128 * 128) + (kk % 4) * 32, 16, 1024);
+                    tc_mma(tmem + w * A::WG_COLS, da, tc_desc(sbase + A::OFF_KH + ko, 16, 1024), idesc_qk, kk > 0);
+                    tc_mma(tmem + w * A::WG_COLS, da, tc_desc(sbase + A::OFF_KL + ko, 16, 1024), idesc_qk, 1);
+                }
+                tc_commit(bar_s0 + 8 * w);
+            }
+        }
+
+        // ---------------- softmax of this thread's column over the stage's rows
+        const bool s_done = mbar_wait_bounded(bar_s0 + 8 * wg, s & 1, p.err);
+        tc_fence_after();
+        uint32_t sr[2][32];
+        tc_ld32(t_s + t_lane, sr[0]);
+        tc_ld32(t_s + t_lane + 32, sr[1]);
+        tc_wait_ld();
+        const float f = ie * ldexpf(1.0f, -ek);
+        float x[tcT];
+#pragma unroll
+        for (int j = 0; j < tcT; ++j) x[j] = __uint_as_float(sr[j >> 5][j & 31]) * f;
+        if (t0 + tcT > lim_lo) {
+            // row t is hidden from query row qi when t >= base0 + qi (this also
+            // hides every row at or past t_end)
+            const int64_t vis = p.base0 + qi - t0;
+#pragma unroll
+            for (int j = 0; j < tcT; ++j)
+                if (j >= vis) x[j] = -INFINITY;
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < tcT; ++j) mt = fmaxf(mt, x[j]);
+        const float mn = fmaxf(m_run, mt);
+        const float mu = mn == -INFINITY ? 0.0f : mn;
+        const float alpha = tc_ex2(m_run - mu);
+        m_run = mn;
+        float ls = 0.0f;
+        {
+            const uint32_t pt = sbase + A::OFF_P + wg * A::PT;
+#pragma unroll
+            for (int c = 0; c < tcT / 8; ++c) {
+                float pv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    pv[i] = tc_ex2(x[8 * c + i] - mu);
+                    ls += pv[i];
+                }
+                sts128(pt + kmaj_off(128, ltid, 8 * c),
+                       make_uint4(tc_pack_f16(pv[0], pv[1]), tc_pack_f16(pv[2], pv[3]), tc_pack_f16(pv[4], pv[5]),
+                                  tc_pack_f16(pv[6], pv[7])));
+            }
+        }
+        l_run = l_run * alpha + ls;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(1 + wg, 128);
+        tc_fence_after();
+        // ---------------- O_stage = P V (this warpgroup), then o = o * alpha + O_stage / 2^ev
+        if (ltid == 0) {
+            constexpr uint32_t idesc_pv = tc_idesc(128, D, 1);
+            constexpr uint32_t SBO = (D / 64) * 1024;
+            const uint32_t pt = sbase + A::OFF_P + wg * A::PT;
+#pragma unroll
+            for (int kk = 0; kk < tcT / 16; ++kk)
+                tc_mma(t_o, tc_desc(pt + kk * 32, 16, 1024), tc_desc(sbase + A::OFF_V + kk * 2 * SBO, 1024, SBO),
+                       idesc_pv, kk > 0);
+            tc_commit(bar_o0 + 8 * wg);
+        }
+        const bool o_done = mbar_wait_bounded(bar_o0 + 8 * wg, s & 1, p.err);
+        tc_fence_after();
+        const float vsc = ldexpf(1.0f, -ev);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            tc_ld32(t_o + t_lane + 32 * c, orr);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[32 * c + j] = fmaf(__uint_as_float(orr[j]), vsc, o[32 * c + j] * alpha);
+        }
+        tc_fence_before();
+        ok = ok && s_done && o_done;
+    }
+    // copies still in flight after an early exit: wait for them (bounded)
+    if (tid == 0)
+        for (int r = s; r < issued; ++r) mbar_wait_bounded(full0 + 8 * (r % tcRing), (r / tcRing) & 1, p.err);
+
+    // ---------------------------------------------------------------- partial of this column
+    {
+        const int64_t pidx = ((bh * p.HB + hb) * p.splits + split) * tcCB + 128 * wg + ltid;
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * D);
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        p.part_ml[2 * pidx] = ok ? m_run : -INFINITY;
+        p.part_ml[2 * pidx + 1] = ok ? l_run : 0.0f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(A::TMEM_COLS));
+}
+
+// ---------------------------------------------------------------- host side
+struct TcPlan {
+    int hb, splits, stage_bytes, smem;
+    int64_t tokens_per_split;
+    int off_ks, off_kz, off_vs, off_v;
+};
+
+template <int D>
+bool tc_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, TcPlan &pl)
+{
+    using A = TcGeo<D>;
+    const int NG = D / 32, rbk = D * c.kb / 8, rbv = D * c.vb / 8;
+    auto r16 = [](int x) { return (x + 15) / 16 * 16; };
+    pl.off_ks = r16(tcT * rbk);
+    pl.off_kz = pl.off_ks + r16(tcT * NG * 2);
+    pl.off_vs = pl.off_kz + r16(tcT * NG * 2);
+    pl.off_v = pl.off_vs + r16(tcT * NG * 2);
+    pl.stage_bytes = (pl.off_v + tcT * rbv + 16 + 127) / 128 * 128;
+    pl.smem = 1024 /*align slack*/ + A::OFF_RING + tcRing * pl.stage_bytes + 256 * 4 /*lut*/ + 16 * 4 /*maxima*/ +
+              (tcRing + 4) * 8 /*barriers*/ + 16;
+    if (pl.smem > 227 * 1024) return false;
+    auto kern = attn_tc_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) != cudaSuccess) return false;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, tcThreads, pl.smem) != cudaSuccess || per_sm < 1)
+        return false;
+    // each CTA holds TMEM_COLS of the SM's 512 tensor-memory columns
+    if (per_sm * A::TMEM_COLS > 512) per_sm = 512 / A::TMEM_COLS;
+    const int64_t cols = (int64_t)(q_heads / c.H) * m;
+    pl.hb = (int)((cols + tcCB - 1) / tcCB);
+    const int64_t units = (int64_t)c.B * c.H * pl.hb;
+    const int64_t nst = (seq_len + tcT - 1) / tcT;
+    const int64_t slots = (int64_t)num_sms() * per_sm;
+    pl.splits = 1;
+    pl.tokens_per_split = nst * tcT;
+    double best = 1e300;
+    for (int waves = 1; waves <= 16; ++waves) {
+        int64_t s = (waves * slots + units - 1) / units;
+        if (s < 1) s = 1;
+        if (s > nst) s = nst;
+        const int64_t per = (nst + s - 1) / s, sp = (nst + per - 1) / per;
+        const double cost = (double)((units * sp + slots - 1) / slots) * (double)(per + 2);
+        if (cost < best - 1e-9) {
+            best = cost;
+            pl.splits = (int)sp;
+            pl.tokens_per_split = per * tcT;
+        }
+    }
+    return true;
+}
+
+template <int D>
+cudaError_t tc_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, int64_t seq_len, float scale, float *out,
+                   void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    TcPlan pl;
+    if (!tc_plan<D>(c, QH, m, seq_len, pl)) return cudaErrorInvalidConfiguration;
+    const int G = QH / c.H;
+    const size_t parts = (size_t)c.B * c.H * pl.hb * pl.splits * tcCB;
+    const size_t need_o = parts * D * 4;
+    if (ws_bytes < need_o + parts * 2 * 4) return cudaErrorInvalidValue;
+    TcParams p{};
+    p.k_codes = c.k_codes;
+    p.v_codes = c.v_codes;
+    p.k_scale = c.k_scale;
+    p.k_zero = c.k_zero;
+    p.v_scale = c.v_scale;
+    p.q = q;
+    p.part_o = static_cast<float *>(ws);
+    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + need_o);
+    p.err = device_error_word();
+    if (!p.err) return cudaErrorInvalidDevice;
+    p.H = c.H;
+    p.QH = QH;
+    p.G = G;
+    p.M = (int)m;
+    p.cols = G * (int)m;
+    p.HB = pl.hb;
+    p.splits = pl.splits;
+    p.kb = c.kb;
+    p.vb = c.vb;
+    p.cap = c.cap;
+    p.seq_len = seq_len;
+    p.tokens_per_split = pl.tokens_per_split;
+    p.base0 = seq_len - m + 1;
+    p.rbk = D * c.kb / 8;
+    p.rbv = D * c.vb / 8;
+    p.off_ks = pl.off_ks;
+    p.off_kz = pl.off_kz;
+    p.off_vs = pl.off_vs;
+    p.off_v = pl.off_v;
+    p.stage_bytes = pl.stage_bytes;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.kcmax = c.kb == 8 ? 127.0f : (float)((1 << c.kb) - 1);
+    const Tables &tab = codebook_tables(c.vb);
+    float cm = 0.0f;
+    for (int i = 0; i < (1 << c.vb); ++i) {
+        p.cen[i] = tab.centroids[i];
+        cm = cm > fabsf(tab.centroids[i]) ? cm : fabsf(tab.centroids[i]);
+    }
+    p.vcmax = cm;
+    if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
+    attn_tc_kernel<D><<<dim3(pl.splits, c.H * pl.hb, c.B), tcThreads, pl.smem, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, (int)m, pl.hb, tcCB, pl.splits, s);
+}
+
+}  // namespace
+
+bool attention_tc_applies(const CacheView &c, int q_heads, int64_t m)
+{
+    return (c.d == 64 || c.d == 128) && (int64_t)(q_heads / c.H) * m >= 128;
+}
+
+size_t attention_tc_workspace_bytes(const CacheView &c, int q_heads, int64_t m, int64_t seq_len)
+{
+    TcPlan pl;
+    bool ok = c.d == 64 ? tc_plan<64>(c, q_heads, m, seq_len, pl) : c.d == 128 ? tc_plan<128>(c, q_heads, m, seq_len, pl)
+                                                                                 : false;
+    if (!ok) return 0;
+    return (size_t)c.B * c.H * pl.hb * pl.splits * tcCB * (c.d + 2) * 4;
+}
+
+cudaError_t launch_attention_tc(const CacheView &c, const uint16_t *q, int q_heads, int64_t m, int64_t seq_len,
+                                float scale, float *out, void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    switch (c.d) {
+    case 64: return tc_run<64>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
+    case 128: return tc_run<128>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tq

@@ -52,6 +52,18 @@ size_t attention_generic_workspace_bytes(const CacheView &c, int q_heads, int64_
 cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int q_heads, int64_t m, int64_t seq_len,
                                      float scale, float *out, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// Merge split partials (o, m, l) laid out [B][H][hb][splits][cb][d] (+ [..][cb][2])
+// into out [B][m][QH][d]: log-sum-exp over splits, then the inverse rotation.
+cudaError_t launch_attention_combine_parts(int d, const float *part_o, const float *part_ml, float *out, int B, int H,
+                                           int QH, int m, int hb, int cb, int splits, cudaStream_t s);
+
+// Multi-token attention on the tcgen05 tensor cores: head_dim 64 or 128 with
+// at least 128 (query row, q-head) columns per kv-head.
+bool attention_tc_applies(const CacheView &c, int q_heads, int64_t m);
+size_t attention_tc_workspace_bytes(const CacheView &c, int q_heads, int64_t m, int64_t seq_len);
+cudaError_t launch_attention_tc(const CacheView &c, const uint16_t *q, int q_heads, int64_t m, int64_t seq_len,
+                                float scale, float *out, void *ws, size_t ws_bytes, cudaStream_t s);
+
 // Deferred fetch, un-rotation and cache row copy / clear (src null: zeros).
 cudaError_t launch_decode_rotated(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out, cudaStream_t s);
 cudaError_t launch_unrotate(int d, bool in_f32, const void *x, int64_t rows, bool out_f32, void *out, cudaStream_t s);

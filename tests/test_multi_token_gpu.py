@@ -94,3 +94,21 @@ def test_verify_flow_append_then_attend(cuda):
         want = oracle.attention_multi(planes_from_device(cache), q, t)
         assert np.abs(out.cpu().numpy() - want).max() < TOL
     assert cuda.tq_device_error() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kb,vb", [(kb, vb) for kb in (2, 4, 5, 8) for vb in (2, 3, 4, 5, 8)])
+def test_tensor_core_path_every_width(cuda, d, kb, vb):
+    """Chunks of 16 rows x 8 q-heads (128 columns per kv-head): the tcgen05
+    kernel at head_dim 64 and 128, every key/value width."""
+    err = _run(cuda, d, kb, vb, B=1, H=2, G=8, M=16, T=333, step=kb * 10 + vb)
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("d,G,M,T", [(128, 8, 15, 260), (128, 8, 16, 64), (128, 6, 50, 700), (64, 16, 40, 2100),
+                                     (128, 1, 300, 300), (256, 8, 16, 290)])
+def test_around_the_tensor_core_threshold(cuda, d, G, M, T):
+    """Just below 128 columns (generic kernel), exactly 128, ragged column
+    blocks of 256, one q-head per kv-head, and head_dim 256 (generic)."""
+    err = _run(cuda, d, 8, 3, B=2, H=2, G=G, M=M, T=T, step=M)
+    assert err < TOL, err
