@@ -112,3 +112,38 @@ def test_around_the_tensor_core_threshold(cuda, d, G, M, T):
     blocks of 256, one q-head per kv-head, and head_dim 256 (generic)."""
     err = _run(cuda, d, 8, 3, B=2, H=2, G=G, M=M, T=T, step=M)
     assert err < TOL, err
+
+
+def _slab(cache, b, h):
+    """One (sequence, kv-head) of a device cache as a 1 x 1 oracle cache."""
+    g = oracle.Planes(1, 1, cache.head_dim, cache.k_bits, cache.v_bits, cache.capacity)
+    for ga, src in zip(g.arrays(), cache.planes()):
+        ga[0, 0] = src[b, h].cpu().numpy().view(ga.dtype)
+    return g
+
+
+@pytest.mark.parametrize("kb,M", [(8, 128), (4, 16)])
+def test_full_size_chunk_sampled(cuda, kb, M):
+    """The measured shape: 8 sequences x 8 kv-heads x 32769 rows (d128, 64
+    q-heads, the decode workload's heavy-tailed keys), a chunk of M rows at the
+    end; sampled (sequence, kv-head, query row) outputs against the oracle."""
+    w = tq_synth.WORKLOADS["decode"]
+    B, H, T, d, G = 8, 8, 32769, 128, 8
+    cache = cuda.Cache(B, H, d, T, k_bits=kb, v_bits=3)
+    for b0 in range(B):
+        k = torch.empty((1, H, T, d), dtype=torch.int16, device="cuda")
+        v = torch.empty_like(k)
+        tq_synth.device_kv(w, k, v, B=1, H=H, d=d, n=T, b_offset=b0)
+        cuda.tq_encode_append(cache.batch_slice(b0, 1), k.view(torch.bfloat16), v.view(torch.bfloat16), 0)
+        del k, v
+    q = torch.empty((B, M * G * H, d), dtype=torch.int16, device="cuda")
+    tq_synth.device_q(w, 0, q, B=B, QH=M * G * H, d=d)
+    out = cuda.tq_multi_token_attention(cache, q.view(torch.bfloat16).view(B, M, G * H, d), T).cpu().numpy()
+    qh = q.cpu().numpy().view(np.uint16).reshape(B, M, G * H, d)
+    assert cuda.tq_device_error() == 0
+    for (b, h) in [(0, 0), (B - 1, 5)]:
+        g = _slab(cache, b, h)
+        for i in (0, 1, M // 2, M - 1):
+            want = oracle.attention(g, np.ascontiguousarray(qh[b:b + 1, i, h * G:(h + 1) * G]), T - M + i + 1)
+            err = np.abs(out[b, i, h * G:(h + 1) * G] - want[0]).max()
+            assert err < TOL, (b, h, i, err)
