@@ -239,30 +239,61 @@ def run_ours(args, rank, world, local_rank):
     parts = {k: v / K for k, v in parts.items()}
     assert tq.tq_device_error() == 0
 
-    # --- end to end through the public API with pinned host buffers
+    # --- end to end through the public API with pinned host buffers.  Steps
+    # are independent, so they are pipelined the way a serving loop would run
+    # them: step s's host-to-device copies (copy-in stream), compute (the
+    # compute stream) and device-to-host reads (copy-out stream) overlap with
+    # the neighbouring steps', on two sets of device buffers.  Every step still
+    # copies all of its inputs in and its results out inside the timed region.
     kp_h, vp_h = kp.cpu().pin_memory(), vp.cpu().pin_memory()
     kn_h, vn_h, q_h = knew.cpu().pin_memory(), vnew.cpu().pin_memory(), q.cpu().pin_memory()
     ko_h, vo_h = torch.empty_like(kp_h).pin_memory(), torch.empty_like(vp_h).pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    sets = [dict(kp=kp, vp=vp, knew=knew, vnew=vnew, q=q, ko=ko, vo=vo, out=out)]
+    sets.append({k: torch.empty_like(t) for k, t in sets[0].items()})
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    for e in comp_done + out_done:
+        e.record(stream)
 
     def e2e_step(s):
-        kp.copy_(kp_h, non_blocking=True)
-        vp.copy_(vp_h, non_blocking=True)
-        knew.copy_(kn_h, non_blocking=True)
-        vnew.copy_(vn_h, non_blocking=True)
-        q.copy_(q_h, non_blocking=True)
-        step(s)
-        ko_h.copy_(ko, non_blocking=True)
-        vo_h.copy_(vo, non_blocking=True)
-        out_h.copy_(out, non_blocking=True)
+        i = s % 2
+        bs = sets[i]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(comp_done[i])  # set i's inputs were read by step s - 2
+            bs["kp"].copy_(kp_h, non_blocking=True)
+            bs["vp"].copy_(vp_h, non_blocking=True)
+            bs["knew"].copy_(kn_h, non_blocking=True)
+            bs["vnew"].copy_(vn_h, non_blocking=True)
+            bs["q"].copy_(q_h, non_blocking=True)
+            in_done[i].record(s_in)
+        stream.wait_event(in_done[i])
+        stream.wait_event(out_done[i])  # set i's outputs were read back by step s - 2
+        tq.tq_encode_append(pre[s % 2], bs["kp"], bs["vp"], 0)
+        tq.tq_decode(pre[(s + 1) % 2], 0, P["T"], dtype=torch.bfloat16, k_out=bs["ko"], v_out=bs["vo"])
+        tq.tq_encode_append(dcache, bs["knew"], bs["vnew"], T)
+        tq.tq_decode_attention(dcache, bs["q"], T + 1, out=bs["out"], workspace=ws)
+        comp_done[i].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[i])
+            ko_h.copy_(bs["ko"], non_blocking=True)
+            vo_h.copy_(bs["vo"], non_blocking=True)
+            out_h.copy_(bs["out"], non_blocking=True)
+            out_done[i].record(s_out)
 
     Ke = max(3, min(K, 20))
-    e2e_step(0)
+    for s in range(2):
+        e2e_step(s)
     torch.cuda.synchronize()
     a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    s_in.wait_event(a)  # no copy of the timed steps starts before the start mark
     for s in range(Ke):
         e2e_step(s)
+    for e in out_done:  # the last reads back are inside the timed region
+        stream.wait_event(e)
     bb.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(bb) / Ke
@@ -327,7 +358,8 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_bytes_per_launch": ab["attention"],
         },
         "e2e": {"value": round(world * ab["total"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "pipelined": "copy-in, compute and copy-out streams overlap neighbouring steps (2 buffer sets)"},
         "gpu_launches": 8 * K,
         "clocks": clocks.summary(),
     }
