@@ -345,26 +345,29 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                          kcvt(shr_fma<12>(w1), p), bq[2 * G + 1][0], bq[2 * G + 1][1]);
             }
         }
-        // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum)
+        // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum),
+        // both heads of the lane at once on packed fp32 pairs
         float S[2][2];
         {
             const uint2 s0 = lds64(st + A::OFF_KS + r0 * 8), s1 = lds64(st + A::OFF_KS + r1 * 8);
             const uint2 z0 = lds64(st + A::OFF_KZ + r0 * 8), z1 = lds64(st + A::OFF_KZ + r1 * 8);
             const uint32_t sw[2][2] = {{s0.x, s0.y}, {s1.x, s1.y}}, zw[2][2] = {{z0.x, z0.y}, {z1.x, z1.y}};
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < 2; ++i) {
+                float2 sacc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    float sacc = 0.0f;
-#pragma unroll
-                    for (int G = 0; G < 4; ++G) {
-                        const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
-                        const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
-                        const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
-                        sacc = fmaf(sc, fmaf(zc, qs[G][j], acc[G][2 * i + j]), sacc);
-                    }
-                    S[i][j] = sacc * ie[j];
+                for (int G = 0; G < 4; ++G) {
+                    const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
+                    const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
+                    const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
+                    const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[G][0], qs[G][1]),
+                                                make_float2(acc[G][2 * i], acc[G][2 * i + 1]));
+                    sacc = __ffma2_rn(make_float2(sc, sc), t, sacc);
                 }
+                const float2 sv = __fmul2_rn(sacc, make_float2(ie[0], ie[1]));
+                S[i][0] = sv.x;
+                S[i][1] = sv.y;
+            }
             if (tile_t0 + 16 > t_end) {  // ragged tail: mask rows past the range
                 if (tile_t0 + g >= t_end) S[0][0] = S[0][1] = -INFINITY;
                 if (tile_t0 + g + 8 >= t_end) S[1][0] = S[1][1] = -INFINITY;

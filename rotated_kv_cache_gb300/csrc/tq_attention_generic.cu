@@ -326,11 +326,18 @@ __global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
                     const uint2 bq = g_lds64(qf_lane + nb * QF_NB + (2 * G + jj) * 32);
                     g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq.x, bq.y);
                 }
-                const float qs0 = qsum[G * CB + nb * gN + 2 * c], qs1 = qsum[G * CB + nb * gN + 2 * c + 1];
-                S[nb][0][0] = fmaf(sc0, fmaf(zc0, qs0, acc[0]), S[nb][0][0]);
-                S[nb][0][1] = fmaf(sc0, fmaf(zc0, qs1, acc[1]), S[nb][0][1]);
-                S[nb][1][0] = fmaf(sc1, fmaf(zc1, qs0, acc[2]), S[nb][1][0]);
-                S[nb][1][1] = fmaf(sc1, fmaf(zc1, qs1, acc[3]), S[nb][1][1]);
+                // both columns of the lane at once on packed fp32 pairs
+                const float2 qs = make_float2(qsum[G * CB + nb * gN + 2 * c], qsum[G * CB + nb * gN + 2 * c + 1]);
+                const float2 s0 = __ffma2_rn(make_float2(sc0, sc0),
+                                             __ffma2_rn(make_float2(zc0, zc0), qs, make_float2(acc[0], acc[1])),
+                                             make_float2(S[nb][0][0], S[nb][0][1]));
+                const float2 s1 = __ffma2_rn(make_float2(sc1, sc1),
+                                             __ffma2_rn(make_float2(zc1, zc1), qs, make_float2(acc[2], acc[3])),
+                                             make_float2(S[nb][1][0], S[nb][1][1]));
+                S[nb][0][0] = s0.x;
+                S[nb][0][1] = s0.y;
+                S[nb][1][0] = s1.x;
+                S[nb][1][1] = s1.y;
             }
         }
 #pragma unroll
