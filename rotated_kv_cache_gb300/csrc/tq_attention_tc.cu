@@ -176,7 +176,59 @@ struct TcGeo {
     static constexpr int WG_COLS = TMEM_COLS / tcWG;
 };
 
-template <int D>
+// ---------------------------------------------------------------- dequantisation of one 8-element item
+// Keys: 8 codes from the 64-bit window (w1:w0) >> sh; kv = (code + zero) * scale * 2^e.
+template <int KB>
+__device__ __forceinline__ void key_values(uint32_t w0, uint32_t w1, int sh, int kb, float sc, float cz, float (&kv)[8])
+{
+    uint32_t m[8];
+    if constexpr (KB == 8) {
+        const uint32_t a = w0 ^ 0x80808080u, b = w1 ^ 0x80808080u;  // int8 -> code + 128
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m[i] = __byte_perm(a, 0x4B000000u, 0x7440 + i);
+            m[4 + i] = __byte_perm(b, 0x4B000000u, 0x7440 + i);
+        }
+    } else if constexpr (KB == 4) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = ((w0 >> (4 * i)) & 0xFu) | 0x4B000000u;
+    } else {
+        const uint64_t v = ((uint64_t)w1 << 32 | w0) >> sh;
+        const uint32_t mask = (1u << kb) - 1u, flip = kb == 8 ? 0x80u : 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = ((((uint32_t)(v >> (i * kb))) & mask) ^ flip) | 0x4B000000u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const float2 f = __fmul2_rn(fsub2(make_float2(__uint_as_float(m[i]), __uint_as_float(m[i + 1])),
+                                          make_float2(cz, cz)),
+                                    make_float2(sc, sc));
+        kv[i] = f.x;
+        kv[i + 1] = f.y;
+    }
+}
+
+// Values: 8 codes from (w1:w0) >> sh; vv = centroid * rms * 2^ev.
+template <int VB>
+__device__ __forceinline__ void value_values(uint32_t w0, uint32_t w1, int sh, int vb, float sv, uint32_t lut,
+                                             float (&vv)[8])
+{
+    uint32_t c[8];
+    if constexpr (VB == 3) {
+        const uint32_t x = __funnelshift_r(w0, w1, sh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = (x >> (3 * i)) & 7u;
+    } else {
+        const uint64_t v = ((uint64_t)w1 << 32 | w0) >> sh;
+        const uint32_t mask = (1u << vb) - 1u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = (uint32_t)(v >> (i * vb)) & mask;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) vv[i] = __uint_as_float(tc_lds32(lut + 4 * c[i])) * sv;
+}
+
+template <int D, int KB, int VB>
 __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p)
 {
     using A = TcGeo<D>;
@@ -281,8 +333,7 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
     bool ok = true;
     const uint32_t lut_a = smem_addr(lut);
     const float magic_off = p.kb == 8 ? 8388736.0f : 8388608.0f;  // 2^23 (+ 128: int8 codes read as code + 128)
-    const uint32_t code_flip = p.kb == 8 ? 0x80u : 0u;
-    const uint32_t kmask = (1u << p.kb) - 1u, vmask = (1u << p.vb) - 1u;
+    const int kb = KB ? KB : p.kb, vb = VB ? VB : p.vb;  // compile-time widths for the common schemes
 
     int s = 0;
     for (; s < n_stages; ++s) {
@@ -334,15 +385,11 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
                 const float sc = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_ks + 2 * (t * NG + G))) * sk;
                 const float zc = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_kz + 2 * (t * NG + G)));
                 const float cz = magic_off - zc;  // exact: |zero| <= 65504
-                const int kbyte = c8 * p.kb;
+                const int kbyte = c8 * kb;
                 const uint32_t ka = st + t * p.rbk + (kbyte & ~3);
-                const uint64_t kw = ((uint64_t)tc_lds32(ka + 4) << 32 | tc_lds32(ka)) >> ((kbyte & 3) * 8);
+                const uint32_t k0 = tc_lds32(ka), k1 = (kbyte & 3) + kb > 4 ? tc_lds32(ka + 4) : 0u;
                 float kv[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t code = ((uint32_t)(kw >> (i * p.kb)) & kmask) ^ code_flip;
-                    kv[i] = (__uint_as_float(0x4B000000u | code) - cz) * sc;
-                }
+                key_values<KB>(k0, k1, (kbyte & 3) * 8, kb, sc, cz, kv);
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -354,15 +401,11 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
                 lo4 = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 // values: 8 codes of vb bits at bit 8 * c8 * vb of row t
                 const float sv = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_vs + 2 * (t * NG + G))) * svs;
-                const int vbit = 8 * c8 * p.vb;
+                const int vbit = 8 * c8 * vb;
                 const uint32_t va = st + p.off_v + t * p.rbv + 4 * (vbit >> 5);
-                const uint64_t vw = ((uint64_t)tc_lds32(va + 4) << 32 | tc_lds32(va)) >> (vbit & 31);
+                const uint32_t v0 = tc_lds32(va), v1 = (vbit & 31) + 8 * vb > 32 ? tc_lds32(va + 4) : 0u;
                 float vv[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t code = (uint32_t)(vw >> (i * p.vb)) & vmask;
-                    vv[i] = __uint_as_float(tc_lds32(lut_a + 4 * code)) * sv;
-                }
+                value_values<VB>(v0, v1, vbit & 31, vb, sv, lut_a, vv);
                 v4 = make_uint4(tc_pack_f16(vv[0], vv[1]), tc_pack_f16(vv[2], vv[3]), tc_pack_f16(vv[4], vv[5]),
                                 tc_pack_f16(vv[6], vv[7]));
             }
@@ -490,7 +533,7 @@ struct TcPlan {
     int off_ks, off_kz, off_vs, off_v;
 };
 
-template <int D>
+template <int D, int KB, int VB>
 bool tc_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, TcPlan &pl)
 {
     using A = TcGeo<D>;
@@ -504,7 +547,7 @@ bool tc_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, TcPlan
     pl.smem = 1024 /*align slack*/ + A::OFF_RING + tcRing * pl.stage_bytes + 256 * 4 /*lut*/ + 16 * 4 /*maxima*/ +
               (tcRing + 4) * 8 /*barriers*/ + 16;
     if (pl.smem > 227 * 1024) return false;
-    auto kern = attn_tc_kernel<D>;
+    auto kern = attn_tc_kernel<D, KB, VB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) != cudaSuccess) return false;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, tcThreads, pl.smem) != cudaSuccess || per_sm < 1)
@@ -534,12 +577,12 @@ bool tc_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, TcPlan
     return true;
 }
 
-template <int D>
+template <int D, int KB, int VB>
 cudaError_t tc_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, int64_t seq_len, float scale, float *out,
                    void *ws, size_t ws_bytes, cudaStream_t s)
 {
     TcPlan pl;
-    if (!tc_plan<D>(c, QH, m, seq_len, pl)) return cudaErrorInvalidConfiguration;
+    if (!tc_plan<D, KB, VB>(c, QH, m, seq_len, pl)) return cudaErrorInvalidConfiguration;
     const int G = QH / c.H;
     const size_t parts = (size_t)c.B * c.H * pl.hb * pl.splits * tcCB;
     const size_t need_o = parts * D * 4;
@@ -585,10 +628,28 @@ cudaError_t tc_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, int
     }
     p.vcmax = cm;
     if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
-    attn_tc_kernel<D><<<dim3(pl.splits, c.H * pl.hb, c.B), tcThreads, pl.smem, s>>>(p);
+    attn_tc_kernel<D, KB, VB><<<dim3(pl.splits, c.H * pl.hb, c.B), tcThreads, pl.smem, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, (int)m, pl.hb, tcCB, pl.splits, s);
+}
+
+// compile-time code widths for the common schemes, run-time ones otherwise
+template <int D>
+cudaError_t tc_dispatch(const CacheView &c, const uint16_t *q, int QH, int64_t m, int64_t seq_len, float scale,
+                        float *out, void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    if (c.kb == 8 && c.vb == 3) return tc_run<D, 8, 3>(c, q, QH, m, seq_len, scale, out, ws, ws_bytes, s);
+    if (c.kb == 4 && c.vb == 3) return tc_run<D, 4, 3>(c, q, QH, m, seq_len, scale, out, ws, ws_bytes, s);
+    return tc_run<D, 0, 0>(c, q, QH, m, seq_len, scale, out, ws, ws_bytes, s);
+}
+
+template <int D>
+bool tc_plan_any(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, TcPlan &pl)
+{
+    if (c.kb == 8 && c.vb == 3) return tc_plan<D, 8, 3>(c, q_heads, m, seq_len, pl);
+    if (c.kb == 4 && c.vb == 3) return tc_plan<D, 4, 3>(c, q_heads, m, seq_len, pl);
+    return tc_plan<D, 0, 0>(c, q_heads, m, seq_len, pl);
 }
 
 }  // namespace
@@ -601,7 +662,7 @@ bool attention_tc_applies(const CacheView &c, int q_heads, int64_t m)
 size_t attention_tc_workspace_bytes(const CacheView &c, int q_heads, int64_t m, int64_t seq_len)
 {
     TcPlan pl;
-    bool ok = c.d == 64 ? tc_plan<64>(c, q_heads, m, seq_len, pl) : c.d == 128 ? tc_plan<128>(c, q_heads, m, seq_len, pl)
+    bool ok = c.d == 64 ? tc_plan_any<64>(c, q_heads, m, seq_len, pl) : c.d == 128 ? tc_plan_any<128>(c, q_heads, m, seq_len, pl)
                                                                                  : false;
     if (!ok) return 0;
     return (size_t)c.B * c.H * pl.hb * pl.splits * tcCB * (c.d + 2) * 4;
@@ -611,8 +672,8 @@ cudaError_t launch_attention_tc(const CacheView &c, const uint16_t *q, int q_hea
                                 float scale, float *out, void *ws, size_t ws_bytes, cudaStream_t s)
 {
     switch (c.d) {
-    case 64: return tc_run<64>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
-    case 128: return tc_run<128>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
+    case 64: return tc_dispatch<64>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
+    case 128: return tc_dispatch<128>(c, q, q_heads, m, seq_len, scale, out, ws, ws_bytes, s);
     }
     return cudaErrorInvalidValue;
 }
