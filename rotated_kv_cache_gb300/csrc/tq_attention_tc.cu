@@ -20,9 +20,10 @@
 //     operands with 128-byte swizzle: keys as a two-term split
 //     k = hi + lo (hi = f16(k), lo = f16(k - hi)), so the scores keep the
 //     fp32 key (f16 alone costs ~1e-2 on heavy-tailed keys), K-major; values
-//     centroid * rms, MN-major (rows of dims, as stored).  Each tile is
-//     scaled by a power of two chosen from its group metadata so the f16
-//     range always holds it; the scale is undone on the scores and outputs;
+//     centroid * rms, MN-major (rows of dims, as stored).  Powers of two
+//     keep f16 in range: per key tile, chosen from its group metadata and
+//     undone on the scores; one for all value tiles, fixed by the largest
+//     finite rms, undone on the output;
 //  3. one thread issues S = Q K^T (hi and lo into one accumulator) for both
 //     warpgroups into tensor memory and commits to per-warpgroup mbarriers;
 //  4. each thread reads its column's 64 scores (tcgen05.ld), applies the
@@ -60,7 +61,7 @@ struct TcParams {
     int rbk, rbv, off_ks, off_kz, off_vs, off_v, stage_bytes;
     float scale_log2;   // softmax scale * log2(e)
     float kcmax;        // largest |key code| (127 or 2^kb - 1)
-    float vcmax;        // largest |centroid|
+    float vscale;       // 2^ev: every value tile holds centroid * rms * 2^ev
     float cen[256];     // value centroids (fp32)
 };
 
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem + A::OFF_RING;
     float *lut = reinterpret_cast<float *>(ring + tcRing * p.stage_bytes);
-    float *red = lut + 256;                                      // [2][8] per-warp maxima
+    float *red = lut + 256;                                      // per-warp maxima (16 slots)
     uint64_t *bars = reinterpret_cast<uint64_t *>(red + 16);     // full[tcRing], s[2], o[2]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + tcRing + 4);
     const uint32_t sbase = smem_addr(smem);
@@ -343,38 +344,28 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
         const int64_t t0 = t_begin + (int64_t)s * tcT;
         const int live = (int)imin64(tcT, t_end - t0);  // rows below t_end
 
-        // ---------------- tile exponents from the group metadata of the live rows
-        float bk = 0.0f, bv = 0.0f;
+        // ---------------- key tile exponent from the group metadata of the live rows
+        // (values use one fixed scale, so their sums can run across stages)
+        float bk = 0.0f;
         if (arrived)
             for (int i = tid; i < tcT * NG; i += tcThreads)
                 if (i / NG < live) {
                     const float sc = fabsf(f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_ks + 2 * i)));
                     const float zc = fabsf(f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_kz + 2 * i)));
-                    const float sv = fabsf(f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_vs + 2 * i)));
                     bk = fmaxf(bk, sc * (zc + p.kcmax));
-                    bv = fmaxf(bv, sv * p.vcmax);
                 }
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) {
-            bk = fmaxf(bk, __shfl_xor_sync(0xffffffffu, bk, m));
-            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, m));
-        }
-        if (lane == 0) {
-            red[warp] = bk;
-            red[8 + warp] = bv;
-        }
+        for (int m = 16; m > 0; m >>= 1) bk = fmaxf(bk, __shfl_xor_sync(0xffffffffu, bk, m));
+        if (lane == 0) red[warp] = bk;
         if (!__syncthreads_and(arrived && ok)) {
             ok = false;
             break;
         }
-        float mk = 0.0f, mv = 0.0f;
+        float mk = 0.0f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            mk = fmaxf(mk, red[w]);
-            mv = fmaxf(mv, red[8 + w]);
-        }
-        const int ek = tile_exponent(mk), ev = tile_exponent(mv);
-        const float sk = ldexpf(1.0f, ek), svs = ldexpf(1.0f, ev);
+        for (int w = 0; w < 8; ++w) mk = fmaxf(mk, red[w]);
+        const int ek = tile_exponent(mk);
+        const float sk = ldexpf(1.0f, ek);
 
         // ---------------- dequantise keys (hi, lo) and values into the operand tiles
         for (int it = tid; it < tcT * (D / 8); it += tcThreads) {
@@ -400,7 +391,7 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
                 hi4 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 lo4 = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 // values: 8 codes of vb bits at bit 8 * c8 * vb of row t
-                const float sv = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_vs + 2 * (t * NG + G))) * svs;
+                const float sv = f16_bits_to_f32(*reinterpret_cast<const uint16_t *>(ring + slot * p.stage_bytes + p.off_vs + 2 * (t * NG + G))) * p.vscale;
                 const int vbit = 8 * c8 * vb;
                 const uint32_t va = st + p.off_v + t * p.rbv + 4 * (vbit >> 5);
                 const uint32_t v0 = tc_lds32(va), v1 = (vbit & 31) + 8 * vb > 32 ? tc_lds32(va + 4) : 0u;
@@ -442,10 +433,11 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
         tc_ld32(t_s + t_lane, sr[0]);
         tc_ld32(t_s + t_lane + 32, sr[1]);
         tc_wait_ld();
+        // base-2 logits are x * f with f = ie * 2^-ek > 0, so the maximum is taken on x
         const float f = ie * ldexpf(1.0f, -ek);
         float x[tcT];
 #pragma unroll
-        for (int j = 0; j < tcT; ++j) x[j] = __uint_as_float(sr[j >> 5][j & 31]) * f;
+        for (int j = 0; j < tcT; ++j) x[j] = __uint_as_float(sr[j >> 5][j & 31]);
         if (t0 + tcT > lim_lo) {
             // row t is hidden from query row qi when t >= base0 + qi (this also
             // hides every row at or past t_end)
@@ -457,32 +449,31 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
         float mt = -INFINITY;
 #pragma unroll
         for (int j = 0; j < tcT; ++j) mt = fmaxf(mt, x[j]);
-        const float mn = fmaxf(m_run, mt);
+        const float mn = fmaxf(m_run, mt * f);
         const float mu = mn == -INFINITY ? 0.0f : mn;
         const float alpha = tc_ex2(m_run - mu);
         m_run = mn;
-        float ls = 0.0f;
+        float2 ls = make_float2(0.0f, 0.0f);
         {
             const uint32_t pt = sbase + A::OFF_P + wg * A::PT;
 #pragma unroll
             for (int c = 0; c < tcT / 8; ++c) {
                 float pv[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    pv[i] = tc_ex2(x[8 * c + i] - mu);
-                    ls += pv[i];
-                }
+                for (int i = 0; i < 8; ++i) pv[i] = tc_ex2(fmaf(x[8 * c + i], f, -mu));
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) ls = __fadd2_rn(ls, make_float2(pv[i], pv[i + 1]));
                 sts128(pt + kmaj_off(128, ltid, 8 * c),
                        make_uint4(tc_pack_f16(pv[0], pv[1]), tc_pack_f16(pv[2], pv[3]), tc_pack_f16(pv[4], pv[5]),
                                   tc_pack_f16(pv[6], pv[7])));
             }
         }
-        l_run = l_run * alpha + ls;
+        l_run = l_run * alpha + (ls.x + ls.y);
         fence_proxy_async_smem();
         tc_fence_before();
         named_sync(1 + wg, 128);
         tc_fence_after();
-        // ---------------- O_stage = P V (this warpgroup), then o = o * alpha + O_stage / 2^ev
+        // ---------------- O_stage = P V (this warpgroup), then o = o * alpha + O_stage
         if (ltid == 0) {
             constexpr uint32_t idesc_pv = tc_idesc(128, D, 1);
             constexpr uint32_t SBO = (D / 64) * 1024;
@@ -495,14 +486,19 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
         }
         const bool o_done = mbar_wait_bounded(bar_o0 + 8 * wg, s & 1, p.err);
         tc_fence_after();
-        const float vsc = ldexpf(1.0f, -ev);
+        const float2 alpha2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t orr[32];
             tc_ld32(t_o + t_lane + 32 * c, orr);
             tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[32 * c + j] = fmaf(__uint_as_float(orr[j]), vsc, o[32 * c + j] * alpha);
+            for (int j = 0; j < 32; j += 2) {
+                const float2 r = __ffma2_rn(make_float2(o[32 * c + j], o[32 * c + j + 1]), alpha2,
+                                            make_float2(__uint_as_float(orr[j]), __uint_as_float(orr[j + 1])));
+                o[32 * c + j] = r.x;
+                o[32 * c + j + 1] = r.y;
+            }
         }
         tc_fence_before();
         ok = ok && s_done && o_done;
@@ -515,8 +511,10 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
     {
         const int64_t pidx = ((bh * p.HB + hb) * p.splits + split) * tcCB + 128 * wg + ltid;
         float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * D);
+        const float iv = 1.0f / p.vscale;  // a power of two: exact
 #pragma unroll
-        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        for (int i = 0; i < D / 4; ++i)
+            dst[i] = make_float4(o[4 * i] * iv, o[4 * i + 1] * iv, o[4 * i + 2] * iv, o[4 * i + 3] * iv);
         p.part_ml[2 * pidx] = ok ? m_run : -INFINITY;
         p.part_ml[2 * pidx + 1] = ok ? l_run : 0.0f;
     }
@@ -527,6 +525,13 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------- host side
+inline int tile_exponent_host(float bound)
+{
+    int ex;
+    frexpf(bound, &ex);  // bound = f * 2^ex, f in [0.5, 1)
+    return 14 - ex;
+}
+
 struct TcPlan {
     int hb, splits, stage_bytes, smem;
     int64_t tokens_per_split;
@@ -626,7 +631,9 @@ cudaError_t tc_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, int
         p.cen[i] = tab.centroids[i];
         cm = cm > fabsf(tab.centroids[i]) ? cm : fabsf(tab.centroids[i]);
     }
-    p.vcmax = cm;
+    // one power of two for every value tile: the largest finite rms (65504)
+    // times the largest centroid lands in [2^13, 2^14), so f16 always holds them
+    p.vscale = ldexpf(1.0f, tile_exponent_host(65504.0f * cm));
     if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
     attn_tc_kernel<D, KB, VB><<<dim3(pl.splits, c.H * pl.hb, c.B), tcThreads, pl.smem, s>>>(p);
     cudaError_t e = cudaGetLastError();
