@@ -28,8 +28,9 @@
 //     warpgroups into tensor memory and commits to per-warpgroup mbarriers;
 //  4. each thread reads its column's 64 scores (tcgen05.ld), applies the
 //     causal limit, runs the online base-2 softmax in registers and writes
-//     its row of P (f16, K-major) to shared memory;
-//  5. the warpgroup's first thread issues O_stage = P V into tensor memory;
+//     its row of P (f16) over its scores in tensor memory (tcgen05.st);
+//  5. the warpgroup's first thread issues O_stage = P V into tensor memory
+//     (A operand from tensor memory, so P never touches shared memory);
 //     each thread adds its row of O_stage into its register accumulator,
 //     rescaled by the running maximum.
 // The output of a CTA is the per-column (o, m, l) partial; the generic
@@ -91,6 +92,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// A operand in tensor memory (M = 128 lanes, two f16 per 32-bit column, the
+// even k in the low half), B from shared memory
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
 __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -112,7 +123,21 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "r"(taddr));
 }
 
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
@@ -169,9 +194,8 @@ struct TcGeo {
     static constexpr int KT = tcT * D * 2;     // one key tile (hi or lo): 64 rows x D f16
     static constexpr int VT = tcT * D * 2;     // value tile
     static constexpr int QT = 128 * D * 2;     // one warpgroup's q tile
-    static constexpr int PT = 128 * tcT * 2;   // one warpgroup's P tile
-    static constexpr int OFF_KH = 0, OFF_KL = KT, OFF_V = 2 * KT, OFF_Q = 2 * KT + VT, OFF_P = OFF_Q + tcWG * QT;
-    static constexpr int OFF_RING = OFF_P + tcWG * PT;  // packed stages follow (stage_bytes each)
+    static constexpr int OFF_KH = 0, OFF_KL = KT, OFF_V = 2 * KT, OFF_Q = 2 * KT + VT;
+    static constexpr int OFF_RING = OFF_Q + tcWG * QT;  // packed stages follow (stage_bytes each)
     static constexpr int SPAN = 64 + D;                  // tensor-memory columns per warpgroup: S, then O
     static constexpr int TMEM_COLS = tcWG * SPAN <= 256 ? 256 : 512;
     static constexpr int WG_COLS = TMEM_COLS / tcWG;
@@ -453,23 +477,21 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
         const float mu = mn == -INFINITY ? 0.0f : mn;
         const float alpha = tc_ex2(m_run - mu);
         m_run = mn;
+        // P (f16) overwrites the first 32 columns of this thread's score row in
+        // tensor memory: the A operand of P V
         float2 ls = make_float2(0.0f, 0.0f);
         {
-            const uint32_t pt = sbase + A::OFF_P + wg * A::PT;
+            uint32_t pp[tcT / 2];
 #pragma unroll
-            for (int c = 0; c < tcT / 8; ++c) {
-                float pv[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) pv[i] = tc_ex2(fmaf(x[8 * c + i], f, -mu));
-#pragma unroll
-                for (int i = 0; i < 8; i += 2) ls = __fadd2_rn(ls, make_float2(pv[i], pv[i + 1]));
-                sts128(pt + kmaj_off(128, ltid, 8 * c),
-                       make_uint4(tc_pack_f16(pv[0], pv[1]), tc_pack_f16(pv[2], pv[3]), tc_pack_f16(pv[4], pv[5]),
-                                  tc_pack_f16(pv[6], pv[7])));
+            for (int j = 0; j < tcT; j += 2) {
+                const float p0 = tc_ex2(fmaf(x[j], f, -mu)), p1 = tc_ex2(fmaf(x[j + 1], f, -mu));
+                ls = __fadd2_rn(ls, make_float2(p0, p1));
+                pp[j / 2] = tc_pack_f16(p0, p1);
             }
+            tc_st32(t_s + t_lane, pp);
+            tc_wait_st();
         }
         l_run = l_run * alpha + (ls.x + ls.y);
-        fence_proxy_async_smem();
         tc_fence_before();
         named_sync(1 + wg, 128);
         tc_fence_after();
@@ -477,11 +499,9 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
         if (ltid == 0) {
             constexpr uint32_t idesc_pv = tc_idesc(128, D, 1);
             constexpr uint32_t SBO = (D / 64) * 1024;
-            const uint32_t pt = sbase + A::OFF_P + wg * A::PT;
 #pragma unroll
             for (int kk = 0; kk < tcT / 16; ++kk)
-                tc_mma(t_o, tc_desc(pt + kk * 32, 16, 1024), tc_desc(sbase + A::OFF_V + kk * 2 * SBO, 1024, SBO),
-                       idesc_pv, kk > 0);
+                tc_mma_ts(t_o, t_s + kk * 8, tc_desc(sbase + A::OFF_V + kk * 2 * SBO, 1024, SBO), idesc_pv, kk > 0);
             tc_commit(bar_o0 + 8 * wg);
         }
         const bool o_done = mbar_wait_bounded(bar_o0 + 8 * wg, s & 1, p.err);
