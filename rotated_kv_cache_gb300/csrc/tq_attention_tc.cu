@@ -44,7 +44,7 @@
 namespace tq {
 namespace {
 
-constexpr int tcT = 64;            // cache rows per stage (the QK MMA's N, the PV MMA's K)
+constexpr int tcT = 128;           // cache rows per stage (the QK MMA's N, the PV MMA's K)
 constexpr int tcWG = 2;            // warpgroups per CTA
 constexpr int tcThreads = 128 * tcWG;
 constexpr int tcCB = 128 * tcWG;   // columns per CTA
@@ -123,16 +123,14 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "r"(taddr));
 }
 
-// 32 consecutive 32-bit columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
 {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
@@ -191,12 +189,12 @@ __device__ __forceinline__ int tile_exponent(float bound)
 template <int D>
 struct TcGeo {
     static constexpr int NG = D / 32;
-    static constexpr int KT = tcT * D * 2;     // one key tile (hi or lo): 64 rows x D f16
+    static constexpr int KT = tcT * D * 2;     // one key tile (hi or lo): tcT rows x D f16
     static constexpr int VT = tcT * D * 2;     // value tile
     static constexpr int QT = 128 * D * 2;     // one warpgroup's q tile
     static constexpr int OFF_KH = 0, OFF_KL = KT, OFF_V = 2 * KT, OFF_Q = 2 * KT + VT;
     static constexpr int OFF_RING = OFF_Q + tcWG * QT;  // packed stages follow (stage_bytes each)
-    static constexpr int SPAN = 64 + D;                  // tensor-memory columns per warpgroup: S, then O
+    static constexpr int SPAN = tcT + D;                 // tensor-memory columns per warpgroup: S (then P), then O
     static constexpr int TMEM_COLS = tcWG * SPAN <= 256 ? 256 : 512;
     static constexpr int WG_COLS = TMEM_COLS / tcWG;
 };
@@ -348,7 +346,7 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t t_s = tmem + wg * A::WG_COLS, t_o = t_s + 64;
+    const uint32_t t_s = tmem + wg * A::WG_COLS, t_o = t_s + tcT;
     const uint32_t t_lane = (uint32_t)(32 * wq) << 16;
 
     float o[D];
@@ -453,44 +451,48 @@ __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_cons
         // ---------------- softmax of this thread's column over the stage's rows
         const bool s_done = mbar_wait_bounded(bar_s0 + 8 * wg, s & 1, p.err);
         tc_fence_after();
-        uint32_t sr[2][32];
-        tc_ld32(t_s + t_lane, sr[0]);
-        tc_ld32(t_s + t_lane + 32, sr[1]);
-        tc_wait_ld();
-        // base-2 logits are x * f with f = ie * 2^-ek > 0, so the maximum is taken on x
+        // base-2 logits are x * f with f = ie * 2^-ek > 0, so the maximum is taken
+        // on x; rows j >= vis are hidden from this query row (this also hides
+        // every row at or past t_end)
         const float f = ie * ldexpf(1.0f, -ek);
-        float x[tcT];
-#pragma unroll
-        for (int j = 0; j < tcT; ++j) x[j] = __uint_as_float(sr[j >> 5][j & 31]);
-        if (t0 + tcT > lim_lo) {
-            // row t is hidden from query row qi when t >= base0 + qi (this also
-            // hides every row at or past t_end)
-            const int64_t vis = p.base0 + qi - t0;
-#pragma unroll
-            for (int j = 0; j < tcT; ++j)
-                if (j >= vis) x[j] = -INFINITY;
-        }
+        const int64_t vis = t0 + tcT > lim_lo ? p.base0 + qi - t0 : (int64_t)tcT;
+        // pass 1: the maximum over the stage (32 scores at a time)
         float mt = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < tcT / 32; ++c) {
+            uint32_t sr[32];
+            tc_ld32(t_s + t_lane + 32 * c, sr);
+            tc_wait_ld();
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < tcT; ++j) mt = fmaxf(mt, x[j]);
+            for (int j = 0; j < 32; ++j)
+                if (32 * c + j < vis) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sr[j]));
+            mt = fmaxf(mt, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        }
         const float mn = fmaxf(m_run, mt * f);
         const float mu = mn == -INFINITY ? 0.0f : mn;
         const float alpha = tc_ex2(m_run - mu);
         m_run = mn;
-        // P (f16) overwrites the first 32 columns of this thread's score row in
-        // tensor memory: the A operand of P V
+        // pass 2: the weights; P (f16, two per column) overwrites the row's first
+        // tcT / 2 columns in tensor memory, always behind the columns still to
+        // be read, and becomes the A operand of P V
         float2 ls = make_float2(0.0f, 0.0f);
-        {
-            uint32_t pp[tcT / 2];
+#pragma unroll 1
+        for (int c = 0; c < tcT / 32; ++c) {
+            uint32_t sr[32], pp[16];
+            tc_ld32(t_s + t_lane + 32 * c, sr);
+            tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < tcT; j += 2) {
-                const float p0 = tc_ex2(fmaf(x[j], f, -mu)), p1 = tc_ex2(fmaf(x[j + 1], f, -mu));
+            for (int j = 0; j < 32; j += 2) {
+                const float x0 = 32 * c + j < vis ? __uint_as_float(sr[j]) : -INFINITY;
+                const float x1 = 32 * c + j + 1 < vis ? __uint_as_float(sr[j + 1]) : -INFINITY;
+                const float p0 = tc_ex2(fmaf(x0, f, -mu)), p1 = tc_ex2(fmaf(x1, f, -mu));
                 ls = __fadd2_rn(ls, make_float2(p0, p1));
                 pp[j / 2] = tc_pack_f16(p0, p1);
             }
-            tc_st32(t_s + t_lane, pp);
-            tc_wait_st();
+            tc_st16(t_s + t_lane + 16 * c, pp);
         }
+        tc_wait_st();
         l_run = l_run * alpha + (ls.x + ls.y);
         tc_fence_before();
         named_sync(1 + wg, 128);
@@ -558,19 +560,27 @@ struct TcPlan {
     int off_ks, off_kz, off_vs, off_v;
 };
 
-template <int D, int KB, int VB>
-bool tc_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, TcPlan &pl)
+// packed stage layout (key codes, key scales, key zeros, value rms, value
+// codes) and the kernel's dynamic shared memory
+template <int D>
+void tc_layout(int kb, int vb, TcPlan &pl)
 {
-    using A = TcGeo<D>;
-    const int NG = D / 32, rbk = D * c.kb / 8, rbv = D * c.vb / 8;
+    const int NG = D / 32, rbk = D * kb / 8, rbv = D * vb / 8;
     auto r16 = [](int x) { return (x + 15) / 16 * 16; };
     pl.off_ks = r16(tcT * rbk);
     pl.off_kz = pl.off_ks + r16(tcT * NG * 2);
     pl.off_vs = pl.off_kz + r16(tcT * NG * 2);
     pl.off_v = pl.off_vs + r16(tcT * NG * 2);
     pl.stage_bytes = (pl.off_v + tcT * rbv + 16 + 127) / 128 * 128;
-    pl.smem = 1024 /*align slack*/ + A::OFF_RING + tcRing * pl.stage_bytes + 256 * 4 /*lut*/ + 16 * 4 /*maxima*/ +
-              (tcRing + 4) * 8 /*barriers*/ + 16;
+    pl.smem = 1024 /*align slack*/ + TcGeo<D>::OFF_RING + tcRing * pl.stage_bytes + 256 * 4 /*lut*/ +
+              16 * 4 /*maxima*/ + (tcRing + 4) * 8 /*barriers*/ + 16;
+}
+
+template <int D, int KB, int VB>
+bool tc_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, TcPlan &pl)
+{
+    using A = TcGeo<D>;
+    tc_layout<D>(c.kb, c.vb, pl);
     if (pl.smem > 227 * 1024) return false;
     auto kern = attn_tc_kernel<D, KB, VB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) != cudaSuccess) return false;
@@ -683,7 +693,11 @@ bool tc_plan_any(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, Tc
 
 bool attention_tc_applies(const CacheView &c, int q_heads, int64_t m)
 {
-    return (c.d == 64 || c.d == 128) && (int64_t)(q_heads / c.H) * m >= 128;
+    if ((c.d != 64 && c.d != 128) || (int64_t)(q_heads / c.H) * m < 128) return false;
+    TcPlan pl;  // the packed ring must fit beside the operand tiles
+    if (c.d == 64) tc_layout<64>(c.kb, c.vb, pl);
+    else tc_layout<128>(c.kb, c.vb, pl);
+    return pl.smem <= 227 * 1024;
 }
 
 size_t attention_tc_workspace_bytes(const CacheView &c, int q_heads, int64_t m, int64_t seq_len)
