@@ -45,6 +45,7 @@ PREFILL = dict(B=4, H=8, T=8192, d=128, kb=8, vb=3)
 DECODE = dict(B=32, H=8, QH=64, T=32768, d=128, kb=8, vb=3)
 BYTES_PER_TH = 200  # k8v3, d128 (page section "Algorithm", bytes per token-head)
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0  # dense bf16, one earlier GB300 measurement
 
 
 # ------------------------------------------------------------------ helpers
@@ -68,6 +69,16 @@ def measured_peaks():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 tensor peak (cuBLAS, burst) from MEASURED_PEAKS.json, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def attention_traffic(kernel_hash: str):
@@ -510,12 +521,16 @@ def run_sweep(only=None):
             ts.append(a.elapsed_time(b) * 1e3 / reps)
         return statistics.median(ts)
 
+    tpeak, tkind = measured_bf16_tflops()
+
     def emit(kind_, config, us, nbytes, flops=None):
         gbs = nbytes / (us * 1e-6) / 1e9
         line = {"sweep": kind_, "config": config, "us": round(us, 2), "GB/s": round(gbs, 1),
                 "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": kind}
-        if flops is not None:
-            line["TFLOP/s"] = round(flops / (us * 1e-6) / 1e12, 1)
+        if flops is not None:  # a contraction: its roofline is the tensor peak
+            tf = flops / (us * 1e-6) / 1e12
+            line.update({"TFLOP/s": round(tf, 1), "tensor_frac": round(tf / tpeak, 4), "tensor_peak": tpeak,
+                         "tensor_peak_kind": tkind})
         print(json.dumps(line), flush=True)
 
     def filled_cache(B, H, d, T, kb, vb, w):
