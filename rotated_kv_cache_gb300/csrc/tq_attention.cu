@@ -17,7 +17,8 @@
 //    mbarrier; the last warp to finish a stage issues the copies that refill
 //    its slot, so no warp is set aside as a producer (4 CTAs fit on an SM).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
-//    tokens, N = the G = 8 q-heads sharing the kv-head, K = head_dim.  Key codes
+//    tokens, N = 8 columns: the G <= 8 q-heads sharing the kv-head (columns
+//    past G hold zero q and are dropped), K = head_dim.  Key codes
 //    become exact f16 integers with one XOR and byte permutes (1024 + code), so
 //    S = sum_g scale_g * (acc_g + (zero_g - offset) * sum_{j in g} q_j) -- the
 //    per-group affine is applied to the 8-head scores, not to each element.
@@ -40,7 +41,7 @@ namespace tq {
 namespace {
 
 constexpr int kD = 128;            // head_dim covered
-constexpr int kG = 8;              // q-heads per kv-head
+constexpr int kG = 8;              // MMA columns: q-heads per kv-head, up to 8 (the rest zero)
 constexpr int kVB = 3;             // value bits covered
 constexpr int kCW = 4;             // warps per CTA (all compute; the last to finish a stage refills it)
 constexpr int kThreads = kCW * 32;
@@ -73,7 +74,7 @@ struct AttnParams {
     const uint16_t *q;  // [B][QH][D] bf16
     float *part_o;      // [B][H][S][G][D]
     float *part_ml;     // [B][H][S][G][2]
-    int H, QH, splits;
+    int H, QH, G, splits;  // G = QH / H q-heads per kv-head (1..kG)
     int64_t cap, seq_len, tokens_per_split;
     float scale_log2;  // softmax_scale * log2(e)
     uint32_t *err;
@@ -223,12 +224,14 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
     float qs[4][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
     float ie[2];     // per head: 2^-e * softmax_scale * log2(e)
     {
-        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * kG + g) * kD;
+        // heads g >= G are padding columns: zero q, their partials are never read
+        const bool head_real = g < p.G;
+        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (head_real ? g : 0)) * kD;
         float qv[4][8];
         float mx = 0.0f;
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * G + 8 * c);
+            const uint4 w = head_real ? *reinterpret_cast<const uint4 *>(qrow + 32 * G + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
 struct CombineParams {
     const float *part_o, *part_ml;
     float *out;  // [B][QH][D]
-    int H, QH, splits;
+    int H, QH, G, splits, rows;  // rows = B * QH
     float inv_sqrt_d;
 };
 
@@ -536,8 +539,9 @@ struct CombineParams {
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineParams p)
 {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= p.rows) return;  // whole warps only
     const int b = row / p.QH, qh = row % p.QH;
-    const int h = qh / kG, hh = qh % kG;
+    const int h = qh / p.G, hh = qh % p.G;
     const int64_t base = ((int64_t)b * p.H + h) * p.splits;
     float mmax = -INFINITY;
     for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * kG + hh)]);
@@ -669,6 +673,7 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + need_o);
     p.H = c.H;
     p.QH = QH;
+    p.G = QH / c.H;
     p.splits = plan.splits;
     p.cap = c.cap;
     p.seq_len = seq_len;
@@ -702,10 +707,11 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     cp.out = out;
     cp.H = c.H;
     cp.QH = QH;
+    cp.G = QH / c.H;
+    cp.rows = c.B * QH;
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
-    const int rows = c.B * QH;  // multiple of 8 (QH = 8 H)
-    attn_combine_kernel<<<rows / 8, 256, 0, s>>>(cp);
+    attn_combine_kernel<<<(cp.rows + 7) / 8, 256, 0, s>>>(cp);
     return cudaGetLastError();
 }
 
@@ -713,7 +719,7 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
 
 bool attention_supported(int d, int kb, int vb, int group)
 {
-    return d == kD && vb == kVB && group == kG && (kb == 8 || kb == 4);
+    return d == kD && vb == kVB && group >= 1 && group <= kG && (kb == 8 || kb == 4);
 }
 
 size_t attention_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)
@@ -797,6 +803,7 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
     p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + need_o);
     p.H = c.H;
     p.QH = QH;
+    p.G = QH / c.H;
     p.splits = plan.splits;
     p.cap = c.cap;
     p.seq_len = seq_len;
@@ -829,9 +836,11 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
     cp.out = out;
     cp.H = c.H;
     cp.QH = QH;
+    cp.G = QH / c.H;
+    cp.rows = c.B * QH;
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
-    attn_combine_kernel<<<c.B * QH / 8, 256, 0, s>>>(cp);
+    attn_combine_kernel<<<(cp.rows + 7) / 8, 256, 0, s>>>(cp);
     return cudaGetLastError();
 }
 

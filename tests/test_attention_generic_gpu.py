@@ -1,6 +1,6 @@
 """Decode attention for every head_dim, bit pair and GQA group size (the
-generic kernel; head_dim 128 k8/k4 v3 with groups of 8 take the specialised
-kernel) against the binary64 oracle.  Tolerance: 2e-3 max-abs on the fp32
+generic kernel; head_dim 128 k8/k4 v3 with groups of 1 to 8 take the
+specialised kernel) against the binary64 oracle.  Tolerance: 2e-3 max-abs on the fp32
 output, as for the specialised kernel.
 """
 import numpy as np
@@ -38,6 +38,14 @@ def test_every_width_and_head_dim(cuda, d, kb, vb):
 @pytest.mark.parametrize("G", [1, 2, 3, 6, 12, 16])
 def test_group_sizes(cuda, G):
     err = _run(cuda, 128, 8, 3, B=2, H=3, G=G, T=201, step=G)
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("kb,G,T", [(8, 4, 5000), (4, 4, 3001), (8, 7, 2050), (4, 1, 777), (8, 5, 64)])
+def test_specialised_kernel_small_groups(cuda, kb, G, T):
+    """Groups below 8 on the specialised kernel (the MMA's 8 columns, those past
+    G zero): several splits, ragged stage tails, ragged combine blocks."""
+    err = _run(cuda, 128, kb, 3, B=3, H=3, G=G, T=T, cap=T + (16 - T % 16) % 16 + 16, step=G)
     assert err < TOL, err
 
 

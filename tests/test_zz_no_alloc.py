@@ -56,6 +56,18 @@ def test_noalloc_small_ragged(cuda, kb):
 
 
 @pytest.mark.gpu
+def test_noalloc_group_of_four(cuda):
+    """4 q-heads per kv-head (half the specialised kernel's columns)."""
+    w = tq_synth.WORKLOADS["decode"]
+    B, H, T = 3, 2, 1500
+    k, v = tq_synth.host_kv(w, B=B, H=H, n=T)
+    cache = cuda.Cache(B, H, w.d, T, k_bits=8, v_bits=w.vb)
+    cuda.tq_encode_append(cache, to_device_bf16(k), to_device_bf16(v), 0)
+    qs = [to_device_bf16(tq_synth.host_q(w, step, B=B, QH=4 * H)) for step in (0, 1)]
+    _two_calls_match(cuda, cache, qs, T)
+
+
+@pytest.mark.gpu
 def test_noalloc_fewer_splits_than_usual(cuda):
     """64 sequences x 8 kv-heads x 8193 rows: the usual split plan needs more
     than the 16 MiB scratch, so this entry point runs with fewer splits."""
@@ -94,4 +106,5 @@ def test_noalloc_rejects_problems_beyond_the_scratch(tqlib):
     s = tqlib._CacheStruct(128, 8, 3, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
     assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 17, 1.0, 0x20000, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 16, 1.0, 0x20004, None) == S["TQ_ERR_ALIGN"]
-    assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 4, 16, 1.0, 0x20000, None) == S["TQ_ERR_UNSUPPORTED"]
+    # more than 8 q-heads per kv-head is outside the specialised kernel
+    assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 16, 16, 1.0, 0x20000, None) == S["TQ_ERR_UNSUPPORTED"]
