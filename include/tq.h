@@ -205,8 +205,9 @@ TQ_API size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_head
  * with t0 = seq_len - 1), as the page's updateAndFetch does.
  * Every head_dim, bit pair and group size G >= 1 is covered: head_dim 128
  * with 8- or 4-bit keys, 3-bit values and 1 <= G <= 8 run a specialised
- * kernel (8 MMA columns per kv-head, those past G zero), the rest a generic one (code widths read at run time, groups in blocks of 8
- * q-heads); both meet the same tolerance.
+ * kernel (8 MMA columns per kv-head, those past G dropped), the rest a
+ * generic one (code widths read at run time, groups in blocks of 8 q-heads);
+ * both meet the same tolerance.
  */
 TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
                               float softmax_scale, float *out, void *workspace, size_t workspace_bytes,

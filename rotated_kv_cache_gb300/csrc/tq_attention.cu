@@ -18,7 +18,7 @@
 //    its slot, so no warp is set aside as a producer (4 CTAs fit on an SM).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
 //    tokens, N = 8 columns: the G <= 8 q-heads sharing the kv-head (columns
-//    past G hold zero q and are dropped), K = head_dim.  Key codes
+//    past G repeat the last head and are dropped), K = head_dim.  Key codes
 //    become exact f16 integers with one XOR and byte permutes (1024 + code), so
 //    S = sum_g scale_g * (acc_g + (zero_g - offset) * sum_{j in g} q_j) -- the
 //    per-group affine is applied to the 8-head scores, not to each element.
@@ -224,14 +224,14 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
     float qs[4][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
     float ie[2];     // per head: 2^-e * softmax_scale * log2(e)
     {
-        // heads g >= G are padding columns: zero q, their partials are never read
-        const bool head_real = g < p.G;
-        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (head_real ? g : 0)) * kD;
+        // heads g >= G are padding columns: they repeat head G-1 (MMA columns never
+        // mix) and their partials are never read
+        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (g < p.G ? g : p.G - 1)) * kD;
         float qv[4][8];
         float mx = 0.0f;
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
-            const uint4 w = head_real ? *reinterpret_cast<const uint4 *>(qrow + 32 * G + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * G + 8 * c);
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
