@@ -570,7 +570,7 @@ def run_sweep(only=None):
         out = torch.empty((B, G * H, d), dtype=torch.float32, device="cuda")
         ws = torch.empty(tq.tq_attention_workspace_bytes(cache, G * H, T), dtype=torch.uint8, device="cuda")
         us = timed(lambda: tq.tq_decode_attention(cache, qb, T, out=out, workspace=ws))
-        path = "specialised" if (d, vb) == (128, 3) and 1 <= G <= 8 and kb in (8, 4) else "generic"
+        path = "specialised" if (d, vb) == (128, 3) and kb in (8, 4) else "generic"
         emit("attention", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": kb, "vb": vb, "group": G, "kernel": path},
              us, B * H * T * bpt + B * G * H * d * 6)
         del cache, ws, out, q

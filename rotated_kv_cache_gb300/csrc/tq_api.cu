@@ -346,7 +346,7 @@ tq_status tq_decode_attention_noalloc(const tq_cache *c, const void *q, int32_t 
     if (!aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
     if (!tq::attention_supported(c->head_dim, c->k_bits, c->v_bits, q_heads / c->num_kv_heads))
         return TQ_ERR_UNSUPPORTED;
-    if (!tq::noalloc_fits(view(c))) return TQ_ERR_SCRATCH;
+    if (!tq::noalloc_fits(view(c), q_heads)) return TQ_ERR_SCRATCH;
     return cuda_status(tq::launch_attention_noalloc(view(c), static_cast<const uint16_t *>(q), q_heads, seq_len,
                                                     scale, out, (cudaStream_t)stream));
 }

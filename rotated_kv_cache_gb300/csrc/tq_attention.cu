@@ -17,8 +17,10 @@
 //    mbarrier; the last warp to finish a stage issues the copies that refill
 //    its slot, so no warp is set aside as a producer (4 CTAs fit on an SM).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
-//    tokens, N = 8 columns: the G <= 8 q-heads sharing the kv-head (columns
-//    past G repeat the last head and are dropped), K = head_dim.  Key codes
+//    tokens, N = 8 columns: 8 of the G q-heads sharing the kv-head (a group
+//    above 8 takes ceil(G/8) CTAs, neighbours in the grid so their reads of
+//    the same rows meet in L2; columns past G repeat the last head and are
+//    dropped), K = head_dim.  Key codes
 //    become exact f16 integers with one XOR and byte permutes (1024 + code), so
 //    S = sum_g scale_g * (acc_g + (zero_g - offset) * sum_{j in g} q_j) -- the
 //    per-group affine is applied to the 8-head scores, not to each element.
@@ -50,6 +52,9 @@ constexpr int kStages = 3;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// blocks of kG q-heads (MMA columns) per kv-head
+inline int col_blocks(int group) { return (group + kG - 1) / kG; }
+
 template <int KB>
 struct AGeo {
     static constexpr int KROW = kD * KB / 8;                   // key code bytes per token
@@ -74,7 +79,7 @@ struct AttnParams {
     const uint16_t *q;  // [B][QH][D] bf16
     float *part_o;      // [B][H][S][G][D]
     float *part_ml;     // [B][H][S][G][2]
-    int H, QH, G, splits;  // G = QH / H q-heads per kv-head (1..kG)
+    int H, QH, G, NB, splits;  // G = QH / H q-heads per kv-head; NB = ceil(G / kG) column blocks
     int64_t cap, seq_len, tokens_per_split;
     float scale_log2;  // softmax_scale * log2(e)
     uint32_t *err;
@@ -185,7 +190,10 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
     const uint32_t full0 = smem_addr(bars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // blockIdx.y = (kv-head, block of kG q-heads); the blocks of one kv-head are
+    // neighbours in the grid, so their reads of the same rows meet in L2
+    const int split = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    const int h = hv / p.NB, hb = hv - h * p.NB;
     const int64_t bh = (int64_t)b * p.H + h;
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = imin64(p.seq_len, t_begin + p.tokens_per_split);
@@ -224,9 +232,10 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
     float qs[4][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
     float ie[2];     // per head: 2^-e * softmax_scale * log2(e)
     {
-        // heads g >= G are padding columns: they repeat head G-1 (MMA columns never
-        // mix) and their partials are never read
-        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (g < p.G ? g : p.G - 1)) * kD;
+        // columns past the last q-head are padding: they repeat head G-1 (MMA
+        // columns never mix) and their partials are never read
+        const int gq = kG * hb + g;
+        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (gq < p.G ? gq : p.G - 1)) * kD;
         float qv[4][8];
         float mx = 0.0f;
 #pragma unroll
@@ -517,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 8; ++i) ov[i] += m2[hh * kD + d8 + i] * wt;
     }
-    const int64_t pidx = (bh * p.splits + split) * kG + hh;
+    const int64_t pidx = (((int64_t)b * p.H * p.NB + hv) * p.splits + split) * kG + hh;
     float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * kD + d8);
     dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
     dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
@@ -531,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
 struct CombineParams {
     const float *part_o, *part_ml;
     float *out;  // [B][QH][D]
-    int H, QH, G, splits, rows;  // rows = B * QH
+    int H, QH, G, NB, splits, rows;  // rows = B * QH
     float inv_sqrt_d;
 };
 
@@ -541,8 +550,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= p.rows) return;  // whole warps only
     const int b = row / p.QH, qh = row % p.QH;
-    const int h = qh / p.G, hh = qh % p.G;
-    const int64_t base = ((int64_t)b * p.H + h) * p.splits;
+    const int h = qh / p.G, hq = qh % p.G;
+    const int hh = hq % kG;  // column of block hq / kG
+    const int64_t base = ((int64_t)b * p.H * p.NB + (int64_t)h * p.NB + hq / kG) * p.splits;
     float mmax = -INFINITY;
     for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * kG + hh)]);
     const float mu = mmax == -INFINITY ? 0.0f : mmax;
@@ -646,9 +656,10 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     using A = AGeo<KB>;
     cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
     if (e != cudaSuccess) return e;
-    const SplitPlan plan = plan_splits(c.B, c.H, seq_len, ctas_per_sm_for<KB>());
-    const size_t need_o = (size_t)c.B * c.H * plan.splits * kG * kD * 4;
-    const size_t need = need_o + (size_t)c.B * c.H * plan.splits * kG * 2 * 4;
+    const int NB = col_blocks(QH / c.H);
+    const SplitPlan plan = plan_splits(c.B, c.H * NB, seq_len, ctas_per_sm_for<KB>());
+    const size_t need_o = (size_t)c.B * c.H * NB * plan.splits * kG * kD * 4;
+    const size_t need = need_o + (size_t)c.B * c.H * NB * plan.splits * kG * 2 * 4;
     if (ws_bytes < need) return cudaErrorInvalidValue;
 
     auto fn = encode_fn();
@@ -674,6 +685,7 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     p.H = c.H;
     p.QH = QH;
     p.G = QH / c.H;
+    p.NB = col_blocks(p.G);
     p.splits = plan.splits;
     p.cap = c.cap;
     p.seq_len = seq_len;
@@ -696,7 +708,7 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     p.k_const = KB == 8 ? 0xFF00FF00u : 0xFFF0FFF0u;
     p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
 
-    dim3 grid(plan.splits, c.H, c.B);
+    dim3 grid(plan.splits, c.H * p.NB, c.B);
     attn_split_kernel<KB><<<grid, kThreads, A::SMEM, s>>>(map, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -708,6 +720,7 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     cp.H = c.H;
     cp.QH = QH;
     cp.G = QH / c.H;
+    cp.NB = col_blocks(cp.G);
     cp.rows = c.B * QH;
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
@@ -719,15 +732,16 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
 
 bool attention_supported(int d, int kb, int vb, int group)
 {
-    return d == kD && vb == kVB && group >= 1 && group <= kG && (kb == 8 || kb == 4);
+    return d == kD && vb == kVB && group >= 1 && (kb == 8 || kb == 4);
 }
 
 size_t attention_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)
 {
     if (!attention_supported(c.d, c.kb, c.vb, q_heads / c.H)) return 0;
     const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
-    const SplitPlan plan = plan_splits(c.B, c.H, seq_len, per_sm);
-    return (size_t)c.B * c.H * plan.splits * kG * (kD + 2) * 4;
+    const int NB = col_blocks(q_heads / c.H);
+    const SplitPlan plan = plan_splits(c.B, c.H * NB, seq_len, per_sm);
+    return (size_t)c.B * c.H * NB * plan.splits * kG * (kD + 2) * 4;
 }
 
 cudaError_t launch_attention(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
@@ -779,7 +793,7 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
     using A = AGeo<KB>;
     cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
     if (e != cudaSuccess) return e;
-    const size_t need_o = (size_t)c.B * c.H * plan.splits * kG * kD * 4;
+    const size_t need_o = (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * kD * 4;
 
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
@@ -804,6 +818,7 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
     p.H = c.H;
     p.QH = QH;
     p.G = QH / c.H;
+    p.NB = col_blocks(p.G);
     p.splits = plan.splits;
     p.cap = c.cap;
     p.seq_len = seq_len;
@@ -825,7 +840,7 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
     p.k_const = KB == 8 ? 0xFF00FF00u : 0xFFF0FFF0u;
     p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
 
-    dim3 grid(plan.splits, c.H, c.B);
+    dim3 grid(plan.splits, c.H * p.NB, c.B);
     attn_split_kernel<KB><<<grid, kThreads, A::SMEM, s>>>(map, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -837,6 +852,7 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
     cp.H = c.H;
     cp.QH = QH;
     cp.G = QH / c.H;
+    cp.NB = col_blocks(cp.G);
     cp.rows = c.B * QH;
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
@@ -848,7 +864,10 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
 
 size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
-bool noalloc_fits(const CacheView &c) { return (size_t)c.B * c.H * kG * (kD + 2) * 4 <= kNoAllocScratchBytes; }
+bool noalloc_fits(const CacheView &c, int q_heads)
+{
+    return (size_t)c.B * c.H * col_blocks(q_heads / c.H) * kG * (kD + 2) * 4 <= kNoAllocScratchBytes;
+}
 
 cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
                                      float *out, cudaStream_t s)
@@ -857,8 +876,9 @@ cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int 
     if (!scratch) return cudaErrorInvalidSymbol;
     // the usual split plan, with fewer splits if its partials would not fit
     const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
-    SplitPlan plan = plan_splits(c.B, c.H, seq_len, per_sm);
-    const size_t per_split = (size_t)c.B * c.H * kG * (kD + 2) * 4;
+    const int NB = col_blocks(q_heads / c.H);
+    SplitPlan plan = plan_splits(c.B, c.H * NB, seq_len, per_sm);
+    const size_t per_split = (size_t)c.B * c.H * NB * kG * (kD + 2) * 4;
     const int64_t max_splits = (int64_t)(kNoAllocScratchBytes / per_split);
     if (max_splits < 1) return cudaErrorInvalidValue;
     if (plan.splits > max_splits) {

@@ -82,7 +82,7 @@ int num_sms();
 
 // Allocation-free decode attention: partials in a library-owned device array.
 size_t noalloc_scratch_bytes();
-bool noalloc_fits(const CacheView &c);
+bool noalloc_fits(const CacheView &c, int q_heads);
 cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
                                      float *out, cudaStream_t s);
 

@@ -1,6 +1,6 @@
 """Decode attention for every head_dim, bit pair and GQA group size (the
-generic kernel; head_dim 128 k8/k4 v3 with groups of 1 to 8 take the
-specialised kernel) against the binary64 oracle.  Tolerance: 2e-3 max-abs on the fp32
+generic kernel; head_dim 128 k8/k4 v3 take the specialised kernel, in
+blocks of 8 q-heads) against the binary64 oracle.  Tolerance: 2e-3 max-abs on the fp32
 output, as for the specialised kernel.
 """
 import numpy as np
@@ -41,10 +41,12 @@ def test_group_sizes(cuda, G):
     assert err < TOL, err
 
 
-@pytest.mark.parametrize("kb,G,T", [(8, 4, 5000), (4, 4, 3001), (8, 7, 2050), (4, 1, 777), (8, 5, 64)])
-def test_specialised_kernel_small_groups(cuda, kb, G, T):
-    """Groups below 8 on the specialised kernel (the MMA's 8 columns, those past
-    G zero): several splits, ragged stage tails, ragged combine blocks."""
+@pytest.mark.parametrize("kb,G,T", [(8, 4, 5000), (4, 4, 3001), (8, 7, 2050), (4, 1, 777), (8, 5, 64),
+                                    (8, 16, 4000), (4, 12, 2500), (8, 24, 900), (4, 9, 1234)])
+def test_specialised_kernel_group_sizes(cuda, kb, G, T):
+    """Groups other than 8 on the specialised kernel (blocks of the MMA's 8
+    columns, those past G dropped): several splits, ragged stage tails, ragged
+    combine blocks, one to three column blocks per kv-head."""
     err = _run(cuda, 128, kb, 3, B=3, H=3, G=G, T=T, cap=T + (16 - T % 16) % 16 + 16, step=G)
     assert err < TOL, err
 
