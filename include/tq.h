@@ -284,6 +284,20 @@ TQ_API int tq_attention_supported(int32_t head_dim, int32_t k_bits, int32_t v_bi
  */
 TQ_API tq_status tq_device_error(uint32_t *host_code);
 
+/* Code a bounded wait that gave up ORs into the device error word. */
+#define TQ_DEVICE_ERR_WAIT_TIMEOUT 1u
+
+/*
+ * Failure-path check (no counterpart in the pages): launches one warp that
+ * waits, through the same bounded wait every kernel of the library uses for
+ * its asynchronous copies, on a shared-memory barrier that nothing will ever
+ * complete.  The wait gives up after its limit (about 2 s of device time),
+ * ORs TQ_DEVICE_ERR_WAIT_TIMEOUT into the device error word, and the kernel
+ * returns.  It touches no memory outside its own shared memory and the error
+ * word, and the context stays usable.  TQ_ERR_CUDA if the launch fails.
+ */
+TQ_API tq_status tq_check_wait_timeout(tq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

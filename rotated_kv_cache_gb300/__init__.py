@@ -24,20 +24,22 @@ __all__ = [
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
     "tq_attention_supported", "tq_device_error", "tq_plane_bytes", "tq_decode_attention_noalloc",
     "tq_decode_values_rotated", "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows",
-    "tq_multi_token_workspace_bytes", "tq_multi_token_attention",
+    "tq_multi_token_workspace_bytes", "tq_multi_token_attention", "tq_check_wait_timeout",
+    "TQ_DEVICE_ERR_WAIT_TIMEOUT",
 ]
 
 HEAD_DIMS = (64, 128, 256, 512)
 K_BITS = (2, 4, 5, 8)
 V_BITS = (2, 3, 4, 5, 8)
 TQ_BF16, TQ_F32 = 0, 1
+TQ_DEVICE_ERR_WAIT_TIMEOUT = 1  # device error word: a bounded wait gave up
 
 EXPORTS = (
     "tq_status_string", "tq_bytes_per_token_head", "tq_plane_bytes", "tq_sign_vector", "tq_codebook",
     "tq_encode_append", "tq_decode", "tq_attention_workspace_bytes", "tq_decode_attention",
     "tq_attention_supported", "tq_device_error", "tq_decode_attention_noalloc", "tq_decode_values_rotated",
     "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows", "tq_multi_token_workspace_bytes",
-    "tq_multi_token_attention",
+    "tq_multi_token_attention", "tq_check_wait_timeout",
 )
 
 
@@ -85,6 +87,7 @@ def lib() -> ctypes.CDLL:
     so.tq_decode_attention.argtypes = [_CP, _P, _I32, _I64, ctypes.c_float, _P, _P, _SZ, _P]
     so.tq_attention_supported.argtypes = [_I32, _I32, _I32, _I32]
     so.tq_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    so.tq_check_wait_timeout.argtypes = [_P]
     so.tq_decode_attention_noalloc.argtypes = [_CP, _P, _I32, _I64, ctypes.c_float, _P, _P]
     so.tq_decode_values_rotated.argtypes = [_CP, _I64, _I64, ctypes.c_int, _P, _P]
     so.tq_unrotate.argtypes = [_I32, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P]
@@ -357,6 +360,13 @@ def tq_multi_token_attention(cache: Cache, q: torch.Tensor, seq_len: int, softma
                                           out.data_ptr(), ws_ptr, ws_bytes, _stream(stream)),
            "tq_multi_token_attention")
     return out
+
+
+def tq_check_wait_timeout(stream=None) -> None:
+    """Enqueue the failure-path check: one warp whose bounded wait on a barrier
+    nothing completes gives up after ~2 s and records TQ_DEVICE_ERR_WAIT_TIMEOUT
+    (read it with tq_device_error())."""
+    _check(lib().tq_check_wait_timeout(_stream(stream)), "tq_check_wait_timeout")
 
 
 def tq_device_error() -> int:

@@ -86,6 +86,21 @@ tq::CacheView view(const tq_cache *c)
 
 tq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
 
+// One warp waits, through the bounded wait of every kernel here, on a barrier
+// that nothing will complete (tq_check_wait_timeout): the wait gives up at its
+// limit, records the timeout code and the kernel returns.
+__global__ void wait_timeout_kernel(uint32_t *err)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t a = tq::smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        tq::mbar_init(a, 1);
+        tq::fence_mbar_init();
+    }
+    __syncwarp();
+    tq::mbar_wait_bounded(a, 0, err);
+}
+
 }  // namespace
 
 extern "C" {
@@ -349,6 +364,14 @@ tq_status tq_decode_attention_noalloc(const tq_cache *c, const void *q, int32_t 
     if (!tq::noalloc_fits(view(c), q_heads)) return TQ_ERR_SCRATCH;
     return cuda_status(tq::launch_attention_noalloc(view(c), static_cast<const uint16_t *>(q), q_heads, seq_len,
                                                     scale, out, (cudaStream_t)stream));
+}
+
+tq_status tq_check_wait_timeout(tq_stream_t stream)
+{
+    uint32_t *err = tq::device_error_word();
+    if (!err) return TQ_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err);
+    return cuda_status(cudaGetLastError());
 }
 
 tq_status tq_device_error(uint32_t *host_code)
