@@ -315,15 +315,20 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
     const int r0 = 16 * warp + g, r1 = r0 + 8;  // key rows of this lane in a stage
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
 
+    // token offsets within the split fit 32 bits: a split never holds 2^31 rows
+    // (136 B per row at the smallest width would take 292 GB)
+    const int split_rows = (int)(t_end - t_begin);
+    const uint32_t ring0 = smem_addr(stages);
     bool ok = true;
+    int slot = 0;
+    uint32_t phase = 0;  // ring slot and barrier parity of stage s
     for (int s = 0; s < n_stages; ++s) {
-        const int slot = s % kStages;
-        if (!mbar_wait_bounded(full0 + 8 * slot, (s / kStages) & 1, p.err)) {
+        if (!mbar_wait_bounded(full0 + 8 * slot, phase, p.err)) {
             ok = false;
             break;
         }
-        const uint32_t st = smem_addr(stages + slot * A::STAGE);
-        const int64_t tile_t0 = t_begin + (int64_t)s * kStageT + 16 * warp;  // first token of this warp's tile
+        const uint32_t st = ring0 + slot * A::STAGE;
+        const int tile_r = s * kStageT + 16 * warp;  // first row of this warp's tile, from the split's start
 
         // ---------------- S = Q K^T for 16 tokens x 8 heads, per key group
         float acc[4][4];
@@ -380,9 +385,9 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                 S[i][0] = sv.x;
                 S[i][1] = sv.y;
             }
-            if (tile_t0 + 16 > t_end) {  // ragged tail: mask rows past the range
-                if (tile_t0 + g >= t_end) S[0][0] = S[0][1] = -INFINITY;
-                if (tile_t0 + g + 8 >= t_end) S[1][0] = S[1][1] = -INFINITY;
+            if (tile_r + 16 > split_rows) {  // ragged tail: mask rows past the range
+                if (tile_r + g >= split_rows) S[0][0] = S[0][1] = -INFINITY;
+                if (tile_r + g + 8 >= split_rows) S[1][0] = S[1][1] = -INFINITY;
             }
         }
         // ---------------- online softmax (base 2) for heads 2c, 2c+1
@@ -393,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
         const bool raise = S[0][0] > m_run[0] || S[1][0] > m_run[0] || S[0][1] > m_run[1] || S[1][1] > m_run[1] ||
                            m_run[0] == -INFINITY || m_run[1] == -INFINITY;
         if (__any_sync(0xffffffffu, raise)) {
+            float alpha[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 float mt = fmaxf(S[0][j], S[1][j]);
@@ -401,16 +407,22 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
                 const float mn = fmaxf(m_run[j], mt);
                 const float mu = mn == -INFINITY ? 0.0f : mn;
-                const float alpha = ex2(m_run[j] - mu);
+                alpha[j] = ex2(m_run[j] - mu);
                 m_run[j] = mn;
                 pr[0][j] = ex2(S[0][j] - mu);
                 pr[1][j] = ex2(S[1][j] - mu);
-                l_run[j] = l_run[j] * alpha + pr[0][j] + pr[1][j];
+                l_run[j] = l_run[j] * alpha[j] + pr[0][j] + pr[1][j];
+            }
+            // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
+            const float2 a2 = make_float2(alpha[0], alpha[1]);
 #pragma unroll
-                for (int mt2 = 0; mt2 < 8; ++mt2) {
-                    o[mt2][j] *= alpha;
-                    o[mt2][2 + j] *= alpha;
-                }
+            for (int mt2 = 0; mt2 < 8; ++mt2) {
+                const float2 x = __fmul2_rn(make_float2(o[mt2][0], o[mt2][1]), a2);
+                const float2 y = __fmul2_rn(make_float2(o[mt2][2], o[mt2][3]), a2);
+                o[mt2][0] = x.x;
+                o[mt2][1] = x.y;
+                o[mt2][2] = y.x;
+                o[mt2][3] = y.y;
             }
         } else {
 #pragma unroll
@@ -427,10 +439,10 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
         uint2 vs[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) vs[q] = lds64(st + A::OFF_VS + vr[q] * 8);
-        if (tile_t0 + 16 > t_end) {
+        if (tile_r + 16 > split_rows) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                if (tile_t0 + (vr[q] - 16 * warp) >= t_end) vs[q] = make_uint2(0u, 0u);
+                if (tile_r + (vr[q] - 16 * warp) >= split_rows) vs[q] = make_uint2(0u, 0u);
         }
         // ---------------- O^T += V^T P'^T, per value group
 #pragma unroll
@@ -480,6 +492,10 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                 done[slot] = 0;
                 if (s + kStages < n_stages) issue(s + kStages);
             }
+        }
+        if (++slot == kStages) {
+            slot = 0;
+            phase ^= 1u;
         }
     }
     __syncthreads();  // every warp is done with the ring before it holds the merge
