@@ -315,6 +315,19 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
     const int r0 = 16 * warp + g, r1 = r0 + 8;  // key rows of this lane in a stage
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
 
+    // lane-constant byte offsets in a stage: key chunks of row r0 per group (row r1 is
+    // 8 rows on), value words of token vr[q] for group 0 (group G is 12 G bytes on)
+    uint32_t koff[4];
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+        if constexpr (KB == 8)  // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
+            koff[G] = A::OFF_K + r0 * A::KROW + ((uint32_t)((2 * G + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
+        else  // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
+            koff[G] = A::OFF_K + r0 * A::KROW + ((uint32_t)(G ^ ((g >> 1) & 3)) << 4) + 4 * c;
+    }
+    uint32_t voff[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) voff[q] = A::OFF_V + vr[q] * (kD * kVB / 8) + 4 * v_word;
     // token offsets within the split fit 32 bits: a split never holds 2^31 rows
     // (136 B per row at the smallest width would take 292 GB)
     const int split_rows = (int)(t_end - t_begin);
@@ -340,10 +353,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
         for (int G = 0; G < 4; ++G) {
             if constexpr (KB == 8) {
                 // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
-                const uint32_t chunk = (uint32_t)((2 * G + (c >> 1)) ^ g);
-                const uint32_t off = (chunk << 4) + ((c & 1) << 3);
-                const uint2 k0 = lds64(st + A::OFF_K + r0 * A::KROW + off);
-                const uint2 k1 = lds64(st + A::OFF_K + r1 * A::KROW + off);
+                const uint2 k0 = lds64(st + koff[G]);
+                const uint2 k1 = lds64(st + koff[G] + 8 * A::KROW);
                 // bytes 0 and 2 (then 1 and 3) of a word -> f16 (1024 + (byte ^ 0x80)):
                 // dims (8c+0, 8c+2), (8c+1, 8c+3), then +4
                 mma16816(acc[G], kcvt(k0.x, p), kcvt(k1.x, p), kcvt(shr_fma<8>(k0.x), p), kcvt(shr_fma<8>(k1.x), p),
@@ -352,9 +363,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                          bq[2 * G + 1][0], bq[2 * G + 1][1]);
             } else {
                 // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
-                const uint32_t off = ((uint32_t)(G ^ ((g >> 1) & 3)) << 4) + 4 * c;
-                const uint32_t w0 = lds32(st + A::OFF_K + r0 * A::KROW + off);
-                const uint32_t w1 = lds32(st + A::OFF_K + r1 * A::KROW + off);
+                const uint32_t w0 = lds32(st + koff[G]);
+                const uint32_t w1 = lds32(st + koff[G] + 8 * A::KROW);
                 // nibbles k and k+4 -> f16 (1024 + nibble)
                 mma16816(acc[G], kcvt(w0, p), kcvt(w1, p), kcvt(shr_fma<4>(w0), p), kcvt(shr_fma<4>(w1), p), bq[2 * G][0],
                          bq[2 * G][1]);
@@ -459,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
             uint32_t x[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint32_t base = st + A::OFF_V + vr[q] * (kD * kVB / 8) + 4 * (3 * G + v_word);
+                const uint32_t base = st + voff[q] + 12 * G;
                 x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
             }
 #pragma unroll
@@ -469,7 +479,9 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                 // 0..3, of the second in nibbles 4..7
                 const uint32_t w = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
                 const uint32_t y = (w & 0x003F003Fu) | ((w & 0x0FC00FC0u) * 4u);
-                const uint32_t e = (y & 0x07070707u) | ((y & 0x38383838u) * 2u);
+                // each byte of y holds two codes (bits 0-2, 3-5); adding the upper code
+                // to itself moves it to bits 4-6, and nothing carries out of a byte
+                const uint32_t e = y + (y & 0x38383838u);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     // selector: codes (r, r+1) of the first token, then of the second
