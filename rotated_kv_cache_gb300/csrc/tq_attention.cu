@@ -10,8 +10,9 @@
 //
 // GB300 design (one GPU, sm_103a):
 //  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
-//    a 3-stage shared-memory ring; each of its 4 warps takes 16 tokens of a
-//    64-token stage.  A stage is one 2-D TMA load of the key codes (128/64-byte
+//    a 2-stage shared-memory ring; each of its 4 warps takes two 16-token tiles
+//    of a 128-token stage and works on both at once (independent dependency
+//    chains to interleave).  A stage is one 2-D TMA load of the key codes (128/64-byte
 //    swizzle, so the per-row fragment reads of the MMA are bank-conflict-free)
 //    and four 1-D bulk copies of the other planes, completing on the slot's
 //    mbarrier; the last warp to finish a stage issues the copies that refill
@@ -47,8 +48,8 @@ constexpr int kG = 8;              // MMA columns: q-heads per kv-head, up to 8 
 constexpr int kVB = 3;             // value bits covered
 constexpr int kCW = 4;             // warps per CTA (all compute; the last to finish a stage refills it)
 constexpr int kThreads = kCW * 32;
-constexpr int kStageT = 64;        // tokens per stage
-constexpr int kStages = 3;
+constexpr int kStageT = 128;       // tokens per stage: two 16-token tiles per warp
+constexpr int kStages = 2;         // ring depth (4 CTAs of 2 x 26 KB fit on an SM)
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -341,162 +342,168 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
             break;
         }
         const uint32_t st = ring0 + slot * A::STAGE;
-        const int tile_r = s * kStageT + 16 * warp;  // first row of this warp's tile, from the split's start
+        // two 16-row tiles per warp and stage (rows 16 warp and 64 + 16 warp); unrolled, so
+        // the compiler interleaves their independent chains
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+            const int tile_r = s * kStageT + 64 * t2 + 16 * warp;  // tile's first row from the split's start
 
-        // ---------------- S = Q K^T for 16 tokens x 8 heads, per key group
-        float acc[4][4];
+            // ---------------- S = Q K^T for 16 tokens x 8 heads, per key group
+            float acc[4][4];
 #pragma unroll
-        for (int G = 0; G < 4; ++G)
+            for (int G = 0; G < 4; ++G)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[G][j] = 0.0f;
+                for (int j = 0; j < 4; ++j) acc[G][j] = 0.0f;
 #pragma unroll
-        for (int G = 0; G < 4; ++G) {
-            if constexpr (KB == 8) {
-                // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
-                const uint2 k0 = lds64(st + koff[G]);
-                const uint2 k1 = lds64(st + koff[G] + 8 * A::KROW);
-                // bytes 0 and 2 (then 1 and 3) of a word -> f16 (1024 + (byte ^ 0x80)):
-                // dims (8c+0, 8c+2), (8c+1, 8c+3), then +4
-                mma16816(acc[G], kcvt(k0.x, p), kcvt(k1.x, p), kcvt(shr_fma<8>(k0.x), p), kcvt(shr_fma<8>(k1.x), p),
-                         bq[2 * G][0], bq[2 * G][1]);
-                mma16816(acc[G], kcvt(k0.y, p), kcvt(k1.y, p), kcvt(shr_fma<8>(k0.y), p), kcvt(shr_fma<8>(k1.y), p),
-                         bq[2 * G + 1][0], bq[2 * G + 1][1]);
+            for (int G = 0; G < 4; ++G) {
+                if constexpr (KB == 8) {
+                    // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
+                    const uint2 k0 = lds64(st + koff[G] + t2 * (64 * A::KROW));
+                    const uint2 k1 = lds64(st + koff[G] + t2 * (64 * A::KROW) + 8 * A::KROW);
+                    // bytes 0 and 2 (then 1 and 3) of a word -> f16 (1024 + (byte ^ 0x80)):
+                    // dims (8c+0, 8c+2), (8c+1, 8c+3), then +4
+                    mma16816(acc[G], kcvt(k0.x, p), kcvt(k1.x, p), kcvt(shr_fma<8>(k0.x), p), kcvt(shr_fma<8>(k1.x), p),
+                             bq[2 * G][0], bq[2 * G][1]);
+                    mma16816(acc[G], kcvt(k0.y, p), kcvt(k1.y, p), kcvt(shr_fma<8>(k0.y), p), kcvt(shr_fma<8>(k1.y), p),
+                             bq[2 * G + 1][0], bq[2 * G + 1][1]);
+                } else {
+                    // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
+                    const uint32_t w0 = lds32(st + koff[G] + t2 * (64 * A::KROW));
+                    const uint32_t w1 = lds32(st + koff[G] + t2 * (64 * A::KROW) + 8 * A::KROW);
+                    // nibbles k and k+4 -> f16 (1024 + nibble)
+                    mma16816(acc[G], kcvt(w0, p), kcvt(w1, p), kcvt(shr_fma<4>(w0), p), kcvt(shr_fma<4>(w1), p), bq[2 * G][0],
+                             bq[2 * G][1]);
+                    mma16816(acc[G], kcvt(shr_fma<8>(w0), p), kcvt(shr_fma<8>(w1), p), kcvt(shr_fma<12>(w0), p),
+                             kcvt(shr_fma<12>(w1), p), bq[2 * G + 1][0], bq[2 * G + 1][1]);
+                }
+            }
+            // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum),
+            // both heads of the lane at once on packed fp32 pairs
+            float S[2][2];
+            {
+                const uint32_t m0 = (r0 + 64 * t2) * 8, m1 = (r1 + 64 * t2) * 8;
+                const uint2 s0 = lds64(st + A::OFF_KS + m0), s1 = lds64(st + A::OFF_KS + m1);
+                const uint2 z0 = lds64(st + A::OFF_KZ + m0), z1 = lds64(st + A::OFF_KZ + m1);
+                const uint32_t sw[2][2] = {{s0.x, s0.y}, {s1.x, s1.y}}, zw[2][2] = {{z0.x, z0.y}, {z1.x, z1.y}};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    float2 sacc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int G = 0; G < 4; ++G) {
+                        const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
+                        const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
+                        const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
+                        const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[G][0], qs[G][1]),
+                                                    make_float2(acc[G][2 * i], acc[G][2 * i + 1]));
+                        sacc = __ffma2_rn(make_float2(sc, sc), t, sacc);
+                    }
+                    const float2 sv = __fmul2_rn(sacc, make_float2(ie[0], ie[1]));
+                    S[i][0] = sv.x;
+                    S[i][1] = sv.y;
+                }
+                if (tile_r + 16 > split_rows) {  // ragged tail: mask rows past the range
+                    if (tile_r + g >= split_rows) S[0][0] = S[0][1] = -INFINITY;
+                    if (tile_r + g + 8 >= split_rows) S[1][0] = S[1][1] = -INFINITY;
+                }
+            }
+            // ---------------- online softmax (base 2) for heads 2c, 2c+1
+            // The running max is reduced across the tile's rows only when some lane
+            // sees a score above it (or no max exists yet); otherwise the weights
+            // are 2^(S - m) with the max unchanged, which is the same arithmetic.
+            float pr[2][2];
+            const bool raise = S[0][0] > m_run[0] || S[1][0] > m_run[0] || S[0][1] > m_run[1] || S[1][1] > m_run[1] ||
+                               m_run[0] == -INFINITY || m_run[1] == -INFINITY;
+            if (__any_sync(0xffffffffu, raise)) {
+                float alpha[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float mt = fmaxf(S[0][j], S[1][j]);
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                    const float mn = fmaxf(m_run[j], mt);
+                    const float mu = mn == -INFINITY ? 0.0f : mn;
+                    alpha[j] = ex2(m_run[j] - mu);
+                    m_run[j] = mn;
+                    pr[0][j] = ex2(S[0][j] - mu);
+                    pr[1][j] = ex2(S[1][j] - mu);
+                    l_run[j] = l_run[j] * alpha[j] + pr[0][j] + pr[1][j];
+                }
+                // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
+                const float2 a2 = make_float2(alpha[0], alpha[1]);
+#pragma unroll
+                for (int mt2 = 0; mt2 < 8; ++mt2) {
+                    const float2 x = __fmul2_rn(make_float2(o[mt2][0], o[mt2][1]), a2);
+                    const float2 y = __fmul2_rn(make_float2(o[mt2][2], o[mt2][3]), a2);
+                    o[mt2][0] = x.x;
+                    o[mt2][1] = x.y;
+                    o[mt2][2] = y.x;
+                    o[mt2][3] = y.y;
+                }
             } else {
-                // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
-                const uint32_t w0 = lds32(st + koff[G]);
-                const uint32_t w1 = lds32(st + koff[G] + 8 * A::KROW);
-                // nibbles k and k+4 -> f16 (1024 + nibble)
-                mma16816(acc[G], kcvt(w0, p), kcvt(w1, p), kcvt(shr_fma<4>(w0), p), kcvt(shr_fma<4>(w1), p), bq[2 * G][0],
-                         bq[2 * G][1]);
-                mma16816(acc[G], kcvt(shr_fma<8>(w0), p), kcvt(shr_fma<8>(w1), p), kcvt(shr_fma<12>(w0), p),
-                         kcvt(shr_fma<12>(w1), p), bq[2 * G + 1][0], bq[2 * G + 1][1]);
-            }
-        }
-        // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum),
-        // both heads of the lane at once on packed fp32 pairs
-        float S[2][2];
-        {
-            const uint2 s0 = lds64(st + A::OFF_KS + r0 * 8), s1 = lds64(st + A::OFF_KS + r1 * 8);
-            const uint2 z0 = lds64(st + A::OFF_KZ + r0 * 8), z1 = lds64(st + A::OFF_KZ + r1 * 8);
-            const uint32_t sw[2][2] = {{s0.x, s0.y}, {s1.x, s1.y}}, zw[2][2] = {{z0.x, z0.y}, {z1.x, z1.y}};
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                float2 sacc = make_float2(0.0f, 0.0f);
-#pragma unroll
-                for (int G = 0; G < 4; ++G) {
-                    const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
-                    const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
-                    const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
-                    const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[G][0], qs[G][1]),
-                                                make_float2(acc[G][2 * i], acc[G][2 * i + 1]));
-                    sacc = __ffma2_rn(make_float2(sc, sc), t, sacc);
-                }
-                const float2 sv = __fmul2_rn(sacc, make_float2(ie[0], ie[1]));
-                S[i][0] = sv.x;
-                S[i][1] = sv.y;
-            }
-            if (tile_r + 16 > split_rows) {  // ragged tail: mask rows past the range
-                if (tile_r + g >= split_rows) S[0][0] = S[0][1] = -INFINITY;
-                if (tile_r + g + 8 >= split_rows) S[1][0] = S[1][1] = -INFINITY;
-            }
-        }
-        // ---------------- online softmax (base 2) for heads 2c, 2c+1
-        // The running max is reduced across the tile's rows only when some lane
-        // sees a score above it (or no max exists yet); otherwise the weights
-        // are 2^(S - m) with the max unchanged, which is the same arithmetic.
-        float pr[2][2];
-        const bool raise = S[0][0] > m_run[0] || S[1][0] > m_run[0] || S[0][1] > m_run[1] || S[1][1] > m_run[1] ||
-                           m_run[0] == -INFINITY || m_run[1] == -INFINITY;
-        if (__any_sync(0xffffffffu, raise)) {
-            float alpha[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mt = fmaxf(S[0][j], S[1][j]);
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-                const float mn = fmaxf(m_run[j], mt);
-                const float mu = mn == -INFINITY ? 0.0f : mn;
-                alpha[j] = ex2(m_run[j] - mu);
-                m_run[j] = mn;
-                pr[0][j] = ex2(S[0][j] - mu);
-                pr[1][j] = ex2(S[1][j] - mu);
-                l_run[j] = l_run[j] * alpha[j] + pr[0][j] + pr[1][j];
-            }
-            // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
-            const float2 a2 = make_float2(alpha[0], alpha[1]);
-#pragma unroll
-            for (int mt2 = 0; mt2 < 8; ++mt2) {
-                const float2 x = __fmul2_rn(make_float2(o[mt2][0], o[mt2][1]), a2);
-                const float2 y = __fmul2_rn(make_float2(o[mt2][2], o[mt2][3]), a2);
-                o[mt2][0] = x.x;
-                o[mt2][1] = x.y;
-                o[mt2][2] = y.x;
-                o[mt2][3] = y.y;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                pr[0][j] = ex2(S[0][j] - m_run[j]);
-                pr[1][j] = ex2(S[1][j] - m_run[j]);
-                l_run[j] += pr[0][j] + pr[1][j];
-            }
-        }
-        // ---------------- P^T as the B operand (tokens x heads), transposed in registers
-        const uint32_t pt0 = movmatrix_trans(pack_f16x2(pr[0][0], pr[0][1]));  // tokens 2c, 2c+1; head g
-        const uint32_t pt1 = movmatrix_trans(pack_f16x2(pr[1][0], pr[1][1]));  // tokens 2c+8, 2c+9
-        // value scales of this lane's four tokens (zero past the range)
-        uint2 vs[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) vs[q] = lds64(st + A::OFF_VS + vr[q] * 8);
-        if (tile_r + 16 > split_rows) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (tile_r + (vr[q] - 16 * warp) >= split_rows) vs[q] = make_uint2(0u, 0u);
-        }
-        // ---------------- O^T += V^T P'^T, per value group
-#pragma unroll
-        for (int G = 0; G < 4; ++G) {
-            const int sh = 16 * (G & 1);
-            const uint32_t sp0 = __byte_perm(G < 2 ? vs[0].x : vs[0].y, G < 2 ? vs[1].x : vs[1].y,
-                                             sh ? 0x7632u : 0x5410u);
-            const uint32_t sp1 = __byte_perm(G < 2 ? vs[2].x : vs[2].y, G < 2 ? vs[3].x : vs[3].y,
-                                             sh ? 0x7632u : 0x5410u);
-            const uint32_t b0 = hmul2(pt0, sp0), b1 = hmul2(pt1, sp1);
-            uint32_t av[2][2][2];  // [token pair][m-tile half][row g, row g+8]
-            // 12-bit fields (codes of dims 32G + 4g + 0..3 at bits 0, 3, 6, 9) of
-            // the lane's four tokens; bits above 11 are don't-care
-            uint32_t x[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t base = st + voff[q] + 12 * G;
-                x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
-            }
-#pragma unroll
-            for (int pr2 = 0; pr2 < 2; ++pr2) {  // token pairs (2c, 2c+1) and (2c+8, 2c+9)
-                // both tokens' fields side by side (first in bits 0-15), then one
-                // code per nibble: codes r0..r3 of the first token in nibbles
-                // 0..3, of the second in nibbles 4..7
-                const uint32_t w = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
-                const uint32_t y = (w & 0x003F003Fu) | ((w & 0x0FC00FC0u) * 4u);
-                // each byte of y holds two codes (bits 0-2, 3-5); adding the upper code
-                // to itself moves it to bits 4-6, and nothing carries out of a byte
-                const uint32_t e = y + (y & 0x38383838u);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    // selector: codes (r, r+1) of the first token, then of the second
-                    const uint32_t sel = __byte_perm(e, 0u, half ? 0x0031u : 0x0020u);
-                    const uint32_t lo = prmt(p.tl0, p.tl1, sel);  // low f16 bytes of the 4 centroids
-                    const uint32_t hi = prmt(p.th0, p.th1, sel);  // high f16 bytes
-                    av[pr2][half][0] = __byte_perm(lo, hi, 0x6240u);  // dim r: (first, second)
-                    av[pr2][half][1] = __byte_perm(lo, hi, 0x7351u);  // dim r + 1
+                for (int j = 0; j < 2; ++j) {
+                    pr[0][j] = ex2(S[0][j] - m_run[j]);
+                    pr[1][j] = ex2(S[1][j] - m_run[j]);
+                    l_run[j] += pr[0][j] + pr[1][j];
                 }
             }
+            // ---------------- P^T as the B operand (tokens x heads), transposed in registers
+            const uint32_t pt0 = movmatrix_trans(pack_f16x2(pr[0][0], pr[0][1]));  // tokens 2c, 2c+1; head g
+            const uint32_t pt1 = movmatrix_trans(pack_f16x2(pr[1][0], pr[1][1]));  // tokens 2c+8, 2c+9
+            // value scales of this lane's four tokens (zero past the range)
+            uint2 vs[4];
 #pragma unroll
-            for (int half = 0; half < 2; ++half)
-                mma16816(o[2 * G + half], av[0][half][0], av[0][half][1], av[1][half][0], av[1][half][1], b0, b1);
+            for (int q = 0; q < 4; ++q) vs[q] = lds64(st + A::OFF_VS + (vr[q] + 64 * t2) * 8);
+            if (tile_r + 16 > split_rows) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (tile_r + (vr[q] - 16 * warp) >= split_rows) vs[q] = make_uint2(0u, 0u);
+            }
+            // ---------------- O^T += V^T P'^T, per value group
+#pragma unroll
+            for (int G = 0; G < 4; ++G) {
+                const int sh = 16 * (G & 1);
+                const uint32_t sp0 = __byte_perm(G < 2 ? vs[0].x : vs[0].y, G < 2 ? vs[1].x : vs[1].y,
+                                                 sh ? 0x7632u : 0x5410u);
+                const uint32_t sp1 = __byte_perm(G < 2 ? vs[2].x : vs[2].y, G < 2 ? vs[3].x : vs[3].y,
+                                                 sh ? 0x7632u : 0x5410u);
+                const uint32_t b0 = hmul2(pt0, sp0), b1 = hmul2(pt1, sp1);
+                uint32_t av[2][2][2];  // [token pair][m-tile half][row g, row g+8]
+                // 12-bit fields (codes of dims 32G + 4g + 0..3 at bits 0, 3, 6, 9) of
+                // the lane's four tokens; bits above 11 are don't-care
+                uint32_t x[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t base = st + voff[q] + t2 * (64 * (kD * kVB / 8)) + 12 * G;
+                    x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
+                }
+#pragma unroll
+                for (int pr2 = 0; pr2 < 2; ++pr2) {  // token pairs (2c, 2c+1) and (2c+8, 2c+9)
+                    // both tokens' fields side by side (first in bits 0-15), then one
+                    // code per nibble: codes r0..r3 of the first token in nibbles
+                    // 0..3, of the second in nibbles 4..7
+                    const uint32_t w = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
+                    const uint32_t y = (w & 0x003F003Fu) | ((w & 0x0FC00FC0u) * 4u);
+                    // each byte of y holds two codes (bits 0-2, 3-5); adding the upper code
+                    // to itself moves it to bits 4-6, and nothing carries out of a byte
+                    const uint32_t e = y + (y & 0x38383838u);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        // selector: codes (r, r+1) of the first token, then of the second
+                        const uint32_t sel = __byte_perm(e, 0u, half ? 0x0031u : 0x0020u);
+                        const uint32_t lo = prmt(p.tl0, p.tl1, sel);  // low f16 bytes of the 4 centroids
+                        const uint32_t hi = prmt(p.th0, p.th1, sel);  // high f16 bytes
+                        av[pr2][half][0] = __byte_perm(lo, hi, 0x6240u);  // dim r: (first, second)
+                        av[pr2][half][1] = __byte_perm(lo, hi, 0x7351u);  // dim r + 1
+                    }
+                }
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+                    mma16816(o[2 * G + half], av[0][half][0], av[0][half][1], av[1][half][0], av[1][half][1], b0, b1);
+            }
+            // the last warp to finish this stage refills its slot with stage s + kStages
         }
-        // the last warp to finish this stage refills its slot with stage s + kStages
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();

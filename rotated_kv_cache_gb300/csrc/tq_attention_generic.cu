@@ -13,7 +13,7 @@
 // to the cache including them: query row i of M sees the rows before
 // seq_len - M + i + 1).
 //
-// Design, as in the specialised kernel: split-KV CTAs stream 64-token stages
+// Design, after the specialised kernel's: split-KV CTAs stream 64-token stages
 // through a shared-memory ring (bulk copies completing on an mbarrier; the
 // last warp to finish a stage refills it); each of the 4 warps takes 16
 // tokens.  QK^T and PV run on mma.sync m16n8k16 (f16 in, f32 accumulate).

@@ -69,17 +69,26 @@ def test_noalloc_group_of_four(cuda):
 
 @pytest.mark.gpu
 def test_noalloc_fewer_splits_than_usual(cuda):
-    """64 sequences x 8 kv-heads x 8193 rows: the usual split plan needs more
-    than the 16 MiB scratch, so this entry point runs with fewer splits."""
+    """8 kv-heads x 8193 rows and the smallest batch (64 to 512 sequences) whose
+    usual split plan needs more than the 16 MiB scratch, so this entry point
+    runs with fewer splits."""
     w = tq_synth.WORKLOADS["decode"]
-    B, H, T = 64, 8, 8193
+    H, T = 8, 8193
+
+    def usual_workspace(B):  # the size query reads no device memory
+        s = cuda._CacheStruct(w.d, 8, w.vb, H, B, 0, T + 15, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+        return cuda.lib().tq_attention_workspace_bytes(ctypes.byref(s), 8 * H, T)
+
+    B = next(b for b in (64, 128, 256, 512) if usual_workspace(b) > SCRATCH_BYTES)
     cache = cuda.Cache(B, H, w.d, T, k_bits=8, v_bits=w.vb)
-    k = torch.empty((B, H, T, w.d), dtype=torch.int16, device="cuda")
-    v = torch.empty_like(k)
-    tq_synth.device_kv(w, k, v, B=B, H=H, n=T)
-    cuda.tq_encode_append(cache, k.view(torch.bfloat16), v.view(torch.bfloat16), 0)
-    del k, v
     assert cuda.tq_attention_workspace_bytes(cache, 8 * H, T) > SCRATCH_BYTES
+    for b0 in range(0, B, 64):
+        nb = min(64, B - b0)
+        k = torch.empty((nb, H, T, w.d), dtype=torch.int16, device="cuda")
+        v = torch.empty_like(k)
+        tq_synth.device_kv(w, k, v, B=nb, H=H, n=T, b_offset=b0)
+        cuda.tq_encode_append(cache.batch_slice(b0, nb), k.view(torch.bfloat16), v.view(torch.bfloat16), 0)
+        del k, v
     qs = []
     for step in (0, 1):
         q = torch.empty((B, 8 * H, w.d), dtype=torch.int16, device="cuda")
