@@ -10,13 +10,13 @@
 //
 // GB300 design (one GPU, sm_103a):
 //  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
-//    a 2-stage shared-memory ring; each of its 4 warps takes two 16-token tiles
-//    of a 128-token stage and works on both at once (independent dependency
+//    a 2-stage shared-memory ring; each of its 2 warps takes two 16-token tiles
+//    of a 64-token stage and works on both at once (independent dependency
 //    chains to interleave).  A stage is one 2-D TMA load of the key codes (128/64-byte
 //    swizzle, so the per-row fragment reads of the MMA are bank-conflict-free)
 //    and four 1-D bulk copies of the other planes, completing on the slot's
 //    mbarrier; the last warp to finish a stage issues the copies that refill
-//    its slot, so no warp is set aside as a producer (4 CTAs fit on an SM).
+//    its slot, so no warp is set aside as a producer (8 CTAs fit on an SM).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
 //    tokens, N = 8 columns: 8 of the G q-heads sharing the kv-head (a group
 //    above 8 takes ceil(G/8) CTAs, neighbours in the grid so their reads of
@@ -46,10 +46,11 @@ namespace {
 constexpr int kD = 128;            // head_dim covered
 constexpr int kG = 8;              // MMA columns: q-heads per kv-head, up to 8 (the rest zero)
 constexpr int kVB = 3;             // value bits covered
-constexpr int kCW = 4;             // warps per CTA (all compute; the last to finish a stage refills it)
+constexpr int kCW = 2;             // warps per CTA (all compute; the last to finish a stage refills it)
 constexpr int kThreads = kCW * 32;
-constexpr int kStageT = 128;       // tokens per stage: two 16-token tiles per warp
-constexpr int kStages = 2;         // ring depth (4 CTAs of 2 x 26 KB fit on an SM)
+constexpr int kTiles = 2;          // 16-token tiles per warp and stage, worked on together
+constexpr int kStageT = 16 * kTiles * kCW;  // tokens per stage
+constexpr int kStages = 2;         // ring depth (8 CTAs of 2 x 13 KB fit on an SM)
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -178,7 +179,7 @@ __device__ __forceinline__ uint32_t shr_fma(uint32_t x)
 
 // ---------------------------------------------------------------- the split kernel
 template <int KB>
-__global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                   const __grid_constant__ AttnParams p)
 {
     using A = AGeo<KB>;
@@ -342,11 +343,11 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
             break;
         }
         const uint32_t st = ring0 + slot * A::STAGE;
-        // two 16-row tiles per warp and stage (rows 16 warp and 64 + 16 warp); unrolled, so
-        // the compiler interleaves their independent chains
+        // two 16-row tiles per warp and stage (rows 16 warp and 16 kCW + 16 warp); unrolled,
+        // so the compiler interleaves their independent chains
 #pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2) {
-            const int tile_r = s * kStageT + 64 * t2 + 16 * warp;  // tile's first row from the split's start
+        for (int t2 = 0; t2 < kTiles; ++t2) {
+            const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
 
             // ---------------- S = Q K^T for 16 tokens x 8 heads, per key group
             float acc[4][4];
@@ -358,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
             for (int G = 0; G < 4; ++G) {
                 if constexpr (KB == 8) {
                     // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
-                    const uint2 k0 = lds64(st + koff[G] + t2 * (64 * A::KROW));
-                    const uint2 k1 = lds64(st + koff[G] + t2 * (64 * A::KROW) + 8 * A::KROW);
+                    const uint2 k0 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::KROW));
+                    const uint2 k1 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::KROW) + 8 * A::KROW);
                     // bytes 0 and 2 (then 1 and 3) of a word -> f16 (1024 + (byte ^ 0x80)):
                     // dims (8c+0, 8c+2), (8c+1, 8c+3), then +4
                     mma16816(acc[G], kcvt(k0.x, p), kcvt(k1.x, p), kcvt(shr_fma<8>(k0.x), p), kcvt(shr_fma<8>(k1.x), p),
@@ -368,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                              bq[2 * G + 1][0], bq[2 * G + 1][1]);
                 } else {
                     // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
-                    const uint32_t w0 = lds32(st + koff[G] + t2 * (64 * A::KROW));
-                    const uint32_t w1 = lds32(st + koff[G] + t2 * (64 * A::KROW) + 8 * A::KROW);
+                    const uint32_t w0 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::KROW));
+                    const uint32_t w1 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::KROW) + 8 * A::KROW);
                     // nibbles k and k+4 -> f16 (1024 + nibble)
                     mma16816(acc[G], kcvt(w0, p), kcvt(w1, p), kcvt(shr_fma<4>(w0), p), kcvt(shr_fma<4>(w1), p), bq[2 * G][0],
                              bq[2 * G][1]);
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
             // both heads of the lane at once on packed fp32 pairs
             float S[2][2];
             {
-                const uint32_t m0 = (r0 + 64 * t2) * 8, m1 = (r1 + 64 * t2) * 8;
+                const uint32_t m0 = (r0 + (16 * kCW) * t2) * 8, m1 = (r1 + (16 * kCW) * t2) * 8;
                 const uint2 s0 = lds64(st + A::OFF_KS + m0), s1 = lds64(st + A::OFF_KS + m1);
                 const uint2 z0 = lds64(st + A::OFF_KZ + m0), z1 = lds64(st + A::OFF_KZ + m1);
                 const uint32_t sw[2][2] = {{s0.x, s0.y}, {s1.x, s1.y}}, zw[2][2] = {{z0.x, z0.y}, {z1.x, z1.y}};
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
             // value scales of this lane's four tokens (zero past the range)
             uint2 vs[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) vs[q] = lds64(st + A::OFF_VS + (vr[q] + 64 * t2) * 8);
+            for (int q = 0; q < 4; ++q) vs[q] = lds64(st + A::OFF_VS + (vr[q] + (16 * kCW) * t2) * 8);
             if (tile_r + 16 > split_rows) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
                 uint32_t x[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint32_t base = st + voff[q] + t2 * (64 * (kD * kVB / 8)) + 12 * G;
+                    const uint32_t base = st + voff[q] + t2 * ((16 * kCW) * (kD * kVB / 8)) + 12 * G;
                     x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
                 }
 #pragma unroll
@@ -546,28 +547,30 @@ __global__ void __launch_bounds__(kThreads, 4) attn_split_kernel(const __grid_co
         }
     }
     __syncthreads();
-    // 128 threads: thread -> (head, 8 dims)
-    const int tid = threadIdx.x, hh = tid >> 4, d8 = (tid & 15) * 8;
-    float mmax = -INFINITY;
+    // items (head, 8 dims), kG x 16 of them, over the CTA's threads
+    for (int item = threadIdx.x; item < kG * 16; item += kThreads) {
+        const int hh = item >> 4, d8 = (item & 15) * 8;
+        float mmax = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) mmax = fmaxf(mmax, merge[w * kG * (kD + 2) + kG * kD + hh]);
-    const float mu = mmax == -INFINITY ? 0.0f : mmax;
-    float ov[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lsum = 0.0f;
+        for (int w = 0; w < kCW; ++w) mmax = fmaxf(mmax, merge[w * kG * (kD + 2) + kG * kD + hh]);
+        const float mu = mmax == -INFINITY ? 0.0f : mmax;
+        float ov[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lsum = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) {
-        const float *m2 = merge + w * kG * (kD + 2);
-        const float wt = ex2(m2[kG * kD + hh] - mu);
-        lsum += m2[kG * kD + kG + hh] * wt;
+        for (int w = 0; w < kCW; ++w) {
+            const float *m2 = merge + w * kG * (kD + 2);
+            const float wt = ex2(m2[kG * kD + hh] - mu);
+            lsum += m2[kG * kD + kG + hh] * wt;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ov[i] += m2[hh * kD + d8 + i] * wt;
-    }
-    const int64_t pidx = (((int64_t)b * p.H * p.NB + hv) * p.splits + split) * kG + hh;
-    float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * kD + d8);
-    dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
-    dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
-    if ((tid & 15) == 0) {
-        p.part_ml[2 * pidx] = mmax;
-        p.part_ml[2 * pidx + 1] = lsum;
+            for (int i = 0; i < 8; ++i) ov[i] += m2[hh * kD + d8 + i] * wt;
+        }
+        const int64_t pidx = (((int64_t)b * p.H * p.NB + hv) * p.splits + split) * kG + hh;
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * kD + d8);
+        dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
+        dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
+        if ((item & 15) == 0) {
+            p.part_ml[2 * pidx] = mmax;
+            p.part_ml[2 * pidx + 1] = lsum;
+        }
     }
 }
 
