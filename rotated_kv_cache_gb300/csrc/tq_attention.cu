@@ -343,8 +343,10 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
             break;
         }
         const uint32_t st = ring0 + slot * A::STAGE;
-        // two 16-row tiles per warp and stage (rows 16 warp and 16 kCW + 16 warp); unrolled,
-        // so the compiler interleaves their independent chains
+        // two 16-row tiles per warp and stage (rows 16 warp and 16 kCW + 16 warp): Q K^T for
+        // both, one softmax step over both, P V for both; the tile loops are unrolled so
+        // the compiler interleaves the tiles' independent chains
+        float S[kTiles][2][2];  // scores: [tile][row g, row g + 8][head 2c, 2c + 1]
 #pragma unroll
         for (int t2 = 0; t2 < kTiles; ++t2) {
             const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
@@ -380,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
             }
             // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum),
             // both heads of the lane at once on packed fp32 pairs
-            float S[2][2];
             {
                 const uint32_t m0 = (r0 + (16 * kCW) * t2) * 8, m1 = (r1 + (16 * kCW) * t2) * 8;
                 const uint2 s0 = lds64(st + A::OFF_KS + m0), s1 = lds64(st + A::OFF_KS + m1);
@@ -399,59 +400,78 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
                         sacc = __ffma2_rn(make_float2(sc, sc), t, sacc);
                     }
                     const float2 sv = __fmul2_rn(sacc, make_float2(ie[0], ie[1]));
-                    S[i][0] = sv.x;
-                    S[i][1] = sv.y;
+                    S[t2][i][0] = sv.x;
+                    S[t2][i][1] = sv.y;
                 }
                 if (tile_r + 16 > split_rows) {  // ragged tail: mask rows past the range
-                    if (tile_r + g >= split_rows) S[0][0] = S[0][1] = -INFINITY;
-                    if (tile_r + g + 8 >= split_rows) S[1][0] = S[1][1] = -INFINITY;
+                    if (tile_r + g >= split_rows) S[t2][0][0] = S[t2][0][1] = -INFINITY;
+                    if (tile_r + g + 8 >= split_rows) S[t2][1][0] = S[t2][1][1] = -INFINITY;
                 }
             }
-            // ---------------- online softmax (base 2) for heads 2c, 2c+1
-            // The running max is reduced across the tile's rows only when some lane
-            // sees a score above it (or no max exists yet); otherwise the weights
-            // are 2^(S - m) with the max unchanged, which is the same arithmetic.
-            float pr[2][2];
-            const bool raise = S[0][0] > m_run[0] || S[1][0] > m_run[0] || S[0][1] > m_run[1] || S[1][1] > m_run[1] ||
-                               m_run[0] == -INFINITY || m_run[1] == -INFINITY;
-            if (__any_sync(0xffffffffu, raise)) {
-                float alpha[2];
+        }
+        // ---------------- online softmax (base 2) over the warp's tiles, heads 2c, 2c+1
+        // The running max is reduced across the rows only when some lane sees a
+        // score above it (or no max exists yet); otherwise the weights are
+        // 2^(S - m) with the max unchanged, which is the same arithmetic.
+        float pr[kTiles][2][2];
+        bool raise = m_run[0] == -INFINITY || m_run[1] == -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    float mt = fmaxf(S[0][j], S[1][j]);
-                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-                    const float mn = fmaxf(m_run[j], mt);
-                    const float mu = mn == -INFINITY ? 0.0f : mn;
-                    alpha[j] = ex2(m_run[j] - mu);
-                    m_run[j] = mn;
-                    pr[0][j] = ex2(S[0][j] - mu);
-                    pr[1][j] = ex2(S[1][j] - mu);
-                    l_run[j] = l_run[j] * alpha[j] + pr[0][j] + pr[1][j];
-                }
-                // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
-                const float2 a2 = make_float2(alpha[0], alpha[1]);
+        for (int t2 = 0; t2 < kTiles; ++t2)
 #pragma unroll
-                for (int mt2 = 0; mt2 < 8; ++mt2) {
-                    const float2 x = __fmul2_rn(make_float2(o[mt2][0], o[mt2][1]), a2);
-                    const float2 y = __fmul2_rn(make_float2(o[mt2][2], o[mt2][3]), a2);
-                    o[mt2][0] = x.x;
-                    o[mt2][1] = x.y;
-                    o[mt2][2] = y.x;
-                    o[mt2][3] = y.y;
-                }
-            } else {
+            for (int i = 0; i < 2; ++i) raise = raise || S[t2][i][0] > m_run[0] || S[t2][i][1] > m_run[1];
+        if (__any_sync(0xffffffffu, raise)) {
+            float alpha[2];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    pr[0][j] = ex2(S[0][j] - m_run[j]);
-                    pr[1][j] = ex2(S[1][j] - m_run[j]);
-                    l_run[j] += pr[0][j] + pr[1][j];
+            for (int j = 0; j < 2; ++j) {
+                float mt = fmaxf(S[0][0][j], S[0][1][j]);
+#pragma unroll
+                for (int t2 = 1; t2 < kTiles; ++t2) mt = fmaxf(mt, fmaxf(S[t2][0][j], S[t2][1][j]));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                const float mn = fmaxf(m_run[j], mt);
+                const float mu = mn == -INFINITY ? 0.0f : mn;
+                alpha[j] = ex2(m_run[j] - mu);
+                m_run[j] = mn;
+                float ls = 0.0f;
+#pragma unroll
+                for (int t2 = 0; t2 < kTiles; ++t2) {
+                    pr[t2][0][j] = ex2(S[t2][0][j] - mu);
+                    pr[t2][1][j] = ex2(S[t2][1][j] - mu);
+                    ls += pr[t2][0][j] + pr[t2][1][j];
                 }
+                l_run[j] = l_run[j] * alpha[j] + ls;
             }
+            // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
+            const float2 a2 = make_float2(alpha[0], alpha[1]);
+#pragma unroll
+            for (int mt2 = 0; mt2 < 8; ++mt2) {
+                const float2 x = __fmul2_rn(make_float2(o[mt2][0], o[mt2][1]), a2);
+                const float2 y = __fmul2_rn(make_float2(o[mt2][2], o[mt2][3]), a2);
+                o[mt2][0] = x.x;
+                o[mt2][1] = x.y;
+                o[mt2][2] = y.x;
+                o[mt2][3] = y.y;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float ls = 0.0f;
+#pragma unroll
+                for (int t2 = 0; t2 < kTiles; ++t2) {
+                    pr[t2][0][j] = ex2(S[t2][0][j] - m_run[j]);
+                    pr[t2][1][j] = ex2(S[t2][1][j] - m_run[j]);
+                    ls += pr[t2][0][j] + pr[t2][1][j];
+                }
+                l_run[j] += ls;
+            }
+        }
+#pragma unroll
+        for (int t2 = 0; t2 < kTiles; ++t2) {
+            const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
             // ---------------- P^T as the B operand (tokens x heads), transposed in registers
-            const uint32_t pt0 = movmatrix_trans(pack_f16x2(pr[0][0], pr[0][1]));  // tokens 2c, 2c+1; head g
-            const uint32_t pt1 = movmatrix_trans(pack_f16x2(pr[1][0], pr[1][1]));  // tokens 2c+8, 2c+9
+            const uint32_t pt0 = movmatrix_trans(pack_f16x2(pr[t2][0][0], pr[t2][0][1]));  // tokens 2c, 2c+1; head g
+            const uint32_t pt1 = movmatrix_trans(pack_f16x2(pr[t2][1][0], pr[t2][1][1]));  // tokens 2c+8, 2c+9
             // value scales of this lane's four tokens (zero past the range)
             uint2 vs[4];
 #pragma unroll
@@ -503,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
                 for (int half = 0; half < 2; ++half)
                     mma16816(o[2 * G + half], av[0][half][0], av[0][half][1], av[1][half][0], av[1][half][1], b0, b1);
             }
-            // the last warp to finish this stage refills its slot with stage s + kStages
         }
+        // the last warp to finish this stage refills its slot with stage s + kStages
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();
