@@ -14,9 +14,11 @@
 // seq_len - M + i + 1).
 //
 // Design, after the specialised kernel's: split-KV CTAs stream 64-token stages
-// through a shared-memory ring (bulk copies completing on an mbarrier; the
-// last warp to finish a stage refills it); each of the 4 warps takes 16
-// tokens.  QK^T and PV run on mma.sync m16n8k16 (f16 in, f32 accumulate).
+// through a 2-deep shared-memory ring (bulk copies completing on an mbarrier;
+// the last warp to finish a stage refills it); each of the 2 warps takes two
+// 16-token tiles and works on both inside every group iteration, with one
+// softmax step over both (4 warps of one tile at head_dim 512).  QK^T and PV
+// run on mma.sync m16n8k16 (f16 in, f32 accumulate).
 // The MMA's N runs over "columns", a column being one (query row, q-head) of
 // the kv-head's G * M; a CTA takes NB blocks of 8 columns (NB = 1, 2 or 4 by
 // head_dim), so each dequantised key and value fragment feeds NB MMAs and a
@@ -35,8 +37,6 @@
 namespace tq {
 namespace {
 
-constexpr int gW = 4;               // warps per CTA
-constexpr int gThreads = gW * 32;
 constexpr int gT = 64;              // tokens per stage
 constexpr int gN = 8;               // q-heads per CTA (the MMA's N)
 constexpr int gMaxStages = 3;
@@ -161,14 +161,18 @@ struct GGeo {
     static constexpr int CB = gN * NB;                      // columns per CTA
     static constexpr int QF = CB * KS * 4 * 8;              // q fragments: [column][k-step][c] x (b0, b1)
     static constexpr int QS = (NG + 1) * CB * 4;            // group sums of the f16 q, then per-column score scale
-    static constexpr int MERGE = gW * CB * (D + 2) * 4;     // per-warp partials (reuse the ring)
+    // warps per CTA and 16-row tiles per warp and stage (worked on together): 2 x 2,
+    // except at head_dim 512, whose registers and stage ring leave room for two CTAs
+    // per SM, where 4 warps of one tile each keep 8 warps resident
+    static constexpr int W = D >= 512 ? 4 : 2, TILES = D >= 512 ? 1 : 2, THREADS = 32 * W;
+    static constexpr int MERGE = W * CB * (D + 2) * 4;      // per-warp partials (reuse the ring)
     // resident CTAs per SM the register budget is sized for: the output
     // accumulators take D * NB / 4 registers a thread
-    static constexpr int MIN_BLOCKS = D >= 512 ? 1 : (D * NB / 4 <= 32 ? 3 : 2);
+    static constexpr int MIN_BLOCKS = D >= 512 ? 1 : (D * NB / 4 <= 32 ? 6 : 4);
 };
 
 template <int D, int NB>
-__global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
+__global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
     attn_generic_kernel(const __grid_constant__ GenParams p)
 {
     using A = GGeo<D, NB>;
@@ -227,8 +231,8 @@ __global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
     // scaled by a power of two so its largest |q| lands in [2^14, 2^15) before
     // the f16 rounding; columns past the last are zero.
 #pragma unroll 1
-    for (int nb = 0; nb < NB; ++nb) {
-        const int n = nb * gN + 2 * warp + (lane >> 4), l16 = lane & 15;
+    for (int u = warp; u < NB * (gN / 2); u += A::W) {
+        const int n = (u / (gN / 2)) * gN + 2 * (u % (gN / 2)) + (lane >> 4), l16 = lane & 15;
         const int col = col0 + n;
         const bool real = col < p.cols;
         const int qi = real ? col / p.G : 0, qw = real ? col - qi * p.G : 0;
@@ -289,8 +293,10 @@ __global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
         m_run[nb][0] = m_run[nb][1] = -INFINITY;
         l_run[nb][0] = l_run[nb][1] = 0.0f;
     }
+    // tile t2 of this warp holds stage rows 16 warp + 16 W t2 + {0..15}
     const int r0 = 16 * warp + g, r1 = r0 + 8;
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
+    constexpr int TR = 16 * A::W;              // rows between a warp's tiles
     constexpr int QF_NB = gN * A::KS * 4 * 8;  // bytes of q fragments per block of 8 columns
     const uint32_t qf_lane = smem_addr(qf) + (g * A::KS * 4 + c) * 8, lut_a = smem_addr(lut);
 
@@ -302,79 +308,101 @@ __global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
             break;
         }
         const uint32_t st = smem_addr(stages + slot * p.stage_bytes);
-        const int64_t tile_t0 = t_begin + (int64_t)s * gT + 16 * warp;
+        const int64_t tile_t0 = t_begin + (int64_t)s * gT + 16 * warp;  // first row of tile 0
 
-        // ---------------- S = Q K^T, group by group, with the group affine;
-        // the dequantised key fragments serve every block of columns
-        float S[NB][2][2];
+        // ---------------- S = Q K^T, group by group, with the group affine, for
+        // both tiles; the dequantised key fragments serve every block of columns
+        float S[A::TILES][NB][2][2];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) S[nb][0][0] = S[nb][0][1] = S[nb][1][0] = S[nb][1][1] = 0.0f;
+        for (int t2 = 0; t2 < A::TILES; ++t2)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) S[t2][nb][0][0] = S[t2][nb][0][1] = S[t2][nb][1][0] = S[t2][nb][1][1] = 0.0f;
 #pragma unroll 1
         for (int G = 0; G < A::NG; ++G) {
-            uint32_t k0[4], k1[4];
-            key_pairs(st + r0 * p.rbk, G, c, p.kb, k0);
-            key_pairs(st + r1 * p.rbk, G, c, p.kb, k1);
-            const float sc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (r0 * NG + G) * 2));
-            const float sc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (r1 * NG + G) * 2));
-            const float zc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (r0 * NG + G) * 2)) - p.koff;
-            const float zc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (r1 * NG + G) * 2)) - p.koff;
+            uint2 bq[NB][2];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const uint2 bq = g_lds64(qf_lane + nb * QF_NB + (2 * G + jj) * 32);
-                    g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq.x, bq.y);
+                for (int jj = 0; jj < 2; ++jj) bq[nb][jj] = g_lds64(qf_lane + nb * QF_NB + (2 * G + jj) * 32);
+#pragma unroll
+            for (int t2 = 0; t2 < A::TILES; ++t2) {
+                const int ra = r0 + TR * t2, rb = r1 + TR * t2;
+                uint32_t k0[4], k1[4];
+                key_pairs(st + ra * p.rbk, G, c, p.kb, k0);
+                key_pairs(st + rb * p.rbk, G, c, p.kb, k1);
+                const float sc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (ra * NG + G) * 2));
+                const float sc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (rb * NG + G) * 2));
+                const float zc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (ra * NG + G) * 2)) - p.koff;
+                const float zc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (rb * NG + G) * 2)) - p.koff;
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+                        g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq[nb][jj].x, bq[nb][jj].y);
+                    // both columns of the lane at once on packed fp32 pairs
+                    const float2 qs = make_float2(qsum[G * CB + nb * gN + 2 * c], qsum[G * CB + nb * gN + 2 * c + 1]);
+                    const float2 s0 = __ffma2_rn(make_float2(sc0, sc0),
+                                                 __ffma2_rn(make_float2(zc0, zc0), qs, make_float2(acc[0], acc[1])),
+                                                 make_float2(S[t2][nb][0][0], S[t2][nb][0][1]));
+                    const float2 s1 = __ffma2_rn(make_float2(sc1, sc1),
+                                                 __ffma2_rn(make_float2(zc1, zc1), qs, make_float2(acc[2], acc[3])),
+                                                 make_float2(S[t2][nb][1][0], S[t2][nb][1][1]));
+                    S[t2][nb][0][0] = s0.x;
+                    S[t2][nb][0][1] = s0.y;
+                    S[t2][nb][1][0] = s1.x;
+                    S[t2][nb][1][1] = s1.y;
                 }
-                // both columns of the lane at once on packed fp32 pairs
-                const float2 qs = make_float2(qsum[G * CB + nb * gN + 2 * c], qsum[G * CB + nb * gN + 2 * c + 1]);
-                const float2 s0 = __ffma2_rn(make_float2(sc0, sc0),
-                                             __ffma2_rn(make_float2(zc0, zc0), qs, make_float2(acc[0], acc[1])),
-                                             make_float2(S[nb][0][0], S[nb][0][1]));
-                const float2 s1 = __ffma2_rn(make_float2(sc1, sc1),
-                                             __ffma2_rn(make_float2(zc1, zc1), qs, make_float2(acc[2], acc[3])),
-                                             make_float2(S[nb][1][0], S[nb][1][1]));
-                S[nb][0][0] = s0.x;
-                S[nb][0][1] = s0.y;
-                S[nb][1][0] = s1.x;
-                S[nb][1][1] = s1.y;
             }
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             const float ie0 = qsum[NG * CB + nb * gN + 2 * c], ie1 = qsum[NG * CB + nb * gN + 2 * c + 1];
-            S[nb][0][0] *= ie0; S[nb][1][0] *= ie0;
-            S[nb][0][1] *= ie1; S[nb][1][1] *= ie1;
+#pragma unroll
+            for (int t2 = 0; t2 < A::TILES; ++t2) {
+                S[t2][nb][0][0] *= ie0; S[t2][nb][1][0] *= ie0;
+                S[t2][nb][0][1] *= ie1; S[t2][nb][1][1] *= ie1;
+            }
         }
         // causal mask: row t is hidden from query row i when t >= base0 + i
         // (this also hides every row past t_end, which is at most the last
         // column's limit, or the split's end when the tile stops there)
-        if (tile_t0 + 16 > lim_lo) {
-            const int64_t ta = tile_t0 + g - p.base0, tb = ta + 8;
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
+        for (int t2 = 0; t2 < A::TILES; ++t2) {
+            const int64_t tt0 = tile_t0 + TR * t2;
+            if (tt0 + 16 > lim_lo) {
+                const int64_t ta = tt0 + g - p.base0, tb = ta + 8;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int col = col0 + nb * gN + 2 * c + j;
-                    const int64_t qi = col < p.cols ? col / p.G : p.M - 1;
-                    if (ta >= qi) S[nb][0][j] = -INFINITY;
-                    if (tb >= qi) S[nb][1][j] = -INFINITY;
-                }
+                for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int col = col0 + nb * gN + 2 * c + j;
+                        const int64_t qi = col < p.cols ? col / p.G : p.M - 1;
+                        if (ta >= qi) S[t2][nb][0][j] = -INFINITY;
+                        if (tb >= qi) S[t2][nb][1][j] = -INFINITY;
+                    }
+            }
         }
-        // ---------------- online softmax (base 2), columns 2c, 2c+1 of each block
-        float pr[NB][2][2];
+        // ---------------- online softmax (base 2) over both tiles, columns 2c, 2c+1 of each block
+        float pr[A::TILES][NB][2][2];
         bool raise = false;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-                raise |= S[nb][0][j] > m_run[nb][j] || S[nb][1][j] > m_run[nb][j] || m_run[nb][j] == -INFINITY;
+            for (int j = 0; j < 2; ++j) {
+                raise |= m_run[nb][j] == -INFINITY;
+#pragma unroll
+                for (int t2 = 0; t2 < A::TILES; ++t2)
+                    raise |= S[t2][nb][0][j] > m_run[nb][j] || S[t2][nb][1][j] > m_run[nb][j];
+            }
         if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    float mt = fmaxf(S[nb][0][j], S[nb][1][j]);
+                    float mt = fmaxf(S[0][nb][0][j], S[0][nb][1][j]);
+#pragma unroll
+                    for (int t2 = 1; t2 < A::TILES; ++t2) mt = fmaxf(mt, fmaxf(S[t2][nb][0][j], S[t2][nb][1][j]));
                     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
                     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
                     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
@@ -382,9 +410,14 @@ __global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
                     const float mu = mn == -INFINITY ? 0.0f : mn;
                     const float alpha = g_ex2(m_run[nb][j] - mu);
                     m_run[nb][j] = mn;
-                    pr[nb][0][j] = g_ex2(S[nb][0][j] - mu);
-                    pr[nb][1][j] = g_ex2(S[nb][1][j] - mu);
-                    l_run[nb][j] = l_run[nb][j] * alpha + pr[nb][0][j] + pr[nb][1][j];
+                    float ls = 0.0f;
+#pragma unroll
+                    for (int t2 = 0; t2 < A::TILES; ++t2) {
+                        pr[t2][nb][0][j] = g_ex2(S[t2][nb][0][j] - mu);
+                        pr[t2][nb][1][j] = g_ex2(S[t2][nb][1][j] - mu);
+                        ls += pr[t2][nb][0][j] + pr[t2][nb][1][j];
+                    }
+                    l_run[nb][j] = l_run[nb][j] * alpha + ls;
 #pragma unroll
                     for (int mt2 = 0; mt2 < A::KS; ++mt2) {
                         o[nb][mt2][j] *= alpha;
@@ -396,53 +429,65 @@ __global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    pr[nb][0][j] = g_ex2(S[nb][0][j] - m_run[nb][j]);
-                    pr[nb][1][j] = g_ex2(S[nb][1][j] - m_run[nb][j]);
-                    l_run[nb][j] += pr[nb][0][j] + pr[nb][1][j];
+                    float ls = 0.0f;
+#pragma unroll
+                    for (int t2 = 0; t2 < A::TILES; ++t2) {
+                        pr[t2][nb][0][j] = g_ex2(S[t2][nb][0][j] - m_run[nb][j]);
+                        pr[t2][nb][1][j] = g_ex2(S[t2][nb][1][j] - m_run[nb][j]);
+                        ls += pr[t2][nb][0][j] + pr[t2][nb][1][j];
+                    }
+                    l_run[nb][j] += ls;
                 }
         }
-        uint32_t pt0[NB], pt1[NB];
+        uint32_t pt0[A::TILES][NB], pt1[A::TILES][NB];
+        bool vlive[A::TILES][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            pt0[nb] = g_trans(g_pack_f16x2(pr[nb][0][0], pr[nb][0][1]));  // tokens 2c, 2c+1; column g
-            pt1[nb] = g_trans(g_pack_f16x2(pr[nb][1][0], pr[nb][1][1]));  // tokens 2c+8, 2c+9
-        }
-        bool vlive[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) vlive[q] = tile_t0 + (vr[q] - 16 * warp) < t_end;
-        // ---------------- O^T += V^T (P * rms)^T, group by group; the value
-        // fragments serve every block of columns
-#pragma unroll
-        for (int G = 0; G < A::NG; ++G) {
-            uint32_t sv[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) sv[q] = vlive[q] ? g_lds16(st + p.off_vs + (vr[q] * NG + G) * 2) : 0u;
-            const uint32_t sv01 = sv[0] | (sv[1] << 16), sv23 = sv[2] | (sv[3] << 16);
-            uint32_t hv[4][4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) value_quad(st + p.off_v + vr[q] * p.rbv, G, g, p.vb, lut_a, hv[q]);
-            uint32_t a[2][4];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                // rows g, g+8 of the m-tile: dims 32G + 4g + 2 half + {0, 1}
-                const int r = 2 * half;
-                a[half][0] = hv[0][r] | (hv[1][r] << 16);
-                a[half][1] = hv[0][r + 1] | (hv[1][r + 1] << 16);
-                a[half][2] = hv[2][r] | (hv[3][r] << 16);
-                a[half][3] = hv[2][r + 1] | (hv[3][r + 1] << 16);
-            }
+        for (int t2 = 0; t2 < A::TILES; ++t2) {
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-                const uint32_t b0 = g_hmul2(pt0[nb], sv01), b1 = g_hmul2(pt1[nb], sv23);
+                pt0[t2][nb] = g_trans(g_pack_f16x2(pr[t2][nb][0][0], pr[t2][nb][0][1]));  // tokens 2c, 2c+1; column g
+                pt1[t2][nb] = g_trans(g_pack_f16x2(pr[t2][nb][1][0], pr[t2][nb][1][1]));  // tokens 2c+8, 2c+9
+            }
 #pragma unroll
-                for (int half = 0; half < 2; ++half)
-                    g_mma(o[nb][2 * G + half], a[half][0], a[half][1], a[half][2], a[half][3], b0, b1);
+            for (int q = 0; q < 4; ++q) vlive[t2][q] = tile_t0 + TR * t2 + (vr[q] - 16 * warp) < t_end;
+        }
+        // ---------------- O^T += V^T (P * rms)^T, group by group, both tiles; the
+        // value fragments serve every block of columns
+#pragma unroll
+        for (int G = 0; G < A::NG; ++G) {
+#pragma unroll
+            for (int t2 = 0; t2 < A::TILES; ++t2) {
+                uint32_t sv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    sv[q] = vlive[t2][q] ? g_lds16(st + p.off_vs + ((vr[q] + TR * t2) * NG + G) * 2) : 0u;
+                const uint32_t sv01 = sv[0] | (sv[1] << 16), sv23 = sv[2] | (sv[3] << 16);
+                uint32_t hv[4][4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) value_quad(st + p.off_v + (vr[q] + TR * t2) * p.rbv, G, g, p.vb, lut_a, hv[q]);
+                uint32_t a[2][4];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    // rows g, g+8 of the m-tile: dims 32G + 4g + 2 half + {0, 1}
+                    const int r = 2 * half;
+                    a[half][0] = hv[0][r] | (hv[1][r] << 16);
+                    a[half][1] = hv[0][r + 1] | (hv[1][r + 1] << 16);
+                    a[half][2] = hv[2][r] | (hv[3][r] << 16);
+                    a[half][3] = hv[2][r + 1] | (hv[3][r + 1] << 16);
+                }
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    const uint32_t b0 = g_hmul2(pt0[t2][nb], sv01), b1 = g_hmul2(pt1[t2][nb], sv23);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+                        g_mma(o[nb][2 * G + half], a[half][0], a[half][1], a[half][2], a[half][3], b0, b1);
+                }
             }
         }
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();
-            if (atomicAdd(&done[slot], 1u) == gW - 1) {
+            if (atomicAdd(&done[slot], 1u) == A::W - 1) {
                 done[slot] = 0;
                 if (s + p.stages < n_stages) issue(s + p.stages);
             }
@@ -483,17 +528,16 @@ __global__ void __launch_bounds__(gThreads, GGeo<D, NB>::MIN_BLOCKS)
     constexpr int PER = D / 16;
     const int d0 = (threadIdx.x & 15) * PER;
 #pragma unroll 1
-    for (int nb = 0; nb < NB; ++nb) {
-        const int hh = nb * gN + (threadIdx.x >> 4);
+    for (int hh = threadIdx.x >> 4; hh < CB; hh += A::THREADS / 16) {
         float mmax = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < gW; ++w) mmax = fmaxf(mmax, merge[w * CB * (D + 2) + CB * D + hh]);
+        for (int w = 0; w < A::W; ++w) mmax = fmaxf(mmax, merge[w * CB * (D + 2) + CB * D + hh]);
         const float mu = mmax == -INFINITY ? 0.0f : mmax;
         float ov[PER], lsum = 0.0f;
 #pragma unroll
         for (int i = 0; i < PER; ++i) ov[i] = 0.0f;
 #pragma unroll
-        for (int w = 0; w < gW; ++w) {
+        for (int w = 0; w < A::W; ++w) {
             const float *m2 = merge + w * CB * (D + 2);
             const float wt = g_ex2(m2[CB * D + hh] - mu);
             lsum += m2[CB * D + CB + hh] * wt;
@@ -595,7 +639,7 @@ int gen_ctas_per_sm(int smem)
     int n = 0;
     auto kern = attn_generic_kernel<D, NB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, gThreads, smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, GGeo<D, NB>::THREADS, smem) != cudaSuccess) return 0;
     return n;
 }
 
@@ -611,7 +655,7 @@ bool gen_plan_nb(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, Ge
     pl.off_vs = pl.off_kz + r16(gT * NG * 2);
     pl.off_v = pl.off_vs + r16(gT * NG * 2);
     pl.stage_bytes = (pl.off_v + gT * rbv + 16 + 127) / 128 * 128;
-    pl.stages = 3 * pl.stage_bytes <= 80 * 1024 ? 3 : 2;
+    pl.stages = 2;  // with 2-warp CTAs a deeper ring only costs resident CTAs
     const int ring = pl.stages * pl.stage_bytes > A::MERGE ? pl.stages * pl.stage_bytes : A::MERGE;
     pl.smem = 128 /*align slack*/ + ring + A::QF + A::QS + 512 /*lut*/ + gMaxStages * 12 /*barriers, counters*/;
     const int per_sm = gen_ctas_per_sm<D, NB>(pl.smem);
@@ -707,9 +751,9 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
     const dim3 grid(pl.splits, c.H * pl.hb, c.B);
     switch (pl.nb) {
-    case 1: attn_generic_kernel<D, 1><<<grid, gThreads, pl.smem, s>>>(p); break;
-    case 2: if constexpr (D <= 256) attn_generic_kernel<D, 2><<<grid, gThreads, pl.smem, s>>>(p); break;
-    case 4: if constexpr (D <= 128) attn_generic_kernel<D, 4><<<grid, gThreads, pl.smem, s>>>(p); break;
+    case 1: attn_generic_kernel<D, 1><<<grid, GGeo<D, 1>::THREADS, pl.smem, s>>>(p); break;
+    case 2: if constexpr (D <= 256) attn_generic_kernel<D, 2><<<grid, GGeo<D, 2>::THREADS, pl.smem, s>>>(p); break;
+    case 4: if constexpr (D <= 128) attn_generic_kernel<D, 4><<<grid, GGeo<D, 4>::THREADS, pl.smem, s>>>(p); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
