@@ -574,6 +574,23 @@ def run_sweep(only=None):
         emit("attention", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": kb, "vb": vb, "group": G, "kernel": path},
              us, B * H * T * bpt + B * G * H * d * 6)
         del cache, ws, out, q
+    # long-context serving scale: 32 sequences x 8 kv-heads x 131072 cached rows
+    # plus the appended one, k4v3 (4.56 GB packed), one decode step
+    if want("long_context_attention"):
+        wl = tq_synth.WORKLOADS["longctx"]
+        B, Tl, G = wl.B, wl.T + 1, wl.QH // wl.H
+        cache = filled_cache(B, wl.H, wl.d, Tl, wl.kb, wl.vb, wl)
+        q = torch.empty((B, wl.QH, wl.d), dtype=torch.int16, device="cuda")
+        tq_synth.device_q(wl, 0, q, B=B, QH=wl.QH, d=wl.d)
+        qb = q.view(torch.bfloat16)
+        out = torch.empty((B, wl.QH, wl.d), dtype=torch.float32, device="cuda")
+        ws = torch.empty(tq.tq_attention_workspace_bytes(cache, wl.QH, Tl), dtype=torch.uint8, device="cuda")
+        us = timed(lambda: tq.tq_decode_attention(cache, qb, Tl, out=out, workspace=ws))
+        bpt = tq.tq_bytes_per_token_head(wl.d, wl.kb, wl.vb)
+        emit("long_context_attention", {"B": B, "kv_heads": wl.H, "rows": Tl, "d": wl.d, "kb": wl.kb, "vb": wl.vb,
+                                        "group": G, "kernel": "specialised"},
+             us, B * wl.H * Tl * bpt + B * wl.QH * wl.d * 6)
+        del cache, ws, out, q, qb
     # multi-token attention: chunks of M = 4 and 128 query rows (the page's
     # forward shapes) over a 32769-row cache.  The MMA work is 4 d flops per
     # (column, cache row), a column being one (query row, q-head).
@@ -630,8 +647,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="measure the paths beyond the headline step instead (one JSON line each)")
     ap.add_argument("--only", default="",
-                    help="with --sweep: comma-separated kinds to run (attention, multi_token_attention, "
-                         "rotated_fetch, unrotate, copy_rows, clear_rows)")
+                    help="with --sweep: comma-separated kinds to run (attention, long_context_attention, "
+                         "multi_token_attention, rotated_fetch, unrotate, copy_rows, clear_rows)")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(set(filter(None, args.only.split(","))))
