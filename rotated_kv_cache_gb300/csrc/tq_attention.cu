@@ -44,7 +44,7 @@ namespace tq {
 namespace {
 
 constexpr int kD = 128;            // head_dim covered
-constexpr int kG = 8;              // MMA columns: q-heads per kv-head, up to 8 (the rest zero)
+constexpr int kG = 8;              // MMA columns: a block of 8 of a kv-head's q-heads
 constexpr int kVB = 3;             // value bits covered
 constexpr int kCW = 2;             // warps per CTA (all compute; the last to finish a stage refills it)
 constexpr int kThreads = kCW * 32;
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
 
     // V field extraction: lane g owns dims 32G + 4g + {0..3}: 12 bits at 96G + 12g
     const int v_word = (12 * g) >> 5, v_shift = (12 * g) & 31;
-    const int r0 = 16 * warp + g, r1 = r0 + 8;  // key rows of this lane in a stage
+    const int r0 = 16 * warp + g, r1 = r0 + 8;  // key rows of this lane in the warp's first tile
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
 
     // lane-constant byte offsets in a stage: key chunks of row r0 per group (row r1 is
