@@ -489,14 +489,14 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
     *reinterpret_cast<uint32_t *>(p.scale + crow * (D / 32) + 2 * part) = sw;
 }
 
-// ------------------------------------------------------------------ kernel
+// ------------------------------------------------------------------ kernels
+// The work of CTA `cta` of `ncta` encoding keys (KEY) or values.
 template <int D, int BITS, bool KEY>
-__global__ void __launch_bounds__(kWarps * 32)
-    encode_kernel(const __grid_constant__ EncodeParams p, const __grid_constant__ CUtensorMap map)
+__device__ __forceinline__ void encode_body(const EncodeParams &p, const CUtensorMap &map, uint8_t *smem_raw,
+                                            uint32_t cta, uint32_t ncta)
 {
     using G = EGeo<D, KEY>;
     constexpr int SB = (!KEY && BITS > 3) ? 1024 : 0;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
     // tiles need 1024-byte alignment (swizzle atoms); the rest follows them
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -532,8 +532,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 
     const int r = lane % G::ROWS, part = lane / G::ROWS;
     const uint32_t my_mtab = smem_addr(mtab) + part * 272;
-    const uint32_t W = gridDim.x * kWarps;
-    uint32_t item = blockIdx.x * kWarps + warp;
+    const uint32_t W = ncta * kWarps;
+    uint32_t item = cta * kWarps + warp;
     if (item < p.items) issue_tile<D, KEY>(p, map, item, buf0, bar0, lane);
     for (uint32_t k = 0; item < p.items; item += W, ++k) {
         const uint32_t next = item + W;
@@ -585,11 +585,41 @@ __global__ void __launch_bounds__(kWarps * 32)
 }
 
 template <int D, int BITS, bool KEY>
-cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
+__global__ void __launch_bounds__(kWarps * 32)
+    encode_kernel(const __grid_constant__ EncodeParams p, const __grid_constant__ CUtensorMap map)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    encode_body<D, BITS, KEY>(p, map, smem_raw, blockIdx.x, gridDim.x);
+}
+
+// Keys and values of a small append in one launch (the two encodes of a
+// one-token step are latency, not bandwidth): CTAs [0, key_ctas) encode the
+// keys, the others the values.
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(kWarps * 32)
+    encode_kv_kernel(const __grid_constant__ EncodeParams pk, const __grid_constant__ CUtensorMap mk,
+                     const __grid_constant__ EncodeParams pv, const __grid_constant__ CUtensorMap mv, uint32_t key_ctas)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    if (blockIdx.x < key_ctas)
+        encode_body<D, KB, true>(pk, mk, smem_raw, blockIdx.x, key_ctas);
+    else
+        encode_body<D, VB, false>(pv, mv, smem_raw, blockIdx.x - key_ctas, gridDim.x - key_ctas);
+}
+
+// dynamic shared memory of encode_body<D, BITS, KEY>
+template <int D, int BITS, bool KEY>
+constexpr size_t encode_smem()
 {
     using G = EGeo<D, KEY>;
-    const size_t smem = 1024 /*alignment slack*/ + (size_t)kWarps * 2 * G::TILE + 16 * kWarps +
-                        ((!KEY && BITS > 3) ? 1024 : 0) + G::MTAB + (size_t)kWarps * (KEY ? 0 : VStage<D, BITS>::BYTES);
+    return 1024 /*alignment slack*/ + (size_t)kWarps * 2 * G::TILE + 16 * kWarps + ((!KEY && BITS > 3) ? 1024 : 0) +
+           G::MTAB + (size_t)kWarps * (KEY ? 0 : VStage<D, BITS>::BYTES);
+}
+
+template <int D, int BITS, bool KEY>
+cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
+{
+    const size_t smem = encode_smem<D, BITS, KEY>();
     auto kern = encode_kernel<D, BITS, KEY>;
     static int per_sm = 0;  // same on every GB300; only a successful query is kept
     if (!per_sm) {
@@ -603,6 +633,24 @@ cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
     const int64_t want = ((int64_t)p.items + kWarps - 1) / kWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
     kern<<<grid, kWarps * 32, smem, s>>>(p, map);
+    return cudaGetLastError();
+}
+
+// keys and values in one launch (encode_kv_kernel); every CTA is resident at once
+template <int D, int KB, int VB>
+cudaError_t run_kv(const EncodeParams &pk, const CUtensorMap &mk, const EncodeParams &pv, const CUtensorMap &mv,
+                   uint32_t key_ctas, uint32_t value_ctas, cudaStream_t s)
+{
+    constexpr size_t sk = encode_smem<D, KB, true>(), sv = encode_smem<D, VB, false>();
+    constexpr size_t smem = sk > sv ? sk : sv;
+    auto kern = encode_kv_kernel<D, KB, VB>;
+    static bool attr = false;  // same on every GB300; only a successful call is kept
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    kern<<<key_ctas + value_ctas, kWarps * 32, smem, s>>>(pk, mk, pv, mv, key_ctas);
     return cudaGetLastError();
 }
 
@@ -675,26 +723,36 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     const Tables &tab = codebook_tables(c.vb);
     for (int i = 0; i < (1 << c.vb) - 1; ++i) p.bnd[i] = tab.boundaries[i];
 
-    CUtensorMap map{};
-    p.src = k;
-    p.sb = ks[0]; p.sh = ks[1]; p.st = ks[2];
-    p.codes = c.k_codes;
-    p.scale = c.k_scale;
-    p.zero = c.k_zero;
-    p.div_h = make_fastdiv((uint32_t)c.H);
-    if (!set_items(p, n, EGeo<D, true>::TROWS, c)) return cudaErrorInvalidValue;
-    p.use_tma = input_map(&map, k, D, n, c.H, c.B, ks, EGeo<D, true>::TROWS) ? 1 : 0;
-    cudaError_t e = dispatch_key<D>(c.kb, p, map, s);
-    if (e != cudaSuccess) return e;
+    EncodeParams pk = p, pv = p;
+    CUtensorMap mk{}, mv{};
+    pk.src = k;
+    pk.sb = ks[0]; pk.sh = ks[1]; pk.st = ks[2];
+    pk.codes = c.k_codes;
+    pk.scale = c.k_scale;
+    pk.zero = c.k_zero;
+    pk.div_h = make_fastdiv((uint32_t)c.H);
+    if (!set_items(pk, n, EGeo<D, true>::TROWS, c)) return cudaErrorInvalidValue;
+    pk.use_tma = input_map(&mk, k, D, n, c.H, c.B, ks, EGeo<D, true>::TROWS) ? 1 : 0;
 
-    p.src = v;
-    p.sb = vs[0]; p.sh = vs[1]; p.st = vs[2];
-    p.codes = c.v_codes;
-    p.scale = c.v_scale;
-    p.zero = nullptr;
-    if (!set_items(p, n, EGeo<D, false>::TROWS, c)) return cudaErrorInvalidValue;
-    p.use_tma = input_map(&map, v, D, n, c.H, c.B, vs, EGeo<D, false>::TROWS) ? 1 : 0;
-    return dispatch_value<D>(c.vb, p, map, s);
+    pv.src = v;
+    pv.sb = vs[0]; pv.sh = vs[1]; pv.st = vs[2];
+    pv.codes = c.v_codes;
+    pv.scale = c.v_scale;
+    pv.zero = nullptr;
+    pv.div_h = make_fastdiv((uint32_t)c.H);
+    if (!set_items(pv, n, EGeo<D, false>::TROWS, c)) return cudaErrorInvalidValue;
+    pv.use_tma = input_map(&mv, v, D, n, c.H, c.B, vs, EGeo<D, false>::TROWS) ? 1 : 0;
+
+    // a small append (a few rows per sequence-head, as in a decode step) runs
+    // keys and values in one launch when both grids fit one CTA per SM
+    const uint32_t gk = (pk.items + kWarps - 1) / kWarps, gv = (pv.items + kWarps - 1) / kWarps;
+    if ((int64_t)gk + gv <= num_sms() && c.vb == 3 && (c.kb == 8 || c.kb == 4)) {
+        if (c.kb == 8) return run_kv<D, 8, 3>(pk, mk, pv, mv, gk, gv, s);
+        return run_kv<D, 4, 3>(pk, mk, pv, mv, gk, gv, s);
+    }
+    cudaError_t e = dispatch_key<D>(c.kb, pk, mk, s);
+    if (e != cudaSuccess) return e;
+    return dispatch_value<D>(c.vb, pv, mv, s);
 }
 
 }  // namespace
