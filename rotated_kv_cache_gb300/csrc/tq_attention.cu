@@ -603,23 +603,51 @@ struct CombineParams {
 };
 
 // one warp per (sequence, q-head); lane holds dims 4*lane .. 4*lane+3
-__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineParams p)
+// One CTA of kCombineWarps warps per (sequence, q-head): the warps merge
+// interleaved subsets of the splits, then warp 0 merges the warps' results
+// (a few hundred splits at batch 1 would be a long serial chain for one warp).
+constexpr int kCombineWarps = 4;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const __grid_constant__ CombineParams p)
 {
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (row >= p.rows) return;  // whole warps only
+    __shared__ float4 wo[kCombineWarps][32];
+    __shared__ float wm[kCombineWarps], wl[kCombineWarps];
+    const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = row / p.QH, qh = row % p.QH;
     const int h = qh / p.G, hq = qh % p.G;
     const int hh = hq % kG;  // column of block hq / kG
     const int64_t base = ((int64_t)b * p.H * p.NB + (int64_t)h * p.NB + hq / kG) * p.splits;
+    // this warp's splits: warp, warp + kCombineWarps, ...
+    float mw = -INFINITY;
+    for (int s = warp; s < p.splits; s += kCombineWarps) mw = fmaxf(mw, p.part_ml[2 * ((base + s) * kG + hh)]);
+    const float muw = mw == -INFINITY ? 0.0f : mw;
+    float4 xw = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float lw = 0.0f;
+    for (int s = warp; s < p.splits; s += kCombineWarps) {
+        const int64_t pi = (base + s) * kG + hh;
+        const float wt = ex2(p.part_ml[2 * pi] - muw);
+        lw += p.part_ml[2 * pi + 1] * wt;
+        const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pi * kD + 4 * lane);
+        xw.x += v.x * wt; xw.y += v.y * wt; xw.z += v.z * wt; xw.w += v.w * wt;
+    }
+    wo[warp][lane] = xw;
+    if (lane == 0) {
+        wm[warp] = mw;
+        wl[warp] = lw;
+    }
+    __syncthreads();
+    if (warp != 0) return;
     float mmax = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * kG + hh)]);
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) mmax = fmaxf(mmax, wm[w]);
     const float mu = mmax == -INFINITY ? 0.0f : mmax;
     float x[4] = {0, 0, 0, 0}, l = 0.0f;
-    for (int s = 0; s < p.splits; ++s) {
-        const int64_t pi = (base + s) * kG + hh;
-        const float wt = ex2(p.part_ml[2 * pi] - mu);
-        l += p.part_ml[2 * pi + 1] * wt;
-        const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pi * kD + 4 * lane);
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+        // a warp without live splits carries zeros; the others rescale to the common max
+        const float wt = wm[w] == -INFINITY ? 0.0f : ex2(wm[w] - mu);
+        l += wl[w] * wt;
+        const float4 v = wo[w][lane];
         x[0] += v.x * wt; x[1] += v.y * wt; x[2] += v.z * wt; x[3] += v.w * wt;
     }
     const float inv_l = 1.0f / l;
@@ -782,7 +810,7 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     cp.rows = c.B * QH;
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
-    attn_combine_kernel<<<(cp.rows + 7) / 8, 256, 0, s>>>(cp);
+    attn_combine_kernel<<<cp.rows, kCombineWarps * 32, 0, s>>>(cp);
     return cudaGetLastError();
 }
 
@@ -914,7 +942,7 @@ cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, i
     cp.rows = c.B * QH;
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
-    attn_combine_kernel<<<(cp.rows + 7) / 8, 256, 0, s>>>(cp);
+    attn_combine_kernel<<<cp.rows, kCombineWarps * 32, 0, s>>>(cp);
     return cudaGetLastError();
 }
 
