@@ -563,30 +563,66 @@ struct GenCombineParams {
     float inv_sqrt_d;
 };
 
-// one warp per (sequence, query row, q-head); lane holds dims PER*lane .. +PER-1
-template <int D>
-__global__ void __launch_bounds__(256) attn_generic_combine(const __grid_constant__ GenCombineParams p)
+// CTAs of gCombineWarps warps; each (sequence, query row, q-head) takes W of
+// them: W = 4 when there are many splits (the warps merge interleaved subsets,
+// then the first merges their results), else W = 1 and one warp walks them.
+// Lane holds dims PER*lane .. +PER-1.
+constexpr int gCombineWarps = 4;
+
+template <int D, int W>
+__global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const __grid_constant__ GenCombineParams p)
 {
     constexpr int PER = D / 32;
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (row >= p.rows) return;
+    __shared__ float wo[W > 1 ? gCombineWarps : 1][PER][32];  // [warp][k][lane]: conflict-free
+    __shared__ float wm[gCombineWarps], wl[gCombineWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (gCombineWarps / W) + warp / W, wid = warp % W, lead = warp - wid;
+    const bool live = row < p.rows;
+    if (W == 1 && !live) return;  // no barrier below when W = 1
     const int per_seq = p.M * p.QH;
     const int b = row / per_seq, rem = row - b * per_seq, i = rem / p.QH, qh = rem - i * p.QH;
     const int h = qh / p.G, col = i * p.G + (qh - h * p.G), hb = col / p.CB, n = col - hb * p.CB;
     const int64_t base = (((int64_t)b * p.H + h) * p.HB + hb) * p.splits;
-    float mmax = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mmax = fmaxf(mmax, p.part_ml[2 * ((base + s) * p.CB + n)]);
-    const float mu = mmax == -INFINITY ? 0.0f : mmax;
+    float mw = -INFINITY;
+    if (live)
+        for (int s = wid; s < p.splits; s += W) mw = fmaxf(mw, p.part_ml[2 * ((base + s) * p.CB + n)]);
+    const float muw = mw == -INFINITY ? 0.0f : mw;
     float x[PER], l = 0.0f;
 #pragma unroll
     for (int k = 0; k < PER; ++k) x[k] = 0.0f;
-    for (int s = 0; s < p.splits; ++s) {
-        const int64_t pi = (base + s) * p.CB + n;
-        const float wt = g_ex2(p.part_ml[2 * pi] - mu);
-        l += p.part_ml[2 * pi + 1] * wt;
-        const float *src = p.part_o + pi * D + PER * lane;
+    if (live)
+        for (int s = wid; s < p.splits; s += W) {
+            const int64_t pi = (base + s) * p.CB + n;
+            const float wt = g_ex2(p.part_ml[2 * pi] - muw);
+            l += p.part_ml[2 * pi + 1] * wt;
+            const float *src = p.part_o + pi * D + PER * lane;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) x[k] += src[k] * wt;
+            for (int k = 0; k < PER; ++k) x[k] += src[k] * wt;
+        }
+    if constexpr (W > 1) {
+#pragma unroll
+        for (int k = 0; k < PER; ++k) wo[warp][k][lane] = x[k];
+        if (lane == 0) {
+            wm[warp] = mw;
+            wl[warp] = l;
+        }
+        __syncthreads();
+        if (wid != 0 || !live) return;
+        float mmax = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) mmax = fmaxf(mmax, wm[lead + w]);
+        const float mu = mmax == -INFINITY ? 0.0f : mmax;
+        l = 0.0f;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) x[k] = 0.0f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            // a warp without live splits carries zeros; the others rescale to the common max
+            const float wt = wm[lead + w] == -INFINITY ? 0.0f : g_ex2(wm[lead + w] - mu);
+            l += wl[lead + w] * wt;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) x[k] += wo[lead + w][k][lane] * wt;
+        }
     }
     const float inv_l = 1.0f / l;
 #pragma unroll
@@ -617,6 +653,16 @@ __global__ void __launch_bounds__(256) attn_generic_combine(const __grid_constan
 }
 
 // ---------------------------------------------------------------- host side
+// 4 warps per row from 8 splits up, else one warp per row (4 rows per CTA)
+template <int D>
+void launch_generic_combine(const GenCombineParams &cp, cudaStream_t s)
+{
+    if (cp.splits >= 8)
+        attn_generic_combine<D, 4><<<cp.rows, gCombineWarps * 32, 0, s>>>(cp);
+    else
+        attn_generic_combine<D, 1><<<(cp.rows + gCombineWarps - 1) / gCombineWarps, gCombineWarps * 32, 0, s>>>(cp);
+}
+
 struct GenPlan {
     int nb, hb, splits, stages, stage_bytes, smem;
     int64_t tokens_per_split;
@@ -760,7 +806,7 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     const int rows = c.B * (int)m * QH;
     GenCombineParams cp{p.part_o, p.part_ml, out, c.H, QH, G, (int)m, pl.hb, CB, pl.splits, rows,
                         inv_sqrt_head_dim(D)};
-    attn_generic_combine<D><<<(rows + 7) / 8, 256, 0, s>>>(cp);
+    launch_generic_combine<D>(cp, s);
     return cudaGetLastError();
 }
 
@@ -771,12 +817,11 @@ cudaError_t launch_attention_combine_parts(int d, const float *part_o, const flo
 {
     const int rows = B * m * QH;
     GenCombineParams cp{part_o, part_ml, out, H, QH, QH / H, m, hb, cb, splits, rows, inv_sqrt_head_dim(d)};
-    const dim3 grid((rows + 7) / 8);
     switch (d) {
-    case 64: attn_generic_combine<64><<<grid, 256, 0, s>>>(cp); break;
-    case 128: attn_generic_combine<128><<<grid, 256, 0, s>>>(cp); break;
-    case 256: attn_generic_combine<256><<<grid, 256, 0, s>>>(cp); break;
-    case 512: attn_generic_combine<512><<<grid, 256, 0, s>>>(cp); break;
+    case 64: launch_generic_combine<64>(cp, s); break;
+    case 128: launch_generic_combine<128>(cp, s); break;
+    case 256: launch_generic_combine<256>(cp, s); break;
+    case 512: launch_generic_combine<512>(cp, s); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
