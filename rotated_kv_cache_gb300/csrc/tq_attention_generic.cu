@@ -171,7 +171,10 @@ struct GGeo {
     static constexpr int MIN_BLOCKS = D >= 512 ? 1 : (D * NB / 4 <= 32 ? 6 : 4);
 };
 
-template <int D, int NB>
+// LUT3: 3-bit values looked up with byte permutes in registers instead of the
+// shared-memory table.  A separate instantiation: the same choice made at run
+// time inside one kernel cost more than it saved (the larger unrolled body).
+template <int D, int NB, bool LUT3 = false>
 __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
     attn_generic_kernel(const __grid_constant__ GenParams p)
 {
@@ -297,6 +300,21 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
     const int r0 = 16 * warp + g, r1 = r0 + 8;
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
     constexpr int TR = 16 * A::W;              // rows between a warp's tiles
+    // LUT3: the f16 centroid table as byte-permute operands (low bytes of c0..c7,
+    // then high bytes), so a lookup is a register operation
+    uint32_t tl0 = 0, tl1 = 0, th0 = 0, th1 = 0;
+    if constexpr (LUT3)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t cb = lut[i], sh = 8 * (i & 3);
+            if (i < 4) {
+                tl0 |= (cb & 0xFFu) << sh;
+                th0 |= (cb >> 8) << sh;
+            } else {
+                tl1 |= (cb & 0xFFu) << sh;
+                th1 |= (cb >> 8) << sh;
+            }
+        }
     constexpr int QF_NB = gN * A::KS * 4 * 8;  // bytes of q fragments per block of 8 columns
     const uint32_t qf_lane = smem_addr(qf) + (g * A::KS * 4 + c) * 8, lut_a = smem_addr(lut);
 
@@ -462,18 +480,46 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
                 for (int q = 0; q < 4; ++q)
                     sv[q] = vlive[t2][q] ? g_lds16(st + p.off_vs + ((vr[q] + TR * t2) * NG + G) * 2) : 0u;
                 const uint32_t sv01 = sv[0] | (sv[1] << 16), sv23 = sv[2] | (sv[3] << 16);
-                uint32_t hv[4][4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) value_quad(st + p.off_v + (vr[q] + TR * t2) * p.rbv, G, g, p.vb, lut_a, hv[q]);
+                // a[half]: rows g, g+8 of the m-tile = dims 32G + 4g + 2 half + {0, 1};
+                // registers 0, 1 pair tokens q0, q1, registers 2, 3 tokens q2, q3
                 uint32_t a[2][4];
+                if constexpr (LUT3) {
+                    // the four tokens' 12-bit fields (dims 32G + 4g .. +3), two tokens side
+                    // by side, spread to one code per nibble, looked up 4 at a time
+                    const int bit = (32 * G + 4 * g) * 3;
+                    uint32_t x[4];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    // rows g, g+8 of the m-tile: dims 32G + 4g + 2 half + {0, 1}
-                    const int r = 2 * half;
-                    a[half][0] = hv[0][r] | (hv[1][r] << 16);
-                    a[half][1] = hv[0][r + 1] | (hv[1][r + 1] << 16);
-                    a[half][2] = hv[2][r] | (hv[3][r] << 16);
-                    a[half][3] = hv[2][r + 1] | (hv[3][r + 1] << 16);
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t ad = st + p.off_v + (vr[q] + TR * t2) * p.rbv + 4 * (bit >> 5);
+                        x[q] = __funnelshift_r(g_lds32(ad), g_lds32(ad + 4), bit & 31);
+                    }
+#pragma unroll
+                    for (int pr2 = 0; pr2 < 2; ++pr2) {
+                        const uint32_t w = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
+                        const uint32_t y = (w & 0x003F003Fu) | ((w & 0x0FC00FC0u) * 4u);
+                        // each byte of y holds two codes; adding the upper one to itself
+                        // moves it to bits 4-6, and nothing carries out of a byte
+                        const uint32_t e = y + (y & 0x38383838u);
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t sel = __byte_perm(e, 0u, half ? 0x0031u : 0x0020u);
+                            const uint32_t lo = __byte_perm(tl0, tl1, sel), hi = __byte_perm(th0, th1, sel);
+                            a[half][2 * pr2] = __byte_perm(lo, hi, 0x6240u);      // dim r: (first, second)
+                            a[half][2 * pr2 + 1] = __byte_perm(lo, hi, 0x7351u);  // dim r + 1
+                        }
+                    }
+                } else {
+                    uint32_t hv[4][4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) value_quad(st + p.off_v + (vr[q] + TR * t2) * p.rbv, G, g, p.vb, lut_a, hv[q]);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int r = 2 * half;
+                        a[half][0] = hv[0][r] | (hv[1][r] << 16);
+                        a[half][1] = hv[0][r + 1] | (hv[1][r + 1] << 16);
+                        a[half][2] = hv[2][r] | (hv[3][r] << 16);
+                        a[half][3] = hv[2][r + 1] | (hv[3][r + 1] << 16);
+                    }
                 }
 #pragma unroll
                 for (int nb = 0; nb < NB; ++nb) {
@@ -665,6 +711,7 @@ void launch_generic_combine(const GenCombineParams &cp, cudaStream_t s)
 
 struct GenPlan {
     int nb, hb, splits, stages, stage_bytes, smem;
+    bool lut3;  // 3-bit values: the LUT3 instantiation
     int64_t tokens_per_split;
     int off_ks, off_kz, off_vs, off_v;
 };
@@ -679,11 +726,11 @@ inline int gen_nb(int d, int64_t cols)
     return nb < cap ? nb : cap;
 }
 
-template <int D, int NB>
+template <int D, int NB, bool LUT3>
 int gen_ctas_per_sm(int smem)
 {
     int n = 0;
-    auto kern = attn_generic_kernel<D, NB>;
+    auto kern = attn_generic_kernel<D, NB, LUT3>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, GGeo<D, NB>::THREADS, smem) != cudaSuccess) return 0;
     return n;
@@ -696,6 +743,7 @@ bool gen_plan_nb(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, Ge
     const int NG = D / 32, rbk = D * c.kb / 8, rbv = D * c.vb / 8;
     auto r16 = [](int x) { return (x + 15) / 16 * 16; };
     pl.nb = NB;
+    pl.lut3 = c.vb == 3;
     pl.off_ks = r16(gT * rbk);
     pl.off_kz = pl.off_ks + r16(gT * NG * 2);
     pl.off_vs = pl.off_kz + r16(gT * NG * 2);
@@ -704,7 +752,7 @@ bool gen_plan_nb(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, Ge
     pl.stages = 2;  // with 2-warp CTAs a deeper ring only costs resident CTAs
     const int ring = pl.stages * pl.stage_bytes > A::MERGE ? pl.stages * pl.stage_bytes : A::MERGE;
     pl.smem = 128 /*align slack*/ + ring + A::QF + A::QS + 512 /*lut*/ + gMaxStages * 12 /*barriers, counters*/;
-    const int per_sm = gen_ctas_per_sm<D, NB>(pl.smem);
+    const int per_sm = pl.lut3 ? gen_ctas_per_sm<D, NB, true>(pl.smem) : gen_ctas_per_sm<D, NB, false>(pl.smem);
     if (per_sm < 1) return false;
     const int64_t cols = (int64_t)(q_heads / c.H) * m;
     pl.hb = (int)((cols + A::CB - 1) / A::CB);
@@ -797,9 +845,28 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
     const dim3 grid(pl.splits, c.H * pl.hb, c.B);
     switch (pl.nb) {
-    case 1: attn_generic_kernel<D, 1><<<grid, GGeo<D, 1>::THREADS, pl.smem, s>>>(p); break;
-    case 2: if constexpr (D <= 256) attn_generic_kernel<D, 2><<<grid, GGeo<D, 2>::THREADS, pl.smem, s>>>(p); break;
-    case 4: if constexpr (D <= 128) attn_generic_kernel<D, 4><<<grid, GGeo<D, 4>::THREADS, pl.smem, s>>>(p); break;
+    case 1:
+        if (pl.lut3)
+            attn_generic_kernel<D, 1, true><<<grid, GGeo<D, 1>::THREADS, pl.smem, s>>>(p);
+        else
+            attn_generic_kernel<D, 1, false><<<grid, GGeo<D, 1>::THREADS, pl.smem, s>>>(p);
+        break;
+    case 2:
+        if constexpr (D <= 256) {
+            if (pl.lut3)
+                attn_generic_kernel<D, 2, true><<<grid, GGeo<D, 2>::THREADS, pl.smem, s>>>(p);
+            else
+                attn_generic_kernel<D, 2, false><<<grid, GGeo<D, 2>::THREADS, pl.smem, s>>>(p);
+        }
+        break;
+    case 4:
+        if constexpr (D <= 128) {
+            if (pl.lut3)
+                attn_generic_kernel<D, 4, true><<<grid, GGeo<D, 4>::THREADS, pl.smem, s>>>(p);
+            else
+                attn_generic_kernel<D, 4, false><<<grid, GGeo<D, 4>::THREADS, pl.smem, s>>>(p);
+        }
+        break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
