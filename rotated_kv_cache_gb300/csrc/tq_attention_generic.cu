@@ -102,6 +102,13 @@ __device__ __forceinline__ uint32_t g_lds32(uint32_t a)
     return v;
 }
 
+__device__ __forceinline__ uint32_t g_lds8(uint32_t a)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t g_lds16(uint32_t a)
 {
     uint16_t v;
@@ -171,10 +178,11 @@ struct GGeo {
     static constexpr int MIN_BLOCKS = D >= 512 ? 1 : (D * NB / 4 <= 32 ? 6 : 4);
 };
 
-// LUT3: 3-bit values looked up with byte permutes in registers instead of the
-// shared-memory table.  A separate instantiation: the same choice made at run
-// time inside one kernel cost more than it saved (the larger unrolled body).
-template <int D, int NB, bool LUT3 = false>
+// VLUT: how value codes become f16 centroids.  0: a shared-memory table; 3 or
+// 2: 3- or 2-bit values looked up with byte permutes in registers.  Separate
+// instantiations: the same choice made at run time inside one kernel cost more
+// than it saved (the larger unrolled body).
+template <int D, int NB, int VLUT = 0>
 __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
     attn_generic_kernel(const __grid_constant__ GenParams p)
 {
@@ -300,10 +308,14 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
     const int r0 = 16 * warp + g, r1 = r0 + 8;
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
     constexpr int TR = 16 * A::W;              // rows between a warp's tiles
-    // LUT3: the f16 centroid table as byte-permute operands (low bytes of c0..c7,
-    // then high bytes), so a lookup is a register operation
+    // VLUT 3: the f16 centroid table as byte-permute operands (low bytes of
+    // c0..c7, then high bytes); VLUT 2: the four f16 centroids, two per register
     uint32_t tl0 = 0, tl1 = 0, th0 = 0, th1 = 0;
-    if constexpr (LUT3)
+    if constexpr (VLUT == 2) {
+        tl0 = (uint32_t)lut[0] | ((uint32_t)lut[1] << 16);
+        tl1 = (uint32_t)lut[2] | ((uint32_t)lut[3] << 16);
+    }
+    if constexpr (VLUT == 3)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t cb = lut[i], sh = 8 * (i & 3);
@@ -483,7 +495,23 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
                 // a[half]: rows g, g+8 of the m-tile = dims 32G + 4g + 2 half + {0, 1};
                 // registers 0, 1 pair tokens q0, q1, registers 2, 3 tokens q2, q3
                 uint32_t a[2][4];
-                if constexpr (LUT3) {
+                if constexpr (VLUT == 2) {
+                    // the four tokens' 8-bit fields (dims 32G + 4g .. +3) are bytes; per
+                    // dim r and token pair, selector nibbles (2a, 2a+1, 2b, 2b+1) pick the
+                    // f16 centroids c[a], c[b] of the two tokens' codes in one permute
+                    uint32_t x[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) x[q] = g_lds8(st + p.off_v + (vr[q] + TR * t2) * p.rbv + 8 * G + g);
+#pragma unroll
+                    for (int pr2 = 0; pr2 < 2; ++pr2) {
+                        const uint32_t u = x[2 * pr2] | (x[2 * pr2 + 1] << 8);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const uint32_t ab = (u >> (2 * r)) & 0x0303u;  // code of the first token, of the second
+                            a[r >> 1][2 * pr2 + (r & 1)] = __byte_perm(tl0, tl1, ab * 0x22u + 0x1010u);
+                        }
+                    }
+                } else if constexpr (VLUT == 3) {
                     // the four tokens' 12-bit fields (dims 32G + 4g .. +3), two tokens side
                     // by side, spread to one code per nibble, looked up 4 at a time
                     const int bit = (32 * G + 4 * g) * 3;
@@ -711,7 +739,7 @@ void launch_generic_combine(const GenCombineParams &cp, cudaStream_t s)
 
 struct GenPlan {
     int nb, hb, splits, stages, stage_bytes, smem;
-    bool lut3;  // 3-bit values: the LUT3 instantiation
+    int vlut;  // VLUT of the instantiation: 3 or 2 for 3- or 2-bit values, else 0
     int64_t tokens_per_split;
     int off_ks, off_kz, off_vs, off_v;
 };
@@ -726,11 +754,11 @@ inline int gen_nb(int d, int64_t cols)
     return nb < cap ? nb : cap;
 }
 
-template <int D, int NB, bool LUT3>
+template <int D, int NB, int VLUT>
 int gen_ctas_per_sm(int smem)
 {
     int n = 0;
-    auto kern = attn_generic_kernel<D, NB, LUT3>;
+    auto kern = attn_generic_kernel<D, NB, VLUT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, GGeo<D, NB>::THREADS, smem) != cudaSuccess) return 0;
     return n;
@@ -743,7 +771,7 @@ bool gen_plan_nb(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, Ge
     const int NG = D / 32, rbk = D * c.kb / 8, rbv = D * c.vb / 8;
     auto r16 = [](int x) { return (x + 15) / 16 * 16; };
     pl.nb = NB;
-    pl.lut3 = c.vb == 3;
+    pl.vlut = c.vb == 3 ? 3 : (c.vb == 2 ? 2 : 0);
     pl.off_ks = r16(gT * rbk);
     pl.off_kz = pl.off_ks + r16(gT * NG * 2);
     pl.off_vs = pl.off_kz + r16(gT * NG * 2);
@@ -752,7 +780,9 @@ bool gen_plan_nb(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, Ge
     pl.stages = 2;  // with 2-warp CTAs a deeper ring only costs resident CTAs
     const int ring = pl.stages * pl.stage_bytes > A::MERGE ? pl.stages * pl.stage_bytes : A::MERGE;
     pl.smem = 128 /*align slack*/ + ring + A::QF + A::QS + 512 /*lut*/ + gMaxStages * 12 /*barriers, counters*/;
-    const int per_sm = pl.lut3 ? gen_ctas_per_sm<D, NB, true>(pl.smem) : gen_ctas_per_sm<D, NB, false>(pl.smem);
+    const int per_sm = pl.vlut == 3   ? gen_ctas_per_sm<D, NB, 3>(pl.smem)
+                       : pl.vlut == 2 ? gen_ctas_per_sm<D, NB, 2>(pl.smem)
+                                      : gen_ctas_per_sm<D, NB, 0>(pl.smem);
     if (per_sm < 1) return false;
     const int64_t cols = (int64_t)(q_heads / c.H) * m;
     pl.hb = (int)((cols + A::CB - 1) / A::CB);
@@ -786,6 +816,17 @@ bool gen_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, GenPl
     case 4: if constexpr (D <= 128) return gen_plan_nb<D, 4>(c, q_heads, m, seq_len, pl); break;
     }
     return false;
+}
+
+template <int D, int NB>
+void gen_launch(const GenPlan &pl, dim3 grid, const GenParams &p, cudaStream_t s)
+{
+    if (pl.vlut == 3)
+        attn_generic_kernel<D, NB, 3><<<grid, GGeo<D, NB>::THREADS, pl.smem, s>>>(p);
+    else if (pl.vlut == 2)
+        attn_generic_kernel<D, NB, 2><<<grid, GGeo<D, NB>::THREADS, pl.smem, s>>>(p);
+    else
+        attn_generic_kernel<D, NB, 0><<<grid, GGeo<D, NB>::THREADS, pl.smem, s>>>(p);
 }
 
 template <int D>
@@ -845,28 +886,9 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
     const dim3 grid(pl.splits, c.H * pl.hb, c.B);
     switch (pl.nb) {
-    case 1:
-        if (pl.lut3)
-            attn_generic_kernel<D, 1, true><<<grid, GGeo<D, 1>::THREADS, pl.smem, s>>>(p);
-        else
-            attn_generic_kernel<D, 1, false><<<grid, GGeo<D, 1>::THREADS, pl.smem, s>>>(p);
-        break;
-    case 2:
-        if constexpr (D <= 256) {
-            if (pl.lut3)
-                attn_generic_kernel<D, 2, true><<<grid, GGeo<D, 2>::THREADS, pl.smem, s>>>(p);
-            else
-                attn_generic_kernel<D, 2, false><<<grid, GGeo<D, 2>::THREADS, pl.smem, s>>>(p);
-        }
-        break;
-    case 4:
-        if constexpr (D <= 128) {
-            if (pl.lut3)
-                attn_generic_kernel<D, 4, true><<<grid, GGeo<D, 4>::THREADS, pl.smem, s>>>(p);
-            else
-                attn_generic_kernel<D, 4, false><<<grid, GGeo<D, 4>::THREADS, pl.smem, s>>>(p);
-        }
-        break;
+    case 1: gen_launch<D, 1>(pl, grid, p, s); break;
+    case 2: if constexpr (D <= 256) gen_launch<D, 2>(pl, grid, p, s); break;
+    case 4: if constexpr (D <= 128) gen_launch<D, 4>(pl, grid, p, s); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
