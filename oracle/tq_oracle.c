@@ -104,9 +104,9 @@ uint16_t tqo_f32_to_bf16(float f)
 /* Sign vector: SplitMix64 (Steele, Lea & Flood, OOPSLA 2014)                */
 /* ------------------------------------------------------------------------ */
 /* The pages draw the +-1 value signs from a seeded generator and hardcode one
- * vector per head_dim ("signs in {+-1}^d ... hardcoded constants per
- * head_dim").  This build states its own generator: output i of SplitMix64
- * started at `seed`; sign i is -1 when the top bit of that output is set. */
+ * vector per head_dim as constants.  The codec here fixes its own generator:
+ * output i of SplitMix64 started at `seed`; sign i is -1 when the top bit of
+ * that output is set. */
 uint64_t tqo_splitmix64(uint64_t seed, uint64_t i)
 {
     uint64_t z = seed + (i + 1u) * 0x9E3779B97F4A7C15ull;
@@ -325,8 +325,8 @@ static int32_t clip_round(float r, float lo, float hi)
  *             zero = round((max + min)/(2 scale)); idx = clip(round(x/scale - zero), -127, 127)
  *   unsigned: max_val = 2^bits - 1; scale = (max - min)/max_val;
  *             zero = round(min/scale); idx = clip(round(x/scale - zero), 0, max_val)
- * all in fp32 ("our port upcasts the affine arithmetic to fp32 and casts only
- * scale/zero to fp16 at the end"); round = round-half-to-even (rintf).  No
+ * all in fp32: the pages compute the affine in fp32 and round only the stored
+ * scale and zero to fp16; round = round-half-to-even (rintf).  No
  * epsilon: a constant group gives scale 0 and an infinite (or NaN) zero, the
  * reference defect the pages reproduce on purpose. */
 void tqo_key_group(const float *x, int bits, int32_t *idx, uint16_t *scale_h, uint16_t *zero_h)
