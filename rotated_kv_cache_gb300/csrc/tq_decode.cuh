@@ -140,6 +140,33 @@ __device__ __forceinline__ void load_value_lane(const ValueDecodeParams &p, int6
     sc = *reinterpret_cast<const uint32_t *>(p.scale + crow * (D / 32) + 2 * part);
 }
 
+// head_dim 128 (two lanes per row): the transform of fwht_pairs with half its
+// cross-lane traffic.  Part-1 lanes hold every pair swapped, (element j + 32,
+// element j) of their part, so both lanes of a row send their .y in one shuffle.
+// Afterwards lane part p holds (element 32 p + j, element 64 + 32 p + j), the
+// second negated when p = 1.  Each output is the same operation on the same
+// operands as in fwht_pairs, so the results are identical.
+template <int ROWS>
+__device__ __forceinline__ void fwht_pairs_d128(float2 (&P)[32], int part)
+{
+    bfly_stage<1>(P);
+    bfly_stage<2>(P);
+    bfly_stage<4>(P);
+    bfly_stage<8>(P);
+    bfly_stage<16>(P);
+    const float sg = part ? -1.0f : 1.0f;  // stride 32: (x + y, x - y), or (y - x, x + y) on swapped pairs
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float x = P[j].x, y = P[j].y;
+        P[j] = make_float2(__fmaf_rn(sg, x, y), __fmaf_rn(-sg, y, x));
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {  // stride 64 across the row's two lanes
+        const float o = __shfl_xor_sync(0xffffffffu, P[j].y, ROWS), a = P[j].x;
+        P[j] = make_float2(__fadd_rn(a, o), __fsub_rn(a, o));
+    }
+}
+
 template <int D, int VB, bool F32>
 __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid_constant__ ValueDecodeParams p)
 {
@@ -148,9 +175,12 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
     __shared__ __align__(16) float2 smul[G::LPR][34];  // (+-1/sqrt d) of elements (j, j+32) of each part, padded
     for (int i = threadIdx.x; i < (1 << VB); i += blockDim.x) scen[i] = p.cen[i];
     for (int i = threadIdx.x; i < G::LPR * 32; i += blockDim.x) {
-        const int part = i >> 5, j = i & 31, e = 64 * part + j;
-        smul[part][j] = make_float2(sign_negative(e) ? -p.inv_sqrt_d : p.inv_sqrt_d,
-                                    sign_negative(e + 32) ? -p.inv_sqrt_d : p.inv_sqrt_d);
+        const int part = i >> 5, j = i & 31;
+        // elements of P[j] after the transform, and the sign the d128 form leaves on the second
+        const int e0 = D == 128 ? 32 * part + j : 64 * part + j, e1 = D == 128 ? 64 + 32 * part + j : e0 + 32;
+        const float n1 = D == 128 && part ? -1.0f : 1.0f;
+        smul[part][j] = make_float2(sign_negative(e0) ? -p.inv_sqrt_d : p.inv_sqrt_d,
+                                    n1 * (sign_negative(e1) ? -p.inv_sqrt_d : p.inv_sqrt_d));
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,6 +206,17 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
         uint32_t w[2 * VB], sc = nsc;
 #pragma unroll
         for (int k = 0; k < 2 * VB; ++k) w[k] = nw[k];
+        if constexpr (D == 128) {
+            if (part) {  // swapped pairs: the second group's codes and scale first
+#pragma unroll
+                for (int k = 0; k < VB; ++k) {
+                    const uint32_t u = w[k];
+                    w[k] = w[k + VB];
+                    w[k + VB] = u;
+                }
+                sc = __byte_perm(sc, 0u, 0x1032u);
+            }
+        }
         int64_t t, crow;
         uint32_t bh;
         locate(item, t, crow, bh);
@@ -200,7 +241,10 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
 #pragma unroll
             for (int j = 0; j < 32; ++j) P[j] = make_float2(0.0f, 0.0f);
         }
-        fwht_pairs<G::LPR, G::ROWS>(P, part);
+        if constexpr (D == 128)
+            fwht_pairs_d128<G::ROWS>(P, part);
+        else
+            fwht_pairs<G::LPR, G::ROWS>(P, part);
         if (valid) {
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -208,7 +252,9 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
                 P[j] = __fmul2_rn(P[j], make_float2(m.x, m.y));
                 P[j + 1] = __fmul2_rn(P[j + 1], make_float2(m.z, m.w));
             }
-            const int64_t o = ((int64_t)bh * p.n + t) * D + 64 * part;  // whole 32-byte sectors per store
+            // P[j].x, P[j].y: elements X0 + j, Y0 + j of the row (whole 32-byte sectors per store)
+            constexpr int XS = D == 128 ? 32 : 64, Y0 = D == 128 ? 64 : 32;
+            const int64_t o = ((int64_t)bh * p.n + t) * D + XS * part;
             if constexpr (F32) {
                 float *dst = static_cast<float *>(p.out) + o;
 #pragma unroll
@@ -217,7 +263,7 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
                     st_global_v8(dst + 8 * i, __float_as_uint(q[0].x), __float_as_uint(q[1].x), __float_as_uint(q[2].x),
                                  __float_as_uint(q[3].x), __float_as_uint(q[4].x), __float_as_uint(q[5].x),
                                  __float_as_uint(q[6].x), __float_as_uint(q[7].x));
-                    st_global_v8(dst + 32 + 8 * i, __float_as_uint(q[0].y), __float_as_uint(q[1].y), __float_as_uint(q[2].y),
+                    st_global_v8(dst + Y0 + 8 * i, __float_as_uint(q[0].y), __float_as_uint(q[1].y), __float_as_uint(q[2].y),
                                  __float_as_uint(q[3].y), __float_as_uint(q[4].y), __float_as_uint(q[5].y),
                                  __float_as_uint(q[6].y), __float_as_uint(q[7].y));
                 }
@@ -229,7 +275,7 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
                     st_global_v8(dst + 16 * i, pack_bf16x2(q[0].x, q[1].x), pack_bf16x2(q[2].x, q[3].x), pack_bf16x2(q[4].x, q[5].x),
                                  pack_bf16x2(q[6].x, q[7].x), pack_bf16x2(q[8].x, q[9].x), pack_bf16x2(q[10].x, q[11].x),
                                  pack_bf16x2(q[12].x, q[13].x), pack_bf16x2(q[14].x, q[15].x));
-                    st_global_v8(dst + 32 + 16 * i, pack_bf16x2(q[0].y, q[1].y), pack_bf16x2(q[2].y, q[3].y),
+                    st_global_v8(dst + Y0 + 16 * i, pack_bf16x2(q[0].y, q[1].y), pack_bf16x2(q[2].y, q[3].y),
                                  pack_bf16x2(q[4].y, q[5].y), pack_bf16x2(q[6].y, q[7].y), pack_bf16x2(q[8].y, q[9].y),
                                  pack_bf16x2(q[10].y, q[11].y), pack_bf16x2(q[12].y, q[13].y), pack_bf16x2(q[14].y, q[15].y));
                 }
