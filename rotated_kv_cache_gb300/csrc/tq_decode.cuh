@@ -140,33 +140,6 @@ __device__ __forceinline__ void load_value_lane(const ValueDecodeParams &p, int6
     sc = *reinterpret_cast<const uint32_t *>(p.scale + crow * (D / 32) + 2 * part);
 }
 
-// head_dim 128 (two lanes per row): the transform of fwht_pairs with half its
-// cross-lane traffic.  Part-1 lanes hold every pair swapped, (element j + 32,
-// element j) of their part, so both lanes of a row send their .y in one shuffle.
-// Afterwards lane part p holds (element 32 p + j, element 64 + 32 p + j), the
-// second negated when p = 1.  Each output is the same operation on the same
-// operands as in fwht_pairs, so the results are identical.
-template <int ROWS>
-__device__ __forceinline__ void fwht_pairs_d128(float2 (&P)[32], int part)
-{
-    bfly_stage<1>(P);
-    bfly_stage<2>(P);
-    bfly_stage<4>(P);
-    bfly_stage<8>(P);
-    bfly_stage<16>(P);
-    const float sg = part ? -1.0f : 1.0f;  // stride 32: (x + y, x - y), or (y - x, x + y) on swapped pairs
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float x = P[j].x, y = P[j].y;
-        P[j] = make_float2(__fmaf_rn(sg, x, y), __fmaf_rn(-sg, y, x));
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {  // stride 64 across the row's two lanes
-        const float o = __shfl_xor_sync(0xffffffffu, P[j].y, ROWS), a = P[j].x;
-        P[j] = make_float2(__fadd_rn(a, o), __fsub_rn(a, o));
-    }
-}
-
 template <int D, int VB, bool F32>
 __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid_constant__ ValueDecodeParams p)
 {

@@ -375,7 +375,11 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
                                                   uint32_t mtab, uint32_t stage, int64_t crow, int r, int part, bool valid)
 {
     using G = EGeo<D, false>;
-    float2 P[32];  // P[j] = (element j, element j + 32) of this lane's 64
+    // P[j] = (element j, element j + 32) of this lane's 64; at head_dim 128 part-1
+    // lanes hold them swapped (their two 64-byte halves are read in the other
+    // order), for the transform's half-traffic stride-64 stage
+    float2 P[32];
+    if constexpr (D == 128) xr ^= 4u * (uint32_t)part;
     if (valid) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -395,10 +399,17 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
 #pragma unroll
         for (int j = 0; j < 32; ++j) P[j] = make_float2(0.0f, 0.0f);
     }
-    fwht_pairs<G::LPR, G::ROWS>(P, part);
+    // afterwards P[j] holds elements j and j + 32 of the lane's 64 (groups 2 part and
+    // 2 part + 1), or at head_dim 128 elements 32 part + j and 64 + 32 part + j
+    // (groups part and 2 + part), the second negated on part-1 lanes
+    if constexpr (D == 128)
+        fwht_pairs_d128<G::ROWS>(P, part);
+    else
+        fwht_pairs<G::LPR, G::ROWS>(P, part);
     if (!valid) return;
-    // y = z / sqrt(d); both groups' sums of squares in element order
-    const float2 c2 = make_float2(p.inv_sqrt_d, p.inv_sqrt_d);
+    // y = z / sqrt(d) (the negation undone with it); both groups' sums of squares in element order
+    const float c2y = D == 128 && part ? -p.inv_sqrt_d : p.inv_sqrt_d;
+    const float2 c2 = make_float2(p.inv_sqrt_d, c2y);
     float2 ss = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -469,6 +480,19 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
             put_code<BITS>(w1, j, value_index<BITS>(p, sbnd, q1));
         }
     }
+    if constexpr (D == 128) {
+        // groups part and 2 + part of the row: 4 BITS bytes of codes and one fp16 scale each
+        constexpr int RB = D * BITS / 8, GB = 4 * BITS;
+        const uint32_t ax = stage + r * RB + part * GB, ay = ax + 2 * GB;
+#pragma unroll
+        for (int k = 0; k < BITS; ++k) {
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(ax + 4 * k), "r"(w0[k]) : "memory");
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(ay + 4 * k), "r"(w1[k]) : "memory");
+        }
+        p.scale[crow * (D / 32) + part] = f32_to_f16_bits(sig0);
+        p.scale[crow * (D / 32) + 2 + part] = f32_to_f16_bits(sig1);
+        return;
+    }
     uint32_t w[2 * BITS];
 #pragma unroll
     for (int k = 0; k < BITS; ++k) {
@@ -516,10 +540,11 @@ __device__ __forceinline__ void encode_body(const EncodeParams &p, const CUtenso
     if constexpr (!KEY) {
         // sign masks: entry (part, k) = elements 64 part + {2k, 2k+1, 2k+32, 2k+33}
         for (int i = threadIdx.x; i < G::LPR * 16; i += blockDim.x) {
-            const int part = i >> 4, k = i & 15, e = 64 * part + 2 * k;
+            const int part = i >> 4, k = i & 15;
+            // at head_dim 128 part-1 lanes hold swapped pairs (element j + 32, element j)
+            const int e = 64 * part + 2 * k + (D == 128 && part ? 32 : 0), f = D == 128 && part ? e - 32 : e + 32;
             const uint4 m = make_uint4(sign_negative(e) ? 0x80000000u : 0u, sign_negative(e + 1) ? 0x80000000u : 0u,
-                                       sign_negative(e + 32) ? 0x80000000u : 0u,
-                                       sign_negative(e + 33) ? 0x80000000u : 0u);
+                                       sign_negative(f) ? 0x80000000u : 0u, sign_negative(f + 1) ? 0x80000000u : 0u);
             *reinterpret_cast<uint4 *>(mtab + part * 272 + 16 * k) = m;
         }
     }
