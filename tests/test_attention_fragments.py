@@ -1,0 +1,115 @@
+"""Host model of the decode attention kernel's QK^T fragments, checked on the CPU.
+
+The head_dim-128 decode kernel reads key codes from a shared-memory tile that a
+TMA copy wrote with a 128-byte (8-bit keys) or 64-byte (4-bit keys) swizzle:
+the 16-byte chunk index of a row is xor-ed with shared-memory address bits 7..9
+(or 7..8).  Each lane (g, c) of a warp reads its rows g and g + 8 at
+precomputed swizzled offsets, turns two codes at a time into an f16 pair
+(1024 + offset code) with one 3-input logic op and a right shift, and feeds
+them to mma.sync m16n8k16 against q fragments permuted the same way.
+
+This test builds the swizzled tile byte by byte.  It replays every lane's
+offsets, loads, conversions and q permutation as the kernel states them, and
+emulates the MMA from its documented fragment layout:
+- A row-major: lane (g, c) holds A[g][2c..2c+1], A[g+8][2c..2c+1],
+  A[g][2c+8..2c+9] and A[g+8][2c+8..2c+9];
+- B column-major: lane (n, c) holds B[2c..2c+1][n] and B[2c+8..2c+9][n].
+
+Each score must equal the plain dot product of the offset codes with q over
+the key group.  CPU only.
+"""
+import numpy as np
+import pytest
+
+from test_key_cuts import f16_value
+
+
+def swizzled_tile(codes_bytes, krow, kb):
+    """Shared-memory image of 16 rows of `krow` bytes under the TMA swizzle of the key map."""
+    img = np.zeros(16 * krow, dtype=np.uint8)
+    for r in range(16):
+        for j in range(krow // 16):
+            base = r * krow + 16 * j  # the unswizzled address of chunk j
+            f = (base >> 7) & (7 if kb == 8 else 3)
+            img[r * krow + 16 * (j ^ f):r * krow + 16 * (j ^ f) + 16] = codes_bytes[r, 16 * j:16 * j + 16]
+    return img
+
+
+def kcvt(w, kb):
+    k_const, k_flip = (0xFF00FF00, 0x64806480) if kb == 8 else (0xFFF0FFF0, 0x64006400)
+    return ((k_const & k_flip) | (~k_const & (w ^ k_flip))) & 0xFFFFFFFF
+
+
+def pair(h):
+    return f16_value(h & 0xFFFF), f16_value(h >> 16)
+
+
+def u32(img, a):
+    return int.from_bytes(img[a:a + 4].tobytes(), "little")
+
+
+def lane_a_fragments(img, g, c, G, kb):
+    """[mma][a0, a1, a2, a3] as pairs of values, rows g (a0, a2) and g + 8 (a1, a3)."""
+    krow = 128 * kb // 8
+    r0 = g  # warp 0, first tile
+    if kb == 8:
+        koff = r0 * krow + (((2 * G + (c >> 1)) ^ g) << 4) + ((c & 1) << 3)
+        k0 = (u32(img, koff), u32(img, koff + 4))
+        k1 = (u32(img, koff + 8 * krow), u32(img, koff + 8 * krow + 4))
+        out = []
+        for half in range(2):
+            w0, w1 = k0[half], k1[half]
+            out.append([pair(kcvt(w0, 8)), pair(kcvt(w1, 8)), pair(kcvt(w0 >> 8, 8)), pair(kcvt(w1 >> 8, 8))])
+        return out
+    koff = r0 * krow + ((G ^ ((g >> 1) & 3)) << 4) + 4 * c
+    w0, w1 = u32(img, koff), u32(img, koff + 8 * krow)
+    return [[pair(kcvt(w0, 4)), pair(kcvt(w1, 4)), pair(kcvt(w0 >> 4, 4)), pair(kcvt(w1 >> 4, 4))],
+            [pair(kcvt(w0 >> 8, 4)), pair(kcvt(w1 >> 8, 4)), pair(kcvt(w0 >> 12, 4)), pair(kcvt(w1 >> 12, 4))]]
+
+
+def lane_b_fragments(q, n, c, G, kb):
+    """[mma][b0, b1] as pairs: q of head n at the dims the A fragments hold."""
+    f = q[n, 32 * G + 8 * c:32 * G + 8 * c + 8]
+    if kb == 8:  # a word's bytes pair as (0, 2), (1, 3)
+        return [[(f[0], f[2]), (f[1], f[3])], [(f[4], f[6]), (f[5], f[7])]]
+    return [[(f[0], f[4]), (f[1], f[5])], [(f[2], f[6]), (f[3], f[7])]]  # nibbles k and k + 4
+
+
+@pytest.mark.parametrize("kb", [8, 4])
+def test_scores_equal_dot_products(kb):
+    rng = np.random.default_rng(kb)
+    krow = 128 * kb // 8
+    if kb == 8:
+        codes = rng.integers(-128, 128, (16, 128))
+        raw = codes.astype(np.int8).view(np.uint8).reshape(16, 128)
+        offset_codes = 1152.0 + codes
+    else:
+        codes = rng.integers(0, 16, (16, 128))
+        raw = np.zeros((16, krow), dtype=np.uint8)
+        for r in range(16):
+            for dd in range(0, 128, 2):
+                raw[r, dd // 2] = codes[r, dd] | (codes[r, dd + 1] << 4)
+        offset_codes = 1024.0 + codes
+    img = swizzled_tile(raw, krow, kb)
+    q = rng.integers(-8, 9, (8, 128)).astype(np.float64)
+    for G in range(4):
+        D = np.zeros((16, 8))
+        for m in range(2):  # the two MMAs of the group
+            for g in range(8):
+                for n in range(8):
+                    for c in range(4):
+                        a = lane_a_fragments(img, g, c, G, kb)[m]
+                        b = lane_b_fragments(q, n, c, G, kb)[m]
+                        # A[row][2c..2c+1] . B[2c..2c+1][n] + A[row][2c+8..+9] . B[2c+8..+9][n]
+                        D[g, n] += a[0][0] * b[0][0] + a[0][1] * b[0][1] + a[2][0] * b[1][0] + a[2][1] * b[1][1]
+                        D[g + 8, n] += a[1][0] * b[0][0] + a[1][1] * b[0][1] + a[3][0] * b[1][0] + a[3][1] * b[1][1]
+        want = offset_codes[:, 32 * G:32 * G + 32] @ q[:, 32 * G:32 * G + 32].T
+        assert np.array_equal(D, want)
+
+
+def test_swizzle_is_a_permutation_of_each_row():
+    raw = np.arange(16 * 128, dtype=np.int64).reshape(16, 128).astype(np.uint8)
+    for kb, krow in ((8, 128), (4, 64)):
+        img = swizzled_tile(raw[:, :krow], krow, kb)
+        for r in range(16):
+            assert sorted(img[r * krow:(r + 1) * krow]) == sorted(raw[r, :krow])
