@@ -1,4 +1,4 @@
-"""Host model of the decode attention kernel's QK^T fragments, checked on the CPU.
+"""Host model of the decode attention kernel's MMA fragments, checked on the CPU.
 
 The head_dim-128 decode kernel reads key codes from a shared-memory tile that a
 TMA copy wrote with a 128-byte (8-bit keys) or 64-byte (4-bit keys) swizzle:
@@ -16,7 +16,10 @@ emulates the MMA from its documented fragment layout:
 - B column-major: lane (n, c) holds B[2c..2c+1][n] and B[2c+8..2c+9][n].
 
 Each score must equal the plain dot product of the offset codes with q over
-the key group.  CPU only.
+the key group.  The P V side is checked the same way: which dims and tokens
+each lane's value fragments hold, P^T with the rms folded in, and the merge's
+map from accumulator rows back to dims must give the plain weighted sum of the
+value rows.  CPU only.
 """
 import numpy as np
 import pytest
@@ -113,3 +116,48 @@ def test_swizzle_is_a_permutation_of_each_row():
         img = swizzled_tile(raw[:, :krow], krow, kb)
         for r in range(16):
             assert sorted(img[r * krow:(r + 1) * krow]) == sorted(raw[r, :krow])
+
+
+def test_pv_fragments_and_merge_give_the_weighted_sum():
+    """O^T += V^T (P * rms)^T per 32-dim group, then the merge's dim map, equals sum_t p v_hat.
+
+    Per the kernel: lane (g, c) holds dims 32G + 4g + {0..3} of tokens 2c, 2c + 1, 2c + 8 and
+    2c + 9.  m-tile 2G + half takes rows g -> dim 32G + 4g + 2 half and g + 8 -> that dim + 1.
+    P^T comes from a transpose of the lane's (token g, heads 2c, 2c + 1) pair, so the lane
+    gets (tokens 2c, 2c + 1; head g); the rms of those tokens' group multiplies it.
+    """
+    rng = np.random.default_rng(11)
+    V = rng.integers(-7, 8, (16, 128)).astype(np.float64)   # centroid values, per token and dim
+    rms = rng.integers(1, 5, (16, 4)).astype(np.float64)    # per token and 32-dim group
+    P = rng.integers(0, 6, (16, 8)).astype(np.float64)      # weights, per token and head
+    o = np.zeros((8, 4, 8, 4))  # [g][c][m-tile][c0..c3] accumulators of each lane
+    for G in range(4):
+        for half in range(2):
+            mt = 2 * G + half
+            for g in range(8):
+                for c in range(4):
+                    acc = np.zeros(4)
+                    for cc in range(4):  # the MMA sums over the k (token) slots of all lanes
+                        toks = (2 * cc, 2 * cc + 1, 2 * cc + 8, 2 * cc + 9)
+                        d0 = 32 * G + 4 * g + 2 * half
+                        # A of lane (g, cc): rows g (dim d0) and g + 8 (dim d0 + 1)
+                        a_row_g = [V[t, d0] for t in toks]
+                        a_row_g8 = [V[t, d0 + 1] for t in toks]
+                        for j in range(2):  # B of lane (n = 2c + j, cc): (P * rms)[toks][n]
+                            n = 2 * c + j
+                            bcol = [P[t, n] * rms[t, G] for t in toks]
+                            acc[j] += sum(x * y for x, y in zip(a_row_g, bcol))
+                            acc[2 + j] += sum(x * y for x, y in zip(a_row_g8, bcol))
+                    o[g, c, mt] += acc
+    merged = np.zeros((8, 128))  # the merge: [head][dim]
+    for g in range(8):
+        for c in range(4):
+            for mt in range(8):
+                G, half = mt >> 1, mt & 1
+                d0 = 32 * G + 4 * g + 2 * half
+                for j in range(2):
+                    merged[2 * c + j, d0] = o[g, c, mt, j]
+                    merged[2 * c + j, d0 + 1] = o[g, c, mt, 2 + j]
+    group_rms = np.repeat(rms, 32, axis=1)  # [token][dim]
+    want = P.T @ (V * group_rms)
+    assert np.array_equal(merged, want)
