@@ -26,6 +26,12 @@
  *    TQ_ERR_CUDA.  Calls on one stream are ordered; calls that touch the same
  *    cache rows from different streams must be ordered by the caller.
  *  - Calls are capturable in a CUDA graph (no allocation, no sync).
+ *  - Calls run on the calling thread's current CUDA device, which must hold
+ *    every pointer.  The intended use is one process per GPU.  Kernel
+ *    shared-memory opt-ins and occupancy figures are set up once per process,
+ *    on the first device a kernel runs on; a process that later calls on
+ *    another device gets TQ_ERR_CUDA if that device needs its own set-up.
+ *    The device error word and the SM count are kept per device.
  */
 #ifndef TQ_H
 #define TQ_H
