@@ -388,6 +388,87 @@ def test_attention_dominant_logit_selects_its_value():
     assert np.allclose(out[0, 0], vo[0, 0, 7], atol=1e-6)
 
 
+def _integer_key_rows(base_rows, d):
+    """Key rows of integers whose every 32-group holds both 127 and -127, so
+    the 8-bit affine has scale (127 - (-127)) / 254 = 1 and zero rint(0) = 0:
+    the codes are the integers themselves and k_hat = x exactly."""
+    k = np.array(base_rows, dtype=np.float64)
+    for g in range(d // 32):
+        k[:, 32 * g] = 127.0
+        k[:, 32 * g + 1] = -127.0
+    return k
+
+
+def _closed_form_cache(k_rows, d=64, seed=0):
+    """One sequence, one kv-head: integer key rows (exact k_hat) and random
+    value rows; returns the planes, the exact keys and the decoded v_hat."""
+    T = k_rows.shape[0]
+    rng = np.random.default_rng(seed)
+    v = _bf16(rng.standard_normal((1, 1, T, d)))
+    p = oracle.Planes(1, 1, d, 8, 3, 16)
+    oracle.encode(p, _bf16(k_rows.reshape(1, 1, T, d)), v)
+    ko, vo = oracle.decode(p, 0, T)
+    assert np.array_equal(ko[0, 0].astype(np.float64), k_rows)  # precondition: k_hat exact
+    return p, vo[0, 0].astype(np.float64)
+
+
+def test_attention_two_rows_closed_form():
+    """Two cache rows: o = (v1 + e^D v2) / (1 + e^D), D = scale * q.(k2 - k1).
+
+    The keys are integers the 8-bit affine reproduces exactly, so D is exact
+    and needs no dequantisation; the weights are written out for two rows (no
+    max subtraction, no running sums).  At the default scale 1/sqrt(d) D = 1;
+    at scale ln(3)/8 the weights are exactly 1/4 and 3/4.  Dropping the scale
+    from the oracle's scores (s_t = dot), or applying it twice, moves the
+    output by more than 0.1 here, far outside the 1e-12 bound (checked by
+    planting that change in the oracle on the CPU)."""
+    d = 64
+    rng = np.random.default_rng(77)
+    base = rng.integers(-60, 61, size=(1, d)).astype(np.float64)
+    k = _integer_key_rows(np.repeat(base, 2, axis=0), d)
+    k[1, 10] = k[0, 10] + 8.0  # rows differ in one dim by 8
+    q = np.zeros(d)
+    q[10] = 1.0
+    q[40] = -2.0  # same in both rows: shifts both logits alike
+    qb = _bf16(q.reshape(1, 1, d))
+    p, vh = _closed_form_cache(k, d, seed=5)
+    dlt = float(q @ (k[1] - k[0]))
+    assert dlt == 8.0
+    # default scale 1/sqrt(64): D = 1
+    e = math.exp(dlt / math.sqrt(d))
+    want = (vh[0] + e * vh[1]) / (1.0 + e)
+    got = oracle.attention(p, qb, 2)[0, 0]
+    assert np.max(np.abs(got - want)) <= 1e-12
+    # scale ln(3)/8: e^D = 3 exactly, so o = (v1 + 3 v2) / 4
+    got = oracle.attention(p, qb, 2, softmax_scale=math.log(3.0) / 8.0)[0, 0]
+    assert np.max(np.abs(got - (vh[0] + 3.0 * vh[1]) / 4.0)) <= 1e-12
+    # the weighting is visible: the two rows' values differ
+    assert np.max(np.abs(vh[0] - vh[1])) > 0.5
+
+
+def test_attention_three_rows_distinct_weights():
+    """Three rows whose scores differ by scale * (0, 8, 16): at scale ln(2)/8 the
+    weights are exactly 1/7, 2/7, 4/7, so a wrong normaliser, a max subtracted
+    from one row only, or a scale applied anywhere but the scores shows; the
+    default scale 1/sqrt(d) is checked against the three-term closed form."""
+    d = 64
+    rng = np.random.default_rng(78)
+    base = rng.integers(-60, 61, size=(1, d)).astype(np.float64)
+    k = _integer_key_rows(np.repeat(base, 3, axis=0), d)
+    k[1, 20] = k[0, 20] + 8.0
+    k[2, 20] = k[0, 20] + 16.0
+    q = np.zeros(d)
+    q[20] = 1.0
+    qb = _bf16(q.reshape(1, 1, d))
+    p, vh = _closed_form_cache(k, d, seed=6)
+    got = oracle.attention(p, qb, 3, softmax_scale=math.log(2.0) / 8.0)[0, 0]
+    assert np.max(np.abs(got - (vh[0] + 2.0 * vh[1] + 4.0 * vh[2]) / 7.0)) <= 1e-12
+    w = np.exp(np.array([0.0, 1.0, 2.0]))  # default scale 1/8: scores differ by 0, 1, 2
+    want = (w[0] * vh[0] + w[1] * vh[1] + w[2] * vh[2]) / w.sum()
+    got = oracle.attention(p, qb, 3)[0, 0]
+    assert np.max(np.abs(got - want)) <= 1e-12
+
+
 def test_attention_deferred_unrotation_equals_eager():
     """Pages, 'Deferred inverse FWHT': attention is linear in V, so un-rotating the
     weighted sum equals the weighted sum of un-rotated rows."""
