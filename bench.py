@@ -46,6 +46,9 @@ DECODE = dict(B=32, H=8, QH=64, T=32768, d=128, kb=8, vb=3)
 BYTES_PER_TH = 200  # k8v3, d128 (page section "Algorithm", bytes per token-head)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0  # dense bf16, one earlier GB300 measurement
+NOMINAL_HBM_GBS = 8000.0  # the codec's stated roofline: bytes moved / 8 TB/s
+LONGCTX = dict(B=32, H=8, QH=64, T=131072, d=128, kb=4, vb=3)
+SWEEP = dict(H=8, T=16384, ds=(64, 256, 512), kbs=(2, 4, 5, 8), vbs=(2, 3, 4))
 
 
 # ------------------------------------------------------------------ helpers
@@ -82,6 +85,14 @@ def measured_bf16_tflops():
 
 
 PRIME_CYCLES = 4_000_000  # ~2 ms of device spin before a timed region starts
+
+
+def rate(nbytes, us, peak):
+    """A part's time with its throughput and its fraction of both rooflines:
+    the measured copy bandwidth (frac) and the nominal 8 TB/s (frac_8tbs)."""
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "frac_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "bytes": int(nbytes)}
 
 
 def attention_traffic(kernel_hash: str):
@@ -346,11 +357,18 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in (kp_h, vp_h, kn_h, vn_h, q_h))
     d2h = sum(t.numel() * t.element_size() for t in (ko_h, vo_h, out_h))
 
+    # --- the other configurations (outside the headline's timed region)
+    ctimes, cbytes = ({}, {}) if args.no_configs else \
+        measure_configs(tq, tq_synth, torch, dev, dcache, knew, vnew, q, T, rank)
+
     # --- aggregate over ranks (max time)
     names = ("encode", "decode", "append", "attention")
-    tt = max_over_ranks([elapsed_ms / K, e2e_ms] + [parts[k] for k in names], world, dev)
+    cnames = sorted(ctimes)
+    tt = max_over_ranks([elapsed_ms / K, e2e_ms] + [parts[k] for k in names] + [ctimes[k] for k in cnames],
+                        world, dev)
     ms, e2e_ms = tt[0], tt[1]
-    parts = dict(zip(names, tt[2:]))
+    parts = dict(zip(names, tt[2:2 + len(names)]))
+    ctimes = dict(zip(cnames, tt[2 + len(names):]))
     if rank != 0:
         return None
 
@@ -382,14 +400,13 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_bytes_per_step": ab["total"],
         },
         "parts": {
-            "encode": {"us": round(parts["encode"] * 1e3, 2), "GB/s": round(gbs(ab["encode"], parts["encode"]), 1),
-                       "frac": round(gbs(ab["encode"], parts["encode"]) / peak, 4)},
-            "decode": {"us": round(parts["decode"] * 1e3, 2), "GB/s": round(gbs(ab["decode"], parts["decode"]), 1),
-                       "frac": round(gbs(ab["decode"], parts["decode"]) / peak, 4)},
-            "append_1_token": {"us": round(parts["append"] * 1e3, 2)},
-            "attention": {"us_per_step": round(parts["attention"] * 1e3, 2), "GB/s": round(attn_gbs, 1),
-                          "frac": round(attn_gbs / peak, 4)},
+            "encode": rate(ab["encode"], parts["encode"] * 1e3, peak),
+            "decode": rate(ab["decode"], parts["decode"] * 1e3, peak),
+            "append_1_token": rate(ab["append"], parts["append"] * 1e3, peak),
+            "attention": {**rate(ab["attention"], parts["attention"] * 1e3, peak),
+                          "us_per_step": round(parts["attention"] * 1e3, 2)},
             "decode_step_us": round((parts["append"] + parts["attention"]) * 1e3, 2),
+            **config_parts(ctimes, cbytes, peak),
         },
         "roofline": {
             "kernel": "attn_split_kernel + attn_combine_kernel (timed together through tq_decode_attention)",
@@ -399,6 +416,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
             "unit": "GB/s",
             "frac": round(attn_gbs / peak, 4),
+            "frac_8tbs": round(attn_gbs / NOMINAL_HBM_GBS, 4),
             "traffic": attention_traffic(kernel_source_hash()),
             "algorithmic_bytes_per_launch": ab["attention"],
         },
@@ -409,6 +427,198 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     return line
+
+
+# ------------------------------------------------------------------ the other configurations
+def flushing_timer(torch, dev):
+    """fn's median device time in µs over `reps` calls, each call preceded by a
+    write of a buffer twice the size of L2 (so its inputs come from HBM) and
+    bracketed by CUDA events on the launching stream; a device spin queued
+    first keeps host launch time out of the marks."""
+    st = torch.cuda.current_stream()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def timed(fn, reps=10, warmup=3):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda._sleep(PRIME_CYCLES)
+        for a, b in evs:
+            flush.zero_()
+            a.record(st)
+            fn()
+            b.record(st)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+    return timed
+
+
+def decode_steps(tq, torch, dev, cache, knew, vnew, q, seq_len, nb, groups, steps):
+    """Decode steps of nb sequences: append each sequence's new token at row
+    seq_len - 1, then attention over seq_len rows.  `groups` disjoint batch
+    slices of the cache take turns, so a slice's rows have left L2 before its
+    next turn (each slice alone may fit in L2).  Returns µs of the append and
+    of the attention (median over calls, CUDA events around each call) and of
+    the whole step replayed from a CUDA graph per slice (mean over steps)."""
+    st = torch.cuda.current_stream()
+    QH, d = q.shape[1], q.shape[2]
+    ws_bytes = tq.tq_attention_workspace_bytes(cache.batch_slice(0, nb), QH, seq_len)
+    sl = []
+    for i in range(groups):
+        b0 = i * nb
+        sl.append(dict(c=cache.batch_slice(b0, nb), kn=knew[b0:b0 + nb], vn=vnew[b0:b0 + nb], q=q[b0:b0 + nb],
+                       out=torch.empty((nb, QH, d), dtype=torch.float32, device=dev),
+                       ws=torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)))
+
+    def append(x):
+        tq.tq_encode_append(x["c"], x["kn"], x["vn"], seq_len - 1)
+
+    def attend(x):
+        tq.tq_decode_attention(x["c"], x["q"], seq_len, out=x["out"], workspace=x["ws"])
+
+    for _ in range(3):
+        for x in sl:
+            append(x)
+            attend(x)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda._sleep(PRIME_CYCLES)
+    for s_, e in enumerate(ev):
+        x = sl[s_ % groups]
+        e[0].record(st)
+        append(x)
+        e[1].record(st)
+        attend(x)
+        e[2].record(st)
+    torch.cuda.synchronize()
+    app_us = statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in ev)
+    att_us = statistics.median(e[1].elapsed_time(e[2]) * 1e3 for e in ev)
+    graphs = []
+    for x in sl:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            append(x)
+            attend(x)
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(PRIME_CYCLES)
+    a.record(st)
+    for s_ in range(steps):
+        graphs[s_ % groups].replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    step_us = a.elapsed_time(b) * 1e3 / steps
+    del graphs
+    return app_us, att_us, step_us
+
+
+def decode_step_bytes(nb, H, QH, d, rows, bpt):
+    """(append, attention) algorithmic bytes of one decode step: the new token's
+    bf16 K, V in and its packed row out; every cached row plus q (bf16) and the
+    output (fp32)."""
+    return nb * H * (4 * d + bpt), nb * H * rows * bpt + nb * QH * d * 6
+
+
+def measure_configs(tq, tq_synth, torch, dev, dcache, knew, vnew, q, T, rank, steps=20):
+    """Device times (µs) of the configurations beside the headline step:
+      decode attention at batch 1 and 8 (slices of the headline decode cache),
+      the long-context step (32 x 8 x 131073 rows, k4v3, 4.56 GB packed),
+      and encode / fetch of every cell of the width and head_dim sweep
+      (8 kv-heads x 16384 tokens; d 64/256/512 x k 2/4/5/8 x v 2/3/4).
+    Returns a flat {name: µs} and {name: algorithmic bytes}."""
+    times, nbytes = {}, {}
+    D = DECODE
+    bpt = tq.tq_bytes_per_token_head(D["d"], D["kb"], D["vb"])
+    for nb in (1, 8):
+        groups = min(4, dcache.batch // nb)
+        if groups < 1:
+            continue
+        app, att, step = decode_steps(tq, torch, dev, dcache, knew, vnew, q, T + 1, nb, groups, steps)
+        ab, tb = decode_step_bytes(nb, D["H"], D["QH"], D["d"], T + 1, bpt)
+        for k_, us, by in (("append", app, ab), ("attention", att, tb), ("step_graph", step, ab + tb)):
+            times[f"decode_b{nb}_{k_}"], nbytes[f"decode_b{nb}_{k_}"] = us, by
+
+    L = LONGCTX
+    wl = tq_synth.WORKLOADS["longctx"]
+    off, _ = rank_shard(rank, int(os.environ.get("WORLD_SIZE", "1")), L["B"])
+    lc = tq.Cache(L["B"], L["H"], L["d"], L["T"] + 1, L["kb"], L["vb"], device=dev)
+    for b0 in range(L["B"]):  # the bf16 source (17 GB in all) is generated one sequence at a time
+        kc = torch.empty((1, L["H"], L["T"] + 1, L["d"]), dtype=torch.int16, device=dev)
+        vc = torch.empty_like(kc)
+        tq_synth.device_kv(wl, kc, vc, B=1, H=L["H"], d=L["d"], n=L["T"] + 1, b_offset=off + b0)
+        tq.tq_encode_append(lc.batch_slice(b0, 1), kc.view(torch.bfloat16)[:, :, :L["T"]],
+                            vc.view(torch.bfloat16)[:, :, :L["T"]], 0)
+        if b0 == 0:
+            kn = torch.empty((L["B"], L["H"], 1, L["d"]), dtype=torch.int16, device=dev)
+            vn = torch.empty_like(kn)
+        kn[b0:b0 + 1].copy_(kc[:, :, L["T"]:])
+        vn[b0:b0 + 1].copy_(vc[:, :, L["T"]:])
+        del kc, vc
+    ql = torch.empty((L["B"], L["QH"], L["d"]), dtype=torch.int16, device=dev)
+    tq_synth.device_q(wl, rank, ql, B=L["B"], QH=L["QH"], d=L["d"])
+    app, att, step = decode_steps(tq, torch, dev, lc, kn.view(torch.bfloat16), vn.view(torch.bfloat16),
+                                  ql.view(torch.bfloat16), L["T"] + 1, L["B"], 1, steps)
+    lbpt = tq.tq_bytes_per_token_head(L["d"], L["kb"], L["vb"])
+    ab, tb = decode_step_bytes(L["B"], L["H"], L["QH"], L["d"], L["T"] + 1, lbpt)
+    for k_, us, by in (("append", app, ab), ("attention", att, tb), ("step_graph", step, ab + tb)):
+        times[f"long_context_{k_}"], nbytes[f"long_context_{k_}"] = us, by
+    del lc, kn, vn, ql
+    torch.cuda.empty_cache()
+
+    timed = flushing_timer(torch, dev)
+    w = tq_synth.WORKLOADS["sweep"]
+    H, Ts = SWEEP["H"], SWEEP["T"]
+    for d in SWEEP["ds"]:
+        k = torch.empty((1, H, Ts, d), dtype=torch.int16, device=dev)
+        v = torch.empty_like(k)
+        tq_synth.device_kv(w, k, v, B=1, H=H, d=d, n=Ts)
+        k16, v16 = k.view(torch.bfloat16), v.view(torch.bfloat16)
+        ko, vo = torch.empty_like(k16), torch.empty_like(v16)
+        for kb in SWEEP["kbs"]:
+            for vb in SWEEP["vbs"]:
+                c = tq.Cache(1, H, d, Ts, kb, vb, device=dev)
+                cb = tq.tq_bytes_per_token_head(d, kb, vb)
+                name = f"sweep_d{d}_k{kb}v{vb}"
+                times[name + "_encode"] = timed(lambda: tq.tq_encode_append(c, k16, v16, 0))
+                times[name + "_decode"] = timed(
+                    lambda: tq.tq_decode(c, 0, Ts, dtype=torch.bfloat16, k_out=ko, v_out=vo))
+                nbytes[name + "_encode"] = nbytes[name + "_decode"] = H * Ts * (4 * d + cb)
+                del c
+        del k, v, k16, v16, ko, vo
+    assert tq.tq_device_error() == 0
+    return times, nbytes
+
+
+def config_parts(times, nbytes, peak):
+    """The measure_configs times as bench-line entries (µs, GB/s, fractions)."""
+    out = {}
+    for pre, desc in (("decode_b1", "decode step, batch 1, 64 q-heads / 8 kv-heads, 32769 rows, d128 k8v3"),
+                      ("decode_b8", "decode step, batch 8, 64 q-heads / 8 kv-heads, 32769 rows, d128 k8v3"),
+                      ("long_context", "decode step, batch 32, 64 q-heads / 8 kv-heads, 131073 rows, d128 k4v3 "
+                                       "(4.56 GB packed)")):
+        if pre + "_attention" not in times:
+            continue
+        out[pre] = {"workload": desc,
+                    "attention": rate(nbytes[pre + "_attention"], times[pre + "_attention"], peak),
+                    "append_1_token": rate(nbytes[pre + "_append"], times[pre + "_append"], peak),
+                    "step_graph": rate(nbytes[pre + "_step_graph"], times[pre + "_step_graph"], peak)}
+    cells = {}
+    for k_ in sorted(times):
+        if k_.startswith("sweep_") and k_.endswith("_encode"):
+            cell = k_[len("sweep_"):-len("_encode")]
+            cells[cell] = {op: rate(nbytes[f"sweep_{cell}_{op}"], times[f"sweep_{cell}_{op}"], peak)
+                           for op in ("encode", "decode")}
+    if cells:
+        out["sweep_codec"] = {"workload": "8 kv-heads x 16384 tokens, K ~ N(0,1) x logN(0,1), V ~ N(0,1); "
+                                          "encode bf16 -> packed, fetch packed -> bf16; L2 flushed before each call",
+                              "cells": cells}
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline and reference arm)
@@ -485,19 +695,79 @@ def run_reference(args):
     }
 
 
-def cpu_baseline():
-    cores = cpu_cores()
-    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
-    # the whole step (all 8192 prefill rows, all 32 decode sequences), run twice:
-    # ~12 s of oracle work on 16 cores (the oracle has nothing to warm up)
-    sample = OracleSample(pre_rows=PREFILL["T"], seqs=DECODE["B"])
-    runs = 2
+def omp_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP regions from here on."""
+    import ctypes
+
+    import oracle
+
+    oracle.lib()  # loads the OpenMP runtime the oracle links
+    ctypes.CDLL("libgomp.so.1").omp_set_num_threads(int(n))
+
+
+class LongContextOracleSample:
+    """The long-context decode step's attention in the oracle for `seqs`
+    sequences x 1 kv-head (8 q-heads each) over all 131073 rows (k4v3)."""
+
+    def __init__(self, seqs: int):
+        import oracle
+        import tq_synth
+
+        L = LONGCTX
+        wl = tq_synth.WORKLOADS["longctx"]
+        self.oracle = oracle
+        self.items = []
+        for b in range(seqs):
+            k, v = tq_synth.host_kv(wl, B=1, H=1, n=L["T"] + 1, b_offset=b)
+            pl = oracle.Planes(1, 1, L["d"], L["kb"], L["vb"], L["T"] + 16)
+            oracle.encode(pl, k, v)
+            q = tq_synth.host_q(wl, 0, B=1, QH=L["QH"] // L["H"], d=L["d"])
+            self.items.append((pl, q))
+            del k, v
+        bpt = oracle.bytes_per_token_head(L["d"], L["kb"], L["vb"])
+        self.bytes = seqs * ((L["T"] + 1) * bpt + (L["QH"] // L["H"]) * L["d"] * 6)
+        self.desc = (f"long-context decode attention of {seqs} sequences x 1 kv-head x 8 q-heads over "
+                     f"{L['T'] + 1} rows, k4v3")
+
+    def run_once(self):
+        for pl, q in self.items:
+            self.oracle.attention(pl, q, LONGCTX["T"] + 1)
+
+
+def _time_sample(sample, runs):
     t = time.perf_counter()
     for _ in range(runs):
         sample.run_once()
     dt = time.perf_counter() - t
-    return {"value": round(runs * sample.bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+    return runs * sample.bytes / dt / 1e9, dt
+
+
+def cpu_baseline():
+    cores = cpu_cores()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    omp_threads(cores)
+    # the whole step (all 8192 prefill rows, all 32 decode sequences), run twice:
+    # ~12 s of oracle work on 16 cores (the oracle has nothing to warm up)
+    sample = OracleSample(pre_rows=PREFILL["T"], seqs=DECODE["B"])
+    runs = 2
+    value, dt = _time_sample(sample, runs)
+    line = {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{runs} passes of {sample.desc}", "seconds": round(dt, 2)}
+    # one thread: a smaller slice of the same step
+    small = OracleSample(pre_rows=512, seqs=1, heads=2)
+    omp_threads(1)
+    v1, dt1 = _time_sample(small, 1)
+    line["single_thread"] = {"value": round(v1, 4), "unit": "GB/s", "cores": 1, "sample": small.desc,
+                             "seconds": round(dt1, 2)}
+    # the long-context step's attention on all cores (16 q-head tasks)
+    omp_threads(cores)
+    lc = LongContextOracleSample(seqs=2)
+    vl, dtl = _time_sample(lc, 1)
+    line["long_context_attention"] = {"value": round(vl, 4), "unit": "GB/s", "cores": cores, "sample": lc.desc,
+                                      "seconds": round(dtl, 2),
+                                      "us_per_full_step": round(
+                                          LONGCTX["B"] * LONGCTX["H"] / 2 * dtl * 1e6, 0)}
+    return line
 
 
 # ------------------------------------------------------------------ main
@@ -635,6 +905,21 @@ def run_sweep(only=None):
         emit("clear_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, B * H * T * 200)
 
 
+def free_port() -> int:
+    import socket
+
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launcher_command(n: int, argv) -> list:
+    """torch.distributed.run with one rank per GPU on this node, rendezvous on
+    127.0.0.1, re-running this script with the same arguments."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__), *argv]
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -642,6 +927,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the configurations beside the headline step (batch 1 and 8 decode, long context, "
+                         "the codec sweep)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="sequences of the decode step (smaller values for profiling captures)")
     ap.add_argument("--sweep", action="store_true",
@@ -656,9 +944,16 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     DECODE["B"] = args.decode_batch
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: start the ranks under torch.distributed.run
+        sys.exit(subprocess.call(launcher_command(args.gpus, sys.argv[1:])))
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE is {world}: launch one rank per GPU")
 
     if args.impl == "reference":
         if rank == 0:

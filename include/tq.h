@@ -97,7 +97,14 @@ typedef struct tq_cache {
     uint16_t *k_zero;     /* device */
     uint8_t *v_codes;     /* device */
     uint16_t *v_scale;    /* device */
+    uint64_t sign_seed;   /* seed of the value sign vector (tq_sign_vector); the
+                             codec's default is TQ_DEFAULT_SIGN_SEED.  Every call
+                             on one cache must use the seed it was encoded with. */
 } tq_cache;
+
+/* The sign-vector seed the codec uses unless a cache states another (the page
+ * draws its vector once from a generator seeded with 42). */
+#define TQ_DEFAULT_SIGN_SEED 42u
 
 /* Human-readable name of a status. */
 TQ_API const char *tq_status_string(tq_status status);
@@ -111,11 +118,14 @@ TQ_API size_t tq_bytes_per_token_head(int32_t head_dim, int32_t k_bits, int32_t 
  * v_scale) for its batch, heads and capacity; pointers are not read. */
 TQ_API tq_status tq_plane_bytes(const tq_cache *cache, size_t out_bytes[5]);
 
-/* The +-1 value sign vector the library applies for head_dim d (host output,
- * d int8 entries).  Output i of SplitMix64 seeded with 42; sign -1 when its
- * top bit is set.  The d=64 vector is a prefix of the d=128 one, and so on.
- * The page fixes one +-1 vector per head_dim, generated once and hardcoded. */
-TQ_API tq_status tq_sign_vector(int32_t head_dim, int8_t *host_out);
+/* The +-1 value sign vector the library applies for head_dim d and a seed
+ * (host output, d int8 entries): entry i is -1 when the top bit of output i of
+ * SplitMix64 started at `seed` is set (Steele, Lea & Flood, OOPSLA 2014),
+ * else +1.  For one seed the d=64 vector is a prefix of the d=128 one, and so
+ * on.  The page fixes one +-1 vector per head_dim, drawn once from a seeded
+ * generator and hardcoded; here the seed is the cache's sign_seed (default
+ * TQ_DEFAULT_SIGN_SEED = 42). */
+TQ_API tq_status tq_sign_vector(int32_t head_dim, uint64_t seed, int8_t *host_out);
 
 /* The Lloyd-Max tables for v_bits (host outputs): 2^v_bits centroids and
  * 2^v_bits - 1 boundaries (midpoints), fp32, ascending; the optimal quantizer
@@ -163,14 +173,16 @@ TQ_API tq_status tq_decode_values_rotated(const tq_cache *cache, int64_t t0, int
 /*
  * Un-rotation of vectors formed in the rotated domain: out = signs *
  * FWHT(x) / sqrt(d) for each of `rows` rows of head_dim elements (the second
- * half of the value dequantisation; page section "Deferred inverse FWHT").
+ * half of the value dequantisation; page section "Deferred inverse FWHT"),
+ * signs being tq_sign_vector(head_dim, sign_seed) -- the seed of the cache
+ * the rows came from.
  *  x, out    device, [rows][head_dim] contiguous, fp32 or bf16 each
  *            (in_dtype, out_dtype); 16-byte aligned; out may equal x when the
  *            dtypes match (in place).
  * rows = 0 is a no-op.
  */
-TQ_API tq_status tq_unrotate(int32_t head_dim, tq_dtype in_dtype, const void *x, int64_t rows, tq_dtype out_dtype,
-                             void *out, tq_stream_t stream);
+TQ_API tq_status tq_unrotate(int32_t head_dim, uint64_t sign_seed, tq_dtype in_dtype, const void *x, int64_t rows,
+                             tq_dtype out_dtype, void *out, tq_stream_t stream);
 
 /*
  * Cache lifecycle: copy token rows [src_t0, src_t0 + n) of every (sequence,
@@ -178,8 +190,8 @@ TQ_API tq_status tq_unrotate(int32_t head_dim, tq_dtype in_dtype, const void *x,
  * byte for byte.  Groups run along head_dim only, so token slices are
  * byte-safe (page section "Architecture in mlx-bun"); with it the caller
  * snapshots, restores and clones caches and grows capacity (copy into a
- * larger cache).  The two caches must agree in head_dim, bit widths, kv-heads
- * and batch; capacities may differ.  Within one cache the ranges must not
+ * larger cache).  The two caches must agree in head_dim, bit widths, kv-heads,
+ * batch and sign_seed (else TQ_ERR_SHAPE); capacities may differ.  Within one cache the ranges must not
  * overlap unless identical (then nothing moves).  n = 0 is a no-op.
  */
 TQ_API tq_status tq_cache_copy_rows(const tq_cache *dst, int64_t dst_t0, const tq_cache *src, int64_t src_t0,

@@ -248,9 +248,10 @@ def bytes_per_token_head(d: int, kb: int, vb: int) -> int:
 class Planes:
     """Host copy of the five cache planes, [B][H][cap][...] each."""
 
-    def __init__(self, B, H, d, kb, vb, cap):
+    def __init__(self, B, H, d, kb, vb, cap, sign_seed=SIGN_SEED):
         g = d // 32
         self.B, self.H, self.d, self.kb, self.vb, self.cap = B, H, d, kb, vb, cap
+        self.sign_seed = sign_seed  # the cache's sign vector: sign_vector(d, sign_seed)
         self.k_codes = np.zeros((B, H, cap, d * kb // 8), dtype=np.uint8)
         self.k_scale = np.zeros((B, H, cap, g), dtype=np.uint16)
         self.k_zero = np.zeros((B, H, cap, g), dtype=np.uint16)
@@ -267,7 +268,7 @@ def encode(planes: Planes, k_bf16: np.ndarray, v_bf16: np.ndarray, t0: int = 0) 
     k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
     v = np.ascontiguousarray(v_bf16, dtype=np.uint16)
     n = k.shape[2]
-    signs = sign_vector(p.d)
+    signs = sign_vector(p.d, p.sign_seed)
     bnd = codebook(p.vb)[1]
     rc = lib().tqo_encode(p.B, p.H, p.d, p.kb, p.vb, p.cap, t0, n, _ptr(k), _ptr(v), _ptr(signs),
                           _ptr(bnd), *[_ptr(a) for a in p.arrays()])
@@ -281,7 +282,7 @@ def decode(planes: Planes, t0: int, n: int, want_k: bool = True, want_v: bool = 
     p = planes
     ko = np.zeros((p.B, p.H, n, p.d), dtype=np.float32) if want_k else None
     vo = np.zeros((p.B, p.H, n, p.d), dtype=np.float32) if want_v else None
-    signs = sign_vector(p.d)
+    signs = sign_vector(p.d, p.sign_seed)
     cen = codebook(p.vb)[0]
     rc = lib().tqo_decode(p.B, p.H, p.d, p.kb, p.vb, p.cap, t0, n, *[_ptr(a) for a in p.arrays()],
                           _ptr(signs), _ptr(cen), _ptr(ko), _ptr(vo))
@@ -324,7 +325,7 @@ def attention(planes: Planes, q_bf16: np.ndarray, seq_len: int, softmax_scale: f
     scale = 1.0 / np.sqrt(p.d) if softmax_scale is None else float(softmax_scale)
     out = np.zeros((p.B, QH, p.d), dtype=np.float64)
     w = None if want is None else np.ascontiguousarray(want, dtype=np.uint8)
-    signs = sign_vector(p.d)
+    signs = sign_vector(p.d, p.sign_seed)
     cen = codebook(p.vb)[0]
     rc = lib().tqo_attention(p.B, p.H, p.d, p.kb, p.vb, p.cap, *[_ptr(a) for a in p.arrays()],
                              _ptr(signs), _ptr(cen), _ptr(q), QH, seq_len, scale, _ptr(w), _ptr(out))

@@ -25,7 +25,7 @@ __all__ = [
     "tq_attention_supported", "tq_device_error", "tq_plane_bytes", "tq_decode_attention_noalloc",
     "tq_decode_values_rotated", "tq_unrotate", "tq_cache_copy_rows", "tq_cache_clear_rows",
     "tq_multi_token_workspace_bytes", "tq_multi_token_attention", "tq_check_wait_timeout",
-    "TQ_DEVICE_ERR_WAIT_TIMEOUT",
+    "TQ_DEVICE_ERR_WAIT_TIMEOUT", "TQ_DEFAULT_SIGN_SEED",
 ]
 
 HEAD_DIMS = (64, 128, 256, 512)
@@ -33,6 +33,7 @@ K_BITS = (2, 4, 5, 8)
 V_BITS = (2, 3, 4, 5, 8)
 TQ_BF16, TQ_F32 = 0, 1
 TQ_DEVICE_ERR_WAIT_TIMEOUT = 1  # device error word: a bounded wait gave up
+TQ_DEFAULT_SIGN_SEED = 42  # the codec's sign-vector seed unless a cache states another
 
 EXPORTS = (
     "tq_status_string", "tq_bytes_per_token_head", "tq_plane_bytes", "tq_sign_vector", "tq_codebook",
@@ -55,7 +56,7 @@ class _CacheStruct(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32), ("batch", ctypes.c_int32), ("reserved", ctypes.c_int32),
         ("capacity", ctypes.c_int64),
         ("k_codes", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("k_zero", ctypes.c_void_p),
-        ("v_codes", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("sign_seed", ctypes.c_uint64),
     ]
 
 
@@ -78,7 +79,7 @@ def lib() -> ctypes.CDLL:
     so.tq_bytes_per_token_head.restype = _SZ
     so.tq_bytes_per_token_head.argtypes = [_I32, _I32, _I32]
     so.tq_plane_bytes.argtypes = [_CP, ctypes.POINTER(_SZ)]
-    so.tq_sign_vector.argtypes = [_I32, _P]
+    so.tq_sign_vector.argtypes = [_I32, ctypes.c_uint64, _P]
     so.tq_codebook.argtypes = [_I32, _P, _P]
     so.tq_encode_append.argtypes = [_CP, _P, ctypes.POINTER(_I64), _P, ctypes.POINTER(_I64), _I64, _I64, _P]
     so.tq_decode.argtypes = [_CP, _I64, _I64, ctypes.c_int, _P, _P, _P]
@@ -90,7 +91,7 @@ def lib() -> ctypes.CDLL:
     so.tq_check_wait_timeout.argtypes = [_P]
     so.tq_decode_attention_noalloc.argtypes = [_CP, _P, _I32, _I64, ctypes.c_float, _P, _P]
     so.tq_decode_values_rotated.argtypes = [_CP, _I64, _I64, ctypes.c_int, _P, _P]
-    so.tq_unrotate.argtypes = [_I32, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P]
+    so.tq_unrotate.argtypes = [_I32, ctypes.c_uint64, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P]
     so.tq_cache_copy_rows.argtypes = [_CP, _I64, _CP, _I64, _I64, _P]
     so.tq_cache_clear_rows.argtypes = [_CP, _I64, _I64, _P]
     so.tq_multi_token_workspace_bytes.restype = _SZ
@@ -125,14 +126,17 @@ class Cache:
     """The five packed planes of one KV cache, [batch][H][capacity][row] each.
 
     capacity is rounded up to a multiple of 16 (the library's row alignment).
+    sign_seed picks the value sign vector (tq_sign_vector); every call on the
+    cache uses it.
     """
 
     def __init__(self, batch: int, num_kv_heads: int, head_dim: int, capacity: int, k_bits: int = 8,
-                 v_bits: int = 3, device="cuda"):
+                 v_bits: int = 3, device="cuda", sign_seed: int = TQ_DEFAULT_SIGN_SEED):
         cap = (int(capacity) + 15) // 16 * 16
         g = head_dim // 32
         self.batch, self.num_kv_heads, self.head_dim = int(batch), int(num_kv_heads), int(head_dim)
         self.k_bits, self.v_bits, self.capacity = int(k_bits), int(v_bits), cap
+        self.sign_seed = int(sign_seed)
         shape = (self.batch, self.num_kv_heads, cap)
         kw = dict(device=device)
         self.k_codes = torch.zeros(*shape, head_dim * k_bits // 8, dtype=torch.uint8, **kw)
@@ -146,7 +150,7 @@ class Cache:
 
     def struct(self) -> _CacheStruct:
         return _CacheStruct(self.head_dim, self.k_bits, self.v_bits, self.num_kv_heads, self.batch, 0,
-                            self.capacity, *[t.data_ptr() for t in self.planes()])
+                            self.capacity, *[t.data_ptr() for t in self.planes()], self.sign_seed)
 
     def batch_slice(self, b0: int, nb: int) -> "Cache":
         """A view of sequences [b0, b0+nb) sharing this cache's storage."""
@@ -173,11 +177,11 @@ def tq_plane_bytes(cache: Cache) -> list:
     return list(out)
 
 
-def tq_sign_vector(head_dim: int):
+def tq_sign_vector(head_dim: int, seed: int = TQ_DEFAULT_SIGN_SEED):
     import numpy as np
 
     out = np.zeros(head_dim, dtype=np.int8)
-    _check(lib().tq_sign_vector(head_dim, out.ctypes.data), "tq_sign_vector")
+    _check(lib().tq_sign_vector(head_dim, int(seed), out.ctypes.data), "tq_sign_vector")
     return out
 
 
@@ -255,8 +259,10 @@ def tq_decode_values_rotated(cache: Cache, t0: int, n: int, dtype=torch.float32,
     return out
 
 
-def tq_unrotate(x: torch.Tensor, out: torch.Tensor | None = None, dtype=None, stream=None) -> torch.Tensor:
-    """signs * FWHT(x)/sqrt(d) for every row of x ([..., d] contiguous, fp32 or bf16)."""
+def tq_unrotate(x: torch.Tensor, out: torch.Tensor | None = None, dtype=None, stream=None,
+                sign_seed: int = TQ_DEFAULT_SIGN_SEED) -> torch.Tensor:
+    """signs * FWHT(x)/sqrt(d) for every row of x ([..., d] contiguous, fp32 or bf16);
+    signs = tq_sign_vector(d, sign_seed), the seed of the cache the rows came from."""
     _require_cuda(x)
     if not x.is_contiguous():
         raise ValueError("x must be contiguous")
@@ -266,8 +272,8 @@ def tq_unrotate(x: torch.Tensor, out: torch.Tensor | None = None, dtype=None, st
     if out.dtype != dtype or out.shape != x.shape or not out.is_contiguous():
         raise ValueError("out must be contiguous, shaped like x, of the requested dtype")
     d = x.shape[-1]
-    _check(lib().tq_unrotate(int(d), _dtype_code(x.dtype), x.data_ptr(), int(x.numel() // d), _dtype_code(dtype),
-                             out.data_ptr(), _stream(stream)), "tq_unrotate")
+    _check(lib().tq_unrotate(int(d), int(sign_seed), _dtype_code(x.dtype), x.data_ptr(), int(x.numel() // d),
+                             _dtype_code(dtype), out.data_ptr(), _stream(stream)), "tq_unrotate")
     return out
 
 

@@ -77,11 +77,26 @@ tq_status check_cache(const tq_cache *c)
     return TQ_OK;
 }
 
+// The sign mask of (seed, head_dim); the last one built on this thread is kept,
+// since one process usually serves a single seed.
+const tq::SignBits &sign_bits(uint64_t seed, int d)
+{
+    thread_local uint64_t k_seed = 0;
+    thread_local int k_d = 0;
+    thread_local tq::SignBits k_bits{};
+    if (k_d != d || k_seed != seed) {
+        k_bits = tq::make_sign_bits(seed, d);
+        k_seed = seed;
+        k_d = d;
+    }
+    return k_bits;
+}
+
 tq::CacheView view(const tq_cache *c)
 {
     return tq::CacheView{c->head_dim, c->k_bits,  c->v_bits,  c->num_kv_heads, c->batch,
                          c->capacity, c->k_codes, c->k_scale, c->k_zero,       c->v_codes,
-                         c->v_scale};
+                         c->v_scale,  sign_bits(c->sign_seed, c->head_dim)};
 }
 
 tq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
@@ -145,11 +160,12 @@ tq_status tq_plane_bytes(const tq_cache *c, size_t out[5])
     return TQ_OK;
 }
 
-tq_status tq_sign_vector(int32_t d, int8_t *out)
+tq_status tq_sign_vector(int32_t d, uint64_t seed, int8_t *out)
 {
     if (!out) return TQ_ERR_NULL;
     if (!valid_head_dim(d)) return TQ_ERR_HEAD_DIM;
-    for (int i = 0; i < d; ++i) out[i] = tq::sign_negative(i) ? -1 : 1;
+    const tq::SignBits s = tq::make_sign_bits(seed, d);
+    for (int i = 0; i < d; ++i) out[i] = tq::sign_negative(s, i) ? -1 : 1;
     return TQ_OK;
 }
 
@@ -210,8 +226,8 @@ tq_status tq_decode_values_rotated(const tq_cache *c, int64_t t0, int64_t n, tq_
     return cuda_status(tq::launch_decode_rotated(view(c), t0, n, dt == TQ_F32, v_out, (cudaStream_t)stream));
 }
 
-tq_status tq_unrotate(int32_t d, tq_dtype in_dt, const void *x, int64_t rows, tq_dtype out_dt, void *out,
-                      tq_stream_t stream)
+tq_status tq_unrotate(int32_t d, uint64_t sign_seed, tq_dtype in_dt, const void *x, int64_t rows, tq_dtype out_dt,
+                      void *out, tq_stream_t stream)
 {
     if (!valid_head_dim(d)) return TQ_ERR_HEAD_DIM;
     if ((in_dt != TQ_BF16 && in_dt != TQ_F32) || (out_dt != TQ_BF16 && out_dt != TQ_F32) || rows < 0) return TQ_ERR_SHAPE;
@@ -219,7 +235,8 @@ tq_status tq_unrotate(int32_t d, tq_dtype in_dt, const void *x, int64_t rows, tq
     if (!x || !out) return TQ_ERR_NULL;
     if (!aligned16(x) || !aligned16(out)) return TQ_ERR_ALIGN;
     if (x == out && in_dt != out_dt) return TQ_ERR_SHAPE;  // in place only with equal element sizes
-    return cuda_status(tq::launch_unrotate(d, in_dt == TQ_F32, x, rows, out_dt == TQ_F32, out, (cudaStream_t)stream));
+    return cuda_status(tq::launch_unrotate(d, sign_bits(sign_seed, d), in_dt == TQ_F32, x, rows, out_dt == TQ_F32, out,
+                                            (cudaStream_t)stream));
 }
 
 tq_status tq_cache_copy_rows(const tq_cache *dst, int64_t dst_t0, const tq_cache *src, int64_t src_t0, int64_t n,
@@ -230,7 +247,7 @@ tq_status tq_cache_copy_rows(const tq_cache *dst, int64_t dst_t0, const tq_cache
     st = check_cache(src);
     if (st != TQ_OK) return st;
     if (dst->head_dim != src->head_dim || dst->k_bits != src->k_bits || dst->v_bits != src->v_bits ||
-        dst->num_kv_heads != src->num_kv_heads || dst->batch != src->batch)
+        dst->num_kv_heads != src->num_kv_heads || dst->batch != src->batch || dst->sign_seed != src->sign_seed)
         return TQ_ERR_SHAPE;
     if (dst_t0 < 0 || src_t0 < 0 || n < 0) return TQ_ERR_SHAPE;
     if (dst_t0 + n > dst->capacity || src_t0 + n > src->capacity) return TQ_ERR_CAPACITY;

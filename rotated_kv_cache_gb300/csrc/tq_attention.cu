@@ -600,6 +600,7 @@ struct CombineParams {
     float *out;  // [B][QH][D]
     int H, QH, G, NB, splits, rows;  // rows = B * QH
     float inv_sqrt_d;
+    SignBits sg;  // value signs
 };
 
 // one warp per (sequence, q-head); lane holds dims 4*lane .. 4*lane+3
@@ -678,9 +679,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int dim = 4 * lane + i;
-        // signs of dims 0..127, two compile-time words per lane quarter
-        const uint32_t word = dim < 32 ? sign_word(0) : dim < 64 ? sign_word(1) : dim < 96 ? sign_word(2) : sign_word(3);
-        const bool neg = (word >> (dim & 31)) & 1u;
+        const bool neg = sign_negative(p.sg, dim);
         rr[i] = x[i] * (neg ? -p.inv_sqrt_d : p.inv_sqrt_d);
     }
     *reinterpret_cast<float4 *>(p.out + ((int64_t)b * p.QH + qh) * kD + 4 * lane) = r;
@@ -735,18 +734,16 @@ int ctas_per_sm_for()
     return cached;
 }
 
+// Launch the split kernel and the combine with a given split plan, the
+// partials in `buf` (at least the plan's bytes; see plan_bytes).
 template <int KB>
-cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
-                          void *ws, size_t ws_bytes, cudaStream_t s)
+cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
+                               void *buf, const SplitPlan &plan, cudaStream_t s)
 {
     using A = AGeo<KB>;
     cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
     if (e != cudaSuccess) return e;
-    const int NB = col_blocks(QH / c.H);
-    const SplitPlan plan = plan_splits(c.B, c.H * NB, seq_len, ctas_per_sm_for<KB>());
-    const size_t need_o = (size_t)c.B * c.H * NB * plan.splits * kG * kD * 4;
-    const size_t need = need_o + (size_t)c.B * c.H * NB * plan.splits * kG * 2 * 4;
-    if (ws_bytes < need) return cudaErrorInvalidValue;
+    const size_t need_o = (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * kD * 4;
 
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
@@ -766,8 +763,8 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     p.v_scale = c.v_scale;
     p.v_codes = c.v_codes;
     p.q = q;
-    p.part_o = static_cast<float *>(ws);
-    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + need_o);
+    p.part_o = static_cast<float *>(buf);
+    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(buf) + need_o);
     p.H = c.H;
     p.QH = QH;
     p.G = QH / c.H;
@@ -810,8 +807,29 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     cp.rows = c.B * QH;
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
+    cp.sg = c.signs;
     attn_combine_kernel<<<cp.rows, kCombineWarps * 32, 0, s>>>(cp);
     return cudaGetLastError();
+}
+
+// Bytes of the split partials of a plan: (d output sums + max + sum) per
+// column of each (sequence, kv-head, column block, split).
+size_t plan_bytes(const CacheView &c, int QH, const SplitPlan &plan)
+{
+    return (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * (kD + 2) * 4;
+}
+
+SplitPlan usual_plan(const CacheView &c, int QH, int64_t seq_len)
+{
+    const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
+    return plan_splits(c.B, c.H * col_blocks(QH / c.H), seq_len, per_sm);
+}
+
+cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
+                          void *buf, const SplitPlan &plan, cudaStream_t s)
+{
+    if (c.kb == 8) return run_attention_plan<8>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    return run_attention_plan<4>(c, q, QH, seq_len, scale, out, buf, plan, s);
 }
 
 }  // namespace
@@ -824,17 +842,15 @@ bool attention_supported(int d, int kb, int vb, int group)
 size_t attention_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)
 {
     if (!attention_supported(c.d, c.kb, c.vb, q_heads / c.H)) return 0;
-    const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
-    const int NB = col_blocks(q_heads / c.H);
-    const SplitPlan plan = plan_splits(c.B, c.H * NB, seq_len, per_sm);
-    return (size_t)c.B * c.H * NB * plan.splits * kG * (kD + 2) * 4;
+    return plan_bytes(c, q_heads, usual_plan(c, q_heads, seq_len));
 }
 
 cudaError_t launch_attention(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
                              float *out, void *ws, size_t ws_bytes, cudaStream_t s)
 {
-    if (c.kb == 8) return run_attention<8>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
-    return run_attention<4>(c, q, q_heads, seq_len, scale, out, ws, ws_bytes, s);
+    const SplitPlan plan = usual_plan(c, q_heads, seq_len);
+    if (ws_bytes < plan_bytes(c, q_heads, plan)) return cudaErrorInvalidValue;
+    return run_attention(c, q, q_heads, seq_len, scale, out, ws, plan, s);
 }
 
 }  // namespace tq
@@ -872,88 +888,11 @@ void *noalloc_scratch_address()
     return g_noalloc_ptr[dev];
 }
 
-template <int KB>
-cudaError_t run_attention_fixed_scratch(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale,
-                                        float *out, void *scratch, const SplitPlan &plan, cudaStream_t s)
-{
-    using A = AGeo<KB>;
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
-    if (e != cudaSuccess) return e;
-    const size_t need_o = (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * kD * 4;
-
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    CUtensorMap map;
-    const cuuint64_t gdim[2] = {(cuuint64_t)A::KROW, (cuuint64_t)c.B * c.H * c.cap};
-    const cuuint64_t gstride[1] = {(cuuint64_t)A::KROW};
-    const cuuint32_t box[2] = {(cuuint32_t)A::KROW, (cuuint32_t)kStageT};
-    const cuuint32_t estride[2] = {1, 1};
-    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k_codes, gdim, gstride, box, estride,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, KB == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-
-    AttnParams p{};
-    p.k_scale = c.k_scale;
-    p.k_zero = c.k_zero;
-    p.v_scale = c.v_scale;
-    p.v_codes = c.v_codes;
-    p.q = q;
-    p.part_o = static_cast<float *>(scratch);
-    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + need_o);
-    p.H = c.H;
-    p.QH = QH;
-    p.G = QH / c.H;
-    p.NB = col_blocks(p.G);
-    p.splits = plan.splits;
-    p.cap = c.cap;
-    p.seq_len = seq_len;
-    p.tokens_per_split = plan.tokens_per_split;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.err = device_error_word();
-    if (!p.err) return cudaErrorInvalidDevice;
-    const Tables &tab = codebook_tables(kVB);
-    uint8_t lo[8], hi[8];
-    for (int i = 0; i < 8; ++i) {
-        const uint16_t hb = __half_as_ushort(__float2half_rn(tab.centroids[i]));
-        lo[i] = (uint8_t)(hb & 0xFF);
-        hi[i] = (uint8_t)(hb >> 8);
-    }
-    p.tl0 = lo[0] | lo[1] << 8 | lo[2] << 16 | (uint32_t)lo[3] << 24;
-    p.tl1 = lo[4] | lo[5] << 8 | lo[6] << 16 | (uint32_t)lo[7] << 24;
-    p.th0 = hi[0] | hi[1] << 8 | hi[2] << 16 | (uint32_t)hi[3] << 24;
-    p.th1 = hi[4] | hi[5] << 8 | hi[6] << 16 | (uint32_t)hi[7] << 24;
-    p.k_const = KB == 8 ? 0xFF00FF00u : 0xFFF0FFF0u;
-    p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
-
-    dim3 grid(plan.splits, c.H * p.NB, c.B);
-    attn_split_kernel<KB><<<grid, kThreads, A::SMEM, s>>>(map, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    CombineParams cp{};
-    cp.part_o = p.part_o;
-    cp.part_ml = p.part_ml;
-    cp.out = out;
-    cp.H = c.H;
-    cp.QH = QH;
-    cp.G = QH / c.H;
-    cp.NB = col_blocks(cp.G);
-    cp.rows = c.B * QH;
-    cp.splits = plan.splits;
-    cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
-    attn_combine_kernel<<<cp.rows, kCombineWarps * 32, 0, s>>>(cp);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
 size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
-bool noalloc_fits(const CacheView &c, int q_heads)
-{
-    return (size_t)c.B * c.H * col_blocks(q_heads / c.H) * kG * (kD + 2) * 4 <= kNoAllocScratchBytes;
-}
+bool noalloc_fits(const CacheView &c, int q_heads) { return plan_bytes(c, q_heads, SplitPlan{1, 0}) <= kNoAllocScratchBytes; }
 
 cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int q_heads, int64_t seq_len, float scale,
                                      float *out, cudaStream_t s)
@@ -961,10 +900,8 @@ cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int 
     void *scratch = noalloc_scratch_address();
     if (!scratch) return cudaErrorInvalidSymbol;
     // the usual split plan, with fewer splits if its partials would not fit
-    const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
-    const int NB = col_blocks(q_heads / c.H);
-    SplitPlan plan = plan_splits(c.B, c.H * NB, seq_len, per_sm);
-    const size_t per_split = (size_t)c.B * c.H * NB * kG * (kD + 2) * 4;
+    SplitPlan plan = usual_plan(c, q_heads, seq_len);
+    const size_t per_split = plan_bytes(c, q_heads, SplitPlan{1, 0});
     const int64_t max_splits = (int64_t)(kNoAllocScratchBytes / per_split);
     if (max_splits < 1) return cudaErrorInvalidValue;
     if (plan.splits > max_splits) {
@@ -972,8 +909,7 @@ cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int 
         const int64_t per = (stages + max_splits - 1) / max_splits;
         plan = SplitPlan{(int)((stages + per - 1) / per), per * kStageT};
     }
-    if (c.kb == 8) return run_attention_fixed_scratch<8>(c, q, q_heads, seq_len, scale, out, scratch, plan, s);
-    return run_attention_fixed_scratch<4>(c, q, q_heads, seq_len, scale, out, scratch, plan, s);
+    return run_attention(c, q, q_heads, seq_len, scale, out, scratch, plan, s);
 }
 
 }  // namespace tq

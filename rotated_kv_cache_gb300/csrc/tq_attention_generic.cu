@@ -11,7 +11,8 @@ namespace tq {
                                               cudaStream_t s);                                                       \
     size_t attention_generic_workspace_d##D(const CacheView &c, int q_heads, int64_t m, int64_t seq_len);             \
     cudaError_t launch_attention_combine_parts_d##D(const float *part_o, const float *part_ml, float *out, int B,    \
-                                                    int H, int QH, int m, int hb, int cb, int splits, cudaStream_t s);
+                                                    int H, int QH, int m, int hb, int cb, int splits,                \
+                                                    const SignBits &sg, cudaStream_t s);
 TQ_DECLARE_GENERIC(64)
 TQ_DECLARE_GENERIC(128)
 TQ_DECLARE_GENERIC(256)
@@ -28,9 +29,10 @@ TQ_DECLARE_GENERIC(512)
     }
 
 cudaError_t launch_attention_combine_parts(int d, const float *part_o, const float *part_ml, float *out, int B, int H,
-                                           int QH, int m, int hb, int cb, int splits, cudaStream_t s)
+                                           int QH, int m, int hb, int cb, int splits, const SignBits &sg,
+                                           cudaStream_t s)
 {
-#define TQ_CALL(D) launch_attention_combine_parts_d##D(part_o, part_ml, out, B, H, QH, m, hb, cb, splits, s)
+#define TQ_CALL(D) launch_attention_combine_parts_d##D(part_o, part_ml, out, B, H, QH, m, hb, cb, splits, sg, s)
     TQ_BY_HEAD_DIM(d, TQ_CALL, cudaErrorInvalidValue)
 #undef TQ_CALL
 }

@@ -648,6 +648,7 @@ struct GenCombineParams {
     float *out;  // [B][M][QH][D]
     int H, QH, G, M, HB, CB, splits, rows;
     float inv_sqrt_d;
+    SignBits sg;  // value signs
 };
 
 // CTAs of gCombineWarps warps; each (sequence, query row, q-head) takes W of
@@ -736,7 +737,7 @@ __global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const
     }
     float *dst = p.out + (int64_t)row * D + PER * lane;
 #pragma unroll
-    for (int k = 0; k < PER; ++k) dst[k] = x[k] * (sign_negative(PER * lane + k) ? -p.inv_sqrt_d : p.inv_sqrt_d);
+    for (int k = 0; k < PER; ++k) dst[k] = x[k] * (sign_negative(p.sg, PER * lane + k) ? -p.inv_sqrt_d : p.inv_sqrt_d);
 }
 
 // ---------------------------------------------------------------- host side
@@ -918,17 +919,17 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     if (e != cudaSuccess) return e;
     const int rows = c.B * (int)m * QH;
     GenCombineParams cp{p.part_o, p.part_ml, out, c.H, QH, G, (int)m, pl.hb, CB, pl.splits, rows,
-                        inv_sqrt_head_dim(D)};
+                        inv_sqrt_head_dim(D), c.signs};
     launch_generic_combine<D>(cp, s);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t combine_parts(const float *part_o, const float *part_ml, float *out, int B, int H, int QH, int m, int hb,
-                          int cb, int splits, cudaStream_t s)
+                          int cb, int splits, const SignBits &sg, cudaStream_t s)
 {
     const int rows = B * m * QH;
-    GenCombineParams cp{part_o, part_ml, out, H, QH, QH / H, m, hb, cb, splits, rows, inv_sqrt_head_dim(D)};
+    GenCombineParams cp{part_o, part_ml, out, H, QH, QH / H, m, hb, cb, splits, rows, inv_sqrt_head_dim(D), sg};
     launch_generic_combine<D>(cp, s);
     return cudaGetLastError();
 }
@@ -950,8 +951,9 @@ cudaError_t combine_parts(const float *part_o, const float *part_ml, float *out,
         return gen_workspace<D>(c, q_heads, m, seq_len);                                                                 \
     }                                                                                                                    \
     cudaError_t launch_attention_combine_parts_d##D(const float *part_o, const float *part_ml, float *out, int B,      \
-                                                    int H, int QH, int m, int hb, int cb, int splits, cudaStream_t s)  \
+                                                    int H, int QH, int m, int hb, int cb, int splits,                  \
+                                                    const SignBits &sg, cudaStream_t s)                                \
     {                                                                                                                    \
-        return combine_parts<D>(part_o, part_ml, out, B, H, QH, m, hb, cb, splits, s);                                   \
+        return combine_parts<D>(part_o, part_ml, out, B, H, QH, m, hb, cb, splits, sg, s);                               \
     }                                                                                                                    \
     }

@@ -13,7 +13,7 @@
 //
 // Design.  A CTA is two warpgroups; each owns 128 columns of one kv-head
 // (the MMA's M = 128, one column per tensor-memory lane and per thread) and
-// the CTA streams the kv-head's rows of one split in 64-row stages:
+// the CTA streams the kv-head's rows of one split in 128-row stages:
 //  1. one thread keeps two packed stages in flight with bulk copies
 //     completing on mbarriers;
 //  2. all 256 threads dequantise the stage into shared memory as f16 MMA
@@ -26,9 +26,10 @@
 //     finite rms, undone on the output;
 //  3. one thread issues S = Q K^T (hi and lo into one accumulator) for both
 //     warpgroups into tensor memory and commits to per-warpgroup mbarriers;
-//  4. each thread reads its column's 64 scores (tcgen05.ld), applies the
-//     causal limit, runs the online base-2 softmax in registers and writes
-//     its row of P (f16) over its scores in tensor memory (tcgen05.st);
+//  4. each thread reads its column's 128 scores (tcgen05.ld, 32 at a time,
+//     twice: the maximum, then the weights), applies the causal limit,
+//     runs the online base-2 softmax in registers and writes its row of P
+//     (f16) over its scores in tensor memory (tcgen05.st);
 //  5. the warpgroup's first thread issues O_stage = P V into tensor memory
 //     (A operand from tensor memory, so P never touches shared memory);
 //     each thread adds its row of O_stage into its register accumulator,
@@ -668,7 +669,8 @@ cudaError_t tc_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, int
     attn_tc_kernel<D, KB, VB><<<dim3(pl.splits, c.H * pl.hb, c.B), tcThreads, pl.smem, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, (int)m, pl.hb, tcCB, pl.splits, s);
+    return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, (int)m, pl.hb, tcCB, pl.splits,
+                                          c.signs, s);
 }
 
 // compile-time code widths for the common schemes, run-time ones otherwise

@@ -5,34 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "tq_kernels.h"
+
 namespace tq {
-
-// ---------------------------------------------------------------- constants
-constexpr uint64_t kSignSeed = 42;  // value signs: SplitMix64 seeded with 42
-
-// Output i of SplitMix64 started at `seed` (Steele, Lea & Flood, OOPSLA 2014).
-__host__ __device__ constexpr uint64_t splitmix64(uint64_t seed, uint64_t i)
-{
-    uint64_t z = seed + (i + 1u) * 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
-}
-
-// Value sign i is -1 when the top bit of output i is set.  Called with
-// compile-time indices inside fully unrolled loops, so it folds to a constant.
-__host__ __device__ constexpr bool sign_negative(int i) { return (splitmix64(kSignSeed, (uint64_t)i) >> 63) != 0; }
-
-__host__ __device__ constexpr float sign_value(int i) { return sign_negative(i) ? -1.0f : 1.0f; }
-
-// 32 sign bits of elements [32w, 32w+32) (bit k = element 32w+k is negative).
-__host__ __device__ constexpr uint32_t sign_word(int w)
-{
-    uint32_t m = 0;
-    for (int k = 0; k < 32; ++k)
-        if (sign_negative(32 * w + k)) m |= 1u << k;
-    return m;
-}
 
 // Device error word codes (see tq_device_error()).
 constexpr uint32_t kErrWaitTimeout = 1u;

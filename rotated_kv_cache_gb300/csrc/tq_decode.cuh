@@ -115,6 +115,7 @@ struct ValueDecodeParams {
     uint32_t tiles_per_bh, items;  // items < 2^31
     FastDiv div_tiles;
     float inv_sqrt_d;
+    SignBits sg;  // value signs
     float cen[256];
 };
 
@@ -152,8 +153,8 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
         // elements of P[j] after the transform, and the sign the d128 form leaves on the second
         const int e0 = D == 128 ? 32 * part + j : 64 * part + j, e1 = D == 128 ? 64 + 32 * part + j : e0 + 32;
         const float n1 = D == 128 && part ? -1.0f : 1.0f;
-        smul[part][j] = make_float2(sign_negative(e0) ? -p.inv_sqrt_d : p.inv_sqrt_d,
-                                    n1 * (sign_negative(e1) ? -p.inv_sqrt_d : p.inv_sqrt_d));
+        smul[part][j] = make_float2(sign_negative(p.sg, e0) ? -p.inv_sqrt_d : p.inv_sqrt_d,
+                                    n1 * (sign_negative(p.sg, e1) ? -p.inv_sqrt_d : p.inv_sqrt_d));
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -296,6 +297,7 @@ cudaError_t run_value(const CacheView &c, int64_t t0, int64_t n, void *out, cuda
     p.items = (uint32_t)items;
     p.div_tiles = make_fastdiv(tiles > 0 ? (uint32_t)tiles : 1u);
     p.inv_sqrt_d = inv_sqrt_head_dim(D);
+    p.sg = c.signs;
     const Tables &tab = codebook_tables(VB);
     for (int i = 0; i < (1 << VB); ++i) p.cen[i] = tab.centroids[i];
     auto kern = decode_value_kernel<D, VB, F32>;

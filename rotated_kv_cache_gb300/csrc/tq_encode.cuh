@@ -68,6 +68,7 @@ struct EncodeParams {
     uint32_t tiles_per_bh, items;  // items < 2^31
     FastDiv div_tiles, div_h;      // x / tiles_per_bh, x / H
     float inv_sqrt_d;
+    SignBits sg;  // value signs
     uint32_t *err;
     int use_tma;     // tiles arrive by tensor copies of the map (else one bulk copy per row)
     float bnd[255];  // value boundaries (ascending)
@@ -543,8 +544,8 @@ __device__ __forceinline__ void encode_body(const EncodeParams &p, const CUtenso
             const int part = i >> 4, k = i & 15;
             // at head_dim 128 part-1 lanes hold swapped pairs (element j + 32, element j)
             const int e = 64 * part + 2 * k + (D == 128 && part ? 32 : 0), f = D == 128 && part ? e - 32 : e + 32;
-            const uint4 m = make_uint4(sign_negative(e) ? 0x80000000u : 0u, sign_negative(e + 1) ? 0x80000000u : 0u,
-                                       sign_negative(f) ? 0x80000000u : 0u, sign_negative(f + 1) ? 0x80000000u : 0u);
+            const uint4 m = make_uint4(sign_negative(p.sg, e) ? 0x80000000u : 0u, sign_negative(p.sg, e + 1) ? 0x80000000u : 0u,
+                                       sign_negative(p.sg, f) ? 0x80000000u : 0u, sign_negative(p.sg, f + 1) ? 0x80000000u : 0u);
             *reinterpret_cast<uint4 *>(mtab + part * 272 + 16 * k) = m;
         }
     }
@@ -743,6 +744,7 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     p.t0 = t0;
     p.n = n;
     p.inv_sqrt_d = inv_sqrt_head_dim(D);
+    p.sg = c.signs;
     p.err = device_error_word();
     if (!p.err) return cudaErrorInvalidDevice;
     const Tables &tab = codebook_tables(c.vb);

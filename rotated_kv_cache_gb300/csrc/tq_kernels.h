@@ -7,6 +7,33 @@
 
 namespace tq {
 
+// Output i of SplitMix64 started at `seed` (Steele, Lea & Flood, OOPSLA 2014).
+__host__ __device__ constexpr uint64_t splitmix64(uint64_t seed, uint64_t i)
+{
+    uint64_t z = seed + (i + 1u) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// The value sign vector of one cache as bits (bit e % 32 of word e / 32 set
+// when sign e is -1): sign e is -1 when the top bit of SplitMix64 output e of
+// the cache's seed is set.  Built on the host once per call and passed to the
+// kernels by value (head_dim <= 512).
+struct SignBits {
+    uint32_t w[16];
+};
+
+inline SignBits make_sign_bits(uint64_t seed, int d)
+{
+    SignBits s{};
+    for (int e = 0; e < d; ++e)
+        if (splitmix64(seed, (uint64_t)e) >> 63) s.w[e >> 5] |= 1u << (e & 31);
+    return s;
+}
+
+__host__ __device__ __forceinline__ bool sign_negative(const SignBits &s, int e) { return (s.w[e >> 5] >> (e & 31)) & 1u; }
+
 struct CacheView {
     int d, kb, vb, H, B;
     int64_t cap;
@@ -14,6 +41,7 @@ struct CacheView {
     uint16_t *k_scale, *k_zero;
     uint8_t *v_codes;
     uint16_t *v_scale;
+    SignBits signs;  // the cache's value sign vector
 };
 
 struct Tables {
@@ -55,7 +83,8 @@ cudaError_t launch_attention_generic(const CacheView &c, const uint16_t *q, int 
 // Merge split partials (o, m, l) laid out [B][H][hb][splits][cb][d] (+ [..][cb][2])
 // into out [B][m][QH][d]: log-sum-exp over splits, then the inverse rotation.
 cudaError_t launch_attention_combine_parts(int d, const float *part_o, const float *part_ml, float *out, int B, int H,
-                                           int QH, int m, int hb, int cb, int splits, cudaStream_t s);
+                                           int QH, int m, int hb, int cb, int splits, const SignBits &sg,
+                                           cudaStream_t s);
 
 // Multi-token attention on the tcgen05 tensor cores: head_dim 64 or 128 with
 // at least 128 (query row, q-head) columns per kv-head.
@@ -66,7 +95,8 @@ cudaError_t launch_attention_tc(const CacheView &c, const uint16_t *q, int q_hea
 
 // Deferred fetch, un-rotation and cache row copy / clear (src null: zeros).
 cudaError_t launch_decode_rotated(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out, cudaStream_t s);
-cudaError_t launch_unrotate(int d, bool in_f32, const void *x, int64_t rows, bool out_f32, void *out, cudaStream_t s);
+cudaError_t launch_unrotate(int d, const SignBits &sg, bool in_f32, const void *x, int64_t rows, bool out_f32, void *out,
+                            cudaStream_t s);
 cudaError_t launch_copy_rows(const CacheView &dst, int64_t dst_t0, const CacheView *src, int64_t src_t0, int64_t n,
                              cudaStream_t s);
 

@@ -111,6 +111,7 @@ struct UnrotParams {
     int64_t rows;
     uint32_t items;  // warp tiles, < 2^31
     float inv_sqrt_d;
+    SignBits sg;  // value signs
 };
 
 template <int D, bool IN_F32, bool OUT_F32>
@@ -120,8 +121,8 @@ __global__ void __launch_bounds__(kUWarps * 32) unrotate_kernel(const __grid_con
     __shared__ __align__(16) float2 smul[LPR][34];  // (+-1/sqrt d) of elements (j, j+32) of each part, padded
     for (int i = threadIdx.x; i < LPR * 32; i += blockDim.x) {
         const int part = i >> 5, j = i & 31, e = 64 * part + j;
-        smul[part][j] = make_float2(sign_negative(e) ? -p.inv_sqrt_d : p.inv_sqrt_d,
-                                    sign_negative(e + 32) ? -p.inv_sqrt_d : p.inv_sqrt_d);
+        smul[part][j] = make_float2(sign_negative(p.sg, e) ? -p.inv_sqrt_d : p.inv_sqrt_d,
+                                    sign_negative(p.sg, e + 32) ? -p.inv_sqrt_d : p.inv_sqrt_d);
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -196,12 +197,12 @@ __global__ void __launch_bounds__(kUWarps * 32) unrotate_kernel(const __grid_con
 }
 
 template <int D, bool IN_F32, bool OUT_F32>
-cudaError_t run_unrotate(const void *x, int64_t rows, void *out, cudaStream_t s)
+cudaError_t run_unrotate(const SignBits &sg, const void *x, int64_t rows, void *out, cudaStream_t s)
 {
     constexpr int ROWS = 32 / (D / 64);
     const int64_t items = (rows + ROWS - 1) / ROWS;
     if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
-    UnrotParams p{x, out, rows, (uint32_t)items, inv_sqrt_head_dim(D)};
+    UnrotParams p{x, out, rows, (uint32_t)items, inv_sqrt_head_dim(D), sg};
     auto kern = unrotate_kernel<D, IN_F32, OUT_F32>;
     static int per_sm = 0;
     if (!per_sm) {
@@ -216,10 +217,12 @@ cudaError_t run_unrotate(const void *x, int64_t rows, void *out, cudaStream_t s)
 }
 
 template <int D>
-cudaError_t unrotate_d(bool in_f32, bool out_f32, const void *x, int64_t rows, void *out, cudaStream_t s)
+cudaError_t unrotate_d(const SignBits &sg, bool in_f32, bool out_f32, const void *x, int64_t rows, void *out,
+                       cudaStream_t s)
 {
-    if (in_f32) return out_f32 ? run_unrotate<D, true, true>(x, rows, out, s) : run_unrotate<D, true, false>(x, rows, out, s);
-    return out_f32 ? run_unrotate<D, false, true>(x, rows, out, s) : run_unrotate<D, false, false>(x, rows, out, s);
+    if (in_f32)
+        return out_f32 ? run_unrotate<D, true, true>(sg, x, rows, out, s) : run_unrotate<D, true, false>(sg, x, rows, out, s);
+    return out_f32 ? run_unrotate<D, false, true>(sg, x, rows, out, s) : run_unrotate<D, false, false>(sg, x, rows, out, s);
 }
 
 // ------------------------------------------------------------------ row copy / clear
@@ -265,13 +268,14 @@ cudaError_t launch_decode_rotated(const CacheView &c, int64_t t0, int64_t n, boo
     return f32 ? rotated_vb<true>(c, t0, n, out, s) : rotated_vb<false>(c, t0, n, out, s);
 }
 
-cudaError_t launch_unrotate(int d, bool in_f32, const void *x, int64_t rows, bool out_f32, void *out, cudaStream_t s)
+cudaError_t launch_unrotate(int d, const SignBits &sg, bool in_f32, const void *x, int64_t rows, bool out_f32, void *out,
+                            cudaStream_t s)
 {
     switch (d) {
-    case 64: return unrotate_d<64>(in_f32, out_f32, x, rows, out, s);
-    case 128: return unrotate_d<128>(in_f32, out_f32, x, rows, out, s);
-    case 256: return unrotate_d<256>(in_f32, out_f32, x, rows, out, s);
-    case 512: return unrotate_d<512>(in_f32, out_f32, x, rows, out, s);
+    case 64: return unrotate_d<64>(sg, in_f32, out_f32, x, rows, out, s);
+    case 128: return unrotate_d<128>(sg, in_f32, out_f32, x, rows, out, s);
+    case 256: return unrotate_d<256>(sg, in_f32, out_f32, x, rows, out, s);
+    case 512: return unrotate_d<512>(sg, in_f32, out_f32, x, rows, out, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -41,6 +41,9 @@ def test_bytes_per_token_head_matches_oracle(tqlib):
 def test_sign_vector_matches_oracle(tqlib):
     for d in tqlib.HEAD_DIMS:
         assert np.array_equal(tqlib.tq_sign_vector(d), oracle.sign_vector(d))
+        for seed in (0, 7, 2**64 - 1):
+            assert np.array_equal(tqlib.tq_sign_vector(d, seed), oracle.sign_vector(d, seed))
+    assert not np.array_equal(tqlib.tq_sign_vector(128, 7), tqlib.tq_sign_vector(128))
 
 
 @pytest.mark.parametrize("vb", [2, 3, 4, 5, 8])
@@ -55,7 +58,7 @@ def test_codebook_bit_identical_to_oracle(tqlib, vb):
 
 def _struct(tqlib, **kw):
     f = dict(head_dim=128, k_bits=8, v_bits=3, num_kv_heads=2, batch=1, reserved=0, capacity=32,
-             k_codes=0x1000, k_scale=0x2000, k_zero=0x3000, v_codes=0x4000, v_scale=0x5000)
+             k_codes=0x1000, k_scale=0x2000, k_zero=0x3000, v_codes=0x4000, v_scale=0x5000, sign_seed=42)
     f.update(kw)
     return tqlib._CacheStruct(*[f[n] for n, _ in tqlib._CacheStruct._fields_])
 
@@ -121,16 +124,18 @@ def test_lifecycle_and_deferred_refusals(tqlib):
     assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 1, None, None) == S["TQ_ERR_NULL"]
     assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 1, 0x10008, None) == S["TQ_ERR_ALIGN"]
     assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 0, 1, None, None) == S["TQ_OK"]
-    assert L.tq_unrotate(96, 1, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_HEAD_DIM"]
-    assert L.tq_unrotate(128, 2, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
-    assert L.tq_unrotate(128, 1, 0x10000, -1, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
-    assert L.tq_unrotate(128, 1, 0x10000, 4, 0, 0x10000, None) == S["TQ_ERR_SHAPE"]  # in place, different sizes
-    assert L.tq_unrotate(128, 1, 0x10004, 4, 1, 0x20000, None) == S["TQ_ERR_ALIGN"]
-    assert L.tq_unrotate(128, 1, None, 4, 1, 0x20000, None) == S["TQ_ERR_NULL"]
-    assert L.tq_unrotate(128, 1, None, 0, 1, None, None) == S["TQ_OK"]
+    assert L.tq_unrotate(96, 42, 1, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_HEAD_DIM"]
+    assert L.tq_unrotate(128, 42, 2, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_unrotate(128, 42, 1, 0x10000, -1, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
+    assert L.tq_unrotate(128, 42, 1, 0x10000, 4, 0, 0x10000, None) == S["TQ_ERR_SHAPE"]  # in place, different sizes
+    assert L.tq_unrotate(128, 42, 1, 0x10004, 4, 1, 0x20000, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_unrotate(128, 42, 1, None, 4, 1, 0x20000, None) == S["TQ_ERR_NULL"]
+    assert L.tq_unrotate(128, 42, 1, None, 0, 1, None, None) == S["TQ_OK"]
     big = _struct(tqlib, capacity=64)
     other = _struct(tqlib, head_dim=64)
     assert L.tq_cache_copy_rows(ctypes.byref(c), 0, ctypes.byref(other), 0, 4, None) == S["TQ_ERR_SHAPE"]
+    reseeded = _struct(tqlib, sign_seed=7)  # rows of another sign vector cannot be mixed in
+    assert L.tq_cache_copy_rows(ctypes.byref(c), 0, ctypes.byref(reseeded), 0, 4, None) == S["TQ_ERR_SHAPE"]
     assert L.tq_cache_copy_rows(ctypes.byref(c), 30, ctypes.byref(b), 0, 4, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_cache_copy_rows(ctypes.byref(c), 0, ctypes.byref(big), 40, 30, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_cache_copy_rows(ctypes.byref(a), 4, ctypes.byref(b), 0, 8, None) == S["TQ_ERR_SHAPE"]  # overlap

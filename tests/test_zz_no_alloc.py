@@ -1,13 +1,16 @@
 """tq_decode_attention_noalloc (decode attention with the library's own fixed
 scratch, for callers that cannot allocate device memory) against
-tq_decode_attention on the same cache and queries.
+tq_decode_attention on the same cache and queries, and against the oracle on
+a sampled (sequence, kv-head) pair where the split plan is the reduced one.
 
-Collected last on purpose: the scratch is shared process state, so this file
-checks it both in a fresh process and after every other test has run.  Each
-case makes two calls in a row with different queries, so a second call that
-read the first call's partials would show.  Tolerance: the attention tests'
-2e-3 max-abs (both entry points run the same kernels, so the outputs agree far
-more closely unless the split count differs).
+Collected last on purpose: the scratch is shared process state, so a run of
+the whole suite exercises it after every other test.  Run on its own
+(``pytest tests/test_zz_no_alloc.py``) the first call of the file is the
+process's first, which covers the scratch address lookup on a fresh context.
+Each case makes two calls in a row with different queries, so a second call
+that read the first call's partials would show.  Tolerance: the attention
+tests' 2e-3 max-abs (both entry points run the same kernels, so the outputs
+agree far more closely unless the split count differs).
 """
 import ctypes
 
@@ -15,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import tq_synth
 from tqtest import to_device_bf16
 
@@ -41,6 +45,17 @@ def _two_calls_match(tq, cache, qs, T):
         err = (g - want).abs().max().item()
         assert err < TOL, err
     assert tq.tq_device_error() == 0
+    return got
+
+
+def _oracle_pair(cache, q, T, b, h, G):
+    """The oracle's attention for sequence b, kv-head h (its G q-heads), on the
+    packed rows read back from the device."""
+    p = oracle.Planes(1, 1, cache.head_dim, cache.k_bits, cache.v_bits, cache.capacity, sign_seed=cache.sign_seed)
+    for dst, src in zip(p.arrays(), cache.planes()):
+        dst[0, 0] = src[b, h].cpu().numpy().view(dst.dtype)
+    qb = q[b:b + 1, h * G:(h + 1) * G].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return oracle.attention(p, qb, T)[0]
 
 
 @pytest.mark.gpu
@@ -68,19 +83,21 @@ def test_noalloc_group_of_four(cuda):
 
 
 @pytest.mark.gpu
-def test_noalloc_fewer_splits_than_usual(cuda):
+@pytest.mark.parametrize("kb", [8, 4])
+def test_noalloc_fewer_splits_than_usual(cuda, kb):
     """8 kv-heads x 8193 rows and the smallest batch (64 to 512 sequences) whose
     usual split plan needs more than the 16 MiB scratch, so this entry point
-    runs with fewer splits."""
+    runs with fewer splits; both key widths (their kernels differ in CTAs per
+    SM, hence in split plans)."""
     w = tq_synth.WORKLOADS["decode"]
     H, T = 8, 8193
 
     def usual_workspace(B):  # the size query reads no device memory
-        s = cuda._CacheStruct(w.d, 8, w.vb, H, B, 0, T + 15, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+        s = cuda._CacheStruct(w.d, kb, w.vb, H, B, 0, T + 15, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
         return cuda.lib().tq_attention_workspace_bytes(ctypes.byref(s), 8 * H, T)
 
     B = next(b for b in (64, 128, 256, 512) if usual_workspace(b) > SCRATCH_BYTES)
-    cache = cuda.Cache(B, H, w.d, T, k_bits=8, v_bits=w.vb)
+    cache = cuda.Cache(B, H, w.d, T, k_bits=kb, v_bits=w.vb)
     assert cuda.tq_attention_workspace_bytes(cache, 8 * H, T) > SCRATCH_BYTES
     for b0 in range(0, B, 64):
         nb = min(64, B - b0)
@@ -94,7 +111,12 @@ def test_noalloc_fewer_splits_than_usual(cuda):
         q = torch.empty((B, 8 * H, w.d), dtype=torch.int16, device="cuda")
         tq_synth.device_q(w, step, q, B=B, QH=8 * H)
         qs.append(q.view(torch.bfloat16))
-    _two_calls_match(cuda, cache, qs, T)
+    got = _two_calls_match(cuda, cache, qs, T)
+    b, h = B - 3, 5  # one sampled pair, checked against the oracle for both calls
+    for q, g in zip(qs, got):
+        want = _oracle_pair(cache, q, T, b, h, 8)
+        err = np.abs(g[b, 8 * h:8 * h + 8].cpu().numpy().astype(np.float64) - want).max()
+        assert err < TOL, err
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(tqlib):
@@ -105,19 +127,19 @@ def test_noalloc_rejects_problems_beyond_the_scratch(tqlib):
                                      "TQ_ERR_CAPACITY", "TQ_ERR_ALIGN", "TQ_ERR_WORKSPACE", "TQ_ERR_CUDA",
                                      "TQ_ERR_UNSUPPORTED", "TQ_ERR_SCRATCH"])}
     def status(B, H):
-        s = tqlib._CacheStruct(128, 8, 3, H, B, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+        s = tqlib._CacheStruct(128, 8, 3, H, B, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
         return L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8 * H, 16, 1.0, 0x20000, None)
     assert status(4033, 1) == S["TQ_ERR_SCRATCH"]
     assert status(1, 4033) == S["TQ_ERR_SCRATCH"]
     assert status(37, 109) == S["TQ_ERR_SCRATCH"]  # 4033 units
     assert "16 MiB" in L.tq_status_string(S["TQ_ERR_SCRATCH"]).decode()
     # the usual argument checks still come first
-    s = tqlib._CacheStruct(128, 8, 3, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+    s = tqlib._CacheStruct(128, 8, 3, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
     assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 17, 1.0, 0x20000, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 16, 1.0, 0x20004, None) == S["TQ_ERR_ALIGN"]
     # value widths other than 3 bits are outside the specialised kernel
-    s2 = tqlib._CacheStruct(128, 8, 2, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+    s2 = tqlib._CacheStruct(128, 8, 2, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
     assert L.tq_decode_attention_noalloc(ctypes.byref(s2), 0x10000, 8, 16, 1.0, 0x20000, None) == S["TQ_ERR_UNSUPPORTED"]
     # a group of 16 takes two column blocks: 2016 sequence-heads already overflow
-    s3 = tqlib._CacheStruct(128, 8, 3, 1, 2017, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+    s3 = tqlib._CacheStruct(128, 8, 3, 1, 2017, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
     assert L.tq_decode_attention_noalloc(ctypes.byref(s3), 0x10000, 16, 16, 1.0, 0x20000, None) == S["TQ_ERR_SCRATCH"]

@@ -11,7 +11,8 @@ def to_device_bf16(bits: np.ndarray):
 
 
 def planes_from_device(cache) -> "oracle.Planes":
-    p = oracle.Planes(cache.batch, cache.num_kv_heads, cache.head_dim, cache.k_bits, cache.v_bits, cache.capacity)
+    p = oracle.Planes(cache.batch, cache.num_kv_heads, cache.head_dim, cache.k_bits, cache.v_bits, cache.capacity,
+                      sign_seed=cache.sign_seed)
     p.k_codes[...] = cache.k_codes.cpu().numpy()
     p.k_scale[...] = cache.k_scale.cpu().numpy().view(np.uint16)
     p.k_zero[...] = cache.k_zero.cpu().numpy().view(np.uint16)
@@ -49,6 +50,7 @@ def compare_value_codes(gpu: "oracle.Planes", ref: "oracle.Planes", v_bits_f32: 
     the exemption, exempt mismatches)."""
     d, vb = ref.d, ref.vb
     bnd = oracle.codebook(vb)[1].astype(np.float64)
+    signs = oracle.sign_vector(d, ref.sign_seed)
     bad = exempt = 0
     for (b, h, t) in rows:
         g = gpu.v_codes[b, h, t0 + t]
@@ -56,7 +58,7 @@ def compare_value_codes(gpu: "oracle.Planes", ref: "oracle.Planes", v_bits_f32: 
         if np.array_equal(g, r):
             continue
         gi, ri = value_indices(g, d, vb), value_indices(r, d, vb)
-        _, _, yn = oracle.value_row(v_bits_f32[b, h, t], vb)
+        _, _, yn = oracle.value_row(v_bits_f32[b, h, t], vb, signs=signs)
         near = np.min(np.abs(yn.astype(np.float64)[:, None] - bnd[None, :]), axis=1) < 1e-5
         diff = gi != ri
         exempt += int(np.sum(diff & near))
