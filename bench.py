@@ -423,7 +423,9 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * ab["total"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                 "pipelined": "copy-in, compute and copy-out streams overlap neighbouring steps (2 buffer sets)"},
-        "gpu_launches": 8 * K,
+        # per step: prefill append (key and value kernels), fetch (one kernel for keys
+        # and values), single-token append (one kernel), attention (split + combine)
+        "gpu_launches": 6 * K,
         "clocks": clocks.summary(),
     }
     return line
@@ -905,6 +907,58 @@ def run_sweep(only=None):
         emit("clear_rows", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": 8, "vb": 3}, us, B * H * T * 200)
 
 
+PROFILE_CASES = {
+    # name: (operation, head_dim, k_bits, v_bits, batch, kv-heads, rows, q-heads per kv-head)
+    "prefill_codec": ("codec", 128, 8, 3, 4, 8, 8192, 0),
+    "decode_attention_b2": ("attention", 128, 8, 3, 2, 8, 32769, 8),
+    "long_context_attention_b2": ("attention", 128, 4, 3, 2, 8, 131073, 8),
+    "sweep_codec_d64_k8v3": ("codec", 64, 8, 3, 1, 8, 16384, 0),
+    "sweep_codec_d512_k4v3": ("codec", 512, 4, 3, 1, 8, 16384, 0),
+    "generic_attention_d256_k8v3_b4": ("attention", 256, 8, 3, 4, 8, 32769, 8),
+    "generic_attention_d64_k8v3_b8": ("attention", 64, 8, 3, 8, 8, 32769, 8),
+    "generic_attention_d128_k8v4_b4": ("attention", 128, 8, 4, 4, 8, 32769, 8),
+}
+
+
+def run_profile_case(name: str, reps: int) -> None:
+    """One small workload for a profiler capture: the cache (and inputs) are
+    built, then the operation runs `reps` times (codec: encode then fetch to
+    bf16; attention: one decode step's attention).  Prints nothing timed."""
+    import torch
+
+    from rotated_kv_cache_gb300 import build as libbuild
+
+    libbuild.build()
+    import rotated_kv_cache_gb300 as tq
+    import tq_synth
+
+    op, d, kb, vb, B, H, T, G = PROFILE_CASES[name]
+    w = tq_synth.WORKLOADS["prefill" if op == "codec" and d == 128 else "sweep" if op == "codec" else "decode"]
+    dev = torch.device("cuda", 0)
+    cache = tq.Cache(B, H, d, T, kb, vb, device=dev)
+    k = torch.empty((B, H, T, d), dtype=torch.int16, device=dev)
+    v = torch.empty_like(k)
+    tq_synth.device_kv(w, k, v, B=B, H=H, d=d, n=T)
+    k16, v16 = k.view(torch.bfloat16), v.view(torch.bfloat16)
+    tq.tq_encode_append(cache, k16, v16, 0)
+    if op == "codec":
+        ko, vo = torch.empty_like(k16), torch.empty_like(v16)
+        for _ in range(reps):
+            tq.tq_encode_append(cache, k16, v16, 0)
+            tq.tq_decode(cache, 0, T, dtype=torch.bfloat16, k_out=ko, v_out=vo)
+    else:
+        del k, v, k16, v16
+        q = torch.empty((B, G * H, d), dtype=torch.int16, device=dev)
+        tq_synth.device_q(w, 0, q, B=B, QH=G * H, d=d)
+        out = torch.empty((B, G * H, d), dtype=torch.float32, device=dev)
+        ws = torch.empty(tq.tq_attention_workspace_bytes(cache, G * H, T), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            tq.tq_decode_attention(cache, q.view(torch.bfloat16), T, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert tq.tq_device_error() == 0
+    print(json.dumps({"profile_case": name, "reps": reps, "ok": True}), flush=True)
+
+
 def free_port() -> int:
     import socket
 
@@ -937,7 +991,13 @@ def main():
     ap.add_argument("--only", default="",
                     help="with --sweep: comma-separated kinds to run (attention, long_context_attention, "
                          "multi_token_attention, rotated_fetch, unrotate, copy_rows, clear_rows)")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                    help="run one small workload `--reps` times for a profiler capture (no timing)")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.reps)
+        return
     if args.sweep:
         run_sweep(set(filter(None, args.only.split(","))))
         return

@@ -55,6 +55,38 @@ __device__ __forceinline__ void magic_codes(const uint32_t (&w)[KB], uint32_t (&
     }
 }
 
+// One key group: codes w (KB words), fp16 scale and zero -> 32 outputs at dst
+// ((code + zero) * scale in fp32, then bf16 by round to nearest even).
+template <int KB, bool F32>
+__device__ __forceinline__ void key_group_out(const uint32_t (&w)[KB], float s, float z, void *dst)
+{
+    // 1.5*2^23 + u - (1.5*2^23 + bias - zero) = idx + zero, exactly
+    const float zz = __fsub_rn(KB == 8 ? 12583040.0f : 12582912.0f, z);
+    uint32_t m[32];
+    magic_codes<KB>(w, m);
+    const float2 nz2 = make_float2(-zz, -zz), s2 = make_float2(s, s);
+    float2 x[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        x[k] = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(m[2 * k]), __uint_as_float(m[2 * k + 1])), nz2), s2);
+    if constexpr (F32) {
+        float *d = static_cast<float *>(dst);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            st_global_v8(d + 8 * j, __float_as_uint(x[4 * j].x), __float_as_uint(x[4 * j].y), __float_as_uint(x[4 * j + 1].x),
+                         __float_as_uint(x[4 * j + 1].y), __float_as_uint(x[4 * j + 2].x), __float_as_uint(x[4 * j + 2].y),
+                         __float_as_uint(x[4 * j + 3].x), __float_as_uint(x[4 * j + 3].y));
+    } else {
+        uint16_t *d = static_cast<uint16_t *>(dst);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            st_global_v8(d + 16 * j, pack_bf16x2(x[8 * j].x, x[8 * j].y), pack_bf16x2(x[8 * j + 1].x, x[8 * j + 1].y),
+                         pack_bf16x2(x[8 * j + 2].x, x[8 * j + 2].y), pack_bf16x2(x[8 * j + 3].x, x[8 * j + 3].y),
+                         pack_bf16x2(x[8 * j + 4].x, x[8 * j + 4].y), pack_bf16x2(x[8 * j + 5].x, x[8 * j + 5].y),
+                         pack_bf16x2(x[8 * j + 6].x, x[8 * j + 6].y), pack_bf16x2(x[8 * j + 7].x, x[8 * j + 7].y));
+    }
+}
+
 template <int KB, bool F32>
 __global__ void __launch_bounds__(256) decode_key_kernel(const __grid_constant__ KeyDecodeParams p)
 {
@@ -68,32 +100,8 @@ __global__ void __launch_bounds__(256) decode_key_kernel(const __grid_constant__
         load_words<KB, A>(p.codes + row0 * (p.d * KB / 8) + gi * (4 * KB), w);
         const int64_t mi = row0 * (p.d / 32) + gi;
         const float s = f16_bits_to_f32(p.scale[mi]), z = f16_bits_to_f32(p.zero[mi]);
-        // 1.5*2^23 + u - (1.5*2^23 + bias - zero) = idx + zero, exactly
-        const float zz = __fsub_rn(KB == 8 ? 12583040.0f : 12582912.0f, z);
-        uint32_t m[32];
-        magic_codes<KB>(w, m);
-        const float2 nz2 = make_float2(-zz, -zz), s2 = make_float2(s, s);
-        float2 x[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            x[k] = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(m[2 * k]), __uint_as_float(m[2 * k + 1])), nz2), s2);
         const int64_t o = bh * p.n * p.d + gi * 32;  // whole 32-byte sectors per store
-        if constexpr (F32) {
-            float *dst = static_cast<float *>(p.out) + o;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                st_global_v8(dst + 8 * j, __float_as_uint(x[4 * j].x), __float_as_uint(x[4 * j].y), __float_as_uint(x[4 * j + 1].x),
-                             __float_as_uint(x[4 * j + 1].y), __float_as_uint(x[4 * j + 2].x), __float_as_uint(x[4 * j + 2].y),
-                             __float_as_uint(x[4 * j + 3].x), __float_as_uint(x[4 * j + 3].y));
-        } else {
-            uint16_t *dst = static_cast<uint16_t *>(p.out) + o;
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-                st_global_v8(dst + 16 * j, pack_bf16x2(x[8 * j].x, x[8 * j].y), pack_bf16x2(x[8 * j + 1].x, x[8 * j + 1].y),
-                             pack_bf16x2(x[8 * j + 2].x, x[8 * j + 2].y), pack_bf16x2(x[8 * j + 3].x, x[8 * j + 3].y),
-                             pack_bf16x2(x[8 * j + 4].x, x[8 * j + 4].y), pack_bf16x2(x[8 * j + 5].x, x[8 * j + 5].y),
-                             pack_bf16x2(x[8 * j + 6].x, x[8 * j + 6].y), pack_bf16x2(x[8 * j + 7].x, x[8 * j + 7].y));
-        }
+        key_group_out<KB, F32>(w, s, z, static_cast<uint8_t *>(p.out) + o * (F32 ? 4 : 2));
     }
 }
 
@@ -110,6 +118,11 @@ struct ValueDecodeParams {
     const uint8_t *codes;
     const uint16_t *scale;
     void *out;
+    // keys of the same rows, fetched by the same warps (k_out null: values only)
+    const uint8_t *k_codes;
+    const uint16_t *k_scale, *k_zero;
+    void *k_out;
+    int kb;
     int H;
     int64_t cap, t0, n;
     uint32_t tiles_per_bh, items;  // items < 2^31
@@ -141,8 +154,86 @@ __device__ __forceinline__ void load_value_lane(const ValueDecodeParams &p, int6
     sc = *reinterpret_cast<const uint32_t *>(p.scale + crow * (D / 32) + 2 * part);
 }
 
+// The keys of a value tile.  The tile's ROWS rows of one (sequence, kv-head)
+// hold 64 key groups, contiguous in every key plane (rows are consecutive);
+// lane l fetches groups l and l + 32.  Their loads are issued before the
+// tile's value work and consumed after it, so the value work hides them.
+struct KeyTile {
+    uint32_t w[2][8];
+    uint32_t s[2], z[2];  // fp16 bits
+};
+
+template <int KB>
+__device__ __forceinline__ void key_words_load(const uint8_t *src, uint32_t (&w)[8])
+{
+    if constexpr (KB == 8) {
+        const uint4 a = reinterpret_cast<const uint4 *>(src)[0], b = reinterpret_cast<const uint4 *>(src)[1];
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else if constexpr (KB == 4) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(src);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    } else if constexpr (KB == 2) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(src);
+        w[0] = a.x; w[1] = a.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < KB; ++i) w[i] = reinterpret_cast<const uint32_t *>(src)[i];
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void key_tile_load(const ValueDecodeParams &p, uint32_t bh, int64_t t_first, int lane,
+                                              KeyTile &k)
+{
+    constexpr int GPR = D / 32;  // groups per row
+    const int64_t g0 = ((int64_t)bh * p.cap + p.t0 + t_first) * GPR;  // first group of the tile in the planes
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int g = lane + 32 * i;
+        if (t_first + g / GPR >= p.n) continue;
+        const int64_t gi = g0 + g;
+        switch (p.kb) {
+        case 8: key_words_load<8>(p.k_codes + gi * 32, k.w[i]); break;
+        case 4: key_words_load<4>(p.k_codes + gi * 16, k.w[i]); break;
+        case 5: key_words_load<5>(p.k_codes + gi * 20, k.w[i]); break;
+        default: key_words_load<2>(p.k_codes + gi * 8, k.w[i]); break;
+        }
+        k.s[i] = p.k_scale[gi];
+        k.z[i] = p.k_zero[gi];
+    }
+}
+
+template <int KB, bool F32>
+__device__ __forceinline__ void key_group_from_tile(const uint32_t (&w8)[8], uint32_t s, uint32_t z, void *dst)
+{
+    uint32_t w[KB];
+#pragma unroll
+    for (int i = 0; i < KB; ++i) w[i] = w8[i];
+    key_group_out<KB, F32>(w, f16_bits_to_f32((uint16_t)s), f16_bits_to_f32((uint16_t)z), dst);
+}
+
+template <int D, bool F32>
+__device__ __forceinline__ void key_tile_store(const ValueDecodeParams &p, uint32_t bh, int64_t t_first, int lane,
+                                               const KeyTile &k)
+{
+    constexpr int GPR = D / 32;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int g = lane + 32 * i;
+        if (t_first + g / GPR >= p.n) continue;
+        // output [bh][t][D]: group g of the tile starts at element (bh n + t_first) D + 32 g
+        void *dst = static_cast<uint8_t *>(p.k_out) + (((int64_t)bh * p.n + t_first) * D + 32 * g) * (F32 ? 4 : 2);
+        switch (p.kb) {
+        case 8: key_group_from_tile<8, F32>(k.w[i], k.s[i], k.z[i], dst); break;
+        case 4: key_group_from_tile<4, F32>(k.w[i], k.s[i], k.z[i], dst); break;
+        case 5: key_group_from_tile<5, F32>(k.w[i], k.s[i], k.z[i], dst); break;
+        default: key_group_from_tile<2, F32>(k.w[i], k.s[i], k.z[i], dst); break;
+        }
+    }
+}
+
 template <int D, int VB, bool F32>
-__global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid_constant__ ValueDecodeParams p)
+__global__ void __launch_bounds__(kVWarps * 32, 4) decode_value_kernel(const __grid_constant__ ValueDecodeParams p)
 {
     using G = VGeo<D>;
     __shared__ __align__(16) float scen[1 << VB];
@@ -195,6 +286,9 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
         uint32_t bh;
         locate(item, t, crow, bh);
         const bool valid = t < p.n;
+        KeyTile kt;
+        const bool keys = p.k_out != nullptr;
+        if (keys) key_tile_load<D>(p, bh, t - r, lane, kt);
         if (item + W < p.items) {
             int64_t t1, crow1;
             uint32_t bh1;
@@ -255,6 +349,7 @@ __global__ void __launch_bounds__(kVWarps * 32) decode_value_kernel(const __grid
                 }
             }
         }
+        if (keys) key_tile_store<D, F32>(p, bh, t - r, lane, kt);
     }
 }
 
@@ -280,13 +375,18 @@ cudaError_t run_key(const CacheView &c, int64_t t0, int64_t n, void *out, cudaSt
 }
 
 template <int D, int VB, bool F32>
-cudaError_t run_value(const CacheView &c, int64_t t0, int64_t n, void *out, cudaStream_t s)
+cudaError_t run_value(const CacheView &c, int64_t t0, int64_t n, void *out, void *k_out, cudaStream_t s)
 {
     using G = VGeo<D>;
     ValueDecodeParams p{};
     p.codes = c.v_codes;
     p.scale = c.v_scale;
     p.out = out;
+    p.k_codes = c.k_codes;
+    p.k_scale = c.k_scale;
+    p.k_zero = c.k_zero;
+    p.k_out = k_out;
+    p.kb = c.kb;
     p.H = c.H;
     p.cap = c.cap;
     p.t0 = t0;
@@ -326,15 +426,16 @@ cudaError_t key_dispatch(const CacheView &c, int64_t t0, int64_t n, void *out, c
     return cudaErrorInvalidValue;
 }
 
+// Values, and the keys of the same rows when k_out is not null (one launch).
 template <int D, bool F32>
-cudaError_t value_dispatch_vb(const CacheView &c, int64_t t0, int64_t n, void *out, cudaStream_t s)
+cudaError_t value_dispatch_vb(const CacheView &c, int64_t t0, int64_t n, void *out, void *k_out, cudaStream_t s)
 {
     switch (c.vb) {
-    case 2: return run_value<D, 2, F32>(c, t0, n, out, s);
-    case 3: return run_value<D, 3, F32>(c, t0, n, out, s);
-    case 4: return run_value<D, 4, F32>(c, t0, n, out, s);
-    case 5: return run_value<D, 5, F32>(c, t0, n, out, s);
-    case 8: return run_value<D, 8, F32>(c, t0, n, out, s);
+    case 2: return run_value<D, 2, F32>(c, t0, n, out, k_out, s);
+    case 3: return run_value<D, 3, F32>(c, t0, n, out, k_out, s);
+    case 4: return run_value<D, 4, F32>(c, t0, n, out, k_out, s);
+    case 5: return run_value<D, 5, F32>(c, t0, n, out, k_out, s);
+    case 8: return run_value<D, 8, F32>(c, t0, n, out, k_out, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -2,8 +2,10 @@
 #include "tq_decode.cuh"
 
 namespace tq {
-cudaError_t launch_decode_values_d256(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out, cudaStream_t s)
+cudaError_t launch_decode_values_d256(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out, void *k_out,
+                                     cudaStream_t s)
 {
-    return f32 ? value_dispatch_vb<256, true>(c, t0, n, out, s) : value_dispatch_vb<256, false>(c, t0, n, out, s);
+    return f32 ? value_dispatch_vb<256, true>(c, t0, n, out, k_out, s)
+               : value_dispatch_vb<256, false>(c, t0, n, out, k_out, s);
 }
 }  // namespace tq

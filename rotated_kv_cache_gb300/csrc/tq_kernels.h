@@ -65,7 +65,7 @@ cudaError_t launch_encode(const CacheView &c, const uint16_t *k, const int64_t k
     cudaError_t launch_encode_d##D(const CacheView &c, const uint16_t *k, const int64_t ks[3], const uint16_t *v, \
                                    const int64_t vs[3], int64_t t0, int64_t n, cudaStream_t s);                  \
     cudaError_t launch_decode_values_d##D(const CacheView &c, int64_t t0, int64_t n, bool f32, void *out,        \
-                                          cudaStream_t s);
+                                          void *k_out, cudaStream_t s);
 TQ_DECLARE_PER_D(64)
 TQ_DECLARE_PER_D(128)
 TQ_DECLARE_PER_D(256)
