@@ -32,13 +32,14 @@ namespace tq {
 namespace {
 
 constexpr int kWarps = 4;  // warps per CTA
+constexpr int kKeyRows = 2;  // key rows (groups) per lane in a warp tile: independent chains that interleave
 
-template <int D, bool KEY>
+template <int D, bool KEY, int KR = kKeyRows>
 struct EGeo {
     static constexpr int E = KEY ? 32 : 64;   // elements per lane and row
     static constexpr int LPR = D / E;          // lanes per row
     static constexpr int ROWS = 32 / LPR;      // rows one pass of the warp covers
-    static constexpr int RPL = KEY ? 4 : 1;    // rows per lane: independent key groups interleave
+    static constexpr int RPL = KEY ? KR : 1;   // rows per lane: independent key groups interleave
     static constexpr int TROWS = ROWS * RPL;   // rows per warp tile
     // Two tile layouts, one read formula (chunk k of a row's 64-column box at
     // base + 16 * (k ^ xr)):
@@ -74,37 +75,56 @@ struct EncodeParams {
     float bnd[255];  // value boundaries (ascending)
 };
 
-template <int D, bool KEY>
-__device__ __forceinline__ void issue_tile(const EncodeParams &p, const CUtensorMap &map, uint32_t item, uint32_t buf,
-                                           uint32_t bar, int lane)
+// Bytes a tile's copies bring into shared memory.
+template <int D, bool KEY, int KR = kKeyRows>
+__device__ __forceinline__ uint32_t tile_bytes(const EncodeParams &p, uint32_t item)
 {
-    using G = EGeo<D, KEY>;
+    using G = EGeo<D, KEY, KR>;
+    if (p.use_tma) return (uint32_t)((D / 64) * G::TROWS * 128);  // rows past n arrive as zeros
+    const uint32_t bh = fast_div(item, p.div_tiles);
+    const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::TROWS;
+    return (uint32_t)(imin64(G::TROWS, p.n - t_first) * D * 2);
+}
+
+// The copies of a tile, completing on `bar` (whose expected bytes the caller
+// has already raised by tile_bytes): one tensor copy per 64-column box, or
+// one bulk copy per row.  Call from every lane of the warp.
+template <int D, bool KEY, int KR = kKeyRows>
+__device__ __forceinline__ void issue_copies(const EncodeParams &p, const CUtensorMap &map, uint32_t item,
+                                             uint32_t buf, uint32_t bar, int lane)
+{
+    using G = EGeo<D, KEY, KR>;
     const uint32_t bh = fast_div(item, p.div_tiles);
     const int64_t t_first = (int64_t)(item - bh * p.tiles_per_bh) * G::TROWS;
     const uint32_t b = fast_div(bh, p.div_h), h = bh - b * (uint32_t)p.H;
     if (p.use_tma) {
-        // one tensor copy per 64-column box; rows past n arrive as zeros
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar, (uint32_t)((D / 64) * G::TROWS * 128));
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) tma_load_4d(buf + c * G::BOX, &map, 64 * c, (int)t_first, (int)h, (int)b, bar);
         }
         return;
     }
     const int rows = (int)imin64(G::TROWS, p.n - t_first);
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows * D * 2));
-    __syncwarp();
     if (lane < rows) {
         const uint16_t *src = p.src + b * p.sb + h * p.sh + t_first * p.st;
         for (int row = lane; row < rows; row += 32) bulk_g2s(buf + row * G::RS, src + row * p.st, D * 2, bar);
     }
 }
 
+template <int D, bool KEY, int KR = kKeyRows>
+__device__ __forceinline__ void issue_tile(const EncodeParams &p, const CUtensorMap &map, uint32_t item, uint32_t buf,
+                                           uint32_t bar, int lane)
+{
+    if (lane == 0) mbar_arrive_expect_tx(bar, tile_bytes<D, KEY, KR>(p, item));
+    __syncwarp();
+    issue_copies<D, KEY, KR>(p, map, item, buf, bar, lane);
+}
+
 // Shared-memory base of a row's 64-column box c and the chunk xor for it.
-template <int D, bool KEY>
+template <int D, bool KEY, int KR = kKeyRows>
 __device__ __forceinline__ uint32_t box_base(const EncodeParams &p, uint32_t buf, int row, int c, uint32_t &xr)
 {
-    using G = EGeo<D, KEY>;
+    using G = EGeo<D, KEY, KR>;
     xr = p.use_tma ? (uint32_t)(row & 7) : 0u;
     return p.use_tma ? buf + c * G::BOX + row * 128 : buf + row * G::RS + 128 * c;
 }
@@ -134,7 +154,23 @@ __device__ __forceinline__ float ms_div(float x, float y, float ry)
     return __fmaf_rn(__fmaf_rn(-y, q0, x), ry, q0);
 }
 
-// ------------------------------------------------------------------ keys
+// RN(a*b + c) saturated to [0, 1] (NaN to 0).
+__device__ __forceinline__ float ffma_sat(float a, float b, float c)
+{
+    float d;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// The power of two K with K * den in [2^40, 2^41), for a positive normal den
+// below 2^127 (den >= 1e-8 here: exponent field 100..254, K's 40..194).
+__device__ __forceinline__ float pow2_scale_for(float den)
+{
+    const uint32_t e = fbits(den) >> 23;
+    return __uint_as_float((294u - e) << 23);
+}
+
+// ------------------------------------------------------------------ keys// ------------------------------------------------------------------ keys
 // Pack codes given as 0x4B400000 + code (code < 2^BITS) into the BITS-bit
 // little-endian stream: accumulate the sums, then subtract what the constant
 // 0x4B400000 part contributed (fields do not overlap, so adding is or-ing).
@@ -287,16 +323,16 @@ __device__ __forceinline__ void key_codes_fast(const uint32_t (&w)[16], const Ke
 
 // A lane's RPL key groups (rows r, r + ROWS, ...): parameters for all first,
 // then the element passes, so the groups' dependency chains interleave.
-template <int D, int BITS>
+template <int D, int BITS, int KR = kKeyRows>
 __device__ __forceinline__ void encode_key_lane(const EncodeParams &p, uint32_t buf, int r, int64_t crow, int part,
                                                 int nvalid)
 {
-    using G = EGeo<D, true>;
+    using G = EGeo<D, true, KR>;
     constexpr int R = G::RPL;
     const uint32_t lo = 4 * (part & 1);  // first 16-byte chunk of this lane's 32 keys in the 64-column box
     uint32_t base[R], xr[R];
 #pragma unroll
-    for (int g = 0; g < R; ++g) base[g] = box_base<D, true>(p, buf, r + g * G::ROWS, part >> 1, xr[g]);
+    for (int g = 0; g < R; ++g) base[g] = box_base<D, true, KR>(p, buf, r + g * G::ROWS, part >> 1, xr[g]);
     uint32_t w[R][16];
 #pragma unroll
     for (int g = 0; g < R; ++g) {
@@ -371,15 +407,14 @@ __device__ __forceinline__ void put_code(uint32_t (&w)[BITS], int j, uint32_t c)
 
 // Value codes of a warp tile are written to a shared staging area (rows x
 // row bytes, the tile's own layout in the cache) and leave in one bulk store.
-template <int D, int BITS>
-__device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const float *sbnd, uint32_t a, uint32_t xr,
-                                                  uint32_t mtab, uint32_t stage, int64_t crow, int r, int part, bool valid)
+// A lane's 64 value inputs from the shared tile, signs applied.
+template <int D>
+__device__ __forceinline__ void value_lane_load(uint32_t a, uint32_t xr, uint32_t mtab, int part, bool valid,
+                                                float2 (&P)[32])
 {
-    using G = EGeo<D, false>;
     // P[j] = (element j, element j + 32) of this lane's 64; at head_dim 128 part-1
     // lanes hold them swapped (their two 64-byte halves are read in the other
     // order), for the transform's half-traffic stride-64 stage
-    float2 P[32];
     if constexpr (D == 128) xr ^= 4u * (uint32_t)part;
     if (valid) {
 #pragma unroll
@@ -400,6 +435,15 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
 #pragma unroll
         for (int j = 0; j < 32; ++j) P[j] = make_float2(0.0f, 0.0f);
     }
+}
+
+// Transform, group RMS, indices and packing of a lane's loaded inputs; the
+// codes go to the warp's staging area, the scales to the cache.
+template <int D, int BITS>
+__device__ __forceinline__ void value_lane_codes(const EncodeParams &p, const float *sbnd, float2 (&P)[32],
+                                                 uint32_t stage, int64_t crow, int r, int part, bool valid)
+{
+    using G = EGeo<D, false>;
     // afterwards P[j] holds elements j and j + 32 of the lane's 64 (groups 2 part and
     // 2 part + 1), or at head_dim 128 elements 32 part + j and 64 + 32 part + j
     // (groups part and 2 + part), the second negated on part-1 lanes
@@ -427,43 +471,74 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
     if constexpr (BITS <= 3) {
         if (den0 < INFINITY && den1 < INFINITY) {
             // The index counts the boundaries b below y/den.  The table is
-            // antisymmetric with b[H-1] = 0, so with m = #{positive b : |y| <
-            // b*den} the index is m for y <= 0 and 2H-1-m for y > 0.  |y| < b*den
-            // is tested as y*y - (b*den)^2 < 0 (one fused step per pair); it can
-            // differ from the division only within a few ulps of a boundary.
+            // antisymmetric with b[H-1] = 0, so with m = #{positive b : b*den <
+            // |y|} the index is H-1-m for y <= 0 and H+m for y > 0, i.e.
+            // 2 idx = 2H-1 + s (2m+1) with s = +1 for y > 0, else -1.
+            // b*den < |y| is read off the sign of K^2 (y^2 - (b den)^2), with a
+            // per-group power of two K putting K den in [2^40, 2^41): any
+            // nonzero value there is at least 2^31 (y^2 has 48 bits, the square
+            // of a threshold 24), so saturating to [0, 1] gives exactly 0 or 1.
+            // At 3 bits the middle threshold picks the outer one to test next.
+            // It can differ from the division only within a few ulps of a
+            // boundary.  The codes are summed as floats, C per chunk weighted
+            // 2^(BITS i) (exact: below 2^22 on top of 1.5*2^23), which keeps
+            // the bit assembly off the integer pipe.
             constexpr int H = 1 << (BITS - 1);
-            float2 nq[H - 1];
+            constexpr int C = 21 / BITS;            // codes per chunk
+            constexpr int NC = (32 + C - 1) / C;    // chunks per group
+            const float K0 = pow2_scale_for(den0), K1 = pow2_scale_for(den1);
+            float2 nt[H - 1];  // -(K b den)^2 for the positive boundaries
 #pragma unroll
             for (int k = 0; k < H - 1; ++k) {
-                const float t0 = __fmul_rn(p.bnd[H + k], den0), t1 = __fmul_rn(p.bnd[H + k], den1);
-                nq[k] = make_float2(-__fmul_rn(t0, t0), -__fmul_rn(t1, t1));
+                const float t0 = __fmul_rn(__fmul_rn(p.bnd[H + k], den0), K0);
+                const float t1 = __fmul_rn(__fmul_rn(p.bnd[H + k], den1), K1);
+                nt[k] = make_float2(-__fmul_rn(t0, t0), -__fmul_rn(t1, t1));
             }
-            // The thresholds tested are a thermometer code (s_k = [|y| < P_k]
-            // rises with k), so m's bits are s_2 (bit 1) and s_1^s_2^s_3 (bit 0),
-            // and every code bit is that bit xor [y > 0] -- all read from bit 31
-            // of the fused results, combined with three-input logic, and shifted
-            // straight into the group's words, highest stream bit first.
-            const float2 m1 = make_float2(-1.0f, -1.0f), z2 = make_float2(0.0f, 0.0f);
+            const float2 nk = make_float2(-K0, -K1), z2 = make_float2(0.0f, 0.0f);
+            constexpr float M = 12582912.0f;  // 1.5 * 2^23
+            float2 acc[NC];
 #pragma unroll
-            for (int j = 31; j >= 0; --j) {
-                float2 e[H - 1];
+            for (int c = 0; c < NC; ++c) {
+                float wsum = 0.0f;  // (2H - 1) * sum of the chunk's weights, plus M
 #pragma unroll
-                for (int k = 0; k < H - 1; ++k) e[k] = __ffma2_rn(P[j], P[j], nq[k]);  // sign set iff y^2 < P_k^2
-                const float2 n = __ffma2_rn(P[j], m1, z2);                             // sign set iff y > 0 (+0 for y = +-0)
-                uint32_t c0[BITS], c1[BITS];  // code bits of element j of each group in bit 31, highest first
+                for (int i = 0; i < C && c * C + i < 32; ++i) wsum += (float)((2 * H - 1) << (BITS * i));
+                acc[c] = make_float2(M + wsum, M + wsum);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float2 kv = __ffma2_rn(P[j], nk, z2);  // -K y: sign set iff y > 0 (+0 for y = +-0)
+                float2 q;                                    // 2m + 1
                 if constexpr (BITS == 3) {
-                    const uint32_t ax = fbits(e[1].x) ^ fbits(n.x), ay = fbits(e[1].y) ^ fbits(n.y);
-                    c0[0] = fbits(n.x); c0[1] = ax; c0[2] = fbits(e[0].x) ^ fbits(e[2].x) ^ ax;
-                    c1[0] = fbits(n.y); c1[1] = ay; c1[2] = fbits(e[0].y) ^ fbits(e[2].y) ^ ay;
+                    const float2 b1 = make_float2(ffma_sat(kv.x, kv.x, nt[1].x), ffma_sat(kv.y, kv.y, nt[1].y));
+                    const float2 nsel = __ffma2_rn(b1, make_float2(nt[2].x - nt[0].x, nt[2].y - nt[0].y), nt[0]);
+                    const float2 b2 = make_float2(ffma_sat(kv.x, kv.x, nsel.x), ffma_sat(kv.y, kv.y, nsel.y));
+                    q = __ffma2_rn(b1, make_float2(4.0f, 4.0f), __ffma2_rn(b2, make_float2(2.0f, 2.0f), make_float2(1.0f, 1.0f)));
                 } else {
-                    c0[0] = fbits(n.x); c0[1] = fbits(e[0].x) ^ fbits(n.x);
-                    c1[0] = fbits(n.y); c1[1] = fbits(e[0].y) ^ fbits(n.y);
+                    const float2 b1 = make_float2(ffma_sat(kv.x, kv.x, nt[0].x), ffma_sat(kv.y, kv.y, nt[0].y));
+                    q = __ffma2_rn(b1, make_float2(2.0f, 2.0f), make_float2(1.0f, 1.0f));
                 }
+                // s (2m + 1): negative unless y > 0
+                const float2 sq = make_float2(__uint_as_float(fbits(q.x) | (~fbits(kv.x) & 0x80000000u)),
+                                              __uint_as_float(fbits(q.y) | (~fbits(kv.y) & 0x80000000u)));
+                const float wj = (float)(1u << (BITS * (j % C)));
+                acc[j / C] = __ffma2_rn(sq, make_float2(wj, wj), acc[j / C]);
+            }
+            // chunk c holds 2 x (codes 7c.. as a C*BITS-bit string) in its low 22 bits; place it at bit C*BITS*c
 #pragma unroll
-                for (int q = 0; q < BITS; ++q) {
-                    const int word = (j * BITS + BITS - 1 - q) >> 5;
-                    w0[word] = __funnelshift_l(c0[q], w0[word], 1);
-                    w1[word] = __funnelshift_l(c1[q], w1[word], 1);
+            for (int c = 0; c < NC; ++c) {
+                const uint32_t u0 = fbits(acc[c].x) & 0x3FFFFFu, u1 = fbits(acc[c].y) & 0x3FFFFFu;
+                const int bit = c * C * BITS, word = bit >> 5, off = bit & 31;
+                const int nbits = (32 - c * C < C ? 32 - c * C : C) * BITS;
+                if (off == 0) {
+                    w0[word] += u0 >> 1;
+                    w1[word] += u1 >> 1;
+                } else {
+                    w0[word] += u0 << (off - 1);
+                    w1[word] += u1 << (off - 1);
+                }
+                if (off + nbits > 32) {
+                    w0[word + 1] += u0 >> (33 - off);
+                    w1[word + 1] += u1 >> (33 - off);
                 }
             }
             done = true;
@@ -512,6 +587,15 @@ __device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const f
     }
     const uint32_t sw = (uint32_t)f32_to_f16_bits(sig0) | ((uint32_t)f32_to_f16_bits(sig1) << 16);
     *reinterpret_cast<uint32_t *>(p.scale + crow * (D / 32) + 2 * part) = sw;
+}
+
+template <int D, int BITS>
+__device__ __forceinline__ void encode_value_lane(const EncodeParams &p, const float *sbnd, uint32_t a, uint32_t xr,
+                                                  uint32_t mtab, uint32_t stage, int64_t crow, int r, int part, bool valid)
+{
+    float2 P[32];
+    value_lane_load<D>(a, xr, mtab, part, valid, P);
+    value_lane_codes<D, BITS>(p, sbnd, P, stage, crow, r, part, valid);
 }
 
 // ------------------------------------------------------------------ kernels

@@ -1,22 +1,25 @@
 """Host model of the value encoder's fast index path (2 and 3 bits), checked on the CPU.
 
 For a group of 32 rotated values y with den = rms + 1e-8 (finite), the encoder
-never divides.  The codebook is antisymmetric with its middle boundary at 0.
-So with s_k = [y^2 < fl(fl(b_k den)^2)] for the positive boundaries b_k,
-m = s_0 + s_1 + ... counts the positive boundaries above |y|, and the index
-is m for y <= 0 and 2^bits - 1 - m for y > 0.
+never divides.  The codebook is antisymmetric with its middle boundary at 0,
+so with m = #{positive b_k : b_k den < |y|} the index is H-1-m for y <= 0 and
+H+m for y > 0 (H = 2^(bits-1)), i.e. 2 idx = 2H-1 + s (2m+1), s = +1 iff y > 0.
 
-The kernel reads these tests from the sign bits of fused multiply-adds:
-- the index bits are m's bits xor [y > 0];
-- for 3 bits, m's bits are s_1 and s_0 ^ s_1 ^ s_2, because the s_k rise
-  together;
-- each bit is shifted into the group's packed words with a funnel shift,
-  highest stream bit first.
+The kernel's steps, replayed here:
+- a power of two K per group with K den in [2^40, 2^41) (from den's exponent);
+- kv = fma(y, -K, 0), whose sign bit is set iff y > 0 (+0 for y = +-0);
+- threshold tests sat(fma(kv, kv, -fl(fl(K fl(b den)))^2)), which must come out
+  exactly 0 or 1 (the model checks that no value lands strictly inside (0, 1));
+- at 3 bits the middle threshold's test picks which outer threshold to test
+  next, through nsel = fma(b1, fl(nt2 - nt0), nt0);
+- s (2m+1) summed into float chunks of C = 21 // bits codes weighted
+  2^(bits i) on top of 1.5*2^23 + (2H-1) * (sum of weights), which must stay
+  exact integers below 2^22 above 1.5*2^23;
+- the chunks' low 22 bits (twice the chunk) placed at bit C*bits*c of the
+  group's little-endian words.
 
-The model replays those steps.  The sign of each fused result is exact in
-binary64: y^2 of a float32 is exact, and rounding keeps a sign.  The model
-must give the codes of an exact count of boundaries below y / den (away from
-the boundaries), packed little-endian at `bits` per code.  CPU only.
+The model must give the codes of an exact count of boundaries below y / den
+(away from the boundaries), packed little-endian at `bits` per code.  CPU only.
 """
 from fractions import Fraction
 
@@ -26,32 +29,58 @@ import pytest
 import oracle
 
 F32 = np.float32
+M = 12582912  # 1.5 * 2^23
 
 
-def neg_sign(x):
-    """Bit 31 of a float32 result, as the kernel reads it."""
-    return 1 if np.signbit(F32(x)) else 0
+def f32_bits(x):
+    return int(np.array([x], dtype=F32).view(np.uint32)[0])
+
+
+def sat_fma(a, b, c):
+    """sat(a*b + c) of float32 operands; the kernel needs the exact value outside (0, 1)."""
+    v = Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c))
+    if v <= 0:
+        return 0
+    assert v >= 1, "a saturated test landed inside (0, 1)"
+    return 1
 
 
 def fast_path_words(y, den, bits, bnd):
-    """The kernel's code bits and packed words for one group (y: 32 float32)."""
+    """The kernel's packed words for one group (y: 32 float32, den float32)."""
     H = 1 << (bits - 1)
-    t = [F32(F32(bnd[H + k]) * den) for k in range(H - 1)]
-    nq = [-float(F32(tk * tk)) for tk in t]
-    w = [0] * bits
-    for j in range(31, -1, -1):
-        yj = float(y[j])
-        e = [neg_sign(yj * yj + nqk) for nqk in nq]  # sign set iff y^2 < fl(t^2)
-        n = neg_sign(-yj + 0.0)                      # sign set iff y > 0 (+0 for y = +-0)
+    C = 21 // bits
+    NC = (32 + C - 1) // C
+    K = F32(np.array([(294 - (f32_bits(den) >> 23)) << 23], dtype=np.uint32).view(F32)[0])
+    assert 2.0 ** 40 <= float(K) * float(den) < 2.0 ** 41
+    t = [F32(F32(F32(bnd[H + k]) * den) * K) for k in range(H - 1)]
+    nt = [F32(-F32(tk * tk)) for tk in t]
+    acc = []
+    for c in range(NC):
+        wsum = sum((2 * H - 1) << (bits * i) for i in range(C) if c * C + i < 32)
+        acc.append(M + wsum)
+    for j in range(32):
+        kv = F32(F32(y[j]) * F32(-K) + F32(0.0))  # fma(y, -K, 0): exact product (power of two)
         if bits == 3:
-            ax = e[1] ^ n
-            c = [n, ax, e[0] ^ e[2] ^ ax]            # index bits, highest first
+            b1 = sat_fma(kv, kv, nt[1])
+            d = F32(nt[2] - nt[0])
+            nsel = nt[0] if b1 == 0 else F32(d + nt[0])
+            b2 = sat_fma(kv, kv, nsel)
+            q = 4 * b1 + 2 * b2 + 1
         else:
-            c = [n, e[0] ^ n]
-        for q in range(bits):
-            word = (j * bits + bits - 1 - q) >> 5
-            w[word] = ((w[word] << 1) | c[q]) & 0xFFFFFFFF  # funnel shift left by one
-    return w
+            q = 2 * sat_fma(kv, kv, nt[0]) + 1
+        s = 1 if np.signbit(kv) else -1  # sign bit of kv set iff y > 0
+        acc[j // C] += s * q * (1 << (bits * (j % C)))
+        assert M <= acc[j // C] < M + (1 << 22)  # exact in float32 (ulp 1 there)
+    w = [0] * bits
+    for c in range(NC):
+        u = (acc[c] - M) & 0x3FFFFF  # the chunk's low 22 bits: twice the chunk
+        bit = c * C * bits
+        word, off = bit >> 5, bit & 31
+        nbits = min(C, 32 - c * C) * bits
+        w[word] += (u >> 1) if off == 0 else ((u << (off - 1)) & 0xFFFFFFFF)
+        if off + nbits > 32:
+            w[word + 1] += u >> (33 - off)
+    return [x & 0xFFFFFFFF for x in w]
 
 
 def exact_index(yj, den, bnd):
@@ -68,12 +97,13 @@ def pack_le(idx, bits):
 @pytest.mark.parametrize("bits", [2, 3])
 def test_fast_index_matches_exact_count(bits):
     """Codes equal the exact count away from boundaries; within 1e-6 of one, either
-    neighbouring cell (the squared test rounds fl(b den)^2); packing is exact."""
+    neighbouring cell (the squared tests round fl(b den)^2, and at 3 bits the
+    outer threshold comes from one more rounding); packing is exact."""
     _, bnd = oracle.codebook(bits)
     rng = np.random.default_rng(bits)
     near_seen = 0
     for trial in range(400):
-        den = F32(np.exp(rng.normal(0, 3)))
+        den = F32(np.exp(rng.normal(0, 3))) + F32(1e-8)
         y = (rng.standard_normal(32) * float(den) * rng.choice([0.3, 1.0, 3.0])).astype(F32)
         if trial % 7 == 0:  # values on a threshold and signed zeros
             y[:4] = [F32(0.0), F32(-0.0), F32(F32(bnd[-1]) * den), -F32(F32(bnd[-1]) * den)]
@@ -100,3 +130,22 @@ def test_signed_zero_takes_the_lower_middle_cell():
         y[1::2] = F32(-0.0)
         H = 1 << (bits - 1)
         assert fast_path_words(y, F32(1.0), bits, bnd) == pack_le([H - 1] * 32, bits)
+
+
+@pytest.mark.parametrize("den", [1e-8, 3e-8, 1.0, 1e20, 3e37])
+def test_extreme_scales(den):
+    """The per-group power of two keeps every test saturating and every chunk exact
+    from the smallest den (rms 0: den = 1e-8) to the largest finite ones."""
+    for bits in (2, 3):
+        _, bnd = oracle.codebook(bits)
+        d = F32(den)
+        rng = np.random.default_rng(int(np.log10(den) + 20) * 10 + bits)
+        y = (rng.standard_normal(32) * float(d)).astype(F32)
+        y = np.clip(y, -5.6 * float(d), 5.6 * float(d)).astype(F32)  # |y| <= sqrt(32) rms
+        got = fast_path_words(y, d, bits, bnd)
+        want = [exact_index(yj, d, bnd) for yj in y]
+        v = sum(wd << (32 * k) for k, wd in enumerate(got))
+        got_idx = [(v >> (i * bits)) & ((1 << bits) - 1) for i in range(32)]
+        for g, w_, yj in zip(got_idx, want, y):
+            if min(abs(float(yj) / float(d) - float(b)) for b in bnd) >= 1e-6:
+                assert g == w_
