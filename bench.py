@@ -910,6 +910,7 @@ def run_sweep(only=None):
 PROFILE_CASES = {
     # name: (operation, head_dim, k_bits, v_bits, batch, kv-heads, rows, q-heads per kv-head)
     "prefill_codec": ("codec", 128, 8, 3, 4, 8, 8192, 0),
+    "decode_attention_b1": ("attention", 128, 8, 3, 1, 8, 32769, 8),
     "decode_attention_b2": ("attention", 128, 8, 3, 2, 8, 32769, 8),
     "long_context_attention_b2": ("attention", 128, 4, 3, 2, 8, 131073, 8),
     "sweep_codec_d64_k8v3": ("codec", 64, 8, 3, 1, 8, 16384, 0),

@@ -603,11 +603,14 @@ struct CombineParams {
     SignBits sg;  // value signs
 };
 
-// one warp per (sequence, q-head); lane holds dims 4*lane .. 4*lane+3
-// One CTA of kCombineWarps warps per (sequence, q-head): the warps merge
-// interleaved subsets of the splits, then warp 0 merges the warps' results
-// (a few hundred splits at batch 1 would be a long serial chain for one warp).
-constexpr int kCombineWarps = 4;
+// One CTA of kCombineWarps warps per (sequence, q-head); lane holds dims
+// 4 lane .. 4 lane + 3.  Warp w merges the splits w, w + kCombineWarps, ...
+// in chunks of 32: the chunk's (max, sum) pairs are read one per lane, the
+// weights 2^(m_s - m) computed one per lane and broadcast, and the chunk's
+// output rows read with independent loads (all in flight at once), so a few
+// hundred splits (batch 1) cost a handful of memory round trips, not one per
+// split.  Warp 0 then merges the warps' results.
+constexpr int kCombineWarps = 8;
 
 __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const __grid_constant__ CombineParams p)
 {
@@ -618,19 +621,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
     const int h = qh / p.G, hq = qh % p.G;
     const int hh = hq % kG;  // column of block hq / kG
     const int64_t base = ((int64_t)b * p.H * p.NB + (int64_t)h * p.NB + hq / kG) * p.splits;
-    // this warp's splits: warp, warp + kCombineWarps, ...
+    // this warp's splits: warp + kCombineWarps * i, i = 0 .. n_mine - 1
+    const int n_mine = p.splits > warp ? (p.splits - warp + kCombineWarps - 1) / kCombineWarps : 0;
     float mw = -INFINITY;
-    for (int s = warp; s < p.splits; s += kCombineWarps) mw = fmaxf(mw, p.part_ml[2 * ((base + s) * kG + hh)]);
+    for (int i = lane; i < n_mine; i += 32)
+        mw = fmaxf(mw, p.part_ml[2 * ((base + warp + (int64_t)kCombineWarps * i) * kG + hh)]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
     const float muw = mw == -INFINITY ? 0.0f : mw;
     float4 xw = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float lw = 0.0f;
-    for (int s = warp; s < p.splits; s += kCombineWarps) {
-        const int64_t pi = (base + s) * kG + hh;
-        const float wt = ex2(p.part_ml[2 * pi] - muw);
-        lw += p.part_ml[2 * pi + 1] * wt;
-        const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pi * kD + 4 * lane);
-        xw.x += v.x * wt; xw.y += v.y * wt; xw.z += v.z * wt; xw.w += v.w * wt;
+    for (int i0 = 0; i0 < n_mine; i0 += 32) {
+        // lane j: weight and sum of split i0 + j
+        float wt = 0.0f;
+        if (i0 + lane < n_mine) {
+            const int64_t pi = (base + warp + (int64_t)kCombineWarps * (i0 + lane)) * kG + hh;
+            const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * pi);
+            wt = ex2(ml.x - muw);
+            lw += ml.y * wt;
+        }
+        const int cnt = n_mine - i0 < 32 ? n_mine - i0 : 32;
+#pragma unroll 8
+        for (int j = 0; j < cnt; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wt, j);
+            const int64_t pi = (base + warp + (int64_t)kCombineWarps * (i0 + j)) * kG + hh;
+            const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pi * kD + 4 * lane);
+            xw.x += v.x * w; xw.y += v.y * w; xw.z += v.z * w; xw.w += v.w * w;
+        }
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
     wo[warp][lane] = xw;
     if (lane == 0) {
         wm[warp] = mw;

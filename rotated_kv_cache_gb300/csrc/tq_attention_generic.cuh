@@ -671,22 +671,37 @@ __global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const
     const int b = row / per_seq, rem = row - b * per_seq, i = rem / p.QH, qh = rem - i * p.QH;
     const int h = qh / p.G, col = i * p.G + (qh - h * p.G), hb = col / p.CB, n = col - hb * p.CB;
     const int64_t base = (((int64_t)b * p.H + h) * p.HB + hb) * p.splits;
+    // this warp's splits wid + W i, i < n_mine, in chunks of 32: (max, sum) one
+    // per lane, weights broadcast, the chunk's output rows read with
+    // independent loads
+    const int n_mine = live && p.splits > wid ? (p.splits - wid + W - 1) / W : 0;
     float mw = -INFINITY;
-    if (live)
-        for (int s = wid; s < p.splits; s += W) mw = fmaxf(mw, p.part_ml[2 * ((base + s) * p.CB + n)]);
+    for (int i = lane; i < n_mine; i += 32) mw = fmaxf(mw, p.part_ml[2 * ((base + wid + (int64_t)W * i) * p.CB + n)]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
     const float muw = mw == -INFINITY ? 0.0f : mw;
     float x[PER], l = 0.0f;
 #pragma unroll
     for (int k = 0; k < PER; ++k) x[k] = 0.0f;
-    if (live)
-        for (int s = wid; s < p.splits; s += W) {
-            const int64_t pi = (base + s) * p.CB + n;
-            const float wt = g_ex2(p.part_ml[2 * pi] - muw);
-            l += p.part_ml[2 * pi + 1] * wt;
-            const float *src = p.part_o + pi * D + PER * lane;
-#pragma unroll
-            for (int k = 0; k < PER; ++k) x[k] += src[k] * wt;
+    for (int i0 = 0; i0 < n_mine; i0 += 32) {
+        float wt = 0.0f;
+        if (i0 + lane < n_mine) {
+            const int64_t pi = (base + wid + (int64_t)W * (i0 + lane)) * p.CB + n;
+            const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * pi);
+            wt = g_ex2(ml.x - muw);
+            l += ml.y * wt;
         }
+        const int cnt = n_mine - i0 < 32 ? n_mine - i0 : 32;
+#pragma unroll 4
+        for (int j = 0; j < cnt; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wt, j);
+            const float *src = p.part_o + ((base + wid + (int64_t)W * (i0 + j)) * p.CB + n) * D + PER * lane;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) x[k] += src[k] * w;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     if constexpr (W > 1) {
 #pragma unroll
         for (int k = 0; k < PER; ++k) wo[warp][k][lane] = x[k];
