@@ -468,7 +468,7 @@ __device__ __forceinline__ void value_lane_codes(const EncodeParams &p, const fl
 #pragma unroll
     for (int k = 0; k < BITS; ++k) w0[k] = w1[k] = 0;
     bool done = false;
-    if constexpr (BITS <= 3) {
+    if constexpr (BITS <= 4) {
         if (den0 < INFINITY && den1 < INFINITY) {
             // The index counts the boundaries b below y/den.  The table is
             // antisymmetric with b[H-1] = 0, so with m = #{positive b : b*den <
@@ -478,7 +478,8 @@ __device__ __forceinline__ void value_lane_codes(const EncodeParams &p, const fl
             // per-group power of two K putting K den in [2^40, 2^41): any
             // nonzero value there is at least 2^31 (y^2 has 48 bits, the square
             // of a threshold 24), so saturating to [0, 1] gives exactly 0 or 1.
-            // At 3 bits the middle threshold picks the outer one to test next.
+            // m is found by binary search: at 3 bits the middle threshold picks
+            // the outer one to test next, at 4 bits two levels pick the next.
             // It can differ from the division only within a few ulps of a
             // boundary.  The codes are summed as floats, C per chunk weighted
             // 2^(BITS i) (exact: below 2^22 on top of 1.5*2^23), which keeps
@@ -508,7 +509,19 @@ __device__ __forceinline__ void value_lane_codes(const EncodeParams &p, const fl
             for (int j = 0; j < 32; ++j) {
                 const float2 kv = __ffma2_rn(P[j], nk, z2);  // -K y: sign set iff y > 0 (+0 for y = +-0)
                 float2 q;                                    // 2m + 1
-                if constexpr (BITS == 3) {
+                if constexpr (BITS == 4) {
+                    // thresholds T1..T7 in nt[0..6]: T4, then T2 or T6, then T1/T3/T5/T7
+                    const float2 b1 = make_float2(ffma_sat(kv.x, kv.x, nt[3].x), ffma_sat(kv.y, kv.y, nt[3].y));
+                    const float2 n2 = __ffma2_rn(b1, make_float2(nt[5].x - nt[1].x, nt[5].y - nt[1].y), nt[1]);
+                    const float2 b2 = make_float2(ffma_sat(kv.x, kv.x, n2.x), ffma_sat(kv.y, kv.y, n2.y));
+                    const float2 lo = __ffma2_rn(b1, make_float2(nt[4].x - nt[0].x, nt[4].y - nt[0].y), nt[0]);
+                    const float2 hi = __ffma2_rn(b1, make_float2(nt[6].x - nt[2].x, nt[6].y - nt[2].y), nt[2]);
+                    const float2 n3 = __ffma2_rn(b2, __fadd2_rn(hi, make_float2(-lo.x, -lo.y)), lo);
+                    const float2 b3 = make_float2(ffma_sat(kv.x, kv.x, n3.x), ffma_sat(kv.y, kv.y, n3.y));
+                    q = __ffma2_rn(b1, make_float2(8.0f, 8.0f),
+                                   __ffma2_rn(b2, make_float2(4.0f, 4.0f),
+                                              __ffma2_rn(b3, make_float2(2.0f, 2.0f), make_float2(1.0f, 1.0f))));
+                } else if constexpr (BITS == 3) {
                     const float2 b1 = make_float2(ffma_sat(kv.x, kv.x, nt[1].x), ffma_sat(kv.y, kv.y, nt[1].y));
                     const float2 nsel = __ffma2_rn(b1, make_float2(nt[2].x - nt[0].x, nt[2].y - nt[0].y), nt[0]);
                     const float2 b2 = make_float2(ffma_sat(kv.x, kv.x, nsel.x), ffma_sat(kv.y, kv.y, nsel.y));

@@ -1,4 +1,4 @@
-"""Host model of the value encoder's fast index path (2 and 3 bits), checked on the CPU.
+"""Host model of the value encoder's fast index path (2, 3 and 4 bits), checked on the CPU.
 
 For a group of 32 rotated values y with den = rms + 1e-8 (finite), the encoder
 never divides.  The codebook is antisymmetric with its middle boundary at 0,
@@ -10,8 +10,9 @@ The kernel's steps, replayed here:
 - kv = fma(y, -K, 0), whose sign bit is set iff y > 0 (+0 for y = +-0);
 - threshold tests sat(fma(kv, kv, -fl(fl(K fl(b den)))^2)), which must come out
   exactly 0 or 1 (the model checks that no value lands strictly inside (0, 1));
-- at 3 bits the middle threshold's test picks which outer threshold to test
-  next, through nsel = fma(b1, fl(nt2 - nt0), nt0);
+- m by binary search: at 3 bits the middle threshold's test picks which outer
+  threshold to test next, through nsel = fma(b1, fl(nt2 - nt0), nt0); at 4
+  bits two levels of such picks (the last from two picked candidates);
 - s (2m+1) summed into float chunks of C = 21 // bits codes weighted
   2^(bits i) on top of 1.5*2^23 + (2H-1) * (sum of weights), which must stay
   exact integers below 2^22 above 1.5*2^23;
@@ -60,7 +61,16 @@ def fast_path_words(y, den, bits, bnd):
         acc.append(M + wsum)
     for j in range(32):
         kv = F32(F32(y[j]) * F32(-K) + F32(0.0))  # fma(y, -K, 0): exact product (power of two)
-        if bits == 3:
+        if bits == 4:
+            b1 = sat_fma(kv, kv, nt[3])
+            n2 = nt[1] if b1 == 0 else F32(F32(nt[5] - nt[1]) + nt[1])
+            b2 = sat_fma(kv, kv, n2)
+            lo = nt[0] if b1 == 0 else F32(F32(nt[4] - nt[0]) + nt[0])
+            hi = nt[2] if b1 == 0 else F32(F32(nt[6] - nt[2]) + nt[2])
+            n3 = lo if b2 == 0 else F32(F32(hi - lo) + lo)
+            b3 = sat_fma(kv, kv, n3)
+            q = 8 * b1 + 4 * b2 + 2 * b3 + 1
+        elif bits == 3:
             b1 = sat_fma(kv, kv, nt[1])
             d = F32(nt[2] - nt[0])
             nsel = nt[0] if b1 == 0 else F32(d + nt[0])
@@ -94,7 +104,7 @@ def pack_le(idx, bits):
     return [(v >> (32 * k)) & 0xFFFFFFFF for k in range(bits)]
 
 
-@pytest.mark.parametrize("bits", [2, 3])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_fast_index_matches_exact_count(bits):
     """Codes equal the exact count away from boundaries; within 1e-6 of one, either
     neighbouring cell (the squared tests round fl(b den)^2, and at 3 bits the
@@ -124,7 +134,7 @@ def test_fast_index_matches_exact_count(bits):
 
 def test_signed_zero_takes_the_lower_middle_cell():
     """y = +0 and -0 are not above the middle boundary 0: index 2^(bits-1) - 1."""
-    for bits in (2, 3):
+    for bits in (2, 3, 4):
         _, bnd = oracle.codebook(bits)
         y = np.full(32, F32(0.0), dtype=F32)
         y[1::2] = F32(-0.0)
@@ -136,7 +146,7 @@ def test_signed_zero_takes_the_lower_middle_cell():
 def test_extreme_scales(den):
     """The per-group power of two keeps every test saturating and every chunk exact
     from the smallest den (rms 0: den = 1e-8) to the largest finite ones."""
-    for bits in (2, 3):
+    for bits in (2, 3, 4):
         _, bnd = oracle.codebook(bits)
         d = F32(den)
         rng = np.random.default_rng(int(np.log10(den) + 20) * 10 + bits)
