@@ -55,7 +55,10 @@ struct GenParams {
     int64_t cap, seq_len, tokens_per_split;
     int64_t base0;                                 // seq_len - M + 1: query row i sees rows [0, base0 + i)
     int rbk, rbv;                                  // packed row bytes of keys and values
-    int off_ks, off_kz, off_vs, off_v, stage_bytes;  // stage layout (keys at 0)
+    // ring layout: the key tiles of all slots (key_bytes each, 1024-byte multiples
+    // for swizzled tiles), then the other planes of all slots (stage_bytes each,
+    // at offsets off_ks .. off_v)
+    int off_ks, off_kz, off_vs, off_v, stage_bytes, key_bytes;
     float scale_log2, koff;                        // softmax scale * log2(e); f16 offset of a key code
     uint16_t cen[256];                             // value centroids as f16 bits
 };
@@ -126,6 +129,15 @@ __device__ __forceinline__ uint2 g_lds64(uint32_t a)
     return v;
 }
 
+__device__ __forceinline__ void g_tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
 // Key codes of dims 32G + 8c .. +7 of one packed row -> four f16x2 pairs
 // (dims 2p, 2p+1), each half koff + code with koff = 1024 (unsigned codes) or
 // 1152 (int8 codes, stored offset by 128).  KEY 8 and 4: the 8 codes are one
@@ -162,6 +174,48 @@ __device__ __forceinline__ void key_pairs(uint32_t row, int G, int c, int kb, ui
     }
 }
 
+// 8- and 4-bit key tiles arrive by tensor copies with a shared-memory swizzle:
+// boxes of BOXB bytes (32, 64 or 128, the row or a 128-byte slice of it) x
+// gT rows, the 16-byte chunk index of a row xor-ed with row bits, so the
+// rows a half-warp reads in one fragment load fall on different banks.
+template <int D, int KEY>
+struct KSwz {
+    static constexpr int RB = D * KEY / 8;
+    static constexpr int BOXB = RB < 128 ? RB : 128;
+    static constexpr int NBOX = RB / BOXB;
+};
+
+// Shared address of byte `off` of stage row r of a swizzled key tile.
+template <int D, int KEY>
+__device__ __forceinline__ uint32_t ksw_addr(uint32_t st, int r, int off)
+{
+    using K = KSwz<D, KEY>;
+    const int box = off / K::BOXB, col = off % K::BOXB;
+    const int x = K::BOXB == 128 ? (r & 7) : K::BOXB == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1);
+    return st + box * (gT * K::BOXB) + r * K::BOXB + ((((col >> 4) ^ x)) << 4) + (col & 15);
+}
+
+// The key pairs of key_pairs<8> / <4> from a swizzled tile.
+template <int D, int KEY>
+__device__ __forceinline__ void key_pairs_sw(uint32_t st, int r, int G, int c, uint32_t (&pr)[4])
+{
+    if constexpr (KEY == 8) {
+        const uint2 w = g_lds64(ksw_addr<D, 8>(st, r, (4 * G + c) * 8));
+        const uint32_t l = w.x ^ 0x80808080u, h = w.y ^ 0x80808080u;  // int8 -> code + 128
+        pr[0] = __byte_perm(l, 0x64646464u, 0x5140);
+        pr[1] = __byte_perm(l, 0x64646464u, 0x5342);
+        pr[2] = __byte_perm(h, 0x64646464u, 0x5140);
+        pr[3] = __byte_perm(h, 0x64646464u, 0x5342);
+    } else {
+        const uint32_t x = g_lds32(ksw_addr<D, 4>(st, r, (4 * G + c) * 4));  // codes k at bits 4k
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t t = x >> (8 * p);  // codes 2p, 2p+1 at bits 0-3, 4-7
+            pr[p] = ((t & 0x0Fu) | ((t << 12) & 0x000F0000u)) | 0x64006400u;
+        }
+    }
+}
+
 // Value codes of dims 32G + 4g .. +3 of one packed row -> their f16 centroids.
 __device__ __forceinline__ void value_quad(uint32_t row, int G, int g, int vb, uint32_t lut, uint32_t (&h)[4])
 {
@@ -178,7 +232,10 @@ struct GGeo {
     static constexpr int NG = D / 32;
     static constexpr int KS = D / 16;                       // k-steps of QK^T, m-tiles of PV
     static constexpr int CB = gN * NB;                      // columns per CTA
-    static constexpr int QF = CB * KS * 4 * 8;              // q fragments: [column][k-step][c] x (b0, b1)
+    // q fragments: [column][k-step][c] x (b0, b1), columns QCOL bytes apart: the
+    // 32-byte pad puts the 4 columns a half-warp reads on different banks
+    static constexpr int QCOL = KS * 4 * 8 + 32;
+    static constexpr int QF = CB * QCOL;
     static constexpr int QS = (NG + 1) * CB * 4;            // group sums of the f16 q, then per-column score scale
     // warps per CTA and 16-row tiles per warp and stage (worked on together): 2 x 2,
     // except at head_dim 512, whose registers and stage ring leave room for two CTAs
@@ -197,19 +254,23 @@ struct GGeo {
 // body).
 template <int D, int NB, int VLUT, int KEY>
 __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
-    attn_generic_kernel(const __grid_constant__ GenParams p)
+    attn_generic_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ GenParams p)
 {
     using A = GGeo<D, NB>;
     constexpr int CB = A::CB;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    const int ring = p.stages * p.stage_bytes > A::MERGE ? p.stages * p.stage_bytes : A::MERGE;
+    // 1024-byte alignment: swizzled key boxes start on a swizzle atom
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int ring_bytes = p.stages * (p.key_bytes + p.stage_bytes);
+    const int ring = ring_bytes > A::MERGE ? ring_bytes : A::MERGE;
     uint8_t *stages = smem;
     float *merge = reinterpret_cast<float *>(smem);
     uint8_t *qf = smem + ring;
     float *qsum = reinterpret_cast<float *>(qf + A::QF);
+    // the f16 centroid table in shared memory serves VLUT 0 only (the others
+    // look centroids up in registers)
     uint16_t *lut = reinterpret_cast<uint16_t *>(qf + A::QF + A::QS);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(qf + A::QF + A::QS + 512);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(qf + A::QF + A::QS + (VLUT == 0 ? 512 : 0));
     uint32_t *done = reinterpret_cast<uint32_t *>(bars + gMaxStages);
     const uint32_t full0 = smem_addr(bars);
 
@@ -231,9 +292,19 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
         const int64_t t = t_begin + (int64_t)s * gT;
         const int rows = (int)imin64(gT, p.cap - t);
         const int64_t row0 = bh * p.cap + t;
-        const uint32_t st = smem_addr(stages + slot * p.stage_bytes), bar = full0 + 8 * slot;
-        mbar_arrive_expect_tx(bar, (uint32_t)(rows * (p.rbk + p.rbv + 3 * NG * 2)));
-        bulk_g2s(st, p.k_codes + row0 * p.rbk, rows * p.rbk, bar);
+        const uint32_t kst = smem_addr(stages + slot * p.key_bytes), bar = full0 + 8 * slot;
+        const uint32_t st = smem_addr(stages + p.stages * p.key_bytes + slot * p.stage_bytes);
+        if constexpr (KEY != 0) {
+            // key rows by tensor copies (whole boxes; rows past the cache arrive as zeros)
+            using K = KSwz<D, KEY>;
+            mbar_arrive_expect_tx(bar, (uint32_t)(gT * K::RB + rows * (p.rbv + 3 * NG * 2)));
+#pragma unroll
+            for (int j = 0; j < K::NBOX; ++j)
+                g_tma_2d(kst + j * gT * K::BOXB, &kmap, j * K::BOXB, (int)row0, bar);
+        } else {
+            mbar_arrive_expect_tx(bar, (uint32_t)(rows * (p.rbk + p.rbv + 3 * NG * 2)));
+            bulk_g2s(kst, p.k_codes + row0 * p.rbk, rows * p.rbk, bar);
+        }
         bulk_g2s(st + p.off_ks, p.k_scale + row0 * NG, rows * NG * 2, bar);
         bulk_g2s(st + p.off_kz, p.k_zero + row0 * NG, rows * NG * 2, bar);
         bulk_g2s(st + p.off_vs, p.v_scale + row0 * NG, rows * NG * 2, bar);
@@ -247,7 +318,8 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
         fence_mbar_init();
         for (int s = 0; s < p.stages && s < n_stages; ++s) issue(s);
     }
-    for (int i = threadIdx.x; i < (1 << p.vb); i += blockDim.x) lut[i] = p.cen[i];
+    if constexpr (VLUT == 0)
+        for (int i = threadIdx.x; i < (1 << p.vb); i += blockDim.x) lut[i] = p.cen[i];
 
     // ---------------------------------------------------------------- q of the CTA's columns
     // Per block of 8 columns, warp w prepares columns 2w, 2w+1; lane l holds
@@ -290,7 +362,7 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
             f[1] = __high2float(*reinterpret_cast<__half2 *>(&hw[0]));
             f[2] = __low2float(*reinterpret_cast<__half2 *>(&hw[1]));
             f[3] = __high2float(*reinterpret_cast<__half2 *>(&hw[1]));
-            uint32_t *slot = reinterpret_cast<uint32_t *>(qf + ((n * A::KS + 2 * G + jj) * 4 + c) * 8);
+            uint32_t *slot = reinterpret_cast<uint32_t *>(qf + n * A::QCOL + ((2 * G + jj) * 4 + c) * 8);
             slot[0] = hw[0];
             slot[1] = hw[1];
             float s = (f[0] + f[1]) + (f[2] + f[3]);
@@ -325,13 +397,13 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
     // c0..c7, then high bytes); VLUT 2: the four f16 centroids, two per register
     uint32_t tl0 = 0, tl1 = 0, th0 = 0, th1 = 0;
     if constexpr (VLUT == 2) {
-        tl0 = (uint32_t)lut[0] | ((uint32_t)lut[1] << 16);
-        tl1 = (uint32_t)lut[2] | ((uint32_t)lut[3] << 16);
+        tl0 = (uint32_t)p.cen[0] | ((uint32_t)p.cen[1] << 16);
+        tl1 = (uint32_t)p.cen[2] | ((uint32_t)p.cen[3] << 16);
     }
     if constexpr (VLUT == 3)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t cb = lut[i], sh = 8 * (i & 3);
+            const uint32_t cb = p.cen[i], sh = 8 * (i & 3);
             if (i < 4) {
                 tl0 |= (cb & 0xFFu) << sh;
                 th0 |= (cb >> 8) << sh;
@@ -340,8 +412,8 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
                 th1 |= (cb >> 8) << sh;
             }
         }
-    constexpr int QF_NB = gN * A::KS * 4 * 8;  // bytes of q fragments per block of 8 columns
-    const uint32_t qf_lane = smem_addr(qf) + (g * A::KS * 4 + c) * 8, lut_a = smem_addr(lut);
+    constexpr int QF_NB = gN * A::QCOL;  // bytes of q fragments per block of 8 columns
+    const uint32_t qf_lane = smem_addr(qf) + g * A::QCOL + c * 8, lut_a = smem_addr(lut);
 
     bool ok = true;
     for (int s = 0; s < n_stages; ++s) {
@@ -350,7 +422,8 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
             ok = false;
             break;
         }
-        const uint32_t st = smem_addr(stages + slot * p.stage_bytes);
+        const uint32_t kst = smem_addr(stages + slot * p.key_bytes);
+        const uint32_t st = smem_addr(stages + p.stages * p.key_bytes + slot * p.stage_bytes);
         const int64_t tile_t0 = t_begin + (int64_t)s * gT + 16 * warp;  // first row of tile 0
 
         // ---------------- S = Q K^T, group by group, with the group affine, for
@@ -371,8 +444,13 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
             for (int t2 = 0; t2 < A::TILES; ++t2) {
                 const int ra = r0 + TR * t2, rb = r1 + TR * t2;
                 uint32_t k0[4], k1[4];
-                key_pairs<KEY>(st + ra * p.rbk, G, c, p.kb, k0);
-                key_pairs<KEY>(st + rb * p.rbk, G, c, p.kb, k1);
+                if constexpr (KEY != 0) {
+                    key_pairs_sw<D, KEY>(kst, ra, G, c, k0);
+                    key_pairs_sw<D, KEY>(kst, rb, G, c, k1);
+                } else {
+                    key_pairs<KEY>(kst + ra * p.rbk, G, c, p.kb, k0);
+                    key_pairs<KEY>(kst + rb * p.rbk, G, c, p.kb, k1);
+                }
                 const float sc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (ra * NG + G) * 2));
                 const float sc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (rb * NG + G) * 2));
                 const float zc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (ra * NG + G) * 2)) - p.koff;
@@ -771,7 +849,7 @@ struct GenPlan {
     int vlut;  // VLUT of the instantiation: 3 or 2 for 3- or 2-bit values, else 0
     int key;   // KEY of the instantiation: 8 or 4 for 8- or 4-bit keys, else 0
     int64_t tokens_per_split;
-    int off_ks, off_kz, off_vs, off_v;
+    int off_ks, off_kz, off_vs, off_v, key_bytes;
 };
 
 // blocks of 8 columns per CTA: enough to cover the columns of one kv-head in
@@ -809,15 +887,19 @@ bool gen_plan_nb(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, Ge
     auto r16 = [](int x) { return (x + 15) / 16 * 16; };
     pl.nb = NB;
     pl.vlut = c.vb == 3 ? 3 : (c.vb == 2 ? 2 : 0);
-    pl.key = c.kb == 8 ? 8 : (c.kb == 4 ? 4 : 0);
-    pl.off_ks = r16(gT * rbk);
+    // 8- and 4-bit keys take swizzled tensor copies (row coordinates are 32-bit)
+    pl.key = (int64_t)c.B * c.H * c.cap < (int64_t(1) << 31) ? (c.kb == 8 ? 8 : (c.kb == 4 ? 4 : 0)) : 0;
+    pl.key_bytes = pl.key != 0 ? (gT * rbk + 1023) / 1024 * 1024 : r16(gT * rbk);
+    pl.off_ks = 0;
     pl.off_kz = pl.off_ks + r16(gT * NG * 2);
     pl.off_vs = pl.off_kz + r16(gT * NG * 2);
     pl.off_v = pl.off_vs + r16(gT * NG * 2);
-    pl.stage_bytes = (pl.off_v + gT * rbv + 16 + 127) / 128 * 128;
+    pl.stage_bytes = r16(pl.off_v + gT * rbv + 16);
     pl.stages = 2;  // with 2-warp CTAs a deeper ring only costs resident CTAs
-    const int ring = pl.stages * pl.stage_bytes > A::MERGE ? pl.stages * pl.stage_bytes : A::MERGE;
-    pl.smem = 128 /*align slack*/ + ring + A::QF + A::QS + 512 /*lut*/ + gMaxStages * 12 /*barriers, counters*/;
+    const int ring = pl.stages * (pl.key_bytes + pl.stage_bytes) > A::MERGE ? pl.stages * (pl.key_bytes + pl.stage_bytes)
+                                                                           : A::MERGE;
+    pl.smem = 1024 /*align slack*/ + ring + A::QF + A::QS + (pl.vlut == 0 ? 512 : 0) /*lut*/ +
+              gMaxStages * 12 /*barriers, counters*/;
     const int per_sm = gen_dispatch<D, NB>(pl, [&](auto kern) {
         int n = 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) != cudaSuccess) return 0;
@@ -861,12 +943,31 @@ bool gen_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, GenPl
 }
 
 template <int D, int NB>
-void gen_launch(const GenPlan &pl, dim3 grid, const GenParams &p, cudaStream_t s)
+void gen_launch(const GenPlan &pl, dim3 grid, const CUtensorMap &kmap, const GenParams &p, cudaStream_t s)
 {
     gen_dispatch<D, NB>(pl, [&](auto kern) {
-        kern<<<grid, GGeo<D, NB>::THREADS, pl.smem, s>>>(p);
+        kern<<<grid, GGeo<D, NB>::THREADS, pl.smem, s>>>(kmap, p);
         return 0;
     });
+}
+
+// Tensor map over the key plane for the swizzled key tiles of 8- and 4-bit
+// keys: [B H cap rows][row bytes], boxes of BOXB bytes x gT rows.
+template <int D>
+bool gen_key_map(const CacheView &c, CUtensorMap *map)
+{
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const int rb = D * c.kb / 8, boxb = rb < 128 ? rb : 128;
+    const cuuint64_t gdim[2] = {(cuuint64_t)rb, (cuuint64_t)c.B * c.H * c.cap};
+    const cuuint64_t gstride[1] = {(cuuint64_t)rb};
+    const cuuint32_t box[2] = {(cuuint32_t)boxb, (cuuint32_t)gT};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUtensorMapSwizzle sw = boxb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : boxb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k_codes, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D>
@@ -919,16 +1020,19 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     p.off_vs = pl.off_vs;
     p.off_v = pl.off_v;
     p.stage_bytes = pl.stage_bytes;
+    p.key_bytes = pl.key_bytes;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.koff = c.kb == 8 ? 1152.0f : 1024.0f;
     const Tables &tab = codebook_tables(c.vb);
     for (int i = 0; i < (1 << c.vb); ++i) p.cen[i] = __half_as_ushort(__float2half_rn(tab.centroids[i]));
     if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
+    CUtensorMap kmap{};
+    if (pl.key != 0 && !gen_key_map<D>(c, &kmap)) return cudaErrorInvalidValue;
     const dim3 grid(pl.splits, c.H * pl.hb, c.B);
     switch (pl.nb) {
-    case 1: gen_launch<D, 1>(pl, grid, p, s); break;
-    case 2: if constexpr (D <= 256) gen_launch<D, 2>(pl, grid, p, s); break;
-    case 4: if constexpr (D <= 128) gen_launch<D, 4>(pl, grid, p, s); break;
+    case 1: gen_launch<D, 1>(pl, grid, kmap, p, s); break;
+    case 2: if constexpr (D <= 256) gen_launch<D, 2>(pl, grid, kmap, p, s); break;
+    case 4: if constexpr (D <= 128) gen_launch<D, 4>(pl, grid, kmap, p, s); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
