@@ -603,29 +603,34 @@ struct CombineParams {
     SignBits sg;  // value signs
 };
 
-// One CTA of kCombineWarps warps per (sequence, q-head); lane holds dims
-// 4 lane .. 4 lane + 3.  Warp w merges the splits w, w + kCombineWarps, ...
-// in chunks of 32: the chunk's (max, sum) pairs are read one per lane, the
-// weights 2^(m_s - m) computed one per lane and broadcast, and the chunk's
-// output rows read with independent loads (all in flight at once), so a few
-// hundred splits (batch 1) cost a handful of memory round trips, not one per
-// split.  Warp 0 then merges the warps' results.
+// CTAs of kCombineWarps warps; each (sequence, q-head) row takes W of them
+// (W = 8 for a few hundred splits at batch 1, fewer when there are few
+// splits, so small merges are not spread thin).  Lane holds dims 4 lane ..
+// 4 lane + 3.  Warp w of a row merges the splits w, w + W, ... in chunks of
+// 32: the chunk's (max, sum) pairs are read one per lane, the weights
+// 2^(m_s - m) computed one per lane and broadcast, and the chunk's output
+// rows read with independent loads, so many splits cost a handful of memory
+// round trips, not one per split.  The row's first warp then merges its
+// warps' results.
 constexpr int kCombineWarps = 8;
 
+template <int W>
 __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const __grid_constant__ CombineParams p)
 {
-    __shared__ float4 wo[kCombineWarps][32];
+    __shared__ float4 wo[W > 1 ? kCombineWarps : 1][32];
     __shared__ float wm[kCombineWarps], wl[kCombineWarps];
-    const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (kCombineWarps / W) + warp / W, wid = warp % W, lead = warp - wid;
+    const bool live = row < p.rows;
+    if (W == 1 && !live) return;  // no barrier below when W = 1
     const int b = row / p.QH, qh = row % p.QH;
     const int h = qh / p.G, hq = qh % p.G;
     const int hh = hq % kG;  // column of block hq / kG
     const int64_t base = ((int64_t)b * p.H * p.NB + (int64_t)h * p.NB + hq / kG) * p.splits;
-    // this warp's splits: warp + kCombineWarps * i, i = 0 .. n_mine - 1
-    const int n_mine = p.splits > warp ? (p.splits - warp + kCombineWarps - 1) / kCombineWarps : 0;
+    // this warp's splits: wid + W i, i = 0 .. n_mine - 1
+    const int n_mine = live && p.splits > wid ? (p.splits - wid + W - 1) / W : 0;
     float mw = -INFINITY;
-    for (int i = lane; i < n_mine; i += 32)
-        mw = fmaxf(mw, p.part_ml[2 * ((base + warp + (int64_t)kCombineWarps * i) * kG + hh)]);
+    for (int i = lane; i < n_mine; i += 32) mw = fmaxf(mw, p.part_ml[2 * ((base + wid + (int64_t)W * i) * kG + hh)]);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
     const float muw = mw == -INFINITY ? 0.0f : mw;
@@ -635,7 +640,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
         // lane j: weight and sum of split i0 + j
         float wt = 0.0f;
         if (i0 + lane < n_mine) {
-            const int64_t pi = (base + warp + (int64_t)kCombineWarps * (i0 + lane)) * kG + hh;
+            const int64_t pi = (base + wid + (int64_t)W * (i0 + lane)) * kG + hh;
             const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * pi);
             wt = ex2(ml.x - muw);
             lw += ml.y * wt;
@@ -644,32 +649,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
 #pragma unroll 8
         for (int j = 0; j < cnt; ++j) {
             const float w = __shfl_sync(0xffffffffu, wt, j);
-            const int64_t pi = (base + warp + (int64_t)kCombineWarps * (i0 + j)) * kG + hh;
+            const int64_t pi = (base + wid + (int64_t)W * (i0 + j)) * kG + hh;
             const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pi * kD + 4 * lane);
             xw.x += v.x * w; xw.y += v.y * w; xw.z += v.z * w; xw.w += v.w * w;
         }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-    wo[warp][lane] = xw;
-    if (lane == 0) {
-        wm[warp] = mw;
-        wl[warp] = lw;
-    }
-    __syncthreads();
-    if (warp != 0) return;
-    float mmax = -INFINITY;
+    float x[4] = {xw.x, xw.y, xw.z, xw.w}, l = lw;
+    if constexpr (W > 1) {
+        wo[warp][lane] = xw;
+        if (lane == 0) {
+            wm[warp] = mw;
+            wl[warp] = lw;
+        }
+        __syncthreads();
+        if (wid != 0 || !live) return;
+        float mmax = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) mmax = fmaxf(mmax, wm[w]);
-    const float mu = mmax == -INFINITY ? 0.0f : mmax;
-    float x[4] = {0, 0, 0, 0}, l = 0.0f;
+        for (int w = 0; w < W; ++w) mmax = fmaxf(mmax, wm[lead + w]);
+        const float mu = mmax == -INFINITY ? 0.0f : mmax;
+        l = 0.0f;
+        x[0] = x[1] = x[2] = x[3] = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {
-        // a warp without live splits carries zeros; the others rescale to the common max
-        const float wt = wm[w] == -INFINITY ? 0.0f : ex2(wm[w] - mu);
-        l += wl[w] * wt;
-        const float4 v = wo[w][lane];
-        x[0] += v.x * wt; x[1] += v.y * wt; x[2] += v.z * wt; x[3] += v.w * wt;
+        for (int w = 0; w < W; ++w) {
+            // a warp without live splits carries zeros; the others rescale to the common max
+            const float wt = wm[lead + w] == -INFINITY ? 0.0f : ex2(wm[lead + w] - mu);
+            l += wl[lead + w] * wt;
+            const float4 v = wo[lead + w][lane];
+            x[0] += v.x * wt; x[1] += v.y * wt; x[2] += v.z * wt; x[3] += v.w * wt;
+        }
     }
     const float inv_l = 1.0f / l;
 #pragma unroll
@@ -828,7 +837,12 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
     cp.sg = c.signs;
-    attn_combine_kernel<<<cp.rows, kCombineWarps * 32, 0, s>>>(cp);
+    if (plan.splits >= 64)
+        attn_combine_kernel<8><<<cp.rows, kCombineWarps * 32, 0, s>>>(cp);
+    else if (plan.splits >= 16)
+        attn_combine_kernel<2><<<(cp.rows + 3) / 4, kCombineWarps * 32, 0, s>>>(cp);
+    else
+        attn_combine_kernel<1><<<(cp.rows + 7) / 8, kCombineWarps * 32, 0, s>>>(cp);
     return cudaGetLastError();
 }
 
