@@ -161,3 +161,58 @@ def test_pv_fragments_and_merge_give_the_weighted_sum():
     group_rms = np.repeat(rms, 32, axis=1)  # [token][dim]
     want = P.T @ (V * group_rms)
     assert np.array_equal(merged, want)
+
+
+# ---------------------------------------------------------------- generic kernel: swizzled key stages
+def tma_stage_image(codes_bytes, rb, boxb):
+    """Shared-memory image of one 64-row stage of `rb`-byte key rows brought in by
+    tensor copies of boxes of `boxb` bytes x 64 rows, box j at j * 64 * boxb, with
+    the TMA swizzle of a `boxb`-byte span: bits 4.. of the offset inside the box
+    (the 16-byte chunk) xor-ed with the same number of bits from bit 7 up."""
+    nbits = {128: 3, 64: 2, 32: 1}[boxb]
+    img = np.zeros(64 * rb, dtype=np.uint8)
+    for j in range(rb // boxb):
+        for r in range(64):
+            for col in range(boxb):
+                lin = r * boxb + col  # offset inside the box before the swizzle
+                sw = lin ^ (((lin >> 7) & ((1 << nbits) - 1)) << 4)
+                img[j * 64 * boxb + sw] = codes_bytes[r, j * boxb + col]
+    return img
+
+
+def ksw_addr(r, off, boxb):
+    """The kernel's read address of byte `off` of stage row r (its per-mode form)."""
+    box, col = off // boxb, off % boxb
+    x = (r & 7) if boxb == 128 else ((r >> 1) & 3) if boxb == 64 else ((r >> 2) & 1)
+    return box * 64 * boxb + r * boxb + (((col >> 4) ^ x) << 4) + (col & 15)
+
+
+@pytest.mark.parametrize("d,kb", [(d, kb) for d in (64, 128, 256, 512) for kb in (4, 8)])
+def test_generic_swizzled_key_reads(d, kb):
+    """Every key word a lane of the generic kernel reads, at every row of a stage,
+    is the packed row's word at that offset; and the lanes served together
+    (a half-warp for 8-byte loads, the warp for 4-byte ones; lane = 4 g + c,
+    row g) conflict at most two ways per load."""
+    rb = d * kb // 8
+    boxb = min(rb, 128)
+    rng = np.random.default_rng(d + kb)
+    raw = rng.integers(0, 256, size=(64, rb), dtype=np.uint8)
+    img = tma_stage_image(raw, rb, boxb)
+    width = 8 if kb == 8 else 4  # bytes one lane loads per group
+    for G in range(d // 32):
+        for r in range(64):
+            for c in range(4):
+                off = (4 * G + c) * width
+                a = ksw_addr(r, off, boxb)
+                assert bytes(img[a:a + width]) == bytes(raw[r, off:off + width])
+        groups = ((0, 4), (4, 8)) if width == 8 else ((0, 8),)
+        for base in (0, 8, 16, 40):  # the rows of a tile: 16 warp + g (+ 8) + 32 tile
+            for g0, g1 in groups:
+                words = {}
+                for g in range(g0, g1):
+                    for c in range(4):
+                        a = ksw_addr(base + g, (4 * G + c) * width, boxb)
+                        for w in range(width // 4):
+                            bank = (a // 4 + w) % 32
+                            words.setdefault(bank, set()).add(a // 4 + w)
+                assert max(len(v) for v in words.values()) <= 2
