@@ -918,6 +918,8 @@ PROFILE_CASES = {
     "generic_attention_d256_k8v3_b4": ("attention", 256, 8, 3, 4, 8, 32769, 8),
     "generic_attention_d64_k8v3_b8": ("attention", 64, 8, 3, 8, 8, 32769, 8),
     "generic_attention_d128_k8v4_b4": ("attention", 128, 8, 4, 4, 8, 32769, 8),
+    # multi-token attention: M = 128 query rows per sequence (the tcgen05 kernel)
+    "multi_token_m128_b2": ("multi128", 128, 8, 3, 2, 8, 32769, 8),
 }
 
 
@@ -947,6 +949,16 @@ def run_profile_case(name: str, reps: int) -> None:
         for _ in range(reps):
             tq.tq_encode_append(cache, k16, v16, 0)
             tq.tq_decode(cache, 0, T, dtype=torch.bfloat16, k_out=ko, v_out=vo)
+    elif op == "multi128":
+        del k, v, k16, v16
+        M = 128
+        q = torch.empty((B, M * G * H, d), dtype=torch.int16, device=dev)
+        tq_synth.device_q(w, 0, q, B=B, QH=M * G * H, d=d)
+        qm = q.view(torch.bfloat16).view(B, M, G * H, d)
+        out = torch.empty((B, M, G * H, d), dtype=torch.float32, device=dev)
+        ws = torch.empty(tq.tq_multi_token_workspace_bytes(cache, G * H, M, T), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            tq.tq_multi_token_attention(cache, qm, T, out=out, workspace=ws)
     else:
         del k, v, k16, v16
         q = torch.empty((B, G * H, d), dtype=torch.int16, device=dev)
