@@ -434,12 +434,14 @@ def run_ours(args, rank, world, local_rank):
 # ------------------------------------------------------------------ the other configurations
 def flushing_timer(torch, dev):
     """fn's median device time in µs over `reps` calls, each call preceded by a
-    write of a buffer twice the size of L2 (so its inputs come from HBM) and
-    bracketed by CUDA events on the launching stream; a device spin queued
-    first keeps host launch time out of the marks."""
+    read of a buffer twice the size of L2 (so its inputs come from HBM, and the
+    previous call's dirty lines are written back before the marks, not inside
+    them) and bracketed by CUDA events on the launching stream; a device spin
+    queued first keeps host launch time out of the marks."""
     st = torch.cuda.current_stream()
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def timed(fn, reps=10, warmup=3):
         for _ in range(warmup):
@@ -448,7 +450,7 @@ def flushing_timer(torch, dev):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         torch.cuda._sleep(PRIME_CYCLES)
         for a, b in evs:
-            flush.zero_()
+            torch.sum(flush, dim=0, out=sink)  # reads the whole buffer
             a.record(st)
             fn()
             b.record(st)
@@ -593,6 +595,45 @@ def measure_configs(tq, tq_synth, torch, dev, dcache, knew, vnew, q, T, rank, st
                 nbytes[name + "_encode"] = nbytes[name + "_decode"] = H * Ts * (4 * d + cb)
                 del c
         del k, v, k16, v16, ko, vo
+
+    # the follow-up paths: multi-token attention (chunks of M = 4 and 128 query
+    # rows over 8 sequences of the decode cache), the deferred fetch and its
+    # un-rotation, row copy and clear (a prefill-shaped cache)
+    D, nb8 = DECODE, min(8, dcache.batch)
+    c8 = dcache.batch_slice(0, nb8)
+    wd = tq_synth.WORKLOADS["decode"]
+    for M in (4, 128):
+        qm = torch.empty((nb8, M * D["QH"], D["d"]), dtype=torch.int16, device=dev)
+        tq_synth.device_q(wd, 0, qm, B=nb8, QH=M * D["QH"], d=D["d"])
+        qmb = qm.view(torch.bfloat16).view(nb8, M, D["QH"], D["d"])
+        om = torch.empty((nb8, M, D["QH"], D["d"]), dtype=torch.float32, device=dev)
+        wsm = torch.empty(tq.tq_multi_token_workspace_bytes(c8, D["QH"], M, T + 1), dtype=torch.uint8, device=dev)
+        name = f"multi_token_m{M}"
+        times[name] = timed(lambda: tq.tq_multi_token_attention(c8, qmb, T + 1, out=om, workspace=wsm), reps=5)
+        nbytes[name] = nb8 * D["H"] * (T + 1) * bpt + nb8 * M * D["QH"] * D["d"] * 6
+        nbytes[name + "_flops"] = 4.0 * D["d"] * D["QH"] * M * nb8 * (T + 1)  # MMA work of one call
+        del qm, qmb, om, wsm
+    P = PREFILL
+    pc = tq.Cache(P["B"], P["H"], P["d"], P["T"], P["kb"], P["vb"], device=dev)
+    kc = torch.empty((P["B"], P["H"], P["T"], P["d"]), dtype=torch.int16, device=dev)
+    vc = torch.empty_like(kc)
+    tq_synth.device_kv(tq_synth.WORKLOADS["prefill"], kc, vc)
+    tq.tq_encode_append(pc, kc.view(torch.bfloat16), vc.view(torch.bfloat16), 0)
+    rows = P["B"] * P["H"] * P["T"]
+    vr = vc.view(torch.bfloat16)  # reused as the output buffers
+    times["rotated_fetch"] = timed(lambda: tq.tq_decode_values_rotated(pc, 0, P["T"], dtype=torch.bfloat16, out=vr))
+    nbytes["rotated_fetch"] = rows * (P["d"] * P["vb"] // 8 + 2 * P["d"] // 32 + 2 * P["d"])
+    xr = kc.view(torch.float32).view(rows // 2, P["d"])  # 134 MB of rows un-rotated in place
+    xr.normal_()
+    times["unrotate"] = timed(lambda: tq.tq_unrotate(xr, out=xr))
+    nbytes["unrotate"] = 2 * xr.numel() * 4
+    snap = tq.Cache(P["B"], P["H"], P["d"], P["T"], P["kb"], P["vb"], device=dev)
+    fmt = rows * tq.tq_bytes_per_token_head(P["d"], P["kb"], P["vb"])
+    times["copy_rows"] = timed(lambda: tq.tq_cache_copy_rows(snap, 0, pc, 0, P["T"]))
+    nbytes["copy_rows"] = 2 * fmt
+    times["clear_rows"] = timed(lambda: tq.tq_cache_clear_rows(snap, 0, P["T"]))
+    nbytes["clear_rows"] = fmt
+    del pc, snap, kc, vc, vr, xr
     assert tq.tq_device_error() == 0
     return times, nbytes
 
@@ -610,6 +651,21 @@ def config_parts(times, nbytes, peak):
                     "attention": rate(nbytes[pre + "_attention"], times[pre + "_attention"], peak),
                     "append_1_token": rate(nbytes[pre + "_append"], times[pre + "_append"], peak),
                     "step_graph": rate(nbytes[pre + "_step_graph"], times[pre + "_step_graph"], peak)}
+    for name, desc in (("multi_token_m4", "causal attention of chunks of 4 query rows, 8 sequences x 8 kv-heads x "
+                                          "32769 rows, 64 q-heads, d128 k8v3 (mma.sync kernel)"),
+                       ("multi_token_m128", "causal attention of chunks of 128 query rows, same cache (tcgen05 kernel)")):
+        if name in times:
+            r = rate(nbytes[name], times[name], peak)
+            tf = nbytes[name + "_flops"] / (times[name] * 1e-6) / 1e12
+            tpeak, tkind = measured_bf16_tflops()
+            out[name] = {"workload": desc, **r, "TFLOP/s": round(tf, 1), "tensor_frac": round(tf / tpeak, 4),
+                         "tensor_peak": tpeak, "tensor_peak_kind": tkind}
+    for name, desc in (("rotated_fetch", "values in the rotated domain, 4 x 8 x 8192 rows, d128 v3, bf16 out"),
+                       ("unrotate", "un-rotation of 131072 rows of d128, fp32 in place"),
+                       ("copy_rows", "row copy between caches, 4 x 8 x 8192 rows, d128 k8v3"),
+                       ("clear_rows", "row clear, 4 x 8 x 8192 rows, d128 k8v3")):
+        if name in times:
+            out[name] = {"workload": desc, **rate(nbytes[name], times[name], peak)}
     cells = {}
     for k_ in sorted(times):
         if k_.startswith("sweep_") and k_.endswith("_encode"):
@@ -618,7 +674,7 @@ def config_parts(times, nbytes, peak):
                            for op in ("encode", "decode")}
     if cells:
         out["sweep_codec"] = {"workload": "8 kv-heads x 16384 tokens, K ~ N(0,1) x logN(0,1), V ~ N(0,1); "
-                                          "encode bf16 -> packed, fetch packed -> bf16; L2 flushed before each call",
+                                          "encode bf16 -> packed, fetch packed -> bf16; L2 flushed (a read of twice its size) before each call",
                               "cells": cells}
     return out
 
