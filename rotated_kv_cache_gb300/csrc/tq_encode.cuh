@@ -707,12 +707,21 @@ __device__ __forceinline__ void encode_body(const EncodeParams &p, const CUtenso
     if (!KEY && lane == 0) bulk_wait0();
 }
 
+// An append is two launches, keys then values, on one stream.  The value
+// launch is a programmatic dependent of the key launch: the key kernel allows
+// it to start at once, so value CTAs take the SMs that key CTAs leave in the
+// key kernel's last round, and the value kernel waits for the key grid only
+// before it ends (it touches none of the key planes; the wait keeps stream
+// order for whatever is queued after the append).  Without a programmatic
+// dependency both instructions do nothing.
 template <int D, int BITS, bool KEY>
 __global__ void __launch_bounds__(kWarps * 32)
     encode_kernel(const __grid_constant__ EncodeParams p, const __grid_constant__ CUtensorMap map)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
+    if constexpr (KEY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     encode_body<D, BITS, KEY>(p, map, smem_raw, blockIdx.x, gridDim.x);
+    if constexpr (!KEY) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Keys and values of a small append in one launch (the two encodes of a
@@ -739,8 +748,10 @@ constexpr size_t encode_smem()
            G::MTAB + (size_t)kWarps * (KEY ? 0 : VStage<D, BITS>::BYTES);
 }
 
+// after_keys: the launch follows this append's key launch on the same stream
+// and becomes its programmatic dependent (values only)
 template <int D, int BITS, bool KEY>
-cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
+cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s, bool after_keys = false)
 {
     const size_t smem = encode_smem<D, BITS, KEY>();
     auto kern = encode_kernel<D, BITS, KEY>;
@@ -755,6 +766,19 @@ cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
     }
     const int64_t want = ((int64_t)p.items + kWarps - 1) / kWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
+    if (!KEY && after_keys) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kWarps * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, p, map);
+    }
     kern<<<grid, kWarps * 32, smem, s>>>(p, map);
     return cudaGetLastError();
 }
@@ -790,14 +814,14 @@ cudaError_t dispatch_key(int kb, const EncodeParams &p, const CUtensorMap &map, 
 }
 
 template <int D>
-cudaError_t dispatch_value(int vb, const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
+cudaError_t dispatch_value(int vb, const EncodeParams &p, const CUtensorMap &map, cudaStream_t s, bool after_keys)
 {
     switch (vb) {
-    case 2: return run<D, 2, false>(p, map, s);
-    case 3: return run<D, 3, false>(p, map, s);
-    case 4: return run<D, 4, false>(p, map, s);
-    case 5: return run<D, 5, false>(p, map, s);
-    case 8: return run<D, 8, false>(p, map, s);
+    case 2: return run<D, 2, false>(p, map, s, after_keys);
+    case 3: return run<D, 3, false>(p, map, s, after_keys);
+    case 4: return run<D, 4, false>(p, map, s, after_keys);
+    case 5: return run<D, 5, false>(p, map, s, after_keys);
+    case 8: return run<D, 8, false>(p, map, s, after_keys);
     }
     return cudaErrorInvalidValue;
 }
@@ -876,7 +900,7 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     }
     cudaError_t e = dispatch_key<D>(c.kb, pk, mk, s);
     if (e != cudaSuccess) return e;
-    return dispatch_value<D>(c.vb, pv, mv, s);
+    return dispatch_value<D>(c.vb, pv, mv, s, true);
 }
 
 }  // namespace
