@@ -60,7 +60,7 @@ typedef enum tq_status {
     TQ_ERR_BITS = 3,      /* k_bits not in {2,4,5,8} or v_bits not in {2,3,4,5,8} */
     TQ_ERR_SHAPE = 4,     /* batch/heads/tokens/strides out of range */
     TQ_ERR_CAPACITY = 5,  /* rows beyond the cache capacity */
-    TQ_ERR_ALIGN = 6,     /* pointer or stride not 16-byte aligned */
+    TQ_ERR_ALIGN = 6,     /* pointer or stride not aligned as the call requires (16 or 32 bytes) */
     TQ_ERR_WORKSPACE = 7, /* workspace missing or too small */
     TQ_ERR_CUDA = 8,      /* a CUDA launch or query failed */
     TQ_ERR_UNSUPPORTED = 9, /* valid codec parameters this kernel does not cover */
@@ -153,7 +153,7 @@ TQ_API tq_status tq_encode_append(const tq_cache *cache, const void *k, const in
  * bf16 (round to nearest even) or fp32 per out_dtype.  Either output may be
  * NULL to skip it.  Keys: (code + zero) * scale in fp32, the add first (page,
  * joint K/V decoder paragraph).  Values: signs * FWHT(centroid[code] * rms)
- * / sqrt(d) (the transform first, the sign multiply after it).  Outputs 16-byte aligned.
+ * / sqrt(d) (the transform first, the sign multiply after it).  Outputs 32-byte aligned.
  */
 TQ_API tq_status tq_decode(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype, void *k_out,
                     void *v_out, tq_stream_t stream);
@@ -165,7 +165,7 @@ TQ_API tq_status tq_decode(const tq_cache *cache, int64_t t0, int64_t n, tq_dtyp
  * product).  Page section "Deferred inverse FWHT": attention is linear in the
  * values, so an attention kernel outside this library can form its weighted
  * sum on these rows and bring the result back once per query row with
- * tq_unrotate.  v_out 16-byte aligned.
+ * tq_unrotate.  v_out 32-byte aligned.
  */
 TQ_API tq_status tq_decode_values_rotated(const tq_cache *cache, int64_t t0, int64_t n, tq_dtype out_dtype,
                                           void *v_out, tq_stream_t stream);
@@ -177,7 +177,7 @@ TQ_API tq_status tq_decode_values_rotated(const tq_cache *cache, int64_t t0, int
  * signs being tq_sign_vector(head_dim, sign_seed) -- the seed of the cache
  * the rows came from.
  *  x, out    device, [rows][head_dim] contiguous, fp32 or bf16 each
- *            (in_dtype, out_dtype); 16-byte aligned; out may equal x when the
+ *            (in_dtype, out_dtype); 32-byte aligned; out may equal x when the
  *            dtypes match (in place).
  * rows = 0 is a no-op.
  */

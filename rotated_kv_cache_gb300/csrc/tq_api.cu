@@ -62,6 +62,8 @@ bool valid_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256 || d == 
 bool valid_kbits(int32_t b) { return b == 2 || b == 4 || b == 5 || b == 8; }
 bool valid_vbits(int32_t b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 8; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// the fetch and un-rotation kernels move 32-byte words
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 tq_status check_cache(const tq_cache *c)
 {
@@ -129,7 +131,7 @@ const char *tq_status_string(tq_status s)
     case TQ_ERR_BITS: return "k_bits must be 2, 4, 5 or 8 and v_bits 2, 3, 4, 5 or 8";
     case TQ_ERR_SHAPE: return "shape, stride or count out of range";
     case TQ_ERR_CAPACITY: return "rows beyond the cache capacity";
-    case TQ_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case TQ_ERR_ALIGN: return "pointer or stride not aligned as the call requires";
     case TQ_ERR_WORKSPACE: return "workspace missing or too small";
     case TQ_ERR_CUDA: return "CUDA launch or query failed";
     case TQ_ERR_UNSUPPORTED: return "parameters not covered by this kernel";
@@ -208,7 +210,7 @@ tq_status tq_decode(const tq_cache *c, int64_t t0, int64_t n, tq_dtype dt, void 
     if (t0 + n > c->capacity) return TQ_ERR_CAPACITY;
     if (dt != TQ_BF16 && dt != TQ_F32) return TQ_ERR_SHAPE;
     if (n == 0 || (!k_out && !v_out)) return TQ_OK;
-    if ((k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out))) return TQ_ERR_ALIGN;
+    if ((k_out && !aligned32(k_out)) || (v_out && !aligned32(v_out))) return TQ_ERR_ALIGN;
     return cuda_status(tq::launch_decode(view(c), t0, n, dt == TQ_F32, k_out, v_out, (cudaStream_t)stream));
 }
 
@@ -222,7 +224,7 @@ tq_status tq_decode_values_rotated(const tq_cache *c, int64_t t0, int64_t n, tq_
     if (dt != TQ_BF16 && dt != TQ_F32) return TQ_ERR_SHAPE;
     if (n == 0) return TQ_OK;
     if (!v_out) return TQ_ERR_NULL;
-    if (!aligned16(v_out)) return TQ_ERR_ALIGN;
+    if (!aligned32(v_out)) return TQ_ERR_ALIGN;
     return cuda_status(tq::launch_decode_rotated(view(c), t0, n, dt == TQ_F32, v_out, (cudaStream_t)stream));
 }
 
@@ -233,7 +235,7 @@ tq_status tq_unrotate(int32_t d, uint64_t sign_seed, tq_dtype in_dt, const void 
     if ((in_dt != TQ_BF16 && in_dt != TQ_F32) || (out_dt != TQ_BF16 && out_dt != TQ_F32) || rows < 0) return TQ_ERR_SHAPE;
     if (rows == 0) return TQ_OK;
     if (!x || !out) return TQ_ERR_NULL;
-    if (!aligned16(x) || !aligned16(out)) return TQ_ERR_ALIGN;
+    if (!aligned32(x) || !aligned32(out)) return TQ_ERR_ALIGN;
     if (x == out && in_dt != out_dt) return TQ_ERR_SHAPE;  // in place only with equal element sizes
     return cuda_status(tq::launch_unrotate(d, sign_bits(sign_seed, d), in_dt == TQ_F32, x, rows, out_dt == TQ_F32, out,
                                             (cudaStream_t)stream));

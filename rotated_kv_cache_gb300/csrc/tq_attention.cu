@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
     uint32_t *done = reinterpret_cast<uint32_t *>(smem + A::RING + kStages * 8);
     const uint32_t full0 = smem_addr(bars);
 
+    pdl_allow_dependents();  // the merge launch waits for this grid's completion anyway
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // blockIdx.y = (kv-head, block of kG q-heads); the blocks of one kv-head are
     // neighbours in the grid, so their reads of the same rows meet in L2
@@ -603,25 +604,30 @@ struct CombineParams {
     SignBits sg;  // value signs
 };
 
-// CTAs of kCombineWarps warps; each (sequence, q-head) row takes W of them
-// (W = 8 for a few hundred splits at batch 1, fewer when there are few
-// splits, so small merges are not spread thin).  Lane holds dims 4 lane ..
-// 4 lane + 3.  Warp w of a row merges the splits w, w + W, ... in chunks of
-// 32: the chunk's (max, sum) pairs are read one per lane, the weights
-// 2^(m_s - m) computed one per lane and broadcast, and the chunk's output
-// rows read with independent loads, so many splits cost a handful of memory
-// round trips, not one per split.  The row's first warp then merges its
-// warps' results.
+// Each (sequence, q-head) row takes W warps (W = 16 or 32 for the hundred or
+// more splits of a small batch, fewer when there are few splits, so small
+// merges are not spread thin); a CTA holds max(8, W) warps.  Lane holds dims
+// 4 lane .. 4 lane + 3.  Warp w of a row merges the splits w, w + W, ...:
+// up to kFew of them with every load issued before any is used (one memory
+// round trip), more in chunks of 32 whose (max, sum) pairs are read one per
+// lane, the weights 2^(m_s - m) computed one per lane and broadcast, and the
+// chunk's output rows read with independent loads.  The row's first warp
+// then merges its warps' results.
 constexpr int kCombineWarps = 8;
+constexpr int kFew = 8;
+
+__host__ __device__ constexpr int combine_cta_warps(int W) { return W > kCombineWarps ? W : kCombineWarps; }
 
 template <int W>
-__global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const __grid_constant__ CombineParams p)
+__global__ void __launch_bounds__(combine_cta_warps(W) * 32) attn_combine_kernel(const __grid_constant__ CombineParams p)
 {
-    __shared__ float4 wo[W > 1 ? kCombineWarps : 1][32];
-    __shared__ float wm[kCombineWarps], wl[kCombineWarps];
+    constexpr int CW = combine_cta_warps(W);
+    __shared__ float4 wo[W > 1 ? CW : 1][32];
+    __shared__ float wm[CW], wl[CW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * (kCombineWarps / W) + warp / W, wid = warp % W, lead = warp - wid;
+    const int row = blockIdx.x * (CW / W) + warp / W, wid = warp % W, lead = warp - wid;
     const bool live = row < p.rows;
+    pdl_wait_primary();  // the split kernel's partials are complete and visible
     if (W == 1 && !live) return;  // no barrier below when W = 1
     const int b = row / p.QH, qh = row % p.QH;
     const int h = qh / p.G, hq = qh % p.G;
@@ -629,29 +635,49 @@ __global__ void __launch_bounds__(kCombineWarps * 32) attn_combine_kernel(const 
     const int64_t base = ((int64_t)b * p.H * p.NB + (int64_t)h * p.NB + hq / kG) * p.splits;
     // this warp's splits: wid + W i, i = 0 .. n_mine - 1
     const int n_mine = live && p.splits > wid ? (p.splits - wid + W - 1) / W : 0;
+    auto split_index = [&](int i) { return (base + wid + (int64_t)W * i) * kG + hh; };
     float mw = -INFINITY;
-    for (int i = lane; i < n_mine; i += 32) mw = fmaxf(mw, p.part_ml[2 * ((base + wid + (int64_t)W * i) * kG + hh)]);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-    const float muw = mw == -INFINITY ? 0.0f : mw;
     float4 xw = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float lw = 0.0f;
-    for (int i0 = 0; i0 < n_mine; i0 += 32) {
-        // lane j: weight and sum of split i0 + j
-        float wt = 0.0f;
-        if (i0 + lane < n_mine) {
-            const int64_t pi = (base + wid + (int64_t)W * (i0 + lane)) * kG + hh;
-            const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * pi);
-            wt = ex2(ml.x - muw);
-            lw += ml.y * wt;
-        }
-        const int cnt = n_mine - i0 < 32 ? n_mine - i0 : 32;
-#pragma unroll 8
-        for (int j = 0; j < cnt; ++j) {
+    if (n_mine <= kFew) {
+        float2 ml = make_float2(-INFINITY, 0.0f);
+        if (lane < n_mine) ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * split_index(lane));
+        float4 v[kFew];
+#pragma unroll
+        for (int j = 0; j < kFew; ++j)
+            v[j] = j < n_mine ? *reinterpret_cast<const float4 *>(p.part_o + split_index(j) * kD + 4 * lane)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        mw = ml.x;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+        const float muw = mw == -INFINITY ? 0.0f : mw;
+        const float wt = lane < n_mine ? ex2(ml.x - muw) : 0.0f;
+        if (lane < n_mine) lw = ml.y * wt;
+#pragma unroll
+        for (int j = 0; j < kFew; ++j) {
             const float w = __shfl_sync(0xffffffffu, wt, j);
-            const int64_t pi = (base + wid + (int64_t)W * (i0 + j)) * kG + hh;
-            const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pi * kD + 4 * lane);
-            xw.x += v.x * w; xw.y += v.y * w; xw.z += v.z * w; xw.w += v.w * w;
+            xw.x += v[j].x * w; xw.y += v[j].y * w; xw.z += v[j].z * w; xw.w += v[j].w * w;
+        }
+    } else {
+        for (int i = lane; i < n_mine; i += 32) mw = fmaxf(mw, p.part_ml[2 * split_index(i)]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+        const float muw = mw == -INFINITY ? 0.0f : mw;
+        for (int i0 = 0; i0 < n_mine; i0 += 32) {
+            // lane j: weight and sum of split i0 + j
+            float wt = 0.0f;
+            if (i0 + lane < n_mine) {
+                const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * split_index(i0 + lane));
+                wt = ex2(ml.x - muw);
+                lw += ml.y * wt;
+            }
+            const int cnt = n_mine - i0 < 32 ? n_mine - i0 : 32;
+#pragma unroll 8
+            for (int j = 0; j < cnt; ++j) {
+                const float w = __shfl_sync(0xffffffffu, wt, j);
+                const float4 v = *reinterpret_cast<const float4 *>(p.part_o + split_index(i0 + j) * kD + 4 * lane);
+                xw.x += v.x * w; xw.y += v.y * w; xw.z += v.z * w; xw.w += v.w * w;
+            }
         }
     }
 #pragma unroll
@@ -837,13 +863,13 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     cp.splits = plan.splits;
     cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
     cp.sg = c.signs;
-    if (plan.splits >= 64)
-        attn_combine_kernel<8><<<cp.rows, kCombineWarps * 32, 0, s>>>(cp);
-    else if (plan.splits >= 16)
-        attn_combine_kernel<2><<<(cp.rows + 3) / 4, kCombineWarps * 32, 0, s>>>(cp);
-    else
-        attn_combine_kernel<1><<<(cp.rows + 7) / 8, kCombineWarps * 32, 0, s>>>(cp);
-    return cudaGetLastError();
+    // the merge is a programmatic dependent of the split kernel: its CTAs take
+    // SMs as split CTAs retire and wait for the whole split grid before reading
+    const dim3 cb(kCombineWarps * 32);
+    if (plan.splits > 128) return launch_dependent(attn_combine_kernel<32>, dim3(cp.rows), dim3(32 * 32), 0, s, cp);
+    if (plan.splits >= 64) return launch_dependent(attn_combine_kernel<16>, dim3(cp.rows), dim3(16 * 32), 0, s, cp);
+    if (plan.splits >= 16) return launch_dependent(attn_combine_kernel<2>, dim3((cp.rows + 3) / 4), cb, 0, s, cp);
+    return launch_dependent(attn_combine_kernel<1>, dim3((cp.rows + 7) / 8), cb, 0, s, cp);
 }
 
 // Bytes of the split partials of a plan: (d output sums + max + sum) per

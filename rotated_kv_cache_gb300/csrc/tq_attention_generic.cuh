@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
 {
     using A = GGeo<D, NB>;
     constexpr int CB = A::CB;
+    pdl_allow_dependents();  // the merge launch waits for this grid's completion anyway
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment: swizzled key boxes start on a swizzle atom
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -744,6 +745,7 @@ __global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * (gCombineWarps / W) + warp / W, wid = warp % W, lead = warp - wid;
     const bool live = row < p.rows;
+    pdl_wait_primary();  // the partials' writer has completed and its writes are visible
     if (W == 1 && !live) return;  // no barrier below when W = 1
     const int per_seq = p.M * p.QH;
     const int b = row / per_seq, rem = row - b * per_seq, i = rem / p.QH, qh = rem - i * p.QH;
@@ -834,14 +836,15 @@ __global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const
 }
 
 // ---------------------------------------------------------------- host side
-// 4 warps per row from 8 splits up, else one warp per row (4 rows per CTA)
+// 4 warps per row from 8 splits up, else one warp per row (4 rows per CTA).
+// The merge is a programmatic dependent of the kernel that wrote the partials
+// (it waits for that grid before reading them).
 template <int D>
-void launch_generic_combine(const GenCombineParams &cp, cudaStream_t s)
+cudaError_t launch_generic_combine(const GenCombineParams &cp, cudaStream_t s)
 {
-    if (cp.splits >= 8)
-        attn_generic_combine<D, 4><<<cp.rows, gCombineWarps * 32, 0, s>>>(cp);
-    else
-        attn_generic_combine<D, 1><<<(cp.rows + gCombineWarps - 1) / gCombineWarps, gCombineWarps * 32, 0, s>>>(cp);
+    const dim3 cb(gCombineWarps * 32);
+    if (cp.splits >= 8) return launch_dependent(attn_generic_combine<D, 4>, dim3(cp.rows), cb, 0, s, cp);
+    return launch_dependent(attn_generic_combine<D, 1>, dim3((cp.rows + gCombineWarps - 1) / gCombineWarps), cb, 0, s, cp);
 }
 
 struct GenPlan {
@@ -1039,8 +1042,7 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     const int rows = c.B * (int)m * QH;
     GenCombineParams cp{p.part_o, p.part_ml, out, c.H, QH, G, (int)m, pl.hb, CB, pl.splits, rows,
                         inv_sqrt_head_dim(D), c.signs};
-    launch_generic_combine<D>(cp, s);
-    return cudaGetLastError();
+    return launch_generic_combine<D>(cp, s);
 }
 
 template <int D>
@@ -1049,8 +1051,7 @@ cudaError_t combine_parts(const float *part_o, const float *part_ml, float *out,
 {
     const int rows = B * m * QH;
     GenCombineParams cp{part_o, part_ml, out, H, QH, QH / H, m, hb, cb, splits, rows, inv_sqrt_head_dim(D), sg};
-    launch_generic_combine<D>(cp, s);
-    return cudaGetLastError();
+    return launch_generic_combine<D>(cp, s);
 }
 
 }  // namespace

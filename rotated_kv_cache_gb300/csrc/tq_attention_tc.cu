@@ -256,6 +256,7 @@ template <int D, int KB, int VB>
 __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p)
 {
     using A = TcGeo<D>;
+    pdl_allow_dependents();  // the merge launch waits for this grid's completion anyway
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem + A::OFF_RING;

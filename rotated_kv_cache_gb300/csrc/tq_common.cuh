@@ -1,5 +1,6 @@
 // tq_common.cuh -- device helpers shared by the codec kernels (sm_103a).
 #pragma once
+#include <utility>
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -142,6 +143,32 @@ __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_
 // Order generic-proxy shared-memory writes before later async-proxy reads.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch.  A kernel launched by launch_dependent may
+// start while the kernel before it on the stream is still running, once every
+// CTA of that kernel has run pdl_allow_dependents (or exited).  It must run
+// pdl_wait_primary before it touches memory the earlier kernel writes or
+// reads; that wait returns when the earlier grid has completed and its writes
+// are visible.  Without a programmatic dependency both do nothing.
+__device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kern` as a programmatic dependent of the previous kernel on `s`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args &&...args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t a)
 {
     uint4 v;
@@ -207,6 +234,14 @@ __device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, 
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4),
                  "r"(a5), "r"(a6), "r"(a7)
                  : "memory");
+}
+
+// 32 bytes from global memory (32-byte aligned) in one access.
+__device__ __forceinline__ void ld_global_v8(const void *p, uint32_t (&v)[8])
+{
+    asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "l"(p));
 }
 
 __host__ __device__ constexpr int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }

@@ -367,7 +367,7 @@ __device__ __forceinline__ void encode_key_lane(const EncodeParams &p, uint32_t 
         uint32_t out[BITS];
         key_codes_fast<BITS>(w[g], kp[g], out);
         if constexpr (BITS == 8) {
-            st_global_v8(p.codes + row * RB + part * LB, out[0], out[1], out[2], out[3], out[4], out[5], out[6], out[7]);
+            store_words<8, 16>(p.codes + row * RB + part * LB, out);  // the planes are 16-byte aligned
         } else {
             constexpr int A = align_of_bytes(RB) < align_of_bytes(LB) ? align_of_bytes(RB) : align_of_bytes(LB);
             store_words<BITS, A>(p.codes + row * RB + part * LB, out);
@@ -719,9 +719,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     encode_kernel(const __grid_constant__ EncodeParams p, const __grid_constant__ CUtensorMap map)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    if constexpr (KEY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if constexpr (KEY) pdl_allow_dependents();
     encode_body<D, BITS, KEY>(p, map, smem_raw, blockIdx.x, gridDim.x);
-    if constexpr (!KEY) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (!KEY) pdl_wait_primary();
 }
 
 // Keys and values of a small append in one launch (the two encodes of a
@@ -766,19 +766,7 @@ cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s, b
     }
     const int64_t want = ((int64_t)p.items + kWarps - 1) / kWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
-    if (!KEY && after_keys) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(kWarps * 32);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, p, map);
-    }
+    if (!KEY && after_keys) return launch_dependent(kern, dim3((unsigned)grid), dim3(kWarps * 32), smem, s, p, map);
     kern<<<grid, kWarps * 32, smem, s>>>(p, map);
     return cudaGetLastError();
 }

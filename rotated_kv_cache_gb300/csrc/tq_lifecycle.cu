@@ -133,26 +133,28 @@ __global__ void __launch_bounds__(kUWarps * 32) unrotate_kernel(const __grid_con
         const int64_t e0 = row * D + 64 * part;  // first element of this lane
         float2 P[32];
         if (valid) {
+            // 32-byte loads (x is 32-byte aligned and rows are whole multiples of 32 bytes)
             if constexpr (IN_F32) {
-                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.x) + e0);
+                const float *src = static_cast<const float *>(p.x) + e0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 a = src[i], b = src[8 + i];
-                    P[4 * i] = make_float2(a.x, b.x);
-                    P[4 * i + 1] = make_float2(a.y, b.y);
-                    P[4 * i + 2] = make_float2(a.z, b.z);
-                    P[4 * i + 3] = make_float2(a.w, b.w);
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t a[8], b[8];
+                    ld_global_v8(src + 8 * k, a);
+                    ld_global_v8(src + 32 + 8 * k, b);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) P[8 * k + q] = make_float2(__uint_as_float(a[q]), __uint_as_float(b[q]));
                 }
             } else {
-                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.x) + e0);
+                const uint16_t *src = static_cast<const uint16_t *>(p.x) + e0;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 a = src[i], b = src[4 + i];
-                    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+                for (int k = 0; k < 2; ++k) {
+                    uint32_t a[8], b[8];
+                    ld_global_v8(src + 16 * k, a);
+                    ld_global_v8(src + 32 + 16 * k, b);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        P[8 * i + 2 * q] = make_float2(bf16_lo(aw[q]), bf16_lo(bw[q]));
-                        P[8 * i + 2 * q + 1] = make_float2(bf16_hi(aw[q]), bf16_hi(bw[q]));
+                    for (int q = 0; q < 8; ++q) {
+                        P[16 * k + 2 * q] = make_float2(bf16_lo(a[q]), bf16_lo(b[q]));
+                        P[16 * k + 2 * q + 1] = make_float2(bf16_hi(a[q]), bf16_hi(b[q]));
                     }
                 }
             }

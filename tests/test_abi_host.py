@@ -101,6 +101,9 @@ def test_refusals_before_launch(tqlib):
     assert L.tq_decode(ctypes.byref(s), 0, 40, 0, 0x10000, None, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_decode(ctypes.byref(s), 0, 4, 7, 0x10000, None, None) == S["TQ_ERR_SHAPE"]
     assert L.tq_decode(ctypes.byref(s), 0, 4, 0, 0x10004, None, None) == S["TQ_ERR_ALIGN"]
+    # the fetch moves 32-byte words: 16-byte alignment is not enough for its outputs
+    assert L.tq_decode(ctypes.byref(s), 0, 4, 0, 0x10010, None, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_decode(ctypes.byref(s), 0, 4, 0, None, 0x10010, None) == S["TQ_ERR_ALIGN"]
     assert L.tq_decode(ctypes.byref(s), 0, 0, 0, 0x10000, None, None) == S["TQ_OK"]
     assert L.tq_decode_attention(ctypes.byref(s), 0x10000, 3, 8, 1.0, 0x20000, None, 0, None) == S["TQ_ERR_SHAPE"]
     assert L.tq_decode_attention(ctypes.byref(s), 0x10000, 4, 33, 1.0, 0x20000, None, 0, None) == S["TQ_ERR_CAPACITY"]
@@ -123,12 +126,15 @@ def test_lifecycle_and_deferred_refusals(tqlib):
     assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 5, 0x10000, None) == S["TQ_ERR_SHAPE"]
     assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 1, None, None) == S["TQ_ERR_NULL"]
     assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 1, 0x10008, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 4, 1, 0x10010, None) == S["TQ_ERR_ALIGN"]
     assert L.tq_decode_values_rotated(ctypes.byref(a), 0, 0, 1, None, None) == S["TQ_OK"]
     assert L.tq_unrotate(96, 42, 1, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_HEAD_DIM"]
     assert L.tq_unrotate(128, 42, 2, 0x10000, 4, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
     assert L.tq_unrotate(128, 42, 1, 0x10000, -1, 1, 0x20000, None) == S["TQ_ERR_SHAPE"]
     assert L.tq_unrotate(128, 42, 1, 0x10000, 4, 0, 0x10000, None) == S["TQ_ERR_SHAPE"]  # in place, different sizes
     assert L.tq_unrotate(128, 42, 1, 0x10004, 4, 1, 0x20000, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_unrotate(128, 42, 1, 0x10010, 4, 1, 0x20000, None) == S["TQ_ERR_ALIGN"]
+    assert L.tq_unrotate(128, 42, 1, 0x10000, 4, 1, 0x20010, None) == S["TQ_ERR_ALIGN"]
     assert L.tq_unrotate(128, 42, 1, None, 4, 1, 0x20000, None) == S["TQ_ERR_NULL"]
     assert L.tq_unrotate(128, 42, 1, None, 0, 1, None, None) == S["TQ_OK"]
     big = _struct(tqlib, capacity=64)
