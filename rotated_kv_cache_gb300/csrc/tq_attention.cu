@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
     uint32_t *done = reinterpret_cast<uint32_t *>(smem + A::RING + kStages * 8);
     const uint32_t full0 = smem_addr(bars);
 
-    pdl_allow_dependents();  // the merge launch waits for this grid's completion anyway
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // blockIdx.y = (kv-head, block of kG q-heads); the blocks of one kv-head are
     // neighbours in the grid, so their reads of the same rows meet in L2
@@ -628,6 +629,7 @@ __global__ void __launch_bounds__(combine_cta_warps(W) * 32) attn_combine_kernel
     const int row = blockIdx.x * (CW / W) + warp / W, wid = warp % W, lead = warp - wid;
     const bool live = row < p.rows;
     pdl_wait_primary();  // the split kernel's partials are complete and visible
+    pdl_allow_dependents();
     if (W == 1 && !live) return;  // no barrier below when W = 1
     const int b = row / p.QH, qh = row % p.QH;
     const int h = qh / p.G, hq = qh % p.G;
@@ -847,8 +849,7 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
 
     dim3 grid(plan.splits, c.H * p.NB, c.B);
-    attn_split_kernel<KB><<<grid, kThreads, A::SMEM, s>>>(map, p);
-    e = cudaGetLastError();
+    e = launch_dependent(attn_split_kernel<KB>, grid, dim3(kThreads), A::SMEM, s, map, p);
     if (e != cudaSuccess) return e;
 
     CombineParams cp{};

@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
 {
     using A = GGeo<D, NB>;
     constexpr int CB = A::CB;
-    pdl_allow_dependents();  // the merge launch waits for this grid's completion anyway
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment: swizzled key boxes start on a swizzle atom
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -746,6 +747,7 @@ __global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const
     const int row = blockIdx.x * (gCombineWarps / W) + warp / W, wid = warp % W, lead = warp - wid;
     const bool live = row < p.rows;
     pdl_wait_primary();  // the partials' writer has completed and its writes are visible
+    pdl_allow_dependents();
     if (W == 1 && !live) return;  // no barrier below when W = 1
     const int per_seq = p.M * p.QH;
     const int b = row / per_seq, rem = row - b * per_seq, i = rem / p.QH, qh = rem - i * p.QH;
@@ -946,12 +948,10 @@ bool gen_plan(const CacheView &c, int q_heads, int64_t m, int64_t seq_len, GenPl
 }
 
 template <int D, int NB>
-void gen_launch(const GenPlan &pl, dim3 grid, const CUtensorMap &kmap, const GenParams &p, cudaStream_t s)
+cudaError_t gen_launch(const GenPlan &pl, dim3 grid, const CUtensorMap &kmap, const GenParams &p, cudaStream_t s)
 {
-    gen_dispatch<D, NB>(pl, [&](auto kern) {
-        kern<<<grid, GGeo<D, NB>::THREADS, pl.smem, s>>>(kmap, p);
-        return 0;
-    });
+    return gen_dispatch<D, NB>(
+        pl, [&](auto kern) { return launch_dependent(kern, grid, dim3(GGeo<D, NB>::THREADS), (size_t)pl.smem, s, kmap, p); });
 }
 
 // Tensor map over the key plane for the swizzled key tiles of 8- and 4-bit
@@ -1032,12 +1032,12 @@ cudaError_t gen_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, in
     CUtensorMap kmap{};
     if (pl.key != 0 && !gen_key_map<D>(c, &kmap)) return cudaErrorInvalidValue;
     const dim3 grid(pl.splits, c.H * pl.hb, c.B);
+    cudaError_t e = cudaErrorInvalidValue;
     switch (pl.nb) {
-    case 1: gen_launch<D, 1>(pl, grid, kmap, p, s); break;
-    case 2: if constexpr (D <= 256) gen_launch<D, 2>(pl, grid, kmap, p, s); break;
-    case 4: if constexpr (D <= 128) gen_launch<D, 4>(pl, grid, kmap, p, s); break;
+    case 1: e = gen_launch<D, 1>(pl, grid, kmap, p, s); break;
+    case 2: if constexpr (D <= 256) e = gen_launch<D, 2>(pl, grid, kmap, p, s); break;
+    case 4: if constexpr (D <= 128) e = gen_launch<D, 4>(pl, grid, kmap, p, s); break;
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int rows = c.B * (int)m * QH;
     GenCombineParams cp{p.part_o, p.part_ml, out, c.H, QH, G, (int)m, pl.hb, CB, pl.splits, rows,

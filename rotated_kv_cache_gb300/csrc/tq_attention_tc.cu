@@ -256,7 +256,8 @@ template <int D, int KB, int VB>
 __global__ void __launch_bounds__(tcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p)
 {
     using A = TcGeo<D>;
-    pdl_allow_dependents();  // the merge launch waits for this grid's completion anyway
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem + A::OFF_RING;
@@ -667,9 +668,8 @@ cudaError_t tc_run(const CacheView &c, const uint16_t *q, int QH, int64_t m, int
     // times the largest centroid lands in [2^13, 2^14), so f16 always holds them
     p.vscale = ldexpf(1.0f, tile_exponent_host(65504.0f * cm));
     if ((int64_t)c.H * pl.hb > 65535 || c.B > 65535) return cudaErrorInvalidValue;
-    attn_tc_kernel<D, KB, VB><<<dim3(pl.splits, c.H * pl.hb, c.B), tcThreads, pl.smem, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const cudaError_t le = launch_dependent(attn_tc_kernel<D, KB, VB>, dim3(pl.splits, c.H * pl.hb, c.B), dim3(tcThreads), pl.smem, s, p);
+    if (le != cudaSuccess) return le;
     return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, (int)m, pl.hb, tcCB, pl.splits,
                                           c.signs, s);
 }

@@ -90,6 +90,8 @@ __device__ __forceinline__ void key_group_out(const uint32_t (&w)[KB], float s, 
 template <int KB, bool F32>
 __global__ void __launch_bounds__(256) decode_key_kernel(const __grid_constant__ KeyDecodeParams p)
 {
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     const int64_t gi = (int64_t)blockIdx.x * 256 + threadIdx.x;  // group within the (sequence, kv-head)'s n rows
     if (gi >= p.groups_per_bh) return;
     constexpr int A = align_of_bytes(4 * KB);
@@ -238,6 +240,8 @@ __global__ void __launch_bounds__(kVWarps * 32, 4) decode_value_kernel(const __g
     using G = VGeo<D>;
     __shared__ __align__(16) float scen[1 << VB];
     __shared__ __align__(16) float2 smul[G::LPR][34];  // (+-1/sqrt d) of elements (j, j+32) of each part, padded
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     for (int i = threadIdx.x; i < (1 << VB); i += blockDim.x) scen[i] = p.cen[i];
     for (int i = threadIdx.x; i < G::LPR * 32; i += blockDim.x) {
         const int part = i >> 5, j = i & 31;
@@ -370,8 +374,7 @@ cudaError_t run_key(const CacheView &c, int64_t t0, int64_t n, void *out, cudaSt
     const int64_t bx = (p.groups_per_bh + 255) / 256;
     if (bx >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)bx, (unsigned)imin64(p.BH, 65535));
-    decode_key_kernel<KB, F32><<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(decode_key_kernel<KB, F32>, grid, dim3(256), 0, s, p);
 }
 
 template <int D, int VB, bool F32>
@@ -410,8 +413,7 @@ cudaError_t run_value(const CacheView &c, int64_t t0, int64_t n, void *out, void
     }
     const int64_t want = (items + kVWarps - 1) / kVWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
-    kern<<<grid, kVWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3((unsigned)grid), dim3(kVWarps * 32), 0, s, p);
 }
 
 template <bool F32>

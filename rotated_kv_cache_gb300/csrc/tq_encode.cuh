@@ -707,32 +707,34 @@ __device__ __forceinline__ void encode_body(const EncodeParams &p, const CUtenso
     if (!KEY && lane == 0) bulk_wait0();
 }
 
-// An append is two launches, keys then values, on one stream.  The value
-// launch is a programmatic dependent of the key launch: the key kernel allows
-// it to start at once, so value CTAs take the SMs that key CTAs leave in the
-// key kernel's last round, and the value kernel waits for the key grid only
-// before it ends (it touches none of the key planes; the wait keeps stream
-// order for whatever is queued after the append).  Without a programmatic
-// dependency both instructions do nothing.
+// Every launch of this library is a programmatic dependent of the kernel
+// before it on the stream and waits for that kernel before touching memory.
+// The exception is the value launch of an append made of two launches (keys,
+// then values): it touches none of the key planes, so it starts as soon as
+// the key kernel has started and takes the SMs that key CTAs leave in their
+// last round; it waits for the key grid only before it ends, which keeps
+// stream order for whatever is queued after the append.
 template <int D, int BITS, bool KEY>
 __global__ void __launch_bounds__(kWarps * 32)
     encode_kernel(const __grid_constant__ EncodeParams p, const __grid_constant__ CUtensorMap map)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    if constexpr (KEY) pdl_allow_dependents();
+    if constexpr (KEY) pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     encode_body<D, BITS, KEY>(p, map, smem_raw, blockIdx.x, gridDim.x);
     if constexpr (!KEY) pdl_wait_primary();
 }
 
-// Keys and values of a small append in one launch (the two encodes of a
-// one-token step are latency, not bandwidth): CTAs [0, key_ctas) encode the
-// keys, the others the values.
+// Keys and values in one launch: CTAs [0, key_ctas) encode the keys, the
+// others the values (see run_kv for how the CTAs are shared out).
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(kWarps * 32)
     encode_kv_kernel(const __grid_constant__ EncodeParams pk, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ EncodeParams pv, const __grid_constant__ CUtensorMap mv, uint32_t key_ctas)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     if (blockIdx.x < key_ctas)
         encode_body<D, KB, true>(pk, mk, smem_raw, blockIdx.x, key_ctas);
     else
@@ -748,10 +750,9 @@ constexpr size_t encode_smem()
            G::MTAB + (size_t)kWarps * (KEY ? 0 : VStage<D, BITS>::BYTES);
 }
 
-// after_keys: the launch follows this append's key launch on the same stream
-// and becomes its programmatic dependent (values only)
+// A value launch must directly follow the key launch of the same append.
 template <int D, int BITS, bool KEY>
-cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s, bool after_keys = false)
+cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
 {
     const size_t smem = encode_smem<D, BITS, KEY>();
     auto kern = encode_kernel<D, BITS, KEY>;
@@ -766,12 +767,11 @@ cudaError_t run(const EncodeParams &p, const CUtensorMap &map, cudaStream_t s, b
     }
     const int64_t want = ((int64_t)p.items + kWarps - 1) / kWarps;
     const int grid = (int)imin64(want, (int64_t)num_sms() * per_sm);
-    if (!KEY && after_keys) return launch_dependent(kern, dim3((unsigned)grid), dim3(kWarps * 32), smem, s, p, map);
-    kern<<<grid, kWarps * 32, smem, s>>>(p, map);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3((unsigned)grid), dim3(kWarps * 32), smem, s, p, map);
 }
 
-// keys and values in one launch (encode_kv_kernel); every CTA is resident at once
+// Keys and values of a small append in one launch (encode_kv_kernel), every
+// CTA resident at once.
 template <int D, int KB, int VB>
 cudaError_t run_kv(const EncodeParams &pk, const CUtensorMap &mk, const EncodeParams &pv, const CUtensorMap &mv,
                    uint32_t key_ctas, uint32_t value_ctas, cudaStream_t s)
@@ -785,8 +785,7 @@ cudaError_t run_kv(const EncodeParams &pk, const CUtensorMap &mk, const EncodePa
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    kern<<<key_ctas + value_ctas, kWarps * 32, smem, s>>>(pk, mk, pv, mv, key_ctas);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(key_ctas + value_ctas), dim3(kWarps * 32), smem, s, pk, mk, pv, mv, key_ctas);
 }
 
 template <int D>
@@ -802,14 +801,14 @@ cudaError_t dispatch_key(int kb, const EncodeParams &p, const CUtensorMap &map, 
 }
 
 template <int D>
-cudaError_t dispatch_value(int vb, const EncodeParams &p, const CUtensorMap &map, cudaStream_t s, bool after_keys)
+cudaError_t dispatch_value(int vb, const EncodeParams &p, const CUtensorMap &map, cudaStream_t s)
 {
     switch (vb) {
-    case 2: return run<D, 2, false>(p, map, s, after_keys);
-    case 3: return run<D, 3, false>(p, map, s, after_keys);
-    case 4: return run<D, 4, false>(p, map, s, after_keys);
-    case 5: return run<D, 5, false>(p, map, s, after_keys);
-    case 8: return run<D, 8, false>(p, map, s, after_keys);
+    case 2: return run<D, 2, false>(p, map, s);
+    case 3: return run<D, 3, false>(p, map, s);
+    case 4: return run<D, 4, false>(p, map, s);
+    case 5: return run<D, 5, false>(p, map, s);
+    case 8: return run<D, 8, false>(p, map, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -880,7 +879,8 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     pv.use_tma = input_map(&mv, v, D, n, c.H, c.B, vs, EGeo<D, false>::TROWS) ? 1 : 0;
 
     // a small append (a few rows per sequence-head, as in a decode step) runs
-    // keys and values in one launch when both grids fit one CTA per SM
+    // keys and values in one launch when both grids fit one CTA per SM; a
+    // larger one as two launches (keys, then values)
     const uint32_t gk = (pk.items + kWarps - 1) / kWarps, gv = (pv.items + kWarps - 1) / kWarps;
     if ((int64_t)gk + gv <= num_sms() && c.vb == 3 && (c.kb == 8 || c.kb == 4)) {
         if (c.kb == 8) return run_kv<D, 8, 3>(pk, mk, pv, mv, gk, gv, s);
@@ -888,7 +888,7 @@ cudaError_t encode_d(const CacheView &c, const uint16_t *k, const int64_t ks[3],
     }
     cudaError_t e = dispatch_key<D>(c.kb, pk, mk, s);
     if (e != cudaSuccess) return e;
-    return dispatch_value<D>(c.vb, pv, mv, s, true);
+    return dispatch_value<D>(c.vb, pv, mv, s);
 }
 
 }  // namespace

@@ -34,6 +34,8 @@ template <int VB, bool F32>
 __global__ void __launch_bounds__(256) rotated_kernel(const __grid_constant__ RotParams p)
 {
     __shared__ float scen[1 << VB];
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     for (int i = threadIdx.x; i < (1 << VB); i += blockDim.x) scen[i] = p.cen[i];
     __syncthreads();
     const int64_t gi = (int64_t)blockIdx.x * 256 + threadIdx.x;
@@ -85,8 +87,7 @@ cudaError_t run_rotated(const CacheView &c, int64_t t0, int64_t n, void *out, cu
     for (int i = 0; i < (1 << VB); ++i) p.cen[i] = tab.centroids[i];
     const int64_t bx = (p.groups_per_bh + 255) / 256;
     if (bx >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
-    rotated_kernel<VB, F32><<<dim3((unsigned)bx, (unsigned)imin64(p.BH, 65535)), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(rotated_kernel<VB, F32>, dim3((unsigned)bx, (unsigned)imin64(p.BH, 65535)), dim3(256), 0, s, p);
 }
 
 template <bool F32>
@@ -119,6 +120,8 @@ __global__ void __launch_bounds__(kUWarps * 32) unrotate_kernel(const __grid_con
 {
     constexpr int LPR = D / 64, ROWS = 32 / LPR;
     __shared__ __align__(16) float2 smul[LPR][34];  // (+-1/sqrt d) of elements (j, j+32) of each part, padded
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     for (int i = threadIdx.x; i < LPR * 32; i += blockDim.x) {
         const int part = i >> 5, j = i & 31, e = 64 * part + j;
         smul[part][j] = make_float2(sign_negative(p.sg, e) ? -p.inv_sqrt_d : p.inv_sqrt_d,
@@ -214,8 +217,7 @@ cudaError_t run_unrotate(const SignBits &sg, const void *x, int64_t rows, void *
         per_sm = k > 0 ? k : 1;
     }
     const int grid = (int)imin64((items + kUWarps - 1) / kUWarps, (int64_t)num_sms() * per_sm);
-    kern<<<grid, kUWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3((unsigned)grid), dim3(kUWarps * 32), 0, s, p);
 }
 
 template <int D>
@@ -243,6 +245,8 @@ struct CopyParams {
 // blockIdx.y = plane; the plane's (segment, word) space is walked grid-stride
 __global__ void __launch_bounds__(256) copy_rows_kernel(const __grid_constant__ CopyParams p)
 {
+    pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
+    pdl_allow_dependents();
     const int plane = blockIdx.y;
     const int64_t rb = p.row_bytes[plane];
     const uint8_t *src_plane = p.src[plane];
@@ -319,8 +323,7 @@ cudaError_t launch_copy_rows(const CacheView &dst, int64_t dst_t0, const CacheVi
         most = most > total ? most : total;
     }
     const int64_t blocks = imin64((most + 255) / 256, (int64_t)num_sms() * 8);
-    copy_rows_kernel<<<dim3((unsigned)(blocks > 0 ? blocks : 1), 5), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(copy_rows_kernel, dim3((unsigned)(blocks > 0 ? blocks : 1), 5), dim3(256), 0, s, p);
 }
 
 }  // namespace tq
