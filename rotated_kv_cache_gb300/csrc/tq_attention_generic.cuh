@@ -731,20 +731,26 @@ struct GenCombineParams {
     SignBits sg;  // value signs
 };
 
-// CTAs of gCombineWarps warps; each (sequence, query row, q-head) takes W of
-// them: W = 4 when there are many splits (the warps merge interleaved subsets,
-// then the first merges their results), else W = 1 and one warp walks them.
-// Lane holds dims PER*lane .. +PER-1.
+// Each (sequence, query row, q-head) row takes W warps (1, 4, 16 or 32 as the
+// splits grow); a CTA holds max(4, W) warps.  Lane holds dims PER*lane ..
+// +PER-1.  Warp w of a row merges the splits w, w + W, ...: up to gFew<D>()
+// of them with every load issued before any is used (one memory round trip),
+// more in chunks of 32 whose (max, sum) pairs are read one per lane, the
+// weights broadcast and the chunk's output rows read with independent loads.
+// The row's first warp then merges its warps' results.
 constexpr int gCombineWarps = 4;
+template <int D>
+__host__ __device__ constexpr int gFew() { return 32 / (D / 32) > 2 ? 32 / (D / 32) : 2; }
+__host__ __device__ constexpr int g_combine_cta_warps(int W) { return W > gCombineWarps ? W : gCombineWarps; }
 
 template <int D, int W>
-__global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const __grid_constant__ GenCombineParams p)
+__global__ void __launch_bounds__(g_combine_cta_warps(W) * 32) attn_generic_combine(const __grid_constant__ GenCombineParams p)
 {
-    constexpr int PER = D / 32;
-    __shared__ float wo[W > 1 ? gCombineWarps : 1][PER][32];  // [warp][k][lane]: conflict-free
-    __shared__ float wm[gCombineWarps], wl[gCombineWarps];
+    constexpr int PER = D / 32, CW = g_combine_cta_warps(W), KF = gFew<D>();
+    __shared__ float wo[W > 1 ? CW : 1][PER][32];  // [warp][k][lane]: conflict-free
+    __shared__ float wm[CW], wl[CW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * (gCombineWarps / W) + warp / W, wid = warp % W, lead = warp - wid;
+    const int row = blockIdx.x * (CW / W) + warp / W, wid = warp % W, lead = warp - wid;
     const bool live = row < p.rows;
     pdl_wait_primary();  // the partials' writer has completed and its writes are visible
     pdl_allow_dependents();
@@ -753,33 +759,54 @@ __global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const
     const int b = row / per_seq, rem = row - b * per_seq, i = rem / p.QH, qh = rem - i * p.QH;
     const int h = qh / p.G, col = i * p.G + (qh - h * p.G), hb = col / p.CB, n = col - hb * p.CB;
     const int64_t base = (((int64_t)b * p.H + h) * p.HB + hb) * p.splits;
-    // this warp's splits wid + W i, i < n_mine, in chunks of 32: (max, sum) one
-    // per lane, weights broadcast, the chunk's output rows read with
-    // independent loads
     const int n_mine = live && p.splits > wid ? (p.splits - wid + W - 1) / W : 0;
+    auto split_index = [&](int j) { return (base + wid + (int64_t)W * j) * p.CB + n; };
     float mw = -INFINITY;
-    for (int i = lane; i < n_mine; i += 32) mw = fmaxf(mw, p.part_ml[2 * ((base + wid + (int64_t)W * i) * p.CB + n)]);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-    const float muw = mw == -INFINITY ? 0.0f : mw;
     float x[PER], l = 0.0f;
 #pragma unroll
     for (int k = 0; k < PER; ++k) x[k] = 0.0f;
-    for (int i0 = 0; i0 < n_mine; i0 += 32) {
-        float wt = 0.0f;
-        if (i0 + lane < n_mine) {
-            const int64_t pi = (base + wid + (int64_t)W * (i0 + lane)) * p.CB + n;
-            const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * pi);
-            wt = g_ex2(ml.x - muw);
-            l += ml.y * wt;
-        }
-        const int cnt = n_mine - i0 < 32 ? n_mine - i0 : 32;
-#pragma unroll 4
-        for (int j = 0; j < cnt; ++j) {
-            const float w = __shfl_sync(0xffffffffu, wt, j);
-            const float *src = p.part_o + ((base + wid + (int64_t)W * (i0 + j)) * p.CB + n) * D + PER * lane;
+    if (n_mine <= KF) {
+        float2 ml = make_float2(-INFINITY, 0.0f);
+        if (lane < n_mine) ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * split_index(lane));
+        float v[KF][PER];
 #pragma unroll
-            for (int k = 0; k < PER; ++k) x[k] += src[k] * w;
+        for (int j = 0; j < KF; ++j) {
+            const float *src = p.part_o + split_index(j) * D + PER * lane;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) v[j][k] = j < n_mine ? src[k] : 0.0f;
+        }
+        mw = ml.x;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+        const float muw = mw == -INFINITY ? 0.0f : mw;
+        const float wt = lane < n_mine ? g_ex2(ml.x - muw) : 0.0f;
+        if (lane < n_mine) l = ml.y * wt;
+#pragma unroll
+        for (int j = 0; j < KF; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wt, j);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) x[k] += v[j][k] * w;
+        }
+    } else {
+        for (int j = lane; j < n_mine; j += 32) mw = fmaxf(mw, p.part_ml[2 * split_index(j)]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+        const float muw = mw == -INFINITY ? 0.0f : mw;
+        for (int i0 = 0; i0 < n_mine; i0 += 32) {
+            float wt = 0.0f;
+            if (i0 + lane < n_mine) {
+                const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * split_index(i0 + lane));
+                wt = g_ex2(ml.x - muw);
+                l += ml.y * wt;
+            }
+            const int cnt = n_mine - i0 < 32 ? n_mine - i0 : 32;
+#pragma unroll 4
+            for (int j = 0; j < cnt; ++j) {
+                const float w = __shfl_sync(0xffffffffu, wt, j);
+                const float *src = p.part_o + split_index(i0 + j) * D + PER * lane;
+#pragma unroll
+                for (int k = 0; k < PER; ++k) x[k] += src[k] * w;
+            }
         }
     }
 #pragma unroll
@@ -838,15 +865,23 @@ __global__ void __launch_bounds__(gCombineWarps * 32) attn_generic_combine(const
 }
 
 // ---------------------------------------------------------------- host side
-// 4 warps per row from 8 splits up, else one warp per row (4 rows per CTA).
-// The merge is a programmatic dependent of the kernel that wrote the partials
-// (it waits for that grid before reading them).
+// The fewest warps per row (1, 4, 16, 32; 16 at most at head_dim 512, whose
+// partials of 32 warps would not fit static shared memory) that give each
+// warp at most gFew<D>() splits; one warp per row packs 4 rows per CTA.  The
+// merge is a programmatic dependent of the kernel that wrote the partials (it
+// waits for that grid before reading them).
 template <int D>
 cudaError_t launch_generic_combine(const GenCombineParams &cp, cudaStream_t s)
 {
-    const dim3 cb(gCombineWarps * 32);
-    if (cp.splits >= 8) return launch_dependent(attn_generic_combine<D, 4>, dim3(cp.rows), cb, 0, s, cp);
-    return launch_dependent(attn_generic_combine<D, 1>, dim3((cp.rows + gCombineWarps - 1) / gCombineWarps), cb, 0, s, cp);
+    constexpr int KF = gFew<D>();
+    if (cp.splits <= KF)
+        return launch_dependent(attn_generic_combine<D, 1>, dim3((cp.rows + gCombineWarps - 1) / gCombineWarps),
+                                dim3(gCombineWarps * 32), 0, s, cp);
+    if (cp.splits <= 4 * KF) return launch_dependent(attn_generic_combine<D, 4>, dim3(cp.rows), dim3(4 * 32), 0, s, cp);
+    if (D == 512 || cp.splits <= 16 * KF)
+        return launch_dependent(attn_generic_combine<D, 16>, dim3(cp.rows), dim3(16 * 32), 0, s, cp);
+    if constexpr (D < 512) return launch_dependent(attn_generic_combine<D, 32>, dim3(cp.rows), dim3(32 * 32), 0, s, cp);
+    return cudaErrorInvalidValue;
 }
 
 struct GenPlan {
