@@ -435,46 +435,61 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
         for (int t2 = 0; t2 < A::TILES; ++t2)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) S[t2][nb][0][0] = S[t2][nb][0][1] = S[t2][nb][1][0] = S[t2][nb][1][1] = 0.0f;
+        // groups two at a time: a row's fp16 scales (zeros) of groups G0, G0 + 1 are
+        // one 32-bit word (NG is even, rows are NG * 2 bytes apart)
 #pragma unroll 1
-        for (int G = 0; G < A::NG; ++G) {
-            uint2 bq[NB][2];
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) bq[nb][jj] = g_lds64(qf_lane + nb * QF_NB + (2 * G + jj) * 32);
+        for (int G0 = 0; G0 < A::NG; G0 += 2) {
+            uint32_t scp[A::TILES][2], zcp[A::TILES][2];  // [tile][row g, row g + 8]
 #pragma unroll
             for (int t2 = 0; t2 < A::TILES; ++t2) {
                 const int ra = r0 + TR * t2, rb = r1 + TR * t2;
-                uint32_t k0[4], k1[4];
-                if constexpr (KEY != 0) {
-                    key_pairs_sw<D, KEY>(kst, ra, G, c, k0);
-                    key_pairs_sw<D, KEY>(kst, rb, G, c, k1);
-                } else {
-                    key_pairs<KEY>(kst + ra * p.rbk, G, c, p.kb, k0);
-                    key_pairs<KEY>(kst + rb * p.rbk, G, c, p.kb, k1);
-                }
-                const float sc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (ra * NG + G) * 2));
-                const float sc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_ks + (rb * NG + G) * 2));
-                const float zc0 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (ra * NG + G) * 2)) - p.koff;
-                const float zc1 = f16_bits_to_f32((uint16_t)g_lds16(st + p.off_kz + (rb * NG + G) * 2)) - p.koff;
+                scp[t2][0] = g_lds32(st + p.off_ks + (ra * NG + G0) * 2);
+                scp[t2][1] = g_lds32(st + p.off_ks + (rb * NG + G0) * 2);
+                zcp[t2][0] = g_lds32(st + p.off_kz + (ra * NG + G0) * 2);
+                zcp[t2][1] = g_lds32(st + p.off_kz + (rb * NG + G0) * 2);
+            }
 #pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int gg = 0; gg < 2; ++gg) {
+                const int G = G0 + gg;
+                uint2 bq[NB][2];
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj)
-                        g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq[nb][jj].x, bq[nb][jj].y);
-                    // both columns of the lane at once on packed fp32 pairs
-                    const float2 qs = make_float2(qsum[G * CB + nb * gN + 2 * c], qsum[G * CB + nb * gN + 2 * c + 1]);
-                    const float2 s0 = __ffma2_rn(make_float2(sc0, sc0),
-                                                 __ffma2_rn(make_float2(zc0, zc0), qs, make_float2(acc[0], acc[1])),
-                                                 make_float2(S[t2][nb][0][0], S[t2][nb][0][1]));
-                    const float2 s1 = __ffma2_rn(make_float2(sc1, sc1),
-                                                 __ffma2_rn(make_float2(zc1, zc1), qs, make_float2(acc[2], acc[3])),
-                                                 make_float2(S[t2][nb][1][0], S[t2][nb][1][1]));
-                    S[t2][nb][0][0] = s0.x;
-                    S[t2][nb][0][1] = s0.y;
-                    S[t2][nb][1][0] = s1.x;
-                    S[t2][nb][1][1] = s1.y;
+                for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) bq[nb][jj] = g_lds64(qf_lane + nb * QF_NB + (2 * G + jj) * 32);
+#pragma unroll
+                for (int t2 = 0; t2 < A::TILES; ++t2) {
+                    const int ra = r0 + TR * t2, rb = r1 + TR * t2;
+                    uint32_t k0[4], k1[4];
+                    if constexpr (KEY != 0) {
+                        key_pairs_sw<D, KEY>(kst, ra, G, c, k0);
+                        key_pairs_sw<D, KEY>(kst, rb, G, c, k1);
+                    } else {
+                        key_pairs<KEY>(kst + ra * p.rbk, G, c, p.kb, k0);
+                        key_pairs<KEY>(kst + rb * p.rbk, G, c, p.kb, k1);
+                    }
+                    const float sc0 = f16_bits_to_f32((uint16_t)(scp[t2][0] >> (16 * gg)));
+                    const float sc1 = f16_bits_to_f32((uint16_t)(scp[t2][1] >> (16 * gg)));
+                    const float zc0 = f16_bits_to_f32((uint16_t)(zcp[t2][0] >> (16 * gg))) - p.koff;
+                    const float zc1 = f16_bits_to_f32((uint16_t)(zcp[t2][1] >> (16 * gg))) - p.koff;
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) {
+                        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj)
+                            g_mma(acc, k0[2 * jj], k1[2 * jj], k0[2 * jj + 1], k1[2 * jj + 1], bq[nb][jj].x, bq[nb][jj].y);
+                        // both columns of the lane at once on packed fp32 pairs
+                        const float2 qs = *reinterpret_cast<const float2 *>(&qsum[G * CB + nb * gN + 2 * c]);
+                        const float2 s0 = __ffma2_rn(make_float2(sc0, sc0),
+                                                     __ffma2_rn(make_float2(zc0, zc0), qs, make_float2(acc[0], acc[1])),
+                                                     make_float2(S[t2][nb][0][0], S[t2][nb][0][1]));
+                        const float2 s1 = __ffma2_rn(make_float2(sc1, sc1),
+                                                     __ffma2_rn(make_float2(zc1, zc1), qs, make_float2(acc[2], acc[3])),
+                                                     make_float2(S[t2][nb][1][0], S[t2][nb][1][1]));
+                        S[t2][nb][0][0] = s0.x;
+                        S[t2][nb][0][1] = s0.y;
+                        S[t2][nb][1][0] = s1.x;
+                        S[t2][nb][1][1] = s1.y;
+                    }
                 }
             }
         }
@@ -576,15 +591,21 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
         }
         // ---------------- O^T += V^T (P * rms)^T, group by group, both tiles; the
         // value fragments serve every block of columns
+        // value scales of groups G, G + 1 (G even) as one 32-bit word per token
+        uint32_t svp[A::TILES][4];
 #pragma unroll
         for (int G = 0; G < A::NG; ++G) {
+            if ((G & 1) == 0)
+#pragma unroll
+                for (int t2 = 0; t2 < A::TILES; ++t2)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        svp[t2][q] = vlive[t2][q] ? g_lds32(st + p.off_vs + ((vr[q] + TR * t2) * NG + G) * 2) : 0u;
 #pragma unroll
             for (int t2 = 0; t2 < A::TILES; ++t2) {
-                uint32_t sv[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    sv[q] = vlive[t2][q] ? g_lds16(st + p.off_vs + ((vr[q] + TR * t2) * NG + G) * 2) : 0u;
-                const uint32_t sv01 = sv[0] | (sv[1] << 16), sv23 = sv[2] | (sv[3] << 16);
+                // the two tokens' scales of group G as one f16 pair
+                const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
+                const uint32_t sv01 = __byte_perm(svp[t2][0], svp[t2][1], sel), sv23 = __byte_perm(svp[t2][2], svp[t2][3], sel);
                 // a[half]: rows g, g+8 of the m-tile = dims 32G + 4g + 2 half + {0, 1};
                 // registers 0, 1 pair tokens q0, q1, registers 2, 3 tokens q2, q3
                 uint32_t a[2][4];
