@@ -207,12 +207,12 @@ __device__ __forceinline__ void key_pairs_sw(uint32_t st, int r, int G, int c, u
         pr[2] = __byte_perm(h, 0x64646464u, 0x5140);
         pr[3] = __byte_perm(h, 0x64646464u, 0x5342);
     } else {
-        const uint32_t x = g_lds32(ksw_addr<D, 4>(st, r, (4 * G + c) * 4));  // codes k at bits 4k
+        // codes k at bits 4k; pair p = codes (p, p + 4) as f16 (1024 + code), one
+        // logic op after a shift (the q fragments of 4-bit instantiations hold
+        // the dims in that order)
+        const uint32_t x = g_lds32(ksw_addr<D, 4>(st, r, (4 * G + c) * 4));
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const uint32_t t = x >> (8 * p);  // codes 2p, 2p+1 at bits 0-3, 4-7
-            pr[p] = ((t & 0x0Fu) | ((t << 12) & 0x000F0000u)) | 0x64006400u;
-        }
+        for (int p = 0; p < 4; ++p) pr[p] = ((x >> (4 * p)) & 0x000F000Fu) | 0x64006400u;
     }
 }
 
@@ -365,8 +365,22 @@ __global__ void __launch_bounds__(GGeo<D, NB>::THREADS, GGeo<D, NB>::MIN_BLOCKS)
             f[2] = __low2float(*reinterpret_cast<__half2 *>(&hw[1]));
             f[3] = __high2float(*reinterpret_cast<__half2 *>(&hw[1]));
             uint32_t *slot = reinterpret_cast<uint32_t *>(qf + n * A::QCOL + ((2 * G + jj) * 4 + c) * 8);
-            slot[0] = hw[0];
-            slot[1] = hw[1];
+            if constexpr (KEY == 4) {
+                // dims 8c + {0..3} (jj = 0) and 8c + {4..7} (jj = 1) sit in neighbouring
+                // lanes; the 4-bit key pairs are (k, k + 4), so k-step jj = 0 takes
+                // (8c, 8c+4), (8c+1, 8c+5) and jj = 1 takes (8c+2, 8c+6), (8c+3, 8c+7)
+                const uint32_t o0 = __shfl_xor_sync(0xffffffffu, hw[0], 1), o1 = __shfl_xor_sync(0xffffffffu, hw[1], 1);
+                if (jj == 0) {
+                    slot[0] = __byte_perm(hw[0], o0, 0x5410);  // (own 8c, partner 8c+4)
+                    slot[1] = __byte_perm(hw[0], o0, 0x7632);  // (8c+1, 8c+5)
+                } else {
+                    slot[0] = __byte_perm(o1, hw[1], 0x5410);  // (partner 8c+2, own 8c+6)
+                    slot[1] = __byte_perm(o1, hw[1], 0x7632);  // (8c+3, 8c+7)
+                }
+            } else {
+                slot[0] = hw[0];
+                slot[1] = hw[1];
+            }
             float s = (f[0] + f[1]) + (f[2] + f[3]);
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
