@@ -303,12 +303,32 @@ def run_ours(args, rank, world, local_rank):
     # compute stream) and device-to-host reads (copy-out stream) overlap with
     # the neighbouring steps', on two sets of device buffers.  Every step still
     # copies all of its inputs in and its results out inside the timed region.
-    kp_h, vp_h = kp.cpu().pin_memory(), vp.cpu().pin_memory()
-    kn_h, vn_h, q_h = knew.cpu().pin_memory(), vnew.cpu().pin_memory(), q.cpu().pin_memory()
-    ko_h, vo_h = torch.empty_like(kp_h).pin_memory(), torch.empty_like(vp_h).pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    sets = [dict(kp=kp, vp=vp, knew=knew, vnew=vnew, q=q, ko=ko, vo=vo, out=out)]
-    sets.append({k: torch.empty_like(t) for k, t in sets[0].items()})
+    # A step's inputs (prefill K, V, the new token's K, V, q) live in one pinned
+    # host buffer and one device buffer per set, its results (fetched K, V,
+    # attention output) likewise, so each step is one copy in and one copy out.
+    def packing(tensors):
+        offs, o = [], 0
+        for t in tensors:
+            offs.append(o)
+            o += (t.numel() * t.element_size() + 511) // 512 * 512
+        return offs, o
+
+    def views(buf, offs, like):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, like)]
+
+    ins, outs = (kp, vp, knew, vnew, q), (ko, vo, out)
+    in_offs, in_bytes = packing(ins)
+    out_offs, out_bytes = packing(outs)
+    in_h = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    for hv, t in zip(views(in_h, in_offs, ins), ins):
+        hv.copy_(t.cpu())
+    out_h = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    sets = []
+    for _ in range(2):
+        ib = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        ob = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        sets.append(dict(inb=ib, outb=ob, **dict(zip(("kp", "vp", "knew", "vnew", "q"), views(ib, in_offs, ins))),
+                         **dict(zip(("ko", "vo", "out"), views(ob, out_offs, outs)))))
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     in_done = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
@@ -321,11 +341,7 @@ def run_ours(args, rank, world, local_rank):
         bs = sets[i]
         with torch.cuda.stream(s_in):
             s_in.wait_event(comp_done[i])  # set i's inputs were read by step s - 2
-            bs["kp"].copy_(kp_h, non_blocking=True)
-            bs["vp"].copy_(vp_h, non_blocking=True)
-            bs["knew"].copy_(kn_h, non_blocking=True)
-            bs["vnew"].copy_(vn_h, non_blocking=True)
-            bs["q"].copy_(q_h, non_blocking=True)
+            bs["inb"].copy_(in_h, non_blocking=True)
             in_done[i].record(s_in)
         stream.wait_event(in_done[i])
         stream.wait_event(out_done[i])  # set i's outputs were read back by step s - 2
@@ -336,9 +352,7 @@ def run_ours(args, rank, world, local_rank):
         comp_done[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i])
-            ko_h.copy_(bs["ko"], non_blocking=True)
-            vo_h.copy_(bs["vo"], non_blocking=True)
-            out_h.copy_(bs["out"], non_blocking=True)
+            out_h.copy_(bs["outb"], non_blocking=True)
             out_done[i].record(s_out)
 
     Ke = 20  # pipelined steps: enough that filling and draining the pipeline stay small
@@ -356,8 +370,7 @@ def run_ours(args, rank, world, local_rank):
     bb.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(bb) / Ke
-    h2d = sum(t.numel() * t.element_size() for t in (kp_h, vp_h, kn_h, vn_h, q_h))
-    d2h = sum(t.numel() * t.element_size() for t in (ko_h, vo_h, out_h))
+    h2d, d2h = in_h.numel(), out_h.numel()  # the bytes each step copies (padding included)
 
     # --- the other configurations (outside the headline's timed region)
     ctimes, cbytes = ({}, {}) if args.no_configs else \
@@ -424,7 +437,7 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": {"value": round(world * ab["total"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-                "pipelined": "copy-in, compute and copy-out streams overlap neighbouring steps (2 buffer sets)"},
+                "pipelined": "copy-in, compute and copy-out streams overlap neighbouring steps (2 buffer sets; one copy in and one copy out per step)"},
         # per step: prefill append (key and value kernels), fetch (one kernel for keys
         # and values), single-token append (one kernel), attention (split + combine)
         "gpu_launches": 6 * K,
