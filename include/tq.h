@@ -25,7 +25,12 @@
  *    surface at the caller's next synchronisation.  A launch failure returns
  *    TQ_ERR_CUDA.  Calls on one stream are ordered; calls that touch the same
  *    cache rows from different streams must be ordered by the caller.
- *  - Calls are capturable in a CUDA graph (no allocation, no sync).
+ *  - The calls other than tq_decode_attention_noalloc are capturable in a
+ *    CUDA graph (no allocation, no sync).
+ *  - Each kernel is launched as a programmatic dependent of the kernel before
+ *    it on the stream and waits for that kernel before it touches memory, so
+ *    stream order holds as for ordinary launches; only its start-up overlaps
+ *    the previous kernel's end.
  *  - Calls run on the calling thread's current CUDA device, which must hold
  *    every pointer.  The intended use is one process per GPU.  Kernel
  *    shared-memory opt-ins and occupancy figures are set up once per process,
