@@ -226,11 +226,11 @@ TQ_API size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_head
  *           16-byte aligned; its contents need no initialisation.
  * The token being generated must have been appended first (tq_encode_append
  * with t0 = seq_len - 1), as the page's updateAndFetch does.
- * Every head_dim, bit pair and group size G >= 1 is covered: head_dim 128
- * with 8- or 4-bit keys and 3-bit values run a specialised kernel (blocks
- * of 8 q-heads, one CTA per block, columns past G dropped), the rest a
- * generic one (code widths read at run time, groups in blocks of 8 q-heads);
- * both meet the same tolerance.
+ * Every head_dim, bit pair and group size G >= 1 is covered: head_dims 64,
+ * 128 and 256 with 8- or 4-bit keys and 3-bit values run a specialised
+ * kernel (blocks of 8 q-heads, one CTA per block, columns past G dropped),
+ * the rest a generic one (code widths read at run time, groups in blocks of
+ * 8 q-heads); both meet the same tolerance.
  */
 TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32_t q_heads, int64_t seq_len,
                               float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
@@ -240,8 +240,8 @@ TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32
  * Decode attention without any device allocation -- the pages have no
  * counterpart to this entry point; it exists for callers that cannot obtain
  * scratch memory.  Same arguments, output and tolerance as tq_decode_attention
- * minus the workspace, for the specialised parameters only (head_dim 128, 8-
- * or 4-bit keys, 3-bit values, any group size; others return
+ * minus the workspace, for the specialised parameters only (head_dim 64, 128
+ * or 256, 8- or 4-bit keys, 3-bit values, any group size; others return
  * TQ_ERR_UNSUPPORTED).  Typical callers: code running inside another
  * framework's memory manager that may not call cudaMalloc/cudaFree itself
  * (both can synchronise the device and fragment a pool someone else owns),
@@ -251,7 +251,8 @@ TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32
  *    that loads the library for the life of the process.  The split count is
  *    reduced when needed so the partials fit; if even one split needs more
  *    than 16 MiB (batch * num_kv_heads * ceil(G/8) * 8 * (d+2) * 4 bytes,
- *    i.e. batch * num_kv_heads * ceil(G/8) > 4032),
+ *    i.e. batch * num_kv_heads * ceil(G/8) > 7943, 4032 or 2032 at head_dim
+ *    64, 128 or 256),
  *    the call returns TQ_ERR_SCRATCH and launches nothing.
  *  - The first call on each device looks up the array's device address (a
  *    runtime query, not an allocation); make that first call before any

@@ -8,15 +8,18 @@
 // rotated domain and un-rotated once per query row).  GQA replicates whole
 // kv-heads: q-head h reads kv-head h / G.
 //
-// GB300 design (one GPU, sm_103a):
+// GB300 design (one GPU, sm_103a), for head_dims 64, 128 and 256 with 8- or
+// 4-bit keys and 3-bit values:
 //  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
 //    a 2-stage shared-memory ring; each of its 2 warps takes two 16-token tiles
 //    of a 64-token stage and works on both at once (independent dependency
-//    chains to interleave).  A stage is one 2-D TMA load of the key codes (128/64-byte
-//    swizzle, so the per-row fragment reads of the MMA are bank-conflict-free)
-//    and four 1-D bulk copies of the other planes, completing on the slot's
-//    mbarrier; the last warp to finish a stage issues the copies that refill
-//    its slot, so no warp is set aside as a producer (8 CTAs fit on an SM).
+//    chains to interleave).  A stage is 2-D TMA loads of the key codes (boxes
+//    of at most 128 bytes per row -- two at head_dim 256 with 8-bit keys --
+//    with the swizzle of the box width, so the per-row fragment reads of the
+//    MMA are bank-conflict-free) and four 1-D bulk copies of the other planes,
+//    completing on the slot's mbarrier; the last warp to finish a stage issues
+//    the copies that refill its slot, so no warp is set aside as a producer
+//    (8 CTAs fit on an SM at head_dim 128, 4 at 256).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
 //    tokens, N = 8 columns: 8 of the G q-heads sharing the kv-head (a group
 //    above 8 takes ceil(G/8) CTAs, neighbours in the grid so their reads of
@@ -31,7 +34,8 @@
 //  * Online softmax (base 2) per warp; warps merge in shared memory; each CTA
 //    writes (max, sum, unnormalised o) per head.  A second kernel merges the
 //    splits (log-sum-exp) and applies the inverse transform and signs once per
-//    (sequence, q-head).
+//    (sequence, q-head): the one below at head_dim 128, the generic kernel's
+//    (same partial layout) at 64 and 256.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,7 +47,6 @@
 namespace tq {
 namespace {
 
-constexpr int kD = 128;            // head_dim covered
 constexpr int kG = 8;              // MMA columns: a block of 8 of a kv-head's q-heads
 constexpr int kVB = 3;             // value bits covered
 constexpr int kCW = 2;             // warps per CTA (all compute; the last to finish a stage refills it)
@@ -57,22 +60,29 @@ __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / 
 // blocks of kG q-heads (MMA columns) per kv-head
 inline int col_blocks(int group) { return (group + kG - 1) / kG; }
 
-template <int KB>
+template <int KB, int D>
 struct AGeo {
-    static constexpr int KROW = kD * KB / 8;                   // key code bytes per token
+    static constexpr int NG = D / 32;                          // groups per row
+    static constexpr int KROW = D * KB / 8;                    // key code bytes per token
+    static constexpr int SW = KROW < 128 ? KROW : 128;         // key box row bytes = swizzle span
+    static constexpr int NBOX = KROW / SW;                     // key boxes per row
+    static constexpr int RBV = D * kVB / 8;                    // value code bytes per token
     static constexpr int K_BYTES = kStageT * KROW;
-    static constexpr int SC_BYTES = kStageT * (kD / 32) * 2;   // one fp16 plane
-    static constexpr int V_BYTES = kStageT * kD * kVB / 8;
+    static constexpr int SC_BYTES = kStageT * NG * 2;          // one fp16 plane
+    static constexpr int V_BYTES = kStageT * RBV;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_KS = K_BYTES;
     static constexpr int OFF_KZ = OFF_KS + SC_BYTES;
     static constexpr int OFF_VS = OFF_KZ + SC_BYTES;
     static constexpr int OFF_V = OFF_VS + SC_BYTES;
     static constexpr int STAGE = round_up(OFF_V + V_BYTES + 16, 1024);  // 1024: swizzle atom alignment
-    static constexpr int MERGE = kCW * kG * (kD + 2) * 4;             // per-warp partials (reuse the ring)
+    static constexpr int MERGE = kCW * kG * (D + 2) * 4;              // per-warp partials (reuse the ring)
     static constexpr int RING = kStages * STAGE > MERGE ? kStages * STAGE : MERGE;
     static constexpr int SMEM = 1024 /*align slack*/ + RING + kStages * 8 /*full barriers*/ + kStages * 4 /*counters*/;
     static constexpr float OFFSET = KB == 8 ? 1152.0f : 1024.0f;    // f16 value = OFFSET + code
+    // resident CTAs per SM the register budget is sized for (head_dim 256 holds
+    // twice the q fragments and output accumulators of 128)
+    static constexpr int MIN_BLOCKS = D >= 256 ? 4 : 8;
 };
 
 struct AttnParams {
@@ -142,6 +152,22 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a)
     return v;
 }
 
+// N consecutive 32-bit words of shared memory (N = 1, 2 or 4; the address aligned to 4 N bytes)
+template <int N>
+__device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&w)[N])
+{
+    if constexpr (N == 1) {
+        w[0] = lds32(a);
+    } else if constexpr (N == 2) {
+        const uint2 v = lds64(a);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+        static_assert(N == 4, "one, two or four words");
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(a));
+    }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
 {
     asm volatile(
@@ -178,11 +204,12 @@ __device__ __forceinline__ uint32_t shr_fma(uint32_t x)
 }
 
 // ---------------------------------------------------------------- the split kernel
-template <int KB>
-__global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                  const __grid_constant__ AttnParams p)
+template <int KB, int D>
+__global__ void __launch_bounds__(kThreads, AGeo<KB, D>::MIN_BLOCKS)
+    attn_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ AttnParams p)
 {
-    using A = AGeo<KB>;
+    using A = AGeo<KB, D>;
+    constexpr int NG = A::NG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
@@ -211,12 +238,14 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
         const int rows = (int)imin64(kStageT, p.cap - t);  // multiple of 16
         const int64_t row0 = bh * p.cap + t;
         const uint32_t st = smem_addr(stages + slot * A::STAGE), bar = full0 + 8 * slot;
-        mbar_arrive_expect_tx(bar, (uint32_t)(A::K_BYTES + rows * (3 * (kD / 32) * 2 + kD * kVB / 8)));
-        tma_load_2d(st + A::OFF_K, &kmap, 0, (int)row0, bar);
-        bulk_g2s(st + A::OFF_KS, p.k_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
-        bulk_g2s(st + A::OFF_KZ, p.k_zero + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
-        bulk_g2s(st + A::OFF_VS, p.v_scale + row0 * (kD / 32), rows * (kD / 32) * 2, bar);
-        bulk_g2s(st + A::OFF_V, p.v_codes + row0 * (kD * kVB / 8), rows * (kD * kVB / 8), bar);
+        mbar_arrive_expect_tx(bar, (uint32_t)(A::K_BYTES + rows * (3 * NG * 2 + A::RBV)));
+#pragma unroll
+        for (int j = 0; j < A::NBOX; ++j)  // key rows wider than 128 bytes arrive as several boxes
+            tma_load_2d(st + A::OFF_K + j * (kStageT * A::SW), &kmap, j * A::SW, (int)row0, bar);
+        bulk_g2s(st + A::OFF_KS, p.k_scale + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + A::OFF_KZ, p.k_zero + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + A::OFF_VS, p.v_scale + row0 * NG, rows * NG * 2, bar);
+        bulk_g2s(st + A::OFF_V, p.v_codes + row0 * A::RBV, rows * A::RBV, bar);
     };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -232,18 +261,18 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
     const int g = lane >> 2, c = lane & 3;
     // Q fragments (B operand of QK^T): head n = g; per k-step two f16x2 registers.
     // The dim order inside a 32-group is permuted to match how key codes unpack.
-    uint32_t bq[8][2];
-    float qs[4][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
+    uint32_t bq[2 * NG][2];
+    float qs[NG][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
     float ie[2];     // per head: 2^-e * softmax_scale * log2(e)
     {
         // columns past the last q-head are padding: they repeat head G-1 (MMA
         // columns never mix) and their partials are never read
         const int gq = kG * hb + g;
-        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (gq < p.G ? gq : p.G - 1)) * kD;
-        float qv[4][8];
+        const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (gq < p.G ? gq : p.G - 1)) * D;
+        float qv[NG][8];
         float mx = 0.0f;
 #pragma unroll
-        for (int G = 0; G < 4; ++G) {
+        for (int G = 0; G < NG; ++G) {
             const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * G + 8 * c);
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -261,9 +290,9 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
         if (mx > 0.0f && mx < INFINITY) e = 14 - (((int)(__float_as_uint(mx) >> 23) & 0xFF) - 127);
         e = e < -100 ? -100 : (e > 100 ? 100 : e);
         const float qscale = ldexpf(1.0f, e);
-        float qsum[4];
+        float qsum[NG];
 #pragma unroll
-        for (int G = 0; G < 4; ++G) {
+        for (int G = 0; G < NG; ++G) {
             float f[8];
             uint32_t hw[4];
 #pragma unroll
@@ -295,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
         }
         // group sums per head: head g lives in lanes 4g..4g+3; gather heads 2c, 2c+1
 #pragma unroll
-        for (int G = 0; G < 4; ++G) {
+        for (int G = 0; G < NG; ++G) {
             float s = qsum[G];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
@@ -307,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
         ie[1] = __shfl_sync(0xffffffffu, my_ie, (2 * c + 1) * 4);
     }
 
-    float o[8][4];
+    float o[2 * NG][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 2 * NG; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
@@ -319,19 +348,23 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
     const int r0 = 16 * warp + g, r1 = r0 + 8;  // key rows of this lane in the warp's first tile
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
 
-    // lane-constant byte offsets in a stage: key chunks of row r0 per group (row r1 is
-    // 8 rows on), value words of token vr[q] for group 0 (group G is 12 G bytes on)
-    uint32_t koff[4];
+    // lane-constant byte offsets in a stage: key bytes of row r0 per group (row r1 is
+    // 8 rows on, the next tile 16 kCW rows on, rows SW bytes apart in a box; the
+    // swizzle term is the same for all of them), value words of token vr[q] for
+    // group 0 (group G is 12 G bytes on).  The swizzle of an SW-byte box row
+    // xors the 16-byte chunk index with row % 8 (SW = 128), (row >> 1) % 4
+    // (SW = 64) or (row >> 2) % 2 (SW = 32).
+    const uint32_t xr = A::SW == 128 ? g : A::SW == 64 ? ((g >> 1) & 3) : ((g >> 2) & 1);
+    uint32_t koff[NG];
 #pragma unroll
-    for (int G = 0; G < 4; ++G) {
-        if constexpr (KB == 8)  // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
-            koff[G] = A::OFF_K + r0 * A::KROW + ((uint32_t)((2 * G + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
-        else  // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
-            koff[G] = A::OFF_K + r0 * A::KROW + ((uint32_t)(G ^ ((g >> 1) & 3)) << 4) + 4 * c;
+    for (int G = 0; G < NG; ++G) {
+        const int off = KB == 8 ? 32 * G + 8 * c : 16 * G + 4 * c;  // the lane's bytes of group G in the row
+        const int box = off / A::SW, col = off % A::SW;
+        koff[G] = A::OFF_K + box * (kStageT * A::SW) + r0 * A::SW + ((((uint32_t)col >> 4) ^ xr) << 4) + (col & 15);
     }
     uint32_t voff[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) voff[q] = A::OFF_V + vr[q] * (kD * kVB / 8) + 4 * v_word;
+    for (int q = 0; q < 4; ++q) voff[q] = A::OFF_V + vr[q] * A::RBV + 4 * v_word;
     // token offsets within the split fit 32 bits: a split never holds 2^31 rows
     // (136 B per row at the smallest width would take 292 GB)
     const int split_rows = (int)(t_end - t_begin);
@@ -354,17 +387,16 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
             const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
 
             // ---------------- S = Q K^T for 16 tokens x 8 heads, per key group
-            float acc[4][4];
+            float acc[NG][4];
 #pragma unroll
-            for (int G = 0; G < 4; ++G)
+            for (int G = 0; G < NG; ++G)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[G][j] = 0.0f;
 #pragma unroll
-            for (int G = 0; G < 4; ++G) {
+            for (int G = 0; G < NG; ++G) {
                 if constexpr (KB == 8) {
-                    // 128-byte swizzle: 16-byte chunk index ^= row % 8 (= g for both rows)
-                    const uint2 k0 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::KROW));
-                    const uint2 k1 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::KROW) + 8 * A::KROW);
+                    const uint2 k0 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::SW));
+                    const uint2 k1 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::SW) + 8 * A::SW);
                     // bytes 0 and 2 (then 1 and 3) of a word -> f16 (1024 + (byte ^ 0x80)):
                     // dims (8c+0, 8c+2), (8c+1, 8c+3), then +4
                     mma16816(acc[G], kcvt(k0.x, p), kcvt(k1.x, p), kcvt(shr_fma<8>(k0.x), p), kcvt(shr_fma<8>(k1.x), p),
@@ -372,9 +404,8 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
                     mma16816(acc[G], kcvt(k0.y, p), kcvt(k1.y, p), kcvt(shr_fma<8>(k0.y), p), kcvt(shr_fma<8>(k1.y), p),
                              bq[2 * G + 1][0], bq[2 * G + 1][1]);
                 } else {
-                    // 64-byte swizzle: chunk index ^= (row >> 1) % 4 (= g >> 1 for both rows)
-                    const uint32_t w0 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::KROW));
-                    const uint32_t w1 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::KROW) + 8 * A::KROW);
+                    const uint32_t w0 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::SW));
+                    const uint32_t w1 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::SW) + 8 * A::SW);
                     // nibbles k and k+4 -> f16 (1024 + nibble)
                     mma16816(acc[G], kcvt(w0, p), kcvt(w1, p), kcvt(shr_fma<4>(w0), p), kcvt(shr_fma<4>(w1), p), bq[2 * G][0],
                              bq[2 * G][1]);
@@ -385,15 +416,18 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
             // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum),
             // both heads of the lane at once on packed fp32 pairs
             {
-                const uint32_t m0 = (r0 + (16 * kCW) * t2) * 8, m1 = (r1 + (16 * kCW) * t2) * 8;
-                const uint2 s0 = lds64(st + A::OFF_KS + m0), s1 = lds64(st + A::OFF_KS + m1);
-                const uint2 z0 = lds64(st + A::OFF_KZ + m0), z1 = lds64(st + A::OFF_KZ + m1);
-                const uint32_t sw[2][2] = {{s0.x, s0.y}, {s1.x, s1.y}}, zw[2][2] = {{z0.x, z0.y}, {z1.x, z1.y}};
+                // a row's NG fp16 scales (zero points) are NG / 2 words
+                const uint32_t m0 = (r0 + (16 * kCW) * t2) * (NG * 2), m1 = (r1 + (16 * kCW) * t2) * (NG * 2);
+                uint32_t sw[2][NG / 2], zw[2][NG / 2];
+                lds_words(st + A::OFF_KS + m0, sw[0]);
+                lds_words(st + A::OFF_KS + m1, sw[1]);
+                lds_words(st + A::OFF_KZ + m0, zw[0]);
+                lds_words(st + A::OFF_KZ + m1, zw[1]);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     float2 sacc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                    for (int G = 0; G < 4; ++G) {
+                    for (int G = 0; G < NG; ++G) {
                         const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
                         const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
                         const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
@@ -474,23 +508,23 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
             // ---------------- P^T as the B operand (tokens x heads), transposed in registers
             const uint32_t pt0 = movmatrix_trans(pack_f16x2(pr[t2][0][0], pr[t2][0][1]));  // tokens 2c, 2c+1; head g
             const uint32_t pt1 = movmatrix_trans(pack_f16x2(pr[t2][1][0], pr[t2][1][1]));  // tokens 2c+8, 2c+9
-            // value scales of this lane's four tokens (zero past the range)
-            uint2 vs[4];
+            // value scales of this lane's four tokens, NG / 2 words each (zero past the range)
+            uint32_t vs[4][NG / 2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) vs[q] = lds64(st + A::OFF_VS + (vr[q] + (16 * kCW) * t2) * 8);
+            for (int q = 0; q < 4; ++q) lds_words(st + A::OFF_VS + (vr[q] + (16 * kCW) * t2) * (NG * 2), vs[q]);
             if (tile_r + 16 > split_rows) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    if (tile_r + (vr[q] - 16 * warp) >= split_rows) vs[q] = make_uint2(0u, 0u);
+                    if (tile_r + (vr[q] - 16 * warp) >= split_rows)
+#pragma unroll
+                        for (int k = 0; k < NG / 2; ++k) vs[q][k] = 0u;
             }
             // ---------------- O^T += V^T P'^T, per value group
 #pragma unroll
-            for (int G = 0; G < 4; ++G) {
-                const int sh = 16 * (G & 1);
-                const uint32_t sp0 = __byte_perm(G < 2 ? vs[0].x : vs[0].y, G < 2 ? vs[1].x : vs[1].y,
-                                                 sh ? 0x7632u : 0x5410u);
-                const uint32_t sp1 = __byte_perm(G < 2 ? vs[2].x : vs[2].y, G < 2 ? vs[3].x : vs[3].y,
-                                                 sh ? 0x7632u : 0x5410u);
+            for (int G = 0; G < NG; ++G) {
+                const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
+                const uint32_t sp0 = __byte_perm(vs[0][G >> 1], vs[1][G >> 1], sel);
+                const uint32_t sp1 = __byte_perm(vs[2][G >> 1], vs[3][G >> 1], sel);
                 const uint32_t b0 = hmul2(pt0, sp0), b1 = hmul2(pt1, sp1);
                 uint32_t av[2][2][2];  // [token pair][m-tile half][row g, row g+8]
                 // 12-bit fields (codes of dims 32G + 4g + 0..3 at bits 0, 3, 6, 9) of
@@ -498,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
                 uint32_t x[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint32_t base = st + voff[q] + t2 * ((16 * kCW) * (kD * kVB / 8)) + 12 * G;
+                    const uint32_t base = st + voff[q] + t2 * ((16 * kCW) * A::RBV) + 12 * G;
                     x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
                 }
 #pragma unroll
@@ -550,46 +584,46 @@ __global__ void __launch_bounds__(kThreads, 8) attn_split_kernel(const __grid_co
         l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
         l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
     }
-    float *mw = merge + warp * kG * (kD + 2);  // [head][D] o, then [head] m, [head] l
+    float *mw = merge + warp * kG * (D + 2);  // [head][D] o, then [head] m, [head] l
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
+    for (int mt = 0; mt < 2 * NG; ++mt) {
         const int G = mt >> 1, half = mt & 1;
         const int d0 = 32 * G + 4 * g + 2 * half;  // row g -> d0, row g+8 -> d0 + 1
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            mw[(2 * c + j) * kD + d0] = o[mt][j];
-            mw[(2 * c + j) * kD + d0 + 1] = o[mt][2 + j];
+            mw[(2 * c + j) * D + d0] = o[mt][j];
+            mw[(2 * c + j) * D + d0 + 1] = o[mt][2 + j];
         }
     }
     if (g == 0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            mw[kG * kD + 2 * c + j] = ok ? m_run[j] : -INFINITY;
-            mw[kG * kD + kG + 2 * c + j] = ok ? l_run[j] : 0.0f;
+            mw[kG * D + 2 * c + j] = ok ? m_run[j] : -INFINITY;
+            mw[kG * D + kG + 2 * c + j] = ok ? l_run[j] : 0.0f;
         }
     }
     __syncthreads();
-    // items (head, 8 dims), kG x 16 of them, over the CTA's threads
-    for (int item = threadIdx.x; item < kG * 16; item += kThreads) {
-        const int hh = item >> 4, d8 = (item & 15) * 8;
+    // items (head, 8 dims), kG x D / 8 of them, over the CTA's threads
+    for (int item = threadIdx.x; item < kG * (D / 8); item += kThreads) {
+        const int hh = item / (D / 8), d8 = (item % (D / 8)) * 8;
         float mmax = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) mmax = fmaxf(mmax, merge[w * kG * (kD + 2) + kG * kD + hh]);
+        for (int w = 0; w < kCW; ++w) mmax = fmaxf(mmax, merge[w * kG * (D + 2) + kG * D + hh]);
         const float mu = mmax == -INFINITY ? 0.0f : mmax;
         float ov[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lsum = 0.0f;
 #pragma unroll
         for (int w = 0; w < kCW; ++w) {
-            const float *m2 = merge + w * kG * (kD + 2);
-            const float wt = ex2(m2[kG * kD + hh] - mu);
-            lsum += m2[kG * kD + kG + hh] * wt;
+            const float *m2 = merge + w * kG * (D + 2);
+            const float wt = ex2(m2[kG * D + hh] - mu);
+            lsum += m2[kG * D + kG + hh] * wt;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ov[i] += m2[hh * kD + d8 + i] * wt;
+            for (int i = 0; i < 8; ++i) ov[i] += m2[hh * D + d8 + i] * wt;
         }
         const int64_t pidx = (((int64_t)b * p.H * p.NB + hv) * p.splits + split) * kG + hh;
-        float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * kD + d8);
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * D + d8);
         dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
         dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
-        if ((item & 15) == 0) {
+        if (d8 == 0) {
             p.part_ml[2 * pidx] = mmax;
             p.part_ml[2 * pidx + 1] = lsum;
         }
@@ -616,6 +650,7 @@ struct CombineParams {
 // then merges its warps' results.
 constexpr int kCombineWarps = 8;
 constexpr int kFew = 8;
+constexpr int kCombD = 128;  // head_dim of this merge (other head_dims take the generic kernel's)
 
 __host__ __device__ constexpr int combine_cta_warps(int W) { return W > kCombineWarps ? W : kCombineWarps; }
 
@@ -647,7 +682,7 @@ __global__ void __launch_bounds__(combine_cta_warps(W) * 32) attn_combine_kernel
         float4 v[kFew];
 #pragma unroll
         for (int j = 0; j < kFew; ++j)
-            v[j] = j < n_mine ? *reinterpret_cast<const float4 *>(p.part_o + split_index(j) * kD + 4 * lane)
+            v[j] = j < n_mine ? *reinterpret_cast<const float4 *>(p.part_o + split_index(j) * kCombD + 4 * lane)
                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         mw = ml.x;
 #pragma unroll
@@ -677,7 +712,7 @@ __global__ void __launch_bounds__(combine_cta_warps(W) * 32) attn_combine_kernel
 #pragma unroll 8
             for (int j = 0; j < cnt; ++j) {
                 const float w = __shfl_sync(0xffffffffu, wt, j);
-                const float4 v = *reinterpret_cast<const float4 *>(p.part_o + split_index(i0 + j) * kD + 4 * lane);
+                const float4 v = *reinterpret_cast<const float4 *>(p.part_o + split_index(i0 + j) * kCombD + 4 * lane);
                 xw.x += v.x * w; xw.y += v.y * w; xw.z += v.z * w; xw.w += v.w * w;
             }
         }
@@ -739,7 +774,7 @@ __global__ void __launch_bounds__(combine_cta_warps(W) * 32) attn_combine_kernel
         const bool neg = sign_negative(p.sg, dim);
         rr[i] = x[i] * (neg ? -p.inv_sqrt_d : p.inv_sqrt_d);
     }
-    *reinterpret_cast<float4 *>(p.out + ((int64_t)b * p.QH + qh) * kD + 4 * lane) = r;
+    *reinterpret_cast<float4 *>(p.out + ((int64_t)b * p.QH + qh) * kCombD + 4 * lane) = r;
 }
 
 // ---------------------------------------------------------------- host side
@@ -773,15 +808,15 @@ SplitPlan plan_splits(int B, int H, int64_t seq_len, int ctas_per_sm)
     return best;
 }
 
-template <int KB>
+template <int KB, int D>
 int ctas_per_sm_for()
 {
     static int cached = 0;  // same on every GB300; only a successful query is kept
     if (!cached) {
         int n = 0;
-        if (cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, AGeo<KB>::SMEM) ==
-                cudaSuccess &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<KB>, kThreads, AGeo<KB>::SMEM) ==
+        if (cudaFuncSetAttribute(attn_split_kernel<KB, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AGeo<KB, D>::SMEM) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<KB, D>, kThreads, AGeo<KB, D>::SMEM) ==
                 cudaSuccess &&
             n > 0)
             cached = n;
@@ -793,25 +828,26 @@ int ctas_per_sm_for()
 
 // Launch the split kernel and the combine with a given split plan, the
 // partials in `buf` (at least the plan's bytes; see plan_bytes).
-template <int KB>
+template <int KB, int D>
 cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
                                void *buf, const SplitPlan &plan, cudaStream_t s)
 {
-    using A = AGeo<KB>;
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+    using A = AGeo<KB, D>;
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
     if (e != cudaSuccess) return e;
-    const size_t need_o = (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * kD * 4;
+    const size_t need_o = (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * D * 4;
 
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)A::KROW, (cuuint64_t)c.B * c.H * c.cap};
     const cuuint64_t gstride[1] = {(cuuint64_t)A::KROW};
-    const cuuint32_t box[2] = {(cuuint32_t)A::KROW, (cuuint32_t)kStageT};
+    const cuuint32_t box[2] = {(cuuint32_t)A::SW, (cuuint32_t)kStageT};
     const cuuint32_t estride[2] = {1, 1};
-    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k_codes, gdim, gstride, box, estride,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, KB == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    const CUtensorMapSwizzle swz =
+        A::SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : A::SW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k_codes, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
     AttnParams p{};
@@ -849,8 +885,11 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
 
     dim3 grid(plan.splits, c.H * p.NB, c.B);
-    e = launch_dependent(attn_split_kernel<KB>, grid, dim3(kThreads), A::SMEM, s, map, p);
+    e = launch_dependent(attn_split_kernel<KB, D>, grid, dim3(kThreads), A::SMEM, s, map, p);
     if (e != cudaSuccess) return e;
+    if constexpr (D != kCombD)  // the generic kernel's merge: the same partial layout (one query row)
+        return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, 1, p.NB, kG, plan.splits,
+                                              c.signs, s);
 
     CombineParams cp{};
     cp.part_o = p.part_o;
@@ -862,7 +901,7 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     cp.NB = col_blocks(cp.G);
     cp.rows = c.B * QH;
     cp.splits = plan.splits;
-    cp.inv_sqrt_d = inv_sqrt_head_dim(kD);
+    cp.inv_sqrt_d = inv_sqrt_head_dim(kCombD);
     cp.sg = c.signs;
     // the merge is a programmatic dependent of the split kernel: its CTAs take
     // SMs as split CTAs retire and wait for the whole split grid before reading
@@ -877,27 +916,46 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
 // column of each (sequence, kv-head, column block, split).
 size_t plan_bytes(const CacheView &c, int QH, const SplitPlan &plan)
 {
-    return (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * (kD + 2) * 4;
+    return (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * (c.d + 2) * 4;
+}
+
+int ctas_per_sm(const CacheView &c)
+{
+    switch (c.d) {
+    case 64: return c.kb == 8 ? ctas_per_sm_for<8, 64>() : ctas_per_sm_for<4, 64>();
+    case 256: return c.kb == 8 ? ctas_per_sm_for<8, 256>() : ctas_per_sm_for<4, 256>();
+    default: return c.kb == 8 ? ctas_per_sm_for<8, 128>() : ctas_per_sm_for<4, 128>();
+    }
 }
 
 SplitPlan usual_plan(const CacheView &c, int QH, int64_t seq_len)
 {
-    const int per_sm = c.kb == 8 ? ctas_per_sm_for<8>() : ctas_per_sm_for<4>();
-    return plan_splits(c.B, c.H * col_blocks(QH / c.H), seq_len, per_sm);
+    return plan_splits(c.B, c.H * col_blocks(QH / c.H), seq_len, ctas_per_sm(c));
+}
+
+template <int D>
+cudaError_t run_attention_d(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
+                            void *buf, const SplitPlan &plan, cudaStream_t s)
+{
+    if (c.kb == 8) return run_attention_plan<8, D>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    return run_attention_plan<4, D>(c, q, QH, seq_len, scale, out, buf, plan, s);
 }
 
 cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
                           void *buf, const SplitPlan &plan, cudaStream_t s)
 {
-    if (c.kb == 8) return run_attention_plan<8>(c, q, QH, seq_len, scale, out, buf, plan, s);
-    return run_attention_plan<4>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    switch (c.d) {
+    case 64: return run_attention_d<64>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    case 256: return run_attention_d<256>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    default: return run_attention_d<128>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    }
 }
 
 }  // namespace
 
 bool attention_supported(int d, int kb, int vb, int group)
 {
-    return d == kD && vb == kVB && group >= 1 && (kb == 8 || kb == 4);
+    return (d == 64 || d == 128 || d == 256) && vb == kVB && group >= 1 && (kb == 8 || kb == 4);
 }
 
 size_t attention_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)

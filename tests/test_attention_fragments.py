@@ -216,3 +216,26 @@ def test_generic_swizzled_key_reads(d, kb):
                             bank = (a // 4 + w) % 32
                             words.setdefault(bank, set()).add(a // 4 + w)
                 assert max(len(v) for v in words.values()) <= 2
+
+
+@pytest.mark.parametrize("d,kb", [(d, kb) for d in (64, 128, 256) for kb in (4, 8)])
+def test_specialised_key_offsets(d, kb):
+    """The specialised kernel's per-lane key offsets (one per group, computed once:
+    koff[G] = box * 64 * SW + r0 * SW + ((chunk ^ xr) << 4) + byte, with the second
+    row of a tile 8 SW on and the warp's second tile 32 SW on) are the swizzled
+    addresses of the lane's bytes of rows r0, r0 + 8, r0 + 32, r0 + 40."""
+    rb = d * kb // 8
+    sw = min(rb, 128)
+    for warp in range(2):
+        for lane in range(32):
+            g, c = lane >> 2, lane & 3
+            r0 = 16 * warp + g
+            xr = g if sw == 128 else ((g >> 1) & 3) if sw == 64 else ((g >> 2) & 1)
+            for G in range(d // 32):
+                off = 32 * G + 8 * c if kb == 8 else 16 * G + 4 * c
+                box, col = off // sw, off % sw
+                koff = box * 64 * sw + r0 * sw + (((col >> 4) ^ xr) << 4) + (col & 15)
+                for t2 in range(2):
+                    for i in range(2):
+                        r = r0 + 8 * i + 32 * t2
+                        assert koff + t2 * 32 * sw + i * 8 * sw == ksw_addr(r, off, sw)

@@ -1,7 +1,7 @@
 """Decode attention for every head_dim, bit pair and GQA group size (the
-generic kernel; head_dim 128 k8/k4 v3 take the specialised kernel, in
-blocks of 8 q-heads) against the binary64 oracle.  Tolerance: 2e-3 max-abs on the fp32
-output, as for the specialised kernel.
+generic kernel; head_dims 64, 128 and 256 at k8/k4 v3 take the specialised
+kernel, in blocks of 8 q-heads) against the binary64 oracle.  Tolerance: 2e-3
+max-abs on the fp32 output, as for the specialised kernel.
 """
 import numpy as np
 import pytest
@@ -48,6 +48,17 @@ def test_specialised_kernel_group_sizes(cuda, kb, G, T):
     columns, those past G dropped): several splits, ragged stage tails, ragged
     combine blocks, one to three column blocks per kv-head."""
     err = _run(cuda, 128, kb, 3, B=3, H=3, G=G, T=T, cap=T + (16 - T % 16) % 16 + 16, step=G)
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("d,kb,G,T", [(64, 8, 8, 5000), (64, 4, 12, 3001), (256, 8, 4, 4133), (256, 4, 16, 2050),
+                                      (256, 8, 8, 777), (64, 8, 1, 64)])
+def test_specialised_kernel_head_dims(cuda, d, kb, G, T):
+    """The specialised kernel at head_dims 64 and 256 (one 32-byte, 64-byte or
+    128-byte swizzled key box per row, or two at d256 k8; the generic kernel's
+    merge): several splits, ragged stage tails, one or two column blocks per
+    kv-head, padding columns."""
+    err = _run(cuda, d, kb, 3, B=3, H=2, G=G, T=T, cap=T + (16 - T % 16) % 16 + 16, step=G)
     assert err < TOL, err
 
 

@@ -71,6 +71,23 @@ def test_noalloc_small_ragged(cuda, kb):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("d,kb", [(64, 8), (256, 4)])
+def test_noalloc_other_head_dims(cuda, d, kb):
+    """The specialised kernel's other head_dims (partials merged by the generic
+    kernel's merge), against tq_decode_attention and the oracle."""
+    w = tq_synth.WORKLOADS["decode"]
+    B, H, T = 2, 2, 777
+    k, v = tq_synth.host_kv(w, B=B, H=H, d=d, n=T)
+    cache = cuda.Cache(B, H, d, T + 7, k_bits=kb, v_bits=w.vb)
+    cuda.tq_encode_append(cache, to_device_bf16(k), to_device_bf16(v), 0)
+    qs = [to_device_bf16(tq_synth.host_q(w, step, B=B, QH=8 * H, d=d)) for step in (0, 1)]
+    got = _two_calls_match(cuda, cache, qs, T)
+    want = _oracle_pair(cache, qs[1], T, 1, 1, 8)
+    err = np.abs(got[1][1, 8:16].cpu().numpy().astype(np.float64) - want).max()
+    assert err < TOL, err
+
+
+@pytest.mark.gpu
 def test_noalloc_group_of_four(cuda):
     """4 q-heads per kv-head (half the specialised kernel's columns)."""
     w = tq_synth.WORKLOADS["decode"]
