@@ -47,8 +47,8 @@ BYTES_PER_TH = 200  # k8v3, d128 (page section "Algorithm", bytes per token-head
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0  # dense bf16, one earlier GB300 measurement
 NOMINAL_HBM_GBS = 8000.0  # the codec's stated roofline: bytes moved / 8 TB/s
-# decode attention on the generic kernel: (head_dim, key bits, value bits, sequences), ~0.4 GB each
-GENERIC_ATTN = ((256, 8, 3, 4), (64, 8, 3, 15), (128, 8, 4, 7))
+# decode attention at other head_dims and widths: (head_dim, key bits, value bits, sequences), ~0.4 GB each
+OTHER_ATTN = ((256, 8, 3, 4), (64, 8, 3, 15), (128, 8, 4, 7))
 LONGCTX = dict(B=32, H=8, QH=64, T=131072, d=128, kb=4, vb=3)
 SWEEP = dict(H=8, T=16384, ds=(64, 256, 512), kbs=(2, 4, 5, 8), vbs=(2, 3, 4))
 
@@ -611,11 +611,11 @@ def measure_configs(tq, tq_synth, torch, dev, dcache, knew, vnew, q, T, rank, st
                 del c
         del k, v, k16, v16, ko, vo
 
-    # decode attention on the generic kernel (head_dims and widths beside d128
-    # k8v3 / k4v3): ~0.4 GB caches of 32769 rows per sequence and kv-head
+    # decode attention at other head_dims (the specialised kernel) and widths
+    # (the generic kernel): ~0.4 GB caches of 32769 rows per sequence and kv-head
     wd = tq_synth.WORKLOADS["decode"]
     Tg = T + 1
-    for d, kb, vb, nbg in GENERIC_ATTN:
+    for d, kb, vb, nbg in OTHER_ATTN:
         goff, _ = rank_shard(rank, int(os.environ.get("WORLD_SIZE", "1")), nbg)
         gc = tq.Cache(nbg, D["H"], d, Tg + (16 - Tg % 16) % 16, kb, vb, device=dev)
         for b0 in range(nbg):
@@ -629,7 +629,7 @@ def measure_configs(tq, tq_synth, torch, dev, dcache, knew, vnew, q, T, rank, st
         qgb = qg.view(torch.bfloat16)
         og = torch.empty((nbg, D["QH"], d), dtype=torch.float32, device=dev)
         wsg = torch.empty(tq.tq_attention_workspace_bytes(gc, D["QH"], Tg), dtype=torch.uint8, device=dev)
-        name = f"generic_attention_d{d}_k{kb}v{vb}"
+        name = f"attention_d{d}_k{kb}v{vb}"
         times[name] = timed(lambda: tq.tq_decode_attention(gc, qgb, Tg, out=og, workspace=wsg))
         nbytes[name] = nbg * D["H"] * Tg * tq.tq_bytes_per_token_head(d, kb, vb) + nbg * D["QH"] * d * 6
         del gc, qg, qgb, og, wsg
@@ -698,10 +698,11 @@ def config_parts(times, nbytes, peak):
             tpeak, tkind = measured_bf16_tflops()
             out[name] = {"workload": desc, **r, "TFLOP/s": round(tf, 1), "tensor_frac": round(tf / tpeak, 4),
                          "tensor_peak": tpeak, "tensor_peak_kind": tkind}
-    for d, kb, vb, nbg in GENERIC_ATTN:
-        name = f"generic_attention_d{d}_k{kb}v{vb}"
+    for d, kb, vb, nbg in OTHER_ATTN:
+        name = f"attention_d{d}_k{kb}v{vb}"
+        kern = "specialised" if vb == 3 and kb in (8, 4) and d in (64, 128, 256) else "generic"
         if name in times:
-            out[name] = {"workload": f"decode attention on the generic kernel, {nbg} sequences x 8 kv-heads x 32769 rows, "
+            out[name] = {"workload": f"decode attention ({kern} kernel), {nbg} sequences x 8 kv-heads x 32769 rows, "
                                      f"64 q-heads, d{d} k{kb}v{vb}",
                          **rate(nbytes[name], times[name], peak)}
     for name, desc in (("rotated_fetch", "values in the rotated domain, 4 x 8 x 8192 rows, d128 v3, bf16 out"),
