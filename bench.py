@@ -933,7 +933,8 @@ def run_sweep(only=None):
     w = tq_synth.WORKLOADS["decode"]
     H, T = 8, 32769
     for d, kb, vb, G in [] if not want("attention") else [(128, 8, 3, 8), (128, 4, 3, 8), (128, 4, 2, 8), (128, 8, 4, 8), (128, 5, 2, 8),
-                         (128, 8, 3, 4), (128, 8, 3, 16), (64, 8, 3, 8), (256, 8, 3, 8), (512, 4, 3, 4)]:
+                         (128, 8, 3, 4), (128, 8, 3, 16), (64, 8, 3, 8), (256, 8, 3, 8), (64, 4, 3, 8),
+                         (256, 4, 3, 8), (512, 4, 3, 4)]:
         bpt = tq.tq_bytes_per_token_head(d, kb, vb)
         B = max(1, round(4e8 / (H * T * bpt)))
         cache = filled_cache(B, H, d, T, kb, vb, w)
@@ -943,7 +944,7 @@ def run_sweep(only=None):
         out = torch.empty((B, G * H, d), dtype=torch.float32, device="cuda")
         ws = torch.empty(tq.tq_attention_workspace_bytes(cache, G * H, T), dtype=torch.uint8, device="cuda")
         us = timed(lambda: tq.tq_decode_attention(cache, qb, T, out=out, workspace=ws))
-        path = "specialised" if (d, vb) == (128, 3) and kb in (8, 4) else "generic"
+        path = "specialised" if vb == 3 and kb in (8, 4) and d in (64, 128, 256) else "generic"
         emit("attention", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": kb, "vb": vb, "group": G, "kernel": path},
              us, B * H * T * bpt + B * G * H * d * 6)
         del cache, ws, out, q
