@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0  # dense bf16, one earlier GB300 measurement
 NOMINAL_HBM_GBS = 8000.0  # the codec's stated roofline: bytes moved / 8 TB/s
 # decode attention at other head_dims and widths: (head_dim, key bits, value bits, sequences), ~0.4 GB each
-OTHER_ATTN = ((256, 8, 3, 4), (64, 8, 3, 15), (128, 8, 4, 7))
+OTHER_ATTN = ((256, 8, 3, 4), (64, 8, 3, 15), (128, 8, 4, 7), (128, 5, 2, 11))
 LONGCTX = dict(B=32, H=8, QH=64, T=131072, d=128, kb=4, vb=3)
 SWEEP = dict(H=8, T=16384, ds=(64, 256, 512), kbs=(2, 4, 5, 8), vbs=(2, 3, 4))
 
@@ -700,7 +700,7 @@ def config_parts(times, nbytes, peak):
                          "tensor_peak": tpeak, "tensor_peak_kind": tkind}
     for d, kb, vb, nbg in OTHER_ATTN:
         name = f"attention_d{d}_k{kb}v{vb}"
-        kern = "specialised" if vb == 3 and kb in (8, 4) and d in (64, 128, 256) else "generic"
+        kern = "specialised" if vb in (2, 3, 4) and kb in (8, 4) and d in (64, 128, 256) else "generic"
         if name in times:
             out[name] = {"workload": f"decode attention ({kern} kernel), {nbg} sequences x 8 kv-heads x 32769 rows, "
                                      f"64 q-heads, d{d} k{kb}v{vb}",
@@ -944,7 +944,7 @@ def run_sweep(only=None):
         out = torch.empty((B, G * H, d), dtype=torch.float32, device="cuda")
         ws = torch.empty(tq.tq_attention_workspace_bytes(cache, G * H, T), dtype=torch.uint8, device="cuda")
         us = timed(lambda: tq.tq_decode_attention(cache, qb, T, out=out, workspace=ws))
-        path = "specialised" if vb == 3 and kb in (8, 4) and d in (64, 128, 256) else "generic"
+        path = "specialised" if vb in (2, 3, 4) and kb in (8, 4) and d in (64, 128, 256) else "generic"
         emit("attention", {"B": B, "kv_heads": H, "rows": T, "d": d, "kb": kb, "vb": vb, "group": G, "kernel": path},
              us, B * H * T * bpt + B * G * H * d * 6)
         del cache, ws, out, q

@@ -227,8 +227,9 @@ TQ_API size_t tq_attention_workspace_bytes(const tq_cache *cache, int32_t q_head
  * The token being generated must have been appended first (tq_encode_append
  * with t0 = seq_len - 1), as the page's updateAndFetch does.
  * Every head_dim, bit pair and group size G >= 1 is covered: head_dims 64,
- * 128 and 256 with 8- or 4-bit keys and 3-bit values run a specialised
- * kernel (blocks of 8 q-heads, one CTA per block, columns past G dropped),
+ * 128 and 256 with 8- or 4-bit keys and 2-, 3- or 4-bit values run a
+ * specialised kernel (blocks of 8 q-heads, one CTA per block, columns past G
+ * dropped),
  * the rest a generic one (code widths read at run time, groups in blocks of
  * 8 q-heads); both meet the same tolerance.
  */
@@ -241,8 +242,8 @@ TQ_API tq_status tq_decode_attention(const tq_cache *cache, const void *q, int32
  * counterpart to this entry point; it exists for callers that cannot obtain
  * scratch memory.  Same arguments, output and tolerance as tq_decode_attention
  * minus the workspace, for the specialised parameters only (head_dim 64, 128
- * or 256, 8- or 4-bit keys, 3-bit values, any group size; others return
- * TQ_ERR_UNSUPPORTED).  Typical callers: code running inside another
+ * or 256, 8- or 4-bit keys, 2-, 3- or 4-bit values, any group size; others
+ * return TQ_ERR_UNSUPPORTED).  Typical callers: code running inside another
  * framework's memory manager that may not call cudaMalloc/cudaFree itself
  * (both can synchronise the device and fragment a pool someone else owns),
  * and plugin-style integrations with no allocator handle to pass a workspace

@@ -9,7 +9,7 @@
 // kv-heads: q-head h reads kv-head h / G.
 //
 // GB300 design (one GPU, sm_103a), for head_dims 64, 128 and 256 with 8- or
-// 4-bit keys and 3-bit values:
+// 4-bit keys and 2-, 3- or 4-bit values:
 //  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
 //    a 2-stage shared-memory ring; each of its 2 warps takes two 16-token tiles
 //    of a 64-token stage and works on both at once (independent dependency
@@ -29,8 +29,11 @@
 //    S = sum_g scale_g * (acc_g + (zero_g - offset) * sum_{j in g} q_j) -- the
 //    per-group affine is applied to the 8-head scores, not to each element.
 //  * PV in the rotated domain (mma.sync, M = 16 dims, N = 8 heads, K = 16
-//    tokens): 3-bit codes are mapped to f16 centroids by byte-permute table
-//    lookups in registers; the per-group RMS scale is folded into P.
+//    tokens): value codes are mapped to f16 centroids by byte-permute table
+//    lookups in registers (3 bits: four codes spread to nibbles per lookup;
+//    2 bits: one f16 pair of the four centroids per lookup; 4 bits: the
+//    magnitude index and sign of each code, the table being odd); the
+//    per-group RMS scale is folded into P.
 //  * Online softmax (base 2) per warp; warps merge in shared memory; each CTA
 //    writes (max, sum, unnormalised o) per head.  A second kernel merges the
 //    splits (log-sum-exp) and applies the inverse transform and signs once per
@@ -48,7 +51,6 @@ namespace tq {
 namespace {
 
 constexpr int kG = 8;              // MMA columns: a block of 8 of a kv-head's q-heads
-constexpr int kVB = 3;             // value bits covered
 constexpr int kCW = 2;             // warps per CTA (all compute; the last to finish a stage refills it)
 constexpr int kThreads = kCW * 32;
 constexpr int kTiles = 2;          // 16-token tiles per warp and stage, worked on together
@@ -60,13 +62,13 @@ __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / 
 // blocks of kG q-heads (MMA columns) per kv-head
 inline int col_blocks(int group) { return (group + kG - 1) / kG; }
 
-template <int KB, int D>
+template <int KB, int D, int VB>
 struct AGeo {
     static constexpr int NG = D / 32;                          // groups per row
     static constexpr int KROW = D * KB / 8;                    // key code bytes per token
     static constexpr int SW = KROW < 128 ? KROW : 128;         // key box row bytes = swizzle span
     static constexpr int NBOX = KROW / SW;                     // key boxes per row
-    static constexpr int RBV = D * kVB / 8;                    // value code bytes per token
+    static constexpr int RBV = D * VB / 8;                     // value code bytes per token
     static constexpr int K_BYTES = kStageT * KROW;
     static constexpr int SC_BYTES = kStageT * NG * 2;          // one fp16 plane
     static constexpr int V_BYTES = kStageT * RBV;
@@ -95,7 +97,11 @@ struct AttnParams {
     int64_t cap, seq_len, tokens_per_split;
     float scale_log2;  // softmax_scale * log2(e)
     uint32_t *err;
-    uint32_t tl0, tl1, th0, th1;  // f16 centroid bytes: low bytes (c0..c7), high bytes
+    // value centroids as byte-permute tables: 3 bits -- low bytes of the f16
+    // c0..c7 (tl0, tl1), then their high bytes (th0, th1); 2 bits -- the f16
+    // c0, c1 (tl0) and c2, c3 (tl1); 4 bits -- low and high bytes of the f16
+    // magnitudes c8..c15 (the table is odd: c[15 - k] = -c[k])
+    uint32_t tl0, tl1, th0, th1;
     uint32_t k_const, k_flip;     // key byte -> f16 (1024 + byte ^ 0x80) as one logic op (see below)
 };
 
@@ -204,11 +210,11 @@ __device__ __forceinline__ uint32_t shr_fma(uint32_t x)
 }
 
 // ---------------------------------------------------------------- the split kernel
-template <int KB, int D>
-__global__ void __launch_bounds__(kThreads, AGeo<KB, D>::MIN_BLOCKS)
+template <int KB, int D, int VB>
+__global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
     attn_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ AttnParams p)
 {
-    using A = AGeo<KB, D>;
+    using A = AGeo<KB, D, VB>;
     constexpr int NG = A::NG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -343,8 +349,9 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D>::MIN_BLOCKS)
         for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
 
-    // V field extraction: lane g owns dims 32G + 4g + {0..3}: 12 bits at 96G + 12g
-    const int v_word = (12 * g) >> 5, v_shift = (12 * g) & 31;
+    // V field extraction: lane g owns dims 32G + 4g + {0..3}: 4 VB bits at bit
+    // (32G + 4g) VB of the row (word 32G VB / 32 + v_word, shift v_shift)
+    const int v_word = (4 * VB * g) >> 5, v_shift = (4 * VB * g) & 31;
     const int r0 = 16 * warp + g, r1 = r0 + 8;  // key rows of this lane in the warp's first tile
     const int vr[4] = {16 * warp + 2 * c, 16 * warp + 2 * c + 1, 16 * warp + 2 * c + 8, 16 * warp + 2 * c + 9};
 
@@ -527,32 +534,65 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D>::MIN_BLOCKS)
                 const uint32_t sp1 = __byte_perm(vs[2][G >> 1], vs[3][G >> 1], sel);
                 const uint32_t b0 = hmul2(pt0, sp0), b1 = hmul2(pt1, sp1);
                 uint32_t av[2][2][2];  // [token pair][m-tile half][row g, row g+8]
-                // 12-bit fields (codes of dims 32G + 4g + 0..3 at bits 0, 3, 6, 9) of
-                // the lane's four tokens; bits above 11 are don't-care
+                // the 4 VB-bit field (codes of dims 32G + 4g + 0..3 at bits 0, VB, 2 VB,
+                // 3 VB) of the lane's four tokens; bits above 4 VB are don't-care
                 uint32_t x[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint32_t base = st + voff[q] + t2 * ((16 * kCW) * A::RBV) + 12 * G;
-                    x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
+                    const uint32_t base = st + voff[q] + t2 * ((16 * kCW) * A::RBV) + 4 * VB * G;
+                    if constexpr (VB == 3)  // 12-bit fields may straddle two words
+                        x[q] = __funnelshift_r(lds32(base), lds32(base + 4), v_shift);
+                    else  // 8- or 16-bit fields sit inside one word
+                        x[q] = lds32(base) >> v_shift;
                 }
 #pragma unroll
                 for (int pr2 = 0; pr2 < 2; ++pr2) {  // token pairs (2c, 2c+1) and (2c+8, 2c+9)
-                    // both tokens' fields side by side (first in bits 0-15), then one
-                    // code per nibble: codes r0..r3 of the first token in nibbles
-                    // 0..3, of the second in nibbles 4..7
-                    const uint32_t w = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
-                    const uint32_t y = (w & 0x003F003Fu) | ((w & 0x0FC00FC0u) * 4u);
-                    // each byte of y holds two codes (bits 0-2, 3-5); adding the upper code
-                    // to itself moves it to bits 4-6, and nothing carries out of a byte
-                    const uint32_t e = y + (y & 0x38383838u);
+                    if constexpr (VB == 3) {
+                        // both tokens' fields side by side (first in bits 0-15), then one
+                        // code per nibble: codes r0..r3 of the first token in nibbles
+                        // 0..3, of the second in nibbles 4..7
+                        const uint32_t w = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
+                        const uint32_t y = (w & 0x003F003Fu) | ((w & 0x0FC00FC0u) * 4u);
+                        // each byte of y holds two codes (bits 0-2, 3-5); adding the upper code
+                        // to itself moves it to bits 4-6, and nothing carries out of a byte
+                        const uint32_t e = y + (y & 0x38383838u);
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        // selector: codes (r, r+1) of the first token, then of the second
-                        const uint32_t sel = __byte_perm(e, 0u, half ? 0x0031u : 0x0020u);
-                        const uint32_t lo = prmt(p.tl0, p.tl1, sel);  // low f16 bytes of the 4 centroids
-                        const uint32_t hi = prmt(p.th0, p.th1, sel);  // high f16 bytes
-                        av[pr2][half][0] = __byte_perm(lo, hi, 0x6240u);  // dim r: (first, second)
-                        av[pr2][half][1] = __byte_perm(lo, hi, 0x7351u);  // dim r + 1
+                        for (int half = 0; half < 2; ++half) {
+                            // selector: codes (r, r+1) of the first token, then of the second
+                            const uint32_t sel = __byte_perm(e, 0u, half ? 0x0031u : 0x0020u);
+                            const uint32_t lo = prmt(p.tl0, p.tl1, sel);  // low f16 bytes of the 4 centroids
+                            const uint32_t hi = prmt(p.th0, p.th1, sel);  // high f16 bytes
+                            av[pr2][half][0] = __byte_perm(lo, hi, 0x6240u);  // dim r: (first, second)
+                            av[pr2][half][1] = __byte_perm(lo, hi, 0x7351u);  // dim r + 1
+                        }
+                    } else if constexpr (VB == 2) {
+                        // both tokens' bytes side by side; for dim r the two codes (a, b)
+                        // pick the f16 pair (c[a], c[b]) out of c0..c3 in one permute:
+                        // selector nibbles (2a, 2a+1, 2b, 2b+1)
+                        const uint32_t u = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x0040u);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const uint32_t ab = (u >> (2 * r)) & 0x0303u;
+                            av[pr2][r >> 1][r & 1] = prmt(p.tl0, p.tl1, ab * 0x22u + 0x1010u);
+                        }
+                    } else {
+                        // the two tokens' 16-bit fields side by side (a nibble per code);
+                        // the table is odd, so a code is a magnitude index (code - 8 for
+                        // code >= 8, 7 - code below) and a sign (negative below 8):
+                        // t has bit 4i set where code i < 8, m the magnitude indices
+                        const uint32_t u = __byte_perm(x[2 * pr2], x[2 * pr2 + 1], 0x5410u);
+                        const uint32_t t = (~u >> 3) & 0x11111111u;
+                        const uint32_t m = (u ^ (t * 7u)) & 0x77777777u;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t sel = __byte_perm(m, 0u, half ? 0x0031u : 0x0020u);
+                            const uint32_t lo = prmt(p.tl0, p.tl1, sel), hi = prmt(p.th0, p.th1, sel);
+                            // dim r = 2 half (+1): the two tokens' sign bits (bits 4r and 16 + 4r
+                            // of t) moved to the f16 sign positions 15 and 31
+                            const int r = 2 * half;
+                            av[pr2][half][0] = __byte_perm(lo, hi, 0x6240u) ^ ((t << (15 - 4 * r)) & 0x80008000u);
+                            av[pr2][half][1] = __byte_perm(lo, hi, 0x7351u) ^ ((t << (11 - 4 * r)) & 0x80008000u);
+                        }
                     }
                 }
 #pragma unroll
@@ -808,16 +848,16 @@ SplitPlan plan_splits(int B, int H, int64_t seq_len, int ctas_per_sm)
     return best;
 }
 
-template <int KB, int D>
+template <int KB, int D, int VB>
 int ctas_per_sm_for()
 {
     static int cached = 0;  // same on every GB300; only a successful query is kept
     if (!cached) {
         int n = 0;
-        if (cudaFuncSetAttribute(attn_split_kernel<KB, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 AGeo<KB, D>::SMEM) == cudaSuccess &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<KB, D>, kThreads, AGeo<KB, D>::SMEM) ==
-                cudaSuccess &&
+        if (cudaFuncSetAttribute(attn_split_kernel<KB, D, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AGeo<KB, D, VB>::SMEM) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<KB, D, VB>, kThreads,
+                                                          AGeo<KB, D, VB>::SMEM) == cudaSuccess &&
             n > 0)
             cached = n;
         else
@@ -828,12 +868,13 @@ int ctas_per_sm_for()
 
 // Launch the split kernel and the combine with a given split plan, the
 // partials in `buf` (at least the plan's bytes; see plan_bytes).
-template <int KB, int D>
+template <int KB, int D, int VB>
 cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
                                void *buf, const SplitPlan &plan, cudaStream_t s)
 {
-    using A = AGeo<KB, D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<KB, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+    using A = AGeo<KB, D, VB>;
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_split_kernel<KB, D, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
     if (e != cudaSuccess) return e;
     const size_t need_o = (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * D * 4;
 
@@ -869,23 +910,31 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return cudaErrorInvalidDevice;
-    const Tables &tab = codebook_tables(kVB);
-    uint8_t lo[8], hi[8];
-    for (int i = 0; i < 8; ++i) {
-        const uint16_t hb = __half_as_ushort(__float2half_rn(tab.centroids[i]));
-        lo[i] = (uint8_t)(hb & 0xFF);
-        hi[i] = (uint8_t)(hb >> 8);
+    const Tables &tab = codebook_tables(VB);
+    auto f16b = [](float x) { return (uint32_t)__half_as_ushort(__float2half_rn(x)); };
+    if constexpr (VB == 2) {
+        p.tl0 = f16b(tab.centroids[0]) | f16b(tab.centroids[1]) << 16;
+        p.tl1 = f16b(tab.centroids[2]) | f16b(tab.centroids[3]) << 16;
+    } else {
+        // 3 bits: the eight centroids; 4 bits: the eight magnitudes c8..c15
+        const int first = VB == 3 ? 0 : 8;
+        uint32_t lo[8], hi[8];
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t hb = f16b(tab.centroids[first + i]);
+            lo[i] = hb & 0xFF;
+            hi[i] = hb >> 8;
+        }
+        p.tl0 = lo[0] | lo[1] << 8 | lo[2] << 16 | lo[3] << 24;
+        p.tl1 = lo[4] | lo[5] << 8 | lo[6] << 16 | lo[7] << 24;
+        p.th0 = hi[0] | hi[1] << 8 | hi[2] << 16 | hi[3] << 24;
+        p.th1 = hi[4] | hi[5] << 8 | hi[6] << 16 | hi[7] << 24;
     }
-    p.tl0 = lo[0] | lo[1] << 8 | lo[2] << 16 | (uint32_t)lo[3] << 24;
-    p.tl1 = lo[4] | lo[5] << 8 | lo[6] << 16 | (uint32_t)lo[7] << 24;
-    p.th0 = hi[0] | hi[1] << 8 | hi[2] << 16 | (uint32_t)hi[3] << 24;
-    p.th1 = hi[4] | hi[5] << 8 | hi[6] << 16 | (uint32_t)hi[7] << 24;
     // bits where R1 is set take R2; the others take byte ^ R2 (flip bit 7 and 23)
     p.k_const = KB == 8 ? 0xFF00FF00u : 0xFFF0FFF0u;
     p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
 
     dim3 grid(plan.splits, c.H * p.NB, c.B);
-    e = launch_dependent(attn_split_kernel<KB, D>, grid, dim3(kThreads), A::SMEM, s, map, p);
+    e = launch_dependent(attn_split_kernel<KB, D, VB>, grid, dim3(kThreads), A::SMEM, s, map, p);
     if (e != cudaSuccess) return e;
     if constexpr (D != kCombD)  // the generic kernel's merge: the same partial layout (one query row)
         return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, 1, p.NB, kG, plan.splits,
@@ -919,13 +968,21 @@ size_t plan_bytes(const CacheView &c, int QH, const SplitPlan &plan)
     return (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * (c.d + 2) * 4;
 }
 
+template <int D, int VB>
+int ctas_per_sm_dv(const CacheView &c)
+{
+    return c.kb == 8 ? ctas_per_sm_for<8, D, VB>() : ctas_per_sm_for<4, D, VB>();
+}
+
+template <int D>
+int ctas_per_sm_d(const CacheView &c)
+{
+    return c.vb == 2 ? ctas_per_sm_dv<D, 2>(c) : c.vb == 4 ? ctas_per_sm_dv<D, 4>(c) : ctas_per_sm_dv<D, 3>(c);
+}
+
 int ctas_per_sm(const CacheView &c)
 {
-    switch (c.d) {
-    case 64: return c.kb == 8 ? ctas_per_sm_for<8, 64>() : ctas_per_sm_for<4, 64>();
-    case 256: return c.kb == 8 ? ctas_per_sm_for<8, 256>() : ctas_per_sm_for<4, 256>();
-    default: return c.kb == 8 ? ctas_per_sm_for<8, 128>() : ctas_per_sm_for<4, 128>();
-    }
+    return c.d == 64 ? ctas_per_sm_d<64>(c) : c.d == 256 ? ctas_per_sm_d<256>(c) : ctas_per_sm_d<128>(c);
 }
 
 SplitPlan usual_plan(const CacheView &c, int QH, int64_t seq_len)
@@ -933,12 +990,21 @@ SplitPlan usual_plan(const CacheView &c, int QH, int64_t seq_len)
     return plan_splits(c.B, c.H * col_blocks(QH / c.H), seq_len, ctas_per_sm(c));
 }
 
+template <int D, int VB>
+cudaError_t run_attention_dv(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
+                             void *buf, const SplitPlan &plan, cudaStream_t s)
+{
+    if (c.kb == 8) return run_attention_plan<8, D, VB>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    return run_attention_plan<4, D, VB>(c, q, QH, seq_len, scale, out, buf, plan, s);
+}
+
 template <int D>
 cudaError_t run_attention_d(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
                             void *buf, const SplitPlan &plan, cudaStream_t s)
 {
-    if (c.kb == 8) return run_attention_plan<8, D>(c, q, QH, seq_len, scale, out, buf, plan, s);
-    return run_attention_plan<4, D>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    if (c.vb == 2) return run_attention_dv<D, 2>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    if (c.vb == 4) return run_attention_dv<D, 4>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    return run_attention_dv<D, 3>(c, q, QH, seq_len, scale, out, buf, plan, s);
 }
 
 cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
@@ -951,11 +1017,23 @@ cudaError_t run_attention(const CacheView &c, const uint16_t *q, int QH, int64_t
     }
 }
 
+// The 4-bit lookup reads magnitudes and a sign: the table must be odd
+// (c[15 - k] = -c[k], as the optimum for a symmetric density is).
+bool four_bit_table_odd()
+{
+    const Tables &t = codebook_tables(4);
+    for (int k = 0; k < 8; ++k)
+        if (t.centroids[15 - k] != -t.centroids[k]) return false;
+    return true;
+}
+
 }  // namespace
 
 bool attention_supported(int d, int kb, int vb, int group)
 {
-    return (d == 64 || d == 128 || d == 256) && vb == kVB && group >= 1 && (kb == 8 || kb == 4);
+    static const bool odd4 = four_bit_table_odd();
+    return (d == 64 || d == 128 || d == 256) && (vb == 3 || vb == 2 || (vb == 4 && odd4)) && group >= 1 &&
+           (kb == 8 || kb == 4);
 }
 
 size_t attention_workspace_bytes(const CacheView &c, int q_heads, int64_t seq_len)

@@ -1,9 +1,9 @@
 // tq_attention_generic.cuh -- fused dequantise-on-fetch attention for every
 // head_dim, bit pair and GQA group size, with one or several query rows per
 // sequence.  The kernel in tq_attention.cu is the specialised one-row path for
-// head_dims 64, 128 and 256, 8- or 4-bit keys, 3-bit values and groups of 8
-// q-heads; this one covers the rest with the same method and the same
-// tolerance.
+// head_dims 64, 128 and 256, 8- or 4-bit keys, 2-, 3- or 4-bit values and
+// groups of 8 q-heads; this one covers the rest with the same method and the
+// same tolerance.
 //
 // Method: mlx-bun "TurboQuant -- rotation-based quantization", Part A:
 // "Architecture in mlx-bun" (attention reads the dequantised window),

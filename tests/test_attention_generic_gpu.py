@@ -1,6 +1,7 @@
 """Decode attention for every head_dim, bit pair and GQA group size (the
-generic kernel; head_dims 64, 128 and 256 at k8/k4 v3 take the specialised
-kernel, in blocks of 8 q-heads) against the binary64 oracle.  Tolerance: 2e-3
+generic kernel; head_dims 64, 128 and 256 with 8- or 4-bit keys and 2-, 3-
+or 4-bit values take the specialised kernel, in blocks of 8 q-heads) against
+the binary64 oracle.  Tolerance: 2e-3
 max-abs on the fp32 output, as for the specialised kernel.
 """
 import numpy as np
@@ -59,6 +60,16 @@ def test_specialised_kernel_head_dims(cuda, d, kb, G, T):
     merge): several splits, ragged stage tails, one or two column blocks per
     kv-head, padding columns."""
     err = _run(cuda, d, kb, 3, B=3, H=2, G=G, T=T, cap=T + (16 - T % 16) % 16 + 16, step=G)
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("d,kb,vb,G,T", [(128, 8, 4, 8, 5000), (128, 4, 2, 12, 3001), (256, 8, 4, 4, 4133),
+                                         (64, 4, 2, 8, 2050), (256, 4, 2, 16, 777), (64, 8, 4, 3, 1234)])
+def test_specialised_kernel_value_widths(cuda, d, kb, vb, G, T):
+    """2- and 4-bit values on the specialised kernel (one permute per f16 pair
+    out of the four 2-bit centroids; 4-bit codes as a magnitude index and a
+    sign, the table being odd): several splits, ragged tails, padding columns."""
+    err = _run(cuda, d, kb, vb, B=3, H=2, G=G, T=T, cap=T + (16 - T % 16) % 16 + 16, step=G)
     assert err < TOL, err
 
 

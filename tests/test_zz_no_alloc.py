@@ -154,8 +154,8 @@ def test_noalloc_rejects_problems_beyond_the_scratch(tqlib):
     s = tqlib._CacheStruct(128, 8, 3, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
     assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 17, 1.0, 0x20000, None) == S["TQ_ERR_CAPACITY"]
     assert L.tq_decode_attention_noalloc(ctypes.byref(s), 0x10000, 8, 16, 1.0, 0x20004, None) == S["TQ_ERR_ALIGN"]
-    # value widths other than 3 bits are outside the specialised kernel
-    s2 = tqlib._CacheStruct(128, 8, 2, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
+    # value widths other than 2, 3 and 4 bits are outside the specialised kernel
+    s2 = tqlib._CacheStruct(128, 8, 5, 1, 1, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
     assert L.tq_decode_attention_noalloc(ctypes.byref(s2), 0x10000, 8, 16, 1.0, 0x20000, None) == S["TQ_ERR_UNSUPPORTED"]
     # a group of 16 takes two column blocks: 2016 sequence-heads already overflow
     s3 = tqlib._CacheStruct(128, 8, 3, 1, 2017, 0, 16, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 42)
