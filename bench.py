@@ -1019,8 +1019,8 @@ PROFILE_CASES = {
     "sweep_codec_d512_k4v3": ("codec", 512, 4, 3, 1, 8, 16384, 0),
     "attention_d256_k8v3_b4": ("attention", 256, 8, 3, 4, 8, 32769, 8),
     "attention_d64_k8v3_b8": ("attention", 64, 8, 3, 8, 8, 32769, 8),
-    "generic_attention_d128_k8v4_b4": ("attention", 128, 8, 4, 4, 8, 32769, 8),
-    "generic_attention_d256_k8v4_b4": ("attention", 256, 8, 4, 4, 8, 32769, 8),
+    "attention_d128_k8v4_b4": ("attention", 128, 8, 4, 4, 8, 32769, 8),
+    "generic_attention_d512_k4v3_b3": ("attention", 512, 4, 3, 3, 8, 32769, 4),
     # multi-token attention: M = 128 query rows per sequence (the tcgen05 kernel)
     "multi_token_m128_b2": ("multi128", 128, 8, 3, 2, 8, 32769, 8),
 }
