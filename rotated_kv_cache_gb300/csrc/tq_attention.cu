@@ -679,9 +679,9 @@ struct CombineParams {
     SignBits sg;  // value signs
 };
 
-// Each (sequence, q-head) row takes W warps (W = 16 or 32 for the hundred or
-// more splits of a small batch, fewer when there are few splits, so small
-// merges are not spread thin); a CTA holds max(8, W) warps.  Lane holds dims
+// Each (sequence, q-head) row takes W warps (32 above 128 splits, 16 from 64,
+// 4 from 16, else 1, so small merges are not spread thin); a CTA holds
+// max(8, W) warps.  Lane holds dims
 // 4 lane .. 4 lane + 3.  Warp w of a row merges the splits w, w + W, ...:
 // up to kFew of them with every load issued before any is used (one memory
 // round trip), more in chunks of 32 whose (max, sum) pairs are read one per
@@ -957,7 +957,7 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     const dim3 cb(kCombineWarps * 32);
     if (plan.splits > 128) return launch_dependent(attn_combine_kernel<32>, dim3(cp.rows), dim3(32 * 32), 0, s, cp);
     if (plan.splits >= 64) return launch_dependent(attn_combine_kernel<16>, dim3(cp.rows), dim3(16 * 32), 0, s, cp);
-    if (plan.splits >= 16) return launch_dependent(attn_combine_kernel<2>, dim3((cp.rows + 3) / 4), cb, 0, s, cp);
+    if (plan.splits >= 16) return launch_dependent(attn_combine_kernel<4>, dim3((cp.rows + 1) / 2), cb, 0, s, cp);
     return launch_dependent(attn_combine_kernel<1>, dim3((cp.rows + 7) / 8), cb, 0, s, cp);
 }
 
