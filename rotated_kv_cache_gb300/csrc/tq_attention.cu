@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
             // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
             const float2 a2 = make_float2(alpha[0], alpha[1]);
 #pragma unroll
-            for (int mt2 = 0; mt2 < 8; ++mt2) {
+            for (int mt2 = 0; mt2 < 2 * NG; ++mt2) {
                 const float2 x = __fmul2_rn(make_float2(o[mt2][0], o[mt2][1]), a2);
                 const float2 y = __fmul2_rn(make_float2(o[mt2][2], o[mt2][3]), a2);
                 o[mt2][0] = x.x;

@@ -73,6 +73,16 @@ def test_specialised_kernel_value_widths(cuda, d, kb, vb, G, T):
     assert err < TOL, err
 
 
+@pytest.mark.parametrize("d,kb,vb,T", [(256, 8, 3, 8200), (256, 4, 4, 8200), (64, 8, 3, 16400), (64, 4, 2, 16400)])
+def test_specialised_kernel_many_stages_per_split(cuda, d, kb, vb, T):
+    """Enough (sequence, kv-head) pairs (4 x 8) that the split plan fills the
+    GPU with few splits, so each CTA walks several 64-row stages and its
+    running max rises after the first: every output m-tile (2 head_dim / 32
+    of them) must be rescaled then, not only the first eight."""
+    err = _run(cuda, d, kb, vb, B=4, H=8, G=8, T=T, step=d + kb)
+    assert err < TOL, err
+
+
 @pytest.mark.parametrize("d,kb,vb,G,T", [(256, 4, 2, 4, 5000), (64, 8, 4, 8, 9000), (512, 5, 3, 2, 1500)])
 def test_long_contexts_split(cuda, d, kb, vb, G, T):
     """Several splits per (sequence, kv-head) and ragged stage tails."""
