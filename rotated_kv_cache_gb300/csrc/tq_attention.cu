@@ -21,10 +21,13 @@
 //    the copies that refill its slot, so no warp is set aside as a producer
 //    (8 CTAs fit on an SM at head_dim 128, 4 at 256).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
-//    tokens, N = 8 columns: 8 of the G q-heads sharing the kv-head (a group
-//    above 8 takes ceil(G/8) CTAs, neighbours in the grid so their reads of
-//    the same rows meet in L2; columns past G repeat the last head and are
-//    dropped), K = head_dim.  Key codes
+//    tokens, N = 8 columns: 8 of the G q-heads sharing the kv-head, K =
+//    head_dim.  A group above 8 has ceil(G/8) column blocks: at head_dims 64
+//    and 128 a CTA takes two of them, so the key and value codes it unpacks
+//    serve 16 columns (4 CTAs per SM at 128, for the doubled registers); at
+//    256 each block is its own CTA, neighbours in the grid so their reads of
+//    the same rows meet in L2.  Columns past G repeat the last head and are
+//    dropped.  Key codes
 //    become exact f16 integers with one XOR and byte permutes (1024 + code), so
 //    S = sum_g scale_g * (acc_g + (zero_g - offset) * sum_{j in g} q_j) -- the
 //    per-group affine is applied to the 8-head scores, not to each element.
@@ -62,7 +65,9 @@ __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / 
 // blocks of kG q-heads (MMA columns) per kv-head
 inline int col_blocks(int group) { return (group + kG - 1) / kG; }
 
-template <int KB, int D, int VB>
+// NBC: column blocks per CTA (2 at head_dims up to 128 when a kv-head has
+// more than kG q-heads: the key and value codes are unpacked once for both)
+template <int KB, int D, int VB, int NBC = 1>
 struct AGeo {
     static constexpr int NG = D / 32;                          // groups per row
     static constexpr int KROW = D * KB / 8;                    // key code bytes per token
@@ -78,13 +83,13 @@ struct AGeo {
     static constexpr int OFF_VS = OFF_KZ + SC_BYTES;
     static constexpr int OFF_V = OFF_VS + SC_BYTES;
     static constexpr int STAGE = round_up(OFF_V + V_BYTES + 16, 1024);  // 1024: swizzle atom alignment
-    static constexpr int MERGE = kCW * kG * (D + 2) * 4;              // per-warp partials (reuse the ring)
+    static constexpr int MERGE = kCW * NBC * kG * (D + 2) * 4;        // per-warp partials (reuse the ring)
     static constexpr int RING = kStages * STAGE > MERGE ? kStages * STAGE : MERGE;
     static constexpr int SMEM = 1024 /*align slack*/ + RING + kStages * 8 /*full barriers*/ + kStages * 4 /*counters*/;
     static constexpr float OFFSET = KB == 8 ? 1152.0f : 1024.0f;    // f16 value = OFFSET + code
-    // resident CTAs per SM the register budget is sized for (head_dim 256 holds
-    // twice the q fragments and output accumulators of 128)
-    static constexpr int MIN_BLOCKS = D >= 256 ? 4 : 8;
+    // resident CTAs per SM the register budget is sized for (head_dim 256, or
+    // two column blocks, hold twice the q fragments and output accumulators)
+    static constexpr int MIN_BLOCKS = D * NBC >= 256 ? 4 : 8;
 };
 
 struct AttnParams {
@@ -210,12 +215,13 @@ __device__ __forceinline__ uint32_t shr_fma(uint32_t x)
 }
 
 // ---------------------------------------------------------------- the split kernel
-template <int KB, int D, int VB>
-__global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
+template <int KB, int D, int VB, int NBC>
+__global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
     attn_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ AttnParams p)
 {
-    using A = AGeo<KB, D, VB>;
+    using A = AGeo<KB, D, VB, NBC>;
     constexpr int NG = A::NG;
+    constexpr int NH = NBC * kG;  // MMA columns of the CTA
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
@@ -227,10 +233,11 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
     pdl_wait_primary();  // whatever the previous kernel on the stream writes or reads is settled
     pdl_allow_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // blockIdx.y = (kv-head, block of kG q-heads); the blocks of one kv-head are
-    // neighbours in the grid, so their reads of the same rows meet in L2
+    // blockIdx.y = (kv-head, NBC blocks of kG q-heads); the CTAs of one kv-head
+    // are neighbours in the grid, so their reads of the same rows meet in L2
+    const int nbp = (p.NB + NBC - 1) / NBC;  // CTAs per kv-head
     const int split = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-    const int h = hv / p.NB, hb = hv - h * p.NB;
+    const int h = hv / nbp, hb0 = (hv - h * nbp) * NBC;  // the CTA's first column block
     const int64_t bh = (int64_t)b * p.H + h;
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = imin64(p.seq_len, t_begin + p.tokens_per_split);
@@ -267,13 +274,15 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
     const int g = lane >> 2, c = lane & 3;
     // Q fragments (B operand of QK^T): head n = g; per k-step two f16x2 registers.
     // The dim order inside a 32-group is permuted to match how key codes unpack.
-    uint32_t bq[2 * NG][2];
-    float qs[NG][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
-    float ie[2];     // per head: 2^-e * softmax_scale * log2(e)
-    {
-        // columns past the last q-head are padding: they repeat head G-1 (MMA
-        // columns never mix) and their partials are never read
-        const int gq = kG * hb + g;
+    uint32_t bq[NBC][2 * NG][2];
+    float qs[NBC][NG][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
+    float ie[NBC][2];      // per head: 2^-e * softmax_scale * log2(e)
+#pragma unroll
+    for (int nb = 0; nb < NBC; ++nb) {
+        // columns past the last q-head are padding (a whole block of them past the
+        // last block): they repeat head G-1 (MMA columns never mix) and their
+        // partials are never written
+        const int gq = kG * (hb0 + nb) + g;
         const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (gq < p.G ? gq : p.G - 1)) * D;
         float qv[NG][8];
         float mx = 0.0f;
@@ -315,17 +324,17 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
             if constexpr (KB == 8) {
                 // a word holds dims 8c+{0..3} (then {4..7}); its bytes pair as (0, 2), (1, 3)
                 auto pr = [&](int i, int j) { return pack_f16x2(f[i], f[j]); };
-                bq[2 * G][0] = pr(0, 2);
-                bq[2 * G][1] = pr(1, 3);
-                bq[2 * G + 1][0] = pr(4, 6);
-                bq[2 * G + 1][1] = pr(5, 7);
+                bq[nb][2 * G][0] = pr(0, 2);
+                bq[nb][2 * G][1] = pr(1, 3);
+                bq[nb][2 * G + 1][0] = pr(4, 6);
+                bq[nb][2 * G + 1][1] = pr(5, 7);
             } else {
                 // nibble k of the word = dim 8c+k; unpacked pairs are (k, k+4)
                 auto pr = [&](int i, int j) { return pack_f16x2(f[i], f[j]); };
-                bq[2 * G][0] = pr(0, 4);
-                bq[2 * G][1] = pr(1, 5);
-                bq[2 * G + 1][0] = pr(2, 6);
-                bq[2 * G + 1][1] = pr(3, 7);
+                bq[nb][2 * G][0] = pr(0, 4);
+                bq[nb][2 * G][1] = pr(1, 5);
+                bq[nb][2 * G + 1][0] = pr(2, 6);
+                bq[nb][2 * G + 1][1] = pr(3, 7);
             }
         }
         // group sums per head: head g lives in lanes 4g..4g+3; gather heads 2c, 2c+1
@@ -334,20 +343,25 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
             float s = qsum[G];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            qs[G][0] = __shfl_sync(0xffffffffu, s, (2 * c) * 4);
-            qs[G][1] = __shfl_sync(0xffffffffu, s, (2 * c + 1) * 4);
+            qs[nb][G][0] = __shfl_sync(0xffffffffu, s, (2 * c) * 4);
+            qs[nb][G][1] = __shfl_sync(0xffffffffu, s, (2 * c + 1) * 4);
         }
         const float my_ie = ldexpf(1.0f, -e) * p.scale_log2;
-        ie[0] = __shfl_sync(0xffffffffu, my_ie, (2 * c) * 4);
-        ie[1] = __shfl_sync(0xffffffffu, my_ie, (2 * c + 1) * 4);
+        ie[nb][0] = __shfl_sync(0xffffffffu, my_ie, (2 * c) * 4);
+        ie[nb][1] = __shfl_sync(0xffffffffu, my_ie, (2 * c + 1) * 4);
     }
 
-    float o[2 * NG][4];
+    float o[NBC][2 * NG][4];
+    float m_run[NBC][2], l_run[NBC][2];
 #pragma unroll
-    for (int i = 0; i < 2 * NG; ++i)
+    for (int nb = 0; nb < NBC; ++nb) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+        for (int i = 0; i < 2 * NG; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[nb][i][j] = 0.0f;
+        m_run[nb][0] = m_run[nb][1] = -INFINITY;
+        l_run[nb][0] = l_run[nb][1] = 0.0f;
+    }
 
     // V field extraction: lane g owns dims 32G + 4g + {0..3}: 4 VB bits at bit
     // (32G + 4g) VB of the row (word 32G VB / 32 + v_word, shift v_shift)
@@ -388,36 +402,45 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
         // two 16-row tiles per warp and stage (rows 16 warp and 16 kCW + 16 warp): Q K^T for
         // both, one softmax step over both, P V for both; the tile loops are unrolled so
         // the compiler interleaves the tiles' independent chains
-        float S[kTiles][2][2];  // scores: [tile][row g, row g + 8][head 2c, 2c + 1]
+        float S[NBC][kTiles][2][2];  // scores: [block][tile][row g, row g + 8][head 2c, 2c + 1]
 #pragma unroll
         for (int t2 = 0; t2 < kTiles; ++t2) {
             const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
 
-            // ---------------- S = Q K^T for 16 tokens x 8 heads, per key group
-            float acc[NG][4];
+            // ---------------- S = Q K^T for 16 tokens x 8 heads per block, per key group
+            float acc[NBC][NG][4];
 #pragma unroll
-            for (int G = 0; G < NG; ++G)
+            for (int nb = 0; nb < NBC; ++nb)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[G][j] = 0.0f;
+                for (int G = 0; G < NG; ++G)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[nb][G][j] = 0.0f;
 #pragma unroll
             for (int G = 0; G < NG; ++G) {
+                uint32_t ka[2][4];  // A fragments of the group's two k-steps, shared by the blocks
                 if constexpr (KB == 8) {
                     const uint2 k0 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::SW));
                     const uint2 k1 = lds64(st + koff[G] + t2 * ((16 * kCW) * A::SW) + 8 * A::SW);
                     // bytes 0 and 2 (then 1 and 3) of a word -> f16 (1024 + (byte ^ 0x80)):
                     // dims (8c+0, 8c+2), (8c+1, 8c+3), then +4
-                    mma16816(acc[G], kcvt(k0.x, p), kcvt(k1.x, p), kcvt(shr_fma<8>(k0.x), p), kcvt(shr_fma<8>(k1.x), p),
-                             bq[2 * G][0], bq[2 * G][1]);
-                    mma16816(acc[G], kcvt(k0.y, p), kcvt(k1.y, p), kcvt(shr_fma<8>(k0.y), p), kcvt(shr_fma<8>(k1.y), p),
-                             bq[2 * G + 1][0], bq[2 * G + 1][1]);
+                    ka[0][0] = kcvt(k0.x, p); ka[0][1] = kcvt(k1.x, p);
+                    ka[0][2] = kcvt(shr_fma<8>(k0.x), p); ka[0][3] = kcvt(shr_fma<8>(k1.x), p);
+                    ka[1][0] = kcvt(k0.y, p); ka[1][1] = kcvt(k1.y, p);
+                    ka[1][2] = kcvt(shr_fma<8>(k0.y), p); ka[1][3] = kcvt(shr_fma<8>(k1.y), p);
                 } else {
                     const uint32_t w0 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::SW));
                     const uint32_t w1 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::SW) + 8 * A::SW);
                     // nibbles k and k+4 -> f16 (1024 + nibble)
-                    mma16816(acc[G], kcvt(w0, p), kcvt(w1, p), kcvt(shr_fma<4>(w0), p), kcvt(shr_fma<4>(w1), p), bq[2 * G][0],
-                             bq[2 * G][1]);
-                    mma16816(acc[G], kcvt(shr_fma<8>(w0), p), kcvt(shr_fma<8>(w1), p), kcvt(shr_fma<12>(w0), p),
-                             kcvt(shr_fma<12>(w1), p), bq[2 * G + 1][0], bq[2 * G + 1][1]);
+                    ka[0][0] = kcvt(w0, p); ka[0][1] = kcvt(w1, p);
+                    ka[0][2] = kcvt(shr_fma<4>(w0), p); ka[0][3] = kcvt(shr_fma<4>(w1), p);
+                    ka[1][0] = kcvt(shr_fma<8>(w0), p); ka[1][1] = kcvt(shr_fma<8>(w1), p);
+                    ka[1][2] = kcvt(shr_fma<12>(w0), p); ka[1][3] = kcvt(shr_fma<12>(w1), p);
+                }
+#pragma unroll
+                for (int nb = 0; nb < NBC; ++nb) {
+                    mma16816(acc[nb][G], ka[0][0], ka[0][1], ka[0][2], ka[0][3], bq[nb][2 * G][0], bq[nb][2 * G][1]);
+                    mma16816(acc[nb][G], ka[1][0], ka[1][1], ka[1][2], ka[1][3], bq[nb][2 * G + 1][0],
+                             bq[nb][2 * G + 1][1]);
                 }
             }
             // per-group affine applied to the scores: S = sum_g scale (acc + (zero - off) qsum),
@@ -432,23 +455,34 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
                 lds_words(st + A::OFF_KZ + m1, zw[1]);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    float2 sacc = make_float2(0.0f, 0.0f);
+                    float2 sacc[NBC];
+#pragma unroll
+                    for (int nb = 0; nb < NBC; ++nb) sacc[nb] = make_float2(0.0f, 0.0f);
 #pragma unroll
                     for (int G = 0; G < NG; ++G) {
                         const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
                         const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
                         const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
-                        const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[G][0], qs[G][1]),
-                                                    make_float2(acc[G][2 * i], acc[G][2 * i + 1]));
-                        sacc = __ffma2_rn(make_float2(sc, sc), t, sacc);
+#pragma unroll
+                        for (int nb = 0; nb < NBC; ++nb) {
+                            const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[nb][G][0], qs[nb][G][1]),
+                                                        make_float2(acc[nb][G][2 * i], acc[nb][G][2 * i + 1]));
+                            sacc[nb] = __ffma2_rn(make_float2(sc, sc), t, sacc[nb]);
+                        }
                     }
-                    const float2 sv = __fmul2_rn(sacc, make_float2(ie[0], ie[1]));
-                    S[t2][i][0] = sv.x;
-                    S[t2][i][1] = sv.y;
+#pragma unroll
+                    for (int nb = 0; nb < NBC; ++nb) {
+                        const float2 sv = __fmul2_rn(sacc[nb], make_float2(ie[nb][0], ie[nb][1]));
+                        S[nb][t2][i][0] = sv.x;
+                        S[nb][t2][i][1] = sv.y;
+                    }
                 }
                 if (tile_r + 16 > split_rows) {  // ragged tail: mask rows past the range
-                    if (tile_r + g >= split_rows) S[t2][0][0] = S[t2][0][1] = -INFINITY;
-                    if (tile_r + g + 8 >= split_rows) S[t2][1][0] = S[t2][1][1] = -INFINITY;
+#pragma unroll
+                    for (int nb = 0; nb < NBC; ++nb) {
+                        if (tile_r + g >= split_rows) S[nb][t2][0][0] = S[nb][t2][0][1] = -INFINITY;
+                        if (tile_r + g + 8 >= split_rows) S[nb][t2][1][0] = S[nb][t2][1][1] = -INFINITY;
+                    }
                 }
             }
         }
@@ -456,65 +490,73 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
         // The running max is reduced across the rows only when some lane sees a
         // score above it (or no max exists yet); otherwise the weights are
         // 2^(S - m) with the max unchanged, which is the same arithmetic.
-        float pr[kTiles][2][2];
-        bool raise = m_run[0] == -INFINITY || m_run[1] == -INFINITY;
+        float pr[NBC][kTiles][2][2];
 #pragma unroll
-        for (int t2 = 0; t2 < kTiles; ++t2)
+        for (int nb = 0; nb < NBC; ++nb) {
+            bool raise = m_run[nb][0] == -INFINITY || m_run[nb][1] == -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) raise = raise || S[t2][i][0] > m_run[0] || S[t2][i][1] > m_run[1];
-        if (__any_sync(0xffffffffu, raise)) {
-            float alpha[2];
+            for (int t2 = 0; t2 < kTiles; ++t2)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mt = fmaxf(S[0][0][j], S[0][1][j]);
+                for (int i = 0; i < 2; ++i)
+                    raise = raise || S[nb][t2][i][0] > m_run[nb][0] || S[nb][t2][i][1] > m_run[nb][1];
+            if (__any_sync(0xffffffffu, raise)) {
+                float alpha[2];
 #pragma unroll
-                for (int t2 = 1; t2 < kTiles; ++t2) mt = fmaxf(mt, fmaxf(S[t2][0][j], S[t2][1][j]));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-                const float mn = fmaxf(m_run[j], mt);
-                const float mu = mn == -INFINITY ? 0.0f : mn;
-                alpha[j] = ex2(m_run[j] - mu);
-                m_run[j] = mn;
-                float ls = 0.0f;
+                for (int j = 0; j < 2; ++j) {
+                    float mt = fmaxf(S[nb][0][0][j], S[nb][0][1][j]);
 #pragma unroll
-                for (int t2 = 0; t2 < kTiles; ++t2) {
-                    pr[t2][0][j] = ex2(S[t2][0][j] - mu);
-                    pr[t2][1][j] = ex2(S[t2][1][j] - mu);
-                    ls += pr[t2][0][j] + pr[t2][1][j];
+                    for (int t2 = 1; t2 < kTiles; ++t2) mt = fmaxf(mt, fmaxf(S[nb][t2][0][j], S[nb][t2][1][j]));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                    const float mn = fmaxf(m_run[nb][j], mt);
+                    const float mu = mn == -INFINITY ? 0.0f : mn;
+                    alpha[j] = ex2(m_run[nb][j] - mu);
+                    m_run[nb][j] = mn;
+                    float ls = 0.0f;
+#pragma unroll
+                    for (int t2 = 0; t2 < kTiles; ++t2) {
+                        pr[nb][t2][0][j] = ex2(S[nb][t2][0][j] - mu);
+                        pr[nb][t2][1][j] = ex2(S[nb][t2][1][j] - mu);
+                        ls += pr[nb][t2][0][j] + pr[nb][t2][1][j];
+                    }
+                    l_run[nb][j] = l_run[nb][j] * alpha[j] + ls;
                 }
-                l_run[j] = l_run[j] * alpha[j] + ls;
-            }
-            // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
-            const float2 a2 = make_float2(alpha[0], alpha[1]);
+                // o[mt][0, 1] and o[mt][2, 3] are (head 2c, head 2c+1) pairs
+                const float2 a2 = make_float2(alpha[0], alpha[1]);
 #pragma unroll
-            for (int mt2 = 0; mt2 < 2 * NG; ++mt2) {
-                const float2 x = __fmul2_rn(make_float2(o[mt2][0], o[mt2][1]), a2);
-                const float2 y = __fmul2_rn(make_float2(o[mt2][2], o[mt2][3]), a2);
-                o[mt2][0] = x.x;
-                o[mt2][1] = x.y;
-                o[mt2][2] = y.x;
-                o[mt2][3] = y.y;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float ls = 0.0f;
-#pragma unroll
-                for (int t2 = 0; t2 < kTiles; ++t2) {
-                    pr[t2][0][j] = ex2(S[t2][0][j] - m_run[j]);
-                    pr[t2][1][j] = ex2(S[t2][1][j] - m_run[j]);
-                    ls += pr[t2][0][j] + pr[t2][1][j];
+                for (int mt2 = 0; mt2 < 2 * NG; ++mt2) {
+                    const float2 x = __fmul2_rn(make_float2(o[nb][mt2][0], o[nb][mt2][1]), a2);
+                    const float2 y = __fmul2_rn(make_float2(o[nb][mt2][2], o[nb][mt2][3]), a2);
+                    o[nb][mt2][0] = x.x;
+                    o[nb][mt2][1] = x.y;
+                    o[nb][mt2][2] = y.x;
+                    o[nb][mt2][3] = y.y;
                 }
-                l_run[j] += ls;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float ls = 0.0f;
+#pragma unroll
+                    for (int t2 = 0; t2 < kTiles; ++t2) {
+                        pr[nb][t2][0][j] = ex2(S[nb][t2][0][j] - m_run[nb][j]);
+                        pr[nb][t2][1][j] = ex2(S[nb][t2][1][j] - m_run[nb][j]);
+                        ls += pr[nb][t2][0][j] + pr[nb][t2][1][j];
+                    }
+                    l_run[nb][j] += ls;
+                }
             }
         }
 #pragma unroll
         for (int t2 = 0; t2 < kTiles; ++t2) {
             const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
             // ---------------- P^T as the B operand (tokens x heads), transposed in registers
-            const uint32_t pt0 = movmatrix_trans(pack_f16x2(pr[t2][0][0], pr[t2][0][1]));  // tokens 2c, 2c+1; head g
-            const uint32_t pt1 = movmatrix_trans(pack_f16x2(pr[t2][1][0], pr[t2][1][1]));  // tokens 2c+8, 2c+9
+            uint32_t pt0[NBC], pt1[NBC];
+#pragma unroll
+            for (int nb = 0; nb < NBC; ++nb) {
+                pt0[nb] = movmatrix_trans(pack_f16x2(pr[nb][t2][0][0], pr[nb][t2][0][1]));  // tokens 2c, 2c+1; head g
+                pt1[nb] = movmatrix_trans(pack_f16x2(pr[nb][t2][1][0], pr[nb][t2][1][1]));  // tokens 2c+8, 2c+9
+            }
             // value scales of this lane's four tokens, NG / 2 words each (zero past the range)
             uint32_t vs[4][NG / 2];
 #pragma unroll
@@ -532,7 +574,12 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
                 const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
                 const uint32_t sp0 = __byte_perm(vs[0][G >> 1], vs[1][G >> 1], sel);
                 const uint32_t sp1 = __byte_perm(vs[2][G >> 1], vs[3][G >> 1], sel);
-                const uint32_t b0 = hmul2(pt0, sp0), b1 = hmul2(pt1, sp1);
+                uint32_t b0[NBC], b1[NBC];
+#pragma unroll
+                for (int nb = 0; nb < NBC; ++nb) {
+                    b0[nb] = hmul2(pt0[nb], sp0);
+                    b1[nb] = hmul2(pt1[nb], sp1);
+                }
                 uint32_t av[2][2][2];  // [token pair][m-tile half][row g, row g+8]
                 // the 4 VB-bit field (codes of dims 32G + 4g + 0..3 at bits 0, VB, 2 VB,
                 // 3 VB) of the lane's four tokens; bits above 4 VB are don't-care
@@ -597,7 +644,10 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
                 }
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
-                    mma16816(o[2 * G + half], av[0][half][0], av[0][half][1], av[1][half][0], av[1][half][1], b0, b1);
+#pragma unroll
+                    for (int nb = 0; nb < NBC; ++nb)
+                        mma16816(o[nb][2 * G + half], av[0][half][0], av[0][half][1], av[1][half][0], av[1][half][1],
+                                 b0[nb], b1[nb]);
             }
         }
         // the last warp to finish this stage refills its slot with stage s + kStages
@@ -619,47 +669,54 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB>::MIN_BLOCKS)
     // ---------------------------------------------------------------- merge the warps
     // per-lane partial row sums -> per-head sums (lanes with equal c)
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
-    }
-    float *mw = merge + warp * kG * (D + 2);  // [head][D] o, then [head] m, [head] l
-#pragma unroll
-    for (int mt = 0; mt < 2 * NG; ++mt) {
-        const int G = mt >> 1, half = mt & 1;
-        const int d0 = 32 * G + 4 * g + 2 * half;  // row g -> d0, row g+8 -> d0 + 1
+    for (int nb = 0; nb < NBC; ++nb)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            mw[(2 * c + j) * D + d0] = o[mt][j];
-            mw[(2 * c + j) * D + d0 + 1] = o[mt][2 + j];
+            l_run[nb][j] += __shfl_xor_sync(0xffffffffu, l_run[nb][j], 4);
+            l_run[nb][j] += __shfl_xor_sync(0xffffffffu, l_run[nb][j], 8);
+            l_run[nb][j] += __shfl_xor_sync(0xffffffffu, l_run[nb][j], 16);
         }
-    }
-    if (g == 0) {
+    float *mw = merge + warp * NH * (D + 2);  // [column][D] o, then [column] m, [column] l
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            mw[kG * D + 2 * c + j] = ok ? m_run[j] : -INFINITY;
-            mw[kG * D + kG + 2 * c + j] = ok ? l_run[j] : 0.0f;
+    for (int nb = 0; nb < NBC; ++nb) {
+#pragma unroll
+        for (int mt = 0; mt < 2 * NG; ++mt) {
+            const int G = mt >> 1, half = mt & 1;
+            const int d0 = 32 * G + 4 * g + 2 * half;  // row g -> d0, row g+8 -> d0 + 1
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                mw[(kG * nb + 2 * c + j) * D + d0] = o[nb][mt][j];
+                mw[(kG * nb + 2 * c + j) * D + d0 + 1] = o[nb][mt][2 + j];
+            }
+        }
+        if (g == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                mw[NH * D + kG * nb + 2 * c + j] = ok ? m_run[nb][j] : -INFINITY;
+                mw[NH * D + NH + kG * nb + 2 * c + j] = ok ? l_run[nb][j] : 0.0f;
+            }
         }
     }
     __syncthreads();
-    // items (head, 8 dims), kG x D / 8 of them, over the CTA's threads
-    for (int item = threadIdx.x; item < kG * (D / 8); item += kThreads) {
+    // items (column, 8 dims), NH x D / 8 of them, over the CTA's threads
+    for (int item = threadIdx.x; item < NH * (D / 8); item += kThreads) {
         const int hh = item / (D / 8), d8 = (item % (D / 8)) * 8;
+        const int hb = hb0 + hh / kG;
+        if (hb >= p.NB) break;  // a padding block (columns are in block order)
         float mmax = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) mmax = fmaxf(mmax, merge[w * kG * (D + 2) + kG * D + hh]);
+        for (int w = 0; w < kCW; ++w) mmax = fmaxf(mmax, merge[w * NH * (D + 2) + NH * D + hh]);
         const float mu = mmax == -INFINITY ? 0.0f : mmax;
         float ov[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lsum = 0.0f;
 #pragma unroll
         for (int w = 0; w < kCW; ++w) {
-            const float *m2 = merge + w * kG * (D + 2);
-            const float wt = ex2(m2[kG * D + hh] - mu);
-            lsum += m2[kG * D + kG + hh] * wt;
+            const float *m2 = merge + w * NH * (D + 2);
+            const float wt = ex2(m2[NH * D + hh] - mu);
+            lsum += m2[NH * D + NH + hh] * wt;
 #pragma unroll
             for (int i = 0; i < 8; ++i) ov[i] += m2[hh * D + d8 + i] * wt;
         }
-        const int64_t pidx = (((int64_t)b * p.H * p.NB + hv) * p.splits + split) * kG + hh;
+        const int64_t pidx = ((((int64_t)b * p.H + h) * p.NB + hb) * p.splits + split) * kG + hh % kG;
         float4 *dst = reinterpret_cast<float4 *>(p.part_o + pidx * D + d8);
         dst[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
         dst[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
@@ -848,16 +905,16 @@ SplitPlan plan_splits(int B, int H, int64_t seq_len, int ctas_per_sm)
     return best;
 }
 
-template <int KB, int D, int VB>
+template <int KB, int D, int VB, int NBC>
 int ctas_per_sm_for()
 {
     static int cached = 0;  // same on every GB300; only a successful query is kept
     if (!cached) {
         int n = 0;
-        if (cudaFuncSetAttribute(attn_split_kernel<KB, D, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 AGeo<KB, D, VB>::SMEM) == cudaSuccess &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<KB, D, VB>, kThreads,
-                                                          AGeo<KB, D, VB>::SMEM) == cudaSuccess &&
+        if (cudaFuncSetAttribute(attn_split_kernel<KB, D, VB, NBC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AGeo<KB, D, VB, NBC>::SMEM) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<KB, D, VB, NBC>, kThreads,
+                                                          AGeo<KB, D, VB, NBC>::SMEM) == cudaSuccess &&
             n > 0)
             cached = n;
         else
@@ -868,13 +925,13 @@ int ctas_per_sm_for()
 
 // Launch the split kernel and the combine with a given split plan, the
 // partials in `buf` (at least the plan's bytes; see plan_bytes).
-template <int KB, int D, int VB>
+template <int KB, int D, int VB, int NBC>
 cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
                                void *buf, const SplitPlan &plan, cudaStream_t s)
 {
-    using A = AGeo<KB, D, VB>;
+    using A = AGeo<KB, D, VB, NBC>;
     cudaError_t e =
-        cudaFuncSetAttribute(attn_split_kernel<KB, D, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+        cudaFuncSetAttribute(attn_split_kernel<KB, D, VB, NBC>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
     if (e != cudaSuccess) return e;
     const size_t need_o = (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * D * 4;
 
@@ -933,8 +990,8 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     p.k_const = KB == 8 ? 0xFF00FF00u : 0xFFF0FFF0u;
     p.k_flip = KB == 8 ? 0x64806480u : 0x64006400u;
 
-    dim3 grid(plan.splits, c.H * p.NB, c.B);
-    e = launch_dependent(attn_split_kernel<KB, D, VB>, grid, dim3(kThreads), A::SMEM, s, map, p);
+    dim3 grid(plan.splits, c.H * ((p.NB + NBC - 1) / NBC), c.B);
+    e = launch_dependent(attn_split_kernel<KB, D, VB, NBC>, grid, dim3(kThreads), A::SMEM, s, map, p);
     if (e != cudaSuccess) return e;
     if constexpr (D != kCombD)  // the generic kernel's merge: the same partial layout (one query row)
         return launch_attention_combine_parts(D, p.part_o, p.part_ml, out, c.B, c.H, QH, 1, p.NB, kG, plan.splits,
@@ -968,34 +1025,53 @@ size_t plan_bytes(const CacheView &c, int QH, const SplitPlan &plan)
     return (size_t)c.B * c.H * col_blocks(QH / c.H) * plan.splits * kG * (c.d + 2) * 4;
 }
 
-template <int D, int VB>
-int ctas_per_sm_dv(const CacheView &c)
+// Column blocks per CTA: two where a kv-head has more than one block and the
+// head_dim is at most 128 (at 256 the doubled registers would not fit), else one.
+int blocks_per_cta(const CacheView &c, int QH) { return c.d <= 128 && col_blocks(QH / c.H) >= 2 ? 2 : 1; }
+
+template <int D, int VB, int NBC>
+int ctas_per_sm_dvn(const CacheView &c)
 {
-    return c.kb == 8 ? ctas_per_sm_for<8, D, VB>() : ctas_per_sm_for<4, D, VB>();
+    return c.kb == 8 ? ctas_per_sm_for<8, D, VB, NBC>() : ctas_per_sm_for<4, D, VB, NBC>();
+}
+
+template <int D, int VB>
+int ctas_per_sm_dv(const CacheView &c, int nbc)
+{
+    if constexpr (D <= 128)
+        if (nbc == 2) return ctas_per_sm_dvn<D, VB, 2>(c);
+    return ctas_per_sm_dvn<D, VB, 1>(c);
 }
 
 template <int D>
-int ctas_per_sm_d(const CacheView &c)
+int ctas_per_sm_d(const CacheView &c, int nbc)
 {
-    return c.vb == 2 ? ctas_per_sm_dv<D, 2>(c) : c.vb == 4 ? ctas_per_sm_dv<D, 4>(c) : ctas_per_sm_dv<D, 3>(c);
+    return c.vb == 2 ? ctas_per_sm_dv<D, 2>(c, nbc) : c.vb == 4 ? ctas_per_sm_dv<D, 4>(c, nbc) : ctas_per_sm_dv<D, 3>(c, nbc);
 }
 
-int ctas_per_sm(const CacheView &c)
+int ctas_per_sm(const CacheView &c, int nbc)
 {
-    return c.d == 64 ? ctas_per_sm_d<64>(c) : c.d == 256 ? ctas_per_sm_d<256>(c) : ctas_per_sm_d<128>(c);
+    return c.d == 64 ? ctas_per_sm_d<64>(c, nbc) : c.d == 256 ? ctas_per_sm_d<256>(c, nbc) : ctas_per_sm_d<128>(c, nbc);
 }
 
 SplitPlan usual_plan(const CacheView &c, int QH, int64_t seq_len)
 {
-    return plan_splits(c.B, c.H * col_blocks(QH / c.H), seq_len, ctas_per_sm(c));
+    const int nbc = blocks_per_cta(c, QH);
+    return plan_splits(c.B, c.H * ((col_blocks(QH / c.H) + nbc - 1) / nbc), seq_len, ctas_per_sm(c, nbc));
 }
 
 template <int D, int VB>
 cudaError_t run_attention_dv(const CacheView &c, const uint16_t *q, int QH, int64_t seq_len, float scale, float *out,
                              void *buf, const SplitPlan &plan, cudaStream_t s)
 {
-    if (c.kb == 8) return run_attention_plan<8, D, VB>(c, q, QH, seq_len, scale, out, buf, plan, s);
-    return run_attention_plan<4, D, VB>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    if constexpr (D <= 128) {
+        if (blocks_per_cta(c, QH) == 2) {
+            if (c.kb == 8) return run_attention_plan<8, D, VB, 2>(c, q, QH, seq_len, scale, out, buf, plan, s);
+            return run_attention_plan<4, D, VB, 2>(c, q, QH, seq_len, scale, out, buf, plan, s);
+        }
+    }
+    if (c.kb == 8) return run_attention_plan<8, D, VB, 1>(c, q, QH, seq_len, scale, out, buf, plan, s);
+    return run_attention_plan<4, D, VB, 1>(c, q, QH, seq_len, scale, out, buf, plan, s);
 }
 
 template <int D>

@@ -47,7 +47,8 @@ def test_group_sizes(cuda, G):
 def test_specialised_kernel_group_sizes(cuda, kb, G, T):
     """Groups other than 8 on the specialised kernel (blocks of the MMA's 8
     columns, those past G dropped): several splits, ragged stage tails, ragged
-    combine blocks, one to three column blocks per kv-head."""
+    combine blocks, one to three column blocks per kv-head (two per CTA above
+    8, the last CTA of G = 24 holding one real block and one of padding)."""
     err = _run(cuda, 128, kb, 3, B=3, H=3, G=G, T=T, cap=T + (16 - T % 16) % 16 + 16, step=G)
     assert err < TOL, err
 
@@ -73,13 +74,15 @@ def test_specialised_kernel_value_widths(cuda, d, kb, vb, G, T):
     assert err < TOL, err
 
 
-@pytest.mark.parametrize("d,kb,vb,T", [(256, 8, 3, 8200), (256, 4, 4, 8200), (64, 8, 3, 16400), (64, 4, 2, 16400)])
-def test_specialised_kernel_many_stages_per_split(cuda, d, kb, vb, T):
+@pytest.mark.parametrize("d,kb,vb,G,T", [(256, 8, 3, 8, 8200), (256, 4, 4, 8, 8200), (64, 8, 3, 8, 16400),
+                                         (64, 4, 2, 8, 16400), (128, 4, 3, 16, 8200), (64, 8, 3, 12, 16400)])
+def test_specialised_kernel_many_stages_per_split(cuda, d, kb, vb, G, T):
     """Enough (sequence, kv-head) pairs (4 x 8) that the split plan fills the
     GPU with few splits, so each CTA walks several 64-row stages and its
     running max rises after the first: every output m-tile (2 head_dim / 32
-    of them) must be rescaled then, not only the first eight."""
-    err = _run(cuda, d, kb, vb, B=4, H=8, G=8, T=T, step=d + kb)
+    of them, per column block) must be rescaled then, not only the first
+    eight; two column blocks per CTA at G = 12 and 16."""
+    err = _run(cuda, d, kb, vb, B=4, H=8, G=G, T=T, step=d + kb + G)
     assert err < TOL, err
 
 

@@ -100,6 +100,24 @@ def test_noalloc_group_of_four(cuda):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("d,G", [(128, 16), (64, 12)])
+def test_noalloc_two_column_blocks(cuda, d, G):
+    """More than 8 q-heads per kv-head at head_dims 64 and 128: each CTA of the
+    specialised kernel takes two blocks of 8 columns (at G = 12 the second is
+    half padding), against tq_decode_attention and the oracle."""
+    w = tq_synth.WORKLOADS["decode"]
+    B, H, T = 2, 2, 1234
+    k, v = tq_synth.host_kv(w, B=B, H=H, d=d, n=T)
+    cache = cuda.Cache(B, H, d, T + 14, k_bits=8, v_bits=w.vb)
+    cuda.tq_encode_append(cache, to_device_bf16(k), to_device_bf16(v), 0)
+    qs = [to_device_bf16(tq_synth.host_q(w, step, B=B, QH=G * H, d=d)) for step in (0, 1)]
+    got = _two_calls_match(cuda, cache, qs, T)
+    want = _oracle_pair(cache, qs[1], T, 1, 1, G)
+    err = np.abs(got[1][1, G:2 * G].cpu().numpy().astype(np.float64) - want).max()
+    assert err < TOL, err
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("kb", [8, 4])
 def test_noalloc_fewer_splits_than_usual(cuda, kb):
     """8 kv-heads x 8193 rows and the smallest batch (64 to 512 sequences) whose
