@@ -28,9 +28,12 @@
 //    256 each block is its own CTA, neighbours in the grid so their reads of
 //    the same rows meet in L2.  Columns past G repeat the last head and are
 //    dropped.  Key codes
-//    become exact f16 integers with one XOR and byte permutes (1024 + code), so
-//    S = sum_g scale_g * (acc_g + (zero_g - offset) * sum_{j in g} q_j) -- the
-//    per-group affine is applied to the 8-head scores, not to each element.
+//    become exact f16 integers with one logic op each: offset + code (a
+//    shift first for the upper bytes; 4-bit codes in odd nibbles are read in
+//    place as 1024 + 16 code, their q taken / 16), so
+//    S = sum_g scale_g * (acc_g + zero_g * sum_{j in g} q_j - offsets' share)
+//    -- the per-group affine is applied to the 8-head scores, not to each
+//    element.
 //  * PV in the rotated domain (mma.sync, M = 16 dims, N = 8 heads, K = 16
 //    tokens): value codes are mapped to f16 centroids by byte-permute table
 //    lookups in registers (3 bits: four codes spread to nibbles per lookup;
@@ -86,7 +89,7 @@ struct AGeo {
     static constexpr int MERGE = kCW * NBC * kG * (D + 2) * 4;        // per-warp partials (reuse the ring)
     static constexpr int RING = kStages * STAGE > MERGE ? kStages * STAGE : MERGE;
     static constexpr int SMEM = 1024 /*align slack*/ + RING + kStages * 8 /*full barriers*/ + kStages * 4 /*counters*/;
-    static constexpr float OFFSET = KB == 8 ? 1152.0f : 1024.0f;    // f16 value = OFFSET + code
+    static constexpr float OFFSET = 1152.0f;  // 8-bit keys: f16 value = OFFSET + signed code
     // resident CTAs per SM the register budget is sized for (head_dim 256, or
     // two column blocks, hold twice the q fragments and output accumulators)
     static constexpr int MIN_BLOCKS = D * NBC >= 256 ? 4 : 8;
@@ -276,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
     // The dim order inside a 32-group is permuted to match how key codes unpack.
     uint32_t bq[NBC][2 * NG][2];
     float qs[NBC][NG][2];  // sum over group of the f16 (scaled) q, heads 2c and 2c+1
+    float qo[NBC][KB == 4 ? NG : 1][2];  // 4-bit keys: the code offsets' share of the QK^T dot
     float ie[NBC][2];      // per head: 2^-e * softmax_scale * log2(e)
 #pragma unroll
     for (int nb = 0; nb < NBC; ++nb) {
@@ -285,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
         const int gq = kG * (hb0 + nb) + g;
         const uint16_t *qrow = p.q + ((int64_t)b * p.QH + (int64_t)h * p.G + (gq < p.G ? gq : p.G - 1)) * D;
         float qv[NG][8];
+        float qoff[NG];
         float mx = 0.0f;
 #pragma unroll
         for (int G = 0; G < NG; ++G) {
@@ -329,12 +334,19 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
                 bq[nb][2 * G + 1][0] = pr(4, 6);
                 bq[nb][2 * G + 1][1] = pr(5, 7);
             } else {
-                // nibble k of the word = dim 8c+k; unpacked pairs are (k, k+4)
+                // nibble k of the word = dim 8c+k; unpacked pairs are (k, k+4).  Odd
+                // nibbles are read in place (1024 + 16 code), so their q is taken / 16
                 auto pr = [&](int i, int j) { return pack_f16x2(f[i], f[j]); };
+                auto pr16 = [&](int i, int j) { return pack_f16x2(f[i] * 0.0625f, f[j] * 0.0625f); };
                 bq[nb][2 * G][0] = pr(0, 4);
-                bq[nb][2 * G][1] = pr(1, 5);
+                bq[nb][2 * G][1] = pr16(1, 5);
                 bq[nb][2 * G + 1][0] = pr(2, 6);
-                bq[nb][2 * G + 1][1] = pr(3, 7);
+                bq[nb][2 * G + 1][1] = pr16(3, 7);
+                // the 1024 of every key element times the q it meets in the MMA
+                const __half2 h1 = *reinterpret_cast<const __half2 *>(&bq[nb][2 * G][1]);
+                const __half2 h3 = *reinterpret_cast<const __half2 *>(&bq[nb][2 * G + 1][1]);
+                const float so = __low2float(h1) + __high2float(h1) + __low2float(h3) + __high2float(h3);
+                qoff[G] = 1024.0f * (f[0] + f[2] + f[4] + f[6] + so);
             }
         }
         // group sums per head: head g lives in lanes 4g..4g+3; gather heads 2c, 2c+1
@@ -345,6 +357,13 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             qs[nb][G][0] = __shfl_sync(0xffffffffu, s, (2 * c) * 4);
             qs[nb][G][1] = __shfl_sync(0xffffffffu, s, (2 * c + 1) * 4);
+            if constexpr (KB == 4) {
+                float so = qoff[G];
+                so += __shfl_xor_sync(0xffffffffu, so, 1);
+                so += __shfl_xor_sync(0xffffffffu, so, 2);
+                qo[nb][G][0] = -__shfl_sync(0xffffffffu, so, (2 * c) * 4);
+                qo[nb][G][1] = -__shfl_sync(0xffffffffu, so, (2 * c + 1) * 4);
+            }
         }
         const float my_ie = ldexpf(1.0f, -e) * p.scale_log2;
         ie[nb][0] = __shfl_sync(0xffffffffu, my_ie, (2 * c) * 4);
@@ -430,11 +449,13 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
                 } else {
                     const uint32_t w0 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::SW));
                     const uint32_t w1 = lds32(st + koff[G] + t2 * ((16 * kCW) * A::SW) + 8 * A::SW);
-                    // nibbles k and k+4 -> f16 (1024 + nibble)
+                    // nibbles k and k+4 -> f16: 1024 + nibble for even k, 1024 + 16 nibble
+                    // (read in place) for odd k
+                    const uint32_t v0 = shr_fma<8>(w0), v1 = shr_fma<8>(w1);
                     ka[0][0] = kcvt(w0, p); ka[0][1] = kcvt(w1, p);
-                    ka[0][2] = kcvt(shr_fma<4>(w0), p); ka[0][3] = kcvt(shr_fma<4>(w1), p);
-                    ka[1][0] = kcvt(shr_fma<8>(w0), p); ka[1][1] = kcvt(shr_fma<8>(w1), p);
-                    ka[1][2] = kcvt(shr_fma<12>(w0), p); ka[1][3] = kcvt(shr_fma<12>(w1), p);
+                    ka[0][2] = (w0 & 0x00F000F0u) | 0x64006400u; ka[0][3] = (w1 & 0x00F000F0u) | 0x64006400u;
+                    ka[1][0] = kcvt(v0, p); ka[1][1] = kcvt(v1, p);
+                    ka[1][2] = (v0 & 0x00F000F0u) | 0x64006400u; ka[1][3] = (v1 & 0x00F000F0u) | 0x64006400u;
                 }
 #pragma unroll
                 for (int nb = 0; nb < NBC; ++nb) {
@@ -462,12 +483,23 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
                     for (int G = 0; G < NG; ++G) {
                         const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
                         const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
-                        const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
+                        if constexpr (KB == 8) {
+                            const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
 #pragma unroll
-                        for (int nb = 0; nb < NBC; ++nb) {
-                            const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[nb][G][0], qs[nb][G][1]),
-                                                        make_float2(acc[nb][G][2 * i], acc[nb][G][2 * i + 1]));
-                            sacc[nb] = __ffma2_rn(make_float2(sc, sc), t, sacc[nb]);
+                            for (int nb = 0; nb < NBC; ++nb) {
+                                const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[nb][G][0], qs[nb][G][1]),
+                                                            make_float2(acc[nb][G][2 * i], acc[nb][G][2 * i + 1]));
+                                sacc[nb] = __ffma2_rn(make_float2(sc, sc), t, sacc[nb]);
+                            }
+                        } else {
+                            const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh);
+#pragma unroll
+                            for (int nb = 0; nb < NBC; ++nb) {
+                                const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[nb][G][0], qs[nb][G][1]),
+                                                            make_float2(acc[nb][G][2 * i], acc[nb][G][2 * i + 1]));
+                                sacc[nb] = __ffma2_rn(make_float2(sc, sc), __fadd2_rn(t, make_float2(qo[nb][G][0], qo[nb][G][1])),
+                                                      sacc[nb]);
+                            }
                         }
                     }
 #pragma unroll

@@ -5,8 +5,9 @@ TMA copy wrote with a 128-byte (8-bit keys) or 64-byte (4-bit keys) swizzle:
 the 16-byte chunk index of a row is xor-ed with shared-memory address bits 7..9
 (or 7..8).  Each lane (g, c) of a warp reads its rows g and g + 8 at
 precomputed swizzled offsets, turns two codes at a time into an f16 pair
-(1024 + offset code) with one 3-input logic op and a right shift, and feeds
-them to mma.sync m16n8k16 against q fragments permuted the same way.
+(offset + code) with one 3-input logic op and a right shift, and feeds
+them to mma.sync m16n8k16 against q fragments permuted the same way.  4-bit
+codes in odd nibbles are read in place (1024 + 16 code) and meet q / 16.
 
 This test builds the swizzled tile byte by byte.  It replays every lane's
 offsets, loads, conversions and q permutation as the kernel states them, and
@@ -66,8 +67,13 @@ def lane_a_fragments(img, g, c, G, kb):
         return out
     koff = r0 * krow + ((G ^ ((g >> 1) & 3)) << 4) + 4 * c
     w0, w1 = u32(img, koff), u32(img, koff + 8 * krow)
-    return [[pair(kcvt(w0, 4)), pair(kcvt(w1, 4)), pair(kcvt(w0 >> 4, 4)), pair(kcvt(w1 >> 4, 4))],
-            [pair(kcvt(w0 >> 8, 4)), pair(kcvt(w1 >> 8, 4)), pair(kcvt(w0 >> 12, 4)), pair(kcvt(w1 >> 12, 4))]]
+    v0, v1 = w0 >> 8, w1 >> 8
+
+    def odd(w):  # nibbles 1 and 5 of the word in place: 1024 + 16 code
+        return (w & 0x00F000F0) | 0x64006400
+
+    return [[pair(kcvt(w0, 4)), pair(kcvt(w1, 4)), pair(odd(w0)), pair(odd(w1))],
+            [pair(kcvt(v0, 4)), pair(kcvt(v1, 4)), pair(odd(v0)), pair(odd(v1))]]
 
 
 def lane_b_fragments(q, n, c, G, kb):
@@ -75,28 +81,33 @@ def lane_b_fragments(q, n, c, G, kb):
     f = q[n, 32 * G + 8 * c:32 * G + 8 * c + 8]
     if kb == 8:  # a word's bytes pair as (0, 2), (1, 3)
         return [[(f[0], f[2]), (f[1], f[3])], [(f[4], f[6]), (f[5], f[7])]]
-    return [[(f[0], f[4]), (f[1], f[5])], [(f[2], f[6]), (f[3], f[7])]]  # nibbles k and k + 4
+    # nibbles k and k + 4; the odd ones meet q / 16
+    return [[(f[0], f[4]), (f[1] / 16, f[5] / 16)], [(f[2], f[6]), (f[3] / 16, f[7] / 16)]]
 
 
 @pytest.mark.parametrize("kb", [8, 4])
 def test_scores_equal_dot_products(kb):
+    """The MMAs give code . q plus the offsets' share: the offset (1152 for
+    8-bit keys, 1024 for 4-bit) times the sum of the q values the codes met,
+    which is what the kernel subtracts."""
     rng = np.random.default_rng(kb)
     krow = 128 * kb // 8
     if kb == 8:
         codes = rng.integers(-128, 128, (16, 128))
         raw = codes.astype(np.int8).view(np.uint8).reshape(16, 128)
-        offset_codes = 1152.0 + codes
+        offset = 1152.0
     else:
         codes = rng.integers(0, 16, (16, 128))
         raw = np.zeros((16, krow), dtype=np.uint8)
         for r in range(16):
             for dd in range(0, 128, 2):
                 raw[r, dd // 2] = codes[r, dd] | (codes[r, dd + 1] << 4)
-        offset_codes = 1024.0 + codes
+        offset = 1024.0
     img = swizzled_tile(raw, krow, kb)
     q = rng.integers(-8, 9, (8, 128)).astype(np.float64)
     for G in range(4):
         D = np.zeros((16, 8))
+        share = np.zeros(8)  # per head: offset x the q values of the B fragments
         for m in range(2):  # the two MMAs of the group
             for g in range(8):
                 for n in range(8):
@@ -106,8 +117,10 @@ def test_scores_equal_dot_products(kb):
                         # A[row][2c..2c+1] . B[2c..2c+1][n] + A[row][2c+8..+9] . B[2c+8..+9][n]
                         D[g, n] += a[0][0] * b[0][0] + a[0][1] * b[0][1] + a[2][0] * b[1][0] + a[2][1] * b[1][1]
                         D[g + 8, n] += a[1][0] * b[0][0] + a[1][1] * b[0][1] + a[3][0] * b[1][0] + a[3][1] * b[1][1]
-        want = offset_codes[:, 32 * G:32 * G + 32] @ q[:, 32 * G:32 * G + 32].T
-        assert np.array_equal(D, want)
+                        if g == 0:
+                            share[n] += offset * (b[0][0] + b[0][1] + b[1][0] + b[1][1])
+        want = codes[:, 32 * G:32 * G + 32] @ q[:, 32 * G:32 * G + 32].T
+        assert np.array_equal(D - share[None, :], want)
 
 
 def test_swizzle_is_a_permutation_of_each_row():
