@@ -933,7 +933,7 @@ def run_sweep(only=None):
     w = tq_synth.WORKLOADS["decode"]
     H, T = 8, 32769
     for d, kb, vb, G in [] if not want("attention") else [(128, 8, 3, 8), (128, 4, 3, 8), (128, 4, 2, 8), (128, 8, 4, 8), (128, 5, 2, 8),
-                         (128, 8, 3, 4), (128, 8, 3, 16), (64, 8, 3, 8), (256, 8, 3, 8), (64, 4, 3, 8),
+                         (128, 8, 3, 4), (128, 8, 3, 16), (64, 8, 3, 16), (64, 8, 3, 8), (256, 8, 3, 8), (64, 4, 3, 8),
                          (256, 4, 3, 8), (512, 4, 3, 4)]:
         bpt = tq.tq_bytes_per_token_head(d, kb, vb)
         B = max(1, round(4e8 / (H * T * bpt)))
@@ -1020,6 +1020,7 @@ PROFILE_CASES = {
     "attention_d256_k8v3_b4": ("attention", 256, 8, 3, 4, 8, 32769, 8),
     "attention_d64_k8v3_b8": ("attention", 64, 8, 3, 8, 8, 32769, 8),
     "attention_d128_k8v4_b4": ("attention", 128, 8, 4, 4, 8, 32769, 8),
+    "attention_group16_b2": ("attention", 128, 8, 3, 2, 8, 32769, 16),
     "generic_attention_d512_k4v3_b3": ("attention", 512, 4, 3, 3, 8, 32769, 4),
     # multi-token attention: M = 128 query rows per sequence (the tcgen05 kernel)
     "multi_token_m128_b2": ("multi128", 128, 8, 3, 2, 8, 32769, 8),
