@@ -12,14 +12,15 @@
 // 4-bit keys and 2-, 3- or 4-bit values:
 //  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
 //    a 2-stage shared-memory ring; each of its 2 warps takes two 16-token tiles
-//    of a 64-token stage and works on both at once (independent dependency
-//    chains to interleave).  A stage is 2-D TMA loads of the key codes (boxes
+//    of a 64-token stage (four of a 128-token stage at head_dim 64, whose rows
+//    are short) and works on them at once (independent dependency chains to
+//    interleave).  A stage is 2-D TMA loads of the key codes (boxes
 //    of at most 128 bytes per row -- two at head_dim 256 with 8-bit keys --
 //    with the swizzle of the box width, so the per-row fragment reads of the
 //    MMA are bank-conflict-free) and four 1-D bulk copies of the other planes,
 //    completing on the slot's mbarrier; the last warp to finish a stage issues
 //    the copies that refill its slot, so no warp is set aside as a producer
-//    (8 CTAs fit on an SM at head_dim 128, 4 at 256).
+//    (8 CTAs fit on an SM at head_dims 64 and 128, 4 at 256).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
 //    tokens, N = 8 columns: 8 of the G q-heads sharing the kv-head, K =
 //    head_dim.  A group above 8 has ceil(G/8) column blocks: at head_dims 64
@@ -59,8 +60,6 @@ namespace {
 constexpr int kG = 8;              // MMA columns: a block of 8 of a kv-head's q-heads
 constexpr int kCW = 2;             // warps per CTA (all compute; the last to finish a stage refills it)
 constexpr int kThreads = kCW * 32;
-constexpr int kTiles = 2;          // 16-token tiles per warp and stage, worked on together
-constexpr int kStageT = 16 * kTiles * kCW;  // tokens per stage
 constexpr int kStages = 2;         // ring depth (8 CTAs of 2 x 13 KB fit on an SM)
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -72,14 +71,19 @@ inline int col_blocks(int group) { return (group + kG - 1) / kG; }
 // more than kG q-heads: the key and value codes are unpacked once for both)
 template <int KB, int D, int VB, int NBC = 1>
 struct AGeo {
+    // 16-token tiles per warp and stage, worked on together (four at head_dim 64
+    // with one column block: its rows are short, so the per-stage work is spread
+    // over more of them), and tokens per stage
+    static constexpr int TILES = D == 64 && NBC == 1 ? 4 : 2;
+    static constexpr int ST = 16 * TILES * kCW;
     static constexpr int NG = D / 32;                          // groups per row
     static constexpr int KROW = D * KB / 8;                    // key code bytes per token
     static constexpr int SW = KROW < 128 ? KROW : 128;         // key box row bytes = swizzle span
     static constexpr int NBOX = KROW / SW;                     // key boxes per row
     static constexpr int RBV = D * VB / 8;                     // value code bytes per token
-    static constexpr int K_BYTES = kStageT * KROW;
-    static constexpr int SC_BYTES = kStageT * NG * 2;          // one fp16 plane
-    static constexpr int V_BYTES = kStageT * RBV;
+    static constexpr int K_BYTES = ST * KROW;
+    static constexpr int SC_BYTES = ST * NG * 2;               // one fp16 plane
+    static constexpr int V_BYTES = ST * RBV;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_KS = K_BYTES;
     static constexpr int OFF_KZ = OFF_KS + SC_BYTES;
@@ -244,20 +248,20 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
     const int64_t bh = (int64_t)b * p.H + h;
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = imin64(p.seq_len, t_begin + p.tokens_per_split);
-    const int n_stages = t_end > t_begin ? (int)((t_end - t_begin + kStageT - 1) / kStageT) : 0;
+    const int n_stages = t_end > t_begin ? (int)((t_end - t_begin + A::ST - 1) / A::ST) : 0;
 
     // stage s -> ring slot s % kStages: one 2-D TMA load (key codes) and four
     // 1-D bulk copies (the other planes) completing on the slot's barrier
     auto issue = [&](int s) {
         const int slot = s % kStages;
-        const int64_t t = t_begin + (int64_t)s * kStageT;
-        const int rows = (int)imin64(kStageT, p.cap - t);  // multiple of 16
+        const int64_t t = t_begin + (int64_t)s * A::ST;
+        const int rows = (int)imin64(A::ST, p.cap - t);  // multiple of 16
         const int64_t row0 = bh * p.cap + t;
         const uint32_t st = smem_addr(stages + slot * A::STAGE), bar = full0 + 8 * slot;
         mbar_arrive_expect_tx(bar, (uint32_t)(A::K_BYTES + rows * (3 * NG * 2 + A::RBV)));
 #pragma unroll
         for (int j = 0; j < A::NBOX; ++j)  // key rows wider than 128 bytes arrive as several boxes
-            tma_load_2d(st + A::OFF_K + j * (kStageT * A::SW), &kmap, j * A::SW, (int)row0, bar);
+            tma_load_2d(st + A::OFF_K + j * (A::ST * A::SW), &kmap, j * A::SW, (int)row0, bar);
         bulk_g2s(st + A::OFF_KS, p.k_scale + row0 * NG, rows * NG * 2, bar);
         bulk_g2s(st + A::OFF_KZ, p.k_zero + row0 * NG, rows * NG * 2, bar);
         bulk_g2s(st + A::OFF_VS, p.v_scale + row0 * NG, rows * NG * 2, bar);
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
     for (int G = 0; G < NG; ++G) {
         const int off = KB == 8 ? 32 * G + 8 * c : 16 * G + 4 * c;  // the lane's bytes of group G in the row
         const int box = off / A::SW, col = off % A::SW;
-        koff[G] = A::OFF_K + box * (kStageT * A::SW) + r0 * A::SW + ((((uint32_t)col >> 4) ^ xr) << 4) + (col & 15);
+        koff[G] = A::OFF_K + box * (A::ST * A::SW) + r0 * A::SW + ((((uint32_t)col >> 4) ^ xr) << 4) + (col & 15);
     }
     uint32_t voff[4];
 #pragma unroll
@@ -421,10 +425,10 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
         // two 16-row tiles per warp and stage (rows 16 warp and 16 kCW + 16 warp): Q K^T for
         // both, one softmax step over both, P V for both; the tile loops are unrolled so
         // the compiler interleaves the tiles' independent chains
-        float S[NBC][kTiles][2][2];  // scores: [block][tile][row g, row g + 8][head 2c, 2c + 1]
+        float S[NBC][A::TILES][2][2];  // scores: [block][tile][row g, row g + 8][head 2c, 2c + 1]
 #pragma unroll
-        for (int t2 = 0; t2 < kTiles; ++t2) {
-            const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
+        for (int t2 = 0; t2 < A::TILES; ++t2) {
+            const int tile_r = s * A::ST + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
 
             // ---------------- S = Q K^T for 16 tokens x 8 heads per block, per key group
             float acc[NBC][NG][4];
@@ -522,12 +526,12 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
         // The running max is reduced across the rows only when some lane sees a
         // score above it (or no max exists yet); otherwise the weights are
         // 2^(S - m) with the max unchanged, which is the same arithmetic.
-        float pr[NBC][kTiles][2][2];
+        float pr[NBC][A::TILES][2][2];
 #pragma unroll
         for (int nb = 0; nb < NBC; ++nb) {
             bool raise = m_run[nb][0] == -INFINITY || m_run[nb][1] == -INFINITY;
 #pragma unroll
-            for (int t2 = 0; t2 < kTiles; ++t2)
+            for (int t2 = 0; t2 < A::TILES; ++t2)
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
                     raise = raise || S[nb][t2][i][0] > m_run[nb][0] || S[nb][t2][i][1] > m_run[nb][1];
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
                 for (int j = 0; j < 2; ++j) {
                     float mt = fmaxf(S[nb][0][0][j], S[nb][0][1][j]);
 #pragma unroll
-                    for (int t2 = 1; t2 < kTiles; ++t2) mt = fmaxf(mt, fmaxf(S[nb][t2][0][j], S[nb][t2][1][j]));
+                    for (int t2 = 1; t2 < A::TILES; ++t2) mt = fmaxf(mt, fmaxf(S[nb][t2][0][j], S[nb][t2][1][j]));
                     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
                     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
                     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
@@ -547,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
                     m_run[nb][j] = mn;
                     float ls = 0.0f;
 #pragma unroll
-                    for (int t2 = 0; t2 < kTiles; ++t2) {
+                    for (int t2 = 0; t2 < A::TILES; ++t2) {
                         pr[nb][t2][0][j] = ex2(S[nb][t2][0][j] - mu);
                         pr[nb][t2][1][j] = ex2(S[nb][t2][1][j] - mu);
                         ls += pr[nb][t2][0][j] + pr[nb][t2][1][j];
@@ -570,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
                 for (int j = 0; j < 2; ++j) {
                     float ls = 0.0f;
 #pragma unroll
-                    for (int t2 = 0; t2 < kTiles; ++t2) {
+                    for (int t2 = 0; t2 < A::TILES; ++t2) {
                         pr[nb][t2][0][j] = ex2(S[nb][t2][0][j] - m_run[nb][j]);
                         pr[nb][t2][1][j] = ex2(S[nb][t2][1][j] - m_run[nb][j]);
                         ls += pr[nb][t2][0][j] + pr[nb][t2][1][j];
@@ -580,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
             }
         }
 #pragma unroll
-        for (int t2 = 0; t2 < kTiles; ++t2) {
-            const int tile_r = s * kStageT + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
+        for (int t2 = 0; t2 < A::TILES; ++t2) {
+            const int tile_r = s * A::ST + (16 * kCW) * t2 + 16 * warp;  // tile's first row from the split's start
             // ---------------- P^T as the B operand (tokens x heads), transposed in registers
             uint32_t pt0[NBC], pt1[NBC];
 #pragma unroll
@@ -914,12 +918,12 @@ struct SplitPlan {
     int64_t tokens_per_split;
 };
 
-SplitPlan plan_splits(int B, int H, int64_t seq_len, int ctas_per_sm)
+SplitPlan plan_splits(int B, int H, int64_t seq_len, int ctas_per_sm, int stage_t)
 {
     const int64_t units = (int64_t)B * H;
-    const int64_t stages = (seq_len + kStageT - 1) / kStageT;
+    const int64_t stages = (seq_len + stage_t - 1) / stage_t;
     const int64_t slots = (int64_t)num_sms() * ctas_per_sm;
-    SplitPlan best{1, stages * kStageT};
+    SplitPlan best{1, stages * stage_t};
     double best_cost = 1e300;
     for (int waves = 1; waves <= 16; ++waves) {
         int64_t s = (waves * slots + units - 1) / units;
@@ -931,7 +935,7 @@ SplitPlan plan_splits(int B, int H, int64_t seq_len, int ctas_per_sm)
         const double cost = (double)((ctas + slots - 1) / slots) * (double)(per + 2);  // +2: fixed cost per CTA
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
-            best = SplitPlan{(int)sp, per * kStageT};
+            best = SplitPlan{(int)sp, per * stage_t};
         }
     }
     return best;
@@ -972,7 +976,7 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)A::KROW, (cuuint64_t)c.B * c.H * c.cap};
     const cuuint64_t gstride[1] = {(cuuint64_t)A::KROW};
-    const cuuint32_t box[2] = {(cuuint32_t)A::SW, (cuuint32_t)kStageT};
+    const cuuint32_t box[2] = {(cuuint32_t)A::SW, (cuuint32_t)A::ST};
     const cuuint32_t estride[2] = {1, 1};
     const CUtensorMapSwizzle swz =
         A::SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : A::SW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
@@ -1086,10 +1090,14 @@ int ctas_per_sm(const CacheView &c, int nbc)
     return c.d == 64 ? ctas_per_sm_d<64>(c, nbc) : c.d == 256 ? ctas_per_sm_d<256>(c, nbc) : ctas_per_sm_d<128>(c, nbc);
 }
 
+// Tokens per stage of the split kernel that serves this cache and group.
+int stage_rows(const CacheView &c, int QH) { return c.d == 64 && blocks_per_cta(c, QH) == 1 ? 128 : 64; }
+
 SplitPlan usual_plan(const CacheView &c, int QH, int64_t seq_len)
 {
     const int nbc = blocks_per_cta(c, QH);
-    return plan_splits(c.B, c.H * ((col_blocks(QH / c.H) + nbc - 1) / nbc), seq_len, ctas_per_sm(c, nbc));
+    return plan_splits(c.B, c.H * ((col_blocks(QH / c.H) + nbc - 1) / nbc), seq_len, ctas_per_sm(c, nbc),
+                       stage_rows(c, QH));
 }
 
 template <int D, int VB>
@@ -1210,9 +1218,10 @@ cudaError_t launch_attention_noalloc(const CacheView &c, const uint16_t *q, int 
     const int64_t max_splits = (int64_t)(kNoAllocScratchBytes / per_split);
     if (max_splits < 1) return cudaErrorInvalidValue;
     if (plan.splits > max_splits) {
-        const int64_t stages = (seq_len + kStageT - 1) / kStageT;
+        const int st = stage_rows(c, q_heads);
+        const int64_t stages = (seq_len + st - 1) / st;
         const int64_t per = (stages + max_splits - 1) / max_splits;
-        plan = SplitPlan{(int)((stages + per - 1) / per), per * kStageT};
+        plan = SplitPlan{(int)((stages + per - 1) / per), per * st};
     }
     return run_attention(c, q, q_heads, seq_len, scale, out, scratch, plan, s);
 }

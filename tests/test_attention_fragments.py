@@ -193,11 +193,12 @@ def tma_stage_image(codes_bytes, rb, boxb):
     return img
 
 
-def ksw_addr(r, off, boxb):
-    """The kernel's read address of byte `off` of stage row r (its per-mode form)."""
+def ksw_addr(r, off, boxb, rows=64):
+    """The kernel's read address of byte `off` of row r of a stage of `rows` rows
+    (its per-mode form)."""
     box, col = off // boxb, off % boxb
     x = (r & 7) if boxb == 128 else ((r >> 1) & 3) if boxb == 64 else ((r >> 2) & 1)
-    return box * 64 * boxb + r * boxb + (((col >> 4) ^ x) << 4) + (col & 15)
+    return box * rows * boxb + r * boxb + (((col >> 4) ^ x) << 4) + (col & 15)
 
 
 @pytest.mark.parametrize("d,kb", [(d, kb) for d in (64, 128, 256, 512) for kb in (4, 8)])
@@ -234,11 +235,14 @@ def test_generic_swizzled_key_reads(d, kb):
 @pytest.mark.parametrize("d,kb", [(d, kb) for d in (64, 128, 256) for kb in (4, 8)])
 def test_specialised_key_offsets(d, kb):
     """The specialised kernel's per-lane key offsets (one per group, computed once:
-    koff[G] = box * 64 * SW + r0 * SW + ((chunk ^ xr) << 4) + byte, with the second
-    row of a tile 8 SW on and the warp's second tile 32 SW on) are the swizzled
-    addresses of the lane's bytes of rows r0, r0 + 8, r0 + 32, r0 + 40."""
+    koff[G] = box * ST * SW + r0 * SW + ((chunk ^ xr) << 4) + byte, with the second
+    row of a tile 8 SW on and the warp's next tiles 32 SW apart) are the swizzled
+    addresses of the lane's bytes of rows r0, r0 + 8, r0 + 32, r0 + 40, ... of a
+    stage of ST rows (64 in two tiles per warp; 128 in four at head_dim 64)."""
     rb = d * kb // 8
     sw = min(rb, 128)
+    tiles = 4 if d == 64 else 2
+    st = 32 * tiles
     for warp in range(2):
         for lane in range(32):
             g, c = lane >> 2, lane & 3
@@ -247,8 +251,8 @@ def test_specialised_key_offsets(d, kb):
             for G in range(d // 32):
                 off = 32 * G + 8 * c if kb == 8 else 16 * G + 4 * c
                 box, col = off // sw, off % sw
-                koff = box * 64 * sw + r0 * sw + (((col >> 4) ^ xr) << 4) + (col & 15)
-                for t2 in range(2):
+                koff = box * st * sw + r0 * sw + (((col >> 4) ^ xr) << 4) + (col & 15)
+                for t2 in range(tiles):
                     for i in range(2):
                         r = r0 + 8 * i + 32 * t2
-                        assert koff + t2 * 32 * sw + i * 8 * sw == ksw_addr(r, off, sw)
+                        assert koff + t2 * 32 * sw + i * 8 * sw == ksw_addr(r, off, sw, st)

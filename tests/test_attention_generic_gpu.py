@@ -78,7 +78,8 @@ def test_specialised_kernel_value_widths(cuda, d, kb, vb, G, T):
                                          (64, 4, 2, 8, 16400), (128, 4, 3, 16, 8200), (64, 8, 3, 12, 16400)])
 def test_specialised_kernel_many_stages_per_split(cuda, d, kb, vb, G, T):
     """Enough (sequence, kv-head) pairs (4 x 8) that the split plan fills the
-    GPU with few splits, so each CTA walks several 64-row stages and its
+    GPU with few splits, so each CTA walks several stages (64 rows, 128 at
+    head_dim 64) and its
     running max rises after the first: every output m-tile (2 head_dim / 32
     of them, per column block) must be rescaled then, not only the first
     eight; two column blocks per CTA at G = 12 and 16."""
