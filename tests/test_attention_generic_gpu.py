@@ -79,10 +79,9 @@ def test_specialised_kernel_value_widths(cuda, d, kb, vb, G, T):
 def test_specialised_kernel_many_stages_per_split(cuda, d, kb, vb, G, T):
     """Enough (sequence, kv-head) pairs (4 x 8) that the split plan fills the
     GPU with few splits, so each CTA walks several stages (64 rows, 128 at
-    head_dim 64) and its
-    running max rises after the first: every output m-tile (2 head_dim / 32
-    of them, per column block) must be rescaled then, not only the first
-    eight; two column blocks per CTA at G = 12 and 16."""
+    head_dim 64) and its running max rises after the first: every output
+    m-tile (2 head_dim / 32 of them, per column block) must be rescaled then,
+    not only the first eight; two column blocks per CTA at G = 12 and 16."""
     err = _run(cuda, d, kb, vb, B=4, H=8, G=G, T=T, step=d + kb + G)
     assert err < TOL, err
 
