@@ -61,6 +61,7 @@ constexpr int kG = 8;              // MMA columns: a block of 8 of a kv-head's q
 constexpr int kCW = 2;             // warps per CTA (all compute; the last to finish a stage refills it)
 constexpr int kThreads = kCW * 32;
 constexpr int kStages = 2;         // ring depth (8 CTAs of 2 x 13 KB fit on an SM)
+constexpr float kOffset8 = 1152.0f;  // 8-bit keys: f16 value = 1152 + signed code
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -93,7 +94,6 @@ struct AGeo {
     static constexpr int MERGE = kCW * NBC * kG * (D + 2) * 4;        // per-warp partials (reuse the ring)
     static constexpr int RING = kStages * STAGE > MERGE ? kStages * STAGE : MERGE;
     static constexpr int SMEM = 1024 /*align slack*/ + RING + kStages * 8 /*full barriers*/ + kStages * 4 /*counters*/;
-    static constexpr float OFFSET = 1152.0f;  // 8-bit keys: f16 value = OFFSET + signed code
     // resident CTAs per SM the register budget is sized for (head_dim 256, or
     // two column blocks, hold twice the q fragments and output accumulators)
     static constexpr int MIN_BLOCKS = D * NBC >= 256 ? 4 : 8;
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, AGeo<KB, D, VB, NBC>::MIN_BLOCKS)
                         const uint16_t sh = (uint16_t)(sw[i][G >> 1] >> (16 * (G & 1)));
                         const uint16_t zh = (uint16_t)(zw[i][G >> 1] >> (16 * (G & 1)));
                         if constexpr (KB == 8) {
-                            const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - A::OFFSET;
+                            const float sc = f16_bits_to_f32(sh), zc = f16_bits_to_f32(zh) - kOffset8;
 #pragma unroll
                             for (int nb = 0; nb < NBC; ++nb) {
                                 const float2 t = __ffma2_rn(make_float2(zc, zc), make_float2(qs[nb][G][0], qs[nb][G][1]),

@@ -580,26 +580,26 @@ __device__ __forceinline__ void value_lane_codes(const EncodeParams &p, const fl
         }
         p.scale[crow * (D / 32) + part] = f32_to_f16_bits(sig0);
         p.scale[crow * (D / 32) + 2 + part] = f32_to_f16_bits(sig1);
-        return;
-    }
-    uint32_t w[2 * BITS];
+    } else {
+        uint32_t w[2 * BITS];
 #pragma unroll
-    for (int k = 0; k < BITS; ++k) {
-        w[k] = w0[k];
-        w[BITS + k] = w1[k];
-    }
-    constexpr int RB = D * BITS / 8, LB = 8 * BITS;
-    constexpr int A = align_of_bytes(LB) < 8 ? align_of_bytes(LB) : 8;
-    const uint32_t at = stage + r * RB + part * LB;
+        for (int k = 0; k < BITS; ++k) {
+            w[k] = w0[k];
+            w[BITS + k] = w1[k];
+        }
+        constexpr int RB = D * BITS / 8, LB = 8 * BITS;
+        constexpr int A = align_of_bytes(LB) < 8 ? align_of_bytes(LB) : 8;
+        const uint32_t at = stage + r * RB + part * LB;
 #pragma unroll
-    for (int i = 0; i < 2 * BITS; i += A / 4) {
-        if constexpr (A == 8)
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(at + 4 * i), "r"(w[i]), "r"(w[i + 1]) : "memory");
-        else
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(at + 4 * i), "r"(w[i]) : "memory");
+        for (int i = 0; i < 2 * BITS; i += A / 4) {
+            if constexpr (A == 8)
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(at + 4 * i), "r"(w[i]), "r"(w[i + 1]) : "memory");
+            else
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(at + 4 * i), "r"(w[i]) : "memory");
+        }
+        const uint32_t sw = (uint32_t)f32_to_f16_bits(sig0) | ((uint32_t)f32_to_f16_bits(sig1) << 16);
+        *reinterpret_cast<uint32_t *>(p.scale + crow * (D / 32) + 2 * part) = sw;
     }
-    const uint32_t sw = (uint32_t)f32_to_f16_bits(sig0) | ((uint32_t)f32_to_f16_bits(sig1) << 16);
-    *reinterpret_cast<uint32_t *>(p.scale + crow * (D / 32) + 2 * part) = sw;
 }
 
 template <int D, int BITS>
