@@ -65,7 +65,8 @@ def test_specialised_kernel_head_dims(cuda, d, kb, G, T):
 
 
 @pytest.mark.parametrize("d,kb,vb,G,T", [(128, 8, 4, 8, 5000), (128, 4, 2, 12, 3001), (256, 8, 4, 4, 4133),
-                                         (64, 4, 2, 8, 2050), (256, 4, 2, 16, 777), (64, 8, 4, 3, 1234)])
+                                         (64, 4, 2, 8, 2050), (256, 4, 2, 16, 777), (64, 8, 4, 3, 1234),
+                                         (128, 8, 4, 16, 2222), (64, 4, 4, 16, 1500), (64, 8, 2, 10, 999)])
 def test_specialised_kernel_value_widths(cuda, d, kb, vb, G, T):
     """2- and 4-bit values on the specialised kernel (one permute per f16 pair
     out of the four 2-bit centroids; 4-bit codes as a magnitude index and a
