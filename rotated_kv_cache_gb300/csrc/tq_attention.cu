@@ -13,8 +13,8 @@
 //  * Split-KV: CTA (split, kv-head, sequence) streams its token range through
 //    a 2-stage shared-memory ring; each of its 2 warps takes two 16-token tiles
 //    of a 64-token stage (four of a 128-token stage at head_dim 64, whose rows
-//    are short) and works on them at once (independent dependency chains to
-//    interleave).  A stage is 2-D TMA loads of the key codes (boxes
+//    are short; three of a 96-token stage at head_dim 128 with 4-bit keys) and
+//    works on them at once (independent dependency chains to interleave).  A stage is 2-D TMA loads of the key codes (boxes
 //    of at most 128 bytes per row -- two at head_dim 256 with 8-bit keys --
 //    with the swizzle of the box width, so the per-row fragment reads of the
 //    MMA are bank-conflict-free) and four 1-D bulk copies of the other planes,
@@ -72,10 +72,11 @@ inline int col_blocks(int group) { return (group + kG - 1) / kG; }
 // more than kG q-heads: the key and value codes are unpacked once for both)
 template <int KB, int D, int VB, int NBC = 1>
 struct AGeo {
-    // 16-token tiles per warp and stage, worked on together (four at head_dim 64
-    // with one column block: its rows are short, so the per-stage work is spread
-    // over more of them), and tokens per stage
-    static constexpr int TILES = D == 64 && NBC == 1 ? 4 : 2;
+    // 16-token tiles per warp and stage, worked on together, and tokens per
+    // stage: with one column block, four at head_dim 64 and three at 128 with
+    // 4-bit keys (short rows: the per-stage work is spread over more of them;
+    // the registers and the 2-slot ring still fit 8 CTAs on an SM)
+    static constexpr int TILES = NBC != 1 ? 2 : D == 64 ? 4 : (D == 128 && KB == 4) ? 3 : 2;
     static constexpr int ST = 16 * TILES * kCW;
     static constexpr int NG = D / 32;                          // groups per row
     static constexpr int KROW = D * KB / 8;                    // key code bytes per token
@@ -966,6 +967,7 @@ cudaError_t run_attention_plan(const CacheView &c, const uint16_t *q, int QH, in
                                void *buf, const SplitPlan &plan, cudaStream_t s)
 {
     using A = AGeo<KB, D, VB, NBC>;
+    if (plan.tokens_per_split % A::ST != 0) return cudaErrorInvalidValue;  // splits start on stage boundaries
     cudaError_t e =
         cudaFuncSetAttribute(attn_split_kernel<KB, D, VB, NBC>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
     if (e != cudaSuccess) return e;
@@ -1091,7 +1093,21 @@ int ctas_per_sm(const CacheView &c, int nbc)
 }
 
 // Tokens per stage of the split kernel that serves this cache and group.
-int stage_rows(const CacheView &c, int QH) { return c.d == 64 && blocks_per_cta(c, QH) == 1 ? 128 : 64; }
+// (the stage size depends on the key width, head_dim and column blocks, not
+// on the value width)
+int stage_rows(const CacheView &c, int QH)
+{
+    const bool two = blocks_per_cta(c, QH) == 2;
+    switch (c.d) {
+    case 64:
+        if (two) return c.kb == 8 ? AGeo<8, 64, 3, 2>::ST : AGeo<4, 64, 3, 2>::ST;
+        return c.kb == 8 ? AGeo<8, 64, 3, 1>::ST : AGeo<4, 64, 3, 1>::ST;
+    case 256: return c.kb == 8 ? AGeo<8, 256, 3, 1>::ST : AGeo<4, 256, 3, 1>::ST;
+    default:
+        if (two) return c.kb == 8 ? AGeo<8, 128, 3, 2>::ST : AGeo<4, 128, 3, 2>::ST;
+        return c.kb == 8 ? AGeo<8, 128, 3, 1>::ST : AGeo<4, 128, 3, 1>::ST;
+    }
+}
 
 SplitPlan usual_plan(const CacheView &c, int QH, int64_t seq_len)
 {

@@ -238,10 +238,11 @@ def test_specialised_key_offsets(d, kb):
     koff[G] = box * ST * SW + r0 * SW + ((chunk ^ xr) << 4) + byte, with the second
     row of a tile 8 SW on and the warp's next tiles 32 SW apart) are the swizzled
     addresses of the lane's bytes of rows r0, r0 + 8, r0 + 32, r0 + 40, ... of a
-    stage of ST rows (64 in two tiles per warp; 128 in four at head_dim 64)."""
+    stage of ST rows (64 in two tiles per warp; 128 in four at head_dim 64; 96
+    in three at head_dim 128 with 4-bit keys)."""
     rb = d * kb // 8
     sw = min(rb, 128)
-    tiles = 4 if d == 64 else 2
+    tiles = 4 if d == 64 else 3 if (d, kb) == (128, 4) else 2
     st = 32 * tiles
     for warp in range(2):
         for lane in range(32):

@@ -76,13 +76,15 @@ def test_specialised_kernel_value_widths(cuda, d, kb, vb, G, T):
 
 
 @pytest.mark.parametrize("d,kb,vb,G,T", [(256, 8, 3, 8, 8200), (256, 4, 4, 8, 8200), (64, 8, 3, 8, 16400),
-                                         (64, 4, 2, 8, 16400), (128, 4, 3, 16, 8200), (64, 8, 3, 12, 16400)])
+                                         (64, 4, 2, 8, 16400), (128, 4, 3, 16, 8200), (64, 8, 3, 12, 16400),
+                                         (128, 4, 3, 8, 8200), (128, 4, 4, 8, 8200)])
 def test_specialised_kernel_many_stages_per_split(cuda, d, kb, vb, G, T):
     """Enough (sequence, kv-head) pairs (4 x 8) that the split plan fills the
     GPU with few splits, so each CTA walks several stages (64 rows, 128 at
     head_dim 64) and its running max rises after the first: every output
     m-tile (2 head_dim / 32 of them, per column block) must be rescaled then,
-    not only the first eight; two column blocks per CTA at G = 12 and 16."""
+    not only the first eight; two column blocks per CTA at G = 12 and 16; three
+    tiles per warp (96-row stages) at d128 with 4-bit keys."""
     err = _run(cuda, d, kb, vb, B=4, H=8, G=G, T=T, step=d + kb + G)
     assert err < TOL, err
 
