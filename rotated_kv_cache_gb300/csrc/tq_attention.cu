@@ -14,13 +14,14 @@
 //    a 2-stage shared-memory ring; each of its 2 warps takes two 16-token tiles
 //    of a 64-token stage (four of a 128-token stage at head_dim 64, whose rows
 //    are short; three of a 96-token stage at head_dim 128 with 4-bit keys) and
-//    works on them at once (independent dependency chains to interleave).  A stage is 2-D TMA loads of the key codes (boxes
-//    of at most 128 bytes per row -- two at head_dim 256 with 8-bit keys --
-//    with the swizzle of the box width, so the per-row fragment reads of the
-//    MMA are bank-conflict-free) and four 1-D bulk copies of the other planes,
-//    completing on the slot's mbarrier; the last warp to finish a stage issues
-//    the copies that refill its slot, so no warp is set aside as a producer
-//    (8 CTAs fit on an SM at head_dims 64 and 128, 4 at 256).
+//    works on them at once (independent dependency chains to interleave).  A
+//    stage is 2-D TMA loads of the key codes (boxes of at most 128 bytes per
+//    row -- two at head_dim 256 with 8-bit keys -- with the swizzle of the box
+//    width, so the per-row fragment reads of the MMA are bank-conflict-free)
+//    and four 1-D bulk copies of the other planes, completing on the slot's
+//    mbarrier; the last warp to finish a stage issues the copies that refill
+//    its slot, so no warp is set aside as a producer (8 CTAs fit on an SM at
+//    head_dims 64 and 128, 4 at 256).
 //  * QK^T on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate): M = 16
 //    tokens, N = 8 columns: 8 of the G q-heads sharing the kv-head, K =
 //    head_dim.  A group above 8 has ceil(G/8) column blocks: at head_dims 64
@@ -28,10 +29,9 @@
 //    serve 16 columns (4 CTAs per SM at 128, for the doubled registers); at
 //    256 each block is its own CTA, neighbours in the grid so their reads of
 //    the same rows meet in L2.  Columns past G repeat the last head and are
-//    dropped.  Key codes
-//    become exact f16 integers with one logic op each: offset + code (a
-//    shift first for the upper bytes; 4-bit codes in odd nibbles are read in
-//    place as 1024 + 16 code, their q taken / 16), so
+//    dropped.  Key codes become exact f16 integers with one logic op each:
+//    offset + code (a shift first for the upper bytes; 4-bit codes in odd
+//    nibbles are read in place as 1024 + 16 code, their q taken / 16), so
 //    S = sum_g scale_g * (acc_g + zero_g * sum_{j in g} q_j - offsets' share)
 //    -- the per-group affine is applied to the 8-head scores, not to each
 //    element.
